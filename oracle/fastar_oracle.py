@@ -1,0 +1,352 @@
+"""Plain CPU oracle of the FAST-AR per-chunk attention step.  TEST INFRASTRUCTURE.
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline arm may
+import or run this module.  It shares no code with the CUDA path and imports nothing
+from it; the product path never calls it.
+
+Everything is computed in float64 NumPy, one head at a time, straight from the
+definitions.  Source: "Fast Autoregressive Video Diffusion and World Models with
+Temporal Cache Compression and Sparse Attention" (FAST-AR), as described on the
+pages about it:
+  * TempCache (technical summary §2.A; blog §1): for each current-frame query, the
+    top-1 nearest cached key from previous frames; keys that track the same content
+    are grouped, only the most recent representative stays; in practice keys merge
+    when their similarity passes a threshold.
+  * AnnCA (technical summary §2.B; blog §2): keep the prompt tokens that share an
+    ANN bucket with at least one of the frame's queries; cross-attention over that
+    subset only.
+  * AnnSA (technical summary §2.C; blog §3): reuse the same buckets; each query
+    attends only to keys in its own bucket(s).
+  * Problem statement: the cache grows with the rollout and is to be bounded.
+The pages leave the ANN method open; the spec that accompanies them fixes it:
+per-head unit centroids, key -> argmax-dot centroid, query -> top-r centroids, ties
+to the lowest index, softmax scale 1/sqrt(d), inclusive thresholds, FIFO cap M.
+
+Conventions: a "cosine" of two vectors is a.b / (|a| |b|), and 0 when either norm
+is 0.  "-inf" marks "no candidate".  Every index tie goes to the lowest index.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = float("-inf")
+
+
+class CapacityError(ValueError):
+    """The cache cap M cannot hold one chunk (M < Nq)."""
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------------
+# primitives
+# ----------------------------------------------------------------------------------
+
+def cosine_matrix(A, B) -> np.ndarray:
+    """[na, nb] cosines between the rows of A and the rows of B (0 on a zero norm)."""
+    A = _f64(A)
+    B = _f64(B)
+    na = np.linalg.norm(A, axis=1)
+    nb = np.linalg.norm(B, axis=1)
+    dots = A @ B.T
+    den = np.outer(na, nb)
+    out = np.zeros_like(dots)
+    np.divide(dots, den, out=out, where=den > 0)
+    return out
+
+
+def cosine_rows(A, B) -> np.ndarray:
+    """[n] cosines between A[i] and B[i]."""
+    A = _f64(A)
+    B = _f64(B)
+    den = np.linalg.norm(A, axis=1) * np.linalg.norm(B, axis=1)
+    dots = np.einsum("nd,nd->n", A, B)
+    out = np.zeros_like(dots)
+    np.divide(dots, den, out=out, where=den > 0)
+    return out
+
+
+def order_desc(scores: np.ndarray) -> np.ndarray:
+    """Indices sorted by (score descending, index ascending), along the last axis."""
+    return np.argsort(-_f64(scores), axis=-1, kind="stable")
+
+
+# ----------------------------------------------------------------------------------
+# ANN bucketing (AnnSA §2.C / AnnCA §2.B; method fixed by the spec)
+# ----------------------------------------------------------------------------------
+
+def centroid_scores(X, C) -> np.ndarray:
+    """[n, B] dot products <C[c], x> (the bucketing score; dot, not cosine)."""
+    return _f64(X) @ _f64(C).T
+
+
+def key_buckets(K, C) -> np.ndarray:
+    """b(k) = argmax_c <C[c], k>, lowest c on ties.  int64 [n]."""
+    S = centroid_scores(K, C)
+    if S.shape[0] == 0:
+        return np.zeros(0, np.int64)
+    return order_desc(S)[:, 0].astype(np.int64)
+
+
+def query_buckets(Q, C, r: int) -> np.ndarray:
+    """R(q) = the r centroids with the largest <C[c], q>, ordered by (score desc, c asc).
+    int64 [n, r]."""
+    S = centroid_scores(Q, C)
+    if r > S.shape[1]:
+        raise ValueError("r > B")
+    return order_desc(S)[:, :r].astype(np.int64)
+
+
+# ----------------------------------------------------------------------------------
+# TempCache (technical summary §2.A)
+# ----------------------------------------------------------------------------------
+
+def tempcache_match(Q, K_cache):
+    """Top-1 temporal correspondence of each current query among the cached keys.
+
+    Q [nq, d]; K_cache [n, d] in age order (oldest first).
+    Returns (top1 int64 [nq], s1 [nq], s2 [nq]):
+      top1[i] = argmax_j cos(q_i, k_j), lowest j (oldest) on ties; -1 if n == 0
+      s1[i]   = the best cosine; s2[i] = the best cosine over j != top1[i]
+                (-inf when there is no such j).
+    """
+    Q = _f64(Q)
+    K = _f64(K_cache)
+    nq, n = Q.shape[0], K.shape[0]
+    if n == 0:
+        return (np.full(nq, -1, np.int64), np.full(nq, NEG_INF), np.full(nq, NEG_INF))
+    S = cosine_matrix(Q, K)
+    top1 = np.argmax(S, axis=1).astype(np.int64)       # first maximum = lowest j
+    rows = np.arange(nq)
+    s1 = S[rows, top1].copy()
+    if n > 1:
+        S[rows, top1] = NEG_INF
+        s2 = S.max(axis=1)
+    else:
+        s2 = np.full(nq, NEG_INF)
+    return top1, s1, s2
+
+
+def evict_flags(top1, K_cur, K_cache, tau: float):
+    """e_j = 1 iff some query i has top1[i] = j and cos(kcur_i, k_j) >= tau.
+
+    kcur_i is the current key at query i's token position (the key that becomes the
+    "most recent representative" of the content the query tracks).  Returns
+    (evict bool [n], cos_evict [nq]) where cos_evict[i] = cos(kcur_i, k_top1[i]) (-inf
+    when top1[i] < 0)."""
+    top1 = np.asarray(top1, np.int64)
+    n = np.asarray(K_cache).shape[0]
+    e = np.zeros(n, bool)
+    ce = np.full(top1.shape[0], NEG_INF)
+    ok = top1 >= 0
+    if ok.any():
+        ce[ok] = cosine_rows(np.asarray(K_cur)[ok], np.asarray(K_cache)[top1[ok]])
+        hit = ok.copy()
+        hit[ok] = ce[ok] >= tau
+        e[top1[hit]] = True
+    return e, ce
+
+
+def compact_plan(evict, n: int, nq: int, M: int):
+    """The post-step cache order.
+
+    Survivors (old entries with e_j = 0) in age order, then the nq current entries in
+    token order; while longer than M, drop from the front (oldest).  Returns
+    (index_map int64 [M], length): index_map[s] = j for an old entry, n + i for the
+    current token i, -1 for s >= length.
+    """
+    if M < nq:
+        raise CapacityError(f"M={M} < Nq={nq}")
+    ev = np.asarray(evict, bool)[:n]
+    order = np.concatenate([np.flatnonzero(~ev), n + np.arange(nq)]).astype(np.int64)
+    if order.shape[0] > M:
+        order = order[order.shape[0] - M:]
+    imap = np.full(M, -1, np.int64)
+    imap[: order.shape[0]] = order
+    return imap, int(order.shape[0])
+
+
+def gather_rows(index_map, length: int, old_rows, cur_rows) -> np.ndarray:
+    """Rows of the compacted cache: old_rows[j] for j < n, cur_rows[j - n] otherwise."""
+    old = np.asarray(old_rows)
+    cur = np.asarray(cur_rows)
+    n = old.shape[0]
+    src = np.asarray(index_map, np.int64)[:length]
+    out = np.empty((length,) + cur.shape[1:], dtype=np.result_type(old, cur))
+    is_old = src < n
+    out[is_old] = old[src[is_old]]
+    out[~is_old] = cur[src[~is_old] - n]
+    return out
+
+
+# ----------------------------------------------------------------------------------
+# attention (AnnSA §2.C, AnnCA §2.B, dense baseline)
+# ----------------------------------------------------------------------------------
+
+def masked_softmax_attention(Q, K, V, allowed, scale: float):
+    """o_i = sum_{s allowed} softmax_s(q_i.k_s * scale) v_s, max-subtracted.
+
+    allowed: bool [nq, nk] (None = all).  A row with nothing allowed gets o = 0 and
+    lse = -inf.  Returns (O [nq, dv], lse [nq]) with lse = log sum exp(scores)."""
+    Q = _f64(Q)
+    K = _f64(K)
+    V = _f64(V)
+    nq, nk = Q.shape[0], K.shape[0]
+    O = np.zeros((nq, V.shape[1]))
+    lse = np.full(nq, NEG_INF)
+    if nk == 0 or nq == 0:
+        return O, lse
+    step = max(1, (1 << 24) // max(nk, 1))           # row blocks bound the memory
+    for a in range(0, nq, step):
+        b = min(nq, a + step)
+        S = (Q[a:b] @ K.T) * scale
+        if allowed is not None:
+            S = np.where(allowed[a:b], S, NEG_INF)
+        m = S.max(axis=1)
+        live = np.isfinite(m)
+        if not live.any():
+            continue
+        Pm = np.exp(S[live] - m[live, None])
+        l = Pm.sum(axis=1)
+        O[a:b][live] = (Pm @ V) / l[:, None]
+        lse[a:b][live] = m[live] + np.log(l)
+    return O, lse
+
+
+def annsa_attention(Q, R, K, V, kb, scale: float):
+    """Bucket-restricted self-attention: query i sees the keys s with kb[s] in R(i).
+
+    Q [nq, d]; R [nq, r]; K, V [L, d] (the post-compaction cache, which holds the
+    current chunk); kb [L].  Returns (O, lse, n_empty)."""
+    R = np.asarray(R, np.int64)
+    kb = np.asarray(kb, np.int64)
+    allowed = (kb[None, :, None] == R[:, None, :]).any(axis=2)
+    O, lse = masked_softmax_attention(Q, K, V, allowed, scale)
+    return O, lse, int((~allowed.any(axis=1)).sum())
+
+
+def dense_attention(Q, K, V, scale: float):
+    """Full softmax attention (the dense baseline)."""
+    return masked_softmax_attention(Q, K, V, None, scale)
+
+
+def annca_select(Q, R, Kp, pb, F: int, Tf: int, tau_ca: float, topk: int, gate: bool = True):
+    """Frame-relevant prompt tokens (technical summary §2.B).
+
+    For frame f (queries i in [f*Tf, (f+1)*Tf)) and prompt token p:
+      score[f, p] = max over the frame's queries i with pb[p] in R(i) of cos(q_i, kp_p)
+                    (gate=False drops the bucket condition); -inf if there is none.
+      rank = position in the order (score desc, p asc), -inf after every finite score.
+      keep[f, p] = score >= tau_ca  or  rank < min(topk, P).
+    Returns (keep bool [F, P], kidx list of int64 arrays (kept p ascending),
+             kcnt int64 [F], score [F, P])."""
+    Kp = _f64(Kp)
+    P = Kp.shape[0]
+    R = np.asarray(R, np.int64)
+    pb = np.asarray(pb, np.int64)
+    score = np.full((F, P), NEG_INF)
+    keep = np.zeros((F, P), bool)
+    kidx, kcnt = [], np.zeros(F, np.int64)
+    for f in range(F):
+        Qf = _f64(Q)[f * Tf:(f + 1) * Tf]
+        if P > 0 and Qf.shape[0] > 0:
+            Cf = cosine_matrix(Qf, Kp)
+            if gate:
+                shared = (R[f * Tf:(f + 1) * Tf, :, None] == pb[None, None, :]).any(axis=1)
+                Cf = np.where(shared, Cf, NEG_INF)
+            score[f] = Cf.max(axis=0)
+        order = order_desc(score[f])
+        rank = np.empty(P, np.int64)
+        rank[order] = np.arange(P)
+        keep[f] = (score[f] >= tau_ca) | (rank < min(topk, P))
+        idx = np.flatnonzero(keep[f]).astype(np.int64)
+        kidx.append(idx)
+        kcnt[f] = idx.shape[0]
+    return keep, kidx, kcnt, score
+
+
+def cross_attention_subset(Q, Kp, Vp, kidx, F: int, Tf: int, scale: float):
+    """Cross-attention of each frame's queries over its kept prompt tokens only."""
+    Q = _f64(Q)
+    O = np.zeros((Q.shape[0], np.asarray(Vp).shape[1]))
+    lse = np.full(Q.shape[0], NEG_INF)
+    for f in range(F):
+        idx = np.asarray(kidx[f], np.int64)
+        o, l = masked_softmax_attention(Q[f * Tf:(f + 1) * Tf], _f64(Kp)[idx], _f64(Vp)[idx], None, scale)
+        O[f * Tf:(f + 1) * Tf] = o
+        lse[f * Tf:(f + 1) * Tf] = l
+    return O, lse
+
+
+# ----------------------------------------------------------------------------------
+# one head, one chunk
+# ----------------------------------------------------------------------------------
+
+def head_step(q, k_cur, v_cur, cache_k, cache_v, C, kp, vp, *, F, Tf, tau, M, r, tau_ca,
+              topk, scale, gate=True, decisions=None):
+    """The whole per-chunk step for one head.
+
+    cache_k/cache_v [n, d]: the cache entering the step, oldest first.
+    decisions: optional dict of discrete choices to take instead of the oracle's own
+    (keys 'qb', 'kb_cur', 'kb_cache', 'pb', 'top1', 'evict', 'keep'); the tests use it
+    only with choices they have first checked to be valid alternatives (near-ties).
+    Returns a dict of every intermediate and output.
+    """
+    dec = decisions or {}
+    n, nq = np.asarray(cache_k).shape[0], np.asarray(q).shape[0]
+    qb = dec.get("qb")
+    qb = query_buckets(q, C, r) if qb is None else np.asarray(qb, np.int64)
+    kb_cur = dec.get("kb_cur")
+    kb_cur = key_buckets(k_cur, C) if kb_cur is None else np.asarray(kb_cur, np.int64)
+    kb_cache = dec.get("kb_cache")
+    kb_cache = key_buckets(cache_k, C) if kb_cache is None else np.asarray(kb_cache, np.int64)
+    pb = dec.get("pb")
+    pb = key_buckets(kp, C) if pb is None else np.asarray(pb, np.int64)
+
+    top1, s1, s2 = tempcache_match(q, cache_k)
+    if dec.get("top1") is not None:
+        top1 = np.asarray(dec["top1"], np.int64)
+    evict, cos_evict = evict_flags(top1, k_cur, cache_k, tau)
+    if dec.get("evict") is not None:
+        evict = np.asarray(dec["evict"], bool)
+    imap, length = compact_plan(evict, n, nq, M)
+    new_k = gather_rows(imap, length, cache_k, k_cur)
+    new_v = gather_rows(imap, length, cache_v, v_cur)
+    new_kb = gather_rows(imap, length, kb_cache, kb_cur)
+
+    o_self, lse_self, n_empty = annsa_attention(q, qb, new_k, new_v, new_kb, scale)
+
+    keep, kidx, kcnt, score = annca_select(q, qb, kp, pb, F, Tf, tau_ca, topk, gate)
+    if dec.get("keep") is not None:
+        keep = np.asarray(dec["keep"], bool)
+        kidx = [np.flatnonzero(keep[f]).astype(np.int64) for f in range(F)]
+        kcnt = np.array([len(x) for x in kidx], np.int64)
+    o_cross, lse_cross = cross_attention_subset(q, kp, vp, kidx, F, Tf, scale)
+
+    return dict(qb=qb, kb_cur=kb_cur, kb_cache=kb_cache, pb=pb, top1=top1, s1=s1, s2=s2,
+                cos_evict=cos_evict, evict=evict, index_map=imap, length=length,
+                new_k=new_k, new_v=new_v, new_kb=new_kb, o_self=o_self, lse_self=lse_self,
+                n_empty=n_empty, keep=keep, kidx=kidx, kcnt=kcnt, score=score,
+                o_cross=o_cross, lse_cross=lse_cross)
+
+
+def head_dense_step(q, history_k, history_v, k_cur, v_cur, kp, vp, scale):
+    """The dense baseline for one head: attention over every past key plus the
+    current chunk (append-only cache), and cross-attention over the whole prompt."""
+    K = np.concatenate([_f64(history_k), _f64(k_cur)], axis=0)
+    V = np.concatenate([_f64(history_v), _f64(v_cur)], axis=0)
+    o_self, lse_self = dense_attention(q, K, V, scale)
+    o_cross, lse_cross = dense_attention(q, kp, vp, scale)
+    return dict(o_self=o_self, lse_self=lse_self, o_cross=o_cross, lse_cross=lse_cross)
+
+
+def tempcache_only_advance(q, k_cur, v_cur, cache_k, cache_v, *, tau, M):
+    """The TempCache part alone (match, evict, compact): advances a cache by one chunk.
+    Used to warm a cache through earlier chunks.  Returns (new_k, new_v, info)."""
+    top1, _, _ = tempcache_match(q, cache_k)
+    evict, _ = evict_flags(top1, k_cur, cache_k, tau)
+    imap, length = compact_plan(evict, np.asarray(cache_k).shape[0], np.asarray(q).shape[0], M)
+    return (gather_rows(imap, length, cache_k, k_cur), gather_rows(imap, length, cache_v, v_cur),
+            dict(evicted=int(evict.sum()), length=length, index_map=imap))
