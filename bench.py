@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Throughput of one FAST-AR attention layer step (TempCache + AnnSA + AnnCA) on GB300.
+
+Prints ONE JSON line (rank 0).  Workload: a Wan2.1-1.3B-shaped layer (12 heads, d=128,
+chunks of 3 latent frames x 30x52 tokens, cache cap M=9360, 64 buckets, r=2, 512
+prompt tokens), its cache warmed by running the step itself through 7 earlier
+chunks (21 frames).  One timed step = the whole per-chunk step captured as one CUDA
+graph; L2 is flushed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fastar|reference]
+
+Under torchrun every rank runs its own layer instance (independent head groups: the
+step has no cross-rank exchange), so scaling is weak and value = all ranks' query
+tokens / the slowest rank's time.  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FAST-AR layer query-tokens/s at Wan-1.3B shape; % of HBM/TC roofline"
+UNIT = "query-tokens/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="fastar", choices=["fastar", "reference"])
+    p.add_argument("--config", default="wan13b_layer")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-dense", action="store_true", help="skip the dense-baseline timing")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------------------
+# process group (one process per GPU)
+# ---------------------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(tokens_per_rank: int, seconds_per_rank: float, world: int):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    t = reduce_max(seconds_per_rank, world)
+    return tokens_per_rank * world / t, t
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# roofline bookkeeping (algorithmic units per launch)
+# ---------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def stage_units(cfg, layer, n_in):
+    """Algorithmic bytes and flops of each stage for the measured step (bf16 = 2 B).
+
+    n_in: per-head cache length entering the step.  Counts follow the definitions:
+    every operand read once, every result written once, flops of the contractions
+    the method defines (2 per multiply-add); the sparse attention counts
+    4*d*sum_b |Q_b||K_b| from the step's own bucket histograms."""
+    import numpy as np
+    H, d, Nq, B, r, P, F, Tf = cfg.H, cfg.d, cfg.Nq, cfg.B, cfg.r, cfg.P, cfg.F, cfg.Tf
+    e = 2 if cfg.dtype == "bf16" else 4
+    row = d * e
+    qoff = layer.qoff.cpu().numpy().astype(np.int64)
+    koff = layer.koff.cpu().numpy().astype(np.int64)
+    qcnt, kcnt_b = np.diff(qoff, axis=1), np.diff(koff, axis=1)
+    pairs = float((qcnt * kcnt_b).sum())
+    L_out = layer.caches[1 - layer.cur].len.cpu().numpy().astype(np.int64)
+    kcnt = layer.kcnt.cpu().numpy().astype(np.int64)
+    n_tot = float(np.sum(n_in))
+    u = {}
+    u["bucket_assign"] = dict(bytes=2 * H * Nq * row + 2 * H * B * row, flops=2.0 * 2 * H * Nq * B * d)
+    u["tempcache_match"] = dict(bytes=H * Nq * row * 2 + n_tot * (row + 4), flops=2.0 * Nq * d * n_tot)
+    u["cache_compact"] = dict(bytes=2 * 2 * float(L_out.sum()) * row, flops=0.0)
+    u["bucket_sort"] = dict(bytes=4.0 * (float(L_out.sum()) * 2 + H * Nq * r * 2), flops=0.0)
+    u["sparse_attn"] = dict(bytes=H * Nq * row * 2 + 2 * float(L_out.sum()) * row, flops=4.0 * d * pairs)
+    u["annca_select"] = dict(bytes=H * Nq * row + H * P * row, flops=2.0 * H * Nq * P * d)
+    u["cross_attn_subset"] = dict(bytes=H * Nq * row * 2 + 2 * float(kcnt.sum()) * row,
+                                  flops=4.0 * d * Tf * float(kcnt.sum()))
+    return u
+
+
+def roofline_of(name, avg_ms, units, peaks, sustained=True):
+    b, f = units["bytes"], units["flops"]
+    tpk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_mem = b / (peaks["hbm_gbs"] * 1e9)
+    t_tc = f / (tpk * 1e12)
+    s = avg_ms * 1e-3
+    if t_tc >= t_mem:
+        ach = f / s / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 3), "peak": tpk, "unit": "TFLOP/s",
+                "frac": round(ach / tpk, 5), "traffic": None, "algorithmic_flops": f, "avg_ms": round(avg_ms, 4),
+                "peak_source": peaks["source"] + (" sustained" if sustained else " burst")}
+    ach = b / s / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 5), "traffic": None, "algorithmic_bytes": b,
+            "avg_ms": round(avg_ms, 4), "peak_source": peaks["source"]}
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------------------
+
+def run_fastar(args, rank, world, local):
+    import numpy as np
+    import torch
+    from kv_cache_tempcache_gb300 import synth, _lib
+    from kv_cache_tempcache_gb300.build_lib import build
+    from kv_cache_tempcache_gb300.layer import FastARLayer, DenseLayer
+
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "kv_cache_tempcache_gb300", "libfastar.so")):
+        build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS[args.config]
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(tdt)
+
+    gen = synth.DriftingMixture(cfg, seed=args.seed + rank)
+    layer = FastARLayer(H=cfg.H, d=cfg.d, Tf=cfg.Tf, F=cfg.F, M=cfg.M, B=cfg.B, r=cfg.r, P=cfg.P, tau=cfg.tau,
+                        tau_ca=cfg.tau_ca, topk=cfg.topk, dtype=tdt, device=dev)
+    layer.set_centroids(up(gen.centroids))
+    kp, vp = gen.prompt
+    layer.set_prompt(up(kp), up(vp))
+    hist_k, hist_v = [], []
+    n_prior_chunks = cfg.prior_frames // cfg.F
+    for _ in range(n_prior_chunks):             # warm the cache through the earlier chunks
+        k, v, q = gen.next_chunk()
+        hist_k.append(k)
+        hist_v.append(v)
+        layer.step(up(q), up(k), up(v))
+    k, v, q = gen.next_chunk()                  # the measured chunk
+    q_d, k_d, v_d = up(q), up(k), up(v)
+    torch.cuda.synchronize(dev)
+    n_in = layer.cache.len.cpu().numpy()
+    l0 = _lib.kernel_launches()
+    layer.step(q_d, k_d, v_d, advance=False)
+    torch.cuda.synchronize(dev)
+    launches_per_step = _lib.kernel_launches() - l0
+    assert layer.status() == 0, f"device status {layer.status()}"
+    graph = layer.capture(q_d, k_d, v_d)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = sum(step_ms) / len(step_ms)
+    value, t_max = aggregate(cfg.Nq * args.steps, sum(step_ms) * 1e-3, world)
+
+    # per-stage timing (eager, events on each stage's own stream)
+    stage_ev = {}
+
+    def timer(name, stream, phase):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        stage_ev.setdefault(name, []).append(e)
+
+    for _ in range(args.steps):
+        flush.zero_()
+        layer.step(q_d, k_d, v_d, advance=False, timer=timer)
+    torch.cuda.synchronize(dev)
+    stages = {}
+    for name, es in stage_ev.items():
+        d = [es[i].elapsed_time(es[i + 1]) for i in range(0, len(es), 2)]
+        stages[name] = sum(d) / len(d)
+    peaks = load_peaks()
+    units = stage_units(cfg, layer, n_in)
+    dom = max((s for s in stages if s in units), key=lambda s: stages[s])
+    roof = roofline_of(dom, stages[dom], units[dom], peaks)
+    roof_all = {s: roofline_of(s, stages[s], units[s], peaks) for s in stages if s in units}
+    roof_time = sum(max(units[s]["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                        units[s]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) for s in units)
+
+    # end to end through the public API: pinned host inputs in, outputs back out
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(tdt).pin_memory()
+    q_h, k_h, v_h = pin(q), pin(k), pin(v)
+    os_h = torch.empty_like(layer.o_self, device="cpu").pin_memory()
+    oc_h = torch.empty_like(layer.o_cross, device="cpu").pin_memory()
+    e2e = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        graph.replay()
+        os_h.copy_(layer.o_self, non_blocking=True)
+        oc_h.copy_(layer.o_cross, non_blocking=True)
+        e1.record()
+        e2e.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e]
+    e2e_val, _ = aggregate(cfg.Nq * args.steps, sum(e2e_ms) * 1e-3, world)
+    nb = lambda t: t.numel() * t.element_size()
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(t_max * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded drifting Gaussian-mixture keys; no dataset, no weights)",
+        "config": {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} chunk={cfg.F}x{cfg.Tf} (Nq={cfg.Nq}) "
+                               f"M={cfg.M} B={cfg.B} r={cfg.r} P={cfg.P} tau={cfg.tau} tau_ca={cfg.tau_ca}",
+                   "cache": f"warmed by {n_prior_chunks} earlier chunks ({cfg.prior_frames} frames); "
+                            f"{int(n_in.sum())} entries in, {int(layer.caches[1 - layer.cur].len.sum())} out",
+                   "l2": "flushed between timed steps (256 MiB memset outside the events)",
+                   "parallelism": f"replicas x{world} (independent head groups, no exchange)"},
+        "latent_frames_per_s": round(value / cfg.Tf, 2),
+        "roofline": roof,
+        "step_roofline": {"time_us": round(roof_time * 1e6, 2), "frac": round(roof_time * 1e3 / ms, 5),
+                          "note": "sum over stages of max(bytes/HBM, flops/bf16 sustained) / measured step"},
+        "stages_ms": {s: round(v, 4) for s, v in stages.items()},
+        "stages_roofline_frac": {s: r["frac"] for s, r in roof_all.items()},
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": nb(q_h) + nb(k_h) + nb(v_h),
+                "d2h_bytes_per_step": nb(os_h) + nb(oc_h)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk,
+        "device_bytes": layer.device_bytes(),
+    }
+    # dense baseline from the same build: append-only cache, full attention
+    if not args.no_dense:
+        hk = np.concatenate(hist_k, axis=1)
+        hv = np.concatenate(hist_v, axis=1)
+        dense = DenseLayer(cfg.H, cfg.d, cfg.Nq, hk.shape[1] + cfg.Nq, cfg.P, dtype=tdt, device=dev)
+        dense.load_history(up(hk), up(hv))
+        dense.set_prompt(up(kp), up(vp))
+        for _ in range(2):
+            dense.step(q_d, k_d, v_d, advance=False)
+        dts = []
+        for _ in range(max(3, args.steps // 4)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dense.step(q_d, k_d, v_d, advance=False)
+            e1.record()
+            dts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        dms = sum(a.elapsed_time(b) for a, b in dts) / len(dts)
+        out["dense"] = {"ms_per_step": round(dms, 4), "keys": int(hk.shape[1] + cfg.Nq),
+                        "speedup_fastar_vs_dense": round(dms / ms, 3)}
+        del dense
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=15.0)
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------------------
+
+def _oracle_case(cfg, seed):
+    from kv_cache_tempcache_gb300 import synth
+    inp = synth.layer_step_inputs(cfg, seed=seed)
+    n = min(cfg.M, inp["history_k"].shape[1])
+    return inp, inp["history_k"][:, -n:], inp["history_v"][:, -n:]
+
+
+def _oracle_head(cfg, inp, ck, cv, h):
+    from oracle import fastar_oracle as O
+    return O.head_step(inp["q"][h], inp["k_cur"][h], inp["v_cur"][h], ck[h], cv[h], inp["centroids"][h],
+                       inp["kp"][h], inp["vp"][h], F=cfg.F, Tf=cfg.Tf, tau=cfg.tau, M=cfg.M, r=cfg.r,
+                       tau_ca=cfg.tau_ca, topk=cfg.topk, scale=cfg.scale)
+
+
+def cpu_baseline(cfg, seed, budget_s=15.0):
+    """The oracle as it stands, on whole heads of the same step until the budget is
+    spent; scaled to query tokens per second of the whole layer."""
+    inp, ck, cv = _oracle_case(cfg, seed)
+    t0 = time.perf_counter()
+    heads = 0
+    while heads < cfg.H and (heads == 0 or time.perf_counter() - t0 < budget_s):
+        _oracle_head(cfg, inp, ck, cv, heads)
+        heads += 1
+    dt = time.perf_counter() - t0
+    per_step = dt / heads * cfg.H
+    return {"value": round(cfg.Nq / per_step, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads} of {cfg.H} heads of one {cfg.name} step (float64 NumPy, cache of the "
+                      f"{ck.shape[1]} most recent history entries), scaled by {cfg.H}/{heads}",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from kv_cache_tempcache_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    inp, ck, cv = _oracle_case(cfg, args.seed)
+    W = max(args.warmup, 3)
+    # one step = one head of the layer step (a bounded sample); warm-up steps are
+    # capped at one so the run stays within minutes
+    for i in range(min(W, 1)):
+        _oracle_head(cfg, inp, ck, cv, 0)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_head(cfg, inp, ck, cv, i % cfg.H)
+        times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times) * cfg.H
+    value = cfg.Nq / per_step
+    sample = f"each step: 1 of {cfg.H} heads of one {cfg.name} step, scaled by {cfg.H}"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": W, "ms_per_step": round(per_step * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} Nq={cfg.Nq} M={cfg.M} B={cfg.B} r={cfg.r} "
+                                   f"P={cfg.P}", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_fastar(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * fastar.h — C ABI of libfastar.so: the per-chunk attention step of FAST-AR
+ * ("Fast Autoregressive Video Diffusion and World Models with Temporal Cache
+ * Compression and Sparse Attention") on one NVIDIA GB300 (sm_103a).
+ *
+ * One layer step for one chunk of Nq = F * Tf current tokens is
+ *   1. fastar_bucket_assign   (queries: top-r buckets; current keys: 1 bucket + norm)
+ *   2. fastar_tempcache_match (top-1 cosine match against the cache + eviction flags)
+ *   3. fastar_cache_compact   (drop evicted entries, append the chunk, FIFO cap M)
+ *   4. fastar_bucket_sort     (cache keys and (query, slot) pairs grouped by bucket)
+ *   5. fastar_sparse_attn     (bucket-restricted self-attention)
+ *   6. fastar_annca_select    (frame-relevant prompt tokens)
+ *   7. fastar_cross_attn_subset (cross-attention over the kept prompt tokens)
+ * and fastar_dense_attn is the dense baseline the speed-up is measured against.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless stated otherwise.  The caller allocates
+ *     and owns every buffer, including the workspace sized by
+ *     fastar_workspace_bytes(); the library never allocates or frees memory and
+ *     keeps no pointer after a call returns.
+ *   - dtype is FASTAR_F32 or FASTAR_BF16 and applies to every floating-point
+ *     tensor input and attention output of the call; scores, norms and lse are
+ *     always float32.  The arithmetic is fp32 (bf16 inputs, fp32 accumulation).
+ *   - Head dimension d is 64 or 128 and is contiguous.  Token tensors are
+ *     addressed as base + h*head_stride + t*token_stride + c (strides in
+ *     ELEMENTS), so both [H,N,d] and [N,H,d] layouts work without copies; strides
+ *     and base pointers must be 16-byte aligned.  Cache tensors are contiguous
+ *     [H, M, d]; per-entry metadata is [H, M]; prompt tensors are [H, P, d].
+ *   - All work is enqueued on `stream`; no call synchronises the host.  Lengths
+ *     that change from step to step (cache length, bucket counts, kept counts)
+ *     live in device memory, so a whole step can be captured in a CUDA graph.
+ *   - Every call returns FASTAR_OK or a negative FASTAR_E* code.  Arguments are
+ *     validated on the host before anything is enqueued; an error return
+ *     enqueues nothing.  Data-dependent faults found on the device (a cache
+ *     length above M, a bucket id out of range) are OR-ed as FASTAR_DEV_* bits
+ *     into the caller's int32 dev_status word (optional where noted) and the
+ *     offending element is skipped.  No kernel traps, asserts or waits on
+ *     another block.
+ *   - Ties of every arg-max / top-k decision go to the lowest index.
+ */
+#ifndef FASTAR_H_
+#define FASTAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- element types ---------------------------------------------------------- */
+#define FASTAR_F32 0
+#define FASTAR_BF16 1
+
+/* ---- host return codes -------------------------------------------------------- */
+#define FASTAR_OK 0
+#define FASTAR_EINVAL (-1)       /* null/misaligned pointer, bad size or stride   */
+#define FASTAR_EUNSUPPORTED (-2) /* dtype or head dimension not built             */
+#define FASTAR_ECAPACITY (-3)    /* shape beyond a documented limit (M < Nq, ...) */
+#define FASTAR_EWORKSPACE (-4)   /* workspace smaller than fastar_workspace_bytes */
+#define FASTAR_ECUDA (-5)        /* a launch failed (cudaGetLastError captured)   */
+
+/* ---- device status bits (OR-ed into *dev_status) ------------------------------ */
+#define FASTAR_DEV_BAD_LEN 1      /* a cache length was outside [0, M]            */
+#define FASTAR_DEV_BAD_BUCKET 2   /* a bucket id was outside [0, B)               */
+#define FASTAR_DEV_BAD_INDEX 4    /* an index list pointed outside its range      */
+
+/* ---- limits ------------------------------------------------------------------------ */
+#define FASTAR_MAX_B 256          /* buckets per head                              */
+#define FASTAR_MAX_R 8            /* buckets per query                             */
+#define FASTAR_MAX_P 1024         /* prompt tokens per head                        */
+
+/* ---- workspace queries --------------------------------------------------------- */
+#define FASTAR_OP_MATCH 1
+#define FASTAR_OP_SORT 2
+#define FASTAR_OP_SPARSE_ATTN 3
+#define FASTAR_OP_ANNCA 4
+
+/* Bytes of workspace `op` needs for the given sizes (0 if it needs none).
+ * MATCH: n = Nq, M = cache capacity.  SORT: n = elements per head before the
+ * r fan-out.  SPARSE_ATTN: n = Nq.  ANNCA: F frames, P prompt tokens.
+ * Unused arguments are ignored.  Returns 0 for an unknown op. */
+size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r,
+                              int64_t P, int F);
+
+/* Human-readable text for a FASTAR_* return code (static storage). */
+const char* fastar_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int fastar_version(void);
+
+/* Number of kernels the library has enqueued in this process so far (a
+ * diagnostic: the difference across a captured step is that step's launch count). */
+long long fastar_kernel_launches(void);
+
+/* ---- 1. ANN bucket assignment ---------------------------------------------------
+ * FAST-AR technical summary §2.C (AnnSA assigns tokens to ANN buckets, "semantic
+ * neighbourhoods") and §2.B (AnnCA shares the buckets); the random unit-centroid
+ * ANN itself is fixed by the method spec (the pages name only "LSH or
+ * quantization").
+ * For every row x = X[h, t, :] (t < n) and centroids C[h] ([H, B, d], same dtype,
+ * contiguous):
+ *   score_c = <C[h, c], x>;  ids[h, t, 0..r) = the r largest scores, ordered by
+ *   (score desc, c asc).  r = 1 gives the key bucket argmax_c score_c.
+ * Outputs: ids int32 [H, n, r] (required); scores float [H, n, r] (optional, the
+ * chosen scores); norms float [H, n] (optional, |x|_2).  n = 0 is a no-op.
+ * Limits: 1 <= r <= min(B, FASTAR_MAX_R), B <= FASTAR_MAX_B. */
+int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d,
+                         int64_t head_stride, int64_t token_stride,
+                         const void* centroids, int B, int r,
+                         int32_t* ids, float* scores, float* norms, cudaStream_t stream);
+
+/* ---- 2. TempCache match + eviction flags ------------------------------------------
+ * FAST-AR technical summary §2.A and blog §1: for each current-frame query, the
+ * top-1 nearest key among the cached (previous-frame) keys; a cached entry whose
+ * content the current chunk re-expresses closely enough (similarity threshold)
+ * is merged away, leaving the most recent representative.
+ * For each head h and query i < nq, over the n = cache_len[h] cached entries
+ * (age order, oldest first):
+ *   top1[h,i] = argmax_j cos(q_i, k_j)   (lowest j on ties; -1 when n == 0)
+ *   s1[h,i], s2[h,i] = best and second-best cosine (-inf when absent)
+ *   evict[h, top1] = 1 if cos(kcur_i, k_top1) >= tau (kcur_i = current key i).
+ * cos(a,b) = a.b/(|a||b|), 0 on a zero norm.  cache_knorm[h,j] must hold |k_j|
+ * (fastar_bucket_assign's norms / fastar_cache_compact maintain it).
+ * q and k_cur share (head_stride, token_stride).  evict is [H, M] uint8 and is
+ * cleared to 0 inside the call before the flags are set.  s1/s2 may be NULL.
+ * Workspace: fastar_workspace_bytes(FASTAR_OP_MATCH, H, nq, M, d, ...).
+ * cache_len values outside [0, M] are clamped and flag FASTAR_DEV_BAD_LEN. */
+int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                           int64_t head_stride, int64_t token_stride,
+                           const void* cache_k, const float* cache_knorm,
+                           const int32_t* cache_len, int64_t M, float tau,
+                           int32_t* top1, float* s1, float* s2, uint8_t* evict,
+                           int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* ---- 3. cache compaction -------------------------------------------------------
+ * FAST-AR technical summary §2.A ("merging ... bounds the growth of the KV
+ * cache") and blog §1 ("only the most recent representative stays in the
+ * cache"); FIFO hard cap M from the method spec.
+ * Per head: the new cache is [old entries j < len_in with evict[j] == 0, in age
+ * order] ++ [current tokens i = 0..nq-1]; while longer than M the oldest entries
+ * are dropped.  Written: k_out, v_out [H,M,d]; knorm_out [H,M] (|k|);
+ * kb_out [H,M] (key bucket); len_out [H]; index_map [H,M] int32 with the source
+ * of each slot: j (< n) for an old entry, n + i for current token i, -1 past
+ * len_out.  Slots past len_out keep stale rows.
+ * Current rows come from k_cur/v_cur (head_stride, token_stride) with their norm
+ * kcur_norm [H,nq] and bucket kcur_bucket [H,nq] (from fastar_bucket_assign).
+ * Out-of-place: the *_in and *_out buffers must not overlap.
+ * Requires M >= nq (else FASTAR_ECAPACITY).  dev_status optional. */
+int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M,
+                         const void* k_cur, const void* v_cur, int64_t head_stride,
+                         int64_t token_stride, const float* kcur_norm, const int32_t* kcur_bucket,
+                         const void* k_in, const void* v_in, const float* knorm_in,
+                         const int32_t* kb_in, const int32_t* len_in, const uint8_t* evict,
+                         void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
+                         int32_t* len_out, int32_t* index_map, int32_t* dev_status,
+                         cudaStream_t stream);
+
+/* ---- 4. counting sort by bucket --------------------------------------------------
+ * Groups tokens by ANN bucket so that bucket-restricted attention runs on dense
+ * blocks (FAST-AR technical summary §2.C: "block-sparse operation"; the
+ * semantic-aware token permutation of Sparse VideoGen2, which the paper builds
+ * on, is the same idea).
+ * ids int32 [H, n, r]; per head the elements are e = t*r + s for t < n_valid[h]
+ * (n_valid may be NULL: all n).  A stable counting sort by ids[e] writes
+ * perm[h, 0..E) (E = n_valid*r; element ids e in bucket order, ascending e within
+ * a bucket) and offsets[h, 0..B] (offsets[b] = first position of bucket b,
+ * offsets[B] = E).  Ids outside [0,B) are skipped and flag FASTAR_DEV_BAD_BUCKET. */
+int fastar_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
+                       const int32_t* n_valid, int32_t* perm, int32_t* offsets,
+                       int32_t* dev_status, cudaStream_t stream);
+
+/* ---- 5. bucket-restricted (AnnSA) self-attention -------------------------------------
+ * FAST-AR technical summary §2.C and blog §3: each query attends only to the keys
+ * in its own bucket(s).
+ *   O[h,i] = sum_{s < len, kb[s] in R(i)} softmax_s(q_i . k_s * scale) v_s
+ * over the compacted cache k, v [H,M,d].  The caller passes the two bucket
+ * orders from fastar_bucket_sort: qperm/qoff over the (query, slot) pairs of
+ * the [H,nq,r] query buckets, kperm/koff over the cache's key buckets.  A query
+ * whose buckets hold no key gets O = 0 and lse = -inf.
+ * out: dtype, addressed with (o_head_stride, o_token_stride); lse float [H,nq]
+ * (optional).  Workspace: fastar_workspace_bytes(FASTAR_OP_SPARSE_ATTN, H, nq, M, d, B, r, ...). */
+int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d,
+                       int64_t q_head_stride, int64_t q_token_stride, int r, int B,
+                       const int32_t* qperm, const int32_t* qoff,
+                       const void* k, const void* v, int64_t M,
+                       const int32_t* kperm, const int32_t* koff, float scale,
+                       void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* ---- 6. AnnCA prompt selection ---------------------------------------------------
+ * FAST-AR technical summary §2.B and blog §2: keep the prompt tokens that share
+ * an ANN bucket with at least one of the frame's queries; the always-keep top-k
+ * by max query cosine and the threshold tau_ca are fixed by the method spec.
+ * Queries i of frame f are i in [f*tpf, (f+1)*tpf).  For prompt token p (< P):
+ *   score[h,f,p] = max over the frame's i with pb[h,p] in qb[h,i,0..r) of
+ *                  cos(q_i, kp_p)   (gate = 0 drops the bucket condition);
+ *                  -inf when there is no such i.
+ *   keep[h,f,p] = score >= tau_ca, or p is among the first min(topk, P) in the
+ *                 order (score desc, p asc) with -inf after every finite score.
+ * Outputs: keep uint8 [H,F,P]; kidx int32 [H,F,P] (kept p ascending, then -1);
+ * kcnt int32 [H,F]; score float [H,F,P] (optional).  kp is [H,P,d] contiguous.
+ * Workspace: fastar_workspace_bytes(FASTAR_OP_ANNCA, H, ..., P, F).  P <= FASTAR_MAX_P. */
+int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d,
+                        int64_t q_head_stride, int64_t q_token_stride,
+                        const int32_t* qb, int r, const void* kp, const int32_t* pb, int64_t P,
+                        float tau_ca, int topk, int gate,
+                        uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---- 7. cross-attention over the kept prompt subset --------------------------------
+ * FAST-AR technical summary §2.B ("cross-attention computed over ... the
+ * frame-relevant prompt subset").  For query i of frame f:
+ *   O[h,i] = sum_{t < kcnt[h,f]} softmax_t(q_i . kp_{kidx[h,f,t]} * scale) vp_{kidx[h,f,t]}
+ * kp, vp [H,P,d] contiguous; kidx/kcnt from fastar_annca_select.  kcnt = 0 gives
+ * O = 0, lse = -inf.  lse float [H, F*tpf] optional. */
+int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d,
+                             int64_t q_head_stride, int64_t q_token_stride,
+                             const void* kp, const void* vp, int64_t P,
+                             const int32_t* kidx, const int32_t* kcnt, float scale,
+                             void* out, int64_t o_head_stride, int64_t o_token_stride,
+                             float* lse, cudaStream_t stream);
+
+/* ---- 8. dense attention (the baseline) ------------------------------------------
+ * The dense softmax attention FAST-AR is compared against (technical summary,
+ * Key Results: speed-ups versus dense FlashAttention-3).
+ *   O[h,i] = sum_{j < nk} softmax_j(q_i . k_j * scale) v_j
+ * k, v addressed with (kv_head_stride, kv_token_stride).  lse optional. */
+int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d,
+                      int64_t q_head_stride, int64_t q_token_stride,
+                      const void* k, const void* v, int64_t nk,
+                      int64_t kv_head_stride, int64_t kv_token_stride, float scale,
+                      void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                      cudaStream_t stream);
+
+/* Appends nq rows of k_cur/v_cur to an append-only dense cache [H, cap, d] at row
+ * `at` (the dense baseline's growing cache).  Requires at + nq <= cap. */
+int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,
+                        int64_t head_stride, int64_t token_stride, void* k_cache, void* v_cache,
+                        int64_t cap, int64_t at, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FASTAR_H_ */

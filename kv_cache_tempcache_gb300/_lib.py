@@ -1,0 +1,223 @@
+"""ctypes binding of libfastar.so: one Python function per C entry point, same name.
+
+Argument marshalling only: tensors become (pointer, strides), the current CUDA
+stream is passed through, and a non-zero return code raises FastarError.  All
+computation happens in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfastar.so")
+
+F32, BF16 = 0, 1
+OK, EINVAL, EUNSUPPORTED, ECAPACITY, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
+DEV_BAD_LEN, DEV_BAD_BUCKET, DEV_BAD_INDEX = 1, 2, 4
+OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA = 1, 2, 3, 4
+MAX_B, MAX_R, MAX_P = 256, 8, 1024
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+
+# name -> argtypes (restype int unless listed in _RESTYPES)
+_SIGS = {
+    "fastar_version": [],
+    "fastar_kernel_launches": [],
+    "fastar_status_string": [_I],
+    "fastar_workspace_bytes": [_I, _I, _L, _L, _I, _I, _I, _L, _I],
+    "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
+    "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _S,
+                               _P],
+    "fastar_cache_compact": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                             _P, _P, _P, _P],
+    "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
+    "fastar_sparse_attn": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P,
+                           _P, _S, _P],
+    "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P, _P, _S,
+                            _P],
+    "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P],
+    "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
+    "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
+}
+_RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
+             "fastar_kernel_launches": ctypes.c_longlong}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class FastarError(RuntimeError):
+    def __init__(self, name: str, code: int):
+        super().__init__(f"{name} returned {code}: {status_string(code)}")
+        self.code = code
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Opens a libfastar build and declares every symbol; raises if it is missing."""
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with `python -m kv_cache_tempcache_gb300.build_lib`")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _RESTYPES.get(name, ctypes.c_int)
+    return lib
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """The process-wide libfastar handle (opened on first use)."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(path)
+    return _lib
+
+
+def symbols():
+    return list(_SIGS)
+
+
+def status_string(code: int) -> str:
+    return load().fastar_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return load().fastar_version()
+
+
+def kernel_launches() -> int:
+    return int(load().fastar_kernel_launches())
+
+
+def workspace_bytes(op, H, n, M=0, d=128, B=1, r=1, P=0, F=0) -> int:
+    return int(load().fastar_workspace_bytes(op, H, n, M, d, B, r, P, F))
+
+
+# ---- marshalling helpers -------------------------------------------------------------------
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return F32
+    if t == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    """Device address of a tensor the library addresses as dense (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_contiguous() and t.dim() == 3 and t.stride(2) == 1:
+        return t.data_ptr()          # a strided token view; strides are passed separately
+    if not t.is_contiguous():
+        raise ValueError("index/metadata/output buffers must be contiguous")
+    return t.data_ptr()
+
+
+def stream_handle(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def tok_strides(t: torch.Tensor):
+    """(head_stride, token_stride) of a [H, N, d] view with a contiguous last dim."""
+    if t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError("token tensors must be [H, N, d] views with a contiguous last dimension")
+    return t.stride(0), t.stride(1)
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != OK:
+        raise FastarError(name, rc)
+
+
+# ---- entry points --------------------------------------------------------------------------
+
+def fastar_bucket_assign(x, centroids, r, ids, scores=None, norms=None, stream=None):
+    H, n, d = x.shape
+    hs, ts = tok_strides(x)
+    _call("fastar_bucket_assign", ptr(x), dtype_code(x.dtype), H, n, d, hs, ts, ptr(centroids),
+          centroids.shape[1], r, ptr(ids), ptr(scores), ptr(norms), stream_handle(stream))
+
+
+def fastar_tempcache_match(q, k_cur, cache_k, cache_knorm, cache_len, tau, top1, s1, s2, evict, dev_status,
+                           workspace, stream=None):
+    H, nq, d = q.shape
+    hs, ts = tok_strides(q)
+    if tok_strides(k_cur) != (hs, ts):
+        raise ValueError("q and k_cur must share strides")
+    _call("fastar_tempcache_match", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, nq, d, hs, ts, ptr(cache_k),
+          ptr(cache_knorm), ptr(cache_len), cache_k.shape[1], float(tau), ptr(top1), ptr(s1), ptr(s2), ptr(evict),
+          ptr(dev_status), ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+          stream_handle(stream))
+
+
+def fastar_cache_compact(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict,
+                         k_out, v_out, knorm_out, kb_out, len_out, index_map, dev_status, stream=None):
+    H, nq, d = k_cur.shape
+    hs, ts = tok_strides(k_cur)
+    if tok_strides(v_cur) != (hs, ts):
+        raise ValueError("k_cur and v_cur must share strides")
+    _call("fastar_cache_compact", dtype_code(k_cur.dtype), H, nq, d, k_in.shape[1], ptr(k_cur), ptr(v_cur), hs,
+          ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(len_in),
+          ptr(evict), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out), ptr(len_out), ptr(index_map),
+          ptr(dev_status), stream_handle(stream))
+
+
+def fastar_bucket_sort(ids, B, perm, offsets, n_valid=None, dev_status=None, stream=None):
+    H, n, r = ids.shape
+    _call("fastar_bucket_sort", ptr(ids), H, n, r, B, ptr(n_valid), ptr(perm), ptr(offsets), ptr(dev_status),
+          stream_handle(stream))
+
+
+def fastar_sparse_attn(q, r, B, qperm, qoff, k, v, kperm, koff, scale, out, lse, dev_status, workspace,
+                       stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    oh, ot = tok_strides(out)
+    _call("fastar_sparse_attn", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, r, B, ptr(qperm), ptr(qoff), ptr(k),
+          ptr(v), k.shape[1], ptr(kperm), ptr(koff), float(scale), ptr(out), oh, ot, ptr(lse), ptr(dev_status),
+          ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+          stream_handle(stream))
+
+
+def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, score=None, workspace=None,
+                        stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    tpf = nq // F
+    _call("fastar_annca_select", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2], ptr(kp),
+          ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), ptr(keep), ptr(kidx), ptr(kcnt), ptr(score),
+          ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+          stream_handle(stream))
+
+
+def fastar_cross_attn_subset(q, F, kp, vp, kidx, kcnt, scale, out, lse=None, stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    oh, ot = tok_strides(out)
+    _call("fastar_cross_attn_subset", ptr(q), dtype_code(q.dtype), H, F, nq // F, d, qh, qt, ptr(kp), ptr(vp),
+          kp.shape[1], ptr(kidx), ptr(kcnt), float(scale), ptr(out), oh, ot, ptr(lse), stream_handle(stream))
+
+
+def fastar_dense_attn(q, k, v, nk, scale, out, lse=None, stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    kh, kt = tok_strides(k)
+    oh, ot = tok_strides(out)
+    _call("fastar_dense_attn", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, ptr(k), ptr(v), int(nk), kh, kt,
+          float(scale), ptr(out), oh, ot, ptr(lse), stream_handle(stream))
+
+
+def fastar_dense_append(k_cur, v_cur, k_cache, v_cache, at, stream=None):
+    H, nq, d = k_cur.shape
+    hs, ts = tok_strides(k_cur)
+    _call("fastar_dense_append", dtype_code(k_cur.dtype), H, nq, d, ptr(k_cur), ptr(v_cur), hs, ts, ptr(k_cache),
+          ptr(v_cache), k_cache.shape[1], int(at), stream_handle(stream))

@@ -1,0 +1,287 @@
+// The C ABI of libfastar: argument validation, workspace sizing and dispatch.
+// Every check runs on the host before anything is enqueued.
+#include <atomic>
+#include <cstdint>
+
+#include "fastar.h"
+#include "kernels.h"
+
+using fastar::TokView;
+
+namespace fastar {
+static std::atomic<long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace fastar
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t esize(int dtype) { return dtype == FASTAR_BF16 ? 2 : 4; }
+
+int check_dtype_d(int dtype, int d) {
+  if (dtype != FASTAR_F32 && dtype != FASTAR_BF16) return FASTAR_EUNSUPPORTED;
+  if (d != 64 && d != 128) return FASTAR_EUNSUPPORTED;
+  return FASTAR_OK;
+}
+
+// A token tensor: non-null (when rows exist), 16-byte aligned base and strides, and
+// rows that do not overlap.
+int check_tok(const void* p, int dtype, int d, int64_t hs, int64_t ts, int64_t nrows, int H) {
+  if (nrows == 0 || H == 0) return FASTAR_OK;
+  if (!p || !aligned16(p)) return FASTAR_EINVAL;
+  const int64_t es = (int64_t)esize(dtype);
+  if (ts < d || hs < 0 || ((ts * es) & 15) || ((hs * es) & 15)) return FASTAR_EINVAL;
+  if (H > 1 && hs < d) return FASTAR_EINVAL;
+  return FASTAR_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FASTAR_OK : FASTAR_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fastar_version(void) { return 100; }
+
+long long fastar_kernel_launches(void) { return fastar::g_launches.load(std::memory_order_relaxed); }
+
+const char* fastar_status_string(int status) {
+  switch (status) {
+    case FASTAR_OK: return "ok";
+    case FASTAR_EINVAL: return "invalid argument (null or misaligned pointer, bad size or stride)";
+    case FASTAR_EUNSUPPORTED: return "unsupported dtype or head dimension";
+    case FASTAR_ECAPACITY: return "shape beyond a documented capacity limit";
+    case FASTAR_EWORKSPACE: return "workspace smaller than fastar_workspace_bytes()";
+    case FASTAR_ECUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r, int64_t P,
+                              int F) {
+  if (H <= 0 || n < 0) return 0;
+  switch (op) {
+    case FASTAR_OP_MATCH: return fastar::match_workspace(H, n, M);
+    case FASTAR_OP_SORT: return 0;
+    case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r);
+    case FASTAR_OP_ANNCA: return fastar::annca_workspace(H, F, P);
+    default: return 0;
+  }
+}
+
+int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d, int64_t head_stride,
+                         int64_t token_stride, const void* centroids, int B, int r, int32_t* ids,
+                         float* scores, float* norms, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || n < 0 || B < 1 || r < 1) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B || r > FASTAR_MAX_R || r > B) return FASTAR_ECAPACITY;
+  if (H == 0 || n == 0) return FASTAR_OK;
+  if ((rc = check_tok(x, dtype, d, head_stride, token_stride, n, H))) return rc;
+  if (!centroids || !aligned16(centroids) || !ids) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_bucket_assign(dtype, d, TokView{x, head_stride, token_stride}, H, n,
+                                              centroids, B, r, ids, scores, norms, stream));
+}
+
+int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                           int64_t head_stride, int64_t token_stride, const void* cache_k,
+                           const float* cache_knorm, const int32_t* cache_len, int64_t M, float tau,
+                           int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* dev_status,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || nq > INT32_MAX) return FASTAR_EINVAL;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (!cache_k || !aligned16(cache_k) || !cache_knorm || !cache_len || !evict) return FASTAR_EINVAL;
+  if (nq > 0 && !top1) return FASTAR_EINVAL;
+  if (nq > 0) {
+    const size_t need = fastar::match_workspace(H, nq, M);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+  }
+  return cuda_rc(fastar::launch_tempcache_match(
+      dtype, d, TokView{q, head_stride, token_stride}, TokView{k_cur, head_stride, token_stride}, H, nq,
+      cache_k, cache_knorm, cache_len, M, tau, top1, s1, s2, evict, dev_status, workspace, stream));
+}
+
+int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
+                         const void* v_cur, int64_t head_stride, int64_t token_stride,
+                         const float* kcur_norm, const int32_t* kcur_bucket, const void* k_in,
+                         const void* v_in, const float* knorm_in, const int32_t* kb_in,
+                         const int32_t* len_in, const uint8_t* evict, void* k_out, void* v_out,
+                         float* knorm_out, int32_t* kb_out, int32_t* len_out, int32_t* index_map,
+                         int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX) return FASTAR_EINVAL;
+  if (M < nq) return FASTAR_ECAPACITY;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(v_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (nq > 0 && (!kcur_norm || !kcur_bucket)) return FASTAR_EINVAL;
+  const void* ptrs[] = {k_in, v_in, k_out, v_out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return FASTAR_EINVAL;
+  if (!knorm_in || !kb_in || !len_in || !evict || !knorm_out || !kb_out || !len_out || !index_map)
+    return FASTAR_EINVAL;
+  if (k_in == k_out || v_in == v_out || knorm_in == knorm_out || kb_in == kb_out) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_cache_compact(
+      dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
+      kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
+      len_out, index_map, dev_status, stream));
+}
+
+int fastar_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B, const int32_t* n_valid,
+                       int32_t* perm, int32_t* offsets, int32_t* dev_status, cudaStream_t stream) {
+  if (H < 0 || n < 0 || r < 1 || B < 1) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B || r > FASTAR_MAX_R || n * r > INT32_MAX) return FASTAR_ECAPACITY;
+  if (H == 0) return FASTAR_OK;
+  if ((n > 0 && (!ids || !perm)) || !offsets) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_bucket_sort(ids, H, n, r, B, n_valid, perm, offsets, dev_status, stream));
+}
+
+int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                       int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
+                       const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
+                       float scale, void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || M < 1 || r < 1 || B < 1 || M > INT32_MAX) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B || r > FASTAR_MAX_R || nq * r > INT32_MAX) return FASTAR_ECAPACITY;
+  if (H == 0 || nq == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, nq, H))) return rc;
+  if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, nq, H))) return rc;
+  if (!qperm || !qoff || !kperm || !koff || !k || !v || !aligned16(k) || !aligned16(v)) return FASTAR_EINVAL;
+  const size_t need = fastar::sparse_attn_workspace(H, nq, d, r);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+  fastar::AttnArgs a{};
+  a.mode = fastar::kSparse;
+  a.H = H;
+  a.q = TokView{q, q_head_stride, q_token_stride};
+  a.nq = nq;
+  a.k = k;
+  a.v = v;
+  a.r = r;
+  a.B = B;
+  a.qperm = qperm;
+  a.qoff = qoff;
+  a.kperm = kperm;
+  a.koff = koff;
+  a.M = M;
+  a.scale = scale;
+  a.out = out;
+  a.o_hs = o_head_stride;
+  a.o_ts = o_token_stride;
+  a.lse = lse;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = a.part_o + (size_t)H * nq * r * d;
+  a.status = dev_status;
+  return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
+}
+
+int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
+                        int64_t q_token_stride, const int32_t* qb, int r, const void* kp, const int32_t* pb,
+                        int64_t P, float tau_ca, int topk, int gate, uint8_t* keep, int32_t* kidx,
+                        int32_t* kcnt, float* score, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || F < 0 || tpf < 0 || r < 1 || P < 0 || topk < 0) return FASTAR_EINVAL;
+  if (P > FASTAR_MAX_P || r > FASTAR_MAX_R) return FASTAR_ECAPACITY;
+  if (H == 0 || F == 0) return FASTAR_OK;
+  if (!kcnt) return FASTAR_EINVAL;
+  if (P > 0) {
+    if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, (int64_t)F * tpf, H))) return rc;
+    if (tpf > 0 && !qb) return FASTAR_EINVAL;
+    if (!kp || !aligned16(kp) || !pb || !keep || !kidx) return FASTAR_EINVAL;
+    if (!score) {
+      const size_t need = fastar::annca_workspace(H, F, P);
+      if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+    }
+  }
+  return cuda_rc(fastar::launch_annca_select(dtype, d, TokView{q, q_head_stride, q_token_stride}, H, F, tpf,
+                                             qb, r, kp, pb, P, tau_ca, topk, gate, keep, kidx, kcnt, score,
+                                             workspace, stream));
+}
+
+int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
+                             int64_t q_token_stride, const void* kp, const void* vp, int64_t P,
+                             const int32_t* kidx, const int32_t* kcnt, float scale, void* out,
+                             int64_t o_head_stride, int64_t o_token_stride, float* lse, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || F < 0 || tpf < 0 || P < 0) return FASTAR_EINVAL;
+  if (P > FASTAR_MAX_P) return FASTAR_ECAPACITY;
+  if (H == 0 || F == 0 || tpf == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, (int64_t)F * tpf, H))) return rc;
+  if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, (int64_t)F * tpf, H))) return rc;
+  if (!kcnt || (P > 0 && (!kp || !vp || !kidx || !aligned16(kp) || !aligned16(vp)))) return FASTAR_EINVAL;
+  fastar::AttnArgs a{};
+  a.mode = fastar::kCross;
+  a.H = H;
+  a.q = TokView{q, q_head_stride, q_token_stride};
+  a.nq = (int64_t)F * tpf;
+  a.k = kp;
+  a.v = vp;
+  a.F = F;
+  a.tpf = tpf;
+  a.kidx = kidx;
+  a.kcnt = kcnt;
+  a.P = P;
+  a.scale = scale;
+  a.out = out;
+  a.o_hs = o_head_stride;
+  a.o_ts = o_token_stride;
+  a.lse = lse;
+  return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
+}
+
+int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                      int64_t q_token_stride, const void* k, const void* v, int64_t nk, int64_t kv_head_stride,
+                      int64_t kv_token_stride, float scale, void* out, int64_t o_head_stride,
+                      int64_t o_token_stride, float* lse, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || nk < 0 || nq > INT32_MAX) return FASTAR_EINVAL;
+  if (H == 0 || nq == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, nq, H))) return rc;
+  if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, nq, H))) return rc;
+  if ((rc = check_tok(k, dtype, d, kv_head_stride, kv_token_stride, nk, H))) return rc;
+  if ((rc = check_tok(v, dtype, d, kv_head_stride, kv_token_stride, nk, H))) return rc;
+  fastar::AttnArgs a{};
+  a.mode = fastar::kDense;
+  a.H = H;
+  a.q = TokView{q, q_head_stride, q_token_stride};
+  a.nq = nq;
+  a.k = k;
+  a.v = v;
+  a.kv_hs = kv_head_stride;
+  a.kv_ts = kv_token_stride;
+  a.nk = nk;
+  a.scale = scale;
+  a.out = out;
+  a.o_hs = o_head_stride;
+  a.o_ts = o_token_stride;
+  a.lse = lse;
+  return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
+}
+
+int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,
+                        int64_t head_stride, int64_t token_stride, void* k_cache, void* v_cache, int64_t cap,
+                        int64_t at, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || at < 0 || cap < 0) return FASTAR_EINVAL;
+  if (at + nq > cap) return FASTAR_ECAPACITY;
+  if (H == 0 || nq == 0) return FASTAR_OK;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(v_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_dense_append(dtype, d, H, nq, TokView{k_cur, head_stride, token_stride},
+                                             TokView{v_cur, head_stride, token_stride}, k_cache, v_cache, cap,
+                                             at, stream));
+}
+
+}  // extern "C"

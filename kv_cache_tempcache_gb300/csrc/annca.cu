@@ -1,0 +1,232 @@
+// AnnCA: frame-relevant prompt tokens (SIMT path).
+//
+// FAST-AR technical summary §2.B / blog §2: a prompt token is kept for a frame
+// when it shares an ANN bucket with at least one of the frame's queries; the
+// score (max bucket-sharing query cosine), the threshold tau_ca and the
+// always-keep top-k are the method spec's.
+//
+// Kernel 1 scores every (head, frame, prompt token); kernel 2 ranks the scores of
+// one (head, frame) in a single CTA and writes the keep mask and the compacted,
+// ascending index list.
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fastar {
+
+constexpr int kCQ = 64;  // queries per tile
+constexpr int kCP = 64;  // prompt tokens per tile
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+annca_score_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int64_t tpf,
+                   const int32_t* __restrict__ qb, int r, const T* __restrict__ kp,
+                   const int32_t* __restrict__ pb, int64_t P, int gate, float* __restrict__ score) {
+  extern __shared__ __align__(16) float sm_ca[];
+  float* Qs = sm_ca;                // [D][kCQ]
+  float* Ks = Qs + D * kCQ;         // [D][kCP]
+  float* qinv = Ks + D * kCP;       // [kCQ]
+  float* pinv = qinv + kCQ;         // [kCP]
+  float* red = pinv + kCP;          // [16][kCP]
+  int* qbs = reinterpret_cast<int*>(red + 16 * kCP);   // [kCQ][FASTAR_MAX_R]
+  int* pbs = qbs + kCQ * FASTAR_MAX_R;                  // [kCP]
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, f = blockIdx.z;
+  const int64_t p0 = (int64_t)blockIdx.x * kCP;
+  const int64_t nq = (int64_t)F * tpf;
+  // stage the prompt tile (transposed) and its norms / buckets
+  for (int idx = tid; idx < kCP * (D / 8); idx += blockDim.x) {
+    const int col = idx % kCP, c8 = idx / kCP;
+    float v[8];
+    if (p0 + col < P) {
+      load8(kp + ((int64_t)h * P + p0 + col) * D + c8 * 8, v);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) Ks[(c8 * 8 + u) * kCP + col] = v[u];
+  }
+  __syncthreads();
+  if (tid < kCP) {
+    float ss = 0.f;
+    for (int k = 0; k < D; ++k) ss = fmaf(Ks[k * kCP + tid], Ks[k * kCP + tid], ss);
+    const float nrm = sqrtf(ss);
+    pinv[tid] = nrm > 0.f ? 1.0f / nrm : 0.f;
+    pbs[tid] = p0 + tid < P ? pb[(int64_t)h * P + p0 + tid] : -1;
+  }
+  const int ty = tid >> 4, tx = tid & 15;
+  float best[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) best[c] = neg_inf();
+  for (int64_t t0 = 0; t0 < tpf; t0 += kCQ) {
+    __syncthreads();
+    for (int idx = tid; idx < kCQ * (D / 8); idx += blockDim.x) {
+      const int row = idx % kCQ, c8 = idx / kCQ;
+      float v[8];
+      if (t0 + row < tpf) {
+        load8(q + h * hs + ((int64_t)f * tpf + t0 + row) * ts + c8 * 8, v);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) Qs[(c8 * 8 + u) * kCQ + row] = v[u];
+    }
+    for (int idx = tid; idx < kCQ * r; idx += blockDim.x) {
+      const int row = idx / r, s = idx - row * r;
+      qbs[row * FASTAR_MAX_R + s] =
+          t0 + row < tpf ? qb[((int64_t)h * nq + (int64_t)f * tpf + t0 + row) * r + s] : -2;
+    }
+    __syncthreads();
+    if (tid < kCQ) {
+      float ss = 0.f;
+      for (int k = 0; k < D; ++k) ss = fmaf(Qs[k * kCQ + tid], Qs[k * kCQ + tid], ss);
+      const float nrm = sqrtf(ss);
+      qinv[tid] = (t0 + tid < tpf && nrm > 0.f) ? 1.0f / nrm : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) {
+      const float4 qa = *reinterpret_cast<const float4*>(Qs + k * kCQ + ty * 4);
+      const float4 kb = *reinterpret_cast<const float4*>(Ks + k * kCP + tx * 4);
+      const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
+      const float kv[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], kv[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int row = ty * 4 + a;
+      if (t0 + row >= tpf) continue;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int col = tx * 4 + b;
+        bool ok = pbs[col] >= 0;
+        if (ok && gate) {
+          bool shared = false;
+          for (int s = 0; s < r; ++s) shared |= qbs[row * FASTAR_MAX_R + s] == pbs[col];
+          ok = shared;
+        }
+        if (ok) best[b] = fmaxf(best[b], acc[a][b] * qinv[row] * pinv[col]);
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < 4; ++b) red[ty * kCP + tx * 4 + b] = best[b];
+  __syncthreads();
+  if (tid < kCP && p0 + tid < P) {
+    float mx = neg_inf();
+    for (int y = 0; y < 16; ++y) mx = fmaxf(mx, red[y * kCP + tid]);
+    score[((int64_t)h * F + f) * P + p0 + tid] = mx;
+  }
+}
+
+// One CTA per (head, frame): rank = #{p' : (s', p') precedes (s, p)} in the order
+// (score desc, index asc), -inf last; keep = s >= tau_ca or rank < min(topk, P).
+__global__ void __launch_bounds__(1024)
+annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restrict__ score,
+                  uint8_t* __restrict__ keep, int32_t* __restrict__ kidx, int32_t* __restrict__ kcnt) {
+  __shared__ float s[FASTAR_MAX_P];
+  __shared__ int wsum[32];
+  const int hf = blockIdx.x;
+  const int p = threadIdx.x;
+  const float* sc = score + (int64_t)hf * P;
+  if (p < P) s[p] = sc[p];
+  __syncthreads();
+  int k = 0;
+  if (p < P) {
+    const float mine = s[p];
+    int rank = 0;
+    for (int u = 0; u < P; ++u) {
+      const float o = s[u];
+      rank += (o > mine || (o == mine && u < p)) ? 1 : 0;
+    }
+    const int lim = topk < P ? topk : (int)P;
+    k = (mine >= tau_ca || rank < lim) ? 1 : 0;
+    keep[(int64_t)hf * P + p] = (uint8_t)k;
+  }
+  // exclusive scan of the keep flags in index order
+  const int lane = p & 31, warp = p >> 5;
+  int incl = k;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = wsum[lane];
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += v;
+    }
+    wsum[lane] = ti - t;
+  }
+  __syncthreads();
+  const int pos = wsum[warp] + incl - k;
+  __shared__ int total;
+  if (p == blockDim.x - 1) total = pos + k;
+  __syncthreads();
+  if (p < P) {
+    int32_t* out = kidx + (int64_t)hf * P;
+    if (k) out[pos] = p;
+    if (p >= total) out[p] = -1;
+  }
+  if (p == 0) kcnt[hf] = total;
+}
+
+size_t annca_workspace(int H, int F, int64_t P) { return sizeof(float) * (size_t)H * F * P + 256; }
+
+template <typename T, int D>
+static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r,
+                              const void* kp, const int32_t* pb, int64_t P, int gate, float* score,
+                              cudaStream_t s) {
+  const size_t smem = sizeof(float) * ((size_t)D * kCQ + (size_t)D * kCP + kCQ + kCP + 16 * kCP) +
+                      sizeof(int) * ((size_t)kCQ * FASTAR_MAX_R + kCP);
+  auto kern = annca_score_kernel<T, D>;
+  static const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return attr;
+  kern<<<dim3((unsigned)((P + kCP - 1) / kCP), H, F), 256, smem, s>>>(
+      static_cast<const T*>(q.p), q.hs, q.ts, F, tpf, qb, r, static_cast<const T*>(kp), pb, P, gate, score);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb,
+                                int r, const void* kp, const int32_t* pb, int64_t P, float tau_ca, int topk,
+                                int gate, uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
+                                void* ws, cudaStream_t s) {
+  if (H == 0 || F == 0) return cudaSuccess;
+  float* sc = score ? score : static_cast<float*>(ws);
+  cudaError_t e = cudaSuccess;
+  if (P > 0) {
+    if (dtype == FASTAR_BF16) {
+      e = d == 128 ? annca_impl<__nv_bfloat16, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s)
+                   : annca_impl<__nv_bfloat16, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s);
+    } else {
+      e = d == 128 ? annca_impl<float, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s)
+                   : annca_impl<float, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  int threads = (int)((P + 31) / 32 * 32);
+  if (threads < 32) threads = 32;
+  annca_rank_kernel<<<H * F, threads, 0, s>>>(F, P, tau_ca, topk, sc, keep, kidx, kcnt);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace fastar

@@ -1,0 +1,215 @@
+// TempCache compaction: drop evicted entries, append the current chunk as the most
+// recent representatives, keep at most M entries (oldest dropped first).
+//
+// FAST-AR technical summary §2.A ("bounds the growth of the KV cache") and blog §1
+// ("only the most recent representative stays in the cache"); the FIFO hard cap is
+// the method spec's.
+//
+// Two kernels: a one-CTA-per-head scan that writes the slot -> source map and the
+// new length, then a bandwidth kernel that moves rows with 16-byte accesses.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fastar {
+
+constexpr int kScanThreads = 1024;
+
+// Slot s of the new cache takes: survivor number (s + drop) if s + drop < S, else
+// current token (s + drop - S); drop = max(0, S + nq - M).
+__global__ void __launch_bounds__(kScanThreads)
+compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
+                    const uint8_t* __restrict__ evict, int32_t* __restrict__ len_out,
+                    int32_t* __restrict__ index_map, int32_t* status) {
+  __shared__ int warp_tot[kScanThreads / 32];
+  __shared__ int s_total;
+  const int h = blockIdx.x;
+  int64_t n = len_in[h];
+  if (n < 0 || n > M) {
+    if (threadIdx.x == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
+    n = n < 0 ? 0 : M;
+  }
+  const uint8_t* e = evict + (int64_t)h * M;
+  int32_t* imap = index_map + (int64_t)h * M;
+  const int64_t per = (n + kScanThreads - 1) / kScanThreads;
+  const int64_t beg = threadIdx.x * per;
+  const int64_t end = beg + per < n ? beg + per : n;
+  int local = 0;
+  for (int64_t j = beg; j < end; ++j) local += e[j] ? 0 : 1;
+  // block exclusive scan of the per-thread survivor counts
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += v;
+    }
+    warp_tot[lane] = ti - t;
+    if (lane == 31) s_total = ti;
+  }
+  __syncthreads();
+  const int64_t S = s_total;
+  const int64_t total = S + nq;
+  const int64_t drop = total > M ? total - M : 0;
+  const int64_t L = total - drop;
+  int64_t rank = warp_tot[warp] + incl - local;
+  for (int64_t j = beg; j < end; ++j) {
+    if (!e[j]) {
+      const int64_t slot = rank - drop;
+      if (slot >= 0) imap[slot] = (int32_t)j;
+      ++rank;
+    }
+  }
+  for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
+    const int64_t slot = S + i - drop;
+    if (slot >= 0) imap[slot] = (int32_t)(n + i);
+  }
+  for (int64_t s = L + threadIdx.x; s < M; s += blockDim.x) imap[s] = -1;
+  if (threadIdx.x == 0) len_out[h] = (int32_t)L;
+}
+
+// One 16-byte chunk per thread; VPR chunks per row.  Metadata moves with the row.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, const T* __restrict__ vc,
+                    int64_t hs, int64_t ts, const float* __restrict__ kcn, const int32_t* __restrict__ kcb,
+                    const T* __restrict__ kin, const T* __restrict__ vin, const float* __restrict__ knin,
+                    const int32_t* __restrict__ kbin, const int32_t* __restrict__ len_in,
+                    const int32_t* __restrict__ len_out, const int32_t* __restrict__ index_map,
+                    T* __restrict__ kout, T* __restrict__ vout, float* __restrict__ knout,
+                    int32_t* __restrict__ kbout, int32_t* status) {
+  constexpr int VPR = D * (int)sizeof(T) / 16;
+  const int64_t total = (int64_t)H * M * VPR;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = g / VPR;
+    const int c = (int)(g - row * VPR);
+    const int h = (int)(row / M);
+    const int64_t slot = row - (int64_t)h * M;
+    if (slot >= len_out[h]) continue;
+    int64_t n = len_in[h];
+    n = n < 0 ? 0 : (n > M ? M : n);
+    const int64_t src = index_map[row];
+    const uint4* ks;
+    const uint4* vs;
+    float kn;
+    int32_t kb;
+    if (src >= 0 && src < n) {
+      ks = reinterpret_cast<const uint4*>(kin + ((int64_t)h * M + src) * D) + c;
+      vs = reinterpret_cast<const uint4*>(vin + ((int64_t)h * M + src) * D) + c;
+      kn = knin[(int64_t)h * M + src];
+      kb = kbin[(int64_t)h * M + src];
+    } else if (src >= n && src < n + nq) {
+      const int64_t i = src - n;
+      ks = reinterpret_cast<const uint4*>(kc + h * hs + i * ts) + c;
+      vs = reinterpret_cast<const uint4*>(vc + h * hs + i * ts) + c;
+      kn = kcn[(int64_t)h * nq + i];
+      kb = kcb[(int64_t)h * nq + i];
+    } else {
+      if (c == 0) flag_status(status, FASTAR_DEV_BAD_INDEX);
+      continue;
+    }
+    reinterpret_cast<uint4*>(kout + row * D)[c] = __ldg(ks);
+    reinterpret_cast<uint4*>(vout + row * D)[c] = __ldg(vs);
+    if (c == 0) {
+      knout[row] = kn;
+      kbout[row] = kb;
+    }
+  }
+}
+
+template <typename T, int D>
+static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView vc, const float* kcn,
+                             const int32_t* kcb, const void* kin, const void* vin, const float* knin,
+                             const int32_t* kbin, const int32_t* len_in, const int32_t* len_out,
+                             const int32_t* imap, void* kout, void* vout, float* knout, int32_t* kbout,
+                             int32_t* status, cudaStream_t s) {
+  constexpr int VPR = D * (int)sizeof(T) / 16;
+  const int64_t total = (int64_t)H * M * VPR;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  compact_copy_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>(
+      H, nq, M, static_cast<const T*>(kc.p), static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb,
+      static_cast<const T*>(kin), static_cast<const T*>(vin), knin, kbin, len_in, len_out, imap,
+      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M, TokView kc,
+                                 TokView vc, const float* kcn, const int32_t* kcb, const void* kin,
+                                 const void* vin, const float* knin, const int32_t* kbin,
+                                 const int32_t* len_in, const uint8_t* evict, void* kout, void* vout,
+                                 float* knout, int32_t* kbout, int32_t* len_out, int32_t* imap,
+                                 int32_t* status, cudaStream_t s) {
+  compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dtype == FASTAR_BF16) {
+    if (d == 128)
+      return copy_impl<__nv_bfloat16, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+    return copy_impl<__nv_bfloat16, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+  }
+  if (d == 128)
+    return copy_impl<float, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+  return copy_impl<float, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+}
+
+// ---------------------------------------------------------------------------------------
+// Dense baseline: append the current chunk to an append-only cache.
+// ---------------------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+dense_append_kernel(int H, int64_t nq, const T* __restrict__ kc, const T* __restrict__ vc, int64_t hs,
+                    int64_t ts, T* __restrict__ kd, T* __restrict__ vd, int64_t cap, int64_t at) {
+  constexpr int VPR = D * (int)sizeof(T) / 16;
+  const int64_t total = (int64_t)H * nq * VPR;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = g / VPR;
+    const int c = (int)(g - row * VPR);
+    const int h = (int)(row / nq);
+    const int64_t i = row - (int64_t)h * nq;
+    const int64_t dst = ((int64_t)h * cap + at + i) * D;
+    reinterpret_cast<uint4*>(kd + dst)[c] = __ldg(reinterpret_cast<const uint4*>(kc + h * hs + i * ts) + c);
+    reinterpret_cast<uint4*>(vd + dst)[c] = __ldg(reinterpret_cast<const uint4*>(vc + h * hs + i * ts) + c);
+  }
+}
+
+template <typename T, int D>
+static cudaError_t append_impl(int H, int64_t nq, TokView kc, TokView vc, void* kd, void* vd, int64_t cap,
+                               int64_t at, cudaStream_t s) {
+  constexpr int VPR = D * (int)sizeof(T) / 16;
+  int64_t blocks = ((int64_t)H * nq * VPR + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  dense_append_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>(
+      H, nq, static_cast<const T*>(kc.p), static_cast<const T*>(vc.p), kc.hs, kc.ts,
+      static_cast<T*>(kd), static_cast<T*>(vd), cap, at);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_append(int dtype, int d, int H, int64_t nq, TokView kc, TokView vc, void* kd,
+                                void* vd, int64_t cap, int64_t at, cudaStream_t s) {
+  if (nq == 0) return cudaSuccess;
+  if (dtype == FASTAR_BF16) {
+    if (d == 128) return append_impl<__nv_bfloat16, 128>(H, nq, kc, vc, kd, vd, cap, at, s);
+    return append_impl<__nv_bfloat16, 64>(H, nq, kc, vc, kd, vd, cap, at, s);
+  }
+  if (d == 128) return append_impl<float, 128>(H, nq, kc, vc, kd, vd, cap, at, s);
+  return append_impl<float, 64>(H, nq, kc, vc, kd, vd, cap, at, s);
+}
+
+}  // namespace fastar

@@ -1,0 +1,95 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fastar.h"
+
+namespace fastar {
+
+// A token tensor: element (h, t, c) lives at p + h*hs + t*ts + c (elements).
+struct TokView {
+  const void* p;
+  int64_t hs, ts;
+};
+
+// Counts kernels enqueued by the library (a diagnostic the ABI exports).
+void count_launches(int n);
+
+// ---- buckets ------------------------------------------------------------------------
+cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, const void* centroids,
+                                 int B, int r, int32_t* ids, float* scores, float* norms,
+                                 cudaStream_t s);
+cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
+                               const int32_t* n_valid, int32_t* perm, int32_t* offsets,
+                               int32_t* status, cudaStream_t s);
+
+// ---- TempCache ----------------------------------------------------------------------
+int match_splits(int H, int64_t nq, int64_t M);
+size_t match_workspace(int H, int64_t nq, int64_t M);
+cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kcur, int H, int64_t nq,
+                                   const void* cache_k, const float* cache_knorm,
+                                   const int32_t* cache_len, int64_t M, float tau, int32_t* top1,
+                                   float* s1, float* s2, uint8_t* evict, int32_t* status,
+                                   void* ws, cudaStream_t s);
+cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M, TokView kcur,
+                                 TokView vcur, const float* kcur_norm, const int32_t* kcur_bucket,
+                                 const void* k_in, const void* v_in, const float* knorm_in,
+                                 const int32_t* kb_in, const int32_t* len_in, const uint8_t* evict,
+                                 void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
+                                 int32_t* len_out, int32_t* index_map, int32_t* status,
+                                 cudaStream_t s);
+
+// ---- attention ------------------------------------------------------------------------
+enum AttnMode { kDense = 0, kCross = 1, kSparse = 2 };
+
+struct AttnArgs {
+  int mode;
+  int H;
+  TokView q;
+  int64_t nq;
+  // keys/values: dense -> (k, v, kv_hs, kv_ts, nk); cross -> prompt [H,P,d]; sparse -> cache [H,M,d]
+  const void* k;
+  const void* v;
+  int64_t kv_hs, kv_ts, nk;
+  // cross
+  int F;
+  int64_t tpf;
+  const int32_t* kidx;
+  const int32_t* kcnt;
+  int64_t P;
+  // sparse
+  int r, B;
+  const int32_t* qperm;
+  const int32_t* qoff;
+  const int32_t* kperm;
+  const int32_t* koff;
+  int64_t M;
+  float scale;
+  // outputs
+  void* out;
+  int64_t o_hs, o_ts;
+  float* lse;
+  float* part_o;    // sparse partials [H, nq*r, d]
+  float* part_lse;  // [H, nq*r]
+  int32_t* status;
+};
+
+size_t sparse_attn_workspace(int H, int64_t nq, int d, int r);
+cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s);
+
+// ---- AnnCA --------------------------------------------------------------------------
+size_t annca_workspace(int H, int F, int64_t P);
+cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf,
+                                const int32_t* qb, int r, const void* kp, const int32_t* pb,
+                                int64_t P, float tau_ca, int topk, int gate, uint8_t* keep,
+                                int32_t* kidx, int32_t* kcnt, float* score, void* ws,
+                                cudaStream_t s);
+
+// ---- dense cache append --------------------------------------------------------------
+cudaError_t launch_dense_append(int dtype, int d, int H, int64_t nq, TokView kcur, TokView vcur,
+                                void* k_cache, void* v_cache, int64_t cap, int64_t at,
+                                cudaStream_t s);
+
+}  // namespace fastar

@@ -1,0 +1,372 @@
+// TempCache top-1 match on the 5th-generation tensor cores (bf16 inputs).
+//
+// FAST-AR technical summary §2.A / blog §1: for each current-frame query, the top-1
+// nearest cached key (cosine).  Per head this is a GEMM S = Q K^T (M = Nq, N = n,
+// K = d) whose N dimension is reduced on the fly by an arg-max epilogue: scores
+// never leave the SM.
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: the unit's 256 query rows once (two M=128 tiles), then
+//               128-key tiles of the cache through a 4-deep shared-memory ring;
+//   warp 1      owns TMEM (512 columns = 2 accumulator stages x 2 M-tiles x 128
+//               columns) and issues tcgen05.mma (one thread), committing to the
+//               ring's "empty" barriers and the accumulator's "full" barrier;
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant (one per M-tile): load
+//               128 fp32 scores per row with tcgen05.ld, scale by 1/|k_j|, keep
+//               the running top-1 (and top-2 when asked), release the stage.
+// The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
+// 256-query block, key segment); segments split the cache so the unit count
+// fills the machine, and a small finaliser merges the segments' partial top-2s.
+// Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace fastar {
+
+namespace {
+
+constexpr int kQ = 256;         // queries per unit
+constexpr int kN = 128;         // keys per tile
+constexpr int kStages = 4;      // B ring depth
+constexpr int kThreads = 320;   // 10 warps
+constexpr int kTile = 128 * 128; // bytes of one 128-row x 64-element bf16 swizzled block
+
+template <int D>
+struct alignas(1024) MatchSmem {
+  uint8_t a[2][D / 64][kTile];
+  uint8_t b[kStages][D / 64][kTile];
+  float invk[8][kN];
+  uint64_t a_full, a_empty;
+  uint64_t b_full[kStages], b_empty[kStages];
+  uint64_t t_full[2], t_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct MatchGeom {
+  int H, QB, S;
+  int64_t nq, M;
+};
+
+struct Unit {
+  int h, qb, seg, nm, rows;
+  int t_beg, t_end;   // key tiles [t_beg, t_end)
+  int64_t n;
+};
+
+__device__ __forceinline__ Unit decode(const MatchGeom& g, int u, const int32_t* clen) {
+  Unit w;
+  w.seg = u % g.S;
+  const int t = u / g.S;
+  w.qb = t % g.QB;
+  w.h = t / g.QB;
+  const int64_t r = g.nq - (int64_t)w.qb * kQ;
+  w.rows = (int)(r < kQ ? r : kQ);
+  w.nm = (w.rows + 127) / 128;
+  int64_t n = clen[w.h];
+  n = n < 0 ? 0 : (n > g.M ? g.M : n);
+  w.n = n;
+  const int tiles = (int)((n + kN - 1) / kN);
+  const int per = (tiles + g.S - 1) / g.S;
+  w.t_beg = w.seg * per;
+  w.t_end = w.t_beg + per < tiles ? w.t_beg + per : tiles;
+  if (w.t_end < w.t_beg) w.t_end = w.t_beg;
+  return w;
+}
+
+struct Best {
+  float m1;
+  int i1;
+  float m2;
+};
+
+template <bool kTop2>
+__device__ __forceinline__ void fold32(Best& b, const float* w, int j0) {
+  float gm = w[0];
+#pragma unroll
+  for (int i = 1; i < 32; ++i) gm = fmaxf(gm, w[i]);
+  if (kTop2) {
+    if (gm > b.m2) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float v = w[i];
+        if (v > b.m1) {
+          b.m2 = b.m1;
+          b.m1 = v;
+          b.i1 = j0 + i;
+        } else if (v > b.m2) {
+          b.m2 = v;
+        }
+      }
+    }
+  } else if (gm > b.m1) {
+    int idx = 31;
+#pragma unroll
+    for (int i = 31; i >= 0; --i)
+      if (w[i] == gm) idx = i;
+    b.m1 = gm;
+    b.i1 = j0 + idx;
+  }
+}
+
+template <int D, bool kTop2>
+__global__ void __launch_bounds__(kThreads, 1)
+match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const float* __restrict__ cknorm, const int32_t* __restrict__ clen, MatchGeom g,
+                float4* __restrict__ part, uint8_t* __restrict__ evict, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  MatchSmem<D>& sm = *reinterpret_cast<MatchSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int KH = D / 64;
+  constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kN);
+
+  // clear the eviction flags (the finaliser sets them after this kernel)
+  {
+    const int64_t total = (int64_t)g.H * g.M;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < total; j += (int64_t)gridDim.x * blockDim.x)
+      evict[j] = 0;
+  }
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&sm.a_full, 1);
+    tc::mbar_init(&sm.a_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sm.b_full[s], 1);
+      tc::mbar_init(&sm.b_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&sm.t_full[s], 1);
+      tc::mbar_init(&sm.t_empty[s], 8);
+    }
+    sm.abort = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sm.tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+  const int units = g.H * g.QB * g.S;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+        const Unit w = decode(g, u, clen);
+        if (w.t_end <= w.t_beg) continue;
+        if (!tc::mbar_wait(&sm.a_empty, aph ^ 1, abort)) break;
+        aph ^= 1;
+        tc::mbar_arrive_tx(&sm.a_full, (uint32_t)(w.nm * KH * kTile));
+        for (int m = 0; m < w.nm; ++m)
+          for (int kh = 0; kh < KH; ++kh)
+            tc::tma_load_3d(sm.a[m][kh], &tm_q, kh * 64, w.qb * kQ + m * 128, w.h, &sm.a_full);
+        for (int t = w.t_beg; t < w.t_end; ++t) {
+          if (!tc::mbar_wait(&sm.b_empty[stage], ph ^ 1, abort)) break;
+          tc::mbar_arrive_tx(&sm.b_full[stage], (uint32_t)(KH * kTile));
+          for (int kh = 0; kh < KH; ++kh)
+            tc::tma_load_3d(sm.b[stage][kh], &tm_k, kh * 64, t * kN, w.h, &sm.b_full[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t ph = 0, aph = 0, tph = 0;
+      for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+        const Unit w = decode(g, u, clen);
+        if (w.t_end <= w.t_beg) continue;
+        if (!tc::mbar_wait(&sm.a_full, aph, abort)) break;
+        aph ^= 1;
+        tc::tc_fence_after();
+        for (int t = w.t_beg; t < w.t_end; ++t) {
+          if (!tc::mbar_wait(&sm.b_full[stage], ph, abort)) break;
+          if (!tc::mbar_wait(&sm.t_empty[acc], tph ^ 1, abort)) break;
+          tc::tc_fence_after();
+          for (int m = 0; m < w.nm; ++m) {
+            const uint32_t d = tmem + (uint32_t)(acc * 256 + m * 128);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t koff = (uint32_t)((k & 3) * 32);
+              const uint64_t ad = tc::sw128_desc(tc::smem_u32(sm.a[m][k >> 2]) + koff);
+              const uint64_t bd = tc::sw128_desc(tc::smem_u32(sm.b[stage][k >> 2]) + koff);
+              tc::mma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(&sm.b_empty[stage]);
+          tc::mma_commit(&sm.t_full[acc]);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1;
+          }
+          if (++acc == 2) {
+            acc = 0;
+            tph ^= 1;
+          }
+        }
+        tc::mma_commit(&sm.a_empty);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;          // 0..7
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int m = ew >> 2;            // which M-tile (accumulator) this warp reads
+    float* inv = sm.invk[ew];
+    int acc = 0;
+    uint32_t tph = 0;
+    for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+      const Unit w = decode(g, u, clen);
+      const int rloc = m * 128 + quad * 32 + lane;
+      const int64_t i = (int64_t)w.qb * kQ + rloc;
+      Best b{neg_inf(), INT_MAX, neg_inf()};
+      const float* kn = cknorm + (int64_t)w.h * g.M;
+      for (int t = w.t_beg; t < w.t_end; ++t) {
+        const int64_t j0 = (int64_t)t * kN;
+        // 1/|k_j| of the tile's 128 keys into this warp's buffer
+        {
+          const int64_t j = j0 + lane * 4;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float x = (j + c < w.n) ? kn[j + c] : 0.f;
+            inv[lane * 4 + c] = x > 0.f ? __frcp_rn(x) : 0.f;
+          }
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
+        tc::tc_fence_after();
+        if (m < w.nm) {
+          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128);
+          const bool partial = j0 + kN > w.n;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tc::tmem_ld32(taddr + c * 32, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 s = *reinterpret_cast<const float4*>(inv + c * 32 + q4 * 4);
+              v[q4 * 4 + 0] *= s.x;
+              v[q4 * 4 + 1] *= s.y;
+              v[q4 * 4 + 2] *= s.z;
+              v[q4 * 4 + 3] *= s.w;
+            }
+            if (partial) {
+#pragma unroll
+              for (int x = 0; x < 32; ++x)
+                if (j0 + c * 32 + x >= w.n) v[x] = neg_inf();
+            }
+            fold32<kTop2>(b, v, (int)(j0 + c * 32));
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          tph ^= 1;
+        }
+      }
+      if (m * 128 < w.rows && rloc < w.rows && !*abort)
+        part[((int64_t)w.seg * g.H + w.h) * g.nq + i] = make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && sm.abort) flag_status(status, FASTAR_DEV_TIMEOUT);
+}
+
+template <int D>
+constexpr size_t match_tc_smem() {
+  return sizeof(MatchSmem<D>) + 1024;
+}
+
+}  // namespace
+
+int match_tc_splits(int H, int64_t nq, int64_t M) {
+  const int nsm = sm_count();
+  const int64_t qb = (nq + kQ - 1) / kQ;
+  const int64_t tiles = (M + kN - 1) / kN;
+  int best_s = 1;
+  double best = 1e30;
+  for (int s = 1; s <= 8; ++s) {
+    const int64_t units = H * qb * s;
+    const int64_t waves = (units + nsm - 1) / nsm;
+    const double cost = (double)waves * ((double)((tiles + s - 1) / s) + 2.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+size_t match_tc_workspace(int H, int64_t nq, int64_t M) {
+  return sizeof(float4) * (size_t)8 * H * (size_t)nq;
+}
+
+// Launches the tensor-core match (writes `part` as [S, H, nq] and clears evict).
+// Returns the number of segments S the finaliser must merge, or -1 on a failure to
+// set the kernel up (tensor maps, attributes).
+template <int D>
+static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, const float* cknorm,
+                                const int32_t* clen, int64_t M, bool top2, float4* part, uint8_t* evict,
+                                int32_t* status, cudaStream_t s) {
+  CUtensorMap tq, tk;
+  if (!make_tmap_bf16_3d(&tq, q.p, D, (uint64_t)nq, (uint64_t)H, (uint64_t)q.ts * 2, (uint64_t)q.hs * 2, 64, 128))
+    return -1;
+  if (!make_tmap_bf16_3d(&tk, ck, D, (uint64_t)M, (uint64_t)H, (uint64_t)D * 2, (uint64_t)M * D * 2, 64, 128))
+    return -1;
+  MatchGeom g;
+  g.H = H;
+  g.nq = nq;
+  g.M = M;
+  g.QB = (int)((nq + kQ - 1) / kQ);
+  g.S = match_tc_splits(H, nq, M);
+  const int units = g.H * g.QB * g.S;
+  const int grid = units < sm_count() ? units : sm_count();
+  constexpr size_t smem = match_tc_smem<D>();
+  if (top2) {
+    static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, true>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a != cudaSuccess) return -1;
+    match_tc_kernel<D, true><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
+  } else {
+    static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, false>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a != cudaSuccess) return -1;
+    match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
+  }
+  count_launches(1);
+  return g.S;
+}
+
+int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,
+                    int64_t M, bool top2, float4* part, uint8_t* evict, int32_t* status, cudaStream_t s) {
+  if (d == 128) return launch_match_tc_impl<128>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, status, s);
+  return launch_match_tc_impl<64>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, status, s);
+}
+
+}  // namespace fastar

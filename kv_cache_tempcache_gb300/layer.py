@@ -1,0 +1,274 @@
+"""One FAST-AR attention layer on one GPU: cache state, the per-chunk step, and the
+dense baseline, all driven through libfastar's C ABI.
+
+PyTorch only supplies device memory, streams, events and CUDA graphs; every stage
+of the step runs in libfastar's kernels (there is no fallback path: a missing
+library raises).
+
+The step for one chunk of Nq = F*Tf tokens (FAST-AR technical summary §2.A–C):
+  1. buckets of the queries (top-r) and of the current keys (argmax, plus |k|)
+  2. TempCache top-1 match of every query against the cache -> eviction flags
+  3. compaction into the other half of a double-buffered cache (FIFO cap M)
+  4. counting sort of the cache keys and of the (query, slot) pairs by bucket
+  5. AnnSA bucket-restricted self-attention -> o_self
+  6. AnnCA prompt selection per latent frame
+  7. cross-attention over the kept prompt tokens -> o_cross
+Stages 6-7 depend only on stage 1, so they run on a second stream alongside 2-5.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+
+def _i32(*shape, dev):
+    return torch.zeros(shape, dtype=torch.int32, device=dev)
+
+
+def _f32(*shape, dev):
+    return torch.zeros(shape, dtype=torch.float32, device=dev)
+
+
+class CacheState:
+    """One half of the double-buffered TempCache: rows, norms, buckets, lengths."""
+
+    def __init__(self, H, M, d, dtype, dev):
+        self.k = torch.zeros((H, M, d), dtype=dtype, device=dev)
+        self.v = torch.zeros((H, M, d), dtype=dtype, device=dev)
+        self.knorm = _f32(H, M, dev=dev)
+        self.kb = _i32(H, M, 1, dev=dev)
+        self.len = _i32(H, dev=dev)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.knorm, self.kb, self.len))
+
+
+class FastARLayer:
+    """Device state and step of one FAST-AR attention layer (one head group, one GPU)."""
+
+    def __init__(self, H: int, d: int, Tf: int, F: int, M: int, B: int, r: int, P: int, tau: float,
+                 tau_ca: float, topk: int = 16, dtype: torch.dtype = torch.bfloat16, gate: bool = True,
+                 device: str | torch.device = "cuda", scale: Optional[float] = None):
+        L.load()
+        if M < F * Tf:
+            raise ValueError(f"cache cap M={M} must hold one chunk of {F * Tf} tokens")
+        self.H, self.d, self.Tf, self.F, self.M, self.B, self.r, self.P = H, d, Tf, F, M, B, r, P
+        self.Nq = F * Tf
+        self.tau, self.tau_ca, self.topk, self.gate = float(tau), float(tau_ca), int(topk), bool(gate)
+        self.dtype = dtype
+        self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+        dev = torch.device(device)
+        self.dev = dev
+        Nq = self.Nq
+        self.caches = [CacheState(H, M, d, dtype, dev), CacheState(H, M, d, dtype, dev)]
+        self.cur = 0
+        # prompt
+        self.kp = torch.zeros((H, P, d), dtype=dtype, device=dev)
+        self.vp = torch.zeros((H, P, d), dtype=dtype, device=dev)
+        self.pb = _i32(H, P, 1, dev=dev)
+        self.centroids = torch.zeros((H, B, d), dtype=dtype, device=dev)
+        # per-step intermediates and outputs
+        self.qb = _i32(H, Nq, r, dev=dev)
+        self.kb_cur = _i32(H, Nq, 1, dev=dev)
+        self.kcur_norm = _f32(H, Nq, dev=dev)
+        self.top1 = _i32(H, Nq, dev=dev)
+        self.s1 = _f32(H, Nq, dev=dev)
+        self.s2 = _f32(H, Nq, dev=dev)
+        self.evict = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+        self.index_map = _i32(H, M, dev=dev)
+        self.kperm = _i32(H, M, dev=dev)
+        self.koff = _i32(H, B + 1, dev=dev)
+        self.qperm = _i32(H, Nq * r, dev=dev)
+        self.qoff = _i32(H, B + 1, dev=dev)
+        self.o_self = torch.zeros((H, Nq, d), dtype=dtype, device=dev)
+        self.lse_self = _f32(H, Nq, dev=dev)
+        self.keep = torch.zeros((H, F, P), dtype=torch.uint8, device=dev)
+        self.kidx = _i32(H, F, P, dev=dev)
+        self.kcnt = _i32(H, F, dev=dev)
+        self.score = _f32(H, F, P, dev=dev)
+        self.o_cross = torch.zeros((H, Nq, d), dtype=dtype, device=dev)
+        self.lse_cross = _f32(H, Nq, dev=dev)
+        self.dev_status = _i32(1, dev=dev)
+
+        def ws(op, **kw):
+            nbytes = L.workspace_bytes(op, H, **kw)
+            return torch.zeros(max(16, (nbytes + 15) // 16 * 16), dtype=torch.uint8, device=dev)
+
+        self.ws_match = ws(L.OP_MATCH, n=Nq, M=M, d=d)
+        self.ws_attn = ws(L.OP_SPARSE_ATTN, n=Nq, M=M, d=d, B=B, r=r)
+        self.side = torch.cuda.Stream(device=dev)
+        self._graph = None
+        self._graph_dir = None
+
+    # ---- state ------------------------------------------------------------------------------
+    @property
+    def cache(self) -> CacheState:
+        return self.caches[self.cur]
+
+    def device_bytes(self) -> int:
+        """Bytes of every device buffer the layer holds (constant over a rollout)."""
+        tot = sum(c.nbytes() for c in self.caches)
+        for t in vars(self).values():
+            if isinstance(t, torch.Tensor):
+                tot += t.numel() * t.element_size()
+        return tot
+
+    def set_centroids(self, C: torch.Tensor):
+        self.centroids.copy_(C)
+
+    def set_prompt(self, kp: torch.Tensor, vp: torch.Tensor):
+        """Installs the prompt and assigns its key buckets (once per rollout)."""
+        self.kp.copy_(kp)
+        self.vp.copy_(vp)
+        if self.P:
+            L.fastar_bucket_assign(self.kp, self.centroids, 1, self.pb)
+
+    def load_cache(self, k: torch.Tensor, v: torch.Tensor):
+        """Installs n raw entries (oldest first) as the current cache: norms and key
+        buckets are computed by the library."""
+        n = k.shape[1]
+        if n > self.M:
+            raise ValueError("more entries than the cache cap")
+        c = self.cache
+        c.k[:, :n].copy_(k)
+        c.v[:, :n].copy_(v)
+        if n:
+            kb = _i32(self.H, n, 1, dev=self.dev)
+            kn = _f32(self.H, n, dev=self.dev)
+            L.fastar_bucket_assign(c.k[:, :n], self.centroids, 1, kb, None, kn)
+            c.kb[:, :n].copy_(kb)
+            c.knorm[:, :n].copy_(kn)
+        c.len.fill_(n)
+
+    def reset(self):
+        for c in self.caches:
+            c.len.zero_()
+        self.cur = 0
+
+    # ---- the step ------------------------------------------------------------------------------
+    def _enqueue(self, q, k_cur, v_cur, src: int, timer=None):
+        """Enqueues one step reading cache `src` and writing cache 1 - src.
+
+        timer: optional callable(name, stream, phase) invoked around each stage
+        ("begin"/"end") on the stream the stage is launched on (for per-stage timing
+        with CUDA events; never used inside a graph capture)."""
+        cin, cout = self.caches[src], self.caches[1 - src]
+        main = torch.cuda.current_stream(self.dev)
+        t = timer or (lambda *a: None)
+        t("bucket_assign", main, "begin")
+        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
+        L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
+        t("bucket_assign", main, "end")
+        # AnnCA branch on the side stream
+        ev = torch.cuda.Event()
+        ev.record(main)
+        self.side.wait_event(ev)
+        with torch.cuda.stream(self.side):
+            t("annca_select", self.side, "begin")
+            L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate,
+                                  self.keep, self.kidx, self.kcnt, self.score)
+            t("annca_select", self.side, "end")
+            t("cross_attn_subset", self.side, "begin")
+            L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale,
+                                       self.o_cross, self.lse_cross)
+            t("cross_attn_subset", self.side, "end")
+        # TempCache + AnnSA on the main stream
+        t("tempcache_match", main, "begin")
+        L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, self.s2,
+                                 self.evict, self.dev_status, self.ws_match)
+        t("tempcache_match", main, "end")
+        t("cache_compact", main, "begin")
+        L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                               cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
+                               self.index_map, self.dev_status)
+        t("cache_compact", main, "end")
+        t("bucket_sort", main, "begin")
+        L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
+        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        t("bucket_sort", main, "end")
+        t("sparse_attn", main, "begin")
+        L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
+                             self.scale, self.o_self, self.lse_self, self.dev_status, self.ws_attn)
+        t("sparse_attn", main, "end")
+        ev2 = torch.cuda.Event()
+        ev2.record(self.side)
+        main.wait_event(ev2)
+
+    def step(self, q, k_cur, v_cur, advance: bool = True, timer=None):
+        """Runs one chunk step (asynchronously, on the current stream).  With
+        advance=False the cache state is not swapped, so the same step can be repeated."""
+        self._enqueue(q, k_cur, v_cur, self.cur, timer)
+        if advance:
+            self.cur = 1 - self.cur
+        return self.o_self, self.o_cross
+
+    # ---- CUDA graph of one step ----------------------------------------------------------------
+    def capture(self, q, k_cur, v_cur):
+        """Captures one step (reading the current cache half) into a CUDA graph; the
+        graph reads q/k_cur/v_cur from these exact tensors."""
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self._enqueue(q, k_cur, v_cur, self.cur)     # warm-up outside capture
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.graph(g, stream=s):
+            self._enqueue(q, k_cur, v_cur, self.cur)
+        torch.cuda.synchronize(self.dev)
+        self._graph, self._graph_dir = g, self.cur
+        return g
+
+    def replay(self):
+        self._graph.replay()
+
+    def status(self) -> int:
+        return int(self.dev_status.item())
+
+
+class DenseLayer:
+    """The dense baseline: an append-only cache and full attention over it, plus
+    cross-attention over the whole prompt."""
+
+    def __init__(self, H, d, Nq, cap, P, dtype=torch.bfloat16, device="cuda", scale=None):
+        L.load()
+        dev = torch.device(device)
+        self.H, self.d, self.Nq, self.cap, self.P = H, d, Nq, cap, P
+        self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+        self.k = torch.zeros((H, cap, d), dtype=dtype, device=dev)
+        self.v = torch.zeros((H, cap, d), dtype=dtype, device=dev)
+        self.kp = torch.zeros((H, P, d), dtype=dtype, device=dev)
+        self.vp = torch.zeros((H, P, d), dtype=dtype, device=dev)
+        self.n = 0
+        self.o_self = torch.zeros((H, Nq, d), dtype=dtype, device=dev)
+        self.o_cross = torch.zeros((H, Nq, d), dtype=dtype, device=dev)
+        self.lse_self = _f32(H, Nq, dev=dev)
+        self.lse_cross = _f32(H, Nq, dev=dev)
+
+    def load_history(self, k, v):
+        n = k.shape[1]
+        self.k[:, :n].copy_(k)
+        self.v[:, :n].copy_(v)
+        self.n = n
+
+    def set_prompt(self, kp, vp):
+        self.kp.copy_(kp)
+        self.vp.copy_(vp)
+
+    def step(self, q, k_cur, v_cur, advance: bool = True, timer=None):
+        nq = q.shape[1]
+        main = torch.cuda.current_stream()
+        t = timer or (lambda *a: None)
+        L.fastar_dense_append(k_cur, v_cur, self.k, self.v, self.n)
+        nk = self.n + nq
+        t("dense_attn", main, "begin")
+        L.fastar_dense_attn(q, self.k, self.v, nk, self.scale, self.o_self, self.lse_self)
+        t("dense_attn", main, "end")
+        L.fastar_dense_attn(q, self.kp, self.vp, self.P, self.scale, self.o_cross, self.lse_cross)
+        if advance:
+            self.n = nk
+        return self.o_self, self.o_cross

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+symbol the header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_tempcache_gb300 import build_lib, _lib
+    build_lib.build()
+    return _lib.load()
+
+
+def header_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fastar_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from kv_cache_tempcache_gb300 import _lib
+    names = header_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.symbols(), f"{n} has no Python binding"
+
+
+def test_status_strings_and_version(lib):
+    from kv_cache_tempcache_gb300 import _lib
+    assert _lib.version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert _lib.status_string(code) != "unknown status"
+    assert _lib.status_string(-99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    from kv_cache_tempcache_gb300 import _lib
+    assert _lib.workspace_bytes(_lib.OP_MATCH, 12, 4680, 9360) >= 12 * 4680 * 16
+    assert _lib.workspace_bytes(_lib.OP_SPARSE_ATTN, 12, 4680, 9360, 128, 64, 2) >= 12 * 4680 * 2 * 129 * 4
+    assert _lib.workspace_bytes(_lib.OP_ANNCA, 12, 0, 0, 128, 64, 2, 512, 3) >= 12 * 3 * 512 * 4
+    assert _lib.workspace_bytes(99, 12, 10) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def test_argument_validation_rejects_before_launch(lib):
+    from kv_cache_tempcache_gb300 import _lib as L
+    s = None
+    # unsupported dtype / head dim
+    assert lib.fastar_bucket_assign(FAKE, 7, 1, 8, 128, 1024, 128, FAKE, 4, 1, FAKE, None, None, s) == L.EUNSUPPORTED
+    assert lib.fastar_bucket_assign(FAKE, L.BF16, 1, 8, 96, 1024, 96, FAKE, 4, 1, FAKE, None, None, s) == L.EUNSUPPORTED
+    # r > B, B too large
+    assert lib.fastar_bucket_assign(FAKE, L.BF16, 1, 8, 128, 1024, 128, FAKE, 4, 5, FAKE, None, None, s) == L.ECAPACITY
+    assert lib.fastar_bucket_assign(FAKE, L.BF16, 1, 8, 128, 1024, 128, FAKE, 300, 1, FAKE, None, None, s) == L.ECAPACITY
+    # misaligned base / stride
+    assert lib.fastar_bucket_assign(FAKE + 2, L.BF16, 1, 8, 128, 1024, 128, FAKE, 4, 1, FAKE, None, None, s) == L.EINVAL
+    assert lib.fastar_bucket_assign(FAKE, L.BF16, 1, 8, 128, 1024, 129, FAKE, 4, 1, FAKE, None, None, s) == L.EINVAL
+    # null output
+    assert lib.fastar_bucket_assign(FAKE, L.BF16, 1, 8, 128, 1024, 128, FAKE, 4, 1, None, None, None, s) == L.EINVAL
+    # M < Nq
+    assert lib.fastar_cache_compact(L.BF16, 1, 100, 128, 50, FAKE, FAKE, 12800, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, FAKE, FAKE + 16, FAKE + 16, FAKE + 16, FAKE + 16, FAKE, FAKE, None,
+                                    s) == L.ECAPACITY
+    # in-place compaction is refused
+    assert lib.fastar_cache_compact(L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, s) == L.EINVAL
+    # workspace too small
+    assert lib.fastar_tempcache_match(FAKE, FAKE, L.BF16, 1, 64, 128, 8192, 128, FAKE, FAKE, FAKE, 128, 0.9, FAKE,
+                                      None, None, FAKE, None, FAKE, 16, s) == L.EWORKSPACE
+    assert lib.fastar_sparse_attn(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE, 128, FAKE, FAKE,
+                                  0.1, FAKE, 8192, 128, None, None, FAKE, 16, s) == L.EWORKSPACE
+    # prompt beyond the limit
+    assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 2000, 0.2, 16, 1,
+                                   FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.ECAPACITY
+    # dense append past capacity
+    assert lib.fastar_dense_append(L.BF16, 1, 64, 128, FAKE, FAKE, 8192, 128, FAKE, FAKE, 100, 50, s) == L.ECAPACITY
+    # empty work is a successful no-op that touches nothing
+    assert lib.fastar_bucket_assign(None, L.BF16, 4, 0, 128, 0, 128, None, 4, 1, None, None, None, s) == L.OK
+    assert lib.fastar_dense_attn(None, L.BF16, 2, 0, 128, 0, 128, None, None, 0, 0, 128, 0.1, None, 0, 128, None,
+                                 s) == L.OK
+
+
+def test_binding_raises_on_error_code(lib):
+    from kv_cache_tempcache_gb300 import _lib as L
+    with pytest.raises(L.FastarError) as ei:
+        L._call("fastar_dense_append", L.BF16, 1, 64, 128, FAKE, FAKE, 8192, 128, FAKE, FAKE, 100, 50, None)
+    assert ei.value.code == L.ECAPACITY
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle, and fails loudly without its library."""
+    pkg = os.path.join(ROOT, "kv_cache_tempcache_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "from oracle" not in src and "import oracle" not in src, f
+    from kv_cache_tempcache_gb300 import _lib
+    with pytest.raises(FileNotFoundError):
+        _lib.open_library("/nonexistent/libfastar.so")

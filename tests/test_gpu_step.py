@@ -1,0 +1,172 @@
+"""GPU parity of the whole FAST-AR layer step against the CPU oracle, stage by stage,
+through the C ABI.  Sizes span several tiles with ragged tails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_tempcache_gb300 import synth
+from oracle import fastar_oracle as O
+import gpu_harness as GH
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg, seed=0, gate=True, q_layout="HND", cache=None):
+    inputs = synth.layer_step_inputs(cfg, seed=seed)
+    ck, cv = GH.raw_window(inputs, cfg) if cache is None else cache(inputs)
+    g, _ = GH.gpu_step(cfg, inputs, ck, cv, gate=gate, q_layout=q_layout)
+    counts = GH.check_step(cfg, inputs, ck, cv, g, gate=gate)
+    return inputs, g, counts
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_fp32_step(seed):
+    _, g, counts = _run(synth.TINY_FP32, seed)
+    assert g["evict"].sum() > 0, "the tiny workload should evict"
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_small_bf16_step(seed):
+    cfg = GH.small_bf16()
+    _, g, counts = _run(cfg, seed)
+    assert g["evict"].sum() > 0
+    assert (g["len_out"] == cfg.M).all()
+
+
+def test_bf16_d64_and_f32_d128():
+    _run(GH.small_bf16().replace(d=64, name="bf16_d64"))
+    _run(GH.small_bf16().replace(dtype="f32", name="f32_d128", H=1, Tf=130, prior_frames=4, M=600))
+
+
+def test_token_major_layout():
+    cfg = GH.small_bf16().replace(H=3)
+    _run(cfg, q_layout="NHD")
+
+
+def test_empty_cache_first_chunk():
+    cfg = GH.small_bf16()
+    inputs = synth.layer_step_inputs(cfg, seed=3)
+    H, d = cfg.H, cfg.d
+    empty = np.zeros((H, 0, d), np.float32)
+    g, _ = GH.gpu_step(cfg, inputs, empty, empty)
+    GH.check_step(cfg, inputs, empty, empty, g)
+    assert (g["top1"] == -1).all() and (g["len_out"] == cfg.Nq).all()
+
+
+def test_partial_cache_no_fifo_drop():
+    cfg = GH.small_bf16().replace(M=2400)
+    _, g, _ = _run(cfg, cache=lambda inp: (inp["history_k"][:, :500], inp["history_v"][:, :500]))
+    assert (g["len_out"] < cfg.M).all()
+
+
+def test_prompt_smaller_than_topk_and_ungated():
+    cfg = GH.small_bf16().replace(P=8, topk=16)
+    _, g, _ = _run(cfg)
+    assert (g["kcnt"] == 8).all()
+    _run(GH.small_bf16(), gate=False)
+
+
+def test_textbook_reduction_on_gpu():
+    # B=1, r=1, tau>1, tau_ca=-1, M >= n+Nq: sparse == dense, nothing evicted, all prompt kept
+    cfg = GH.small_bf16().replace(B=1, r=1, tau=2.0, tau_ca=-1.0, M=2000, prior_frames=4)
+    inputs, g, _ = _run(cfg, cache=lambda inp: (inp["history_k"], inp["history_v"]))
+    assert g["evict"].sum() == 0 and (g["len_out"] == 800 + cfg.Nq).all()
+    assert g["keep"].all()
+    tol = parity.TOL[cfg.dtype]
+    for h in range(cfg.H):
+        K = np.concatenate([inputs["history_k"][h], inputs["k_cur"][h]])
+        V = np.concatenate([inputs["history_v"][h], inputs["v_cur"][h]])
+        o, _ = O.dense_attention(inputs["q"][h], K, V, cfg.scale)
+        parity.close(g["o_self"][h], o, *tol, "reduced AnnSA vs dense")
+
+
+def test_exact_ties_lowest_index():
+    # integer-valued, bf16-exact duplicated keys: every dot product is exact in fp32
+    cfg = synth.LayerConfig(name="ties", H=1, d=64, Tf=64, F=1, prior_frames=0, P=16, C=1, sigma_mix=0, rho=0,
+                            drift=0, qnoise=0, tau=0.999, M=256, B=4, r=2, tau_ca=0.5, topk=4, dtype="bf16")
+    rng = np.random.default_rng(0)
+    base = rng.integers(-3, 4, size=(8, 64)).astype(np.float32)
+    ck = np.concatenate([base, base, 2 * base, base])[None]           # 32 entries, 4 copies of each direction
+    cv = rng.standard_normal((1, 32, 64)).astype(np.float32)
+    q = base[rng.integers(0, 8, size=64)][None]
+    cent = np.zeros((1, 4, 64), np.float32)
+    cent[0, 0, 0] = cent[0, 2, 0] = 1.0                               # duplicated centroids
+    cent[0, 1, 1] = cent[0, 3, 1] = 1.0
+    inputs = dict(q=q, k_cur=q.copy(), v_cur=rng.standard_normal((1, 64, 64)).astype(np.float32),
+                  centroids=cent, kp=base[rng.integers(0, 8, size=16)][None],
+                  vp=rng.standard_normal((1, 16, 64)).astype(np.float32))
+    inputs = {k: synth.bf16_round(v) for k, v in inputs.items()}
+    ck, cv = synth.bf16_round(ck), synth.bf16_round(cv)
+    g, _ = GH.gpu_step(cfg, inputs, ck, cv)
+    # exact: the oldest copy wins every tie, duplicated centroids resolve to the lower index
+    o_top1, _, _ = O.tempcache_match(inputs["q"][0], ck[0])
+    assert np.array_equal(g["top1"][0], o_top1)
+    assert np.array_equal(g["qb"][0], O.query_buckets(inputs["q"][0], cent[0], 2))
+    assert np.array_equal(g["kb_in"][0][:32], O.key_buckets(ck[0], cent[0]))
+    assert set(np.unique(g["kb_in"][0][:32]).tolist()) <= {0, 1}
+    GH.check_step(cfg, inputs, ck, cv, g)
+
+
+def test_dense_baseline_matches_oracle():
+    cfg = GH.small_bf16()
+    inputs = synth.layer_step_inputs(cfg, seed=4)
+    H, d, Nq = cfg.H, cfg.d, cfg.Nq
+    hist = inputs["history_k"].shape[1]
+    dense = GH.DenseLayer(H, d, Nq, hist + Nq, cfg.P, dtype=torch.bfloat16)
+    dense.load_history(GH.to_dev(inputs["history_k"], cfg), GH.to_dev(inputs["history_v"], cfg))
+    dense.set_prompt(GH.to_dev(inputs["kp"], cfg), GH.to_dev(inputs["vp"], cfg))
+    o_s, o_c = dense.step(*(GH.to_dev(inputs[x], cfg) for x in ("q", "k_cur", "v_cur")))
+    torch.cuda.synchronize()
+    tol = parity.TOL["bf16"]
+    for h in range(H):
+        want = O.head_dense_step(inputs["q"][h], inputs["history_k"][h], inputs["history_v"][h], inputs["k_cur"][h],
+                                 inputs["v_cur"][h], inputs["kp"][h], inputs["vp"][h], cfg.scale)
+        parity.close(GH.np_(o_s[h]), want["o_self"], *tol, "dense self")
+        parity.close(GH.np_(o_c[h]), want["o_cross"], *tol, "dense cross")
+
+
+def test_graph_replay_equals_eager():
+    cfg = GH.small_bf16()
+    inputs = synth.layer_step_inputs(cfg, seed=5)
+    ck, cv = GH.raw_window(inputs, cfg)
+    g, layer = GH.gpu_step(cfg, inputs, ck, cv)
+    q, k, v = (GH.to_dev(inputs[x], cfg) for x in ("q", "k_cur", "v_cur"))
+    layer.capture(q, k, v)
+    layer.o_self.zero_()
+    layer.o_cross.zero_()
+    layer.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(GH.np_(layer.o_self), g["o_self"])
+    assert np.array_equal(GH.np_(layer.o_cross), g["o_cross"])
+    assert np.array_equal(GH.np_(layer.index_map), g["index_map"])
+
+
+def test_rollout_matches_oracle_chunk_by_chunk():
+    """From an empty cache, chunk after chunk: GPU and oracle evolve independently and
+    must agree on every cache decision until a validated near-tie (if any)."""
+    cfg = GH.small_bf16().replace(M=900)
+    gen = synth.DriftingMixture(cfg, seed=7)
+    layer = GH.make_layer(cfg)
+    layer.set_centroids(GH.to_dev(gen.centroids, cfg))
+    kp, vp = gen.prompt
+    layer.set_prompt(GH.to_dev(kp, cfg), GH.to_dev(vp, cfg))
+    ck = [np.zeros((0, cfg.d), np.float32) for _ in range(cfg.H)]
+    cv = [np.zeros((0, cfg.d), np.float32) for _ in range(cfg.H)]
+    bytes0 = torch.cuda.memory_allocated()
+    for t in range(8):
+        k, v, q = gen.next_chunk()
+        layer.step(*(GH.to_dev(x, cfg) for x in (q, k, v)))
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        c = layer.cache
+        for h in range(cfg.H):
+            nk, nv, info = O.tempcache_only_advance(q[h], k[h], v[h], ck[h], cv[h], tau=cfg.tau, M=cfg.M)
+            L = int(c.len[h].item())
+            assert L == info["length"] <= cfg.M
+            np.testing.assert_array_equal(GH.np_(c.k[h, :L]), nk)
+            np.testing.assert_array_equal(GH.np_(c.v[h, :L]), nv)
+            ck[h], cv[h] = nk, nv
+        assert torch.cuda.memory_allocated() == bytes0, "the step must not allocate"
