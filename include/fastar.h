@@ -65,6 +65,7 @@ extern "C" {
 #define FASTAR_DEV_BAD_LEN 1      /* a cache length was outside [0, M]            */
 #define FASTAR_DEV_BAD_BUCKET 2   /* a bucket id was outside [0, B)               */
 #define FASTAR_DEV_BAD_INDEX 4    /* an index list pointed outside its range      */
+#define FASTAR_DEV_TIMEOUT 8      /* a bounded on-chip wait gave up; outputs invalid */
 
 /* ---- limits ------------------------------------------------------------------------ */
 #define FASTAR_MAX_B 256          /* buckets per head                              */
