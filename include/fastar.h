@@ -212,6 +212,26 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
                         uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---- 6b. AnnCA prompt selection without any caller allocation ------------------------
+ * The paper has no counterpart: this is a convenience for callers that cannot
+ * allocate device memory when they run the step (a server that reserves all
+ * device memory at start-up, a process under a fixed shared memory budget, a
+ * latency-critical host thread where cudaMalloc may block or synchronise).
+ * Same arguments and results as fastar_annca_select without the score output and
+ * the workspace: the per-token scores go to a fixed scratch array inside the
+ * library's device image (FASTAR_NOALLOC_MAX_SCORES floats, 1 MiB, held on every
+ * GPU that loads the library until the process exits).  H * F * P above that
+ * limit returns FASTAR_ECAPACITY.  The first call on a device (with that device
+ * current) looks up the array's address; make it before any stream capture.
+ * All calls share the array: calls that may overlap on the GPU race and must be
+ * ordered by the caller.  Calls no allocation routine of any kind. */
+#define FASTAR_NOALLOC_MAX_SCORES 262144
+int fastar_annca_select_noalloc(const void* q, int dtype, int H, int F, int64_t tpf, int d,
+                                int64_t q_head_stride, int64_t q_token_stride,
+                                const int32_t* qb, int r, const void* kp, const int32_t* pb, int64_t P,
+                                float tau_ca, int topk, int gate,
+                                uint8_t* keep, int32_t* kidx, int32_t* kcnt, cudaStream_t stream);
+
 /* ---- 7. cross-attention over the kept prompt subset --------------------------------
  * FAST-AR technical summary §2.B ("cross-attention computed over ... the
  * frame-relevant prompt subset").  For query i of frame f:

@@ -43,6 +43,7 @@ _SIGS = {
                            _P, _S, _P],
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P, _P, _S,
                             _P],
+    "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
     "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
@@ -196,6 +197,17 @@ def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, 
     _call("fastar_annca_select", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2], ptr(kp),
           ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), ptr(keep), ptr(kidx), ptr(kcnt), ptr(score),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+          stream_handle(stream))
+
+
+def fastar_annca_select_noalloc(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, stream=None):
+    """fastar_annca_select for callers that cannot allocate: the scores go to the
+    library's fixed scratch array (no workspace, no score output)."""
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    tpf = nq // F
+    _call("fastar_annca_select_noalloc", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2],
+          ptr(kp), ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), ptr(keep), ptr(kidx), ptr(kcnt),
           stream_handle(stream))
 
 
