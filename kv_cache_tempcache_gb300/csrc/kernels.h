@@ -28,6 +28,13 @@ cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int 
 // ---- TempCache ----------------------------------------------------------------------
 int match_splits(int H, int64_t nq, int64_t M);
 size_t match_workspace(int H, int64_t nq, int64_t M);
+int match_tc_splits(int H, int64_t nq, int64_t M);
+size_t match_tc_workspace(int H, int64_t nq, int64_t M);
+// Tensor-core match (bf16): writes [S, H, nq] partial top-2s and clears evict;
+// returns S, or -1 if the launch could not be set up (the caller falls back).
+int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm,
+                    const int32_t* clen, int64_t M, bool top2, float4* part, uint8_t* evict,
+                    int32_t* status, cudaStream_t s);
 cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kcur, int H, int64_t nq,
                                    const void* cache_k, const float* cache_knorm,
                                    const int32_t* cache_len, int64_t M, float tau, int32_t* top1,

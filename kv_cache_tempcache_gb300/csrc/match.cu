@@ -62,7 +62,9 @@ int match_splits(int H, int64_t nq, int64_t M) {
 }
 
 size_t match_workspace(int H, int64_t nq, int64_t M) {
-  return sizeof(float4) * (size_t)match_splits(H, nq, M) * H * (size_t)nq;
+  const size_t simt = sizeof(float4) * (size_t)match_splits(H, nq, M) * H * (size_t)nq;
+  const size_t tcw = match_tc_workspace(H, nq, M);
+  return simt > tcw ? simt : tcw;
 }
 
 // grid (ceil(nq/64), H, splits); 256 threads; thread (ty, tx) owns rows ty*4..+3 and
@@ -233,10 +235,24 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
                               const float* cknorm, const int32_t* clen, int64_t M, float tau,
                               int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* status,
                               void* ws, cudaStream_t s) {
+  float4* part = static_cast<float4*>(ws);
+  if (sizeof(T) == 2 && nq > 0) {
+    // bf16: the tensor-core kernel (the SIMT kernel below only if its set-up is refused)
+    const int tsplits = launch_match_tc(D, q, H, nq, ck, cknorm, clen, M, s2 != nullptr, part, evict, status, s);
+    if (tsplits > 0) {
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      const int64_t warps = (int64_t)H * nq;
+      match_finalize_kernel<T, D><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+          static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
+          static_cast<const T*>(ck), cknorm, clen, M, tau, tsplits, part, top1, s1, s2, evict);
+      count_launches(1);
+      return cudaGetLastError();
+    }
+  }
   const int splits = match_splits(H, nq, M);
   int64_t chunk = (M + splits - 1) / splits;
   chunk = (chunk + kNT - 1) / kNT * kNT;
-  float4* part = static_cast<float4*>(ws);
   const size_t smem = sizeof(float) * ((size_t)D * kMT + (size_t)D * kNT + kNT);
   auto k1 = match_simt_kernel<T, D>;
   static const cudaError_t attr = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

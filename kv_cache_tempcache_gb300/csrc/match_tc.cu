@@ -49,6 +49,7 @@ struct alignas(1024) MatchSmem {
 
 struct MatchGeom {
   int H, QB, S;
+  int q_token_major;   // Q's tensor map is (d, H, nq) instead of (d, nq, H)
   int64_t nq, M;
 };
 
@@ -173,7 +174,10 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc::mbar_arrive_tx(&sm.a_full, (uint32_t)(w.nm * KH * kTile));
         for (int m = 0; m < w.nm; ++m)
           for (int kh = 0; kh < KH; ++kh)
-            tc::tma_load_3d(sm.a[m][kh], &tm_q, kh * 64, w.qb * kQ + m * 128, w.h, &sm.a_full);
+            if (g.q_token_major)
+              tc::tma_load_3d(sm.a[m][kh], &tm_q, kh * 64, w.h, w.qb * kQ + m * 128, &sm.a_full);
+            else
+              tc::tma_load_3d(sm.a[m][kh], &tm_q, kh * 64, w.qb * kQ + m * 128, w.h, &sm.a_full);
         for (int t = w.t_beg; t < w.t_end; ++t) {
           if (!tc::mbar_wait(&sm.b_empty[stage], ph ^ 1, abort)) break;
           tc::mbar_arrive_tx(&sm.b_full[stage], (uint32_t)(KH * kTile));
@@ -335,8 +339,15 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
                                 const int32_t* clen, int64_t M, bool top2, float4* part, uint8_t* evict,
                                 int32_t* status, cudaStream_t s) {
   CUtensorMap tq, tk;
-  if (!make_tmap_bf16_3d(&tq, q.p, D, (uint64_t)nq, (uint64_t)H, (uint64_t)q.ts * 2, (uint64_t)q.hs * 2, 64, 128))
+  const bool token_major = H > 1 && q.hs < q.ts;   // e.g. [N, H, d] storage
+  if (token_major) {
+    if (!make_tmap_bf16_3d(&tq, q.p, D, (uint64_t)H, (uint64_t)nq, (uint64_t)q.hs * 2, (uint64_t)q.ts * 2, 64, 1,
+                           128))
+      return -1;
+  } else if (!make_tmap_bf16_3d(&tq, q.p, D, (uint64_t)nq, (uint64_t)H, (uint64_t)q.ts * 2, (uint64_t)q.hs * 2, 64,
+                                128)) {
     return -1;
+  }
   if (!make_tmap_bf16_3d(&tk, ck, D, (uint64_t)M, (uint64_t)H, (uint64_t)D * 2, (uint64_t)M * D * 2, 64, 128))
     return -1;
   MatchGeom g;
@@ -344,6 +355,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
   g.nq = nq;
   g.M = M;
   g.QB = (int)((nq + kQ - 1) / kQ);
+  g.q_token_major = token_major ? 1 : 0;
   g.S = match_tc_splits(H, nq, M);
   const int units = g.H * g.QB * g.S;
   const int grid = units < sm_count() ? units : sm_count();

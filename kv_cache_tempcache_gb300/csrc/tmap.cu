@@ -25,12 +25,13 @@ EncodeFn encode_fn() {
 }  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                       uint32_t box2) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {d0, d1, d2 > 0 ? d2 : 1};
   cuuint64_t strides[2] = {stride1_bytes, stride2_bytes > 0 ? stride2_bytes : stride1_bytes * d1};
-  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t box[3] = {box0, box1, box2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

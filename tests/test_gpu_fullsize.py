@@ -1,0 +1,63 @@
+"""Parity at the benchmark's full sizes, in the launch configuration the benchmark uses
+(the layer step as one replayed CUDA graph).  The Wan-1.3B-shaped layer is checked on
+every head; the HunyuanVideo-shaped 720p layer (24 heads, 28 800-entry cache) on a
+sampled head, every output of that head, plus size-independent properties on all."""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_tempcache_gb300 import synth
+import gpu_harness as GH
+
+pytestmark = pytest.mark.gpu
+
+
+def _graph_step(cfg, inputs, ck, cv):
+    """Like gpu_harness.gpu_step, but the measured step runs as a replayed CUDA graph."""
+    layer = GH.make_layer(cfg)
+    layer.set_centroids(GH.to_dev(inputs["centroids"], cfg))
+    layer.set_prompt(GH.to_dev(inputs["kp"], cfg), GH.to_dev(inputs["vp"], cfg))
+    layer.load_cache(GH.to_dev(ck, cfg), GH.to_dev(cv, cfg))
+    q, k, v = (GH.to_dev(inputs[x], cfg) for x in ("q", "k_cur", "v_cur"))
+    cin = layer.caches[layer.cur]
+    kb_in = GH.np_(cin.kb)[..., 0].copy()
+    knorm_in = GH.np_(cin.knorm).copy()
+    layer.capture(q, k, v)
+    layer.o_self.zero_()
+    layer.o_cross.zero_()
+    layer.replay()
+    torch.cuda.synchronize()
+    cout = layer.caches[1 - layer.cur]
+    n = GH.np_
+    return dict(qb=n(layer.qb), kb_cur=n(layer.kb_cur)[..., 0], kcur_norm=n(layer.kcur_norm), kb_in=kb_in,
+                knorm_in=knorm_in, pb=n(layer.pb)[..., 0], top1=n(layer.top1), s1=n(layer.s1), s2=n(layer.s2),
+                evict=n(layer.evict), index_map=n(layer.index_map), len_out=n(cout.len), k_out=n(cout.k),
+                v_out=n(cout.v), kb_out=n(cout.kb)[..., 0], knorm_out=n(cout.knorm), kperm=n(layer.kperm),
+                koff=n(layer.koff), qperm=n(layer.qperm), qoff=n(layer.qoff), o_self=n(layer.o_self),
+                lse_self=n(layer.lse_self), keep=n(layer.keep), kidx=n(layer.kidx), kcnt=n(layer.kcnt),
+                score=n(layer.score), o_cross=n(layer.o_cross), status=layer.status())
+
+
+def test_wan13b_layer_full_size_all_heads():
+    cfg = synth.WAN13B_LAYER
+    inputs = synth.layer_step_inputs(cfg, seed=0)
+    ck, cv = GH.raw_window(inputs, cfg)
+    g = _graph_step(cfg, inputs, ck, cv)
+    counts = GH.check_step(cfg, inputs, ck, cv, g)
+    assert g["evict"].sum() > 0 and (g["len_out"] == cfg.M).all()
+    print("near-ties / ambiguous:", counts)
+
+
+def test_hunyuan720p_layer_full_size_sampled_head():
+    cfg = synth.HUNYUAN720P_LAYER
+    inputs = synth.layer_step_inputs(cfg, seed=0)
+    ck, cv = GH.raw_window(inputs, cfg)
+    g = _graph_step(cfg, inputs, ck, cv)
+    assert g["status"] == 0
+    counts = GH.Counts()
+    GH.check_head(cfg, inputs, ck, cv, g, 13, counts=counts)
+    # properties that hold on every head at any size
+    assert (g["len_out"] <= cfg.M).all()
+    assert np.isfinite(g["o_self"]).all() and np.isfinite(g["o_cross"]).all()
+    assert (g["kcnt"] >= cfg.topk).all()
+    print("near-ties / ambiguous:", counts)
