@@ -190,10 +190,162 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
 
 size_t annca_workspace(int H, int F, int64_t P) { return sizeof(float) * (size_t)H * F * P + 256; }
 
+// ---------------------------------------------------------------------------------------
+// Bucket-gated scoring by bucket.  With the gate, prompt token p can only be scored by
+// queries whose bucket set holds pb[p], so one CTA per (head, bucket b) visits exactly
+// the pairs (query with b in R(i), prompt token with pb = b): the ANN buckets turn the
+// frame x prompt score matrix into a union of small dense blocks.  The CTA collects its
+// query list (any order: only maxima are taken), then for chunks of 32 of its prompt
+// tokens and 64 of its queries forms the dot products in fp32 and keeps, per prompt
+// token and latent frame, the largest q.kp/|q|; the score is that times 1/|kp|.
+// ---------------------------------------------------------------------------------------
+constexpr int kBP = 32;          // prompt tokens per chunk
+constexpr int kBQ = 64;          // queries per chunk
+constexpr int kBMaxF = 16;       // frames per chunk supported by this path
+constexpr int kBMaxQ = 16384;    // queries per head supported by this path
+
+// Shared memory of the bucket kernel for a query list of up to `maxq` entries.
+template <int D>
+constexpr size_t annca_bucket_smem(int64_t maxq) {
+  return sizeof(float) * ((size_t)kBP * (D + 4) + (size_t)kBQ * (D + 4) + kBQ + kBP) +
+         sizeof(unsigned) * (size_t)kBP * kBMaxF + sizeof(int) * ((size_t)maxq + FASTAR_MAX_P + kBQ + 4);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+annca_bucket_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int64_t tpf,
+                    const int32_t* __restrict__ qb, int r, const T* __restrict__ kp,
+                    const int32_t* __restrict__ pb, int64_t P, float* __restrict__ score) {
+  extern __shared__ __align__(16) float sm_b[];
+  constexpr int LD = D + 4;                       // padded row stride (floats)
+  float* Ks = sm_b;                               // [kBP][LD]
+  float* Qs = Ks + kBP * LD;                      // [kBQ][LD]
+  float* qinv = Qs + kBQ * LD;                    // [kBQ]
+  float* pinv = qinv + kBQ;                       // [kBP]
+  unsigned* best = reinterpret_cast<unsigned*>(pinv + kBP);   // [kBP][kBMaxF] ordered floats
+  int* plist = reinterpret_cast<int*>(best + kBP * kBMaxF);   // [FASTAR_MAX_P]
+  int* qlist = plist + FASTAR_MAX_P;                           // [F * tpf], placed last
+  int* qfr = qlist + F * tpf;                                  // [kBQ] frame of each chunk query
+  int* cnt = qfr + kBQ;                                        // [0]: queries, [1]: prompt tokens
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int64_t nq = (int64_t)F * tpf;
+  if (tid < 2) cnt[tid] = 0;
+  __syncthreads();
+  for (int64_t p = tid; p < P; p += blockDim.x)
+    if (pb[(int64_t)h * P + p] == b) plist[atomicAdd(&cnt[1], 1)] = (int)p;
+  __syncthreads();
+  const int npb = cnt[1];
+  if (npb == 0) return;   // no prompt token in this bucket (uniform across the CTA)
+  for (int64_t i = tid; i < nq; i += blockDim.x) {
+    bool in = false;
+    for (int s = 0; s < r; ++s) in |= qb[((int64_t)h * nq + i) * r + s] == b;
+    if (in) qlist[atomicAdd(&cnt[0], 1)] = (int)i;
+  }
+  __syncthreads();
+  const int nqb = cnt[0];
+  const unsigned kNegKey = float_to_ordered(neg_inf());
+  for (int pc = 0; pc < npb; pc += kBP) {
+    const int np = npb - pc < kBP ? npb - pc : kBP;
+    __syncthreads();
+    for (int idx = tid; idx < kBP * (D / 8); idx += blockDim.x) {
+      const int row = idx / (D / 8), c8 = idx % (D / 8);
+      float v[8];
+      if (row < np) {
+        load8(kp + ((int64_t)h * P + plist[pc + row]) * D + c8 * 8, v);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = 0.f;
+      }
+      *reinterpret_cast<float4*>(Ks + row * LD + c8 * 8) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(Ks + row * LD + c8 * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    for (int idx = tid; idx < kBP * kBMaxF; idx += blockDim.x) best[idx] = kNegKey;
+    __syncthreads();
+    if (tid < kBP) {
+      float ss = 0.f;
+      for (int k = 0; k < D; ++k) ss = fmaf(Ks[tid * LD + k], Ks[tid * LD + k], ss);
+      const float nrm = sqrtf(ss);
+      pinv[tid] = nrm > 0.f ? 1.0f / nrm : 0.f;
+    }
+    for (int qc = 0; qc < nqb; qc += kBQ) {
+      const int nqc = nqb - qc < kBQ ? nqb - qc : kBQ;
+      __syncthreads();
+      for (int idx = tid; idx < kBQ * (D / 8); idx += blockDim.x) {
+        const int row = idx / (D / 8), c8 = idx % (D / 8);
+        float v[8];
+        if (row < nqc) {
+          load8(q + h * hs + (int64_t)qlist[qc + row] * ts + c8 * 8, v);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = 0.f;
+        }
+        *reinterpret_cast<float4*>(Qs + row * LD + c8 * 8) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(Qs + row * LD + c8 * 8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      }
+      if (tid < kBQ) qfr[tid] = tid < nqc ? (int)(qlist[qc + tid] / tpf) : -1;
+      __syncthreads();
+      if (tid < kBQ) {
+        float ss = 0.f;
+        for (int k = 0; k < D; ++k) ss = fmaf(Qs[tid * LD + k], Qs[tid * LD + k], ss);
+        const float nrm = sqrtf(ss);
+        qinv[tid] = nrm > 0.f ? 1.0f / nrm : 0.f;
+      }
+      __syncthreads();
+      // thread: prompt row pr, queries qg*8 .. qg*8+7
+      const int pr = tid & (kBP - 1), qg = tid >> 5;
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < D; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(Ks + pr * LD + k);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 bq = *reinterpret_cast<const float4*>(Qs + (qg * 8 + u) * LD + k);
+          acc[u] = fmaf(a.x, bq.x, acc[u]);
+          acc[u] = fmaf(a.y, bq.y, acc[u]);
+          acc[u] = fmaf(a.z, bq.z, acc[u]);
+          acc[u] = fmaf(a.w, bq.w, acc[u]);
+        }
+      }
+      if (pr < np) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int qi = qg * 8 + u;
+          const int f = qfr[qi];
+          if (qi < nqc && f >= 0 && f < kBMaxF)
+            atomicMax(&best[pr * kBMaxF + f], float_to_ordered(acc[u] * qinv[qi]));
+        }
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < np * F; idx += blockDim.x) {
+      const int row = idx / F, f = idx % F;
+      const unsigned key = best[row * kBMaxF + f];
+      float sc = neg_inf();
+      if (key != kNegKey) sc = ordered_to_float(key) * pinv[row];
+      score[((int64_t)h * F + f) * P + plist[pc + row]] = sc;
+    }
+  }
+}
+
 template <typename T, int D>
 static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r,
                               const void* kp, const int32_t* pb, int64_t P, int gate, float* score,
                               cudaStream_t s) {
+  if (gate && F <= kBMaxF && (int64_t)F * tpf <= kBMaxQ && P <= FASTAR_MAX_P) {
+    // prompt tokens whose bucket no CTA visits would keep stale scores: the bucket
+    // kernel covers every p (each has exactly one bucket, and every bucket has a CTA)
+    const size_t bsmem = annca_bucket_smem<D>((int64_t)F * tpf);
+    static const cudaError_t battr = cudaFuncSetAttribute(
+        annca_bucket_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)annca_bucket_smem<D>(kBMaxQ));
+    if (battr != cudaSuccess) return battr;
+    annca_bucket_kernel<T, D><<<dim3((unsigned)FASTAR_MAX_B, H), 256, bsmem, s>>>(
+        static_cast<const T*>(q.p), q.hs, q.ts, F, tpf, qb, r, static_cast<const T*>(kp), pb, P, score);
+    count_launches(1);
+    return cudaGetLastError();
+  }
   const size_t smem = sizeof(float) * ((size_t)D * kCQ + (size_t)D * kCP + kCQ + kCP + 16 * kCP) +
                       sizeof(int) * ((size_t)kCQ * FASTAR_MAX_R + kCP);
   auto kern = annca_score_kernel<T, D>;

@@ -319,7 +319,11 @@ static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
     const int64_t tiles = (a.nq * a.r + kAQ - 1) / kAQ + a.B;
     grid = dim3((unsigned)tiles, a.H, 1);
   }
-  kern<<<grid, 256, smem, s>>>(a);
+  if (sizeof(T) == 2 && launch_attn_tc(D, a, s)) {
+    // bf16: tensor-core kernel launched
+  } else {
+    kern<<<grid, 256, smem, s>>>(a);
+  }
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.mode != kSparse) return e;

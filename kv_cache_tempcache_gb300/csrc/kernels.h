@@ -84,6 +84,8 @@ struct AttnArgs {
 };
 
 size_t sparse_attn_workspace(int H, int64_t nq, int d, int r);
+// Tensor-core attention (bf16); false if it could not be set up (caller falls back).
+bool launch_attn_tc(int d, const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s);
 
 // ---- AnnCA --------------------------------------------------------------------------

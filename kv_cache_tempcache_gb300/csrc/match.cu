@@ -177,7 +177,7 @@ match_simt_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int64_t nq,
   }
 }
 
-// One warp per (head, query): merge the split partials, turn the best values into
+// Eight lanes per (head, query): merge the split partials, turn the best values into
 // cosines, and test the matched entry for eviction: cos(kcur_i, k_top1) >= tau.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
@@ -186,38 +186,68 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
                       const int32_t* __restrict__ clen, int64_t M, float tau, int splits,
                       const float4* __restrict__ part, int32_t* __restrict__ top1,
                       float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict) {
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= (int64_t)H * nq) return;
-  const int h = (int)(wid / nq);
-  const int64_t i = wid - (int64_t)h * nq;
+  // eight lanes per query: each lane owns D/8 consecutive elements (vector loads)
+  const int sub = threadIdx.x & 7;
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+  const bool in = wid < (int64_t)H * nq;
+  const int64_t w = in ? wid : 0;
+  const int h = (int)(w / nq);
+  const int64_t i = w - (int64_t)h * nq;
   int64_t n = clen[h];
   n = n < 0 ? 0 : (n > M ? M : n);
   Top2 t{neg_inf(), INT_MAX, neg_inf()};
-  for (int s = 0; s < splits; ++s) {
+  for (int s = sub; s < splits; s += 8) {
     const float4 p = part[((int64_t)s * H + h) * nq + i];
     t = top2_merge(t, Top2{p.x, __float_as_int(p.y), p.z});
   }
-  // |q_i| and |kcur_i|
-  const T* qr = q + h * hs + i * ts;
-  const T* kr = kc + h * hs + i * ts;
-  float qq = 0.f, kk = 0.f;
-  for (int c = lane; c < D; c += 32) {
-    const float a = to_f(qr[c]), b = to_f(kr[c]);
-    qq = fmaf(a, a, qq);
-    kk = fmaf(b, b, kk);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    Top2 u;
+    u.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
+    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    u.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
+    t = top2_merge(t, u);
   }
-  qq = sqrtf(warp_sum(qq));
-  kk = sqrtf(warp_sum(kk));
+  // |q_i| and |kcur_i|
+  constexpr int E = D / 8;
+  const T* qr = q + h * hs + i * ts + sub * E;
+  const T* kr = kc + h * hs + i * ts + sub * E;
+  float kv[E];
+  float qq = 0.f, kk = 0.f;
+#pragma unroll
+  for (int c = 0; c < E; c += 8) {
+    float a[8];
+    load8(qr + c, a);
+    load8(kr + c, kv + c);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      qq = fmaf(a[u], a[u], qq);
+      kk = fmaf(kv[c + u], kv[c + u], kk);
+    }
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+  }
+  qq = sqrtf(qq);
+  kk = sqrtf(kk);
   const bool any = n > 0 && t.i1 != INT_MAX;
   const int j = any ? t.i1 : -1;
   float dot = 0.f;
   if (any) {
-    const T* jr = ck + ((int64_t)h * M + j) * D;
-    for (int c = lane; c < D; c += 32) dot = fmaf(to_f(kr[c]), to_f(jr[c]), dot);
-    dot = warp_sum(dot);
+    const T* jr = ck + ((int64_t)h * M + j) * D + sub * E;
+#pragma unroll
+    for (int c = 0; c < E; c += 8) {
+      float b[8];
+      load8(jr + c, b);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dot = fmaf(kv[c + u], b[u], dot);
+    }
   }
-  if (lane == 0) {
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  if (in && sub == 0) {
     top1[(int64_t)h * nq + i] = j;
     const float inv_q = qq > 0.f ? 1.0f / qq : 0.f;
     if (s1) s1[(int64_t)h * nq + i] = any ? t.m1 * inv_q : neg_inf();
@@ -243,7 +273,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       const int64_t warps = (int64_t)H * nq;
-      match_finalize_kernel<T, D><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+      match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
           static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
           static_cast<const T*>(ck), cknorm, clen, M, tau, tsplits, part, top1, s1, s2, evict);
       count_launches(1);
@@ -272,7 +302,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)H * nq;
-  match_finalize_kernel<T, D><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+  match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
       static_cast<const T*>(ck), cknorm, clen, M, tau, splits, part, top1, s1, s2, evict);
   count_launches(1);

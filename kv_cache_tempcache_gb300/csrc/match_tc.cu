@@ -11,9 +11,10 @@
 //   warp 1      owns TMEM (512 columns = 2 accumulator stages x 2 M-tiles x 128
 //               columns) and issues tcgen05.mma (one thread), committing to the
 //               ring's "empty" barriers and the accumulator's "full" barrier;
-//   warps 2..9  epilogue, two warps per TMEM lane quadrant (one per M-tile): load
-//               128 fp32 scores per row with tcgen05.ld, scale by 1/|k_j|, keep
-//               the running top-1 (and top-2 when asked), release the stage.
+//   warps 2..17 epilogue, four warps per TMEM lane quadrant (M-tile x column half):
+//               load 64 fp32 scores per row with tcgen05.ld, hand the stage back to
+//               the MMA at once, scale by 1/|k_j| (norms prefetched a tile ahead),
+//               keep the running top-1 (and top-2 when asked).
 // The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
 // 256-query block, key segment); segments split the cache so the unit count
 // fills the machine, and a small finaliser merges the segments' partial top-2s.
@@ -32,14 +33,14 @@ namespace {
 constexpr int kQ = 256;         // queries per unit
 constexpr int kN = 128;         // keys per tile
 constexpr int kStages = 4;      // B ring depth
-constexpr int kThreads = 320;   // 10 warps
+constexpr int kThreads = 576;   // 18 warps
 constexpr int kTile = 128 * 128; // bytes of one 128-row x 64-element bf16 swizzled block
 
 template <int D>
 struct alignas(1024) MatchSmem {
   uint8_t a[2][D / 64][kTile];
   uint8_t b[kStages][D / 64][kTile];
-  float invk[8][kN];
+  float invk[16][64];
   uint64_t a_full, a_empty;
   uint64_t b_full[kStages], b_empty[kStages];
   uint64_t t_full[2], t_empty[2];
@@ -141,7 +142,7 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.t_full[s], 1);
-      tc::mbar_init(&sm.t_empty[s], 8);
+      tc::mbar_init(&sm.t_empty[s], 16);
     }
     sm.abort = 0;
     tc::mbar_fence_init();
@@ -231,9 +232,12 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ---------------- epilogue ----------------
-    const int ew = warp - 2;          // 0..7
+    // 16 warps: (lane quadrant, M-tile, column half).  Each thread owns one query row
+    // and 64 of the tile's 128 key columns.
+    const int ew = warp - 2;          // 0..15
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int m = ew >> 2;            // which M-tile (accumulator) this warp reads
+    const int m = (ew >> 2) & 1;      // which M-tile (accumulator) this warp reads
+    const int half = ew >> 3;         // which 64-column half of the tile
     float* inv = sm.invk[ew];
     int acc = 0;
     uint32_t tph = 0;
@@ -243,44 +247,32 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int64_t i = (int64_t)w.qb * kQ + rloc;
       Best b{neg_inf(), INT_MAX, neg_inf()};
       const float* kn = cknorm + (int64_t)w.h * g.M;
-      for (int t = w.t_beg; t < w.t_end; ++t) {
-        const int64_t j0 = (int64_t)t * kN;
-        // 1/|k_j| of the tile's 128 keys into this warp's buffer
-        {
-          const int64_t j = j0 + lane * 4;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float x = (j + c < w.n) ? kn[j + c] : 0.f;
-            inv[lane * 4 + c] = x > 0.f ? __frcp_rn(x) : 0.f;
-          }
+      // |k_j| of this lane's two columns of the first tile (prefetched one tile ahead)
+      float kx0 = 0.f, kx1 = 0.f;
+      {
+        const int64_t j = (int64_t)w.t_beg * kN + half * 64 + lane * 2;
+        if (w.t_beg < w.t_end) {
+          kx0 = j < w.n ? kn[j] : 0.f;
+          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
         }
-        __syncwarp();
+      }
+      for (int t = w.t_beg; t < w.t_end; ++t) {
+        const int64_t j0 = (int64_t)t * kN + half * 64;
         if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
         tc::tc_fence_after();
-        if (m < w.nm) {
-          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128);
-          const bool partial = j0 + kN > w.n;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            tc::tmem_ld32(taddr + c * 32, v);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 s = *reinterpret_cast<const float4*>(inv + c * 32 + q4 * 4);
-              v[q4 * 4 + 0] *= s.x;
-              v[q4 * 4 + 1] *= s.y;
-              v[q4 * 4 + 2] *= s.z;
-              v[q4 * 4 + 3] *= s.w;
-            }
-            if (partial) {
-#pragma unroll
-              for (int x = 0; x < 32; ++x)
-                if (j0 + c * 32 + x >= w.n) v[x] = neg_inf();
-            }
-            fold32<kTop2>(b, v, (int)(j0 + c * 32));
-          }
+        float v[64];
+        const bool active = m < w.nm;
+        if (active) {
+          const uint32_t taddr =
+              tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128 + half * 64);
+          tc::tmem_ld32(taddr, v);
+          tc::tmem_ld32(taddr + 32, v + 32);
         }
+        // 1/|k_j| of this tile into the warp's buffer while the TMEM loads are in flight
+        inv[lane * 2] = kx0 > 0.f ? __frcp_rn(kx0) : 0.f;
+        inv[lane * 2 + 1] = kx1 > 0.f ? __frcp_rn(kx1) : 0.f;
+        if (active) tc::tmem_wait_ld();
+        // the scores are in registers: hand the accumulator stage back to the MMA
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
@@ -288,9 +280,34 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           acc = 0;
           tph ^= 1;
         }
+        // prefetch the next tile's norms
+        if (t + 1 < w.t_end) {
+          const int64_t j = j0 + kN + lane * 2;
+          kx0 = j < w.n ? kn[j] : 0.f;
+          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
+        }
+        if (active) {
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 s = *reinterpret_cast<const float4*>(inv + q4 * 4);
+            v[q4 * 4 + 0] *= s.x;
+            v[q4 * 4 + 1] *= s.y;
+            v[q4 * 4 + 2] *= s.z;
+            v[q4 * 4 + 3] *= s.w;
+          }
+          if (j0 + 64 > w.n) {
+#pragma unroll
+            for (int x = 0; x < 64; ++x)
+              if (j0 + x >= w.n) v[x] = neg_inf();
+          }
+          fold32<kTop2>(b, v, (int)j0);
+          fold32<kTop2>(b, v + 32, (int)(j0 + 32));
+        }
+        __syncwarp();
       }
       if (m * 128 < w.rows && rloc < w.rows && !*abort)
-        part[((int64_t)w.seg * g.H + w.h) * g.nq + i] = make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
+        part[(((int64_t)w.seg * 2 + half) * g.H + w.h) * g.nq + i] =
+            make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
     }
   }
   tc::tc_fence_before();
@@ -328,7 +345,7 @@ int match_tc_splits(int H, int64_t nq, int64_t M) {
 }
 
 size_t match_tc_workspace(int H, int64_t nq, int64_t M) {
-  return sizeof(float4) * (size_t)8 * H * (size_t)nq;
+  return sizeof(float4) * (size_t)16 * H * (size_t)nq;   // up to 8 segments x 2 column halves
 }
 
 // Launches the tensor-core match (writes `part` as [S, H, nq] and clears evict).
@@ -372,7 +389,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
     match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
   }
   count_launches(1);
-  return g.S;
+  return 2 * g.S;   // partial top-2s per (segment, column half)
 }
 
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,
