@@ -107,6 +107,8 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
                                  cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   if (dtype == FASTAR_BF16) {
+    // tensor cores (the SIMT kernel below only if the set-up is refused)
+    if (launch_assign_tc(d, x, H, n, cent, B, r, ids, scores, norms, s)) return cudaGetLastError();
     if (d == 128) return assign_impl<__nv_bfloat16, 128>(x, H, n, cent, B, r, ids, scores, norms, s);
     return assign_impl<__nv_bfloat16, 64>(x, H, n, cent, B, r, ids, scores, norms, s);
   }

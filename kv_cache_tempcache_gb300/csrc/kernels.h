@@ -21,6 +21,9 @@ void count_launches(int n);
 cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, const void* centroids,
                                  int B, int r, int32_t* ids, float* scores, float* norms,
                                  cudaStream_t s);
+// Tensor-core bucket assignment (bf16); false if it could not be set up.
+bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int B, int r, int32_t* ids,
+                      float* scores, float* norms, cudaStream_t s);
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
                                int32_t* status, cudaStream_t s);
