@@ -178,7 +178,8 @@ def stage_units(cfg, layer, n_in):
     u["bucket_assign"] = dict(bytes=2 * H * Nq * row + 2 * H * B * row, flops=2.0 * 2 * H * Nq * B * d)
     u["tempcache_match"] = dict(bytes=H * Nq * row * 2 + n_tot * (row + 4), flops=2.0 * Nq * d * n_tot)
     u["cache_compact"] = dict(bytes=2 * 2 * float(L_out.sum()) * row, flops=0.0)
-    u["bucket_sort"] = dict(bytes=4.0 * (float(L_out.sum()) * 2 + H * Nq * r * 2), flops=0.0)
+    u["bucket_sort"] = dict(bytes=4.0 * float(L_out.sum()) * 2, flops=0.0)
+    u["bucket_sort_q"] = dict(bytes=4.0 * H * Nq * r * 2, flops=0.0)
     u["sparse_attn"] = dict(bytes=H * Nq * row * 2 + 2 * float(L_out.sum()) * row, flops=4.0 * d * pairs)
     u["annca_select"] = dict(bytes=H * Nq * row + H * P * row, flops=2.0 * H * Nq * P * d)
     u["cross_attn_subset"] = dict(bytes=H * Nq * row * 2 + 2 * float(kcnt.sum()) * row,

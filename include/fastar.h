@@ -204,11 +204,16 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d,
  *                 order (score desc, p asc) with -inf after every finite score.
  * Outputs: keep uint8 [H,F,P]; kidx int32 [H,F,P] (kept p ascending, then -1);
  * kcnt int32 [H,F]; score float [H,F,P] (optional).  kp is [H,P,d] contiguous.
+ * B: the bucket count (0 if unknown).  qperm/qoff (optional, need B > 0): the
+ * (query, slot) pairs of qb grouped by bucket, as fastar_bucket_sort writes them;
+ * with them the gated scoring reads each bucket's queries directly instead of
+ * scanning qb (same results either way).
  * Workspace: fastar_workspace_bytes(FASTAR_OP_ANNCA, H, ..., P, F).  P <= FASTAR_MAX_P. */
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                         int64_t q_head_stride, int64_t q_token_stride,
                         const int32_t* qb, int r, const void* kp, const int32_t* pb, int64_t P,
-                        float tau_ca, int topk, int gate,
+                        float tau_ca, int topk, int gate, int B,
+                        const int32_t* qperm, const int32_t* qoff,
                         uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 

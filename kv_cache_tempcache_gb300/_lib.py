@@ -41,8 +41,8 @@ _SIGS = {
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
     "fastar_sparse_attn": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P,
                            _P, _S, _P],
-    "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P, _P, _S,
-                            _P],
+    "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
+                            _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
     "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
@@ -190,12 +190,13 @@ def fastar_sparse_attn(q, r, B, qperm, qoff, k, v, kperm, koff, scale, out, lse,
 
 
 def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, score=None, workspace=None,
-                        stream=None):
+                        stream=None, B=0, qperm=None, qoff=None):
     H, nq, d = q.shape
     qh, qt = tok_strides(q)
     tpf = nq // F
     _call("fastar_annca_select", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2], ptr(kp),
-          ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), ptr(keep), ptr(kidx), ptr(kcnt), ptr(score),
+          ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), int(B), ptr(qperm), ptr(qoff), ptr(keep),
+          ptr(kidx), ptr(kcnt), ptr(score),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))
 

@@ -183,11 +183,13 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
 
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
                         int64_t q_token_stride, const int32_t* qb, int r, const void* kp, const int32_t* pb,
-                        int64_t P, float tau_ca, int topk, int gate, uint8_t* keep, int32_t* kidx,
-                        int32_t* kcnt, float* score, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream) {
+                        int64_t P, float tau_ca, int topk, int gate, int B, const int32_t* qperm,
+                        const int32_t* qoff, uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
+  if (B < 0 || B > FASTAR_MAX_B) return FASTAR_EINVAL;
+  if ((qperm != nullptr) != (qoff != nullptr) || (qperm && B < 1)) return FASTAR_EINVAL;
   if (H < 0 || F < 0 || tpf < 0 || r < 1 || P < 0 || topk < 0) return FASTAR_EINVAL;
   if (P > FASTAR_MAX_P || r > FASTAR_MAX_R) return FASTAR_ECAPACITY;
   if (H == 0 || F == 0) return FASTAR_OK;
@@ -202,8 +204,8 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
     }
   }
   return cuda_rc(fastar::launch_annca_select(dtype, d, TokView{q, q_head_stride, q_token_stride}, H, F, tpf,
-                                             qb, r, kp, pb, P, tau_ca, topk, gate, keep, kidx, kcnt, score,
-                                             workspace, stream));
+                                             qb, r, kp, pb, P, tau_ca, topk, gate, B, qperm, qoff, keep, kidx,
+                                             kcnt, score, workspace, stream));
 }
 
 int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,

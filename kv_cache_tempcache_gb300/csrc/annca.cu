@@ -199,6 +199,14 @@ size_t annca_workspace(int H, int F, int64_t P) { return sizeof(float) * (size_t
 // tokens and 64 of its queries forms the dot products in fp32 and keeps, per prompt
 // token and latent frame, the largest q.kp/|q|; the score is that times 1/|kp|.
 // ---------------------------------------------------------------------------------------
+// Optional bucket order of the (query, slot) pairs (B buckets; qperm/qoff as the
+// counting sort writes them).  qperm == nullptr: scan the query buckets instead.
+struct BucketOrder {
+  int B;
+  const int32_t* qperm;
+  const int32_t* qoff;
+};
+
 constexpr int kBP = 32;          // prompt tokens per chunk
 constexpr int kBQ = 64;          // queries per chunk
 constexpr int kBMaxF = 16;       // frames per chunk supported by this path
@@ -215,7 +223,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 annca_bucket_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int64_t tpf,
                     const int32_t* __restrict__ qb, int r, const T* __restrict__ kp,
-                    const int32_t* __restrict__ pb, int64_t P, float* __restrict__ score) {
+                    const int32_t* __restrict__ pb, int64_t P, const BucketOrder bo, float* __restrict__ score) {
   extern __shared__ __align__(16) float sm_b[];
   constexpr int LD = D + 4;                       // padded row stride (floats)
   float* Ks = sm_b;                               // [kBP][LD]
@@ -237,10 +245,21 @@ annca_bucket_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int6
   __syncthreads();
   const int npb = cnt[1];
   if (npb == 0) return;   // no prompt token in this bucket (uniform across the CTA)
-  for (int64_t i = tid; i < nq; i += blockDim.x) {
-    bool in = false;
-    for (int s = 0; s < r; ++s) in |= qb[((int64_t)h * nq + i) * r + s] == b;
-    if (in) qlist[atomicAdd(&cnt[0], 1)] = (int)i;
+  if (bo.qperm) {
+    // the bucket's (query, slot) pairs are one contiguous range of the sorted order
+    const int32_t* qo = bo.qoff + (int64_t)h * (bo.B + 1);
+    const int64_t beg = qo[b], end = qo[b + 1];
+    const int64_t np = nq * r;
+    for (int64_t pos = beg + tid; pos < end; pos += blockDim.x) {
+      const int e = bo.qperm[(int64_t)h * np + pos];
+      if (e >= 0 && e < np) qlist[atomicAdd(&cnt[0], 1)] = e / r;
+    }
+  } else {
+    for (int64_t i = tid; i < nq; i += blockDim.x) {
+      bool in = false;
+      for (int s = 0; s < r; ++s) in |= qb[((int64_t)h * nq + i) * r + s] == b;
+      if (in) qlist[atomicAdd(&cnt[0], 1)] = (int)i;
+    }
   }
   __syncthreads();
   const int nqb = cnt[0];
@@ -332,8 +351,8 @@ annca_bucket_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int6
 
 template <typename T, int D>
 static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r,
-                              const void* kp, const int32_t* pb, int64_t P, int gate, float* score,
-                              cudaStream_t s) {
+                              const void* kp, const int32_t* pb, int64_t P, int gate, const BucketOrder bo,
+                              float* score, cudaStream_t s) {
   if (gate && F <= kBMaxF && (int64_t)F * tpf <= kBMaxQ && P <= FASTAR_MAX_P) {
     // prompt tokens whose bucket no CTA visits would keep stale scores: the bucket
     // kernel covers every p (each has exactly one bucket, and every bucket has a CTA)
@@ -341,8 +360,9 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
     static const cudaError_t battr = cudaFuncSetAttribute(
         annca_bucket_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)annca_bucket_smem<D>(kBMaxQ));
     if (battr != cudaSuccess) return battr;
-    annca_bucket_kernel<T, D><<<dim3((unsigned)FASTAR_MAX_B, H), 256, bsmem, s>>>(
-        static_cast<const T*>(q.p), q.hs, q.ts, F, tpf, qb, r, static_cast<const T*>(kp), pb, P, score);
+    const unsigned nb = bo.B > 0 ? (unsigned)bo.B : (unsigned)FASTAR_MAX_B;
+    annca_bucket_kernel<T, D><<<dim3(nb, H), 256, bsmem, s>>>(
+        static_cast<const T*>(q.p), q.hs, q.ts, F, tpf, qb, r, static_cast<const T*>(kp), pb, P, bo, score);
     count_launches(1);
     return cudaGetLastError();
   }
@@ -359,18 +379,19 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
 
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb,
                                 int r, const void* kp, const int32_t* pb, int64_t P, float tau_ca, int topk,
-                                int gate, uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
-                                void* ws, cudaStream_t s) {
+                                int gate, int B, const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
+                                int32_t* kidx, int32_t* kcnt, float* score, void* ws, cudaStream_t s) {
   if (H == 0 || F == 0) return cudaSuccess;
   float* sc = score ? score : static_cast<float*>(ws);
   cudaError_t e = cudaSuccess;
+  const BucketOrder bo{B, qperm, qoff};
   if (P > 0) {
     if (dtype == FASTAR_BF16) {
-      e = d == 128 ? annca_impl<__nv_bfloat16, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s)
-                   : annca_impl<__nv_bfloat16, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s);
+      e = d == 128 ? annca_impl<__nv_bfloat16, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s)
+                   : annca_impl<__nv_bfloat16, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s);
     } else {
-      e = d == 128 ? annca_impl<float, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s)
-                   : annca_impl<float, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, sc, s);
+      e = d == 128 ? annca_impl<float, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s)
+                   : annca_impl<float, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s);
     }
     if (e != cudaSuccess) return e;
   }

@@ -32,7 +32,7 @@ struct AssignCtl {
   int abort;
 };
 
-template <int D>
+template <int D, int RT>
 __global__ void __launch_bounds__(128)
 assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c, int H,
                  int64_t n, int token_major, int B, int NP, int r, uint32_t tcols, int32_t* __restrict__ ids,
@@ -88,11 +88,13 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   tc::tc_fence_after();
   const int row = warp * 32 + lane;
   const int64_t t = t0 + row;
-  // sorted top-r (score desc, index asc); ties keep the earlier (lower) index
-  float bv[FASTAR_MAX_R];
-  int bi[FASTAR_MAX_R];
+  // sorted top-r (score desc, index asc); ties keep the earlier (lower) index.  RT > 0
+  // fixes r at compile time so the list lives in registers.
+  constexpr int NR = RT > 0 ? RT : FASTAR_MAX_R;
+  float bv[NR];
+  int bi[NR];
 #pragma unroll
-  for (int s = 0; s < FASTAR_MAX_R; ++s) {
+  for (int s = 0; s < NR; ++s) {
     bv[s] = neg_inf();
     bi[s] = INT_MAX;
   }
@@ -101,11 +103,29 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
       float v[32];
       tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
       tc::tmem_wait_ld();
-#pragma unroll 4
+#pragma unroll
       for (int x = 0; x < 32; ++x) {
         const int j = c + x;
-        const float s = j < B ? v[x] : neg_inf();
-        if (j < B && s > bv[r - 1]) {
+        const float s = v[x];
+        if (j >= B) continue;
+        if (RT == 1) {
+          if (s > bv[0]) {
+            bv[0] = s;
+            bi[0] = j;
+          }
+        } else if (RT == 2) {
+          if (s > bv[NR - 1]) {
+            if (s > bv[0]) {
+              bv[NR - 1] = bv[0];
+              bi[NR - 1] = bi[0];
+              bv[0] = s;
+              bi[0] = j;
+            } else {
+              bv[NR - 1] = s;
+              bi[NR - 1] = j;
+            }
+          }
+        } else if (s > bv[r - 1]) {
           // insert j keeping the order; equal scores stay ahead of it
           int pos = r - 1;
           while (pos > 0 && s > bv[pos - 1]) {
@@ -122,7 +142,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   tc::tc_fence_before();
   if (t < n && ok) {
 #pragma unroll
-    for (int s = 0; s < FASTAR_MAX_R; ++s) {
+    for (int s = 0; s < NR; ++s) {
       if (s < r) {
         ids[((int64_t)h * n + t) * r + s] = bi[s];
         if (scores) scores[((int64_t)h * n + t) * r + s] = bv[s];
@@ -176,11 +196,19 @@ bool assign_tc_impl(TokView x, int H, int64_t n, const void* cent, int B, int r,
   uint32_t tcols = 32;
   while ((int)tcols < NP) tcols <<= 1;
   const size_t smem = assign_tc_smem<D>(NP);
-  static const cudaError_t a = cudaFuncSetAttribute(assign_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    (int)assign_tc_smem<D>(256));
-  if (a != cudaSuccess) return false;
-  assign_tc_kernel<D><<<dim3((unsigned)((n + kRows - 1) / kRows), H), 128, smem, s>>>(
-      tx, tcen, H, n, token_major ? 1 : 0, B, NP, r, tcols, ids, scores, norms, nullptr);
+  const int smax = (int)assign_tc_smem<D>(256);
+  static const cudaError_t a1 = cudaFuncSetAttribute(assign_tc_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+  static const cudaError_t a2 = cudaFuncSetAttribute(assign_tc_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+  static const cudaError_t a0 = cudaFuncSetAttribute(assign_tc_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+  if (a1 != cudaSuccess || a2 != cudaSuccess || a0 != cudaSuccess) return false;
+  const dim3 grid((unsigned)((n + kRows - 1) / kRows), H);
+  const int tm = token_major ? 1 : 0;
+  if (r == 1)
+    assign_tc_kernel<D, 1><<<grid, 128, smem, s>>>(tx, tcen, H, n, tm, B, NP, r, tcols, ids, scores, norms, nullptr);
+  else if (r == 2)
+    assign_tc_kernel<D, 2><<<grid, 128, smem, s>>>(tx, tcen, H, n, tm, B, NP, r, tcols, ids, scores, norms, nullptr);
+  else
+    assign_tc_kernel<D, 0><<<grid, 128, smem, s>>>(tx, tcen, H, n, tm, B, NP, r, tcols, ids, scores, norms, nullptr);
   count_launches(1);
   return true;
 }

@@ -95,7 +95,8 @@ cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s
 size_t annca_workspace(int H, int F, int64_t P);
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf,
                                 const int32_t* qb, int r, const void* kp, const int32_t* pb,
-                                int64_t P, float tau_ca, int topk, int gate, uint8_t* keep,
+                                int64_t P, float tau_ca, int topk, int gate, int B,
+                                const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
                                 int32_t* kidx, int32_t* kcnt, float* score, void* ws,
                                 cudaStream_t s);
 

@@ -88,9 +88,15 @@ struct Best {
 
 template <bool kTop2>
 __device__ __forceinline__ void fold32(Best& b, const float* w, int j0) {
-  float gm = w[0];
+  // balanced max tree (short dependency chains)
+  float t16[16];
 #pragma unroll
-  for (int i = 1; i < 32; ++i) gm = fmaxf(gm, w[i]);
+  for (int i = 0; i < 16; ++i) t16[i] = fmaxf(w[i], w[i + 16]);
+#pragma unroll
+  for (int s = 8; s > 0; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < s; ++i) t16[i] = fmaxf(t16[i], t16[i + s]);
+  const float gm = t16[0];
   if (kTop2) {
     if (gm > b.m2) {
 #pragma unroll
@@ -260,19 +266,44 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int64_t j0 = (int64_t)t * kN + half * 64;
         if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
         tc::tc_fence_after();
-        float v[64];
         const bool active = m < w.nm;
-        if (active) {
-          const uint32_t taddr =
-              tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128 + half * 64);
-          tc::tmem_ld32(taddr, v);
-          tc::tmem_ld32(taddr + 32, v + 32);
-        }
-        // 1/|k_j| of this tile into the warp's buffer while the TMEM loads are in flight
+        const uint32_t taddr =
+            tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128 + half * 64);
+        float v[32];
+        if (active) tc::tmem_ld32(taddr, v);
+        // 1/|k_j| of this tile into the warp's buffer while the TMEM load is in flight
         inv[lane * 2] = kx0 > 0.f ? __frcp_rn(kx0) : 0.f;
         inv[lane * 2 + 1] = kx1 > 0.f ? __frcp_rn(kx1) : 0.f;
-        if (active) tc::tmem_wait_ld();
-        // the scores are in registers: hand the accumulator stage back to the MMA
+        // prefetch the next tile's norms
+        if (t + 1 < w.t_end) {
+          const int64_t j = j0 + kN + lane * 2;
+          kx0 = j < w.n ? kn[j] : 0.f;
+          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
+        }
+        __syncwarp();
+        if (active) {
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            if (c == 1) tc::tmem_ld32(taddr + 32, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 s = *reinterpret_cast<const float4*>(inv + c * 32 + q4 * 4);
+              v[q4 * 4 + 0] *= s.x;
+              v[q4 * 4 + 1] *= s.y;
+              v[q4 * 4 + 2] *= s.z;
+              v[q4 * 4 + 3] *= s.w;
+            }
+            const int64_t jc = j0 + c * 32;
+            if (jc + 32 > w.n) {
+#pragma unroll
+              for (int x = 0; x < 32; ++x)
+                if (jc + x >= w.n) v[x] = neg_inf();
+            }
+            fold32<kTop2>(b, v, (int)jc);
+          }
+        }
+        // hand the accumulator stage back to the MMA
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
@@ -280,30 +311,6 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           acc = 0;
           tph ^= 1;
         }
-        // prefetch the next tile's norms
-        if (t + 1 < w.t_end) {
-          const int64_t j = j0 + kN + lane * 2;
-          kx0 = j < w.n ? kn[j] : 0.f;
-          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
-        }
-        if (active) {
-#pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 s = *reinterpret_cast<const float4*>(inv + q4 * 4);
-            v[q4 * 4 + 0] *= s.x;
-            v[q4 * 4 + 1] *= s.y;
-            v[q4 * 4 + 2] *= s.z;
-            v[q4 * 4 + 3] *= s.w;
-          }
-          if (j0 + 64 > w.n) {
-#pragma unroll
-            for (int x = 0; x < 64; ++x)
-              if (j0 + x >= w.n) v[x] = neg_inf();
-          }
-          fold32<kTop2>(b, v, (int)j0);
-          fold32<kTop2>(b, v + 32, (int)(j0 + 32));
-        }
-        __syncwarp();
       }
       if (m * 128 < w.rows && rloc < w.rows && !*abort)
         part[(((int64_t)w.seg * 2 + half) * g.H + w.h) * g.nq + i] =

@@ -52,13 +52,17 @@ class FastARLayer:
 
     def __init__(self, H: int, d: int, Tf: int, F: int, M: int, B: int, r: int, P: int, tau: float,
                  tau_ca: float, topk: int = 16, dtype: torch.dtype = torch.bfloat16, gate: bool = True,
-                 device: str | torch.device = "cuda", scale: Optional[float] = None):
+                 device: str | torch.device = "cuda", scale: Optional[float] = None,
+                 diagnostics: bool = False):
+        """diagnostics=True also produces the second-best match cosine s2 (a slower
+        match epilogue); the step's results are the same either way."""
         L.load()
         if M < F * Tf:
             raise ValueError(f"cache cap M={M} must hold one chunk of {F * Tf} tokens")
         self.H, self.d, self.Tf, self.F, self.M, self.B, self.r, self.P = H, d, Tf, F, M, B, r, P
         self.Nq = F * Tf
         self.tau, self.tau_ca, self.topk, self.gate = float(tau), float(tau_ca), int(topk), bool(gate)
+        self.diagnostics = bool(diagnostics)
         self.dtype = dtype
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
         dev = torch.device(device)
@@ -163,6 +167,10 @@ class FastARLayer:
         L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
         L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
         t("bucket_assign", main, "end")
+        # the (query, slot) pairs by bucket serve both AnnSA and AnnCA
+        t("bucket_sort_q", main, "begin")
+        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        t("bucket_sort_q", main, "end")
         # AnnCA branch on the side stream
         ev = torch.cuda.Event()
         ev.record(main)
@@ -170,7 +178,8 @@ class FastARLayer:
         with torch.cuda.stream(self.side):
             t("annca_select", self.side, "begin")
             L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate,
-                                  self.keep, self.kidx, self.kcnt, self.score)
+                                  self.keep, self.kidx, self.kcnt, self.score, B=self.B, qperm=self.qperm,
+                                  qoff=self.qoff)
             t("annca_select", self.side, "end")
             t("cross_attn_subset", self.side, "begin")
             L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale,
@@ -178,7 +187,8 @@ class FastARLayer:
             t("cross_attn_subset", self.side, "end")
         # TempCache + AnnSA on the main stream
         t("tempcache_match", main, "begin")
-        L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, self.s2,
+        L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
+                                 self.s2 if self.diagnostics else None,
                                  self.evict, self.dev_status, self.ws_match)
         t("tempcache_match", main, "end")
         t("cache_compact", main, "begin")
@@ -188,7 +198,6 @@ class FastARLayer:
         t("cache_compact", main, "end")
         t("bucket_sort", main, "begin")
         L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
-        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
         t("bucket_sort", main, "end")
         t("sparse_attn", main, "begin")
         L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,

@@ -82,7 +82,12 @@ def test_argument_validation_rejects_before_launch(lib):
                                   0.1, FAKE, 8192, 128, None, None, FAKE, 16, s) == L.EWORKSPACE
     # prompt beyond the limit
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 2000, 0.2, 16, 1,
-                                   FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.ECAPACITY
+                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.ECAPACITY
+    # a bucket order needs the bucket count, and both of its arrays
+    assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
+                                   0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
+    assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
+                                   8, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
     # dense append past capacity
     assert lib.fastar_dense_append(L.BF16, 1, 64, 128, FAKE, FAKE, 8192, 128, FAKE, FAKE, 100, 50, s) == L.ECAPACITY
     # empty work is a successful no-op that touches nothing

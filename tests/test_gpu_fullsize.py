@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 def _graph_step(cfg, inputs, ck, cv):
     """Like gpu_harness.gpu_step, but the measured step runs as a replayed CUDA graph."""
-    layer = GH.make_layer(cfg)
+    layer = GH.make_layer(cfg, diagnostics=False)   # as the benchmark runs it
     layer.set_centroids(GH.to_dev(inputs["centroids"], cfg))
     layer.set_prompt(GH.to_dev(inputs["kp"], cfg), GH.to_dev(inputs["vp"], cfg))
     layer.load_cache(GH.to_dev(ck, cfg), GH.to_dev(cv, cfg))
@@ -30,7 +30,7 @@ def _graph_step(cfg, inputs, ck, cv):
     cout = layer.caches[1 - layer.cur]
     n = GH.np_
     return dict(qb=n(layer.qb), kb_cur=n(layer.kb_cur)[..., 0], kcur_norm=n(layer.kcur_norm), kb_in=kb_in,
-                knorm_in=knorm_in, pb=n(layer.pb)[..., 0], top1=n(layer.top1), s1=n(layer.s1), s2=n(layer.s2),
+                knorm_in=knorm_in, pb=n(layer.pb)[..., 0], top1=n(layer.top1), s1=n(layer.s1), s2=None,
                 evict=n(layer.evict), index_map=n(layer.index_map), len_out=n(cout.len), k_out=n(cout.k),
                 v_out=n(cout.v), kb_out=n(cout.kb)[..., 0], knorm_out=n(cout.knorm), kperm=n(layer.kperm),
                 koff=n(layer.koff), qperm=n(layer.qperm), qoff=n(layer.qoff), o_self=n(layer.o_self),

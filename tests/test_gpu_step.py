@@ -128,6 +128,19 @@ def test_dense_baseline_matches_oracle():
         parity.close(GH.np_(o_c[h]), want["o_cross"], *tol, "dense cross")
 
 
+def test_top1_only_match_equals_top2_match():
+    """The step without the second-best diagnostic (the benchmark's configuration)
+    takes exactly the same decisions and produces the same outputs."""
+    cfg = GH.small_bf16().replace(H=3)
+    inputs = synth.layer_step_inputs(cfg, seed=8)
+    ck, cv = GH.raw_window(inputs, cfg)
+    g1, _ = GH.gpu_step(cfg, inputs, ck, cv, diagnostics=True)
+    g0, _ = GH.gpu_step(cfg, inputs, ck, cv, diagnostics=False)
+    for key in ("top1", "s1", "evict", "index_map", "len_out", "o_self", "o_cross", "keep"):
+        assert np.array_equal(g0[key], g1[key]), key
+    GH.check_step(cfg, inputs, ck, cv, g0)
+
+
 def test_graph_replay_equals_eager():
     cfg = GH.small_bf16()
     inputs = synth.layer_step_inputs(cfg, seed=5)
