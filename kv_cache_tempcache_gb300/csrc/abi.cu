@@ -177,6 +177,7 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   a.lse = lse;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = a.part_o + (size_t)H * nq * r * d;
+  a.cnt = reinterpret_cast<int32_t*>(a.part_lse + (size_t)H * nq * r);
   a.status = dev_status;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
 }

@@ -146,13 +146,18 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
   int k = 0;
   if (p < P) {
     const float mine = s[p];
-    int rank = 0;
-    for (int u = 0; u < P; ++u) {
-      const float o = s[u];
-      rank += (o > mine || (o == mine && u < p)) ? 1 : 0;
-    }
     const int lim = topk < P ? topk : (int)P;
-    k = (mine >= tau_ca || rank < lim) ? 1 : 0;
+    if (mine >= tau_ca) {
+      k = 1;
+    } else {
+      // only "rank < lim" matters: stop counting once lim tokens are known to precede p
+      int rank = 0;
+      for (int u = 0; u < P && rank < lim; ++u) {
+        const float o = s[u];
+        rank += (o > mine || (o == mine && u < p)) ? 1 : 0;
+      }
+      k = rank < lim ? 1 : 0;
+    }
     keep[(int64_t)hf * P + p] = (uint8_t)k;
   }
   // exclusive scan of the keep flags in index order

@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
 }
 
 size_t sparse_attn_workspace(int H, int64_t nq, int d, int r) {
-  return sizeof(float) * (size_t)H * nq * r * (d + 1) + 256;
+  // fp32 partials (o, lse) per (query, slot), then one slot counter per query
+  return sizeof(float) * (size_t)H * nq * r * (d + 1) + sizeof(int32_t) * (size_t)H * nq + 256;
 }
 
 template <typename T, int D>
@@ -319,10 +320,19 @@ static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
     const int64_t tiles = (a.nq * a.r + kAQ - 1) / kAQ + a.B;
     grid = dim3((unsigned)tiles, a.H, 1);
   }
-  if (sizeof(T) == 2 && launch_attn_tc(D, a, s)) {
-    // bf16: tensor-core kernel launched
-  } else {
-    kern<<<grid, 256, smem, s>>>(a);
+  if (sizeof(T) == 2) {
+    // bf16: the tensor-core kernel; for AnnSA it merges the r slots itself (the last
+    // slot of each query to finish does it), counting finished slots in a.cnt
+    if (a.mode == kSparse && a.cnt) {
+      e = cudaMemsetAsync(a.cnt, 0, sizeof(int32_t) * (size_t)a.H * a.nq, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (launch_attn_tc(D, a, s)) return cudaGetLastError();
+  }
+  {
+    AttnArgs b = a;
+    b.cnt = nullptr;
+    kern<<<grid, 256, smem, s>>>(b);
   }
   count_launches(1);
   e = cudaGetLastError();

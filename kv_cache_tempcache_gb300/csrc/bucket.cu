@@ -130,7 +130,7 @@ constexpr int kSortWarps = 32;
 __global__ void __launch_bounds__(kSortWarps * 32)
 bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B,
                    const int32_t* __restrict__ n_valid, int32_t* __restrict__ perm,
-                   int32_t* __restrict__ offsets, int32_t* status) {
+                   int32_t* __restrict__ offsets, int32_t* status, int stage) {
   extern __shared__ int sm_sort[];
   int* cnt = sm_sort;               // [kSortWarps][B]
   int* tot = sm_sort + kSortWarps * B;  // [B + 1]
@@ -148,6 +148,12 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B,
   int32_t* out = perm + (int64_t)h * n * r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kSortWarps * B; i += blockDim.x) cnt[i] = 0;
+  if (stage) {
+    // both passes read the ids: stage them once, coalesced, in shared memory
+    int* ids_s = tot + ((B + 1 + 3) & ~3);
+    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) ids_s[e] = id[e];
+    id = ids_s;
+  }
   __syncthreads();
   const int64_t seg = (E + kSortWarps - 1) / kSortWarps;
   const int64_t beg = warp * seg;
@@ -210,8 +216,15 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B,
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
                                int32_t* status, cudaStream_t s) {
-  const size_t smem = sizeof(int) * ((size_t)kSortWarps * B + B + 1);   // <= 33.8 KB
-  bucket_sort_kernel<<<H, kSortWarps * 32, smem, s>>>(ids, n, r, B, n_valid, perm, offsets, status);
+  // histograms (<= 33.8 KB) plus, when they fit, the head's ids staged in shared memory
+  const size_t base = sizeof(int) * ((size_t)kSortWarps * B + ((B + 1 + 3) & ~3));
+  const size_t staged = base + sizeof(int) * (size_t)(n * r);
+  constexpr size_t kMaxSmem = 200 * 1024;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+  const int stage = (attr == cudaSuccess && staged <= kMaxSmem) ? 1 : 0;
+  bucket_sort_kernel<<<H, kSortWarps * 32, stage ? staged : base, s>>>(ids, n, r, B, n_valid, perm, offsets,
+                                                                         status, stage);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -83,6 +83,7 @@ struct AttnArgs {
   float* lse;
   float* part_o;    // sparse partials [H, nq*r, d]
   float* part_lse;  // [H, nq*r]
+  int32_t* cnt;     // sparse: per-query count of finished slots [H, nq] (tensor-core path)
   int32_t* status;
 };
 

@@ -9,12 +9,14 @@
 //   warp 0      TMA producer: the unit's 256 query rows once (two M=128 tiles), then
 //               128-key tiles of the cache through a 4-deep shared-memory ring;
 //   warp 1      owns TMEM (512 columns = 2 accumulator stages x 2 M-tiles x 128
-//               columns) and issues tcgen05.mma (one thread), committing to the
-//               ring's "empty" barriers and the accumulator's "full" barrier;
-//   warps 2..17 epilogue, four warps per TMEM lane quadrant (M-tile x column half):
-//               load 64 fp32 scores per row with tcgen05.ld, hand the stage back to
-//               the MMA at once, scale by 1/|k_j| (norms prefetched a tile ahead),
-//               keep the running top-1 (and top-2 when asked).
+//               columns) and issues tcgen05.mma (one thread, operand descriptors
+//               as precomputed offsets), committing to the ring's "empty" barriers
+//               and the accumulator's "full" barrier;
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant (one per M-tile): read
+//               each row's 128 fp32 scores in 32-column chunks (the next load in
+//               flight while one is reduced), scale by 1/|k_j| (norms prefetched a
+//               tile ahead, packed f32x2 multiplies), keep the running top-1 (and
+//               top-2 when asked) with three-input max trees.
 // The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
 // 256-query block, key segment); segments split the cache so the unit count
 // fills the machine, and a small finaliser merges the segments' partial top-2s.
@@ -33,17 +35,19 @@ namespace {
 constexpr int kQ = 256;         // queries per unit
 constexpr int kN = 128;         // keys per tile
 constexpr int kStages = 4;      // B ring depth
-constexpr int kThreads = 576;   // 18 warps
+constexpr int kTS = 2;          // TMEM accumulator stages (kTS x 2 M-tiles x kN = 512 columns)
+constexpr int kCPL = kN / 32;   // key columns per epilogue lane for the norm loads
+constexpr int kThreads = 320;   // 10 warps
 constexpr int kTile = 128 * 128; // bytes of one 128-row x 64-element bf16 swizzled block
 
 template <int D>
 struct alignas(1024) MatchSmem {
   uint8_t a[2][D / 64][kTile];
-  uint8_t b[kStages][D / 64][kTile];
-  float invk[16][64];
+  uint8_t b[kStages][D / 64][kN * 128];
+  float invk[8][kN];
   uint64_t a_full, a_empty;
   uint64_t b_full[kStages], b_empty[kStages];
-  uint64_t t_full[2], t_empty[2];
+  uint64_t t_full[kTS], t_empty[kTS];
   uint32_t tmem_base;
   int abort;
 };
@@ -86,17 +90,40 @@ struct Best {
   float m2;
 };
 
+// (a, b) *= (x, y) with one packed f32x2 multiply (each lane rounded to nearest).
+__device__ __forceinline__ void mul2(float& a, float& b, float x, float y) {
+  unsigned long long p =
+      (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+  const unsigned long long q =
+      (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(p) : "l"(q));
+  a = __uint_as_float((unsigned)(p & 0xffffffffull));
+  b = __uint_as_float((unsigned)(p >> 32));
+}
+
+// Three-input maximum (sm_100-family PTX max.f32 with three sources).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <bool kTop2>
 __device__ __forceinline__ void fold32(Best& b, const float* w, int j0) {
-  // balanced max tree (short dependency chains)
-  float t16[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) t16[i] = fmaxf(w[i], w[i + 16]);
-#pragma unroll
-  for (int s = 8; s > 0; s >>= 1)
-#pragma unroll
-    for (int i = 0; i < s; ++i) t16[i] = fmaxf(t16[i], t16[i + s]);
-  const float gm = t16[0];
+  // maximum of the 32 values: four independent three-input chains, then merge
+  float a0 = max3f(w[0], w[1], w[2]), a1 = max3f(w[3], w[4], w[5]);
+  float a2 = max3f(w[6], w[7], w[8]), a3 = max3f(w[9], w[10], w[11]);
+  a0 = max3f(a0, w[12], w[13]);
+  a1 = max3f(a1, w[14], w[15]);
+  a2 = max3f(a2, w[16], w[17]);
+  a3 = max3f(a3, w[18], w[19]);
+  a0 = max3f(a0, w[20], w[21]);
+  a1 = max3f(a1, w[22], w[23]);
+  a2 = max3f(a2, w[24], w[25]);
+  a3 = max3f(a3, w[26], w[27]);
+  a0 = max3f(a0, w[28], w[29]);
+  a1 = max3f(a1, w[30], w[31]);
+  const float gm = max3f(a0, a1, fmaxf(a2, a3));
   if (kTop2) {
     if (gm > b.m2) {
 #pragma unroll
@@ -146,9 +173,9 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc::mbar_init(&sm.b_full[s], 1);
       tc::mbar_init(&sm.b_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kTS; ++s) {
       tc::mbar_init(&sm.t_full[s], 1);
-      tc::mbar_init(&sm.t_empty[s], 16);
+      tc::mbar_init(&sm.t_empty[s], 8);
     }
     sm.abort = 0;
     tc::mbar_fence_init();
@@ -187,7 +214,7 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               tc::tma_load_3d(sm.a[m][kh], &tm_q, kh * 64, w.qb * kQ + m * 128, w.h, &sm.a_full);
         for (int t = w.t_beg; t < w.t_end; ++t) {
           if (!tc::mbar_wait(&sm.b_empty[stage], ph ^ 1, abort)) break;
-          tc::mbar_arrive_tx(&sm.b_full[stage], (uint32_t)(KH * kTile));
+          tc::mbar_arrive_tx(&sm.b_full[stage], (uint32_t)(KH * kN * 128));
           for (int kh = 0; kh < KH; ++kh)
             tc::tma_load_3d(sm.b[stage][kh], &tm_k, kh * 64, t * kN, w.h, &sm.b_full[stage]);
           if (++stage == kStages) {
@@ -202,6 +229,10 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t ph = 0, aph = 0, tph = 0;
+      // descriptors of the first block of A and of the B ring; every other operand
+      // address is a compile-time offset from them (16-byte units in the low field)
+      const uint64_t a_desc0 = tc::sw128_desc(tc::smem_u32(&sm.a[0][0][0]));
+      const uint64_t b_desc0 = tc::sw128_desc(tc::smem_u32(&sm.b[0][0][0]));
       for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
         const Unit w = decode(g, u, clen);
         if (w.t_end <= w.t_beg) continue;
@@ -212,14 +243,17 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (!tc::mbar_wait(&sm.b_full[stage], ph, abort)) break;
           if (!tc::mbar_wait(&sm.t_empty[acc], tph ^ 1, abort)) break;
           tc::tc_fence_after();
-          for (int m = 0; m < w.nm; ++m) {
-            const uint32_t d = tmem + (uint32_t)(acc * 256 + m * 128);
+          const uint64_t bd0 = b_desc0 + (uint64_t)((stage * KH * kN * 128) >> 4);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t koff = (uint32_t)((k & 3) * 32);
-              const uint64_t ad = tc::sw128_desc(tc::smem_u32(sm.a[m][k >> 2]) + koff);
-              const uint64_t bd = tc::sw128_desc(tc::smem_u32(sm.b[stage][k >> 2]) + koff);
-              tc::mma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+          for (int m = 0; m < 2; ++m) {
+            if (m < w.nm) {
+              const uint32_t d = tmem + (uint32_t)(acc * 2 * kN + m * kN);
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k) {
+                const uint64_t ad = a_desc0 + (uint64_t)((m * KH * kTile + (k >> 2) * kTile + (k & 3) * 32) >> 4);
+                const uint64_t bd = bd0 + (uint64_t)(((k >> 2) * kN * 128 + (k & 3) * 32) >> 4);
+                tc::mma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+              }
             }
           }
           tc::mma_commit(&sm.b_empty[stage]);
@@ -228,7 +262,7 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             stage = 0;
             ph ^= 1;
           }
-          if (++acc == 2) {
+          if (++acc == kTS) {
             acc = 0;
             tph ^= 1;
           }
@@ -238,12 +272,12 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ---------------- epilogue ----------------
-    // 16 warps: (lane quadrant, M-tile, column half).  Each thread owns one query row
-    // and 64 of the tile's 128 key columns.
-    const int ew = warp - 2;          // 0..15
+    // 8 warps: (lane quadrant, M-tile).  Each thread owns one query row and the tile's
+    // 128 key columns, read from TMEM in 32-column chunks with the next chunk's load in
+    // flight while the current one is reduced.
+    const int ew = warp - 2;          // 0..7
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int m = (ew >> 2) & 1;      // which M-tile (accumulator) this warp reads
-    const int half = ew >> 3;         // which 64-column half of the tile
+    const int m = ew >> 2;            // which M-tile (accumulator) this warp reads
     float* inv = sm.invk[ew];
     int acc = 0;
     uint32_t tph = 0;
@@ -253,68 +287,67 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int64_t i = (int64_t)w.qb * kQ + rloc;
       Best b{neg_inf(), INT_MAX, neg_inf()};
       const float* kn = cknorm + (int64_t)w.h * g.M;
-      // |k_j| of this lane's two columns of the first tile (prefetched one tile ahead)
-      float kx0 = 0.f, kx1 = 0.f;
-      {
-        const int64_t j = (int64_t)w.t_beg * kN + half * 64 + lane * 2;
-        if (w.t_beg < w.t_end) {
-          kx0 = j < w.n ? kn[j] : 0.f;
-          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
-        }
+      // |k_j| of this lane's four columns of the first tile (prefetched one tile ahead)
+      float kx[kCPL] = {};   // kCPL = kN / 32 columns per lane
+      if (w.t_beg < w.t_end) {
+        const int64_t j = (int64_t)w.t_beg * kN + lane * kCPL;
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
       }
       for (int t = w.t_beg; t < w.t_end; ++t) {
-        const int64_t j0 = (int64_t)t * kN + half * 64;
+        const int64_t j0 = (int64_t)t * kN;
         if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
         tc::tc_fence_after();
         const bool active = m < w.nm;
-        const uint32_t taddr =
-            tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + m * 128 + half * 64);
-        float v[32];
-        if (active) tc::tmem_ld32(taddr, v);
-        // 1/|k_j| of this tile into the warp's buffer while the TMEM load is in flight
-        inv[lane * 2] = kx0 > 0.f ? __frcp_rn(kx0) : 0.f;
-        inv[lane * 2 + 1] = kx1 > 0.f ? __frcp_rn(kx1) : 0.f;
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * kN + m * kN);
+        // the whole row (kN columns) into registers with back-to-back loads, one wait
+        float v[kN];
+        if (active) {
+#pragma unroll
+          for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(taddr + (uint32_t)(c * 32), v + c * 32);
+        }
+        // 1/|k_j| of this tile into the warp's buffer while the TMEM loads are in flight
+#pragma unroll
+        for (int c = 0; c < kCPL; ++c) inv[lane * kCPL + c] = kx[c] > 0.f ? __frcp_rn(kx[c]) : 0.f;
         // prefetch the next tile's norms
         if (t + 1 < w.t_end) {
-          const int64_t j = j0 + kN + lane * 2;
-          kx0 = j < w.n ? kn[j] : 0.f;
-          kx1 = j + 1 < w.n ? kn[j + 1] : 0.f;
+          const int64_t j = j0 + kN + lane * kCPL;
+#pragma unroll
+          for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
         }
+        if (active) tc::tmem_wait_ld();
+        // the scores are in registers: hand the accumulator stage back to the MMA now
+        tc::tc_fence_before();
         __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+        if (++acc == kTS) {
+          acc = 0;
+          tph ^= 1;
+        }
         if (active) {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            if (c == 1) tc::tmem_ld32(taddr + 32, v);
-            tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < kN / 32; ++c) {
+            float* vc = v + c * 32;
+            // scale by 1/|k_j| two lanes at a time (packed f32x2 multiply, round to nearest)
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               const float4 s = *reinterpret_cast<const float4*>(inv + c * 32 + q4 * 4);
-              v[q4 * 4 + 0] *= s.x;
-              v[q4 * 4 + 1] *= s.y;
-              v[q4 * 4 + 2] *= s.z;
-              v[q4 * 4 + 3] *= s.w;
+              mul2(vc[q4 * 4 + 0], vc[q4 * 4 + 1], s.x, s.y);
+              mul2(vc[q4 * 4 + 2], vc[q4 * 4 + 3], s.z, s.w);
             }
             const int64_t jc = j0 + c * 32;
             if (jc + 32 > w.n) {
 #pragma unroll
               for (int x = 0; x < 32; ++x)
-                if (jc + x >= w.n) v[x] = neg_inf();
+                if (jc + x >= w.n) vc[x] = neg_inf();
             }
-            fold32<kTop2>(b, v, (int)jc);
+            fold32<kTop2>(b, vc, (int)jc);
           }
         }
-        // hand the accumulator stage back to the MMA
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          tph ^= 1;
-        }
+        __syncwarp();   // every lane is done with inv before the next tile rewrites it
       }
       if (m * 128 < w.rows && rloc < w.rows && !*abort)
-        part[(((int64_t)w.seg * 2 + half) * g.H + w.h) * g.nq + i] =
-            make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
+        part[((int64_t)w.seg * g.H + w.h) * g.nq + i] = make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
     }
   }
   tc::tc_fence_before();
@@ -372,7 +405,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
                                 128)) {
     return -1;
   }
-  if (!make_tmap_bf16_3d(&tk, ck, D, (uint64_t)M, (uint64_t)H, (uint64_t)D * 2, (uint64_t)M * D * 2, 64, 128))
+  if (!make_tmap_bf16_3d(&tk, ck, D, (uint64_t)M, (uint64_t)H, (uint64_t)D * 2, (uint64_t)M * D * 2, 64, kN))
     return -1;
   MatchGeom g;
   g.H = H;
@@ -396,7 +429,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
     match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
   }
   count_launches(1);
-  return 2 * g.S;   // partial top-2s per (segment, column half)
+  return g.S;   // partial top-2s per segment
 }
 
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,
