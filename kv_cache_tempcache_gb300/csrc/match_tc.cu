@@ -12,14 +12,17 @@
 //               columns) and issues tcgen05.mma (one thread, operand descriptors
 //               as precomputed offsets), committing to the ring's "empty" barriers
 //               and the accumulator's "full" barrier;
-//   warps 2..9  epilogue, two warps per TMEM lane quadrant (one per M-tile): read
-//               each row's 128 fp32 scores in 32-column chunks (the next load in
-//               flight while one is reduced), scale by 1/|k_j| (norms prefetched a
-//               tile ahead, packed f32x2 multiplies), keep the running top-1 (and
-//               top-2 when asked) with three-input max trees.
+//   warps 2..17 epilogue, four warps per TMEM lane quadrant (2 M-tiles x 2 halves
+//               of the tile's columns): each thread reads its row's 64 fp32 scores
+//               in 32-column chunks, scales them by 1/|k_j| (norms prefetched a tile
+//               ahead, packed f32x2 multiplies) and keeps the running top-1 (and
+//               top-2 when asked) with three-input max trees.  The reduction is
+//               latency-bound, so the 16 warps are there to keep enough of it in
+//               flight per SM (8 warps measured about 20% slower).
 // The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
 // 256-query block, key segment); segments split the cache so the unit count
-// fills the machine, and a small finaliser merges the segments' partial top-2s.
+// fills the machine, and a small finaliser merges the partial top-2s of the
+// segments and column halves.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
@@ -36,15 +39,18 @@ constexpr int kQ = 256;         // queries per unit
 constexpr int kN = 128;         // keys per tile
 constexpr int kStages = 4;      // B ring depth
 constexpr int kTS = 2;          // TMEM accumulator stages (kTS x 2 M-tiles x kN = 512 columns)
-constexpr int kCPL = kN / 32;   // key columns per epilogue lane for the norm loads
-constexpr int kThreads = 320;   // 10 warps
+constexpr int kEpW = 16;        // epilogue warps: 4 lane quadrants x 2 M-tiles x kParts column parts
+constexpr int kParts = kEpW / 8;
+constexpr int kCW = kN / kParts;   // key columns per epilogue thread and tile
+constexpr int kCPL = kCW / 32;     // key columns per epilogue lane for the norm loads
+constexpr int kThreads = (2 + kEpW) * 32;
 constexpr int kTile = 128 * 128; // bytes of one 128-row x 64-element bf16 swizzled block
 
 template <int D>
 struct alignas(1024) MatchSmem {
   uint8_t a[2][D / 64][kTile];
   uint8_t b[kStages][D / 64][kN * 128];
-  float invk[8][kN];
+  float invk[kEpW][kCW];
   uint64_t a_full, a_empty;
   uint64_t b_full[kStages], b_empty[kStages];
   uint64_t t_full[kTS], t_empty[kTS];
@@ -152,7 +158,7 @@ template <int D, bool kTop2>
 __global__ void __launch_bounds__(kThreads, 1)
 match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float* __restrict__ cknorm, const int32_t* __restrict__ clen, MatchGeom g,
-                float4* __restrict__ part, uint8_t* __restrict__ evict, int32_t* status) {
+                float4* __restrict__ part_out, uint8_t* __restrict__ evict, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   MatchSmem<D>& sm = *reinterpret_cast<MatchSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -175,7 +181,7 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int s = 0; s < kTS; ++s) {
       tc::mbar_init(&sm.t_full[s], 1);
-      tc::mbar_init(&sm.t_empty[s], 8);
+      tc::mbar_init(&sm.t_empty[s], kEpW);
     }
     sm.abort = 0;
     tc::mbar_fence_init();
@@ -272,12 +278,13 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ---------------- epilogue ----------------
-    // 8 warps: (lane quadrant, M-tile).  Each thread owns one query row and the tile's
-    // 128 key columns, read from TMEM in 32-column chunks with the next chunk's load in
-    // flight while the current one is reduced.
-    const int ew = warp - 2;          // 0..7
+    // kEpW warps: (lane quadrant, M-tile, column part).  Each thread owns one query row
+    // and kCW of the tile's key columns: it loads them from TMEM, hands the stage back
+    // to the MMA, then scales by 1/|k_j| and folds them into its running best.
+    const int ew = warp - 2;          // 0..kEpW-1
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int m = ew >> 2;            // which M-tile (accumulator) this warp reads
+    const int m = (ew >> 2) & 1;      // which M-tile (accumulator) this warp reads
+    const int part = ew >> 3;         // which kCW-column part of the tile
     float* inv = sm.invk[ew];
     int acc = 0;
     uint32_t tph = 0;
@@ -287,26 +294,23 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int64_t i = (int64_t)w.qb * kQ + rloc;
       Best b{neg_inf(), INT_MAX, neg_inf()};
       const float* kn = cknorm + (int64_t)w.h * g.M;
-      // |k_j| of this lane's four columns of the first tile (prefetched one tile ahead)
-      float kx[kCPL] = {};   // kCPL = kN / 32 columns per lane
+      // |k_j| of this lane's columns of the first tile (prefetched one tile ahead)
+      float kx[kCPL] = {};
       if (w.t_beg < w.t_end) {
-        const int64_t j = (int64_t)w.t_beg * kN + lane * kCPL;
+        const int64_t j = (int64_t)w.t_beg * kN + part * kCW + lane * kCPL;
 #pragma unroll
         for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
       }
       for (int t = w.t_beg; t < w.t_end; ++t) {
-        const int64_t j0 = (int64_t)t * kN;
+        const int64_t j0 = (int64_t)t * kN + part * kCW;
         if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
         tc::tc_fence_after();
         const bool active = m < w.nm;
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * kN + m * kN);
-        // the whole row (kN columns) into registers with back-to-back loads, one wait
-        float v[kN];
-        if (active) {
-#pragma unroll
-          for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(taddr + (uint32_t)(c * 32), v + c * 32);
-        }
-        // 1/|k_j| of this tile into the warp's buffer while the TMEM loads are in flight
+        const uint32_t taddr =
+            tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * kN + m * kN + part * kCW);
+        float vc[32];
+        if (active) tc::tmem_ld32(taddr, vc);
+        // 1/|k_j| of this tile into the warp's buffer while the TMEM load is in flight
 #pragma unroll
         for (int c = 0; c < kCPL; ++c) inv[lane * kCPL + c] = kx[c] > 0.f ? __frcp_rn(kx[c]) : 0.f;
         // prefetch the next tile's norms
@@ -315,19 +319,18 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
         }
-        if (active) tc::tmem_wait_ld();
-        // the scores are in registers: hand the accumulator stage back to the MMA now
-        tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
-        if (++acc == kTS) {
-          acc = 0;
-          tph ^= 1;
-        }
         if (active) {
 #pragma unroll
-          for (int c = 0; c < kN / 32; ++c) {
-            float* vc = v + c * 32;
+          for (int c = 0; c < kCW / 32; ++c) {
+            if (c > 0) tc::tmem_ld32(taddr + (uint32_t)(c * 32), vc);
+            tc::tmem_wait_ld();
+            if (c == kCW / 32 - 1) {
+              // the last scores are in registers: hand the stage back to the MMA now
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+            }
             // scale by 1/|k_j| two lanes at a time (packed f32x2 multiply, round to nearest)
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
@@ -343,11 +346,20 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             fold32<kTop2>(b, vc, (int)jc);
           }
+        } else {
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+        }
+        if (++acc == kTS) {
+          acc = 0;
+          tph ^= 1;
         }
         __syncwarp();   // every lane is done with inv before the next tile rewrites it
       }
       if (m * 128 < w.rows && rloc < w.rows && !*abort)
-        part[((int64_t)w.seg * g.H + w.h) * g.nq + i] = make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
+        part_out[(((int64_t)w.seg * kParts + part) * g.H + w.h) * g.nq + i] =
+            make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
     }
   }
   tc::tc_fence_before();
@@ -385,7 +397,7 @@ int match_tc_splits(int H, int64_t nq, int64_t M) {
 }
 
 size_t match_tc_workspace(int H, int64_t nq, int64_t M) {
-  return sizeof(float4) * (size_t)16 * H * (size_t)nq;   // up to 8 segments x 2 column halves
+  return sizeof(float4) * (size_t)8 * kParts * H * (size_t)nq;   // up to 8 segments x kParts column parts
 }
 
 // Launches the tensor-core match (writes `part` as [S, H, nq] and clears evict).
@@ -429,7 +441,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
     match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
   }
   count_launches(1);
-  return g.S;   // partial top-2s per segment
+  return g.S * kParts;   // partial top-2s per (segment, column part)
 }
 
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,

@@ -154,14 +154,17 @@ class FastARLayer:
         self.cur = 0
 
     # ---- the step ------------------------------------------------------------------------------
-    def _enqueue(self, q, k_cur, v_cur, src: int, timer=None):
+    def _enqueue(self, q, k_cur, v_cur, src: int, timer=None, serial: bool = False):
         """Enqueues one step reading cache `src` and writing cache 1 - src.
 
         timer: optional callable(name, stream, phase) invoked around each stage
         ("begin"/"end") on the stream the stage is launched on (for per-stage timing
-        with CUDA events; never used inside a graph capture)."""
+        with CUDA events; never used inside a graph capture).
+        serial: run the AnnCA branch on the main stream too (one kernel at a time,
+        so that per-stage times are those of each stage alone)."""
         cin, cout = self.caches[src], self.caches[1 - src]
         main = torch.cuda.current_stream(self.dev)
+        side = main if serial else self.side
         t = timer or (lambda *a: None)
         t("bucket_assign", main, "begin")
         L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
@@ -172,19 +175,20 @@ class FastARLayer:
         L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
         t("bucket_sort_q", main, "end")
         # AnnCA branch on the side stream
-        ev = torch.cuda.Event()
-        ev.record(main)
-        self.side.wait_event(ev)
-        with torch.cuda.stream(self.side):
-            t("annca_select", self.side, "begin")
+        if not serial:
+            ev = torch.cuda.Event()
+            ev.record(main)
+            side.wait_event(ev)
+        with torch.cuda.stream(side):
+            t("annca_select", side, "begin")
             L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate,
                                   self.keep, self.kidx, self.kcnt, self.score, B=self.B, qperm=self.qperm,
                                   qoff=self.qoff)
-            t("annca_select", self.side, "end")
-            t("cross_attn_subset", self.side, "begin")
+            t("annca_select", side, "end")
+            t("cross_attn_subset", side, "begin")
             L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale,
                                        self.o_cross, self.lse_cross)
-            t("cross_attn_subset", self.side, "end")
+            t("cross_attn_subset", side, "end")
         # TempCache + AnnSA on the main stream
         t("tempcache_match", main, "begin")
         L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
@@ -203,14 +207,16 @@ class FastARLayer:
         L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
                              self.scale, self.o_self, self.lse_self, self.dev_status, self.ws_attn)
         t("sparse_attn", main, "end")
-        ev2 = torch.cuda.Event()
-        ev2.record(self.side)
-        main.wait_event(ev2)
+        if not serial:
+            ev2 = torch.cuda.Event()
+            ev2.record(side)
+            main.wait_event(ev2)
 
-    def step(self, q, k_cur, v_cur, advance: bool = True, timer=None):
+    def step(self, q, k_cur, v_cur, advance: bool = True, timer=None, serial: bool = False):
         """Runs one chunk step (asynchronously, on the current stream).  With
-        advance=False the cache state is not swapped, so the same step can be repeated."""
-        self._enqueue(q, k_cur, v_cur, self.cur, timer)
+        advance=False the cache state is not swapped, so the same step can be repeated;
+        serial=True keeps every kernel on the current stream."""
+        self._enqueue(q, k_cur, v_cur, self.cur, timer, serial)
         if advance:
             self.cur = 1 - self.cur
         return self.o_self, self.o_cross
