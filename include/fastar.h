@@ -91,6 +91,10 @@ const char* fastar_status_string(int status);
 /* Library ABI version (major*100 + minor). */
 int fastar_version(void);
 
+/* Text of the CUDA error behind the calling thread's most recent FASTAR_ECUDA
+ * return ("no error" if there was none); static storage. */
+const char* fastar_last_cuda_error(void);
+
 /* Number of kernels the library has enqueued in this process so far (a
  * diagnostic: the difference across a captured step is that step's launch count). */
 long long fastar_kernel_launches(void);

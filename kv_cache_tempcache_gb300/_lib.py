@@ -31,6 +31,7 @@ _S = ctypes.c_size_t
 _SIGS = {
     "fastar_version": [],
     "fastar_kernel_launches": [],
+    "fastar_last_cuda_error": [],
     "fastar_status_string": [_I],
     "fastar_workspace_bytes": [_I, _I, _L, _L, _I, _I, _I, _L, _I],
     "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
@@ -49,15 +50,17 @@ _SIGS = {
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
 }
 _RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
-             "fastar_kernel_launches": ctypes.c_longlong}
+             "fastar_kernel_launches": ctypes.c_longlong, "fastar_last_cuda_error": ctypes.c_char_p}
 
 _lib: Optional[ctypes.CDLL] = None
 
 
 class FastarError(RuntimeError):
-    def __init__(self, name: str, code: int):
-        super().__init__(f"{name} returned {code}: {status_string(code)}")
+    def __init__(self, name: str, code: int, detail: str | None = None):
+        msg = f"{name} returned {code}: {status_string(code)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.code = code
+        self.detail = detail
 
 
 def open_library(path: str) -> ctypes.CDLL:
@@ -134,9 +137,11 @@ def tok_strides(t: torch.Tensor):
 
 
 def _call(name, *args):
-    rc = getattr(load(), name)(*args)
+    lib = load()
+    rc = getattr(lib, name)(*args)
     if rc != OK:
-        raise FastarError(name, rc)
+        detail = lib.fastar_last_cuda_error().decode() if rc == ECUDA else None
+        raise FastarError(name, rc, detail)
 
 
 # ---- entry points --------------------------------------------------------------------------

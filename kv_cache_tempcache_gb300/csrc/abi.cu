@@ -35,13 +35,21 @@ int check_tok(const void* p, int dtype, int d, int64_t hs, int64_t ts, int64_t n
   return FASTAR_OK;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FASTAR_OK : FASTAR_ECUDA; }
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return FASTAR_OK;
+  g_last_cuda = e;
+  return FASTAR_ECUDA;
+}
 
 }  // namespace
 
 extern "C" {
 
 int fastar_version(void) { return 100; }
+
+const char* fastar_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 long long fastar_kernel_launches(void) { return fastar::g_launches.load(std::memory_order_relaxed); }
 
@@ -63,7 +71,7 @@ size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B,
   switch (op) {
     case FASTAR_OP_MATCH: return fastar::match_workspace(H, n, M);
     case FASTAR_OP_SORT: return 0;
-    case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r);
+    case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r, B);
     case FASTAR_OP_ANNCA: return fastar::annca_workspace(H, F, P);
     default: return 0;
   }
@@ -154,7 +162,7 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, nq, H))) return rc;
   if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, nq, H))) return rc;
   if (!qperm || !qoff || !kperm || !koff || !k || !v || !aligned16(k) || !aligned16(v)) return FASTAR_EINVAL;
-  const size_t need = fastar::sparse_attn_workspace(H, nq, d, r);
+  const size_t need = fastar::sparse_attn_workspace(H, nq, d, r, B);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
   fastar::AttnArgs a{};
   a.mode = fastar::kSparse;
@@ -178,6 +186,12 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = a.part_o + (size_t)H * nq * r * d;
   a.cnt = reinterpret_cast<int32_t*>(a.part_lse + (size_t)H * nq * r);
+  {
+    const uintptr_t at = reinterpret_cast<uintptr_t>(a.cnt + (size_t)H * nq);
+    uint8_t* plan = reinterpret_cast<uint8_t*>((at + 15) & ~static_cast<uintptr_t>(15));
+    a.items = plan;
+    a.n_items = reinterpret_cast<int32_t*>(plan + fastar::sparse_plan_bytes(H, nq, r, B) - 16);
+  }
   a.status = dev_status;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
 }

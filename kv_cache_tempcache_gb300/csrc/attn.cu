@@ -296,9 +296,11 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   if (lane == 0 && a.lse) a.lse[(int64_t)h * a.nq + i] = W > 0.f ? mx + __logf(W) : neg_inf();
 }
 
-size_t sparse_attn_workspace(int H, int64_t nq, int d, int r) {
-  // fp32 partials (o, lse) per (query, slot), then one slot counter per query
-  return sizeof(float) * (size_t)H * nq * r * (d + 1) + sizeof(int32_t) * (size_t)H * nq + 256;
+size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B) {
+  // fp32 partials (o, lse) per (query, slot), one slot counter per query, then (16-byte
+  // aligned) the tensor-core path's work list and its length
+  const size_t head = sizeof(float) * (size_t)H * nq * r * (d + 1) + sizeof(int32_t) * (size_t)H * nq;
+  return ((head + 15) & ~(size_t)15) + sparse_plan_bytes(H, nq, r, B) + 256;
 }
 
 template <typename T, int D>
@@ -323,10 +325,6 @@ static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
   if (sizeof(T) == 2) {
     // bf16: the tensor-core kernel; for AnnSA it merges the r slots itself (the last
     // slot of each query to finish does it), counting finished slots in a.cnt
-    if (a.mode == kSparse && a.cnt) {
-      e = cudaMemsetAsync(a.cnt, 0, sizeof(int32_t) * (size_t)a.H * a.nq, s);
-      if (e != cudaSuccess) return e;
-    }
     if (launch_attn_tc(D, a, s)) return cudaGetLastError();
   }
   {

@@ -9,68 +9,83 @@
 //            against its kept prompt tokens;
 //   dense  — the dense baseline (technical summary, Key Results): every key.
 //
-// One CTA per 128-query tile, warp-specialised:
-//   warps 0-3  gather rows with 16-byte cp.async into 128-byte-swizzled tiles, fence
-//              them to the async proxy and arrive on mbarriers;
-//   warp 4     owns TMEM and issues tcgen05.mma from one thread: S_j = Q K_j^T, then
-//              O += P_j V_j once the softmax has written P_j;
-//   warps 5-8  softmax, one query row per thread: S row from TMEM, running max in
-//              log2 units with lazy rescaling (O in TMEM is rescaled only when the
-//              max grows by more than 2^8), P as bf16 into shared memory, and the
-//              final O / l written out.
-// Two variants (template KV):
-//   KV = 2  streaming: a 2-deep K/V ring (warps 0-1 load even tiles, 2-3 odd ones),
-//           S double-buffered in TMEM so QK_{j+1} overlaps the softmax of tile j.
-//           For long key lists (the dense baseline).  ~195 KB shared, 1 CTA/SM.
-//   KV = 1  compact: one K/V stage, one S buffer, P written over the consumed K tile
-//           (d = 128).  ~100 KB shared and 256 TMEM columns, so two CTAs share an SM
-//           and hide each other's gather latency.  For the short per-bucket and
-//           per-frame lists of AnnSA and AnnCA.
+// A work item is one tile of up to 128 query rows with its key list.  The kernel is
+// persistent (one CTA per SM, items taken round-robin) and warp-specialised so that
+// the gathers of the next item overlap the arithmetic of this one:
+//   warps 0-3   gather rows with 16-byte cp.async into 128-byte-swizzled tiles: the
+//               item's Q tile (two Q stages) and its 128-key K/V tiles (two K/V
+//               stages), keeping up to three copy groups in flight per thread;
+//   warp 4      owns TMEM (S double buffer + one O accumulator per Q stage) and
+//               issues tcgen05.mma from one thread: S_j = Q K_j^T, and O += P_j V_j
+//               once the softmax has written P_j (QK_{j+1} is issued before PV_j);
+//   warps 5-8   softmax, one query row per thread: S row from TMEM, running max in
+//               log2 units with lazy rescaling (O in TMEM is rescaled only when the
+//               max grows by more than 2^8), P as bf16 into shared memory (over the
+//               consumed K tile when d = 128);
+//   warps 9-12  epilogue: O / l from TMEM to the output (or, for AnnSA, the slot
+//               partial and the merge) while the next item is being computed.
+// AnnSA's items (head, bucket, 128-pair tile) are listed by a one-CTA planning kernel
+// that also clears the per-query slot counters.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace fastar {
 namespace {
 
-constexpr int kAT = 128;         // query rows per CTA and keys per tile
-constexpr int kThreadsA = 288;   // 9 warps
-constexpr int kBlkA = 128 * 128; // one 128-row x 64-element bf16 block (128-B swizzle)
+constexpr int kAT = 128;          // query rows per item and keys per tile
+constexpr int kThreadsA = 416;    // 13 warps
+constexpr int kBlkA = 128 * 128;  // one 128-row x 64-element bf16 block (128-B swizzle)
 constexpr int kMmaWarpA = 4;
+constexpr int kSoftWarp0 = 5;
+constexpr int kEpiWarp0 = 9;
+constexpr int kPlanThreads = 1024;
+
+// One AnnSA work item, as listed by the planning kernel.
+struct SparseItem {
+  int h, q0, q1, kbase, nkeys, pad0, pad1, pad2;
+};
+
+struct ItemInfo {
+  int h, T, f, pad;
+  int64_t nkeys, kbase;
+};
 
 struct AttnCtl {
-  int64_t qsrc[kAT];
-  int64_t ksrc[2][kAT];
-  int qdst[kAT];
-  int pre[FASTAR_MAX_B + 1];
-  int wsum[kThreadsA / 32];
-  uint64_t q_full;
+  int64_t qsrc[2][kAT];   // loader-private: source offset of each query row, per Q stage
+  int64_t ksrc[2][kAT];   // loader-private: source offset of each key row, per K/V stage
+  int qdst[2][kAT];       // output row of each query row (-1: none), per Q stage
+  float mrow[2][kAT], lrow[2][kAT];   // softmax max (log2 units) and sum, per Q stage
+  ItemInfo info[2];
+  uint64_t q_full[2], q_empty[2], dst_free[2];
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, p_empty;
+  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t pv_done, fin;
+  uint64_t ml_full[2], o_full[2], o_empty[2];
   uint32_t tmem_base;
   int abort;
-  int item[4];       // valid, -, bucket (sparse) / frame (cross)
-  int64_t range[3];  // query range begin/end (sparse: positions in qperm; else token index), key base
-  int64_t nkeys;
+  int n_items;
 };
 
 // Shared-memory layout (bytes from the 1024-aligned base).
-template <int D, int KV>
+template <int D>
 struct AttnLayout {
   static constexpr int KH = D / 64;
-  static constexpr bool kPAliasK = (KV == 1 && D == 128);   // P (32 KB) over the consumed K tile
+  static constexpr size_t stage = (size_t)KH * kBlkA;   // one 128-row tile of Q, K or V
+  static constexpr bool kPAliasK = D == 128;           // P (128 x 128 bf16) over the consumed K tile
   static constexpr size_t q = 0;
-  static constexpr size_t k = q + (size_t)KH * kBlkA;
-  static constexpr size_t v = k + (size_t)KV * KH * kBlkA;
-  static constexpr size_t p = kPAliasK ? k : v + (size_t)KV * KH * kBlkA;
-  static constexpr size_t ctl = (kPAliasK ? v + (size_t)KV * KH * kBlkA : p + 2 * (size_t)kBlkA);
+  static constexpr size_t k = q + 2 * stage;
+  static constexpr size_t v = k + 2 * stage;
+  static constexpr size_t p = kPAliasK ? k : v + 2 * stage;
+  static constexpr size_t pstride = kPAliasK ? stage : 2 * (size_t)kBlkA;
+  static constexpr size_t ctl = kPAliasK ? v + 2 * stage : p + 2 * pstride;
   static constexpr size_t bytes = ctl + sizeof(AttnCtl) + 1024;
-  static constexpr uint32_t tmem_cols = KV == 2 ? 512 : 256;   // S buffers (KV x 128) + O (128)
-  static constexpr uint32_t o_col = KV * 128;
+  static constexpr uint32_t s_col = 0;      // S buffers: columns [0, 256)
+  static constexpr uint32_t o_col = 256;    // O accumulators: [256 + 128 * stage, ...)
 };
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -90,164 +105,147 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Element offset of key u of the CTA's key list (-1 if out of range).
-__device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const AttnCtl& c, int h, int64_t u, int D) {
-  if (u >= c.nkeys) return -1;
+__device__ __forceinline__ int64_t items_of(const AttnArgs& a) {
+  if (a.mode == kCross) return (int64_t)a.H * a.F * ((a.tpf + kAT - 1) / kAT);
+  if (a.mode == kDense) return (int64_t)a.H * ((a.nq + kAT - 1) / kAT);
+  return 0;   // sparse: from the planning kernel
+}
+
+// Work item u: its head, key count and key base, and its query range [q0, q1) (sparse:
+// positions in the head's qperm row; otherwise token rows).
+__device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemInfo& it, int64_t& q0,
+                                            int64_t& q1) {
+  it.f = 0;
+  it.kbase = 0;
   if (a.mode == kSparse) {
-    const int s = a.kperm[(int64_t)h * a.M + c.range[2] + u];
-    if (s >= 0 && s < a.M) return ((int64_t)h * a.M + s) * D;
+    const int4* p = reinterpret_cast<const int4*>(static_cast<const SparseItem*>(a.items) + u);
+    const int4 x = p[0], y = p[1];
+    it.h = x.x;
+    q0 = x.y;
+    q1 = x.z;
+    it.kbase = x.w;
+    it.nkeys = y.x;
+  } else if (a.mode == kCross) {
+    const int64_t nqt = (a.tpf + kAT - 1) / kAT;
+    const int64_t per = (int64_t)a.F * nqt;
+    it.h = (int)(u / per);
+    const int64_t rem = u % per;
+    it.f = (int)(rem / nqt);
+    const int64_t t0 = (rem % nqt) * kAT;
+    q0 = (int64_t)it.f * a.tpf + t0;
+    q1 = (int64_t)it.f * a.tpf + (t0 + kAT < a.tpf ? t0 + kAT : a.tpf);
+    int64_t nk = a.kcnt[(int64_t)it.h * a.F + it.f];
+    if (nk < 0 || nk > a.P) {
+      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      nk = nk < 0 ? 0 : a.P;
+    }
+    it.nkeys = nk;
+  } else {
+    const int64_t nqt = (a.nq + kAT - 1) / kAT;
+    it.h = (int)(u / nqt);
+    q0 = (u % nqt) * kAT;
+    q1 = q0 + kAT < a.nq ? q0 + kAT : a.nq;
+    it.nkeys = a.nk;
+  }
+  it.T = (int)((it.nkeys + kAT - 1) / kAT);
+}
+
+// Element offset of key u of the item's key list (-1 if out of range).
+__device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const ItemInfo& it, int64_t u, int D) {
+  if (u >= it.nkeys) return -1;
+  if (a.mode == kSparse) {
+    const int s = a.kperm[(int64_t)it.h * a.M + it.kbase + u];
+    if (s >= 0 && s < a.M) return ((int64_t)it.h * a.M + s) * D;
     flag_status(a.status, FASTAR_DEV_BAD_INDEX);
     return -1;
   }
   if (a.mode == kCross) {
-    const int p = a.kidx[((int64_t)h * a.F + c.item[2]) * a.P + u];
-    if (p >= 0 && p < a.P) return ((int64_t)h * a.P + p) * D;
+    const int p = a.kidx[((int64_t)it.h * a.F + it.f) * a.P + u];
+    if (p >= 0 && p < a.P) return ((int64_t)it.h * a.P + p) * D;
     flag_status(a.status, FASTAR_DEV_BAD_INDEX);
     return -1;
   }
-  return h * a.kv_hs + u * a.kv_ts;
+  return it.h * a.kv_hs + u * a.kv_ts;
 }
 
-template <int D, int KV>
-__global__ void __launch_bounds__(kThreadsA, KV == 1 ? 2 : 1) attn_tc_kernel(const AttnArgs a) {
-  using Lay = AttnLayout<D, KV>;
-  constexpr int KH = D / 64;
+// Copy groups a loader thread has committed but not yet signalled (at most two are
+// kept in flight; before any blocking wait all of them are signalled, so a consumer
+// is never left waiting on a copy whose producer is itself waiting).
+struct Pending {
+  uint64_t* b0 = nullptr;
+  uint64_t* b1 = nullptr;
+  __device__ __forceinline__ void flush() {
+    if (!b0) return;
+    tc::cp_async_wait<0>();
+    tc::fence_proxy_async();
+    tc::mbar_arrive(b0);
+    if (b1) tc::mbar_arrive(b1);
+    b0 = b1 = nullptr;
+  }
+  __device__ __forceinline__ void push(uint64_t* b) {
+    if (b1) {
+      tc::cp_async_wait<2>();   // the oldest of the three groups has landed
+      tc::fence_proxy_async();
+      tc::mbar_arrive(b0);
+      b0 = b1;
+      b1 = b;
+    } else if (b0) {
+      b1 = b;
+    } else {
+      b0 = b;
+    }
+  }
+  __device__ __forceinline__ bool acquire(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (tc::mbar_test(bar, parity)) return true;
+    flush();
+    return tc::mbar_wait(bar, parity, abort);
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a) {
+  using Lay = AttnLayout<D>;
   constexpr int CPR = D / 8;   // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sq = base + Lay::q;
-  uint8_t* sk = base + Lay::k;   // [KV][KH][kBlkA]
-  uint8_t* sv = base + Lay::v;   // [KV][KH][kBlkA]
-  uint8_t* sp = base + Lay::p;   // [2][kBlkA]
+  uint8_t* sq = base + Lay::q;   // [2][KH][kBlkA]
+  uint8_t* sk = base + Lay::k;   // [2][KH][kBlkA]
+  uint8_t* sv = base + Lay::v;   // [2][KH][kBlkA]
+  uint8_t* sp = base + Lay::p;   // [2] x pstride
   AttnCtl& sm = *reinterpret_cast<AttnCtl*>(base + Lay::ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q.p);
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(a.v);
-  const int h = blockIdx.y;
   const int64_t np = a.nq * a.r;
 
-  if (a.mode == kSparse) {
-    // exclusive prefix over buckets of their 128-pair tile counts, all threads at once
-    const int t = threadIdx.x;
-    const int32_t* qo = a.qoff + (int64_t)h * (a.B + 1);
-    int v = 0;
-    if (t < a.B) {
-      const int c = qo[t + 1] - qo[t];
-      v = c > 0 ? (c + kAT - 1) / kAT : 0;
-    }
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) sm.wsum[warp] = incl;
-    __syncthreads();
-    if (t == 0) {
-      int run = 0;
-      for (int w2 = 0; w2 < kThreadsA / 32; ++w2) {
-        const int x = sm.wsum[w2];
-        sm.wsum[w2] = run;
-        run += x;
-      }
-    }
-    __syncthreads();
-    if (t < a.B) sm.pre[t] = sm.wsum[warp] + incl - v;
-    if (t == a.B - 1) sm.pre[a.B] = sm.wsum[warp] + incl;
-    __syncthreads();
-  }
   if (threadIdx.x == 0) {
-    tc::mbar_init(&sm.q_full, 128);
-    for (int s = 0; s < KV; ++s) {
-      tc::mbar_init(&sm.kv_full[s], KV == 2 ? 64 : 128);   // the loader group of the stage
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&sm.q_full[s], 128);
+      tc::mbar_init(&sm.q_empty[s], 1);
+      tc::mbar_init(&sm.dst_free[s], 4);
+      tc::mbar_init(&sm.kv_full[s], 128);
       tc::mbar_init(&sm.kv_empty[s], 1);
-    }
-    for (int s = 0; s < KV; ++s) {
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.s_free[s], 4);
+      tc::mbar_init(&sm.p_full[s], 4);
+      tc::mbar_init(&sm.ml_full[s], 4);
+      tc::mbar_init(&sm.o_full[s], 1);
+      tc::mbar_init(&sm.o_empty[s], 4);
     }
-    tc::mbar_init(&sm.p_full, 4);
-    tc::mbar_init(&sm.p_empty, 1);
+    tc::mbar_init(&sm.pv_done, 1);
+    tc::mbar_init(&sm.fin, 1);
     sm.abort = 0;
-    // decode the work item
-    int valid = 1;
-    if (a.mode == kSparse) {
-      const int32_t* qo = a.qoff + (int64_t)h * (a.B + 1);
-      const int acc = sm.pre[a.B];
-      int b = -1;
-      if ((int)blockIdx.x < acc) {
-        int lo = 0, hi = a.B - 1;   // last b with pre[b] <= blockIdx.x
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (sm.pre[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-      }
-      valid = b >= 0;
-      if (valid) {
-        const int64_t q0 = qo[b] + (int64_t)(blockIdx.x - sm.pre[b]) * kAT;
-        const int64_t q1 = qo[b + 1];
-        sm.range[0] = q0;
-        sm.range[1] = q0 + kAT < q1 ? q0 + kAT : q1;
-        const int32_t* ko = a.koff + (int64_t)h * (a.B + 1);
-        sm.range[2] = ko[b];
-        sm.nkeys = ko[b + 1] - ko[b];
-        if (sm.nkeys < 0 || sm.range[2] < 0 || sm.range[2] + sm.nkeys > a.M) {
-          flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-          sm.nkeys = 0;
-        }
-      }
-      sm.item[2] = b;
-    } else if (a.mode == kCross) {
-      const int f = blockIdx.z;
-      const int64_t t0 = (int64_t)blockIdx.x * kAT;
-      sm.range[0] = (int64_t)f * a.tpf + t0;
-      sm.range[1] = (int64_t)f * a.tpf + (t0 + kAT < a.tpf ? t0 + kAT : a.tpf);
-      int64_t nk = a.kcnt[(int64_t)h * a.F + f];
-      if (nk < 0 || nk > a.P) {
-        flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-        nk = nk < 0 ? 0 : a.P;
-      }
-      sm.nkeys = nk;
-      sm.item[2] = f;
-    } else {
-      const int64_t i0 = (int64_t)blockIdx.x * kAT;
-      sm.range[0] = i0;
-      sm.range[1] = i0 + kAT < a.nq ? i0 + kAT : a.nq;
-      sm.nkeys = a.nk;
-    }
-    sm.item[0] = valid;
+    int64_t n = a.mode == kSparse ? (int64_t)*a.n_items : items_of(a);
+    sm.n_items = (int)(n < INT_MAX ? n : INT_MAX);
     tc::mbar_fence_init();
   }
   __syncthreads();
-  if (!sm.item[0]) return;   // no work for this CTA (uniform; nothing allocated yet)
-  // query rows of the tile: source offset and output row
-  if (threadIdx.x < kAT) {
-    const int lt = threadIdx.x;
-    const int64_t pos = sm.range[0] + lt;
-    int64_t src = -1;
-    int dst = -1;
-    if (pos < sm.range[1]) {
-      if (a.mode == kSparse) {
-        const int e = a.qperm[(int64_t)h * np + pos];
-        if (e >= 0 && e < np) {
-          src = h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
-          dst = e;
-        } else {
-          flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-        }
-      } else {
-        src = h * a.q.hs + pos * a.q.ts;
-        dst = (int)pos;
-      }
-    }
-    sm.qsrc[lt] = src;
-    sm.qdst[lt] = dst;
-  }
+  const int n_items = sm.n_items;
+  if ((int)blockIdx.x >= n_items) return;   // no work for this CTA (uniform; nothing allocated)
   if (warp == kMmaWarpA) {
-    tc::tmem_alloc(&sm.tmem_base, Lay::tmem_cols);
+    tc::tmem_alloc(&sm.tmem_base, 512);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -255,130 +253,190 @@ __global__ void __launch_bounds__(kThreadsA, KV == 1 ? 2 : 1) attn_tc_kernel(con
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
-  const int64_t nkeys = sm.nkeys;
-  const int T = (int)((nkeys + kAT - 1) / kAT);
 
   if (warp < 4) {
     // ---------------- row gathers (128 threads) ----------------
-    const int lt = threadIdx.x;
-#pragma unroll 4
-    for (int g = lt; g < kAT * CPR; g += 128) {
-      const int row = g / CPR, c = g % CPR;
-      const int64_t s = sm.qsrc[row];
-      tc::cp_async16(tc::smem_u32(sq + (c >> 3) * kBlkA) + tc::sw128_off(row, c & 7), s >= 0 ? Q + s + c * 8 : Q,
-                     s >= 0 ? 16u : 0u);
-    }
-    tc::cp_async_commit();
-    tc::cp_async_wait<0>();
-    tc::fence_proxy_async();
-    tc::mbar_arrive(&sm.q_full);
-    // K/V tiles.  KV = 2: warps 0-1 load the even tiles into stage 0, warps 2-3 the odd
-    // ones into stage 1 (two tiles in flight, each group signals its own tile).
-    // KV = 1: all four warps load every tile into the single stage.
-    constexpr int GT = KV == 2 ? 64 : 128;
-    const int grp = KV == 2 ? (warp >> 1) : 0;
-    const int gt = threadIdx.x & (GT - 1);
-    for (int j = grp; j < T && !*abort; j += KV) {
-      const int st = grp;
-      if (!tc::mbar_wait(&sm.kv_empty[st], ((j / KV) & 1) ^ 1, abort)) break;
-      for (int row = gt; row < kAT; row += GT) sm.ksrc[st][row] = key_offset(a, sm, h, (int64_t)j * kAT + row, D);
-      tc::named_bar(1 + grp, GT);
-      uint8_t* kst = sk + (size_t)st * KH * kBlkA;
-      uint8_t* vst = sv + (size_t)st * KH * kBlkA;
-#pragma unroll 4
-      for (int g = gt; g < kAT * CPR; g += GT) {
-        const int row = g / CPR, c = g % CPR;
-        const int64_t s = sm.ksrc[st][row];
-        const uint32_t o = (uint32_t)((c >> 3) * kBlkA) + tc::sw128_off(row, c & 7);
-        tc::cp_async16(tc::smem_u32(kst) + o, s >= 0 ? K + s + c * 8 : K, s >= 0 ? 16u : 0u);
-        tc::cp_async16(tc::smem_u32(vst) + o, s >= 0 ? V + s + c * 8 : V, s >= 0 ? 16u : 0u);
+    const int t = threadIdx.x;
+    // Every exit decision is taken by all 128 threads together (named_bar_and): a
+    // thread that left alone would strand the others in the next named barrier.
+    Pending pend;
+    int g = 0, n = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_items && ok; u += gridDim.x, ++n) {
+      const int qs = n & 1;
+      const uint32_t qph = (n >> 1) & 1;
+      bool got = true;
+      if (n >= 2)
+        got = pend.acquire(&sm.q_empty[qs], qph ^ 1, abort) && pend.acquire(&sm.dst_free[qs], qph ^ 1, abort);
+      ItemInfo it;
+      int64_t q0, q1;
+      decode_item(a, u, it, q0, q1);
+      // this thread's query row: source offset and output row
+      {
+        const int64_t pos = q0 + t;
+        int64_t src = -1;
+        int dst = -1;
+        if (pos < q1) {
+          if (a.mode == kSparse) {
+            const int e = a.qperm[(int64_t)it.h * np + pos];
+            if (e >= 0 && e < np) {
+              src = it.h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
+              dst = e;
+            } else {
+              flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+            }
+          } else {
+            src = it.h * a.q.hs + pos * a.q.ts;
+            dst = (int)pos;
+          }
+        }
+        if (got) {
+          sm.qsrc[qs][t] = src;
+          sm.qdst[qs][t] = dst;
+          if (t == 0) sm.info[qs] = it;
+        }
       }
-      tc::cp_async_commit();
-      tc::cp_async_wait<0>();
-      tc::fence_proxy_async();
-      tc::mbar_arrive(&sm.kv_full[st]);
+      if (!tc::named_bar_and(1, 128, got)) {
+        ok = false;
+        break;
+      }
+      {
+        uint8_t* qst = sq + (size_t)qs * Lay::stage;
+#pragma unroll 4
+        for (int gi = t; gi < kAT * CPR; gi += 128) {
+          const int row = gi / CPR, c = gi % CPR;
+          const int64_t s = sm.qsrc[qs][row];
+          tc::cp_async16(tc::smem_u32(qst + (c >> 3) * kBlkA) + tc::sw128_off(row, c & 7),
+                         s >= 0 ? Q + s + c * 8 : Q, s >= 0 ? 16u : 0u);
+        }
+        tc::cp_async_commit();
+        pend.push(&sm.q_full[qs]);
+      }
+      for (int j = 0; j < it.T; ++j, ++g) {
+        const int st = g & 1;
+        const uint32_t ph = (g >> 1) & 1;
+        const bool free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
+        if (free) sm.ksrc[st][t] = key_offset(a, it, (int64_t)j * kAT + t, D);
+        if (!tc::named_bar_and(1, 128, free)) {
+          ok = false;
+          break;
+        }
+        uint8_t* kst = sk + (size_t)st * Lay::stage;
+        uint8_t* vst = sv + (size_t)st * Lay::stage;
+#pragma unroll 4
+        for (int gi = t; gi < kAT * CPR; gi += 128) {
+          const int row = gi / CPR, c = gi % CPR;
+          const int64_t s = sm.ksrc[st][row];
+          const uint32_t o = (uint32_t)((c >> 3) * kBlkA) + tc::sw128_off(row, c & 7);
+          tc::cp_async16(tc::smem_u32(kst) + o, s >= 0 ? K + s + c * 8 : K, s >= 0 ? 16u : 0u);
+          tc::cp_async16(tc::smem_u32(vst) + o, s >= 0 ? V + s + c * 8 : V, s >= 0 ? 16u : 0u);
+        }
+        tc::cp_async_commit();
+        pend.push(&sm.kv_full[st]);
+      }
     }
+    pend.flush();
   } else if (warp == kMmaWarpA) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0 && T > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kAT);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_bmn(128, D);
       const uint64_t q_desc = tc::sw128_desc(tc::smem_u32(sq));
       const uint64_t k_desc = tc::sw128_desc(tc::smem_u32(sk));
       const uint64_t p_desc = tc::sw128_desc(tc::smem_u32(sp));
       const uint64_t v_desc = tc::sw128_mn_desc(tc::smem_u32(sv), kBlkA);
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % KV, b = j % KV;
-        if (!tc::mbar_wait(&sm.kv_full[st], (j / KV) & 1, abort)) return false;
-        if (!tc::mbar_wait(&sm.s_free[b], ((j / KV) & 1) ^ 1, abort)) return false;
+      // O_qs += P_gt V_gt for global tile gt; `first` starts the accumulator
+      auto issue_pv = [&](int gt, int qs, bool first) -> bool {
+        const int st = gt & 1;
+        if (!tc::mbar_wait(&sm.p_full[st], (gt >> 1) & 1, abort)) return false;
         tc::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (uint32_t)((k >> 2) * kBlkA + (k & 3) * 32);
-          tc::mma_bf16(tmem + (uint32_t)(b * 128), q_desc + (off >> 4),
-                       k_desc + ((uint32_t)(st * KH * kBlkA + off) >> 4), idesc_qk, k > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(&sm.s_full[b]);
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        if (!tc::mbar_wait(&sm.p_full, j & 1, abort)) return false;
-        tc::tc_fence_after();
-        const int st = j % KV;
 #pragma unroll
         for (int ks = 0; ks < kAT / 16; ++ks) {
-          const uint32_t aoff = (uint32_t)((ks >> 2) * kBlkA + (ks & 3) * 32);
-          const uint32_t boff = (uint32_t)(st * KH * kBlkA + ks * 2048);
-          tc::mma_bf16(tmem + Lay::o_col, p_desc + (aoff >> 4), v_desc + (boff >> 4), idesc_pv,
-                       (j > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t aoff = (uint32_t)(st * Lay::pstride + (ks >> 2) * kBlkA + (ks & 3) * 32);
+          const uint32_t boff = (uint32_t)(st * Lay::stage + ks * 2048);
+          tc::mma_bf16(tmem + Lay::o_col + (uint32_t)(qs * 128), p_desc + (aoff >> 4), v_desc + (boff >> 4),
+                       idesc_pv, (!first || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&sm.kv_empty[st]);
-        tc::mma_commit(&sm.p_empty);
+        tc::mma_commit(&sm.pv_done);
         return true;
       };
-      bool ok = tc::mbar_wait(&sm.q_full, 0, abort);
-      if (ok) tc::tc_fence_after();
-      ok = ok && issue_qk(0);
-      for (int j = 0; j < T && ok; ++j) {
-        if (KV == 2) {
-          // the next score tile goes into the other S buffer while the softmax runs
-          if (j + 1 < T && !issue_qk(j + 1)) break;
-          if (!issue_pv(j)) break;
-        } else {
-          // one stage: the next K tile can only land once PV_j has consumed this one
-          if (!issue_pv(j)) break;
-          if (j + 1 < T && !issue_qk(j + 1)) break;
+      int g = 0, n = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_items && ok; u += gridDim.x, ++n) {
+        const int qs = n & 1;
+        const uint32_t qph = (n >> 1) & 1;
+        if (!tc::mbar_wait(&sm.q_full[qs], qph, abort)) break;
+        const int T = sm.info[qs].T;
+        if (!tc::mbar_wait(&sm.o_empty[qs], qph ^ 1, abort)) break;
+        tc::tc_fence_after();
+        for (int j = 0; j < T; ++j, ++g) {
+          const int st = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          if (!tc::mbar_wait(&sm.kv_full[st], ph, abort) || !tc::mbar_wait(&sm.s_free[st], ph ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (uint32_t)((k >> 2) * kBlkA + (k & 3) * 32);
+            tc::mma_bf16(tmem + Lay::s_col + (uint32_t)(st * 128), q_desc + ((uint32_t)(qs * Lay::stage + off) >> 4),
+                         k_desc + ((uint32_t)(st * Lay::stage + off) >> 4), idesc_qk, k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sm.s_full[st]);
+          // the previous tile's P.V goes after this tile's Q.K^T (overlaps the softmax)
+          if (j > 0 && !issue_pv(g - 1, qs, j == 1)) {
+            ok = false;
+            break;
+          }
         }
+        if (!ok) break;
+        if (T > 0 && !issue_pv(g - 1, qs, T == 1)) break;
+        tc::mma_commit(&sm.q_empty[qs]);
+        tc::mma_commit(&sm.o_full[qs]);
       }
+      // let every issued MMA finish before TMEM is released
+      tc::mma_commit(&sm.fin);
+      volatile int never = 0;
+      tc::mbar_wait(&sm.fin, 0, &never, 400000000LL);
     }
-  } else {
-    // ---------------- softmax and output ----------------
+  } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
+    // ---------------- softmax ----------------
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
-    float m_used = neg_inf(), l = 0.f;
+    int g = 0, n = 0;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j % KV;
-      if (!wait_all(&sm.s_full[b], (j / KV) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      const int64_t left = nkeys - (int64_t)j * kAT;
-      const int vcols = left < kAT ? (int)left : kAT;
-      if (KV == 1) {
-        // compact variant (two CTAs per SM, ~100 registers): two passes over the S row in
-        // TMEM, 32 columns at a time — the row maximum, then exp / pack / store of P
+    for (int u = blockIdx.x; u < n_items && ok; u += gridDim.x, ++n) {
+      const int qs = n & 1;
+      const uint32_t qph = (n >> 1) & 1;
+      if (!wait_all(&sm.q_full[qs], qph, abort)) break;
+      const int T = sm.info[qs].T;
+      const int64_t nkeys = sm.info[qs].nkeys;
+      const uint32_t o_addr = tmem + lane_addr + Lay::o_col + (uint32_t)(qs * 128);
+      float m_used = neg_inf(), l = 0.f;
+      for (int j = 0; j < T; ++j, ++g) {
+        const int st = g & 1;
+        if (!wait_all(&sm.s_full[st], (g >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const int64_t left = nkeys - (int64_t)j * kAT;
+        const int vcols = left < kAT ? (int)left : kAT;
+        const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * 128);
+        // pass 1: the row maximum of this tile, 64 columns at a time
         float mt = neg_inf();
 #pragma unroll 1
-        for (int c = 0; c < kAT / 32; ++c) {
-          float x[32];
-          tc::tmem_ld32(tmem + lane_addr + (uint32_t)(c * 32), x);
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[64];
+          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
+          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, c * 32 + i < vcols ? x[i] * sl2 : neg_inf());
+          for (int i = 0; i < 64; ++i) mt = fmaxf(mt, hh * 64 + i < vcols ? x[i] * sl2 : neg_inf());
         }
         float alpha = 1.f;
         bool resc = false;
@@ -387,47 +445,55 @@ __global__ void __launch_bounds__(kThreadsA, KV == 1 ? 2 : 1) attn_tc_kernel(con
           alpha = resc ? ex2(m_used - mt) : 0.f;
           m_used = mt;
         }
-        if (j > 0 && !wait_all(&sm.p_empty, (j - 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
         if (__any_sync(0xffffffffu, resc)) {
+          // O holds the previous tiles' P.V: rescale it once that product has landed
+          if (!wait_all(&sm.pv_done, (g - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
           const float f = resc ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tc::tmem_ld32(tmem + lane_addr + Lay::o_col + (uint32_t)(c * 32), o);
+            tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= f;
-            tc::tmem_st32(tmem + lane_addr + Lay::o_col + (uint32_t)(c * 32), o);
+            tc::tmem_st32(o_addr + (uint32_t)(c * 32), o);
           }
           tc::tmem_wait_st();
         }
+        // pass 2: P = 2^(s - m) as bf16 into the P tile, and its row sum
+        uint8_t* pst = sp + (size_t)st * Lay::pstride;
         float sum = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < kAT / 32; ++c) {
-          float x[32];
-          tc::tmem_ld32(tmem + lane_addr + (uint32_t)(c * 32), x);
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[64];
+          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
+          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
           tc::tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float s0 = c * 32 + i < vcols ? x[i] * sl2 : neg_inf();
-            const float s1 = c * 32 + i + 1 < vcols ? x[i + 1] * sl2 : neg_inf();
-            const float p0 = m_used == neg_inf() ? 0.f : ex2(s0 - m_used);
-            const float p1 = m_used == neg_inf() ? 0.f : ex2(s1 - m_used);
-            sum += p0 + p1;
-            pk[i >> 1] = pack_bf16(p0, p1);
-          }
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int c16 = c * 4 + q4;
-            const uint32_t addr = tc::smem_u32(sp + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]),
-                         "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
-                         : "memory");
+            for (int i = 0; i < 32; i += 2) {
+              const int col = hh * 64 + q2 * 32 + i;
+              const float s0 = col < vcols ? x[q2 * 32 + i] * sl2 : neg_inf();
+              const float s1 = col + 1 < vcols ? x[q2 * 32 + i + 1] * sl2 : neg_inf();
+              const float p0 = m_used == neg_inf() ? 0.f : ex2(s0 - m_used);
+              const float p1 = m_used == neg_inf() ? 0.f : ex2(s1 - m_used);
+              sum += p0 + p1;
+              pk[i >> 1] = pack_bf16(p0, p1);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int c16 = hh * 8 + q2 * 4 + q4;   // 16-byte chunk of the 256-byte P row
+              const uint32_t addr = tc::smem_u32(pst + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]),
+                           "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
+                           : "memory");
+            }
           }
         }
         l = l * alpha + sum;
@@ -435,194 +501,282 @@ __global__ void __launch_bounds__(kThreadsA, KV == 1 ? 2 : 1) attn_tc_kernel(con
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          tc::mbar_arrive(&sm.s_free[b]);
-          tc::mbar_arrive(&sm.p_full);
+          tc::mbar_arrive(&sm.s_free[st]);
+          tc::mbar_arrive(&sm.p_full[st]);
         }
-        continue;
       }
-      float x[kAT];
-#pragma unroll
-      for (int c = 0; c < kAT / 32; ++c) tc::tmem_ld32(tmem + lane_addr + (uint32_t)(b * 128 + c * 32), x + c * 32);
-      tc::tmem_wait_ld();
-      tc::tc_fence_before();
+      if (!ok) break;
+      sm.mrow[qs][row] = m_used;
+      sm.lrow[qs][row] = l;
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.s_free[b]);
-      float mt = neg_inf();
-#pragma unroll
-      for (int i = 0; i < kAT; ++i) {
-        x[i] = i < vcols ? x[i] * sl2 : neg_inf();
-        mt = fmaxf(mt, x[i]);
-      }
-      float alpha = 1.f;
-      bool resc = false;
-      if (mt > m_used + 8.f) {
-        resc = m_used != neg_inf();
-        alpha = resc ? ex2(m_used - mt) : 0.f;
-        m_used = mt;
-      }
-      float sum = 0.f;
-      uint32_t pk[kAT / 2];
-#pragma unroll
-      for (int i = 0; i < kAT; i += 2) {
-        const float p0 = m_used == neg_inf() ? 0.f : ex2(x[i] - m_used);
-        const float p1 = m_used == neg_inf() ? 0.f : ex2(x[i + 1] - m_used);
-        sum += p0 + p1;
-        pk[i >> 1] = pack_bf16(p0, p1);
-      }
-      l = l * alpha + sum;
-      if (j > 0 && !wait_all(&sm.p_empty, (j - 1) & 1, abort)) {
-        ok = false;
+      if (lane == 0) tc::mbar_arrive(&sm.ml_full[qs]);
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    int n = 0;
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x, ++n) {
+      const int qs = n & 1;
+      const uint32_t qph = (n >> 1) & 1;
+      if (!wait_all(&sm.q_full[qs], qph, abort) || !wait_all(&sm.ml_full[qs], qph, abort) ||
+          !wait_all(&sm.o_full[qs], qph, abort))
         break;
-      }
       tc::tc_fence_after();
-      if (__any_sync(0xffffffffu, resc)) {
-        const float f = resc ? alpha : 1.f;
+      const int h = sm.info[qs].h;
+      const int T = sm.info[qs].T;
+      const int dst = sm.qdst[qs][row];
+      const float m_used = sm.mrow[qs][row], l = sm.lrow[qs][row];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.dst_free[qs]);
+      const uint32_t o_addr = tmem + lane_addr + Lay::o_col + (uint32_t)(qs * 128);
+      const bool live = T > 0 && l > 0.f;
+      const float inv = live ? 1.0f / l : 0.f;
+      const float lse = live ? (m_used + __log2f(l)) * 0.6931471805599453f : neg_inf();
+      if (a.mode == kSparse) {
+        const bool has = dst >= 0;
+        const int64_t pb_row = (int64_t)h * np + (has ? dst : 0);
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tc::tmem_ld32(tmem + lane_addr + Lay::o_col + (uint32_t)(c * 32), o);
-          tc::tmem_wait_ld();
+          if (T > 0) {
+            tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
+            tc::tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tc::tmem_st32(tmem + lane_addr + Lay::o_col + (uint32_t)(c * 32), o);
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
+          if (has) {
+            float4* po = reinterpret_cast<float4*>(a.part_o + pb_row * D + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              po[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          }
         }
-        tc::tmem_wait_st();
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < kAT / 8; ++c16) {
-        const uint32_t addr = tc::smem_u32(sp + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[c16 * 4]),
-                     "r"(pk[c16 * 4 + 1]), "r"(pk[c16 * 4 + 2]), "r"(pk[c16 * 4 + 3])
-                     : "memory");
-      }
-      tc::fence_proxy_async();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.p_full);
-    }
-    if (ok && T > 0 && !wait_all(&sm.p_empty, (T - 1) & 1, abort)) ok = false;
-    tc::tc_fence_after();
-    const int dst = sm.qdst[row];
-    const bool live = ok && T > 0 && l > 0.f;
-    const float inv = live ? 1.0f / l : 0.f;
-    const float lse = live ? (m_used + __log2f(l)) * 0.6931471805599453f : neg_inf();
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      if (ok && T > 0) {
-        tc::tmem_ld32(tmem + lane_addr + Lay::o_col + (uint32_t)(c * 32), o);
-        tc::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-      }
-      if (dst >= 0 && ok) {
-        if (a.mode == kSparse) {
-          float4* po = reinterpret_cast<float4*>(a.part_o + ((int64_t)h * np + dst) * D + c * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            po[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
-        } else {
-          uint4* po = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs +
-                                               (int64_t)dst * a.o_ts + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            po[i] = make_uint4(pack_bf16(o[8 * i] * inv, o[8 * i + 1] * inv),
-                               pack_bf16(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                               pack_bf16(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                               pack_bf16(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-        }
-      }
-    }
-    if (dst >= 0 && ok) {
-      if (a.mode == kSparse) {
-        a.part_lse[(int64_t)h * np + dst] = lse;
-        if (a.cnt) {
+        int old = -1;
+        const int64_t qi = has ? dst / a.r : 0;
+        if (has) {
+          a.part_lse[pb_row] = lse;
           // the last of the query's r slots to finish merges them (no waiting: the
           // earlier slots only publish their partials)
-          const int64_t qi = dst / a.r;
           __threadfence();
-          const int old = atomicAdd(&a.cnt[(int64_t)h * a.nq + qi], 1);
-          if (old == a.r - 1) {
+          old = atomicAdd(&a.cnt[(int64_t)h * a.nq + qi], 1);
+        }
+        const bool last = has && old == a.r - 1;
+        if (__any_sync(0xffffffffu, last)) {
+          const int own = has ? dst % a.r : 0;
+          const int64_t pb = (int64_t)h * np + qi * a.r;
+          float mx = neg_inf(), W = 0.f;
+          if (last) {
             __threadfence();
-            const int64_t pb = (int64_t)h * np + qi * a.r;
-            float mx = neg_inf();
-            for (int s = 0; s < a.r; ++s) mx = fmaxf(mx, __ldcg(a.part_lse + pb + s));
-            float w[FASTAR_MAX_R];
-            float W = 0.f;
+            for (int s = 0; s < a.r; ++s) mx = fmaxf(mx, s == own ? lse : __ldcg(a.part_lse + pb + s));
             for (int s = 0; s < a.r; ++s) {
-              const float ls = __ldcg(a.part_lse + pb + s);
-              w[s] = (mx == neg_inf() || ls == neg_inf()) ? 0.f : __expf(ls - mx);
-              W += w[s];
+              const float ls = s == own ? lse : __ldcg(a.part_lse + pb + s);
+              W += (mx == neg_inf() || ls == neg_inf()) ? 0.f : __expf(ls - mx);
             }
-            const float invW = W > 0.f ? 1.0f / W : 0.f;
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs + qi * a.o_ts;
+          }
+          const float invW = W > 0.f ? 1.0f / W : 0.f;
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs + qi * a.o_ts;
 #pragma unroll 1
-            for (int c = 0; c < D / 8; ++c) {
-              float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-              for (int s = 0; s < a.r; ++s) {
-                if (w[s] == 0.f) continue;
-                const float4* src = reinterpret_cast<const float4*>(a.part_o + (pb + s) * D + c * 8);
-                const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
-                acc[0] = fmaf(w[s], u0.x, acc[0]);
-                acc[1] = fmaf(w[s], u0.y, acc[1]);
-                acc[2] = fmaf(w[s], u0.z, acc[2]);
-                acc[3] = fmaf(w[s], u0.w, acc[3]);
-                acc[4] = fmaf(w[s], u1.x, acc[4]);
-                acc[5] = fmaf(w[s], u1.y, acc[5]);
-                acc[6] = fmaf(w[s], u1.z, acc[6]);
-                acc[7] = fmaf(w[s], u1.w, acc[7]);
-              }
-              reinterpret_cast<uint4*>(orow)[c] =
-                  make_uint4(pack_bf16(acc[0] * invW, acc[1] * invW), pack_bf16(acc[2] * invW, acc[3] * invW),
-                             pack_bf16(acc[4] * invW, acc[5] * invW), pack_bf16(acc[6] * invW, acc[7] * invW));
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (T > 0) {
+              tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
+              tc::tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0.f;
             }
+            if (last) {
+              // slots in index order whoever merges, so the result does not depend on
+              // which slot finished last
+              float acc[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+              for (int s = 0; s < a.r; ++s) {
+                const float ls = s == own ? lse : __ldcg(a.part_lse + pb + s);
+                if (mx == neg_inf() || ls == neg_inf()) continue;
+                const float w = __expf(ls - mx);
+                if (s == own) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) acc[i] = fmaf(w, o[i] * inv, acc[i]);
+                  continue;
+                }
+                const float4* src = reinterpret_cast<const float4*>(a.part_o + (pb + s) * D + c * 32);
+#pragma unroll
+                for (int h4 = 0; h4 < 2; ++h4) {
+                  float4 y[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) y[i] = __ldcg(src + h4 * 4 + i);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const int e = (h4 * 4 + i) * 4;
+                    acc[e] = fmaf(w, y[i].x, acc[e]);
+                    acc[e + 1] = fmaf(w, y[i].y, acc[e + 1]);
+                    acc[e + 2] = fmaf(w, y[i].z, acc[e + 2]);
+                    acc[e + 3] = fmaf(w, y[i].w, acc[e + 3]);
+                  }
+                }
+              }
+              uint4* po = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                po[i] = make_uint4(pack_bf16(acc[8 * i] * invW, acc[8 * i + 1] * invW),
+                                   pack_bf16(acc[8 * i + 2] * invW, acc[8 * i + 3] * invW),
+                                   pack_bf16(acc[8 * i + 4] * invW, acc[8 * i + 5] * invW),
+                                   pack_bf16(acc[8 * i + 6] * invW, acc[8 * i + 7] * invW));
+            }
+          }
+          if (last) {
             if (a.lse) a.lse[(int64_t)h * a.nq + qi] = W > 0.f ? mx + __logf(W) : neg_inf();
             a.cnt[(int64_t)h * a.nq + qi] = 0;   // ready for the next call
           }
         }
-      } else if (a.lse) {
-        const int64_t nrow = a.mode == kCross ? (int64_t)a.F * a.tpf : a.nq;
-        a.lse[(int64_t)h * nrow + dst] = lse;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          if (T > 0) {
+            tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
+            tc::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
+          if (dst >= 0) {
+            uint4* po = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs +
+                                                 (int64_t)dst * a.o_ts + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              po[i] = make_uint4(pack_bf16(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                 pack_bf16(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                 pack_bf16(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                 pack_bf16(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+          }
+        }
+        if (dst >= 0 && a.lse) {
+          const int64_t nrow = a.mode == kCross ? (int64_t)a.F * a.tpf : a.nq;
+          a.lse[(int64_t)h * nrow + dst] = lse;
+        }
       }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.o_empty[qs]);
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarpA) {
+    __syncwarp();
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, Lay::tmem_cols);
+    tc::tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && sm.abort) flag_status(a.status, FASTAR_DEV_TIMEOUT);
 }
 
-template <int D, int KV>
-bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
-  dim3 grid;
-  if (a.mode == kDense) {
-    grid = dim3((unsigned)((a.nq + kAT - 1) / kAT), a.H, 1);
-  } else if (a.mode == kCross) {
-    grid = dim3((unsigned)((a.tpf + kAT - 1) / kAT), a.H, a.F);
-  } else {
-    grid = dim3((unsigned)((a.nq * a.r + kAT - 1) / kAT + a.B), a.H, 1);
+// Lists AnnSA's work items — (head, bucket, 128-pair tile) in head-major, bucket order,
+// so that the tiles of one bucket run side by side and share its keys in L2 — and
+// clears the per-query slot counters.  One CTA.
+__global__ void __launch_bounds__(kPlanThreads) sparse_plan_kernel(const AttnArgs a) {
+  __shared__ int wsum[kPlanThreads / 32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int64_t i = t; i < (int64_t)a.H * a.nq; i += kPlanThreads) a.cnt[i] = 0;
+  const int64_t np = a.nq * a.r;
+  const int n = a.H * a.B;
+  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int k0 = t * per, k1 = k0 + per < n ? k0 + per : n;
+  // tiles of entry k = (h, b); malformed offsets give no tiles (and a status bit)
+  auto tiles = [&](int k, int& q0, int& q1, int& kb, int& nk) -> int {
+    const int h = k / a.B, b = k % a.B;
+    const int32_t* qo = a.qoff + (int64_t)h * (a.B + 1);
+    const int32_t* ko = a.koff + (int64_t)h * (a.B + 1);
+    q0 = qo[b];
+    q1 = qo[b + 1];
+    kb = ko[b];
+    nk = ko[b + 1] - kb;
+    if (q0 < 0 || q1 < q0 || q1 > np) {
+      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      return 0;
+    }
+    if (kb < 0 || nk < 0 || (int64_t)kb + nk > a.M) {
+      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      nk = 0;
+    }
+    return (q1 - q0 + kAT - 1) / kAT;
+  };
+  int mine = 0;
+  for (int k = k0; k < k1; ++k) {
+    int q0, q1, kb, nk;
+    mine += tiles(k, q0, q1, kb, nk);
   }
-  constexpr size_t smem = AttnLayout<D, KV>::bytes;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = wsum[lane];
+    int s = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wsum[lane] = s - x;   // exclusive prefix of the warp totals
+    if (lane == 31) *a.n_items = s;
+  }
+  __syncthreads();
+  int at = wsum[warp] + incl - mine;
+  SparseItem* items = static_cast<SparseItem*>(a.items);
+  for (int k = k0; k < k1; ++k) {
+    int q0, q1, kb, nk;
+    const int nt = tiles(k, q0, q1, kb, nk);
+    for (int i = 0; i < nt; ++i, ++at) {
+      const int s = q0 + i * kAT;
+      items[at] = SparseItem{k / a.B, s, s + kAT < q1 ? s + kAT : q1, kb, nk, 0, 0, 0};
+    }
+  }
+}
+
+template <int D>
+bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
+  constexpr size_t smem = AttnLayout<D>::bytes;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return false;
-  attn_tc_kernel<D, KV><<<grid, kThreadsA, smem, s>>>(a);
+  int64_t upper;
+  if (a.mode == kSparse) {
+    if (!a.items || !a.n_items || !a.cnt) return false;
+    sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+    count_launches(1);
+    upper = (int64_t)a.H * ((a.nq * a.r + kAT - 1) / kAT + a.B);
+  } else if (a.mode == kCross) {
+    upper = (int64_t)a.H * a.F * ((a.tpf + kAT - 1) / kAT);
+  } else {
+    upper = (int64_t)a.H * ((a.nq + kAT - 1) / kAT);
+  }
+  if (upper <= 0) return true;
+  const int sms = sm_count();
+  const int grid = (int)(upper < sms ? upper : sms);
+  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(a);
   count_launches(1);
   return true;
 }
 
 }  // namespace
 
+size_t sparse_plan_bytes(int H, int64_t nq, int r, int B) {
+  const int64_t upper = (int64_t)H * ((nq * r + kAT - 1) / kAT + B);
+  return sizeof(SparseItem) * (size_t)upper + 16;
+}
+
 bool launch_attn_tc(int d, const AttnArgs& a, cudaStream_t s) {
-  // long key lists stream through a 2-deep ring; the short per-bucket / per-frame lists
-  // use the compact variant so that two CTAs share an SM
-  const bool streaming = a.mode == kDense;
-  if (d == 128) return streaming ? attn_tc_impl<128, 2>(a, s) : attn_tc_impl<128, 1>(a, s);
-  return streaming ? attn_tc_impl<64, 2>(a, s) : attn_tc_impl<64, 1>(a, s);
+  if (d == 128) return attn_tc_impl<128>(a, s);
+  return attn_tc_impl<64>(a, s);
 }
 
 }  // namespace fastar

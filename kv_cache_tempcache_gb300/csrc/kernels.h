@@ -84,10 +84,14 @@ struct AttnArgs {
   float* part_o;    // sparse partials [H, nq*r, d]
   float* part_lse;  // [H, nq*r]
   int32_t* cnt;     // sparse: per-query count of finished slots [H, nq] (tensor-core path)
+  void* items;      // sparse: work list written by the planning kernel (tensor-core path)
+  int32_t* n_items; // sparse: its length
   int32_t* status;
 };
 
-size_t sparse_attn_workspace(int H, int64_t nq, int d, int r);
+size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B);
+// Bytes of the tensor-core AnnSA work list (inside the sparse workspace).
+size_t sparse_plan_bytes(int H, int64_t nq, int r, int B);
 // Tensor-core attention (bf16); false if it could not be set up (caller falls back).
 bool launch_attn_tc(int d, const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s);

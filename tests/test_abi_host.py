@@ -113,3 +113,8 @@ def test_product_path_has_no_cpu_fallback():
     from kv_cache_tempcache_gb300 import _lib
     with pytest.raises(FileNotFoundError):
         _lib.open_library("/nonexistent/libfastar.so")
+
+
+def test_last_cuda_error_starts_clean(lib):
+    # nothing has failed in this process: the CUDA-error diagnostic reports no error
+    assert lib.fastar_last_cuda_error().decode() == "no error"
