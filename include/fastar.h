@@ -37,6 +37,8 @@
  *     offending element is skipped.  No kernel traps, asserts or waits on
  *     another block.
  *   - Ties of every arg-max / top-k decision go to the lowest index.
+ *   - The softmax scale of every attention call must be positive and finite
+ *     (FASTAR_EINVAL otherwise).
  */
 #ifndef FASTAR_H_
 #define FASTAR_H_

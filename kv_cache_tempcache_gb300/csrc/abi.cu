@@ -164,6 +164,7 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   if (!qperm || !qoff || !kperm || !koff || !k || !v || !aligned16(k) || !aligned16(v)) return FASTAR_EINVAL;
   const size_t need = fastar::sparse_attn_workspace(H, nq, d, r, B);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return FASTAR_EINVAL;
   fastar::AttnArgs a{};
   a.mode = fastar::kSparse;
   a.H = H;
@@ -185,9 +186,9 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   a.lse = lse;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = a.part_o + (size_t)H * nq * r * d;
-  a.cnt = reinterpret_cast<int32_t*>(a.part_lse + (size_t)H * nq * r);
+  a.inv = reinterpret_cast<int32_t*>(a.part_lse + (size_t)H * nq * r);
   {
-    const uintptr_t at = reinterpret_cast<uintptr_t>(a.cnt + (size_t)H * nq);
+    const uintptr_t at = reinterpret_cast<uintptr_t>(a.inv + (size_t)H * nq * r);
     uint8_t* plan = reinterpret_cast<uint8_t*>((at + 15) & ~static_cast<uintptr_t>(15));
     a.items = plan;
     a.n_items = reinterpret_cast<int32_t*>(plan + fastar::sparse_plan_bytes(H, nq, r, B) - 16);
@@ -235,6 +236,7 @@ int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf
   if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, (int64_t)F * tpf, H))) return rc;
   if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, (int64_t)F * tpf, H))) return rc;
   if (!kcnt || (P > 0 && (!kp || !vp || !kidx || !aligned16(kp) || !aligned16(vp)))) return FASTAR_EINVAL;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return FASTAR_EINVAL;
   fastar::AttnArgs a{};
   a.mode = fastar::kCross;
   a.H = H;
@@ -267,6 +269,7 @@ int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_
   if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, nq, H))) return rc;
   if ((rc = check_tok(k, dtype, d, kv_head_stride, kv_token_stride, nk, H))) return rc;
   if ((rc = check_tok(v, dtype, d, kv_head_stride, kv_token_stride, nk, H))) return rc;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return FASTAR_EINVAL;
   fastar::AttnArgs a{};
   a.mode = fastar::kDense;
   a.H = H;

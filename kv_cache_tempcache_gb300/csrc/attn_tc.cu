@@ -4,7 +4,7 @@
 //   sparse — AnnSA (FAST-AR technical summary §2.C, blog §3): the (query, slot) pairs
 //            of one bucket against that bucket's cache keys; the r slots of a query
 //            use disjoint key sets (every key has one bucket), so their partial
-//            (o, lse) merge exactly — the last slot to finish merges them in place;
+//            (o, lse) merge exactly;
 //   cross  — AnnCA (technical summary §2.B, blog §2): one latent frame's queries
 //            against its kept prompt tokens;
 //   dense  — the dense baseline (technical summary, Key Results): every key.
@@ -24,8 +24,10 @@
 //               consumed K tile when d = 128);
 //   warps 9-12  epilogue: O / l from TMEM to the output (or, for AnnSA, the slot
 //               partial and the merge) while the next item is being computed.
-// AnnSA's items (head, bucket, 128-pair tile) are listed by a one-CTA planning kernel
-// that also clears the per-query slot counters.
+// AnnSA's items (head, bucket, 128-pair tile) are listed by a one-CTA planning kernel;
+// each item writes its slot partials (o, lse) by sorted position — contiguous rows,
+// staged through shared memory for coalesced stores — and a merge kernel combines the
+// r slots of every query afterwards.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
@@ -51,8 +53,8 @@ struct SparseItem {
 };
 
 struct ItemInfo {
-  int h, T, f, pad;
-  int64_t nkeys, kbase;
+  int h, T, f, nrows;
+  int64_t nkeys, kbase, q0;
 };
 
 struct AttnCtl {
@@ -82,7 +84,9 @@ struct AttnLayout {
   static constexpr size_t v = k + 2 * stage;
   static constexpr size_t p = kPAliasK ? k : v + 2 * stage;
   static constexpr size_t pstride = kPAliasK ? stage : 2 * (size_t)kBlkA;
-  static constexpr size_t ctl = kPAliasK ? v + 2 * stage : p + 2 * pstride;
+  // 128 rows x 32 fp32: the epilogue's transpose buffer for coalesced partial stores
+  static constexpr size_t ostage = kPAliasK ? v + 2 * stage : p + 2 * pstride;
+  static constexpr size_t ctl = ostage + 128 * 32 * sizeof(float);
   static constexpr size_t bytes = ctl + sizeof(AttnCtl) + 1024;
   static constexpr uint32_t s_col = 0;      // S buffers: columns [0, 256)
   static constexpr uint32_t o_col = 256;    // O accumulators: [256 + 128 * stage, ...)
@@ -105,6 +109,90 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Three-input maximum (PTX max.f32 with three sources).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Maximum of 32 scores; with kFull = false the columns from `valid` on count as -inf.
+template <bool kFull>
+__device__ __forceinline__ float max32(const float* v, int valid) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const float a = kFull || 3 * i < valid ? v[3 * i] : neg_inf();
+    const float b = kFull || 3 * i + 1 < valid ? v[3 * i + 1] : neg_inf();
+    const float c = kFull || 3 * i + 2 < valid ? v[3 * i + 2] : neg_inf();
+    t[i] = max3(a, b, c);
+  }
+  t[10] = fmaxf(kFull || 30 < valid ? v[30] : neg_inf(), kFull || 31 < valid ? v[31] : neg_inf());
+  return max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(max3(t[6], t[7], t[8]), t[9], t[10]));
+}
+
+// Softmax pass 1 over one 128-column S row in TMEM: the raw row maximum (scores not yet
+// scaled), 64 columns per TMEM round trip.
+template <bool kFull>
+__device__ __forceinline__ float row_max(uint32_t s_addr, int vcols) {
+  float m = neg_inf();
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    float x[64];
+    tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
+    tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
+    tc::tmem_wait_ld();
+    tc::tmem_pin32(x);
+    tc::tmem_pin32(x + 32);
+    m = max3(m, max32<kFull>(x, vcols - hh * 64), max32<kFull>(x + 32, vcols - hh * 64 - 32));
+  }
+  return m;
+}
+
+// Softmax pass 2: P = 2^(s * sl2 - m) as bf16 into this thread's row of the P tile
+// (128-byte swizzled, two 64-column blocks); returns the row sum of P.
+template <bool kFull>
+__device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, uint8_t* pst, int row) {
+  const float nm = m == neg_inf() ? 0.f : -m;
+  float xa[32], xb[32];
+  float s0 = 0.f, s1 = 0.f;
+  tc::tmem_ld32(s_addr, xa);
+  tc::tmem_wait_ld();
+  tc::tmem_pin32(xa);
+#pragma unroll
+  for (int c = 0; c < kAT / 32; ++c) {
+    float* cur = (c & 1) ? xb : xa;
+    float* nxt = (c & 1) ? xa : xb;
+    if (c + 1 < kAT / 32) tc::tmem_ld32(s_addr + (uint32_t)((c + 1) * 32), nxt);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a0 = fmaf(cur[i], sl2, nm), a1 = fmaf(cur[i + 1], sl2, nm);
+      if (!kFull) {
+        a0 = c * 32 + i < vcols ? a0 : neg_inf();
+        a1 = c * 32 + i + 1 < vcols ? a1 : neg_inf();
+      }
+      const float p0 = ex2(a0), p1 = ex2(a1);
+      s0 += p0;
+      s1 += p1;
+      pk[i >> 1] = pack_bf16(p0, p1);
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int c16 = c * 4 + q4;   // 16-byte chunk of the 256-byte P row
+      const uint32_t addr = tc::smem_u32(pst + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]),
+                   "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
+                   : "memory");
+    }
+    if (c + 1 < kAT / 32) {
+      tc::tmem_wait_ld();
+      tc::tmem_pin32(nxt);
+    }
+  }
+  return s0 + s1;
+}
+
 __device__ __forceinline__ int64_t items_of(const AttnArgs& a) {
   if (a.mode == kCross) return (int64_t)a.H * a.F * ((a.tpf + kAT - 1) / kAT);
   if (a.mode == kDense) return (int64_t)a.H * ((a.nq + kAT - 1) / kAT);
@@ -125,6 +213,10 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
     q1 = x.z;
     it.kbase = x.w;
     it.nkeys = y.x;
+    it.q0 = q0;
+    it.nrows = (int)(q1 - q0);
+    it.T = (int)((it.nkeys + kAT - 1) / kAT);
+    return;
   } else if (a.mode == kCross) {
     const int64_t nqt = (a.tpf + kAT - 1) / kAT;
     const int64_t per = (int64_t)a.F * nqt;
@@ -147,6 +239,8 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
     q1 = q0 + kAT < a.nq ? q0 + kAT : a.nq;
     it.nkeys = a.nk;
   }
+  it.q0 = q0;
+  it.nrows = (int)(q1 - q0);
   it.T = (int)((it.nkeys + kAT - 1) / kAT);
 }
 
@@ -213,6 +307,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
   uint8_t* sk = base + Lay::k;   // [2][KH][kBlkA]
   uint8_t* sv = base + Lay::v;   // [2][KH][kBlkA]
   uint8_t* sp = base + Lay::p;   // [2] x pstride
+  float* so = reinterpret_cast<float*>(base + Lay::ostage);   // [128][32], 16-byte chunks swizzled
   AttnCtl& sm = *reinterpret_cast<AttnCtl*>(base + Lay::ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q.p);
@@ -282,6 +377,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
             if (e >= 0 && e < np) {
               src = it.h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
               dst = e;
+              if (got) a.inv[(int64_t)it.h * np + e] = (int32_t)pos;
             } else {
               flag_status(a.status, FASTAR_DEV_BAD_INDEX);
             }
@@ -427,17 +523,11 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         const int64_t left = nkeys - (int64_t)j * kAT;
         const int vcols = left < kAT ? (int)left : kAT;
         const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * 128);
-        // pass 1: the row maximum of this tile, 64 columns at a time
-        float mt = neg_inf();
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[64];
-          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
-          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 64; ++i) mt = fmaxf(mt, hh * 64 + i < vcols ? x[i] * sl2 : neg_inf());
-        }
+        // pass 1: the row maximum (the scale is positive, so the maximum of the scaled
+        // scores is the scaled maximum, exactly)
+        const bool full = vcols == kAT;
+        const float mr = full ? row_max<true>(s_addr, vcols) : row_max<false>(s_addr, vcols);
+        const float mt = mr * sl2;
         float alpha = 1.f;
         bool resc = false;
         if (mt > m_used + 8.f) {
@@ -466,36 +556,8 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         }
         // pass 2: P = 2^(s - m) as bf16 into the P tile, and its row sum
         uint8_t* pst = sp + (size_t)st * Lay::pstride;
-        float sum = 0.f;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[64];
-          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
-          tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = hh * 64 + q2 * 32 + i;
-              const float s0 = col < vcols ? x[q2 * 32 + i] * sl2 : neg_inf();
-              const float s1 = col + 1 < vcols ? x[q2 * 32 + i + 1] * sl2 : neg_inf();
-              const float p0 = m_used == neg_inf() ? 0.f : ex2(s0 - m_used);
-              const float p1 = m_used == neg_inf() ? 0.f : ex2(s1 - m_used);
-              sum += p0 + p1;
-              pk[i >> 1] = pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int c16 = hh * 8 + q2 * 4 + q4;   // 16-byte chunk of the 256-byte P row
-              const uint32_t addr = tc::smem_u32(pst + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]),
-                           "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
-                           : "memory");
-            }
-          }
-        }
+        const float sum = full ? row_exp<true>(s_addr, vcols, sl2, m_used, pst, row)
+                               : row_exp<false>(s_addr, vcols, sl2, m_used, pst, row);
         l = l * alpha + sum;
         tc::fence_proxy_async();
         tc::tc_fence_before();
@@ -520,9 +582,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
     for (int u = blockIdx.x; u < n_items; u += gridDim.x, ++n) {
       const int qs = n & 1;
       const uint32_t qph = (n >> 1) & 1;
-      if (!wait_all(&sm.q_full[qs], qph, abort) || !wait_all(&sm.ml_full[qs], qph, abort) ||
-          !wait_all(&sm.o_full[qs], qph, abort))
-        break;
+      const bool got = wait_all(&sm.q_full[qs], qph, abort) && wait_all(&sm.ml_full[qs], qph, abort) &&
+                       wait_all(&sm.o_full[qs], qph, abort);
+      // the four epilogue warps leave together (they share named barriers below)
+      if (!tc::named_bar_and(3, 128, got)) break;
       tc::tc_fence_after();
       const int h = sm.info[qs].h;
       const int T = sm.info[qs].T;
@@ -535,104 +598,39 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       const float inv = live ? 1.0f / l : 0.f;
       const float lse = live ? (m_used + __log2f(l)) * 0.6931471805599453f : neg_inf();
       if (a.mode == kSparse) {
-        const bool has = dst >= 0;
-        const int64_t pb_row = (int64_t)h * np + (has ? dst : 0);
+        // slot partials by sorted position: the item's rows q0.. are contiguous, so each
+        // 32-column slice goes through the transpose buffer and leaves as 128-byte rows
+        const int nrows = sm.info[qs].nrows;
+        const int64_t prow0 = (int64_t)h * np + sm.info[qs].q0;
+        const int ew = warp - kEpiWarp0;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           if (T > 0) {
             tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
             tc::tmem_wait_ld();
+            tc::tmem_pin32(o);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0.f;
           }
-          if (has) {
-            float4* po = reinterpret_cast<float4*>(a.part_o + pb_row * D + c * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              po[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          for (int k = 0; k < 8; ++k) {
+            const float4 v4 = make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
+            *reinterpret_cast<float4*>(so + row * 32 + ((k ^ (row & 7)) << 2)) = v4;
           }
-        }
-        int old = -1;
-        const int64_t qi = has ? dst / a.r : 0;
-        if (has) {
-          a.part_lse[pb_row] = lse;
-          // the last of the query's r slots to finish merges them (no waiting: the
-          // earlier slots only publish their partials)
-          __threadfence();
-          old = atomicAdd(&a.cnt[(int64_t)h * a.nq + qi], 1);
-        }
-        const bool last = has && old == a.r - 1;
-        if (__any_sync(0xffffffffu, last)) {
-          const int own = has ? dst % a.r : 0;
-          const int64_t pb = (int64_t)h * np + qi * a.r;
-          float mx = neg_inf(), W = 0.f;
-          if (last) {
-            __threadfence();
-            for (int s = 0; s < a.r; ++s) mx = fmaxf(mx, s == own ? lse : __ldcg(a.part_lse + pb + s));
-            for (int s = 0; s < a.r; ++s) {
-              const float ls = s == own ? lse : __ldcg(a.part_lse + pb + s);
-              W += (mx == neg_inf() || ls == neg_inf()) ? 0.f : __expf(ls - mx);
+          tc::named_bar(2, 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = ew * 32 + k * 4 + (lane >> 3), ch = lane & 7;
+            if (rr < nrows) {
+              const float4 v4 = *reinterpret_cast<const float4*>(so + rr * 32 + ((ch ^ (rr & 7)) << 2));
+              *reinterpret_cast<float4*>(a.part_o + (prow0 + rr) * D + c * 32 + ch * 4) = v4;
             }
           }
-          const float invW = W > 0.f ? 1.0f / W : 0.f;
-          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs + qi * a.o_ts;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            if (T > 0) {
-              tc::tmem_ld32(o_addr + (uint32_t)(c * 32), o);
-              tc::tmem_wait_ld();
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = 0.f;
-            }
-            if (last) {
-              // slots in index order whoever merges, so the result does not depend on
-              // which slot finished last
-              float acc[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-              for (int s = 0; s < a.r; ++s) {
-                const float ls = s == own ? lse : __ldcg(a.part_lse + pb + s);
-                if (mx == neg_inf() || ls == neg_inf()) continue;
-                const float w = __expf(ls - mx);
-                if (s == own) {
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) acc[i] = fmaf(w, o[i] * inv, acc[i]);
-                  continue;
-                }
-                const float4* src = reinterpret_cast<const float4*>(a.part_o + (pb + s) * D + c * 32);
-#pragma unroll
-                for (int h4 = 0; h4 < 2; ++h4) {
-                  float4 y[4];
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) y[i] = __ldcg(src + h4 * 4 + i);
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const int e = (h4 * 4 + i) * 4;
-                    acc[e] = fmaf(w, y[i].x, acc[e]);
-                    acc[e + 1] = fmaf(w, y[i].y, acc[e + 1]);
-                    acc[e + 2] = fmaf(w, y[i].z, acc[e + 2]);
-                    acc[e + 3] = fmaf(w, y[i].w, acc[e + 3]);
-                  }
-                }
-              }
-              uint4* po = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                po[i] = make_uint4(pack_bf16(acc[8 * i] * invW, acc[8 * i + 1] * invW),
-                                   pack_bf16(acc[8 * i + 2] * invW, acc[8 * i + 3] * invW),
-                                   pack_bf16(acc[8 * i + 4] * invW, acc[8 * i + 5] * invW),
-                                   pack_bf16(acc[8 * i + 6] * invW, acc[8 * i + 7] * invW));
-            }
-          }
-          if (last) {
-            if (a.lse) a.lse[(int64_t)h * a.nq + qi] = W > 0.f ? mx + __logf(W) : neg_inf();
-            a.cnt[(int64_t)h * a.nq + qi] = 0;   // ready for the next call
-          }
+          tc::named_bar(2, 128);
         }
+        if (row < nrows) a.part_lse[prow0 + row] = lse;
       } else {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -676,12 +674,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
 }
 
 // Lists AnnSA's work items — (head, bucket, 128-pair tile) in head-major, bucket order,
-// so that the tiles of one bucket run side by side and share its keys in L2 — and
-// clears the per-query slot counters.  One CTA.
+// so that the tiles of one bucket run side by side and share its keys in L2.  One CTA.
 __global__ void __launch_bounds__(kPlanThreads) sparse_plan_kernel(const AttnArgs a) {
   __shared__ int wsum[kPlanThreads / 32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  for (int64_t i = t; i < (int64_t)a.H * a.nq; i += kPlanThreads) a.cnt[i] = 0;
   const int64_t np = a.nq * a.r;
   const int n = a.H * a.B;
   const int per = (n + kPlanThreads - 1) / kPlanThreads;
@@ -742,6 +738,68 @@ __global__ void __launch_bounds__(kPlanThreads) sparse_plan_kernel(const AttnArg
   }
 }
 
+// Merges the r slot partials of every AnnSA query by the exact log-sum-exp rule:
+// o = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s), and
+// lse = max + log(sum_s w_s).  One warp per (head, query); lane l owns columns
+// [l*D/32, (l+1)*D/32), so every slot row is read as one coalesced 4*D-byte line.
+template <int D>
+__global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
+  constexpr int E = D / 32;
+  const int64_t wq = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wq >= (int64_t)a.H * a.nq) return;
+  const int h = (int)(wq / a.nq);
+  const int64_t qi = wq % a.nq;
+  const int64_t np = a.nq * a.r;
+  int pos = -1;
+  float ls = neg_inf();
+  if (lane < a.r) {
+    const int p = a.inv[(int64_t)h * np + qi * a.r + lane];
+    if (p >= 0 && p < np) {
+      pos = p;
+      ls = a.part_lse[(int64_t)h * np + p];
+    } else {
+      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+    }
+  }
+  float mx = ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float w = (mx == neg_inf() || ls == neg_inf()) ? 0.f : __expf(ls - mx);
+  float W = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int sl = 0; sl < a.r; ++sl) {
+    const float ws = __shfl_sync(0xffffffffu, w, sl);
+    const int ps = __shfl_sync(0xffffffffu, pos, sl);
+    if (ws == 0.f || ps < 0) continue;
+    const float* src = a.part_o + ((int64_t)h * np + ps) * D + lane * E;
+    if (E == 4) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
+      acc[0] = fmaf(ws, v.x, acc[0]);
+      acc[1] = fmaf(ws, v.y, acc[1]);
+      acc[2] = fmaf(ws, v.z, acc[2]);
+      acc[3] = fmaf(ws, v.w, acc[3]);
+    } else {
+      const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+      acc[0] = fmaf(ws, v.x, acc[0]);
+      acc[1] = fmaf(ws, v.y, acc[1]);
+    }
+  }
+  const float invW = W > 0.f ? 1.0f / W : 0.f;
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs + qi * a.o_ts + lane * E;
+  if (E == 4) {
+    *reinterpret_cast<uint2*>(orow) =
+        make_uint2(pack_bf16(acc[0] * invW, acc[1] * invW), pack_bf16(acc[2] * invW, acc[3] * invW));
+  } else {
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16(acc[0] * invW, acc[1] * invW);
+  }
+  if (lane == 0 && a.lse) a.lse[(int64_t)h * a.nq + qi] = W > 0.f ? mx + __logf(W) : neg_inf();
+}
+
 template <int D>
 bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   constexpr size_t smem = AttnLayout<D>::bytes;
@@ -750,7 +808,7 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (attr != cudaSuccess) return false;
   int64_t upper;
   if (a.mode == kSparse) {
-    if (!a.items || !a.n_items || !a.cnt) return false;
+    if (!a.items || !a.n_items || !a.inv) return false;
     sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
     count_launches(1);
     upper = (int64_t)a.H * ((a.nq * a.r + kAT - 1) / kAT + a.B);
@@ -764,6 +822,11 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   const int grid = (int)(upper < sms ? upper : sms);
   attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(a);
   count_launches(1);
+  if (a.mode == kSparse) {
+    const int64_t threads = (int64_t)a.H * a.nq * 32;
+    sparse_merge_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
+    count_launches(1);
+  }
   return true;
 }
 
