@@ -39,9 +39,12 @@
 namespace fastar {
 namespace {
 
-constexpr int kAT = 128;          // query rows per item and keys per tile
+constexpr int kAT = 128;          // query rows per item
+constexpr int kKT = 64;           // keys per K/V tile
+constexpr int kKS = 4;            // K/V stages (and S buffers)
 constexpr int kThreadsA = 416;    // 13 warps
 constexpr int kBlkA = 128 * 128;  // one 128-row x 64-element bf16 block (128-B swizzle)
+constexpr int kBlkK = kKT * 128;  // one kKT-row x 64-element bf16 block
 constexpr int kMmaWarpA = 4;
 constexpr int kSoftWarp0 = 5;
 constexpr int kEpiWarp0 = 9;
@@ -59,13 +62,13 @@ struct ItemInfo {
 
 struct AttnCtl {
   int64_t qsrc[2][kAT];   // loader-private: source offset of each query row, per Q stage
-  int64_t ksrc[2][kAT];   // loader-private: source offset of each key row, per K/V stage
+  int64_t ksrc[kKS][kKT]; // loader-private: source offset of each key row, per K/V stage
   int qdst[2][kAT];       // output row of each query row (-1: none), per Q stage
   float mrow[2][kAT], lrow[2][kAT];   // softmax max (log2 units) and sum, per Q stage
   ItemInfo info[2];
   uint64_t q_full[2], q_empty[2], dst_free[2];
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t kv_full[kKS], kv_empty[kKS];
+  uint64_t s_full[kKS], s_free[kKS], p_full[kKS];
   uint64_t pv_done, fin;
   uint64_t ml_full[2], o_full[2], o_empty[2];
   uint32_t tmem_base;
@@ -77,19 +80,23 @@ struct AttnCtl {
 template <int D>
 struct AttnLayout {
   static constexpr int KH = D / 64;
-  static constexpr size_t stage = (size_t)KH * kBlkA;   // one 128-row tile of Q, K or V
-  static constexpr bool kPAliasK = D == 128;           // P (128 x 128 bf16) over the consumed K tile
+  static constexpr size_t qstage = (size_t)KH * kBlkA;   // one 128-row Q tile
+  static constexpr size_t kstage = (size_t)KH * kBlkK;   // one kKT-row K (or V) tile
+  static constexpr size_t pbytes = (size_t)kAT * kKT * 2; // P: 128 x kKT bf16, one swizzled block
+  static constexpr bool kPAliasK = kstage >= pbytes;     // P over the consumed K tile
   static constexpr size_t q = 0;
-  static constexpr size_t k = q + 2 * stage;
-  static constexpr size_t v = k + 2 * stage;
-  static constexpr size_t p = kPAliasK ? k : v + 2 * stage;
-  static constexpr size_t pstride = kPAliasK ? stage : 2 * (size_t)kBlkA;
+  static constexpr size_t k = q + 2 * qstage;
+  static constexpr size_t v = k + kKS * kstage;
+  static constexpr size_t p = kPAliasK ? k : v + kKS * kstage;
+  static constexpr size_t pstride = kPAliasK ? kstage : pbytes;
   // 128 rows x 32 fp32: the epilogue's transpose buffer for coalesced partial stores
-  static constexpr size_t ostage = kPAliasK ? v + 2 * stage : p + 2 * pstride;
+  static constexpr size_t ostage = kPAliasK ? v + kKS * kstage : p + kKS * pstride;
   static constexpr size_t ctl = ostage + 128 * 32 * sizeof(float);
   static constexpr size_t bytes = ctl + sizeof(AttnCtl) + 1024;
-  static constexpr uint32_t s_col = 0;      // S buffers: columns [0, 256)
+  static constexpr uint32_t s_col = 0;      // S buffers: kKS x kKT columns from 0
   static constexpr uint32_t o_col = 256;    // O accumulators: [256 + 128 * stage, ...)
+  static_assert(kKS * kKT <= 256, "S buffers overlap the O accumulators");
+  static_assert(pbytes == kBlkA * (kKT / 64), "P is one 128-row block per 64 keys");
 };
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -131,13 +138,13 @@ __device__ __forceinline__ float max32(const float* v, int valid) {
   return max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(max3(t[6], t[7], t[8]), t[9], t[10]));
 }
 
-// Softmax pass 1 over one 128-column S row in TMEM: the raw row maximum (scores not yet
+// Softmax pass 1 over one kKT-column S row in TMEM: the raw row maximum (scores not yet
 // scaled), 64 columns per TMEM round trip.
 template <bool kFull>
 __device__ __forceinline__ float row_max(uint32_t s_addr, int vcols) {
   float m = neg_inf();
 #pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
+  for (int hh = 0; hh < kKT / 64; ++hh) {
     float x[64];
     tc::tmem_ld32(s_addr + (uint32_t)(hh * 64), x);
     tc::tmem_ld32(s_addr + (uint32_t)(hh * 64 + 32), x + 32);
@@ -150,7 +157,7 @@ __device__ __forceinline__ float row_max(uint32_t s_addr, int vcols) {
 }
 
 // Softmax pass 2: P = 2^(s * sl2 - m) as bf16 into this thread's row of the P tile
-// (128-byte swizzled, two 64-column blocks); returns the row sum of P.
+// (128-byte swizzled, one block per 64 columns); returns the row sum of P.
 template <bool kFull>
 __device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, uint8_t* pst, int row) {
   const float nm = m == neg_inf() ? 0.f : -m;
@@ -160,10 +167,10 @@ __device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, 
   tc::tmem_wait_ld();
   tc::tmem_pin32(xa);
 #pragma unroll
-  for (int c = 0; c < kAT / 32; ++c) {
+  for (int c = 0; c < kKT / 32; ++c) {
     float* cur = (c & 1) ? xb : xa;
     float* nxt = (c & 1) ? xa : xb;
-    if (c + 1 < kAT / 32) tc::tmem_ld32(s_addr + (uint32_t)((c + 1) * 32), nxt);
+    if (c + 1 < kKT / 32) tc::tmem_ld32(s_addr + (uint32_t)((c + 1) * 32), nxt);
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -179,13 +186,13 @@ __device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, 
     }
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-      const int c16 = c * 4 + q4;   // 16-byte chunk of the 256-byte P row
+      const int c16 = c * 4 + q4;   // 16-byte chunk of the P row
       const uint32_t addr = tc::smem_u32(pst + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]),
                    "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
                    : "memory");
     }
-    if (c + 1 < kAT / 32) {
+    if (c + 1 < kKT / 32) {
       tc::tmem_wait_ld();
       tc::tmem_pin32(nxt);
     }
@@ -215,7 +222,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
     it.nkeys = y.x;
     it.q0 = q0;
     it.nrows = (int)(q1 - q0);
-    it.T = (int)((it.nkeys + kAT - 1) / kAT);
+    it.T = (int)((it.nkeys + kKT - 1) / kKT);
     return;
   } else if (a.mode == kCross) {
     const int64_t nqt = (a.tpf + kAT - 1) / kAT;
@@ -241,7 +248,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
   }
   it.q0 = q0;
   it.nrows = (int)(q1 - q0);
-  it.T = (int)((it.nkeys + kAT - 1) / kAT);
+  it.T = (int)((it.nkeys + kKT - 1) / kKT);
 }
 
 // Element offset of key u of the item's key list (-1 if out of range).
@@ -262,32 +269,41 @@ __device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const ItemInfo&
   return it.h * a.kv_hs + u * a.kv_ts;
 }
 
-// Copy groups a loader thread has committed but not yet signalled (at most two are
+// Copy groups a loader thread has committed but not yet signalled (at most four are
 // kept in flight; before any blocking wait all of them are signalled, so a consumer
 // is never left waiting on a copy whose producer is itself waiting).
 struct Pending {
   uint64_t* b0 = nullptr;
   uint64_t* b1 = nullptr;
+  uint64_t* b2 = nullptr;
+  uint64_t* b3 = nullptr;
+  int n = 0;
   __device__ __forceinline__ void flush() {
-    if (!b0) return;
+    if (n == 0) return;
     tc::cp_async_wait<0>();
     tc::fence_proxy_async();
     tc::mbar_arrive(b0);
-    if (b1) tc::mbar_arrive(b1);
-    b0 = b1 = nullptr;
+    if (n > 1) tc::mbar_arrive(b1);
+    if (n > 2) tc::mbar_arrive(b2);
+    if (n > 3) tc::mbar_arrive(b3);
+    n = 0;
   }
   __device__ __forceinline__ void push(uint64_t* b) {
-    if (b1) {
-      tc::cp_async_wait<2>();   // the oldest of the three groups has landed
+    if (n == 4) {
+      tc::cp_async_wait<4>();   // the oldest of the five groups has landed
       tc::fence_proxy_async();
       tc::mbar_arrive(b0);
       b0 = b1;
-      b1 = b;
-    } else if (b0) {
-      b1 = b;
-    } else {
-      b0 = b;
+      b1 = b2;
+      b2 = b3;
+      b3 = b;
+      return;
     }
+    if (n == 0) b0 = b;
+    else if (n == 1) b1 = b;
+    else if (n == 2) b2 = b;
+    else b3 = b;
+    ++n;
   }
   __device__ __forceinline__ bool acquire(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (tc::mbar_test(bar, parity)) return true;
@@ -304,8 +320,8 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sq = base + Lay::q;   // [2][KH][kBlkA]
-  uint8_t* sk = base + Lay::k;   // [2][KH][kBlkA]
-  uint8_t* sv = base + Lay::v;   // [2][KH][kBlkA]
+  uint8_t* sk = base + Lay::k;   // [kKS][KH][kBlkK]
+  uint8_t* sv = base + Lay::v;   // [kKS][KH][kBlkK]
   uint8_t* sp = base + Lay::p;   // [2] x pstride
   float* so = reinterpret_cast<float*>(base + Lay::ostage);   // [128][32], 16-byte chunks swizzled
   AttnCtl& sm = *reinterpret_cast<AttnCtl*>(base + Lay::ctl);
@@ -320,14 +336,16 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       tc::mbar_init(&sm.q_full[s], 128);
       tc::mbar_init(&sm.q_empty[s], 1);
       tc::mbar_init(&sm.dst_free[s], 4);
+      tc::mbar_init(&sm.ml_full[s], 4);
+      tc::mbar_init(&sm.o_full[s], 1);
+      tc::mbar_init(&sm.o_empty[s], 4);
+    }
+    for (int s = 0; s < kKS; ++s) {
       tc::mbar_init(&sm.kv_full[s], 128);
       tc::mbar_init(&sm.kv_empty[s], 1);
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.s_free[s], 4);
       tc::mbar_init(&sm.p_full[s], 4);
-      tc::mbar_init(&sm.ml_full[s], 4);
-      tc::mbar_init(&sm.o_full[s], 1);
-      tc::mbar_init(&sm.o_empty[s], 4);
     }
     tc::mbar_init(&sm.pv_done, 1);
     tc::mbar_init(&sm.fin, 1);
@@ -397,7 +415,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         break;
       }
       {
-        uint8_t* qst = sq + (size_t)qs * Lay::stage;
+        uint8_t* qst = sq + (size_t)qs * Lay::qstage;
 #pragma unroll 4
         for (int gi = t; gi < kAT * CPR; gi += 128) {
           const int row = gi / CPR, c = gi % CPR;
@@ -409,21 +427,21 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         pend.push(&sm.q_full[qs]);
       }
       for (int j = 0; j < it.T; ++j, ++g) {
-        const int st = g & 1;
-        const uint32_t ph = (g >> 1) & 1;
+        const int st = g % kKS;
+        const uint32_t ph = (g / kKS) & 1;
         const bool free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
-        if (free) sm.ksrc[st][t] = key_offset(a, it, (int64_t)j * kAT + t, D);
+        if (free && t < kKT) sm.ksrc[st][t] = key_offset(a, it, (int64_t)j * kKT + t, D);
         if (!tc::named_bar_and(1, 128, free)) {
           ok = false;
           break;
         }
-        uint8_t* kst = sk + (size_t)st * Lay::stage;
-        uint8_t* vst = sv + (size_t)st * Lay::stage;
+        uint8_t* kst = sk + (size_t)st * Lay::kstage;
+        uint8_t* vst = sv + (size_t)st * Lay::kstage;
 #pragma unroll 4
-        for (int gi = t; gi < kAT * CPR; gi += 128) {
+        for (int gi = t; gi < kKT * CPR; gi += 128) {
           const int row = gi / CPR, c = gi % CPR;
           const int64_t s = sm.ksrc[st][row];
-          const uint32_t o = (uint32_t)((c >> 3) * kBlkA) + tc::sw128_off(row, c & 7);
+          const uint32_t o = (uint32_t)((c >> 3) * kBlkK) + tc::sw128_off(row, c & 7);
           tc::cp_async16(tc::smem_u32(kst) + o, s >= 0 ? K + s + c * 8 : K, s >= 0 ? 16u : 0u);
           tc::cp_async16(tc::smem_u32(vst) + o, s >= 0 ? V + s + c * 8 : V, s >= 0 ? 16u : 0u);
         }
@@ -435,21 +453,21 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
   } else if (warp == kMmaWarpA) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kAT);
+      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kKT);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_bmn(128, D);
       const uint64_t q_desc = tc::sw128_desc(tc::smem_u32(sq));
       const uint64_t k_desc = tc::sw128_desc(tc::smem_u32(sk));
       const uint64_t p_desc = tc::sw128_desc(tc::smem_u32(sp));
-      const uint64_t v_desc = tc::sw128_mn_desc(tc::smem_u32(sv), kBlkA);
+      const uint64_t v_desc = tc::sw128_mn_desc(tc::smem_u32(sv), kBlkK);
       // O_qs += P_gt V_gt for global tile gt; `first` starts the accumulator
       auto issue_pv = [&](int gt, int qs, bool first) -> bool {
-        const int st = gt & 1;
-        if (!tc::mbar_wait(&sm.p_full[st], (gt >> 1) & 1, abort)) return false;
+        const int st = gt % kKS;
+        if (!tc::mbar_wait(&sm.p_full[st], (gt / kKS) & 1, abort)) return false;
         tc::tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kAT / 16; ++ks) {
+        for (int ks = 0; ks < kKT / 16; ++ks) {
           const uint32_t aoff = (uint32_t)(st * Lay::pstride + (ks >> 2) * kBlkA + (ks & 3) * 32);
-          const uint32_t boff = (uint32_t)(st * Lay::stage + ks * 2048);
+          const uint32_t boff = (uint32_t)(st * Lay::kstage + ks * 2048);
           tc::mma_bf16(tmem + Lay::o_col + (uint32_t)(qs * 128), p_desc + (aoff >> 4), v_desc + (boff >> 4),
                        idesc_pv, (!first || ks > 0) ? 1u : 0u);
         }
@@ -467,8 +485,8 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         if (!tc::mbar_wait(&sm.o_empty[qs], qph ^ 1, abort)) break;
         tc::tc_fence_after();
         for (int j = 0; j < T; ++j, ++g) {
-          const int st = g & 1;
-          const uint32_t ph = (g >> 1) & 1;
+          const int st = g % kKS;
+          const uint32_t ph = (g / kKS) & 1;
           if (!tc::mbar_wait(&sm.kv_full[st], ph, abort) || !tc::mbar_wait(&sm.s_free[st], ph ^ 1, abort)) {
             ok = false;
             break;
@@ -476,9 +494,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
           tc::tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * kBlkA + (k & 3) * 32);
-            tc::mma_bf16(tmem + Lay::s_col + (uint32_t)(st * 128), q_desc + ((uint32_t)(qs * Lay::stage + off) >> 4),
-                         k_desc + ((uint32_t)(st * Lay::stage + off) >> 4), idesc_qk, k > 0 ? 1u : 0u);
+            const uint32_t qoff = (uint32_t)(qs * Lay::qstage + (k >> 2) * kBlkA + (k & 3) * 32);
+            const uint32_t koff = (uint32_t)(st * Lay::kstage + (k >> 2) * kBlkK + (k & 3) * 32);
+            tc::mma_bf16(tmem + Lay::s_col + (uint32_t)(st * kKT), q_desc + (qoff >> 4), k_desc + (koff >> 4),
+                         idesc_qk, k > 0 ? 1u : 0u);
           }
           tc::mma_commit(&sm.s_full[st]);
           // the previous tile's P.V goes after this tile's Q.K^T (overlaps the softmax)
@@ -514,18 +533,18 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       const uint32_t o_addr = tmem + lane_addr + Lay::o_col + (uint32_t)(qs * 128);
       float m_used = neg_inf(), l = 0.f;
       for (int j = 0; j < T; ++j, ++g) {
-        const int st = g & 1;
-        if (!wait_all(&sm.s_full[st], (g >> 1) & 1, abort)) {
+        const int st = g % kKS;
+        if (!wait_all(&sm.s_full[st], (g / kKS) & 1, abort)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const int64_t left = nkeys - (int64_t)j * kAT;
-        const int vcols = left < kAT ? (int)left : kAT;
-        const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * 128);
+        const int64_t left = nkeys - (int64_t)j * kKT;
+        const int vcols = left < kKT ? (int)left : kKT;
+        const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * kKT);
         // pass 1: the row maximum (the scale is positive, so the maximum of the scaled
         // scores is the scaled maximum, exactly)
-        const bool full = vcols == kAT;
+        const bool full = vcols == kKT;
         const float mr = full ? row_max<true>(s_addr, vcols) : row_max<false>(s_addr, vcols);
         const float mt = mr * sl2;
         float alpha = 1.f;
