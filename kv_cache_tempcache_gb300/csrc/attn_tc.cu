@@ -269,6 +269,27 @@ __device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const ItemInfo&
   return it.h * a.kv_hs + u * a.kv_ts;
 }
 
+// Query row `pos` of item `it` (valid below q1): its source offset and output row
+// (sparse: the (query, slot) pair index; otherwise the token row), or -1 for none.
+__device__ __forceinline__ void query_row(const AttnArgs& a, const ItemInfo& it, int64_t pos, int64_t q1,
+                                          int64_t np, int64_t& src, int& dst) {
+  src = -1;
+  dst = -1;
+  if (pos >= q1) return;
+  if (a.mode == kSparse) {
+    const int e = a.qperm[(int64_t)it.h * np + pos];
+    if (e >= 0 && e < np) {
+      src = it.h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
+      dst = e;
+    } else {
+      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+    }
+  } else {
+    src = it.h * a.q.hs + pos * a.q.ts;
+    dst = (int)pos;
+  }
+}
+
 // Copy groups a loader thread has committed but not yet signalled (at most four are
 // kept in flight; before any blocking wait all of them are signalled, so a consumer
 // is never left waiting on a copy whose producer is itself waiting).
@@ -372,43 +393,37 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
     const int t = threadIdx.x;
     // Every exit decision is taken by all 128 threads together (named_bar_and): a
     // thread that left alone would strand the others in the next named barrier.
+    // Index loads run one step ahead of the copies that use them: the next item's query
+    // row and first key tile while this item's tiles are copied, the next key tile's
+    // rows while this one waits for its stage.
     Pending pend;
     int g = 0, n = 0;
     bool ok = true;
+    ItemInfo it;
+    int64_t qsrc = -1, ksrc = -1;
+    int qdst = -1;
+    auto load_item = [&](int64_t v, ItemInfo& x, int64_t& src, int& dst, int64_t& k0) {
+      int64_t p0, p1;
+      decode_item(a, v, x, p0, p1);
+      query_row(a, x, p0 + t, p1, np, src, dst);
+      k0 = t < kKT && x.T > 0 ? key_offset(a, x, t, D) : -1;
+    };
+    if ((int)blockIdx.x < n_items) load_item(blockIdx.x, it, qsrc, qdst, ksrc);
     for (int u = blockIdx.x; u < n_items && ok; u += gridDim.x, ++n) {
       const int qs = n & 1;
       const uint32_t qph = (n >> 1) & 1;
+      ItemInfo nit{};
+      int64_t nqsrc = -1, nksrc = -1;
+      int nqdst = -1;
+      if (u + (int)gridDim.x < n_items) load_item(u + gridDim.x, nit, nqsrc, nqdst, nksrc);
       bool got = true;
       if (n >= 2)
         got = pend.acquire(&sm.q_empty[qs], qph ^ 1, abort) && pend.acquire(&sm.dst_free[qs], qph ^ 1, abort);
-      ItemInfo it;
-      int64_t q0, q1;
-      decode_item(a, u, it, q0, q1);
-      // this thread's query row: source offset and output row
-      {
-        const int64_t pos = q0 + t;
-        int64_t src = -1;
-        int dst = -1;
-        if (pos < q1) {
-          if (a.mode == kSparse) {
-            const int e = a.qperm[(int64_t)it.h * np + pos];
-            if (e >= 0 && e < np) {
-              src = it.h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
-              dst = e;
-              if (got) a.inv[(int64_t)it.h * np + e] = (int32_t)pos;
-            } else {
-              flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-            }
-          } else {
-            src = it.h * a.q.hs + pos * a.q.ts;
-            dst = (int)pos;
-          }
-        }
-        if (got) {
-          sm.qsrc[qs][t] = src;
-          sm.qdst[qs][t] = dst;
-          if (t == 0) sm.info[qs] = it;
-        }
+      if (got) {
+        sm.qsrc[qs][t] = qsrc;
+        sm.qdst[qs][t] = qdst;
+        if (t == 0) sm.info[qs] = it;
+        if (a.mode == kSparse && qdst >= 0) a.inv[(int64_t)it.h * np + qdst] = (int32_t)(it.q0 + t);
       }
       if (!tc::named_bar_and(1, 128, got)) {
         ok = false;
@@ -429,8 +444,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       for (int j = 0; j < it.T; ++j, ++g) {
         const int st = g % kKS;
         const uint32_t ph = (g / kKS) & 1;
+        const int64_t cur = ksrc;
+        ksrc = t < kKT && j + 1 < it.T ? key_offset(a, it, (int64_t)(j + 1) * kKT + t, D) : -1;
         const bool free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
-        if (free && t < kKT) sm.ksrc[st][t] = key_offset(a, it, (int64_t)j * kKT + t, D);
+        if (free && t < kKT) sm.ksrc[st][t] = cur;
         if (!tc::named_bar_and(1, 128, free)) {
           ok = false;
           break;
@@ -448,6 +465,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         tc::cp_async_commit();
         pend.push(&sm.kv_full[st]);
       }
+      it = nit;
+      qsrc = nqsrc;
+      qdst = nqdst;
+      ksrc = nksrc;
     }
     pend.flush();
   } else if (warp == kMmaWarpA) {
@@ -606,8 +627,12 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       // the four epilogue warps leave together (they share named barriers below)
       if (!tc::named_bar_and(3, 128, got)) break;
       tc::tc_fence_after();
+      // everything this item needs from the stage's shared slots is read before dst_free
+      // lets the loader reuse them
       const int h = sm.info[qs].h;
       const int T = sm.info[qs].T;
+      const int nrows = sm.info[qs].nrows;
+      const int64_t q0 = sm.info[qs].q0;
       const int dst = sm.qdst[qs][row];
       const float m_used = sm.mrow[qs][row], l = sm.lrow[qs][row];
       __syncwarp();
@@ -619,8 +644,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       if (a.mode == kSparse) {
         // slot partials by sorted position: the item's rows q0.. are contiguous, so each
         // 32-column slice goes through the transpose buffer and leaves as 128-byte rows
-        const int nrows = sm.info[qs].nrows;
-        const int64_t prow0 = (int64_t)h * np + sm.info[qs].q0;
+        const int64_t prow0 = (int64_t)h * np + q0;
         const int ew = warp - kEpiWarp0;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
