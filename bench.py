@@ -187,6 +187,29 @@ def stage_units(cfg, layer, n_in):
     return u
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_wan13b_layer.json")
+
+
+def recorded_traffic(stage, workload):
+    """DRAM bytes per launch of a stage from the committed ncu record, or None when the
+    record is for another workload or a source file of the stage changed since."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    if not rec.get("workload", "").startswith(workload + " "):
+        return None
+    e = rec.get("stages", {}).get(stage)
+    if not e:
+        return None
+    for f, h in e.get("sources_sha256", {}).items():
+        path = os.path.join(ROOT, "kv_cache_tempcache_gb300", "csrc", f)
+        if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != h:
+            return None
+    return int(e["bytes_per_launch"])
+
+
 def roofline_of(name, avg_ms, units, peaks, sustained=True):
     b, f = units["bytes"], units["flops"]
     tpk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
@@ -291,8 +314,10 @@ def run_fastar(args, rank, world, local):
     peaks = load_peaks()
     units = stage_units(cfg, layer, n_in)
     dom = max((s for s in stages if s in units), key=lambda s: stages[s])
-    roof = roofline_of(dom, stages[dom], units[dom], peaks)
     roof_all = {s: roofline_of(s, stages[s], units[s], peaks) for s in stages if s in units}
+    for s_, r_ in roof_all.items():
+        r_["traffic"] = recorded_traffic(s_, cfg.name)
+    roof = roof_all[dom]
     roof_time = sum(max(units[s]["bytes"] / (peaks["hbm_gbs"] * 1e9),
                         units[s]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) for s in units)
 
