@@ -34,8 +34,9 @@
  *     enqueues nothing.  Data-dependent faults found on the device (a cache
  *     length above M, a bucket id out of range) are OR-ed as FASTAR_DEV_* bits
  *     into the caller's int32 dev_status word (optional where noted) and the
- *     offending element is skipped.  No kernel traps, asserts or waits on
- *     another block.
+ *     offending element is skipped.  No kernel traps or asserts, and none
+ *     waits on a block outside its own thread-block cluster (whose blocks the
+ *     hardware schedules together).
  *   - Ties of every arg-max / top-k decision go to the lowest index.
  *   - The softmax scale of every attention call must be positive and finite
  *     (FASTAR_EINVAL otherwise).

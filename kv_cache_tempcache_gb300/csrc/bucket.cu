@@ -6,6 +6,8 @@
 // buckets).  The centroid-argmax ANN is the method spec's fixed choice.
 #include <climits>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -117,97 +119,125 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 }
 
 // ---------------------------------------------------------------------------------------
-// Stable counting sort, one CTA per head.
-// Each warp owns a contiguous segment of the element range.  Pass 1 builds a
-// per-warp histogram (warp-level match gives each bucket one leader per batch of
-// 32 elements); an exclusive scan over (bucket, warp) then gives every warp its
-// first position in every bucket; pass 2 replays the segment and scatters each
-// element to start + its rank among same-bucket lanes of the batch.  Element order
-// inside a bucket is therefore ascending element id.  No block waits on another.
+// Stable counting sort: one thread-block cluster of kSortCtas CTAs per head.
+// CTA c of the cluster owns the c-th contiguous chunk of the head's element range and,
+// inside it, each warp a contiguous segment.  Pass 1 builds per-warp histograms (a
+// warp-level match gives each bucket one leader per batch of 32 elements).  The CTA's
+// histogram sits in its shared memory; after a cluster barrier every CTA reads all of
+// the cluster's histograms through distributed shared memory, which gives per bucket
+// the total (the bucket offsets) and the count in the chunks before its own.  Pass 2
+// replays the chunk and scatters each element to bucket offset + earlier chunks +
+// earlier warps + its rank among same-bucket lanes of the batch, so the order inside
+// a bucket is ascending element id.  The CTAs of a cluster are co-scheduled by the
+// hardware and every thread executes both cluster barriers unconditionally.
 // ---------------------------------------------------------------------------------------
-constexpr int kSortWarps = 32;
+constexpr int kSortCtas = 8;
+constexpr int kSortWarpsC = 8;
+constexpr int kSortStage = 8192;   // ids of a chunk staged in shared memory when they fit
 
-__global__ void __launch_bounds__(kSortWarps * 32)
-bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B,
-                   const int32_t* __restrict__ n_valid, int32_t* __restrict__ perm,
-                   int32_t* __restrict__ offsets, int32_t* status, int stage) {
-  extern __shared__ int sm_sort[];
-  int* cnt = sm_sort;               // [kSortWarps][B]
-  int* tot = sm_sort + kSortWarps * B;  // [B + 1]
-  const int h = blockIdx.x;
+__global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortWarpsC * 32)
+bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, const int32_t* __restrict__ n_valid,
+                   int32_t* __restrict__ perm, int32_t* __restrict__ offsets, int32_t* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ int cnt[kSortWarpsC][FASTAR_MAX_B];
+  __shared__ int hist[FASTAR_MAX_B];
+  __shared__ int base[FASTAR_MAX_B];
+  __shared__ int wsum[kSortWarpsC];
+  __shared__ int ids_s[kSortStage];
+  const int c = (int)cluster.block_rank();
+  const int h = blockIdx.x / kSortCtas;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   int64_t nv = n;
   if (n_valid) {
     nv = n_valid[h];
     if (nv < 0 || nv > n) {
-      if (threadIdx.x == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
+      if (t == 0 && c == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
       nv = nv < 0 ? 0 : n;
     }
   }
   const int64_t E = nv * r;
+  const int64_t per = (E + kSortCtas - 1) / kSortCtas;
+  const int64_t cb = (int64_t)c * per < E ? (int64_t)c * per : E;
+  const int64_t ce = cb + per < E ? cb + per : E;
   const int32_t* id = ids + (int64_t)h * n * r;
   int32_t* out = perm + (int64_t)h * n * r;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kSortWarps * B; i += blockDim.x) cnt[i] = 0;
-  if (stage) {
-    // both passes read the ids: stage them once, coalesced, in shared memory
-    int* ids_s = tot + ((B + 1 + 3) & ~3);
-    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) ids_s[e] = id[e];
-    id = ids_s;
-  }
+  for (int i = t; i < kSortWarpsC * FASTAR_MAX_B; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  const bool staged = ce - cb <= kSortStage;
+  if (staged)
+    for (int64_t e = cb + t; e < ce; e += blockDim.x) ids_s[e - cb] = id[e];
   __syncthreads();
-  const int64_t seg = (E + kSortWarps - 1) / kSortWarps;
-  const int64_t beg = warp * seg;
-  const int64_t end = beg + seg < E ? beg + seg : E;
-  for (int64_t base = beg; base < end; base += 32) {
-    const int64_t e = base + lane;
-    int b = e < end ? id[e] : -1;
-    if (e < end && (b < 0 || b >= B)) {
+  auto bucket_of = [&](int64_t e) -> int { return staged ? ids_s[e - cb] : id[e]; };
+  const int64_t wseg = (ce - cb + kSortWarpsC - 1) / kSortWarpsC;
+  const int64_t wb = cb + warp * wseg < ce ? cb + warp * wseg : ce;
+  const int64_t we = wb + wseg < ce ? wb + wseg : ce;
+  for (int64_t bse = wb; bse < we; bse += 32) {
+    const int64_t e = bse + lane;
+    int b = e < we ? bucket_of(e) : -1;
+    if (e < we && (b < 0 || b >= B)) {
       flag_status(status, FASTAR_DEV_BAD_BUCKET);
       b = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, b);
-    if (b >= 0 && lane == __ffs(peers) - 1) cnt[warp * B + b] += __popc(peers);
+    if (b >= 0 && lane == __ffs(peers) - 1) cnt[warp][b] += __popc(peers);
     __syncwarp();
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    int s = 0;
-    for (int w = 0; w < kSortWarps; ++w) s += cnt[w * B + b];
-    tot[b] = s;
+  if (t < B) {
+    int sum = 0;
+#pragma unroll
+    for (int w = 0; w < kSortWarpsC; ++w) sum += cnt[w][t];
+    hist[t] = sum;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = 0; b < B; ++b) {
-      const int t = tot[b];
-      tot[b] = acc;
-      acc += t;
-    }
-    tot[B] = acc;
-  }
-  __syncthreads();
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    int acc = tot[b];
-    for (int w = 0; w < kSortWarps; ++w) {
-      const int t = cnt[w * B + b];
-      cnt[w * B + b] = acc;
-      acc += t;
+  cluster.sync();   // every CTA's histogram is complete
+  int total = 0, before = 0;
+  if (t < B) {
+    for (int k = 0; k < kSortCtas; ++k) {
+      const int v = cluster.map_shared_rank(hist, k)[t];
+      total += v;
+      if (k < c) before += v;
     }
   }
-  for (int b = threadIdx.x; b <= B; b += blockDim.x) offsets[(int64_t)h * (B + 1) + b] = tot[b];
+  cluster.sync();   // no CTA leaves (its histogram) while another may still read it
+  // exclusive scan of the bucket totals (B <= blockDim.x)
+  int incl = total;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  for (int64_t base = beg; base < end; base += 32) {
-    const int64_t e = base + lane;
-    int b = e < end ? id[e] : -1;
-    if (b >= B) b = -1;
-    if (b < -1) b = -1;
+  int wpre = 0;
+  for (int w = 0; w < warp; ++w) wpre += wsum[w];
+  const int off = wpre + incl - total;
+  if (t < B) {
+    base[t] = off + before;
+    if (c == 0) offsets[(int64_t)h * (B + 1) + t] = off;
+  }
+  if (c == 0 && t == B - 1) offsets[(int64_t)h * (B + 1) + B] = off + total;
+  __syncthreads();
+  if (t < B) {
+    int acc = base[t];
+#pragma unroll
+    for (int w = 0; w < kSortWarpsC; ++w) {
+      const int x = cnt[w][t];
+      cnt[w][t] = acc;
+      acc += x;
+    }
+  }
+  __syncthreads();
+  for (int64_t bse = wb; bse < we; bse += 32) {
+    const int64_t e = bse + lane;
+    int b = e < we ? bucket_of(e) : -1;
+    if (b >= B || b < -1) b = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, b);
     int start = 0;
-    if (b >= 0) start = cnt[warp * B + b];
+    if (b >= 0) start = cnt[warp][b];
     __syncwarp();
     if (b >= 0) {
       out[start + __popc(peers & ((1u << lane) - 1u))] = (int32_t)e;
-      if (lane == __ffs(peers) - 1) cnt[warp * B + b] = start + __popc(peers);
+      if (lane == __ffs(peers) - 1) cnt[warp][b] = start + __popc(peers);
     }
     __syncwarp();
   }
@@ -216,15 +246,7 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B,
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
                                int32_t* status, cudaStream_t s) {
-  // histograms (<= 33.8 KB) plus, when they fit, the head's ids staged in shared memory
-  const size_t base = sizeof(int) * ((size_t)kSortWarps * B + ((B + 1 + 3) & ~3));
-  const size_t staged = base + sizeof(int) * (size_t)(n * r);
-  constexpr size_t kMaxSmem = 200 * 1024;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-  const int stage = (attr == cudaSuccess && staged <= kMaxSmem) ? 1 : 0;
-  bucket_sort_kernel<<<H, kSortWarps * 32, stage ? staged : base, s>>>(ids, n, r, B, n_valid, perm, offsets,
-                                                                         status, stage);
+  bucket_sort_kernel<<<H * kSortCtas, kSortWarpsC * 32, 0, s>>>(ids, n, r, B, n_valid, perm, offsets, status);
   count_launches(1);
   return cudaGetLastError();
 }
