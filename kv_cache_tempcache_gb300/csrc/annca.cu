@@ -358,6 +358,10 @@ template <typename T, int D>
 static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r,
                               const void* kp, const int32_t* pb, int64_t P, int gate, const BucketOrder bo,
                               float* score, cudaStream_t s) {
+  // bf16: the tensor-core scorer (dense Kp.Q^T with the bucket condition as a mask)
+  if (sizeof(T) == 2 && gate &&
+      launch_annca_tc(D, q, H, F, tpf, qb, r, kp, pb, P, bo.B > 0 ? bo.B : FASTAR_MAX_B, score, nullptr, s))
+    return cudaGetLastError();
   if (gate && F <= kBMaxF && (int64_t)F * tpf <= kBMaxQ && P <= FASTAR_MAX_P) {
     // prompt tokens whose bucket no CTA visits would keep stale scores: the bucket
     // kernel covers every p (each has exactly one bucket, and every bucket has a CTA)

@@ -98,6 +98,9 @@ cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s
 
 // ---- AnnCA --------------------------------------------------------------------------
 size_t annca_workspace(int H, int F, int64_t P);
+// Tensor-core AnnCA scores (bf16, bucket-gated); false if it could not be set up.
+bool launch_annca_tc(int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r, const void* kp,
+                     const int32_t* pb, int64_t P, int B, float* score, int32_t* status, cudaStream_t s);
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf,
                                 const int32_t* qb, int r, const void* kp, const int32_t* pb,
                                 int64_t P, float tau_ca, int topk, int gate, int B,
