@@ -105,6 +105,8 @@ class FastARLayer:
         self.ws_match = ws(L.OP_MATCH, n=Nq, M=M, d=d)
         self.ws_attn = ws(L.OP_SPARSE_ATTN, n=Nq, M=M, d=d, B=B, r=r)
         self.side = torch.cuda.Stream(device=dev)
+        self.mside = torch.cuda.Stream(device=dev)
+        self.match_first = True
         self._graph = None
         self._graph_dir = None
 
@@ -166,6 +168,25 @@ class FastARLayer:
         main = torch.cuda.current_stream(self.dev)
         side = main if serial else self.side
         t = timer or (lambda *a: None)
+
+        def match(stream):
+            t("tempcache_match", stream, "begin")
+            L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
+                                     self.s2 if self.diagnostics else None,
+                                     self.evict, self.dev_status, self.ws_match)
+            t("tempcache_match", stream, "end")
+
+        # the match needs only the step's inputs and the incoming cache: it starts at once
+        # on its own stream, beside the bucket assignment, the pair sort and AnnCA
+        early = self.match_first and not serial
+        if early:
+            ev0 = torch.cuda.Event()
+            ev0.record(main)
+            self.mside.wait_event(ev0)
+            with torch.cuda.stream(self.mside):
+                match(self.mside)
+            evm = torch.cuda.Event()
+            evm.record(self.mside)
         t("bucket_assign", main, "begin")
         L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
         L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
@@ -190,11 +211,10 @@ class FastARLayer:
                                        self.o_cross, self.lse_cross)
             t("cross_attn_subset", side, "end")
         # TempCache + AnnSA on the main stream
-        t("tempcache_match", main, "begin")
-        L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
-                                 self.s2 if self.diagnostics else None,
-                                 self.evict, self.dev_status, self.ws_match)
-        t("tempcache_match", main, "end")
+        if early:
+            main.wait_event(evm)
+        else:
+            match(main)
         t("cache_compact", main, "begin")
         L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
