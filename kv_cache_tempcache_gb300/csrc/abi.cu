@@ -186,9 +186,8 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   a.lse = lse;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = a.part_o + (size_t)H * nq * r * d;
-  a.inv = reinterpret_cast<int32_t*>(a.part_lse + (size_t)H * nq * r);
   {
-    const uintptr_t at = reinterpret_cast<uintptr_t>(a.inv + (size_t)H * nq * r);
+    const uintptr_t at = reinterpret_cast<uintptr_t>(a.part_lse + (size_t)H * nq * r);
     uint8_t* plan = reinterpret_cast<uint8_t*>((at + 15) & ~static_cast<uintptr_t>(15));
     a.items = plan;
     a.n_items = reinterpret_cast<int32_t*>(plan + fastar::sparse_plan_bytes(H, nq, r, B) - 16);

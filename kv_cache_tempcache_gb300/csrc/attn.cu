@@ -297,9 +297,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
 }
 
 size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B) {
-  // fp32 partials (o, lse) per (query, slot), the pair -> sorted position map, then
-  // (16-byte aligned) the tensor-core path's work list and its length
-  const size_t head = sizeof(float) * (size_t)H * nq * r * (d + 1) + sizeof(int32_t) * (size_t)H * nq * r;
+  // fp32 partials (o, lse) per (query, slot), then (16-byte aligned) the tensor-core
+  // path's work list and its length
+  const size_t head = sizeof(float) * (size_t)H * nq * r * (d + 1);
   return ((head + 15) & ~(size_t)15) + sparse_plan_bytes(H, nq, r, B) + 256;
 }
 
@@ -328,7 +328,6 @@ static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
   }
   {
     AttnArgs b = a;
-    b.inv = nullptr;
     kern<<<grid, 256, smem, s>>>(b);
   }
   count_launches(1);

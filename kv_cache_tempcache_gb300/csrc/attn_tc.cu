@@ -25,9 +25,9 @@
 //   warps 9-12  epilogue: O / l from TMEM to the output (or, for AnnSA, the slot
 //               partial and the merge) while the next item is being computed.
 // AnnSA's items (head, bucket, 128-pair tile) are listed by a one-CTA planning kernel;
-// each item writes its slot partials (o, lse) by sorted position — contiguous rows,
-// staged through shared memory for coalesced stores — and a merge kernel combines the
-// r slots of every query afterwards.
+// each item writes its slot partials (o, lse) at the (query, slot) pair rows — staged
+// through shared memory so every store is a 128-byte row segment — and a merge kernel
+// combines the r adjacent slot rows of every query afterwards.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
@@ -65,6 +65,7 @@ struct AttnCtl {
   int64_t ksrc[kKS][kKT]; // loader-private: source offset of each key row, per K/V stage
   int qdst[2][kAT];       // output row of each query row (-1: none), per Q stage
   float mrow[2][kAT], lrow[2][kAT];   // softmax max (log2 units) and sum, per Q stage
+  int edst[kAT];          // epilogue-private: output row of each row of the item being stored
   ItemInfo info[2];
   uint64_t q_full[2], q_empty[2], dst_free[2];
   uint64_t kv_full[kKS], kv_empty[kKS];
@@ -423,7 +424,6 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         sm.qsrc[qs][t] = qsrc;
         sm.qdst[qs][t] = qdst;
         if (t == 0) sm.info[qs] = it;
-        if (a.mode == kSparse && qdst >= 0) a.inv[(int64_t)it.h * np + qdst] = (int32_t)(it.q0 + t);
       }
       if (!tc::named_bar_and(1, 128, got)) {
         ok = false;
@@ -632,7 +632,6 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       const int h = sm.info[qs].h;
       const int T = sm.info[qs].T;
       const int nrows = sm.info[qs].nrows;
-      const int64_t q0 = sm.info[qs].q0;
       const int dst = sm.qdst[qs][row];
       const float m_used = sm.mrow[qs][row], l = sm.lrow[qs][row];
       __syncwarp();
@@ -642,9 +641,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       const float inv = live ? 1.0f / l : 0.f;
       const float lse = live ? (m_used + __log2f(l)) * 0.6931471805599453f : neg_inf();
       if (a.mode == kSparse) {
-        // slot partials by sorted position: the item's rows q0.. are contiguous, so each
-        // 32-column slice goes through the transpose buffer and leaves as 128-byte rows
-        const int64_t prow0 = (int64_t)h * np + q0;
+        // slot partials at their (query, slot) pair rows: each 32-column slice goes through
+        // the transpose buffer and leaves as 128-byte row segments (edst: the row of each)
+        const int64_t prow0 = (int64_t)h * np;
+        sm.edst[row] = dst;
         const int ew = warp - kEpiWarp0;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -666,14 +666,15 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int rr = ew * 32 + k * 4 + (lane >> 3), ch = lane & 7;
-            if (rr < nrows) {
+            const int er = sm.edst[rr];
+            if (rr < nrows && er >= 0) {
               const float4 v4 = *reinterpret_cast<const float4*>(so + rr * 32 + ((ch ^ (rr & 7)) << 2));
-              *reinterpret_cast<float4*>(a.part_o + (prow0 + rr) * D + c * 32 + ch * 4) = v4;
+              *reinterpret_cast<float4*>(a.part_o + (prow0 + er) * D + c * 32 + ch * 4) = v4;
             }
           }
           tc::named_bar(2, 128);
         }
-        if (row < nrows) a.part_lse[prow0 + row] = lse;
+        if (dst >= 0) a.part_lse[prow0 + dst] = lse;
       } else {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -794,17 +795,8 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   const int h = (int)(wq / a.nq);
   const int64_t qi = wq % a.nq;
   const int64_t np = a.nq * a.r;
-  int pos = -1;
-  float ls = neg_inf();
-  if (lane < a.r) {
-    const int p = a.inv[(int64_t)h * np + qi * a.r + lane];
-    if (p >= 0 && p < np) {
-      pos = p;
-      ls = a.part_lse[(int64_t)h * np + p];
-    } else {
-      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-    }
-  }
+  const int64_t pb = (int64_t)h * np + qi * a.r;   // the query's r slots are adjacent rows
+  const float ls = lane < a.r ? a.part_lse[pb + lane] : neg_inf();
   float mx = ls;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -817,9 +809,8 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   for (int sl = 0; sl < a.r; ++sl) {
     const float ws = __shfl_sync(0xffffffffu, w, sl);
-    const int ps = __shfl_sync(0xffffffffu, pos, sl);
-    if (ws == 0.f || ps < 0) continue;
-    const float* src = a.part_o + ((int64_t)h * np + ps) * D + lane * E;
+    if (ws == 0.f) continue;
+    const float* src = a.part_o + (pb + sl) * D + lane * E;
     if (E == 4) {
       const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
       acc[0] = fmaf(ws, v.x, acc[0]);
@@ -851,7 +842,7 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (attr != cudaSuccess) return false;
   int64_t upper;
   if (a.mode == kSparse) {
-    if (!a.items || !a.n_items || !a.inv) return false;
+    if (!a.items || !a.n_items) return false;
     sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
     count_launches(1);
     upper = (int64_t)a.H * ((a.nq * a.r + kAT - 1) / kAT + a.B);

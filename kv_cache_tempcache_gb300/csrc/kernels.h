@@ -81,9 +81,8 @@ struct AttnArgs {
   void* out;
   int64_t o_hs, o_ts;
   float* lse;
-  float* part_o;    // sparse partials [H, nq*r, d] (SIMT path: by pair; tensor-core path: by sorted position)
+  float* part_o;    // sparse partials [H, nq*r, d], row = (query, slot) pair
   float* part_lse;  // [H, nq*r]
-  int32_t* inv;     // sparse: sorted position of each (query, slot) pair [H, nq*r] (tensor-core path)
   void* items;      // sparse: work list written by the planning kernel (tensor-core path)
   int32_t* n_items; // sparse: its length
   int32_t* status;
