@@ -83,7 +83,8 @@ extern "C" {
 
 /* Bytes of workspace `op` needs for the given sizes (0 if it needs none).
  * MATCH: n = Nq, M = cache capacity.  SORT: n = elements per head before the
- * r fan-out.  SPARSE_ATTN: n = Nq.  ANNCA: F frames, P prompt tokens.
+ * r fan-out.  SPARSE_ATTN: n = Nq, M = cache capacity (the bf16 path keeps a
+ * bucket-ordered copy of the cache K/V in it).  ANNCA: F frames, P prompt tokens.
  * Unused arguments are ignored.  Returns 0 for an unknown op. */
 size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r,
                               int64_t P, int F);

@@ -71,7 +71,7 @@ size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B,
   switch (op) {
     case FASTAR_OP_MATCH: return fastar::match_workspace(H, n, M);
     case FASTAR_OP_SORT: return 0;
-    case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r, B);
+    case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r, B, M);
     case FASTAR_OP_ANNCA: return fastar::annca_workspace(H, F, P);
     default: return 0;
   }
@@ -162,7 +162,7 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
   if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, nq, H))) return rc;
   if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, nq, H))) return rc;
   if (!qperm || !qoff || !kperm || !koff || !k || !v || !aligned16(k) || !aligned16(v)) return FASTAR_EINVAL;
-  const size_t need = fastar::sparse_attn_workspace(H, nq, d, r, B);
+  const size_t need = fastar::sparse_attn_workspace(H, nq, d, r, B, M);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
   if (!(scale > 0.f) || !(scale < 3.0e38f)) return FASTAR_EINVAL;
   fastar::AttnArgs a{};
@@ -191,6 +191,10 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
     uint8_t* plan = reinterpret_cast<uint8_t*>((at + 15) & ~static_cast<uintptr_t>(15));
     a.items = plan;
     a.n_items = reinterpret_cast<int32_t*>(plan + fastar::sparse_plan_bytes(H, nq, r, B) - 16);
+    const uintptr_t kat = reinterpret_cast<uintptr_t>(plan + fastar::sparse_plan_bytes(H, nq, r, B));
+    uint8_t* ks = reinterpret_cast<uint8_t*>((kat + 1023) & ~static_cast<uintptr_t>(1023));
+    a.ksorted = ks;
+    a.vsorted = ks + sizeof(uint16_t) * (size_t)H * M * d;
   }
   a.status = dev_status;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));

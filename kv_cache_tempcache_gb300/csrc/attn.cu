@@ -296,11 +296,13 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
   if (lane == 0 && a.lse) a.lse[(int64_t)h * a.nq + i] = W > 0.f ? mx + __logf(W) : neg_inf();
 }
 
-size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B) {
-  // fp32 partials (o, lse) per (query, slot), then (16-byte aligned) the tensor-core
-  // path's work list and its length
+size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B, int64_t M) {
+  // fp32 partials (o, lse) per (query, slot); then (16-byte aligned) the tensor-core
+  // path's work list and its length; then (1024-byte aligned) its bucket-ordered copy
+  // of the cache K and V (bf16)
   const size_t head = sizeof(float) * (size_t)H * nq * r * (d + 1);
-  return ((head + 15) & ~(size_t)15) + sparse_plan_bytes(H, nq, r, B) + 256;
+  const size_t plan = ((head + 15) & ~(size_t)15) + sparse_plan_bytes(H, nq, r, B);
+  return ((plan + 1023) & ~(size_t)1023) + 2 * sizeof(uint16_t) * (size_t)H * M * d + 1024;
 }
 
 template <typename T, int D>

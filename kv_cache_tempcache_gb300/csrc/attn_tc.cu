@@ -24,12 +24,15 @@
 //               consumed K tile when d = 128);
 //   warps 9-12  epilogue: O / l from TMEM to the output (or, for AnnSA, the slot
 //               partial and the merge) while the next item is being computed.
-// AnnSA's items (head, bucket, 128-pair tile) are listed by a one-CTA planning kernel;
+// AnnSA's items (head, bucket, 128-pair tile) are planned by every CTA in its prologue
+// (an exclusive prefix of the tile counts in shared memory, searched per item) when
+// H·B < 2048, else listed by a one-CTA planning kernel;
 // each item writes its slot partials (o, lse) at the (query, slot) pair rows — staged
 // through shared memory so every store is a 128-byte row segment — and a merge kernel
 // combines the r adjacent slot rows of every query afterwards.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -49,6 +52,7 @@ constexpr int kMmaWarpA = 4;
 constexpr int kSoftWarp0 = 5;
 constexpr int kEpiWarp0 = 9;
 constexpr int kPlanThreads = 1024;
+constexpr int kPrefixMax = 2048;  // (head, bucket) entries + 1 planned inside the kernel
 
 // One AnnSA work item, as listed by the planning kernel.
 struct SparseItem {
@@ -93,7 +97,8 @@ struct AttnLayout {
   // 128 rows x 32 fp32: the epilogue's transpose buffer for coalesced partial stores
   static constexpr size_t ostage = kPAliasK ? v + kKS * kstage : p + kKS * pstride;
   static constexpr size_t ctl = ostage + 128 * 32 * sizeof(float);
-  static constexpr size_t bytes = ctl + sizeof(AttnCtl) + 1024;
+  static constexpr size_t prefix = ctl + ((sizeof(AttnCtl) + 15) & ~(size_t)15);   // kPrefixMax ints
+  static constexpr size_t bytes = prefix + kPrefixMax * sizeof(int) + 1024;
   static constexpr uint32_t s_col = 0;      // S buffers: kKS x kKT columns from 0
   static constexpr uint32_t o_col = 256;    // O accumulators: [256 + 128 * stage, ...)
   static_assert(kKS * kKT <= 256, "S buffers overlap the O accumulators");
@@ -207,12 +212,54 @@ __device__ __forceinline__ int64_t items_of(const AttnArgs& a) {
   return 0;   // sparse: from the planning kernel
 }
 
+// AnnSA entry k = (head, bucket): its query-pair range [q0, q1) in the head's sorted
+// order, its key range (kbase, nk) and the number of 128-pair tiles; malformed offsets
+// give no tiles (or no keys) and a status bit.
+__device__ __forceinline__ int sparse_entry(const AttnArgs& a, int k, int& q0, int& q1, int& kb, int& nk) {
+  const int64_t np = a.nq * a.r;
+  const int h = k / a.B, b = k % a.B;
+  const int32_t* qo = a.qoff + (int64_t)h * (a.B + 1);
+  const int32_t* ko = a.koff + (int64_t)h * (a.B + 1);
+  q0 = qo[b];
+  q1 = qo[b + 1];
+  kb = ko[b];
+  nk = ko[b + 1] - kb;
+  if (q0 < 0 || q1 < q0 || q1 > np) {
+    flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+    return 0;
+  }
+  if (kb < 0 || nk < 0 || (int64_t)kb + nk > a.M) {
+    flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+    nk = 0;
+  }
+  return (q1 - q0 + kAT - 1) / kAT;
+}
+
 // Work item u: its head, key count and key base, and its query range [q0, q1) (sparse:
 // positions in the head's qperm row; otherwise token rows).
 __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemInfo& it, int64_t& q0,
-                                            int64_t& q1) {
+                                            int64_t& q1, const int* pre) {
   it.f = 0;
   it.kbase = 0;
+  if (a.mode == kSparse && !a.items) {
+    // planned in the kernel: pre[k] = tiles of the entries before k; find the entry
+    int lo = 0, hi = a.H * a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    int e0, e1, kb, nk;
+    sparse_entry(a, lo, e0, e1, kb, nk);
+    it.h = lo / a.B;
+    q0 = e0 + (u - pre[lo]) * kAT;
+    q1 = q0 + kAT < e1 ? q0 + kAT : e1;
+    it.kbase = kb;
+    it.nkeys = nk;
+    it.q0 = q0;
+    it.nrows = (int)(q1 - q0);
+    it.T = (int)((it.nkeys + kKT - 1) / kKT);
+    return;
+  }
   if (a.mode == kSparse) {
     const int4* p = reinterpret_cast<const int4*>(static_cast<const SparseItem*>(a.items) + u);
     const int4 x = p[0], y = p[1];
@@ -335,7 +382,8 @@ struct Pending {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreadsA, 1)
+    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using Lay = AttnLayout<D>;
   constexpr int CPR = D / 8;   // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
@@ -363,7 +411,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
       tc::mbar_init(&sm.o_empty[s], 4);
     }
     for (int s = 0; s < kKS; ++s) {
-      tc::mbar_init(&sm.kv_full[s], 128);
+      tc::mbar_init(&sm.kv_full[s], a.kv_tma ? 1 : 128);
       tc::mbar_init(&sm.kv_empty[s], 1);
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.s_free[s], 4);
@@ -372,9 +420,41 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
     tc::mbar_init(&sm.pv_done, 1);
     tc::mbar_init(&sm.fin, 1);
     sm.abort = 0;
-    int64_t n = a.mode == kSparse ? (int64_t)*a.n_items : items_of(a);
-    sm.n_items = (int)(n < INT_MAX ? n : INT_MAX);
     tc::mbar_fence_init();
+  }
+  int* pre = reinterpret_cast<int*>(base + Lay::prefix);
+  if (a.mode == kSparse && !a.items) {
+    // plan the AnnSA items here: exclusive prefix over the (head, bucket) entries of
+    // their tile counts (every thread takes a contiguous run of entries)
+    const int ne = a.H * a.B;
+    const int per = (ne + kThreadsA - 1) / kThreadsA;
+    const int k0 = threadIdx.x * per, k1 = k0 + per < ne ? k0 + per : ne;
+    int mine = 0;
+    for (int k = k0; k < k1; ++k) {
+      int e0, e1, kb, nk;
+      mine += sparse_entry(a, k, e0, e1, kb, nk);
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __shared__ int wtot[kThreadsA / 32];
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int run = 0;
+    for (int w = 0; w < warp; ++w) run += wtot[w];
+    int at = run + incl - mine;
+    for (int k = k0; k < k1; ++k) {
+      pre[k] = at;
+      int e0, e1, kb, nk;
+      at += sparse_entry(a, k, e0, e1, kb, nk);
+    }
+    if (threadIdx.x == kThreadsA - 1) sm.n_items = run + incl;
+  } else if (threadIdx.x == 0) {
+    const int64_t n = a.mode == kSparse ? (int64_t)*a.n_items : items_of(a);
+    sm.n_items = (int)(n < INT_MAX ? n : INT_MAX);
   }
   __syncthreads();
   const int n_items = sm.n_items;
@@ -405,9 +485,9 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
     int qdst = -1;
     auto load_item = [&](int64_t v, ItemInfo& x, int64_t& src, int& dst, int64_t& k0) {
       int64_t p0, p1;
-      decode_item(a, v, x, p0, p1);
+      decode_item(a, v, x, p0, p1, pre);
       query_row(a, x, p0 + t, p1, np, src, dst);
-      k0 = t < kKT && x.T > 0 ? key_offset(a, x, t, D) : -1;
+      k0 = !a.kv_tma && t < kKT && x.T > 0 ? key_offset(a, x, t, D) : -1;
     };
     if ((int)blockIdx.x < n_items) load_item(blockIdx.x, it, qsrc, qdst, ksrc);
     for (int u = blockIdx.x; u < n_items && ok; u += gridDim.x, ++n) {
@@ -440,10 +520,33 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
         }
         tc::cp_async_commit();
         pend.push(&sm.q_full[qs]);
+        // K/V by TMA: nothing else of this thread's is in flight, so signal Q now (no
+        // thread may hold an unsignalled copy while it waits in a named barrier below)
+        if (a.kv_tma) pend.flush();
       }
       for (int j = 0; j < it.T; ++j, ++g) {
         const int st = g % kKS;
         const uint32_t ph = (g / kKS) & 1;
+        if (a.kv_tma) {
+          // one thread brings the K and V tiles (contiguous rows) with the tensor engine
+          bool free = true;
+          if (t == 0) {
+            free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
+            if (free) {
+              const int y = (int)(it.kbase + (int64_t)j * kKT);
+              tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
+              for (int kh = 0; kh < D / 64; ++kh) {
+                tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
+                tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+              }
+            }
+          }
+          if (!tc::named_bar_and(1, 128, free)) {
+            ok = false;
+            break;
+          }
+          continue;
+        }
         const int64_t cur = ksrc;
         ksrc = t < kKT && j + 1 < it.T ? key_offset(a, it, (int64_t)(j + 1) * kKT + t, D) : -1;
         const bool free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
@@ -722,29 +825,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_tc_kernel(const AttnArgs a)
 __global__ void __launch_bounds__(kPlanThreads) sparse_plan_kernel(const AttnArgs a) {
   __shared__ int wsum[kPlanThreads / 32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t np = a.nq * a.r;
   const int n = a.H * a.B;
   const int per = (n + kPlanThreads - 1) / kPlanThreads;
   const int k0 = t * per, k1 = k0 + per < n ? k0 + per : n;
-  // tiles of entry k = (h, b); malformed offsets give no tiles (and a status bit)
-  auto tiles = [&](int k, int& q0, int& q1, int& kb, int& nk) -> int {
-    const int h = k / a.B, b = k % a.B;
-    const int32_t* qo = a.qoff + (int64_t)h * (a.B + 1);
-    const int32_t* ko = a.koff + (int64_t)h * (a.B + 1);
-    q0 = qo[b];
-    q1 = qo[b + 1];
-    kb = ko[b];
-    nk = ko[b + 1] - kb;
-    if (q0 < 0 || q1 < q0 || q1 > np) {
-      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-      return 0;
-    }
-    if (kb < 0 || nk < 0 || (int64_t)kb + nk > a.M) {
-      flag_status(a.status, FASTAR_DEV_BAD_INDEX);
-      nk = 0;
-    }
-    return (q1 - q0 + kAT - 1) / kAT;
-  };
+  auto tiles = [&](int k, int& q0, int& q1, int& kb, int& nk) -> int { return sparse_entry(a, k, q0, q1, kb, nk); };
   int mine = 0;
   for (int k = k0; k < k1; ++k) {
     int q0, q1, kb, nk;
@@ -779,6 +863,40 @@ __global__ void __launch_bounds__(kPlanThreads) sparse_plan_kernel(const AttnArg
       const int s = q0 + i * kAT;
       items[at] = SparseItem{k / a.B, s, s + kAT < q1 ? s + kAT : q1, kb, nk, 0, 0, 0};
     }
+  }
+}
+
+// Copies each head's cache K/V rows into bucket order — rows [koff[b], koff[b+1]) of
+// head h are bucket b's keys — so that the attention kernel reads a bucket's keys as
+// contiguous TMA tiles.  Rows past the head's sorted length are zeroed (a tile may
+// reach into them; their scores are masked and their values must stay finite).
+template <int D>
+__global__ void __launch_bounds__(256) sparse_sort_rows_kernel(const AttnArgs a) {
+  constexpr int CPR = D / 8;   // 16-byte chunks per row
+  const int64_t total = (int64_t)a.H * a.M * CPR;
+  const uint4* K = static_cast<const uint4*>(a.k);
+  const uint4* V = static_cast<const uint4*>(a.v);
+  uint4* KS = static_cast<uint4*>(a.ksorted);
+  uint4* VS = static_cast<uint4*>(a.vsorted);
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < total; g += (int64_t)gridDim.x * 256) {
+    const int64_t row = g / CPR;
+    const int c = (int)(g % CPR);
+    const int h = (int)(row / a.M);
+    const int64_t pos = row % a.M;
+    const int32_t n = a.koff[(int64_t)h * (a.B + 1) + a.B];
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+    if (pos < n && n <= a.M) {
+      const int s = a.kperm[(int64_t)h * a.M + pos];
+      if (s >= 0 && s < a.M) {
+        const int64_t src = ((int64_t)h * a.M + s) * CPR + c;
+        kv = K[src];
+        vv = V[src];
+      } else if (c == 0) {
+        flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      }
+    }
+    KS[g] = kv;
+    VS[g] = vv;
   }
 }
 
@@ -841,10 +959,40 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
       cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return false;
   int64_t upper;
+  AttnArgs b = a;
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  b.kv_tma = 0;
+  if (a.mode == kSparse) {
+    // bucket-ordered copies of the cache rows, read as contiguous tiles
+    if (a.ksorted && a.vsorted &&
+        make_tmap_bf16_3d(&tk, a.ksorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2,
+                          (uint64_t)a.M * D * 2, 64, kKT) &&
+        make_tmap_bf16_3d(&tv, a.vsorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2,
+                          (uint64_t)a.M * D * 2, 64, kKT)) {
+      const int64_t chunks = (int64_t)a.H * a.M * (D / 8);
+      const int64_t blocks = (chunks + 255) / 256;
+      const int grid_c = (int)(blocks < 8 * sm_count() ? blocks : 8 * sm_count());
+      sparse_sort_rows_kernel<D><<<grid_c, 256, 0, s>>>(a);
+      count_launches(1);
+      b.kv_tma = 1;
+    }
+  } else if (a.mode == kDense && a.kv_ts == D && a.nk <= INT_MAX &&
+             make_tmap_bf16_3d(&tk, a.k, D, (uint64_t)a.nk, (uint64_t)a.H, (uint64_t)a.kv_ts * 2,
+                               (uint64_t)a.kv_hs * 2, 64, kKT) &&
+             make_tmap_bf16_3d(&tv, a.v, D, (uint64_t)a.nk, (uint64_t)a.H, (uint64_t)a.kv_ts * 2,
+                               (uint64_t)a.kv_hs * 2, 64, kKT)) {
+    b.kv_tma = 1;   // the dense keys are contiguous rows already
+  }
   if (a.mode == kSparse) {
     if (!a.items || !a.n_items) return false;
-    sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-    count_launches(1);
+    if ((int64_t)a.H * a.B + 1 <= kPrefixMax) {
+      b.items = nullptr;   // planned inside the attention kernel
+    } else {
+      sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+      count_launches(1);
+    }
     upper = (int64_t)a.H * ((a.nq * a.r + kAT - 1) / kAT + a.B);
   } else if (a.mode == kCross) {
     upper = (int64_t)a.H * a.F * ((a.tpf + kAT - 1) / kAT);
@@ -854,7 +1002,7 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (upper <= 0) return true;
   const int sms = sm_count();
   const int grid = (int)(upper < sms ? upper : sms);
-  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(a);
+  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tv);
   count_launches(1);
   if (a.mode == kSparse) {
     const int64_t threads = (int64_t)a.H * a.nq * 32;

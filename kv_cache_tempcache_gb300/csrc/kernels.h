@@ -84,11 +84,14 @@ struct AttnArgs {
   float* part_o;    // sparse partials [H, nq*r, d], row = (query, slot) pair
   float* part_lse;  // [H, nq*r]
   void* items;      // sparse: work list written by the planning kernel (tensor-core path)
+  void* ksorted;    // sparse: the cache K/V rows in bucket order [H, M, d] (tensor-core path)
+  void* vsorted;
+  int kv_tma;       // keys/values arrive as contiguous TMA tiles (set by the launcher)
   int32_t* n_items; // sparse: its length
   int32_t* status;
 };
 
-size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B);
+size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B, int64_t M);
 // Bytes of the tensor-core AnnSA work list (inside the sparse workspace).
 size_t sparse_plan_bytes(int H, int64_t nq, int r, int B);
 // Tensor-core attention (bf16); false if it could not be set up (caller falls back).
