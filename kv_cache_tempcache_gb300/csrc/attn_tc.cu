@@ -383,7 +383,8 @@ struct Pending {
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsA, 1)
-    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_q) {
   using Lay = AttnLayout<D>;
   constexpr int CPR = D / 8;   // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&sm.q_full[s], 128);
+      tc::mbar_init(&sm.q_full[s], a.q_tma ? 1 : 128);
       tc::mbar_init(&sm.q_empty[s], 1);
       tc::mbar_init(&sm.dst_free[s], 4);
       tc::mbar_init(&sm.ml_full[s], 4);
@@ -469,7 +470,56 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp < 4) {
+  if (warp < 4 && a.q_tma) {
+    // ---------------- tensor-engine loads (thread 0 issues every copy) ----------------
+    // Q, K and V tiles are all contiguous rows: thread 0 issues them; the other loader
+    // threads only record their row's output destination.  Nobody holds an unsignalled
+    // copy, so the only barrier (per item) cannot wait on a stuck copy.
+    const int t = threadIdx.x;
+    int g = 0, n = 0;
+    bool tiles_ok = true;
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x, ++n) {
+      const int qs = n & 1;
+      const uint32_t qph = (n >> 1) & 1;
+      bool got = true;
+      if (n >= 2) got = tc::mbar_wait(&sm.q_empty[qs], qph ^ 1, abort) && tc::mbar_wait(&sm.dst_free[qs], qph ^ 1, abort);
+      ItemInfo it;
+      int64_t q0, q1, src;
+      int dst;
+      decode_item(a, u, it, q0, q1, pre);
+      query_row(a, it, q0 + t, q1, np, src, dst);
+      if (got) {
+        sm.qdst[qs][t] = dst;
+        if (t == 0) sm.info[qs] = it;
+      }
+      if (!tc::named_bar_and(1, 128, got && tiles_ok)) break;
+      if (t == 0) {
+        tc::mbar_arrive_tx(&sm.q_full[qs], (uint32_t)Lay::qstage);
+        for (int kh = 0; kh < D / 64; ++kh) {
+          uint8_t* dq = sq + (size_t)qs * Lay::qstage + kh * kBlkA;
+          if (!a.q_token_major)
+            tc::tma_load_3d(dq, &tm_q, kh * 64, (int)q0, it.h, &sm.q_full[qs]);
+          else
+            tc::tma_load_3d(dq, &tm_q, kh * 64, it.h, (int)q0, &sm.q_full[qs]);
+        }
+        for (int j = 0; j < it.T; ++j) {
+          const int st = (g + j) % kKS;
+          const uint32_t ph = ((g + j) / kKS) & 1;
+          if (!tc::mbar_wait(&sm.kv_empty[st], ph ^ 1, abort)) {
+            tiles_ok = false;
+            break;
+          }
+          const int y = (int)(it.kbase + (int64_t)j * kKT);
+          tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
+          for (int kh = 0; kh < D / 64; ++kh) {
+            tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
+            tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+          }
+        }
+      }
+      g += it.T;
+    }
+  } else if (warp < 4) {
     // ---------------- row gathers (128 threads) ----------------
     const int t = threadIdx.x;
     // Every exit decision is taken by all 128 threads together (named_bar_and): a
@@ -960,23 +1010,28 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (attr != cudaSuccess) return false;
   int64_t upper;
   AttnArgs b = a;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
+  memset(&tq, 0, sizeof(tq));
   b.kv_tma = 0;
+  b.q_tma = 0;
+  b.q_token_major = 0;
   if (a.mode == kSparse) {
     // bucket-ordered copies of the cache rows, read as contiguous tiles
+    // (the queries stay gathered: copying the pairs' rows costs more than it saves)
     if (a.ksorted && a.vsorted &&
         make_tmap_bf16_3d(&tk, a.ksorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2,
                           (uint64_t)a.M * D * 2, 64, kKT) &&
         make_tmap_bf16_3d(&tv, a.vsorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2,
                           (uint64_t)a.M * D * 2, 64, kKT)) {
       const int64_t chunks = (int64_t)a.H * a.M * (D / 8);
-      const int64_t blocks = (chunks + 255) / 256;
-      const int grid_c = (int)(blocks < 8 * sm_count() ? blocks : 8 * sm_count());
-      sparse_sort_rows_kernel<D><<<grid_c, 256, 0, s>>>(a);
-      count_launches(1);
-      b.kv_tma = 1;
+      const int64_t blocks = (chunks + 255) / 256;   // one 16-byte chunk per thread
+      if (blocks <= INT_MAX) {
+        sparse_sort_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a);
+        count_launches(1);
+        b.kv_tma = 1;
+      }
     }
   } else if (a.mode == kDense && a.kv_ts == D && a.nk <= INT_MAX &&
              make_tmap_bf16_3d(&tk, a.k, D, (uint64_t)a.nk, (uint64_t)a.H, (uint64_t)a.kv_ts * 2,
@@ -984,6 +1039,16 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
              make_tmap_bf16_3d(&tv, a.v, D, (uint64_t)a.nk, (uint64_t)a.H, (uint64_t)a.kv_ts * 2,
                                (uint64_t)a.kv_hs * 2, 64, kKT)) {
     b.kv_tma = 1;   // the dense keys are contiguous rows already
+    // and so are the queries (a token-major view is read as (d, H, tokens) boxes)
+    const bool tmaj = a.H > 1 && a.q.hs < a.q.ts;
+    const bool qok = tmaj ? make_tmap_bf16_3d(&tq, a.q.p, D, (uint64_t)a.H, (uint64_t)a.nq, (uint64_t)a.q.hs * 2,
+                                              (uint64_t)a.q.ts * 2, 64, 1, kAT)
+                          : make_tmap_bf16_3d(&tq, a.q.p, D, (uint64_t)a.nq, (uint64_t)a.H, (uint64_t)a.q.ts * 2,
+                                              (uint64_t)a.q.hs * 2, 64, kAT);
+    if (qok && a.nq <= INT_MAX) {
+      b.q_tma = 1;
+      b.q_token_major = tmaj ? 1 : 0;
+    }
   }
   if (a.mode == kSparse) {
     if (!a.items || !a.n_items) return false;
@@ -1002,7 +1067,7 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (upper <= 0) return true;
   const int sms = sm_count();
   const int grid = (int)(upper < sms ? upper : sms);
-  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tv);
+  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
   count_launches(1);
   if (a.mode == kSparse) {
     const int64_t threads = (int64_t)a.H * a.nq * 32;

@@ -87,6 +87,8 @@ struct AttnArgs {
   void* ksorted;    // sparse: the cache K/V rows in bucket order [H, M, d] (tensor-core path)
   void* vsorted;
   int kv_tma;       // keys/values arrive as contiguous TMA tiles (set by the launcher)
+  int q_tma;        // so do the query tiles: one thread drives every copy (set by the launcher)
+  int q_token_major;  // the query tensor map is (d, H, tokens) rather than (d, tokens, H)
   int32_t* n_items; // sparse: its length
   int32_t* status;
 };
