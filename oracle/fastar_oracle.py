@@ -129,6 +129,37 @@ def tempcache_match(Q, K_cache):
     return top1, s1, s2
 
 
+def tempcache_match_ann(Q, R, K_cache, kb_cache):
+    """The ANN-restricted variant of the match: each current query is compared only
+    with the cached keys that fall in one of its own buckets (technical summary §2.A:
+    a lightweight approximate nearest-neighbour search instead of full attention
+    matrices; the buckets are the ones AnnSA and AnnCA share).
+
+    Q [nq, d]; R [nq, r] the query bucket sets; K_cache [n, d] in age order with
+    key buckets kb_cache [n].  Returns (top1 int64 [nq], s1 [nq]):
+      top1[i] = argmax over {j : kb_cache[j] in R[i]} of cos(q_i, k_j), lowest j on
+                ties; -1 when no cached key shares a bucket with q_i
+      s1[i]   = that cosine (-inf when top1[i] = -1).
+    """
+    Q = _f64(Q)
+    K = _f64(K_cache)
+    R = np.asarray(R, np.int64).reshape(Q.shape[0], -1)
+    kb = np.asarray(kb_cache, np.int64)
+    nq, n = Q.shape[0], K.shape[0]
+    top1 = np.full(nq, -1, np.int64)
+    s1 = np.full(nq, NEG_INF)
+    if n == 0:
+        return top1, s1
+    S = cosine_matrix(Q, K)
+    allowed = (kb[None, :, None] == R[:, None, :]).any(axis=2)   # [nq, n]
+    S = np.where(allowed, S, NEG_INF)
+    has = allowed.any(axis=1)
+    best = np.argmax(S, axis=1).astype(np.int64)                # first maximum = lowest j
+    top1[has] = best[has]
+    s1[has] = S[np.arange(nq), best][has]
+    return top1, s1
+
+
 def evict_flags(top1, K_cur, K_cache, tau: float):
     """e_j = 1 iff some query i has top1[i] = j and cos(kcur_i, k_j) >= tau.
 

@@ -107,3 +107,21 @@ def step(q, k_cur, v_cur, cache_k, cache_v, C, kp, vp, *, F, Tf, tau, M, r, tau_
         o_cross.append(attend(q[i], [kp[p] for p in idx], [vp[p] for p in idx], [True] * len(idx)))
     return dict(qb=qb, kb_cur=kb_cur, kb_cache=kb_cache, pb=pb, top1=top1, evict=evict,
                 index_map=index_map, length=L, o_self=o_self, keep=keep, o_cross=o_cross)
+
+
+def ann_match(q, R, cache_k, kb):
+    """Bucket-restricted top-1 by enumeration: for each query, every cached key whose
+    bucket is one of the query's buckets is scored by cosine; the first (oldest) key
+    with the largest score wins; (-1, -inf) when no key qualifies."""
+    top1, s1 = [], []
+    for i in range(len(q)):
+        best_j, best = -1, float("-inf")
+        for j in range(len(cache_k)):
+            if kb[j] not in list(R[i]):
+                continue
+            c = cos(q[i], cache_k[j])
+            if best_j < 0 or c > best:
+                best_j, best = j, c
+        top1.append(best_j)
+        s1.append(best)
+    return top1, s1
