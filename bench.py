@@ -379,6 +379,9 @@ def run_fastar(args, rank, world, local):
         "clocks": clk,
         "device_bytes": layer.device_bytes(),
     }
+    # the ANN-restricted match (a variant of the TempCache match): timed beside the exact
+    # match on the measured chunk's incoming cache, with the agreement of their choices
+    out["ann_match"] = time_ann_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib)
     # dense baseline from the same build: append-only cache, full attention
     if not args.no_dense:
         hk = np.concatenate(hist_k, axis=1)
@@ -439,6 +442,52 @@ def cpu_baseline(cfg, seed, budget_s=15.0):
             "sample": f"{heads} of {cfg.H} heads of one {cfg.name} step (float64 NumPy, cache of the "
                       f"{ck.shape[1]} most recent history entries), scaled by {cfg.H}/{heads}",
             "seconds": round(dt, 2)}
+
+
+def time_ann_match(layer, cfg, q_d, k_d, flush, steps, torch, L):
+    dev = q_d.device
+    cin = layer.caches[layer.cur]
+    H, M, B, r, nq = cfg.H, cfg.M, cfg.B, cfg.r, cfg.Nq
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device=dev)
+    kperm, koff, status = i32(H, M), i32(H, B + 1), i32(1)
+    L.fastar_bucket_sort(cin.kb, B, kperm, koff, cin.len, status)     # the incoming cache's bucket order
+    ws = torch.zeros(L.workspace_bytes(L.OP_MATCH_ANN, H, nq, M, cfg.d, B, r), dtype=torch.uint8, device=dev)
+    t_ann, s_ann = i32(H, nq), torch.zeros((H, nq), dtype=torch.float32, device=dev)
+    e_ann = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+    t_ex, s_ex = i32(H, nq), torch.zeros((H, nq), dtype=torch.float32, device=dev)
+    e_ex = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+
+    def ann():
+        L.fastar_tempcache_match_ann(q_d, k_d, r, B, layer.qperm, layer.qoff, cin.k, cin.knorm, cin.len, kperm,
+                                     koff, cfg.tau, t_ann, s_ann, e_ann, status, ws)
+
+    def exact():
+        L.fastar_tempcache_match(q_d, k_d, cin.k, cin.knorm, cin.len, cfg.tau, t_ex, s_ex, None, e_ex, status,
+                                 layer.ws_match)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return sum(ms) / len(ms)
+
+    ann_ms, ex_ms = timed(ann), timed(exact)
+    torch.cuda.synchronize()
+    agree = float((t_ann == t_ex).float().mean().item())
+    return {"ms": round(ann_ms, 4), "exact_ms": round(ex_ms, 4), "speedup_vs_exact": round(ex_ms / ann_ms, 3),
+            "top1_agree_with_exact": round(agree, 4),
+            "evicted": {"ann": int(e_ann.sum().item()), "exact": int(e_ex.sum().item())},
+            "status": int(status.item()),
+            "note": "each query compared only with the incoming cache's keys in its own r buckets; "
+                    "one call incl. the bucket-order copy and the slot merge, L2 flushed before each"}
 
 
 def run_reference(args, rank, world):

@@ -80,11 +80,13 @@ extern "C" {
 #define FASTAR_OP_SORT 2
 #define FASTAR_OP_SPARSE_ATTN 3
 #define FASTAR_OP_ANNCA 4
+#define FASTAR_OP_MATCH_ANN 5
 
 /* Bytes of workspace `op` needs for the given sizes (0 if it needs none).
  * MATCH: n = Nq, M = cache capacity.  SORT: n = elements per head before the
  * r fan-out.  SPARSE_ATTN: n = Nq, M = cache capacity (the bf16 path keeps a
  * bucket-ordered copy of the cache K/V in it).  ANNCA: F frames, P prompt tokens.
+ * MATCH_ANN: n = Nq, M, d, B, r.
  * Unused arguments are ignored.  Returns 0 for an unknown op. */
 size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r,
                               int64_t P, int F);
@@ -143,6 +145,28 @@ int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, i
                            int32_t* top1, float* s1, float* s2, uint8_t* evict,
                            int32_t* dev_status, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+
+/* ---- 2b. ANN-restricted TempCache match (a variant of 2) -----------------------------
+ * FAST-AR technical summary §2.A: the temporal correspondence is searched with a
+ * lightweight approximate nearest-neighbour method instead of full attention
+ * matrices.  Here the ANN is the bucketing that AnnSA and AnnCA share: query i is
+ * compared only with the cached keys whose bucket is one of its r buckets R(i):
+ *   top1[h,i] = argmax_{j < n, kb(k_j) in R(i)} cos(q_i, k_j)  (lowest j on ties;
+ *               -1 when no cached key shares a bucket with q_i)
+ *   s1[h,i]   = that cosine (-inf when top1 = -1)
+ *   evict[h, top1] = 1 if cos(kcur_i, k_top1) >= tau, as in 2 (cleared first).
+ * Inputs beyond 2's: the (query, slot) pairs in bucket order (qperm/qoff from
+ * fastar_bucket_sort of the query buckets, r per query) and the INCOMING cache's keys
+ * in bucket order (kperm/koff from fastar_bucket_sort of its key buckets with
+ * n_valid = cache_len).  bf16 only (FASTAR_EUNSUPPORTED otherwise).
+ * Workspace: fastar_workspace_bytes(FASTAR_OP_MATCH_ANN, H, nq, M, d, B, r, ...). */
+int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                               int64_t head_stride, int64_t token_stride, int r, int B,
+                               const int32_t* qperm, const int32_t* qoff, const void* cache_k,
+                               const float* cache_knorm, const int32_t* cache_len, int64_t M,
+                               const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1,
+                               float* s1, uint8_t* evict, int32_t* dev_status, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
 
 /* ---- 3. cache compaction -------------------------------------------------------
  * FAST-AR technical summary §2.A ("merging ... bounds the growth of the KV

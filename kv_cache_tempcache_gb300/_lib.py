@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libfastar.so")
 F32, BF16 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECAPACITY, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
 DEV_BAD_LEN, DEV_BAD_BUCKET, DEV_BAD_INDEX = 1, 2, 4
-OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA = 1, 2, 3, 4
+OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA, OP_MATCH_ANN = 1, 2, 3, 4, 5
 MAX_B, MAX_R, MAX_P = 256, 8, 1024
 
 _P = ctypes.c_void_p
@@ -37,6 +37,8 @@ _SIGS = {
     "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
     "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _S,
                                _P],
+    "fastar_tempcache_match_ann": [_P, _P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _F, _P,
+                                   _P, _P, _P, _P, _S, _P],
     "fastar_cache_compact": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P],
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
@@ -163,6 +165,18 @@ def fastar_tempcache_match(q, k_cur, cache_k, cache_knorm, cache_len, tau, top1,
           ptr(cache_knorm), ptr(cache_len), cache_k.shape[1], float(tau), ptr(top1), ptr(s1), ptr(s2), ptr(evict),
           ptr(dev_status), ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))
+
+
+def fastar_tempcache_match_ann(q, k_cur, r, B, qperm, qoff, cache_k, cache_knorm, cache_len, kperm, koff, tau,
+                               top1, s1, evict, dev_status, workspace, stream=None):
+    H, nq, d = q.shape
+    hs, ts = tok_strides(q)
+    if tok_strides(k_cur) != (hs, ts):
+        raise ValueError("q and k_cur must share strides")
+    _call("fastar_tempcache_match_ann", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, nq, d, hs, ts, int(r), int(B),
+          ptr(qperm), ptr(qoff), ptr(cache_k), ptr(cache_knorm), ptr(cache_len), cache_k.shape[1], ptr(kperm),
+          ptr(koff), float(tau), ptr(top1), ptr(s1), ptr(evict), ptr(dev_status), ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
 def fastar_cache_compact(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict,

@@ -73,6 +73,9 @@ size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B,
     case FASTAR_OP_SORT: return 0;
     case FASTAR_OP_SPARSE_ATTN: return fastar::sparse_attn_workspace(H, n, d, r, B, M);
     case FASTAR_OP_ANNCA: return fastar::annca_workspace(H, F, P);
+    case FASTAR_OP_MATCH_ANN:
+      if ((d != 64 && d != 128) || B < 1 || r < 1 || M < 1) return 0;
+      return fastar::match_ann_workspace(H, n, d, r, B, M);
     default: return 0;
   }
 }
@@ -111,6 +114,34 @@ int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, i
   return cuda_rc(fastar::launch_tempcache_match(
       dtype, d, TokView{q, head_stride, token_stride}, TokView{k_cur, head_stride, token_stride}, H, nq,
       cache_k, cache_knorm, cache_len, M, tau, top1, s1, s2, evict, dev_status, workspace, stream));
+}
+
+int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                               int64_t head_stride, int64_t token_stride, int r, int B,
+                               const int32_t* qperm, const int32_t* qoff, const void* cache_k,
+                               const float* cache_knorm, const int32_t* cache_len, int64_t M,
+                               const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1,
+                               float* s1, uint8_t* evict, int32_t* dev_status, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (dtype != FASTAR_BF16) return FASTAR_EUNSUPPORTED;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || r < 1 || B < 1) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B || r > FASTAR_MAX_R || nq * r > INT32_MAX) return FASTAR_ECAPACITY;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (!cache_k || !aligned16(cache_k) || !cache_knorm || !cache_len || !evict || !qperm || !qoff || !kperm ||
+      !koff)
+    return FASTAR_EINVAL;
+  if (nq > 0 && (!top1 || !s1)) return FASTAR_EINVAL;
+  const size_t need = fastar::match_ann_workspace(H, nq, d, r, B, M);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+  if (nq == 0) return FASTAR_OK;
+  return cuda_rc(fastar::launch_match_ann(d, TokView{q, head_stride, token_stride},
+                                          TokView{k_cur, head_stride, token_stride}, H, nq, r, B, qperm, qoff,
+                                          cache_k, cache_knorm, cache_len, M, kperm, koff, tau, top1, s1, evict,
+                                          dev_status, workspace, stream));
 }
 
 int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,

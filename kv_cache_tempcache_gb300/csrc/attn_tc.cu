@@ -53,6 +53,7 @@ constexpr int kSoftWarp0 = 5;
 constexpr int kEpiWarp0 = 9;
 constexpr int kPlanThreads = 1024;
 constexpr int kPrefixMax = 2048;  // (head, bucket) entries + 1 planned inside the kernel
+constexpr int kMatchAux = 80 * 4; // bytes of 1/|k| (or of indices) staged per key tile in match mode
 
 // One AnnSA work item, as listed by the planning kernel.
 struct SparseItem {
@@ -212,6 +213,9 @@ __device__ __forceinline__ int64_t items_of(const AttnArgs& a) {
   return 0;   // sparse: from the planning kernel
 }
 
+// Items over (query, slot) pairs in bucket order: AnnSA and the ANN-restricted match.
+__device__ __forceinline__ bool pair_items(const AttnArgs& a) { return a.mode == kSparse || a.mode == kMatchAnn; }
+
 // AnnSA entry k = (head, bucket): its query-pair range [q0, q1) in the head's sorted
 // order, its key range (kbase, nk) and the number of 128-pair tiles; malformed offsets
 // give no tiles (or no keys) and a status bit.
@@ -241,7 +245,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
                                             int64_t& q1, const int* pre) {
   it.f = 0;
   it.kbase = 0;
-  if (a.mode == kSparse && !a.items) {
+  if (pair_items(a) && !a.items) {
     // planned in the kernel: pre[k] = tiles of the entries before k; find the entry
     int lo = 0, hi = a.H * a.B - 1;
     while (lo < hi) {
@@ -260,7 +264,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
     it.T = (int)((it.nkeys + kKT - 1) / kKT);
     return;
   }
-  if (a.mode == kSparse) {
+  if (pair_items(a)) {
     const int4* p = reinterpret_cast<const int4*>(static_cast<const SparseItem*>(a.items) + u);
     const int4 x = p[0], y = p[1];
     it.h = x.x;
@@ -302,7 +306,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs& a, int64_t u, ItemIn
 // Element offset of key u of the item's key list (-1 if out of range).
 __device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const ItemInfo& it, int64_t u, int D) {
   if (u >= it.nkeys) return -1;
-  if (a.mode == kSparse) {
+  if (pair_items(a)) {
     const int s = a.kperm[(int64_t)it.h * a.M + it.kbase + u];
     if (s >= 0 && s < a.M) return ((int64_t)it.h * a.M + s) * D;
     flag_status(a.status, FASTAR_DEV_BAD_INDEX);
@@ -324,7 +328,7 @@ __device__ __forceinline__ void query_row(const AttnArgs& a, const ItemInfo& it,
   src = -1;
   dst = -1;
   if (pos >= q1) return;
-  if (a.mode == kSparse) {
+  if (pair_items(a)) {
     const int e = a.qperm[(int64_t)it.h * np + pos];
     if (e >= 0 && e < np) {
       src = it.h * a.q.hs + (int64_t)(e / a.r) * a.q.ts;
@@ -413,7 +417,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     }
     for (int s = 0; s < kKS; ++s) {
       tc::mbar_init(&sm.kv_full[s], a.kv_tma ? 1 : 128);
-      tc::mbar_init(&sm.kv_empty[s], 1);
+      // match mode: the softmax warps release a stage (they read its 1/|k| and indices)
+      tc::mbar_init(&sm.kv_empty[s], a.mode == kMatchAnn ? 4 : 1);
       tc::mbar_init(&sm.s_full[s], 1);
       tc::mbar_init(&sm.s_free[s], 4);
       tc::mbar_init(&sm.p_full[s], 4);
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tc::mbar_fence_init();
   }
   int* pre = reinterpret_cast<int*>(base + Lay::prefix);
-  if (a.mode == kSparse && !a.items) {
+  if (pair_items(a) && !a.items) {
     // plan the AnnSA items here: exclusive prefix over the (head, bucket) entries of
     // their tile counts (every thread takes a contiguous run of entries)
     const int ne = a.H * a.B;
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     }
     if (threadIdx.x == kThreadsA - 1) sm.n_items = run + incl;
   } else if (threadIdx.x == 0) {
-    const int64_t n = a.mode == kSparse ? (int64_t)*a.n_items : items_of(a);
+    const int64_t n = pair_items(a) ? (int64_t)*a.n_items : items_of(a);
     sm.n_items = (int)(n < INT_MAX ? n : INT_MAX);
   }
   __syncthreads();
@@ -469,6 +474,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  const bool amatch = a.mode == kMatchAnn;   // arg-max of cosines instead of softmax.V
 
   if (warp < 4 && a.q_tma) {
     // ---------------- tensor-engine loads (thread 0 issues every copy) ----------------
@@ -584,10 +590,22 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
             if (free) {
               const int y = (int)(it.kbase + (int64_t)j * kKT);
-              tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
-              for (int kh = 0; kh < D / 64; ++kh) {
-                tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
-                tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+              if (amatch) {
+                // K, and per key 1/|k| and the cache index, into the (unused) V stage: 80
+                // entries from y rounded down to 16 bytes
+                const int64_t y0 = (int64_t)it.h * a.mstride + (y & ~3);
+                uint8_t* vst = sv + (size_t)st * Lay::kstage;
+                tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(Lay::kstage + 2 * kMatchAux));
+                for (int kh = 0; kh < D / 64; ++kh)
+                  tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
+                tc::bulk_load(vst, a.inv_sorted + y0, kMatchAux, &sm.kv_full[st]);
+                tc::bulk_load(vst + kMatchAux, a.j_sorted + y0, kMatchAux, &sm.kv_full[st]);
+              } else {
+                tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
+                for (int kh = 0; kh < D / 64; ++kh) {
+                  tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
+                  tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+                }
               }
             }
           }
@@ -675,13 +693,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
           }
           tc::mma_commit(&sm.s_full[st]);
           // the previous tile's P.V goes after this tile's Q.K^T (overlaps the softmax)
-          if (j > 0 && !issue_pv(g - 1, qs, j == 1)) {
+          if (j > 0 && !amatch && !issue_pv(g - 1, qs, j == 1)) {
             ok = false;
             break;
           }
         }
         if (!ok) break;
-        if (T > 0 && !issue_pv(g - 1, qs, T == 1)) break;
+        if (T > 0 && !amatch && !issue_pv(g - 1, qs, T == 1)) break;
         tc::mma_commit(&sm.q_empty[qs]);
         tc::mma_commit(&sm.o_full[qs]);
       }
@@ -706,6 +724,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       const int64_t nkeys = sm.info[qs].nkeys;
       const uint32_t o_addr = tmem + lane_addr + Lay::o_col + (uint32_t)(qs * 128);
       float m_used = neg_inf(), l = 0.f;
+      float best = neg_inf();   // match mode: best q.k/|k| of the row and its cache index
+      int bidx = -1;
+      const int64_t kbase = sm.info[qs].kbase;
       for (int j = 0; j < T; ++j, ++g) {
         const int st = g % kKS;
         if (!wait_all(&sm.s_full[st], (g / kKS) & 1, abort)) {
@@ -713,6 +734,44 @@ __global__ void __launch_bounds__(kThreadsA, 1)
           break;
         }
         tc::tc_fence_after();
+        if (amatch) {
+          // the staged 1/|k| and indices landed with the K tile (kv_full, already complete)
+          if (!wait_all(&sm.kv_full[st], (g / kKS) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          const int64_t left = nkeys - (int64_t)j * kKT;
+          const int vcols = left < kKT ? (int)left : kKT;
+          const int off = (int)((kbase + (int64_t)j * kKT) & 3);
+          const uint8_t* vst = sv + (size_t)st * Lay::kstage;
+          const float* iv = reinterpret_cast<const float*>(vst) + off;
+          const int32_t* jv = reinterpret_cast<const int32_t*>(vst + kMatchAux) + off;
+          const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * kKT);
+          float x[64];
+          tc::tmem_ld32(s_addr, x);
+          tc::tmem_ld32(s_addr + 32, x + 32);
+          tc::tmem_wait_ld();
+          tc::tmem_pin32(x);
+          tc::tmem_pin32(x + 32);
+          // ascending keys: a strict improvement keeps the lowest cache index on ties
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            if (c < vcols) {
+              const float v = x[c] * iv[c];
+              if (v > best) {
+                best = v;
+                bidx = jv[c];
+              }
+            }
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            tc::mbar_arrive(&sm.s_free[st]);
+            tc::mbar_arrive(&sm.kv_empty[st]);
+          }
+          continue;
+        }
         const int64_t left = nkeys - (int64_t)j * kKT;
         const int vcols = left < kKT ? (int)left : kKT;
         const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * kKT);
@@ -761,8 +820,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
       }
       if (!ok) break;
-      sm.mrow[qs][row] = m_used;
-      sm.lrow[qs][row] = l;
+      sm.mrow[qs][row] = amatch ? best : m_used;
+      sm.lrow[qs][row] = amatch ? __int_as_float(bidx) : l;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.ml_full[qs]);
     }
@@ -789,6 +848,17 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       const float m_used = sm.mrow[qs][row], l = sm.lrow[qs][row];
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.dst_free[qs]);
+      if (amatch) {
+        // the row's best scaled score and cache index for its (query, slot) pair
+        if (dst >= 0) {
+          a.mbest[(int64_t)h * np + dst] = m_used;
+          a.midx[(int64_t)h * np + dst] = __float_as_int(l);
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.o_empty[qs]);
+        continue;
+      }
       const uint32_t o_addr = tmem + lane_addr + Lay::o_col + (uint32_t)(qs * 128);
       const bool live = T > 0 && l > 0.f;
       const float inv = live ? 1.0f / l : 0.f;
@@ -1078,6 +1148,196 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------------------
+// ANN-restricted TempCache match (FAST-AR technical summary §2.A: a lightweight ANN search
+// for the temporal correspondence instead of full attention matrices): each query is
+// compared only with the incoming cache's keys in its own buckets.  The attention engine
+// runs in match mode over (head, bucket, 128-pair) items; a finaliser merges the r slots.
+// ---------------------------------------------------------------------------------------
+
+// The incoming cache in bucket order: K rows (bf16, [H, M, d]), 1/|k| and the cache index
+// of every sorted key ([H, mstride]; past the sorted length: zero row, 0, -1).  Also
+// clears the eviction flags.
+template <int D>
+__global__ void __launch_bounds__(256)
+    ann_sort_rows_kernel(const AttnArgs a, const float* __restrict__ knorm, float* inv_sorted, int32_t* j_sorted,
+                         uint4* ks, uint8_t* evict) {
+  constexpr int CPR = D / 8;
+  const uint4* K = static_cast<const uint4*>(a.k);
+  const int64_t total = (int64_t)a.H * a.mstride * CPR;
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < total; g += (int64_t)gridDim.x * 256) {
+    const int64_t row = g / CPR;
+    const int c = (int)(g % CPR);
+    const int h = (int)(row / a.mstride);
+    const int64_t pos = row % a.mstride;
+    int32_t n = a.koff[(int64_t)h * (a.B + 1) + a.B];
+    n = n < 0 ? 0 : (n > a.M ? (int32_t)a.M : n);
+    int s = -1;
+    if (pos < n) {
+      s = a.kperm[(int64_t)h * a.M + pos];
+      if (s < 0 || s >= a.M) {
+        if (c == 0) flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+        s = -1;
+      }
+    }
+    if (pos < a.M) ks[((int64_t)h * a.M + pos) * CPR + c] = s >= 0 ? K[((int64_t)h * a.M + s) * CPR + c] : make_uint4(0, 0, 0, 0);
+    if (c == 0) {
+      const float kn = s >= 0 ? knorm[(int64_t)h * a.M + s] : 0.f;
+      inv_sorted[row] = kn > 0.f ? 1.0f / kn : 0.f;
+      j_sorted[row] = s;
+    }
+  }
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < (int64_t)a.H * a.M; g += (int64_t)gridDim.x * 256)
+    evict[g] = 0;
+}
+
+// Per query (one warp): the best of its r slots — largest q.k/|k|, then lowest cache
+// index — is top1; s1 = that / |q|; the entry is evicted when cos(kcur_i, k_top1) >= tau.
+template <int D>
+__global__ void __launch_bounds__(256)
+    ann_match_finalize_kernel(const AttnArgs a, TokView kcur, const float* __restrict__ knorm, float tau,
+                              int32_t* top1, float* s1, uint8_t* evict) {
+  constexpr int E = D / 32;
+  const int64_t wq = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wq >= (int64_t)a.H * a.nq) return;
+  const int h = (int)(wq / a.nq);
+  const int64_t i = wq % a.nq;
+  const int64_t pb = ((int64_t)h * a.nq + i) * a.r;
+  float b = neg_inf();
+  int j = -1;
+  if (lane < a.r) {
+    j = a.midx[pb + lane];
+    b = j >= 0 ? a.mbest[pb + lane] : neg_inf();
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, b, o);
+    const int oj = __shfl_xor_sync(0xffffffffu, j, o);
+    if (oj >= 0 && (j < 0 || ob > b || (ob == b && oj < j))) {
+      b = ob;
+      j = oj;
+    }
+  }
+  const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q.p) + h * a.q.hs + i * a.q.ts + lane * E;
+  const __nv_bfloat16* Kc = static_cast<const __nv_bfloat16*>(kcur.p) + h * kcur.hs + i * kcur.ts + lane * E;
+  float qq = 0.f, kk = 0.f, dk = 0.f;
+  const bool have = j >= 0 && j < a.M;
+  const __nv_bfloat16* Kj = static_cast<const __nv_bfloat16*>(a.k) + ((int64_t)h * a.M + (have ? j : 0)) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float qv = __bfloat162float(Q[e]);
+    qq = fmaf(qv, qv, qq);
+    if (have) {
+      const float cv = __bfloat162float(Kc[e]), kv = __bfloat162float(Kj[e]);
+      kk = fmaf(cv, cv, kk);
+      dk = fmaf(cv, kv, dk);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+    dk += __shfl_xor_sync(0xffffffffu, dk, o);
+  }
+  if (lane != 0) return;
+  const float nq_ = sqrtf(qq);
+  top1[(int64_t)h * a.nq + i] = have ? j : -1;
+  s1[(int64_t)h * a.nq + i] = have ? (nq_ > 0.f ? b / nq_ : 0.f) : neg_inf();
+  if (have) {
+    const float den = sqrtf(kk) * knorm[(int64_t)h * a.M + j];
+    const float c = den > 0.f ? dk / den : 0.f;
+    if (c >= tau) evict[(int64_t)h * a.M + j] = 1;
+  }
+}
+
+template <int D>
+cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
+                                  const int32_t* qoff, const void* cache_k, const float* cache_knorm, int64_t M,
+                                  const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1, float* s1,
+                                  uint8_t* evict, int32_t* status, void* ws, cudaStream_t s) {
+  AttnArgs a{};
+  a.mode = kMatchAnn;
+  a.H = H;
+  a.q = q;
+  a.nq = nq;
+  a.k = cache_k;
+  a.r = r;
+  a.B = B;
+  a.qperm = qperm;
+  a.qoff = qoff;
+  a.kperm = kperm;
+  a.koff = koff;
+  a.M = M;
+  a.status = status;
+  a.mstride = (M + 80 + 3) & ~(int64_t)3;
+  const int64_t np = nq * r;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.mbest = reinterpret_cast<float*>(w);
+  a.midx = reinterpret_cast<int32_t*>(w + sizeof(float) * (size_t)H * np);
+  size_t at = (2 * sizeof(float) * (size_t)H * np + 15) & ~(size_t)15;
+  a.items = w + at;
+  a.n_items = reinterpret_cast<int32_t*>(w + at + sparse_plan_bytes(H, nq, r, B) - 16);
+  at = (at + sparse_plan_bytes(H, nq, r, B) + 1023) & ~(size_t)1023;
+  uint4* ks = reinterpret_cast<uint4*>(w + at);
+  at += sizeof(uint16_t) * (size_t)H * M * D;
+  float* inv_sorted = reinterpret_cast<float*>(w + at);
+  at += sizeof(float) * (size_t)H * a.mstride;
+  int32_t* j_sorted = reinterpret_cast<int32_t*>(w + at);
+  a.inv_sorted = inv_sorted;
+  a.j_sorted = j_sorted;
+  const int64_t chunks = (int64_t)H * a.mstride * (D / 8);
+  const int64_t blocks = (chunks + 255) / 256;
+  ann_sort_rows_kernel<D><<<(unsigned)(blocks < 8 * sm_count() ? blocks : 8 * sm_count()), 256, 0, s>>>(
+      a, cache_knorm, inv_sorted, j_sorted, ks, evict);
+  count_launches(1);
+  CUtensorMap tk, tz;
+  memset(&tz, 0, sizeof(tz));
+  if (!make_tmap_bf16_3d(&tk, ks, D, (uint64_t)M, (uint64_t)H, (uint64_t)D * 2, (uint64_t)M * D * 2, 64, kKT))
+    return cudaErrorInvalidValue;
+  AttnArgs b = a;
+  b.kv_tma = 1;
+  if ((int64_t)H * B + 1 <= kPrefixMax) {
+    b.items = nullptr;
+  } else {
+    sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+    count_launches(1);
+  }
+  constexpr size_t smem = AttnLayout<D>::bytes;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return attr;
+  const int64_t upper = (int64_t)H * ((np + kAT - 1) / kAT + B);
+  const int grid = (int)(upper < sm_count() ? upper : sm_count());
+  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tz, tz);
+  count_launches(1);
+  const int64_t threads = (int64_t)H * nq * 32;
+  ann_match_finalize_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, kcur, cache_knorm, tau, top1,
+                                                                                   s1, evict);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+size_t match_ann_workspace(int H, int64_t nq, int d, int r, int B, int64_t M) {
+  const int64_t mstride = (M + 80 + 3) & ~(int64_t)3;
+  size_t at = (2 * sizeof(float) * (size_t)H * nq * r + 15) & ~(size_t)15;
+  at = (at + sparse_plan_bytes(H, nq, r, B) + 1023) & ~(size_t)1023;
+  return at + sizeof(uint16_t) * (size_t)H * M * d + 2 * sizeof(float) * (size_t)H * mstride + 1024;
+}
+
+cudaError_t launch_match_ann(int d, TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
+                             const int32_t* qoff, const void* cache_k, const float* cache_knorm,
+                             const int32_t* cache_len, int64_t M, const int32_t* kperm, const int32_t* koff,
+                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* status, void* ws,
+                             cudaStream_t s) {
+  (void)cache_len;   // the incoming cache's bucket order (koff) carries its length
+  if (d == 128)
+    return launch_match_ann_impl<128>(q, kcur, H, nq, r, B, qperm, qoff, cache_k, cache_knorm, M, kperm, koff, tau,
+                                      top1, s1, evict, status, ws, s);
+  return launch_match_ann_impl<64>(q, kcur, H, nq, r, B, qperm, qoff, cache_k, cache_knorm, M, kperm, koff, tau,
+                                   top1, s1, evict, status, ws, s);
+}
 
 size_t sparse_plan_bytes(int H, int64_t nq, int r, int B) {
   const int64_t upper = (int64_t)H * ((nq * r + kAT - 1) / kAT + B);

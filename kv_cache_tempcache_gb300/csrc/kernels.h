@@ -52,7 +52,7 @@ cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M,
                                  cudaStream_t s);
 
 // ---- attention ------------------------------------------------------------------------
-enum AttnMode { kDense = 0, kCross = 1, kSparse = 2 };
+enum AttnMode { kDense = 0, kCross = 1, kSparse = 2, kMatchAnn = 3 };
 
 struct AttnArgs {
   int mode;
@@ -89,11 +89,26 @@ struct AttnArgs {
   int kv_tma;       // keys/values arrive as contiguous TMA tiles (set by the launcher)
   int q_tma;        // so do the query tiles: one thread drives every copy (set by the launcher)
   int q_token_major;  // the query tensor map is (d, H, tokens) rather than (d, tokens, H)
+  // ANN-restricted match: per bucket-ordered key, 1/|k| and its cache index ([H, mstride]);
+  // per (query, slot) pair, the best scaled score and its index
+  const float* inv_sorted;
+  const int32_t* j_sorted;
+  int64_t mstride;
+  float* mbest;
+  int32_t* midx;
   int32_t* n_items; // sparse: its length
   int32_t* status;
 };
 
 size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B, int64_t M);
+// ANN-restricted TempCache match (bf16, tensor cores): workspace and launch.  The pair
+// order (qperm/qoff) and the incoming cache's bucket order (kperm/koff) are inputs.
+size_t match_ann_workspace(int H, int64_t nq, int d, int r, int B, int64_t M);
+cudaError_t launch_match_ann(int d, TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
+                             const int32_t* qoff, const void* cache_k, const float* cache_knorm,
+                             const int32_t* cache_len, int64_t M, const int32_t* kperm, const int32_t* koff,
+                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* status, void* ws,
+                             cudaStream_t s);
 // Bytes of the tensor-core AnnSA work list (inside the sparse workspace).
 size_t sparse_plan_bytes(int H, int64_t nq, int r, int B);
 // Tensor-core attention (bf16); false if it could not be set up (caller falls back).
