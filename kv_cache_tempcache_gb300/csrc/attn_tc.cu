@@ -754,15 +754,14 @@ __global__ void __launch_bounds__(kThreadsA, 1)
           tc::tmem_pin32(x);
           tc::tmem_pin32(x + 32);
           // ascending keys: a strict improvement keeps the lowest cache index on ties
+          // (branch-free: masked columns score -inf, the choice is a select)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            if (c < vcols) {
-              const float v = x[c] * iv[c];
-              if (v > best) {
-                best = v;
-                bidx = jv[c];
-              }
-            }
+            const float v = c < vcols ? x[c] * iv[c] : neg_inf();
+            const int jc = jv[c];
+            const bool gt = v > best;
+            best = gt ? v : best;
+            bidx = gt ? jc : bidx;
           }
           tc::tc_fence_before();
           __syncwarp();
@@ -1225,12 +1224,26 @@ __global__ void __launch_bounds__(256)
   float qq = 0.f, kk = 0.f, dk = 0.f;
   const bool have = j >= 0 && j < a.M;
   const __nv_bfloat16* Kj = static_cast<const __nv_bfloat16*>(a.k) + ((int64_t)h * a.M + (have ? j : 0)) * D + lane * E;
+  __nv_bfloat16 qe[E], ce[E], ke[E];
+  if (E == 4) {
+    *reinterpret_cast<uint2*>(qe) = *reinterpret_cast<const uint2*>(Q);
+    if (have) {
+      *reinterpret_cast<uint2*>(ce) = *reinterpret_cast<const uint2*>(Kc);
+      *reinterpret_cast<uint2*>(ke) = *reinterpret_cast<const uint2*>(Kj);
+    }
+  } else {
+    *reinterpret_cast<uint32_t*>(qe) = *reinterpret_cast<const uint32_t*>(Q);
+    if (have) {
+      *reinterpret_cast<uint32_t*>(ce) = *reinterpret_cast<const uint32_t*>(Kc);
+      *reinterpret_cast<uint32_t*>(ke) = *reinterpret_cast<const uint32_t*>(Kj);
+    }
+  }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const float qv = __bfloat162float(Q[e]);
+    const float qv = __bfloat162float(qe[e]);
     qq = fmaf(qv, qv, qq);
     if (have) {
-      const float cv = __bfloat162float(Kc[e]), kv = __bfloat162float(Kj[e]);
+      const float cv = __bfloat162float(ce[e]), kv = __bfloat162float(ke[e]);
       kk = fmaf(cv, cv, kk);
       dk = fmaf(cv, kv, dk);
     }
@@ -1289,8 +1302,7 @@ cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, in
   a.j_sorted = j_sorted;
   const int64_t chunks = (int64_t)H * a.mstride * (D / 8);
   const int64_t blocks = (chunks + 255) / 256;
-  ann_sort_rows_kernel<D><<<(unsigned)(blocks < 8 * sm_count() ? blocks : 8 * sm_count()), 256, 0, s>>>(
-      a, cache_knorm, inv_sorted, j_sorted, ks, evict);
+  ann_sort_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a, cache_knorm, inv_sorted, j_sorted, ks, evict);
   count_launches(1);
   CUtensorMap tk, tz;
   memset(&tz, 0, sizeof(tz));
