@@ -18,6 +18,9 @@ pages about it:
   * AnnSA (technical summary §2.C; blog §3): reuse the same buckets; each query
     attends only to keys in its own bucket(s).
   * Problem statement: the cache grows with the rollout and is to be bounded.
+  * The merge variant (technical summary §2.A, "Theoretical Basis", Lemma 5.1):
+    identical keys merge with no error when their values are averaged and their
+    logit is shifted by the size of the group.
 The pages leave the ANN method open; the spec that accompanies them fixes it:
 per-head unit centroids, key -> argmax-dot centroid, query -> top-r centroids, ties
 to the lowest index, softmax scale 1/sqrt(d), inclusive thresholds, FIFO cap M.
@@ -213,14 +216,74 @@ def gather_rows(index_map, length: int, old_rows, cur_rows) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------------
+# the merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1)
+# ----------------------------------------------------------------------------------
+# Every cache entry stands for a group of g >= 1 keys.  When current entry i evicts
+# cached entry j (its top-1 match with cos(kcur_i, k_j) >= tau), j is not dropped but
+# folded into i: i's value becomes the mean over both groups and its count their sum;
+# i's key stays (the most recent representative).  Attention gives every entry the
+# logit q.k*scale + ln g.  Readings: a cached entry evicted by several current entries
+# is folded into the lowest such i only (every other i keeps g = 1 and its own value);
+# the FIFO cap drops the oldest entries with their whole groups.
+
+def evict_owner(top1, cos_evict, tau: float, n: int) -> np.ndarray:
+    """owner[j] = the lowest current index i with top1[i] = j and cos_evict[i] >= tau,
+    -1 when no current entry evicts j.  int64 [n].  owner[j] >= 0 iff e_j = 1."""
+    top1 = np.asarray(top1, np.int64)
+    ce = _f64(cos_evict)
+    owner = np.full(n, -1, np.int64)
+    for i in range(top1.shape[0] - 1, -1, -1):     # descending, so the lowest i wins
+        j = int(top1[i])
+        if j >= 0 and ce[i] >= tau:
+            owner[j] = i
+    return owner
+
+
+def merge_current(owner, top1, v_cur, cache_v, g_cache):
+    """Value and count of each current entry after it absorbs the entry it owns.
+
+    For current i, with j = top1[i] if owner[j] == i:
+        g_i = 1 + g_j,   v_i <- (v_i + g_j * v_j) / g_i      (mean over both groups)
+    otherwise g_i = 1 and v_i is unchanged.  Returns (v [nq, dv], g int64 [nq])."""
+    owner = np.asarray(owner, np.int64)
+    top1 = np.asarray(top1, np.int64)
+    v = _f64(v_cur).copy()
+    cv = _f64(cache_v)
+    gc = np.asarray(g_cache, np.int64)
+    g = np.ones(v.shape[0], np.int64)
+    for i in range(v.shape[0]):
+        j = int(top1[i])
+        if j >= 0 and owner[j] == i:
+            g[i] = 1 + gc[j]
+            v[i] = (v[i] + gc[j] * cv[j]) / g[i]
+    return v, g
+
+
+def compact_merge(evict, owner, top1, cache_k, cache_v, g_cache, k_cur, v_cur, M: int):
+    """The merge variant of the compaction: the plan of `compact_plan` (survivors in
+    age order, then the current chunk, oldest dropped past M), with each current
+    entry's value and count taken from `merge_current`.
+    Returns (new_k, new_v, new_g int64, index_map, length)."""
+    n, nq = np.asarray(cache_k).shape[0], np.asarray(k_cur).shape[0]
+    imap, length = compact_plan(evict, n, nq, M)
+    v_m, g_m = merge_current(owner, top1, v_cur, cache_v, g_cache)
+    new_k = gather_rows(imap, length, cache_k, k_cur)
+    new_v = gather_rows(imap, length, _f64(cache_v), v_m)
+    new_g = gather_rows(imap, length, np.asarray(g_cache, np.int64), g_m)
+    return new_k, new_v, new_g, imap, length
+
+
+# ----------------------------------------------------------------------------------
 # attention (AnnSA §2.C, AnnCA §2.B, dense baseline)
 # ----------------------------------------------------------------------------------
 
-def masked_softmax_attention(Q, K, V, allowed, scale: float):
-    """o_i = sum_{s allowed} softmax_s(q_i.k_s * scale) v_s, max-subtracted.
+def masked_softmax_attention(Q, K, V, allowed, scale: float, log_g=None):
+    """o_i = sum_{s allowed} softmax_s(q_i.k_s * scale + log_g[s]) v_s, max-subtracted.
 
-    allowed: bool [nq, nk] (None = all).  A row with nothing allowed gets o = 0 and
-    lse = -inf.  Returns (O [nq, dv], lse [nq]) with lse = log sum exp(scores)."""
+    allowed: bool [nq, nk] (None = all).  log_g: [nk] per-key logit shift (None = 0;
+    the merge variant passes ln g, -inf for an empty group).  A row with nothing
+    allowed gets o = 0 and lse = -inf.  Returns (O [nq, dv], lse [nq]) with
+    lse = log sum exp(logits)."""
     Q = _f64(Q)
     K = _f64(K)
     V = _f64(V)
@@ -233,6 +296,8 @@ def masked_softmax_attention(Q, K, V, allowed, scale: float):
     for a in range(0, nq, step):
         b = min(nq, a + step)
         S = (Q[a:b] @ K.T) * scale
+        if log_g is not None:
+            S = S + _f64(log_g)[None, :]
         if allowed is not None:
             S = np.where(allowed[a:b], S, NEG_INF)
         m = S.max(axis=1)
@@ -246,21 +311,31 @@ def masked_softmax_attention(Q, K, V, allowed, scale: float):
     return O, lse
 
 
-def annsa_attention(Q, R, K, V, kb, scale: float):
+def group_log(g) -> np.ndarray:
+    """ln g per entry of the merge variant (-inf for g = 0: an empty group)."""
+    g = _f64(g)
+    out = np.full(g.shape, NEG_INF)
+    np.log(g, out=out, where=g > 0)
+    return out
+
+
+def annsa_attention(Q, R, K, V, kb, scale: float, g=None):
     """Bucket-restricted self-attention: query i sees the keys s with kb[s] in R(i).
 
     Q [nq, d]; R [nq, r]; K, V [L, d] (the post-compaction cache, which holds the
-    current chunk); kb [L].  Returns (O, lse, n_empty)."""
+    current chunk); kb [L]; g [L] the group counts of the merge variant (None: every
+    entry is one key).  Returns (O, lse, n_empty)."""
     R = np.asarray(R, np.int64)
     kb = np.asarray(kb, np.int64)
     allowed = (kb[None, :, None] == R[:, None, :]).any(axis=2)
-    O, lse = masked_softmax_attention(Q, K, V, allowed, scale)
+    O, lse = masked_softmax_attention(Q, K, V, allowed, scale, None if g is None else group_log(g))
     return O, lse, int((~allowed.any(axis=1)).sum())
 
 
-def dense_attention(Q, K, V, scale: float):
-    """Full softmax attention (the dense baseline)."""
-    return masked_softmax_attention(Q, K, V, None, scale)
+def dense_attention(Q, K, V, scale: float, g=None):
+    """Full softmax attention (the dense baseline); with group counts g, the dense
+    attention over a merged cache."""
+    return masked_softmax_attention(Q, K, V, None, scale, None if g is None else group_log(g))
 
 
 def annca_select(Q, R, Kp, pb, F: int, Tf: int, tau_ca: float, topk: int, gate: bool = True):
@@ -316,13 +391,16 @@ def cross_attention_subset(Q, Kp, Vp, kidx, F: int, Tf: int, scale: float):
 # ----------------------------------------------------------------------------------
 
 def head_step(q, k_cur, v_cur, cache_k, cache_v, C, kp, vp, *, F, Tf, tau, M, r, tau_ca,
-              topk, scale, gate=True, decisions=None):
+              topk, scale, gate=True, decisions=None, merge=False, g_cache=None):
     """The whole per-chunk step for one head.
 
     cache_k/cache_v [n, d]: the cache entering the step, oldest first.
     decisions: optional dict of discrete choices to take instead of the oracle's own
-    (keys 'qb', 'kb_cur', 'kb_cache', 'pb', 'top1', 'evict', 'keep'); the tests use it
-    only with choices they have first checked to be valid alternatives (near-ties).
+    (keys 'qb', 'kb_cur', 'kb_cache', 'pb', 'top1', 'evict', 'owner', 'keep'); the
+    tests use it only with choices they have first checked to be valid alternatives
+    (near-ties).
+    merge: the Lemma 5.1 variant (evicted entries fold into their owner; attention
+    with a ln g logit shift); g_cache [n] the incoming group counts (None: all 1).
     Returns a dict of every intermediate and output.
     """
     dec = decisions or {}
@@ -342,12 +420,21 @@ def head_step(q, k_cur, v_cur, cache_k, cache_v, C, kp, vp, *, F, Tf, tau, M, r,
     evict, cos_evict = evict_flags(top1, k_cur, cache_k, tau)
     if dec.get("evict") is not None:
         evict = np.asarray(dec["evict"], bool)
-    imap, length = compact_plan(evict, n, nq, M)
-    new_k = gather_rows(imap, length, cache_k, k_cur)
-    new_v = gather_rows(imap, length, cache_v, v_cur)
+    owner, new_g = None, None
+    if merge:
+        owner = evict_owner(top1, cos_evict, tau, n)
+        if dec.get("owner") is not None:
+            owner = np.asarray(dec["owner"], np.int64)
+        gc = np.ones(n, np.int64) if g_cache is None else np.asarray(g_cache, np.int64)
+        new_k, new_v, new_g, imap, length = compact_merge(evict, owner, top1, cache_k, cache_v, gc, k_cur,
+                                                          v_cur, M)
+    else:
+        imap, length = compact_plan(evict, n, nq, M)
+        new_k = gather_rows(imap, length, cache_k, k_cur)
+        new_v = gather_rows(imap, length, cache_v, v_cur)
     new_kb = gather_rows(imap, length, kb_cache, kb_cur)
 
-    o_self, lse_self, n_empty = annsa_attention(q, qb, new_k, new_v, new_kb, scale)
+    o_self, lse_self, n_empty = annsa_attention(q, qb, new_k, new_v, new_kb, scale, new_g)
 
     keep, kidx, kcnt, score = annca_select(q, qb, kp, pb, F, Tf, tau_ca, topk, gate)
     if dec.get("keep") is not None:
@@ -357,7 +444,7 @@ def head_step(q, k_cur, v_cur, cache_k, cache_v, C, kp, vp, *, F, Tf, tau, M, r,
     o_cross, lse_cross = cross_attention_subset(q, kp, vp, kidx, F, Tf, scale)
 
     return dict(qb=qb, kb_cur=kb_cur, kb_cache=kb_cache, pb=pb, top1=top1, s1=s1, s2=s2,
-                cos_evict=cos_evict, evict=evict, index_map=imap, length=length,
+                cos_evict=cos_evict, evict=evict, owner=owner, new_g=new_g, index_map=imap, length=length,
                 new_k=new_k, new_v=new_v, new_kb=new_kb, o_self=o_self, lse_self=lse_self,
                 n_empty=n_empty, keep=keep, kidx=kidx, kcnt=kcnt, score=score,
                 o_cross=o_cross, lse_cross=lse_cross)

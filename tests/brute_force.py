@@ -125,3 +125,47 @@ def ann_match(q, R, cache_k, kb):
         top1.append(best_j)
         s1.append(best)
     return top1, s1
+
+
+def merge_step(q, k_cur, v_cur, cache, *, tau, M):
+    """The merge variant of one TempCache step by enumeration.
+
+    cache: list of entries [k, v, g] (oldest first).  Every query is matched over all
+    cached keys (first maximum), an entry is evicted when a query whose top-1 it is
+    has cos(kcur_i, k_j) >= tau, and it is folded into the FIRST such query's entry:
+    that entry's value becomes the count-weighted mean and its count the sum.  The new
+    cache is the survivors then the current entries, oldest dropped past M.
+    Returns (new cache, top1, owner)."""
+    nq, n = len(q), len(cache)
+    top1 = [argmax_first([cos(q[i], cache[j][0]) for j in range(n)]) if n else -1 for i in range(nq)]
+    owner = [-1] * n
+    for i in range(nq):
+        j = top1[i]
+        if j >= 0 and owner[j] < 0 and cos(k_cur[i], cache[j][0]) >= tau:
+            owner[j] = i
+    cur = []
+    for i in range(nq):
+        k, v, g = list(k_cur[i]), [float(x) for x in v_cur[i]], 1
+        j = top1[i]
+        if j >= 0 and owner[j] == i:
+            gj = cache[j][2]
+            v = [(v[c] + gj * float(cache[j][1][c])) / (1 + gj) for c in range(len(v))]
+            g = 1 + gj
+        cur.append([k, v, g])
+    new = [cache[j] for j in range(n) if owner[j] < 0] + cur
+    while len(new) > M:
+        new.pop(0)
+    return new, top1, owner
+
+
+def grouped_attention(qi, entries, scale):
+    """Attention of one query over entries [k, v, g], each weighted by its count:
+    w_s = g_s * exp(q.k_s * scale - m)."""
+    if not entries:
+        return [0.0] * len(qi)
+    sc = [dot(qi, e[0]) * scale for e in entries]
+    m = max(sc)
+    w = [e[2] * math.exp(x - m) for e, x in zip(entries, sc)]
+    z = sum(w)
+    dv = len(entries[0][1])
+    return [sum(w[s] * float(entries[s][1][c]) for s in range(len(entries))) / z for c in range(dv)]
