@@ -12,6 +12,10 @@
  *   6. fastar_annca_select    (frame-relevant prompt tokens)
  *   7. fastar_cross_attn_subset (cross-attention over the kept prompt tokens)
  * and fastar_dense_attn is the dense baseline the speed-up is measured against.
+ * The merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1 — merging
+ * identical keys is exact when their values are averaged and their logit is shifted
+ * by the group size) replaces step 3 with fastar_cache_compact_merge and step 5 with
+ * fastar_sparse_attn_grouped, using the owner output of step 2.
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers unless stated otherwise.  The caller allocates
@@ -132,17 +136,20 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d,
  *   top1[h,i] = argmax_j cos(q_i, k_j)   (lowest j on ties; -1 when n == 0)
  *   s1[h,i], s2[h,i] = best and second-best cosine (-inf when absent)
  *   evict[h, top1] = 1 if cos(kcur_i, k_top1) >= tau (kcur_i = current key i).
+ *   owner[h, j] (optional, int32 [H, M]; NULL to skip) = the lowest i that evicts j,
+ *               -1 where no query evicts j (the merge variant folds j into owner[j]).
  * cos(a,b) = a.b/(|a||b|), 0 on a zero norm.  cache_knorm[h,j] must hold |k_j|
  * (fastar_bucket_assign's norms / fastar_cache_compact maintain it).
  * q and k_cur share (head_stride, token_stride).  evict is [H, M] uint8 and is
- * cleared to 0 inside the call before the flags are set.  s1/s2 may be NULL.
+ * cleared to 0 (owner to -1) inside the call before the flags are set.  s1/s2 may be
+ * NULL.
  * Workspace: fastar_workspace_bytes(FASTAR_OP_MATCH, H, nq, M, d, ...).
  * cache_len values outside [0, M] are clamped and flag FASTAR_DEV_BAD_LEN. */
 int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
                            int64_t head_stride, int64_t token_stride,
                            const void* cache_k, const float* cache_knorm,
                            const int32_t* cache_len, int64_t M, float tau,
-                           int32_t* top1, float* s1, float* s2, uint8_t* evict,
+                           int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* owner,
                            int32_t* dev_status, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
@@ -154,7 +161,8 @@ int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, i
  *   top1[h,i] = argmax_{j < n, kb(k_j) in R(i)} cos(q_i, k_j)  (lowest j on ties;
  *               -1 when no cached key shares a bucket with q_i)
  *   s1[h,i]   = that cosine (-inf when top1 = -1)
- *   evict[h, top1] = 1 if cos(kcur_i, k_top1) >= tau, as in 2 (cleared first).
+ *   evict[h, top1] = 1 if cos(kcur_i, k_top1) >= tau, and owner (optional) as in 2
+ *   (both cleared first).
  * Inputs beyond 2's: the (query, slot) pairs in bucket order (qperm/qoff from
  * fastar_bucket_sort of the query buckets, r per query) and the INCOMING cache's keys
  * in bucket order (kperm/koff from fastar_bucket_sort of its key buckets with
@@ -165,8 +173,8 @@ int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int 
                                const int32_t* qperm, const int32_t* qoff, const void* cache_k,
                                const float* cache_knorm, const int32_t* cache_len, int64_t M,
                                const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1,
-                               float* s1, uint8_t* evict, int32_t* dev_status, void* workspace,
-                               size_t workspace_bytes, cudaStream_t stream);
+                               float* s1, uint8_t* evict, int32_t* owner, int32_t* dev_status,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---- 3. cache compaction -------------------------------------------------------
  * FAST-AR technical summary §2.A ("merging ... bounds the growth of the KV
@@ -190,6 +198,28 @@ int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M,
                          void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
                          int32_t* len_out, int32_t* index_map, int32_t* dev_status,
                          cudaStream_t stream);
+
+/* ---- 3b. cache compaction, merge variant ----------------------------------------
+ * FAST-AR technical summary §2.A, Theoretical Basis (Lemma 5.1): identical keys merge
+ * with no error when their values are averaged and the logit is shifted by the group
+ * size.  Every entry carries a group count g (int32 [H, M], >= 0; a fresh entry is 1).
+ * The slot order, lengths, index_map, keys, norms and buckets are those of
+ * fastar_cache_compact with the same evict flags.  In addition, current entry i that
+ * owns an evicted entry j (owner[h, j] == i from fastar_tempcache_match, j = top1[h, i])
+ * takes the group: its value becomes (v_i + g_j v_j) / (1 + g_j) (fp32 arithmetic,
+ * rounded once to dtype) and its count 1 + g_j; its key stays k_i.  Other current
+ * entries get g = 1 and their own value; survivors keep theirs.  g_out [H, M] is
+ * written for slots below len_out.  A negative g_j flags FASTAR_DEV_BAD_INDEX and
+ * counts as 0.  Out-of-place like 3 (g_in and g_out must differ). */
+int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M,
+                               const void* k_cur, const void* v_cur, int64_t head_stride,
+                               int64_t token_stride, const float* kcur_norm, const int32_t* kcur_bucket,
+                               const void* k_in, const void* v_in, const float* knorm_in,
+                               const int32_t* kb_in, const int32_t* g_in, const int32_t* len_in,
+                               const uint8_t* evict, const int32_t* top1, const int32_t* owner,
+                               void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
+                               int32_t* g_out, int32_t* len_out, int32_t* index_map,
+                               int32_t* dev_status, cudaStream_t stream);
 
 /* ---- 4. counting sort by bucket --------------------------------------------------
  * Groups tokens by ANN bucket so that bucket-restricted attention runs on dense
@@ -223,6 +253,21 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d,
                        void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
                        int32_t* dev_status, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/* ---- 5b. bucket-restricted self-attention over grouped keys (merge variant) ---------
+ * As 5, with group counts group_count int32 [H, M] (per cache slot, from
+ * fastar_cache_compact_merge): every key's logit is shifted by ln g,
+ *   O[h,i] = sum_s g_s exp(q_i.k_s*scale) v_s / sum_s g_s exp(q_i.k_s*scale)
+ * over the same key sets; lse includes the shifts.  A key with g = 0 is an empty group
+ * (weight 0); a negative g flags FASTAR_DEV_BAD_INDEX and counts as 0.  Same workspace. */
+int fastar_sparse_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d,
+                               int64_t q_head_stride, int64_t q_token_stride, int r, int B,
+                               const int32_t* qperm, const int32_t* qoff,
+                               const void* k, const void* v, int64_t M,
+                               const int32_t* kperm, const int32_t* koff, const int32_t* group_count,
+                               float scale, void* out, int64_t o_head_stride, int64_t o_token_stride,
+                               float* lse, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
 /* ---- 6. AnnCA prompt selection ---------------------------------------------------
  * FAST-AR technical summary §2.B and blog §2: keep the prompt tokens that share
@@ -293,6 +338,18 @@ int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d,
                       int64_t kv_head_stride, int64_t kv_token_stride, float scale,
                       void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
                       cudaStream_t stream);
+
+/* ---- 8b. dense attention over grouped keys (merge variant) ----------------------------
+ * As 8, with the count of key j of head h at group_count[h * g_head_stride + j]
+ * (g_head_stride >= nk when H > 1): logits shifted by ln g, as in 5b.  Dense attention
+ * over a merged cache; with g = 1 everywhere it equals 8. */
+int fastar_dense_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d,
+                              int64_t q_head_stride, int64_t q_token_stride,
+                              const void* k, const void* v, int64_t nk,
+                              int64_t kv_head_stride, int64_t kv_token_stride,
+                              const int32_t* group_count, int64_t g_head_stride, float scale,
+                              void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                              cudaStream_t stream);
 
 /* Appends nq rows of k_cur/v_cur to an append-only dense cache [H, cap, d] at row
  * `at` (the dense baseline's growing cache).  Requires at + nq <= cap. */

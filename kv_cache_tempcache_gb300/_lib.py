@@ -35,20 +35,25 @@ _SIGS = {
     "fastar_status_string": [_I],
     "fastar_workspace_bytes": [_I, _I, _L, _L, _I, _I, _I, _L, _I],
     "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
-    "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _S,
-                               _P],
+    "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _P,
+                               _S, _P],
     "fastar_tempcache_match_ann": [_P, _P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _F, _P,
-                                   _P, _P, _P, _P, _S, _P],
+                                   _P, _P, _P, _P, _P, _S, _P],
     "fastar_cache_compact": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P],
+    "fastar_cache_compact_merge": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
     "fastar_sparse_attn": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P,
                            _P, _S, _P],
+    "fastar_sparse_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _F, _P, _L,
+                                   _L, _P, _P, _P, _S, _P],
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
                             _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
     "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
+    "fastar_dense_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _P, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
 }
 _RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
@@ -156,26 +161,26 @@ def fastar_bucket_assign(x, centroids, r, ids, scores=None, norms=None, stream=N
 
 
 def fastar_tempcache_match(q, k_cur, cache_k, cache_knorm, cache_len, tau, top1, s1, s2, evict, dev_status,
-                           workspace, stream=None):
+                           workspace, stream=None, owner=None):
     H, nq, d = q.shape
     hs, ts = tok_strides(q)
     if tok_strides(k_cur) != (hs, ts):
         raise ValueError("q and k_cur must share strides")
     _call("fastar_tempcache_match", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, nq, d, hs, ts, ptr(cache_k),
           ptr(cache_knorm), ptr(cache_len), cache_k.shape[1], float(tau), ptr(top1), ptr(s1), ptr(s2), ptr(evict),
-          ptr(dev_status), ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
-          stream_handle(stream))
+          ptr(owner), ptr(dev_status), ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
 def fastar_tempcache_match_ann(q, k_cur, r, B, qperm, qoff, cache_k, cache_knorm, cache_len, kperm, koff, tau,
-                               top1, s1, evict, dev_status, workspace, stream=None):
+                               top1, s1, evict, dev_status, workspace, stream=None, owner=None):
     H, nq, d = q.shape
     hs, ts = tok_strides(q)
     if tok_strides(k_cur) != (hs, ts):
         raise ValueError("q and k_cur must share strides")
     _call("fastar_tempcache_match_ann", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, nq, d, hs, ts, int(r), int(B),
           ptr(qperm), ptr(qoff), ptr(cache_k), ptr(cache_knorm), ptr(cache_len), cache_k.shape[1], ptr(kperm),
-          ptr(koff), float(tau), ptr(top1), ptr(s1), ptr(evict), ptr(dev_status), ptr(workspace),
+          ptr(koff), float(tau), ptr(top1), ptr(s1), ptr(evict), ptr(owner), ptr(dev_status), ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
@@ -189,6 +194,19 @@ def fastar_cache_compact(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm
           ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(len_in),
           ptr(evict), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out), ptr(len_out), ptr(index_map),
           ptr(dev_status), stream_handle(stream))
+
+
+def fastar_cache_compact_merge(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, g_in, len_in,
+                               evict, top1, owner, k_out, v_out, knorm_out, kb_out, g_out, len_out, index_map,
+                               dev_status, stream=None):
+    H, nq, d = k_cur.shape
+    hs, ts = tok_strides(k_cur)
+    if tok_strides(v_cur) != (hs, ts):
+        raise ValueError("k_cur and v_cur must share strides")
+    _call("fastar_cache_compact_merge", dtype_code(k_cur.dtype), H, nq, d, k_in.shape[1], ptr(k_cur), ptr(v_cur),
+          hs, ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(g_in),
+          ptr(len_in), ptr(evict), ptr(top1), ptr(owner), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out),
+          ptr(g_out), ptr(len_out), ptr(index_map), ptr(dev_status), stream_handle(stream))
 
 
 def fastar_bucket_sort(ids, B, perm, offsets, n_valid=None, dev_status=None, stream=None):
@@ -206,6 +224,17 @@ def fastar_sparse_attn(q, r, B, qperm, qoff, k, v, kperm, koff, scale, out, lse,
           ptr(v), k.shape[1], ptr(kperm), ptr(koff), float(scale), ptr(out), oh, ot, ptr(lse), ptr(dev_status),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))
+
+
+def fastar_sparse_attn_grouped(q, r, B, qperm, qoff, k, v, kperm, koff, group_count, scale, out, lse, dev_status,
+                               workspace, stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    oh, ot = tok_strides(out)
+    _call("fastar_sparse_attn_grouped", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, r, B, ptr(qperm), ptr(qoff),
+          ptr(k), ptr(v), k.shape[1], ptr(kperm), ptr(koff), ptr(group_count), float(scale), ptr(out), oh, ot,
+          ptr(lse), ptr(dev_status), ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
 def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, score=None, workspace=None,
@@ -246,6 +275,17 @@ def fastar_dense_attn(q, k, v, nk, scale, out, lse=None, stream=None):
     oh, ot = tok_strides(out)
     _call("fastar_dense_attn", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, ptr(k), ptr(v), int(nk), kh, kt,
           float(scale), ptr(out), oh, ot, ptr(lse), stream_handle(stream))
+
+
+def fastar_dense_attn_grouped(q, k, v, nk, group_count, scale, out, lse=None, stream=None):
+    """group_count: [H, >= nk] int32 (row stride = its second dimension)."""
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    kh, kt = tok_strides(k)
+    oh, ot = tok_strides(out)
+    _call("fastar_dense_attn_grouped", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, ptr(k), ptr(v), int(nk), kh,
+          kt, ptr(group_count), group_count.shape[1], float(scale), ptr(out), oh, ot, ptr(lse),
+          stream_handle(stream))
 
 
 def fastar_dense_append(k_cur, v_cur, k_cache, v_cache, at, stream=None):

@@ -47,7 +47,7 @@ int cuda_rc(cudaError_t e) {
 
 extern "C" {
 
-int fastar_version(void) { return 100; }
+int fastar_version(void) { return 110; }
 
 const char* fastar_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
@@ -97,8 +97,8 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d, int6
 int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
                            int64_t head_stride, int64_t token_stride, const void* cache_k,
                            const float* cache_knorm, const int32_t* cache_len, int64_t M, float tau,
-                           int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* dev_status,
-                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                           int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* owner,
+                           int32_t* dev_status, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || nq > INT32_MAX) return FASTAR_EINVAL;
@@ -113,7 +113,7 @@ int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, i
   }
   return cuda_rc(fastar::launch_tempcache_match(
       dtype, d, TokView{q, head_stride, token_stride}, TokView{k_cur, head_stride, token_stride}, H, nq,
-      cache_k, cache_knorm, cache_len, M, tau, top1, s1, s2, evict, dev_status, workspace, stream));
+      cache_k, cache_knorm, cache_len, M, tau, top1, s1, s2, evict, owner, dev_status, workspace, stream));
 }
 
 int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
@@ -121,7 +121,7 @@ int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int 
                                const int32_t* qperm, const int32_t* qoff, const void* cache_k,
                                const float* cache_knorm, const int32_t* cache_len, int64_t M,
                                const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1,
-                               float* s1, uint8_t* evict, int32_t* dev_status, void* workspace,
+                               float* s1, uint8_t* evict, int32_t* owner, int32_t* dev_status, void* workspace,
                                size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
@@ -137,11 +137,16 @@ int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int 
   if (nq > 0 && (!top1 || !s1)) return FASTAR_EINVAL;
   const size_t need = fastar::match_ann_workspace(H, nq, d, r, B, M);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
-  if (nq == 0) return FASTAR_OK;
+  if (nq == 0) {
+    // no current entries: nothing is matched or evicted
+    cudaError_t e = cudaMemsetAsync(evict, 0, (size_t)H * M, stream);
+    if (e == cudaSuccess && owner) e = cudaMemsetAsync(owner, 0xff, sizeof(int32_t) * (size_t)H * M, stream);
+    return cuda_rc(e);
+  }
   return cuda_rc(fastar::launch_match_ann(d, TokView{q, head_stride, token_stride},
                                           TokView{k_cur, head_stride, token_stride}, H, nq, r, B, qperm, qoff,
                                           cache_k, cache_knorm, cache_len, M, kperm, koff, tau, top1, s1, evict,
-                                          dev_status, workspace, stream));
+                                          owner, dev_status, workspace, stream));
 }
 
 int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
@@ -168,7 +173,37 @@ int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M, const v
   return cuda_rc(fastar::launch_cache_compact(
       dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
       kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
-      len_out, index_map, dev_status, stream));
+      len_out, index_map, dev_status, nullptr, nullptr, nullptr, nullptr, stream));
+}
+
+int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
+                               const void* v_cur, int64_t head_stride, int64_t token_stride,
+                               const float* kcur_norm, const int32_t* kcur_bucket, const void* k_in,
+                               const void* v_in, const float* knorm_in, const int32_t* kb_in,
+                               const int32_t* g_in, const int32_t* len_in, const uint8_t* evict,
+                               const int32_t* top1, const int32_t* owner, void* k_out, void* v_out,
+                               float* knorm_out, int32_t* kb_out, int32_t* g_out, int32_t* len_out,
+                               int32_t* index_map, int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX) return FASTAR_EINVAL;
+  if (M < nq) return FASTAR_ECAPACITY;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(v_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (nq > 0 && (!kcur_norm || !kcur_bucket || !top1)) return FASTAR_EINVAL;
+  const void* ptrs[] = {k_in, v_in, k_out, v_out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return FASTAR_EINVAL;
+  if (!knorm_in || !kb_in || !g_in || !len_in || !evict || !owner || !knorm_out || !kb_out || !g_out || !len_out ||
+      !index_map)
+    return FASTAR_EINVAL;
+  if (k_in == k_out || v_in == v_out || knorm_in == knorm_out || kb_in == kb_out || g_in == g_out)
+    return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_cache_compact(
+      dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
+      kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
+      len_out, index_map, dev_status, top1, owner, g_in, g_out, stream));
 }
 
 int fastar_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B, const int32_t* n_valid,
@@ -180,11 +215,16 @@ int fastar_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B, const
   return cuda_rc(fastar::launch_bucket_sort(ids, H, n, r, B, n_valid, perm, offsets, dev_status, stream));
 }
 
-int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
-                       int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
-                       const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
-                       float scale, void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
-                       int32_t* dev_status, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int sparse_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                     int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
+                     const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
+                     const int32_t* group_count, float scale, void* out, int64_t o_head_stride,
+                     int64_t o_token_stride, float* lse, int32_t* dev_status, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || nq < 0 || M < 1 || r < 1 || B < 1 || M > INT32_MAX) return FASTAR_EINVAL;
@@ -226,9 +266,43 @@ int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64
     uint8_t* ks = reinterpret_cast<uint8_t*>((kat + 1023) & ~static_cast<uintptr_t>(1023));
     a.ksorted = ks;
     a.vsorted = ks + sizeof(uint16_t) * (size_t)H * M * d;
+    a.lg_sorted = reinterpret_cast<float*>(ks + 2 * sizeof(uint16_t) * (size_t)H * M * d);
   }
+  a.gcount = group_count;
+  a.gc_hs = M;
   a.status = dev_status;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
+}
+
+int dense_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride, int64_t q_token_stride,
+                    const void* k, const void* v, int64_t nk, int64_t kv_head_stride, int64_t kv_token_stride,
+                    const int32_t* group_count, int64_t g_head_stride, float scale, void* out, int64_t o_head_stride,
+                    int64_t o_token_stride, float* lse, cudaStream_t stream);
+
+}  // namespace
+
+extern "C" {
+
+int fastar_sparse_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                       int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
+                       const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
+                       float scale, void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return sparse_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, r, B, qperm, qoff, k, v, M, kperm, koff,
+                          nullptr, scale, out, o_head_stride, o_token_stride, lse, dev_status, workspace,
+                          workspace_bytes, stream);
+}
+
+int fastar_sparse_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                               int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
+                               const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
+                               const int32_t* group_count, float scale, void* out, int64_t o_head_stride,
+                               int64_t o_token_stride, float* lse, int32_t* dev_status, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  if (!group_count) return FASTAR_EINVAL;
+  return sparse_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, r, B, qperm, qoff, k, v, M, kperm, koff,
+                          group_count, scale, out, o_head_stride, o_token_stride, lse, dev_status, workspace,
+                          workspace_bytes, stream);
 }
 
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
@@ -295,6 +369,29 @@ int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_
                       int64_t q_token_stride, const void* k, const void* v, int64_t nk, int64_t kv_head_stride,
                       int64_t kv_token_stride, float scale, void* out, int64_t o_head_stride,
                       int64_t o_token_stride, float* lse, cudaStream_t stream) {
+  return dense_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, k, v, nk, kv_head_stride,
+                         kv_token_stride, nullptr, 0, scale, out, o_head_stride, o_token_stride, lse, stream);
+}
+
+int fastar_dense_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                              int64_t q_token_stride, const void* k, const void* v, int64_t nk,
+                              int64_t kv_head_stride, int64_t kv_token_stride, const int32_t* group_count,
+                              int64_t g_head_stride, float scale, void* out, int64_t o_head_stride,
+                              int64_t o_token_stride, float* lse, cudaStream_t stream) {
+  if (!group_count || g_head_stride < 0 || (H > 1 && g_head_stride < nk)) return FASTAR_EINVAL;
+  return dense_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, k, v, nk, kv_head_stride,
+                         kv_token_stride, group_count, g_head_stride, scale, out, o_head_stride, o_token_stride, lse,
+                         stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int dense_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride, int64_t q_token_stride,
+                    const void* k, const void* v, int64_t nk, int64_t kv_head_stride, int64_t kv_token_stride,
+                    const int32_t* group_count, int64_t g_head_stride, float scale, void* out, int64_t o_head_stride,
+                    int64_t o_token_stride, float* lse, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || nq < 0 || nk < 0 || nq > INT32_MAX) return FASTAR_EINVAL;
@@ -319,8 +416,14 @@ int fastar_dense_attn(const void* q, int dtype, int H, int64_t nq, int d, int64_
   a.o_hs = o_head_stride;
   a.o_ts = o_token_stride;
   a.lse = lse;
+  a.gcount = group_count;
+  a.gc_hs = g_head_stride;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
 }
+
+}  // namespace
+
+extern "C" {
 
 int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,
                         int64_t head_stride, int64_t token_stride, void* k_cache, void* v_cache, int64_t cap,

@@ -10,7 +10,9 @@
 //            against the cache keys of bucket b; one partial (o, lse) per pair,
 //            merged over the r slots afterwards (the slots' key sets are disjoint
 //            because every key has exactly one bucket, so the merge is exact).
-// Online softmax over 64-key tiles with running max and sum in fp32.
+// Online softmax over 64-key tiles with running max and sum in fp32.  With group counts
+// (the merge variant, technical summary §2.A, Lemma 5.1) every key's logit is shifted
+// by ln g.
 #include <climits>
 
 #include "common.cuh"
@@ -23,7 +25,7 @@ constexpr int kAK = 64;
 
 template <int D>
 __host__ __device__ constexpr size_t attn_simt_smem() {
-  return sizeof(float) * ((size_t)D * kAQ + (size_t)D * kAK + (size_t)kAK * D + (size_t)kAQ * kAK) +
+  return sizeof(float) * ((size_t)D * kAQ + (size_t)D * kAK + (size_t)kAK * D + (size_t)kAQ * kAK + kAK) +
          sizeof(int64_t) * (kAQ + kAK) + sizeof(int) * (kAQ + FASTAR_MAX_B + 8);
 }
 
@@ -39,6 +41,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnArgs a) {
   int* qdst = reinterpret_cast<int*>(koffs + kAK);               // [kAQ] output row id or -1
   int* pre = qdst + kAQ;                                         // [B + 1] tile prefix (sparse)
   int* info = pre + FASTAR_MAX_B + 1;                            // misc
+  float* kbias = reinterpret_cast<float*>(info + 7);             // [kAK] ln g per key (merge variant)
 
   const int tid = threadIdx.x;
   const int h = blockIdx.y;
@@ -153,20 +156,28 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnArgs a) {
     for (int col = tid; col < kAK; col += blockDim.x) {
       const int64_t u = u0 + col;
       int64_t off = -1;
+      int32_t gk = 1;
       if (u < nkeys) {
         if (a.mode == kSparse) {
           const int s = a.kperm[(int64_t)h * a.M + kbase + u];
-          if (s >= 0 && s < a.M) off = ((int64_t)h * a.M + s) * D;
-          else flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+          if (s >= 0 && s < a.M) {
+            off = ((int64_t)h * a.M + s) * D;
+            if (a.gcount) gk = a.gcount[(int64_t)h * a.M + s];
+          } else {
+            flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+          }
         } else if (a.mode == kCross) {
           const int p = a.kidx[((int64_t)h * a.F + blockIdx.z) * a.P + u];
           if (p >= 0 && p < a.P) off = ((int64_t)h * a.P + p) * D;
           else flag_status(a.status, FASTAR_DEV_BAD_INDEX);
         } else {
           off = h * a.kv_hs + u * a.kv_ts;
+          if (a.gcount) gk = a.gcount[(int64_t)h * a.gc_hs + u];
         }
       }
       koffs[col] = off;
+      if (gk < 0) flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      kbias[col] = gk > 0 ? logf((float)gk) : neg_inf();
     }
     __syncthreads();
     for (int idx = tid; idx < kAK * (D / 8); idx += blockDim.x) {
@@ -207,7 +218,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnArgs a) {
       float mx = neg_inf();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        s[r][c] = koffs[tx * 4 + c] >= 0 ? s[r][c] * a.scale : neg_inf();
+        s[r][c] = koffs[tx * 4 + c] >= 0 ? fmaf(s[r][c], a.scale, kbias[tx * 4 + c]) : neg_inf();
         mx = fmaxf(mx, s[r][c]);
       }
 #pragma unroll
@@ -299,10 +310,11 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
 size_t sparse_attn_workspace(int H, int64_t nq, int d, int r, int B, int64_t M) {
   // fp32 partials (o, lse) per (query, slot); then (16-byte aligned) the tensor-core
   // path's work list and its length; then (1024-byte aligned) its bucket-ordered copy
-  // of the cache K and V (bf16)
+  // of the cache K and V (bf16) and of the keys' log2 group counts (float)
   const size_t head = sizeof(float) * (size_t)H * nq * r * (d + 1);
   const size_t plan = ((head + 15) & ~(size_t)15) + sparse_plan_bytes(H, nq, r, B);
-  return ((plan + 1023) & ~(size_t)1023) + 2 * sizeof(uint16_t) * (size_t)H * M * d + 1024;
+  return ((plan + 1023) & ~(size_t)1023) + 2 * sizeof(uint16_t) * (size_t)H * M * d + sizeof(float) * (size_t)H * M +
+         1024;
 }
 
 template <typename T, int D>

@@ -67,7 +67,10 @@ struct ItemInfo {
 
 struct AttnCtl {
   int64_t qsrc[2][kAT];   // loader-private: source offset of each query row, per Q stage
-  int64_t ksrc[kKS][kKT]; // loader-private: source offset of each key row, per K/V stage
+  union {
+    int64_t ksrc[kKS][kKT]; // row gathers, loader-private: source offset of each key row, per stage
+    float kbias[kKS][kKT];  // tensor-engine K/V with group counts: log2 g of each key, per stage
+  };
   int qdst[2][kAT];       // output row of each query row (-1: none), per Q stage
   float mrow[2][kAT], lrow[2][kAT];   // softmax max (log2 units) and sum, per Q stage
   int edst[kAT];          // epilogue-private: output row of each row of the item being stored
@@ -123,6 +126,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The logit shift of a key that stands for a group of g keys, in log2 units (the merge
+// variant, Lemma 5.1): log2 g; an empty group (g = 0) gets -inf, a negative count is a
+// bad input (flagged) and counts as empty.
+__device__ __forceinline__ float group_log2(int32_t g, int32_t* status) {
+  if (g < 0) flag_status(status, FASTAR_DEV_BAD_INDEX);
+  return g > 0 ? log2f((float)g) : neg_inf();
+}
+
 // Three-input maximum (PTX max.f32 with three sources).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float y;
@@ -145,10 +156,11 @@ __device__ __forceinline__ float max32(const float* v, int valid) {
   return max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(max3(t[6], t[7], t[8]), t[9], t[10]));
 }
 
-// Softmax pass 1 over one kKT-column S row in TMEM: the raw row maximum (scores not yet
-// scaled), 64 columns per TMEM round trip.
-template <bool kFull>
-__device__ __forceinline__ float row_max(uint32_t s_addr, int vcols) {
+// Softmax pass 1 over one kKT-column S row in TMEM, 64 columns per TMEM round trip: the
+// raw row maximum (scores not yet scaled); with kBias, the maximum of the shifted logits
+// s * sl2 + bias[c] (log2 units).
+template <bool kFull, bool kBias = false>
+__device__ __forceinline__ float row_max(uint32_t s_addr, int vcols, float sl2 = 0.f, const float* bias = nullptr) {
   float m = neg_inf();
 #pragma unroll 1
   for (int hh = 0; hh < kKT / 64; ++hh) {
@@ -158,15 +170,26 @@ __device__ __forceinline__ float row_max(uint32_t s_addr, int vcols) {
     tc::tmem_wait_ld();
     tc::tmem_pin32(x);
     tc::tmem_pin32(x + 32);
+    if (kBias) {
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 b = *reinterpret_cast<const float4*>(bias + hh * 64 + c);
+        x[c] = fmaf(x[c], sl2, b.x);
+        x[c + 1] = fmaf(x[c + 1], sl2, b.y);
+        x[c + 2] = fmaf(x[c + 2], sl2, b.z);
+        x[c + 3] = fmaf(x[c + 3], sl2, b.w);
+      }
+    }
     m = max3(m, max32<kFull>(x, vcols - hh * 64), max32<kFull>(x + 32, vcols - hh * 64 - 32));
   }
   return m;
 }
 
-// Softmax pass 2: P = 2^(s * sl2 - m) as bf16 into this thread's row of the P tile
-// (128-byte swizzled, one block per 64 columns); returns the row sum of P.
-template <bool kFull>
-__device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, uint8_t* pst, int row) {
+// Softmax pass 2: P = 2^(s * sl2 + bias - m) as bf16 into this thread's row of the P
+// tile (128-byte swizzled, one block per 64 columns); returns the row sum of P.
+template <bool kFull, bool kBias = false>
+__device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, uint8_t* pst, int row,
+                                         const float* bias = nullptr) {
   const float nm = m == neg_inf() ? 0.f : -m;
   float xa[32], xb[32];
   float s0 = 0.f, s1 = 0.f;
@@ -181,7 +204,13 @@ __device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, 
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-      float a0 = fmaf(cur[i], sl2, nm), a1 = fmaf(cur[i + 1], sl2, nm);
+      float b0 = nm, b1 = nm;
+      if (kBias) {
+        const float2 b = *reinterpret_cast<const float2*>(bias + c * 32 + i);
+        b0 = b.x + nm;
+        b1 = b.y + nm;
+      }
+      float a0 = fmaf(cur[i], sl2, b0), a1 = fmaf(cur[i + 1], sl2, b1);
       if (!kFull) {
         a0 = c * 32 + i < vcols ? a0 : neg_inf();
         a1 = c * 32 + i + 1 < vcols ? a1 : neg_inf();
@@ -321,6 +350,15 @@ __device__ __forceinline__ int64_t key_offset(const AttnArgs& a, const ItemInfo&
   return it.h * a.kv_hs + u * a.kv_ts;
 }
 
+// The logit shift (log2 units) of key u of the item's key list when keys stand for
+// groups (the merge variant): AnnSA reads the bucket-ordered copy the sort kernel wrote,
+// the dense path the caller's counts; 0 past the list (those columns are masked).
+__device__ __forceinline__ float key_bias(const AttnArgs& a, const ItemInfo& it, int64_t u) {
+  if (u >= it.nkeys) return 0.f;
+  if (a.mode == kSparse) return a.lg_sorted[(int64_t)it.h * a.M + it.kbase + u];
+  return group_log2(a.gcount[(int64_t)it.h * a.gc_hs + u], a.status);
+}
+
 // Query row `pos` of item `it` (valid below q1): its source offset and output row
 // (sparse: the (query, slot) pair index; otherwise the token row), or -1 for none.
 __device__ __forceinline__ void query_row(const AttnArgs& a, const ItemInfo& it, int64_t pos, int64_t q1,
@@ -385,7 +423,7 @@ struct Pending {
   }
 };
 
-template <int D>
+template <int D, bool kGrouped>
 __global__ void __launch_bounds__(kThreadsA, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_q) {
@@ -475,6 +513,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
   const bool amatch = a.mode == kMatchAnn;   // arg-max of cosines instead of softmax.V
+  constexpr bool grouped = kGrouped;  // keys stand for groups: logit shift log2 g per key
 
   if (warp < 4 && a.q_tma) {
     // ---------------- tensor-engine loads (thread 0 issues every copy) ----------------
@@ -499,27 +538,45 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (t == 0) sm.info[qs] = it;
       }
       if (!tc::named_bar_and(1, 128, got && tiles_ok)) break;
-      if (t == 0) {
-        tc::mbar_arrive_tx(&sm.q_full[qs], (uint32_t)Lay::qstage);
-        for (int kh = 0; kh < D / 64; ++kh) {
-          uint8_t* dq = sq + (size_t)qs * Lay::qstage + kh * kBlkA;
-          if (!a.q_token_major)
-            tc::tma_load_3d(dq, &tm_q, kh * 64, (int)q0, it.h, &sm.q_full[qs]);
-          else
-            tc::tma_load_3d(dq, &tm_q, kh * 64, it.h, (int)q0, &sm.q_full[qs]);
+      if (t < 32) {
+        if (t == 0) {
+          tc::mbar_arrive_tx(&sm.q_full[qs], (uint32_t)Lay::qstage);
+          for (int kh = 0; kh < D / 64; ++kh) {
+            uint8_t* dq = sq + (size_t)qs * Lay::qstage + kh * kBlkA;
+            if (!a.q_token_major)
+              tc::tma_load_3d(dq, &tm_q, kh * 64, (int)q0, it.h, &sm.q_full[qs]);
+            else
+              tc::tma_load_3d(dq, &tm_q, kh * 64, it.h, (int)q0, &sm.q_full[qs]);
+          }
         }
+        // warp 0: lane 0 issues the K/V copies; with group counts every lane also stages
+        // two keys' logit shifts, written before lane 0's arrival publishes the stage
         for (int j = 0; j < it.T; ++j) {
           const int st = (g + j) % kKS;
           const uint32_t ph = ((g + j) / kKS) & 1;
-          if (!tc::mbar_wait(&sm.kv_empty[st], ph ^ 1, abort)) {
+          float b0 = 0.f, b1 = 0.f;
+          if (grouped) {
+            b0 = key_bias(a, it, (int64_t)j * kKT + t);
+            b1 = key_bias(a, it, (int64_t)j * kKT + t + 32);
+          }
+          bool fr = true;
+          if (t == 0 || grouped) fr = tc::mbar_wait(&sm.kv_empty[st], ph ^ 1, abort);
+          if (!__all_sync(0xffffffffu, fr)) {
             tiles_ok = false;
             break;
           }
-          const int y = (int)(it.kbase + (int64_t)j * kKT);
-          tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
-          for (int kh = 0; kh < D / 64; ++kh) {
-            tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
-            tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+          if (grouped) {
+            sm.kbias[st][t] = b0;
+            sm.kbias[st][t + 32] = b1;
+            __syncwarp();
+          }
+          if (t == 0) {
+            const int y = (int)(it.kbase + (int64_t)j * kKT);
+            tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
+            for (int kh = 0; kh < D / 64; ++kh) {
+              tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
+              tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+            }
           }
         }
       }
@@ -586,7 +643,30 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (a.kv_tma) {
           // one thread brings the K and V tiles (contiguous rows) with the tensor engine
           bool free = true;
-          if (t == 0) {
+          if (grouped) {
+            // warp 0 stages the tile's logit shifts (loaded before the wait), then lane 0
+            // issues the copies; nothing of this thread's is in flight (Q was signalled)
+            if (t < 32) {
+              const float b0 = key_bias(a, it, (int64_t)j * kKT + t);
+              const float b1 = key_bias(a, it, (int64_t)j * kKT + t + 32);
+              free = __all_sync(0xffffffffu, tc::mbar_wait(&sm.kv_empty[st], ph ^ 1, abort));
+              if (free) {
+                sm.kbias[st][t] = b0;
+                sm.kbias[st][t + 32] = b1;
+                __syncwarp();
+                if (t == 0) {
+                  const int y = (int)(it.kbase + (int64_t)j * kKT);
+                  tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
+                  for (int kh = 0; kh < D / 64; ++kh) {
+                    tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h,
+                                    &sm.kv_full[st]);
+                    tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h,
+                                    &sm.kv_full[st]);
+                  }
+                }
+              }
+            }
+          } else if (t == 0) {
             free = pend.acquire(&sm.kv_empty[st], ph ^ 1, abort);
             if (free) {
               const int y = (int)(it.kbase + (int64_t)j * kKT);
@@ -774,11 +854,22 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const int64_t left = nkeys - (int64_t)j * kKT;
         const int vcols = left < kKT ? (int)left : kKT;
         const uint32_t s_addr = tmem + lane_addr + Lay::s_col + (uint32_t)(st * kKT);
-        // pass 1: the row maximum (the scale is positive, so the maximum of the scaled
-        // scores is the scaled maximum, exactly)
         const bool full = vcols == kKT;
-        const float mr = full ? row_max<true>(s_addr, vcols) : row_max<false>(s_addr, vcols);
-        const float mt = mr * sl2;
+        const float* bias = sm.kbias[st];
+        // group counts: the staged shifts were published with the K/V tile (kv_full)
+        if (grouped && !wait_all(&sm.kv_full[st], (g / kKS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        // pass 1: the row maximum (the scale is positive, so the maximum of the scaled
+        // scores is the scaled maximum, exactly; with shifts, of the shifted logits)
+        float mt;
+        if (grouped) {
+          mt = full ? row_max<true, true>(s_addr, vcols, sl2, bias) : row_max<false, true>(s_addr, vcols, sl2, bias);
+        } else {
+          const float mr = full ? row_max<true>(s_addr, vcols) : row_max<false>(s_addr, vcols);
+          mt = mr * sl2;
+        }
         float alpha = 1.f;
         bool resc = false;
         if (mt > m_used + 8.f) {
@@ -807,8 +898,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
         // pass 2: P = 2^(s - m) as bf16 into the P tile, and its row sum
         uint8_t* pst = sp + (size_t)st * Lay::pstride;
-        const float sum = full ? row_exp<true>(s_addr, vcols, sl2, m_used, pst, row)
-                               : row_exp<false>(s_addr, vcols, sl2, m_used, pst, row);
+        float sum;
+        if (grouped)
+          sum = full ? row_exp<true, true>(s_addr, vcols, sl2, m_used, pst, row, bias)
+                     : row_exp<false, true>(s_addr, vcols, sl2, m_used, pst, row, bias);
+        else
+          sum = full ? row_exp<true>(s_addr, vcols, sl2, m_used, pst, row)
+                     : row_exp<false>(s_addr, vcols, sl2, m_used, pst, row);
         l = l * alpha + sum;
         tc::fence_proxy_async();
         tc::tc_fence_before();
@@ -1004,18 +1100,21 @@ __global__ void __launch_bounds__(256) sparse_sort_rows_kernel(const AttnArgs a)
     const int64_t pos = row % a.M;
     const int32_t n = a.koff[(int64_t)h * (a.B + 1) + a.B];
     uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+    float lg = 0.f;
     if (pos < n && n <= a.M) {
       const int s = a.kperm[(int64_t)h * a.M + pos];
       if (s >= 0 && s < a.M) {
         const int64_t src = ((int64_t)h * a.M + s) * CPR + c;
         kv = K[src];
         vv = V[src];
+        if (a.gcount && c == 0) lg = group_log2(a.gcount[(int64_t)h * a.M + s], a.status);
       } else if (c == 0) {
         flag_status(a.status, FASTAR_DEV_BAD_INDEX);
       }
     }
     KS[g] = kv;
     VS[g] = vv;
+    if (a.gcount && c == 0) a.lg_sorted[row] = lg;   // group counts: log2 g in bucket order
   }
 }
 
@@ -1075,8 +1174,10 @@ template <int D>
 bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   constexpr size_t smem = AttnLayout<D>::bytes;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (attr != cudaSuccess) return false;
+      cudaFuncSetAttribute(attn_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t attr_g =
+      cudaFuncSetAttribute(attn_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess || attr_g != cudaSuccess) return false;
   int64_t upper;
   AttnArgs b = a;
   CUtensorMap tk, tv, tq;
@@ -1119,6 +1220,8 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
       b.q_token_major = tmaj ? 1 : 0;
     }
   }
+  // group counts need the tensor-engine K/V path (the shifts are staged with its tiles)
+  if (a.gcount && !b.kv_tma) return false;
   if (a.mode == kSparse) {
     if (!a.items || !a.n_items) return false;
     if ((int64_t)a.H * a.B + 1 <= kPrefixMax) {
@@ -1136,7 +1239,11 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (upper <= 0) return true;
   const int sms = sm_count();
   const int grid = (int)(upper < sms ? upper : sms);
-  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
+  // group counts (the merge variant) select the instance that stages the logit shifts
+  if (a.gcount)
+    attn_tc_kernel<D, true><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
+  else
+    attn_tc_kernel<D, false><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
   count_launches(1);
   if (a.mode == kSparse) {
     const int64_t threads = (int64_t)a.H * a.nq * 32;
@@ -1157,11 +1264,11 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
 
 // The incoming cache in bucket order: K rows (bf16, [H, M, d]), 1/|k| and the cache index
 // of every sorted key ([H, mstride]; past the sorted length: zero row, 0, -1).  Also
-// clears the eviction flags.
+// clears the eviction flags and owners.
 template <int D>
 __global__ void __launch_bounds__(256)
     ann_sort_rows_kernel(const AttnArgs a, const float* __restrict__ knorm, float* inv_sorted, int32_t* j_sorted,
-                         uint4* ks, uint8_t* evict) {
+                         uint4* ks, uint8_t* evict, int32_t* owner) {
   constexpr int CPR = D / 8;
   const uint4* K = static_cast<const uint4*>(a.k);
   const int64_t total = (int64_t)a.H * a.mstride * CPR;
@@ -1187,16 +1294,19 @@ __global__ void __launch_bounds__(256)
       j_sorted[row] = s;
     }
   }
-  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < (int64_t)a.H * a.M; g += (int64_t)gridDim.x * 256)
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < (int64_t)a.H * a.M; g += (int64_t)gridDim.x * 256) {
     evict[g] = 0;
+    if (owner) owner[g] = -1;
+  }
 }
 
 // Per query (one warp): the best of its r slots — largest q.k/|k|, then lowest cache
-// index — is top1; s1 = that / |q|; the entry is evicted when cos(kcur_i, k_top1) >= tau.
+// index — is top1; s1 = that / |q|; the entry is evicted when cos(kcur_i, k_top1) >= tau,
+// and its owner is the lowest evicting query (atomic minimum over the unsigned view).
 template <int D>
 __global__ void __launch_bounds__(256)
     ann_match_finalize_kernel(const AttnArgs a, TokView kcur, const float* __restrict__ knorm, float tau,
-                              int32_t* top1, float* s1, uint8_t* evict) {
+                              int32_t* top1, float* s1, uint8_t* evict, int32_t* owner) {
   constexpr int E = D / 32;
   const int64_t wq = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -1261,7 +1371,10 @@ __global__ void __launch_bounds__(256)
   if (have) {
     const float den = sqrtf(kk) * knorm[(int64_t)h * a.M + j];
     const float c = den > 0.f ? dk / den : 0.f;
-    if (c >= tau) evict[(int64_t)h * a.M + j] = 1;
+    if (c >= tau) {
+      evict[(int64_t)h * a.M + j] = 1;
+      if (owner) atomicMin(reinterpret_cast<unsigned int*>(owner) + (int64_t)h * a.M + j, (unsigned int)i);
+    }
   }
 }
 
@@ -1269,7 +1382,7 @@ template <int D>
 cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
                                   const int32_t* qoff, const void* cache_k, const float* cache_knorm, int64_t M,
                                   const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1, float* s1,
-                                  uint8_t* evict, int32_t* status, void* ws, cudaStream_t s) {
+                                  uint8_t* evict, int32_t* owner, int32_t* status, void* ws, cudaStream_t s) {
   AttnArgs a{};
   a.mode = kMatchAnn;
   a.H = H;
@@ -1302,7 +1415,7 @@ cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, in
   a.j_sorted = j_sorted;
   const int64_t chunks = (int64_t)H * a.mstride * (D / 8);
   const int64_t blocks = (chunks + 255) / 256;
-  ann_sort_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a, cache_knorm, inv_sorted, j_sorted, ks, evict);
+  ann_sort_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a, cache_knorm, inv_sorted, j_sorted, ks, evict, owner);
   count_launches(1);
   CUtensorMap tk, tz;
   memset(&tz, 0, sizeof(tz));
@@ -1318,15 +1431,15 @@ cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, in
   }
   constexpr size_t smem = AttnLayout<D>::bytes;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(attn_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return attr;
   const int64_t upper = (int64_t)H * ((np + kAT - 1) / kAT + B);
   const int grid = (int)(upper < sm_count() ? upper : sm_count());
-  attn_tc_kernel<D><<<grid, kThreadsA, smem, s>>>(b, tk, tz, tz);
+  attn_tc_kernel<D, false><<<grid, kThreadsA, smem, s>>>(b, tk, tz, tz);
   count_launches(1);
   const int64_t threads = (int64_t)H * nq * 32;
   ann_match_finalize_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, kcur, cache_knorm, tau, top1,
-                                                                                   s1, evict);
+                                                                                   s1, evict, owner);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -1341,14 +1454,14 @@ size_t match_ann_workspace(int H, int64_t nq, int d, int r, int B, int64_t M) {
 cudaError_t launch_match_ann(int d, TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
                              const int32_t* qoff, const void* cache_k, const float* cache_knorm,
                              const int32_t* cache_len, int64_t M, const int32_t* kperm, const int32_t* koff,
-                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* status, void* ws,
-                             cudaStream_t s) {
+                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* owner, int32_t* status,
+                             void* ws, cudaStream_t s) {
   (void)cache_len;   // the incoming cache's bucket order (koff) carries its length
   if (d == 128)
     return launch_match_ann_impl<128>(q, kcur, H, nq, r, B, qperm, qoff, cache_k, cache_knorm, M, kperm, koff, tau,
-                                      top1, s1, evict, status, ws, s);
+                                      top1, s1, evict, owner, status, ws, s);
   return launch_match_ann_impl<64>(q, kcur, H, nq, r, B, qperm, qoff, cache_k, cache_knorm, M, kperm, koff, tau,
-                                   top1, s1, evict, status, ws, s);
+                                   top1, s1, evict, owner, status, ws, s);
 }
 
 size_t sparse_plan_bytes(int H, int64_t nq, int r, int B) {

@@ -7,6 +7,13 @@
 //
 // Two kernels: a one-CTA-per-head scan that writes the slot -> source map and the
 // new length, then a bandwidth kernel that moves rows with 16-byte accesses.
+//
+// The merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1 — identical
+// keys merge exactly when their values are averaged and the logit is shifted by the
+// group size) keeps a group count g per entry: an evicted entry j is folded into its
+// owner, the lowest current entry i that evicted it, whose value becomes
+// (v_i + g_j v_j) / (1 + g_j) and whose count becomes 1 + g_j; i's key stays.  The slot
+// order is the replace variant's.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -77,8 +84,29 @@ compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
   if (threadIdx.x == 0) len_out[h] = (int32_t)L;
 }
 
+// The group-merge inputs and outputs of the merge variant (all null otherwise).
+struct MergeIO {
+  const int32_t* top1;    // [H, nq] the match's top-1 cache index per current entry
+  const int32_t* owner;   // [H, M] lowest evicting current entry per cached entry, -1 none
+  const int32_t* g_in;    // [H, M] incoming group counts
+  int32_t* g_out;         // [H, M] outgoing group counts
+};
+
+// wa * a + wb * b element-wise over one 16-byte chunk (fp32 arithmetic, rounded once).
+template <typename T>
+__device__ __forceinline__ uint4 blend16(uint4 a, uint4 b, float wa, float wb) {
+  constexpr int N = 16 / (int)sizeof(T);
+  const T* x = reinterpret_cast<const T*>(&a);
+  const T* y = reinterpret_cast<const T*>(&b);
+  uint4 r;
+  T* z = reinterpret_cast<T*>(&r);
+#pragma unroll
+  for (int e = 0; e < N; ++e) z[e] = from_f<T>(fmaf(wa, to_f(x[e]), wb * to_f(y[e])));
+  return r;
+}
+
 // One 16-byte chunk per thread; VPR chunks per row.  Metadata moves with the row.
-template <typename T, int D>
+template <typename T, int D, bool kMerge>
 __global__ void __launch_bounds__(256)
 compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, const T* __restrict__ vc,
                     int64_t hs, int64_t ts, const float* __restrict__ kcn, const int32_t* __restrict__ kcb,
@@ -86,7 +114,7 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
                     const int32_t* __restrict__ kbin, const int32_t* __restrict__ len_in,
                     const int32_t* __restrict__ len_out, const int32_t* __restrict__ index_map,
                     T* __restrict__ kout, T* __restrict__ vout, float* __restrict__ knout,
-                    int32_t* __restrict__ kbout, int32_t* status) {
+                    int32_t* __restrict__ kbout, int32_t* status, const MergeIO mg) {
   constexpr int VPR = D * (int)sizeof(T) / 16;
   const int64_t total = (int64_t)H * M * VPR;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -103,26 +131,46 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
     const uint4* vs;
     float kn;
     int32_t kb;
+    int32_t gc = 1;
+    int64_t absorb = -1;   // merge variant: the cached entry this current entry owns
     if (src >= 0 && src < n) {
       ks = reinterpret_cast<const uint4*>(kin + ((int64_t)h * M + src) * D) + c;
       vs = reinterpret_cast<const uint4*>(vin + ((int64_t)h * M + src) * D) + c;
       kn = knin[(int64_t)h * M + src];
       kb = kbin[(int64_t)h * M + src];
+      if (kMerge) gc = mg.g_in[(int64_t)h * M + src];
     } else if (src >= n && src < n + nq) {
       const int64_t i = src - n;
       ks = reinterpret_cast<const uint4*>(kc + h * hs + i * ts) + c;
       vs = reinterpret_cast<const uint4*>(vc + h * hs + i * ts) + c;
       kn = kcn[(int64_t)h * nq + i];
       kb = kcb[(int64_t)h * nq + i];
+      if (kMerge) {
+        const int32_t j = mg.top1[(int64_t)h * nq + i];
+        if (j >= 0 && j < n && mg.owner[(int64_t)h * M + j] == (int32_t)i) absorb = j;
+      }
     } else {
       if (c == 0) flag_status(status, FASTAR_DEV_BAD_INDEX);
       continue;
     }
     reinterpret_cast<uint4*>(kout + row * D)[c] = __ldg(ks);
-    reinterpret_cast<uint4*>(vout + row * D)[c] = __ldg(vs);
+    if (kMerge && absorb >= 0) {
+      int32_t gj = mg.g_in[(int64_t)h * M + absorb];
+      if (gj < 0) {
+        if (c == 0) flag_status(status, FASTAR_DEV_BAD_INDEX);
+        gj = 0;
+      }
+      const float inv = 1.0f / (1.0f + (float)gj);
+      const uint4 vj = __ldg(reinterpret_cast<const uint4*>(vin + ((int64_t)h * M + absorb) * D) + c);
+      reinterpret_cast<uint4*>(vout + row * D)[c] = blend16<T>(__ldg(vs), vj, inv, (float)gj * inv);
+      gc = 1 + gj;
+    } else {
+      reinterpret_cast<uint4*>(vout + row * D)[c] = __ldg(vs);
+    }
     if (c == 0) {
       knout[row] = kn;
       kbout[row] = kb;
+      if (kMerge) mg.g_out[row] = gc;
     }
   }
 }
@@ -132,16 +180,17 @@ static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView v
                              const int32_t* kcb, const void* kin, const void* vin, const float* knin,
                              const int32_t* kbin, const int32_t* len_in, const int32_t* len_out,
                              const int32_t* imap, void* kout, void* vout, float* knout, int32_t* kbout,
-                             int32_t* status, cudaStream_t s) {
+                             int32_t* status, const MergeIO& mg, cudaStream_t s) {
   constexpr int VPR = D * (int)sizeof(T) / 16;
   const int64_t total = (int64_t)H * M * VPR;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  compact_copy_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>(
+  auto kern = mg.g_out ? compact_copy_kernel<T, D, true> : compact_copy_kernel<T, D, false>;
+  kern<<<(unsigned)blocks, 256, 0, s>>>(
       H, nq, M, static_cast<const T*>(kc.p), static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb,
       static_cast<const T*>(kin), static_cast<const T*>(vin), knin, kbin, len_in, len_out, imap,
-      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status);
+      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -151,19 +200,25 @@ cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M,
                                  const void* vin, const float* knin, const int32_t* kbin,
                                  const int32_t* len_in, const uint8_t* evict, void* kout, void* vout,
                                  float* knout, int32_t* kbout, int32_t* len_out, int32_t* imap,
-                                 int32_t* status, cudaStream_t s) {
+                                 int32_t* status, const int32_t* top1, const int32_t* owner,
+                                 const int32_t* g_in, int32_t* g_out, cudaStream_t s) {
   compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const MergeIO mg{top1, owner, g_in, g_out};
   if (dtype == FASTAR_BF16) {
     if (d == 128)
-      return copy_impl<__nv_bfloat16, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
-    return copy_impl<__nv_bfloat16, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+      return copy_impl<__nv_bfloat16, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap,
+                                           kout, vout, knout, kbout, status, mg, s);
+    return copy_impl<__nv_bfloat16, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap,
+                                        kout, vout, knout, kbout, status, mg, s);
   }
   if (d == 128)
-    return copy_impl<float, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
-  return copy_impl<float, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout, knout, kbout, status, s);
+    return copy_impl<float, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout,
+                                 vout, knout, kbout, status, mg, s);
+  return copy_impl<float, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout,
+                              knout, kbout, status, mg, s);
 }
 
 // ---------------------------------------------------------------------------------------

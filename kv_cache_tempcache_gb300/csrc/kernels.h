@@ -37,19 +37,20 @@ size_t match_tc_workspace(int H, int64_t nq, int64_t M);
 // returns S, or -1 if the launch could not be set up (the caller falls back).
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm,
                     const int32_t* clen, int64_t M, bool top2, float4* part, uint8_t* evict,
-                    int32_t* status, cudaStream_t s);
+                    int32_t* owner, int32_t* status, cudaStream_t s);
 cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kcur, int H, int64_t nq,
                                    const void* cache_k, const float* cache_knorm,
                                    const int32_t* cache_len, int64_t M, float tau, int32_t* top1,
-                                   float* s1, float* s2, uint8_t* evict, int32_t* status,
-                                   void* ws, cudaStream_t s);
+                                   float* s1, float* s2, uint8_t* evict, int32_t* owner,
+                                   int32_t* status, void* ws, cudaStream_t s);
 cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M, TokView kcur,
                                  TokView vcur, const float* kcur_norm, const int32_t* kcur_bucket,
                                  const void* k_in, const void* v_in, const float* knorm_in,
                                  const int32_t* kb_in, const int32_t* len_in, const uint8_t* evict,
                                  void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
                                  int32_t* len_out, int32_t* index_map, int32_t* status,
-                                 cudaStream_t s);
+                                 const int32_t* top1, const int32_t* owner, const int32_t* g_in,
+                                 int32_t* g_out, cudaStream_t s);
 
 // ---- attention ------------------------------------------------------------------------
 enum AttnMode { kDense = 0, kCross = 1, kSparse = 2, kMatchAnn = 3 };
@@ -97,6 +98,12 @@ struct AttnArgs {
   float* mbest;
   int32_t* midx;
   int32_t* n_items; // sparse: its length
+  // merge variant (Lemma 5.1): keys stand for groups of gcount keys and get the logit
+  // shift ln g.  sparse: [H, M] per cache slot (gc_hs = M); dense: h * gc_hs + key.
+  // lg_sorted: the tensor-core AnnSA path's log2 g in bucket order ([H, M], workspace).
+  const int32_t* gcount;
+  int64_t gc_hs;
+  float* lg_sorted;
   int32_t* status;
 };
 
@@ -107,8 +114,8 @@ size_t match_ann_workspace(int H, int64_t nq, int d, int r, int B, int64_t M);
 cudaError_t launch_match_ann(int d, TokView q, TokView kcur, int H, int64_t nq, int r, int B, const int32_t* qperm,
                              const int32_t* qoff, const void* cache_k, const float* cache_knorm,
                              const int32_t* cache_len, int64_t M, const int32_t* kperm, const int32_t* koff,
-                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* status, void* ws,
-                             cudaStream_t s);
+                             float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* owner, int32_t* status,
+                             void* ws, cudaStream_t s);
 // Bytes of the tensor-core AnnSA work list (inside the sparse workspace).
 size_t sparse_plan_bytes(int H, int64_t nq, int r, int B);
 // Tensor-core attention (bf16); false if it could not be set up (caller falls back).

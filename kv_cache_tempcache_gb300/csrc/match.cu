@@ -74,18 +74,22 @@ __global__ void __launch_bounds__(256)
 match_simt_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int64_t nq,
                   const T* __restrict__ ck, const float* __restrict__ cknorm,
                   const int32_t* __restrict__ clen, int64_t M, int64_t chunk,
-                  float4* __restrict__ part, uint8_t* __restrict__ evict, int32_t* status) {
+                  float4* __restrict__ part, uint8_t* __restrict__ evict, int32_t* __restrict__ owner,
+                  int32_t* status) {
   extern __shared__ float sm_match[];
   float* Qs = sm_match;            // [D][kMT]
   float* Ks = Qs + D * kMT;        // [D][kNT]
   float* invk = Ks + D * kNT;      // [kNT]
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
-  // clear the eviction flags of this head (the finaliser sets them afterwards)
+  // clear the eviction flags and owners of this head (the finaliser sets them afterwards)
   {
     const int64_t nblk = (int64_t)gridDim.x * gridDim.z;
     const int64_t b = (int64_t)blockIdx.z * gridDim.x + blockIdx.x;
-    for (int64_t j = b * blockDim.x + tid; j < M; j += nblk * blockDim.x) evict[h * M + j] = 0;
+    for (int64_t j = b * blockDim.x + tid; j < M; j += nblk * blockDim.x) {
+      evict[h * M + j] = 0;
+      if (owner) owner[h * M + j] = -1;
+    }
   }
   int64_t n = clen[h];
   if (n < 0 || n > M) {
@@ -178,14 +182,17 @@ match_simt_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int64_t nq,
 }
 
 // Eight lanes per (head, query): merge the split partials, turn the best values into
-// cosines, and test the matched entry for eviction: cos(kcur_i, k_top1) >= tau.
+// cosines, and test the matched entry for eviction: cos(kcur_i, k_top1) >= tau.  The
+// owner of an evicted entry is the lowest evicting query (an atomic minimum over the
+// unsigned view, where the cleared value -1 is the largest).
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t hs, int64_t ts,
                       int64_t nq, int H, const T* __restrict__ ck, const float* __restrict__ cknorm,
                       const int32_t* __restrict__ clen, int64_t M, float tau, int splits,
                       const float4* __restrict__ part, int32_t* __restrict__ top1,
-                      float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict) {
+                      float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict,
+                      int32_t* __restrict__ owner) {
   // eight lanes per query: each lane owns D/8 consecutive elements (vector loads)
   const int sub = threadIdx.x & 7;
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
@@ -255,7 +262,10 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
     if (any) {
       const float den = kk * cknorm[(int64_t)h * M + j];
       const float c = den > 0.f ? dot / den : 0.f;
-      if (c >= tau) evict[(int64_t)h * M + j] = 1;
+      if (c >= tau) {
+        evict[(int64_t)h * M + j] = 1;
+        if (owner) atomicMin(reinterpret_cast<unsigned int*>(owner) + (int64_t)h * M + j, (unsigned int)i);
+      }
     }
   }
 }
@@ -263,19 +273,20 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
 template <typename T, int D>
 static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const void* ck,
                               const float* cknorm, const int32_t* clen, int64_t M, float tau,
-                              int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* status,
-                              void* ws, cudaStream_t s) {
+                              int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* owner,
+                              int32_t* status, void* ws, cudaStream_t s) {
   float4* part = static_cast<float4*>(ws);
   if (sizeof(T) == 2 && nq > 0) {
     // bf16: the tensor-core kernel (the SIMT kernel below only if its set-up is refused)
-    const int tsplits = launch_match_tc(D, q, H, nq, ck, cknorm, clen, M, s2 != nullptr, part, evict, status, s);
+    const int tsplits =
+        launch_match_tc(D, q, H, nq, ck, cknorm, clen, M, s2 != nullptr, part, evict, owner, status, s);
     if (tsplits > 0) {
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       const int64_t warps = (int64_t)H * nq;
       match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
           static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-          static_cast<const T*>(ck), cknorm, clen, M, tau, tsplits, part, top1, s1, s2, evict);
+          static_cast<const T*>(ck), cknorm, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner);
       count_launches(1);
       return cudaGetLastError();
     }
@@ -292,11 +303,15 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   if (nq > 0) {
     k1<<<dim3(gx, H, splits), 256, smem, s>>>(static_cast<const T*>(q.p), q.hs, q.ts, nq,
                                               static_cast<const T*>(ck), cknorm, clen, M, chunk,
-                                              part, evict, status);
+                                              part, evict, owner, status);
     count_launches(1);
   } else {
     e = cudaMemsetAsync(evict, 0, (size_t)H * M, s);
     if (e != cudaSuccess) return e;
+    if (owner) {
+      e = cudaMemsetAsync(owner, 0xff, sizeof(int32_t) * (size_t)H * M, s);
+      if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
   }
   e = cudaGetLastError();
@@ -304,7 +319,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   const int64_t warps = (int64_t)H * nq;
   match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-      static_cast<const T*>(ck), cknorm, clen, M, tau, splits, part, top1, s1, s2, evict);
+      static_cast<const T*>(ck), cknorm, clen, M, tau, splits, part, top1, s1, s2, evict, owner);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -312,15 +327,17 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
 cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kc, int H, int64_t nq,
                                    const void* ck, const float* cknorm, const int32_t* clen,
                                    int64_t M, float tau, int32_t* top1, float* s1, float* s2,
-                                   uint8_t* evict, int32_t* status, void* ws, cudaStream_t s) {
+                                   uint8_t* evict, int32_t* owner, int32_t* status, void* ws, cudaStream_t s) {
   if (dtype == FASTAR_BF16) {
     if (d == 128)
-      return match_impl<__nv_bfloat16, 128>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, status, ws, s);
-    return match_impl<__nv_bfloat16, 64>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, status, ws, s);
+      return match_impl<__nv_bfloat16, 128>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner,
+                                            status, ws, s);
+    return match_impl<__nv_bfloat16, 64>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner,
+                                         status, ws, s);
   }
   if (d == 128)
-    return match_impl<float, 128>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, status, ws, s);
-  return match_impl<float, 64>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, status, ws, s);
+    return match_impl<float, 128>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner, status, ws, s);
+  return match_impl<float, 64>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner, status, ws, s);
 }
 
 }  // namespace fastar

@@ -158,7 +158,8 @@ template <int D, bool kTop2>
 __global__ void __launch_bounds__(kThreads, 1)
 match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const float* __restrict__ cknorm, const int32_t* __restrict__ clen, MatchGeom g,
-                float4* __restrict__ part_out, uint8_t* __restrict__ evict, int32_t* status) {
+                float4* __restrict__ part_out, uint8_t* __restrict__ evict, int32_t* __restrict__ owner,
+                int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   MatchSmem<D>& sm = *reinterpret_cast<MatchSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -166,11 +167,13 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   constexpr int KH = D / 64;
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kN);
 
-  // clear the eviction flags (the finaliser sets them after this kernel)
+  // clear the eviction flags and owners (the finaliser sets them after this kernel)
   {
     const int64_t total = (int64_t)g.H * g.M;
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < total; j += (int64_t)gridDim.x * blockDim.x)
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < total; j += (int64_t)gridDim.x * blockDim.x) {
       evict[j] = 0;
+      if (owner) owner[j] = -1;
+    }
   }
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.a_full, 1);
@@ -406,7 +409,7 @@ size_t match_tc_workspace(int H, int64_t nq, int64_t M) {
 template <int D>
 static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, const float* cknorm,
                                 const int32_t* clen, int64_t M, bool top2, float4* part, uint8_t* evict,
-                                int32_t* status, cudaStream_t s) {
+                                int32_t* owner, int32_t* status, cudaStream_t s) {
   CUtensorMap tq, tk;
   const bool token_major = H > 1 && q.hs < q.ts;   // e.g. [N, H, d] storage
   if (token_major) {
@@ -433,21 +436,22 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
     static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, true>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (a != cudaSuccess) return -1;
-    match_tc_kernel<D, true><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
+    match_tc_kernel<D, true><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, owner, status);
   } else {
     static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, false>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (a != cudaSuccess) return -1;
-    match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, status);
+    match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, owner, status);
   }
   count_launches(1);
   return g.S * kParts;   // partial top-2s per (segment, column part)
 }
 
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,
-                    int64_t M, bool top2, float4* part, uint8_t* evict, int32_t* status, cudaStream_t s) {
-  if (d == 128) return launch_match_tc_impl<128>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, status, s);
-  return launch_match_tc_impl<64>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, status, s);
+                    int64_t M, bool top2, float4* part, uint8_t* evict, int32_t* owner, int32_t* status,
+                    cudaStream_t s) {
+  if (d == 128) return launch_match_tc_impl<128>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, owner, status, s);
+  return launch_match_tc_impl<64>(q, H, nq, ck, cknorm, clen, M, top2, part, evict, owner, status, s);
 }
 
 }  // namespace fastar

@@ -14,6 +14,11 @@ The step for one chunk of Nq = F*Tf tokens (FAST-AR technical summary §2.A–C)
   6. AnnCA prompt selection per latent frame
   7. cross-attention over the kept prompt tokens -> o_cross
 Stages 6-7 depend only on stage 1, so they run on a second stream alongside 2-5.
+
+merge=True runs the merge variant (technical summary §2.A, Theoretical Basis: Lemma
+5.1): every cache entry carries a group count g; an evicted entry is folded into the
+current entry that owns it (count-weighted mean value, summed count) instead of being
+dropped, and AnnSA shifts every key's logit by ln g.
 """
 from __future__ import annotations
 
@@ -34,17 +39,20 @@ def _f32(*shape, dev):
 
 
 class CacheState:
-    """One half of the double-buffered TempCache: rows, norms, buckets, lengths."""
+    """One half of the double-buffered TempCache: rows, norms, buckets, lengths (and,
+    for the merge variant, group counts)."""
 
-    def __init__(self, H, M, d, dtype, dev):
+    def __init__(self, H, M, d, dtype, dev, grouped=False):
         self.k = torch.zeros((H, M, d), dtype=dtype, device=dev)
         self.v = torch.zeros((H, M, d), dtype=dtype, device=dev)
         self.knorm = _f32(H, M, dev=dev)
         self.kb = _i32(H, M, 1, dev=dev)
         self.len = _i32(H, dev=dev)
+        self.g = _i32(H, M, dev=dev) if grouped else None
 
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.knorm, self.kb, self.len))
+        ts = [self.k, self.v, self.knorm, self.kb, self.len] + ([self.g] if self.g is not None else [])
+        return sum(t.numel() * t.element_size() for t in ts)
 
 
 class FastARLayer:
@@ -53,9 +61,10 @@ class FastARLayer:
     def __init__(self, H: int, d: int, Tf: int, F: int, M: int, B: int, r: int, P: int, tau: float,
                  tau_ca: float, topk: int = 16, dtype: torch.dtype = torch.bfloat16, gate: bool = True,
                  device: str | torch.device = "cuda", scale: Optional[float] = None,
-                 diagnostics: bool = False):
+                 diagnostics: bool = False, merge: bool = False):
         """diagnostics=True also produces the second-best match cosine s2 (a slower
-        match epilogue); the step's results are the same either way."""
+        match epilogue); the step's results are the same either way.  merge=True: the
+        Lemma 5.1 merge variant (group counts, folded values, ln g logit shift)."""
         L.load()
         if M < F * Tf:
             raise ValueError(f"cache cap M={M} must hold one chunk of {F * Tf} tokens")
@@ -63,12 +72,13 @@ class FastARLayer:
         self.Nq = F * Tf
         self.tau, self.tau_ca, self.topk, self.gate = float(tau), float(tau_ca), int(topk), bool(gate)
         self.diagnostics = bool(diagnostics)
+        self.merge = bool(merge)
         self.dtype = dtype
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
         dev = torch.device(device)
         self.dev = dev
         Nq = self.Nq
-        self.caches = [CacheState(H, M, d, dtype, dev), CacheState(H, M, d, dtype, dev)]
+        self.caches = [CacheState(H, M, d, dtype, dev, self.merge), CacheState(H, M, d, dtype, dev, self.merge)]
         self.cur = 0
         # prompt
         self.kp = torch.zeros((H, P, d), dtype=dtype, device=dev)
@@ -83,6 +93,7 @@ class FastARLayer:
         self.s1 = _f32(H, Nq, dev=dev)
         self.s2 = _f32(H, Nq, dev=dev)
         self.evict = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+        self.owner = _i32(H, M, dev=dev) if self.merge else None
         self.index_map = _i32(H, M, dev=dev)
         self.kperm = _i32(H, M, dev=dev)
         self.koff = _i32(H, B + 1, dev=dev)
@@ -133,9 +144,10 @@ class FastARLayer:
         if self.P:
             L.fastar_bucket_assign(self.kp, self.centroids, 1, self.pb)
 
-    def load_cache(self, k: torch.Tensor, v: torch.Tensor):
+    def load_cache(self, k: torch.Tensor, v: torch.Tensor, g: Optional[torch.Tensor] = None):
         """Installs n raw entries (oldest first) as the current cache: norms and key
-        buckets are computed by the library."""
+        buckets are computed by the library.  g: group counts [H, n] (merge variant;
+        default 1 each)."""
         n = k.shape[1]
         if n > self.M:
             raise ValueError("more entries than the cache cap")
@@ -148,6 +160,11 @@ class FastARLayer:
             L.fastar_bucket_assign(c.k[:, :n], self.centroids, 1, kb, None, kn)
             c.kb[:, :n].copy_(kb)
             c.knorm[:, :n].copy_(kn)
+        if c.g is not None:
+            if g is None:
+                c.g[:, :n].fill_(1)
+            else:
+                c.g[:, :n].copy_(g)
         c.len.fill_(n)
 
     def reset(self):
@@ -173,7 +190,7 @@ class FastARLayer:
             t("tempcache_match", stream, "begin")
             L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
                                      self.s2 if self.diagnostics else None,
-                                     self.evict, self.dev_status, self.ws_match)
+                                     self.evict, self.dev_status, self.ws_match, owner=self.owner)
             t("tempcache_match", stream, "end")
 
         # the match needs only the step's inputs and the incoming cache: it starts at once
@@ -216,16 +233,26 @@ class FastARLayer:
         else:
             match(main)
         t("cache_compact", main, "begin")
-        L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
-                               cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
-                               self.index_map, self.dev_status)
+        if self.merge:
+            L.fastar_cache_compact_merge(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                                         cin.g, cin.len, self.evict, self.top1, self.owner, cout.k, cout.v,
+                                         cout.knorm, cout.kb, cout.g, cout.len, self.index_map, self.dev_status)
+        else:
+            L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                                   cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
+                                   self.index_map, self.dev_status)
         t("cache_compact", main, "end")
         t("bucket_sort", main, "begin")
         L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
         t("bucket_sort", main, "end")
         t("sparse_attn", main, "begin")
-        L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
-                             self.scale, self.o_self, self.lse_self, self.dev_status, self.ws_attn)
+        if self.merge:
+            L.fastar_sparse_attn_grouped(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm,
+                                         self.koff, cout.g, self.scale, self.o_self, self.lse_self, self.dev_status,
+                                         self.ws_attn)
+        else:
+            L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
+                                 self.scale, self.o_self, self.lse_self, self.dev_status, self.ws_attn)
         t("sparse_attn", main, "end")
         if not serial:
             ev2 = torch.cuda.Event()

@@ -86,6 +86,25 @@ def check_evict(cos_at_gpu_top1: np.ndarray, gpu_top1: np.ndarray, gpu_evict: np
     return int((e & ~must).sum())
 
 
+def check_owner(cos_at_gpu_top1: np.ndarray, gpu_top1: np.ndarray, gpu_evict: np.ndarray, gpu_owner: np.ndarray,
+                n: int, tau: float):
+    """The merge variant's owner of each evicted entry: exactly the evicted entries have
+    one; it is a query whose (validated) top-1 is that entry and whose cosine passes the
+    threshold (up to a near-threshold case); no lower query with the same top-1 clearly
+    passes it.  Entries past n have none."""
+    top1 = np.asarray(gpu_top1, np.int64)
+    owner = np.asarray(gpu_owner, np.int64)
+    e = np.asarray(gpu_evict[:n], bool)
+    assert np.array_equal(owner[:n] >= 0, e), "owners and eviction flags disagree"
+    assert np.all(owner[n:] == -1), "an owner past the cache length"
+    for j in np.flatnonzero(e):
+        o = owner[j]
+        assert 0 <= o < top1.shape[0] and top1[o] == j, f"entry {j}: owner {o} does not match it"
+        assert cos_at_gpu_top1[o] > tau - MARGIN, f"entry {j}: owner {o} is clearly below the threshold"
+        lower = np.flatnonzero((top1[:o] == j) & (cos_at_gpu_top1[:o] >= tau + MARGIN))
+        assert lower.size == 0, f"entry {j}: a lower query {lower[:3]} clearly evicts it"
+
+
 def check_keep(score: np.ndarray, got_keep: np.ndarray, tau_ca: float, topk: int, what: str):
     """keep[p] == score >= tau_ca or rank < topk, up to near-ties at either boundary."""
     score = np.asarray(score, np.float64)

@@ -77,7 +77,7 @@ def test_argument_validation_rejects_before_launch(lib):
                                     FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, s) == L.EINVAL
     # workspace too small
     assert lib.fastar_tempcache_match(FAKE, FAKE, L.BF16, 1, 64, 128, 8192, 128, FAKE, FAKE, FAKE, 128, 0.9, FAKE,
-                                      None, None, FAKE, None, FAKE, 16, s) == L.EWORKSPACE
+                                      None, None, FAKE, None, None, FAKE, 16, s) == L.EWORKSPACE
     assert lib.fastar_sparse_attn(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE, 128, FAKE, FAKE,
                                   0.1, FAKE, 8192, 128, None, None, FAKE, 16, s) == L.EWORKSPACE
     # prompt beyond the limit
@@ -88,6 +88,21 @@ def test_argument_validation_rejects_before_launch(lib):
                                    0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
                                    8, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
+    # merge variant: the group counts are required, and compaction stays out-of-place for them too
+    assert lib.fastar_cache_compact_merge(L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE,
+                                          FAKE + 16, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE + 32, FAKE + 48,
+                                          FAKE, FAKE, FAKE, FAKE, FAKE, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_merge(L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE,
+                                          FAKE + 16, FAKE, FAKE, FAKE + 64, FAKE, FAKE, FAKE, FAKE, FAKE + 32,
+                                          FAKE + 48, FAKE + 4, FAKE + 8, FAKE + 64, FAKE, FAKE, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_merge(L.BF16, 1, 100, 128, 50, FAKE, FAKE, 12800, 128, FAKE, FAKE, FAKE,
+                                          FAKE + 16, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 32, FAKE + 48,
+                                          FAKE, FAKE, FAKE, FAKE, FAKE, None, s) == L.ECAPACITY
+    assert lib.fastar_sparse_attn_grouped(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE, 128,
+                                          FAKE, FAKE, None, 0.1, FAKE, 8192, 128, None, None, FAKE, 1 << 30,
+                                          s) == L.EINVAL
+    assert lib.fastar_dense_attn_grouped(FAKE, L.BF16, 2, 64, 128, 8192, 128, FAKE, FAKE, 100, 12800, 128, FAKE, 50,
+                                         0.1, FAKE, 8192, 128, None, s) == L.EINVAL
     # dense append past capacity
     assert lib.fastar_dense_append(L.BF16, 1, 64, 128, FAKE, FAKE, 8192, 128, FAKE, FAKE, 100, 50, s) == L.ECAPACITY
     # empty work is a successful no-op that touches nothing

@@ -42,12 +42,13 @@ def _run(cfg, seed, cache_len=None):
     ws = torch.zeros(L.workspace_bytes(L.OP_MATCH_ANN, H, nq, M, d, B, r), dtype=torch.uint8, device=dev)
     top1, s1 = i32(H, nq), torch.zeros((H, nq), dtype=torch.float32, device=dev)
     evict = torch.ones((H, M), dtype=torch.uint8, device=dev)
+    owner = torch.full((H, M), 7, dtype=torch.int32, device=dev)
     L.fastar_tempcache_match_ann(q, kc, r, B, qperm, qoff, cache, knorm, clen, kperm, koff, cfg.tau, top1, s1,
-                                 evict, status, ws)
+                                 evict, status, ws, owner=owner)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return inp, ck, lens, dict(qb=GH.np_(qb), kb=GH.np_(kb)[..., 0], top1=GH.np_(top1), s1=GH.np_(s1),
-                               evict=GH.np_(evict))
+                               evict=GH.np_(evict), owner=GH.np_(owner))
 
 
 def _check(cfg, inp, ck, lens, g):
@@ -75,6 +76,7 @@ def _check(cfg, inp, ck, lens, g):
         assert np.all(np.isneginf(g["s1"][h][~has]))
         _, ce = O.evict_flags(got_t, inp["k_cur"][h], Kh, cfg.tau)
         stats["ambiguous"] += parity.check_evict(ce, got_t, g["evict"][h], n, cfg.tau)
+        parity.check_owner(ce, got_t, g["evict"][h], g["owner"][h], n, cfg.tau)
         assert not g["evict"][h][n:].any(), "flags beyond the cache length"
         stats["matched"] += int(has.sum())
     return stats
