@@ -105,14 +105,33 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def ready(self, n: int = 2) -> bool:
+        """True once n samples are in (or there is no sampler)."""
+        return self.proc is None or self.proc.poll() is not None or self._lines() >= n
+
+    def _lines(self) -> int:
+        self.out.flush()
+        try:
+            with open(self.path) as fh:
+                return sum(1 for _ in fh)
+        except OSError:
+            return 0
+
+    def _wait_lines(self, n: int, timeout: float):
+        t0 = time.time()
+        while self._lines() < n and time.time() - t0 < timeout and self.proc.poll() is None:
+            time.sleep(0.01)
+
     def stop(self):
         if self.proc is None:
             return None
+        # one more sample after the timed region, so that the samples bracket it
+        self._wait_lines(self._lines() + 1, 1.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -138,7 +157,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "every 50 ms from before the warm-up steps to just after the timed "
+                                              "steps"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -272,13 +292,23 @@ def run_fastar(args, rank, world, local):
     graph = layer.capture(q_d, k_d, v_d)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU under load while the clock sampler comes up (at most 5 s), so that
+    # its samples see the clocks of a busy GPU; then the counted warm-up steps
+    t_soak = time.time()
+    soak = 0
+    while not clocks.ready(2) and time.time() - t_soak < 5.0:
+        for _ in range(20):
+            flush.zero_()
+            graph.replay()
+        soak += 20
+        torch.cuda.synchronize(dev)
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         graph.replay()
     torch.cuda.synchronize(dev)
     barrier(world)
-    clocks = ClockSampler(local)
-    clocks.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -365,6 +395,7 @@ def run_fastar(args, rank, world, local):
                    "cache": f"warmed by {n_prior_chunks} earlier chunks ({cfg.prior_frames} frames); "
                             f"{int(n_in.sum())} entries in, {int(layer.caches[1 - layer.cur].len.sum())} out",
                    "l2": "flushed between timed steps (256 MiB memset outside the events)",
+                   "warmup_extra": f"{soak} untimed replays while the clock sampler started",
                    "stages": "per-stage times from an eager pass with all kernels on one stream",
                    "parallelism": f"replicas x{world} (independent head groups, no exchange)"},
         "latent_frames_per_s": round(value / cfg.Tf, 2),
@@ -382,6 +413,9 @@ def run_fastar(args, rank, world, local):
     # the ANN-restricted match (a variant of the TempCache match): timed beside the exact
     # match on the measured chunk's incoming cache, with the agreement of their choices
     out["ann_match"] = time_ann_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib)
+    # the merge variant (Lemma 5.1): its own layer warmed through the same chunks, its
+    # step timed as a graph beside the replace step above
+    out["merge"] = time_merge_variant(cfg, args.seed + rank, up, flush, args.steps, ms, torch, dev)
     # dense baseline from the same build: append-only cache, full attention
     if not args.no_dense:
         hk = np.concatenate(hist_k, axis=1)
@@ -488,6 +522,63 @@ def time_ann_match(layer, cfg, q_d, k_d, flush, steps, torch, L):
             "status": int(status.item()),
             "note": "each query compared only with the incoming cache's keys in its own r buckets; "
                     "one call incl. the bucket-order copy and the slot merge, L2 flushed before each"}
+
+
+def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):
+    from kv_cache_tempcache_gb300 import synth
+    from kv_cache_tempcache_gb300.layer import FastARLayer
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    gen = synth.DriftingMixture(cfg, seed=seed)
+    layer = FastARLayer(H=cfg.H, d=cfg.d, Tf=cfg.Tf, F=cfg.F, M=cfg.M, B=cfg.B, r=cfg.r, P=cfg.P, tau=cfg.tau,
+                        tau_ca=cfg.tau_ca, topk=cfg.topk, dtype=tdt, device=dev, merge=True)
+    layer.set_centroids(up(gen.centroids))
+    kp, vp = gen.prompt
+    layer.set_prompt(up(kp), up(vp))
+    for _ in range(cfg.prior_frames // cfg.F):
+        k, v, q = gen.next_chunk()
+        layer.step(up(q), up(k), up(v))
+    k, v, q = gen.next_chunk()
+    q_d, k_d, v_d = up(q), up(k), up(v)
+    graph = layer.capture(q_d, k_d, v_d)
+    for _ in range(3):
+        flush.zero_()
+        graph.replay()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    stage_ev = {}
+
+    def timer(name, stream, phase):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        stage_ev.setdefault(name, []).append(e)
+
+    for _ in range(steps):
+        flush.zero_()
+        layer.step(q_d, k_d, v_d, advance=False, timer=timer, serial=True)
+    torch.cuda.synchronize(dev)
+    stages = {}
+    for name in ("cache_compact", "sparse_attn"):
+        es = stage_ev[name]
+        stages[name] = round(sum(es[i].elapsed_time(es[i + 1]) for i in range(0, len(es), 2)) / (len(es) // 2), 4)
+    cin, cout = layer.caches[layer.cur], layer.caches[1 - layer.cur]
+    n_in = cin.len.long()
+    g_in = sum(int(cin.g[h, :int(n_in[h])].sum().item()) for h in range(cfg.H))
+    out = {"ms_per_step": round(ms, 4), "replace_ms_per_step": round(replace_ms, 4),
+           "ratio_to_replace": round(ms / replace_ms, 3), "stages_ms": stages,
+           "entries_in": int(n_in.sum().item()), "keys_represented_in": g_in,
+           "merged_this_step": int((layer.owner >= 0).sum().item()), "status": layer.status(),
+           "note": "Lemma 5.1 merge variant: evicted entries fold into their owner (mean value, summed count), "
+                   "AnnSA with a ln g logit shift; same chunks and graph protocol as the main step"}
+    del layer, graph
+    return out
 
 
 def run_reference(args, rank, world):
