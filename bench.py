@@ -41,6 +41,7 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-dense", action="store_true", help="skip the dense-baseline timing")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
+    p.add_argument("--no-rollout", action="store_true", help="skip the long-rollout stability run")
     return p.parse_args()
 
 
@@ -438,6 +439,8 @@ def run_fastar(args, rank, world, local):
         out["dense"] = {"ms_per_step": round(dms, 4), "keys": int(hk.shape[1] + cfg.Nq),
                         "speedup_fastar_vs_dense": round(dms / ms, 3)}
         del dense
+    if not args.no_rollout and cfg.name == "wan13b_layer":
+        out["rollout"] = measure_rollout(cfg, args.seed + rank, flush, torch, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=15.0)
     return out
@@ -522,6 +525,83 @@ def time_ann_match(layer, cfg, q_d, k_d, flush, steps, torch, L):
             "status": int(status.item()),
             "note": "each query compared only with the incoming cache's keys in its own r buckets; "
                     "one call incl. the bucket-order copy and the slot merge, L2 flushed before each"}
+
+
+def measure_rollout(cfg, seed, flush, torch, dev):
+    """The layer stepped through a 200-frame rollout from an empty cache (67 chunks of 3
+    frames): per chunk the step's time (its CUDA graph for the cache half it reads, L2
+    flushed before), the cache length, evictions and FIFO drops, and the device bytes;
+    beside it the dense path from the same build, whose append-only cache grows."""
+    import numpy as np
+    from kv_cache_tempcache_gb300 import synth
+    from kv_cache_tempcache_gb300.layer import FastARLayer, DenseLayer
+    chunks = synth.WAN13B_ROLLOUT_CHUNKS
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    gen = synth.DriftingMixture(cfg, seed=seed)
+    layer = FastARLayer(H=cfg.H, d=cfg.d, Tf=cfg.Tf, F=cfg.F, M=cfg.M, B=cfg.B, r=cfg.r, P=cfg.P, tau=cfg.tau,
+                        tau_ca=cfg.tau_ca, topk=cfg.topk, dtype=tdt, device=dev)
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(tdt).pin_memory()
+    layer.set_centroids(up(gen.centroids).to(dev))
+    kp, vp = gen.prompt
+    layer.set_prompt(up(kp).to(dev), up(vp).to(dev))
+    dense = DenseLayer(cfg.H, cfg.d, cfg.Nq, chunks * cfg.Nq, cfg.P, dtype=tdt, device=dev)
+    dense.set_prompt(up(kp).to(dev), up(vp).to(dev))
+    q_d, k_d, v_d = (torch.zeros((cfg.H, cfg.Nq, cfg.d), dtype=tdt, device=dev) for _ in range(3))
+    # one graph per direction of the double-buffered cache, then start from empty
+    graphs = [layer.capture(q_d, k_d, v_d)]
+    layer.cur = 1
+    graphs.append(layer.capture(q_d, k_d, v_d))
+    layer.reset()
+    torch.cuda.synchronize(dev)
+    ms, dense_ms, lens, lens_in, evicted, dropped, dev_bytes, alloc = [], [], [], [], [], [], [], []
+    for t in range(chunks):
+        k, v, q = gen.next_chunk()
+        q_d.copy_(up(q))
+        k_d.copy_(up(k))
+        v_d.copy_(up(v))
+        n_in = int(layer.cache.len.sum().item())
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graphs[layer.cur].replay()
+        b.record()
+        layer.cur = 1 - layer.cur
+        flush.zero_()
+        c, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record()
+        dense.step(q_d, k_d, v_d)
+        e.record()
+        torch.cuda.synchronize(dev)
+        ms.append(a.elapsed_time(b))
+        dense_ms.append(c.elapsed_time(e))
+        n_out = int(layer.cache.len.sum().item())
+        ev = int(layer.evict.sum().item())
+        lens_in.append(n_in)
+        lens.append(n_out)
+        evicted.append(ev)
+        dropped.append(n_in - ev + cfg.H * cfg.Nq - n_out)
+        dev_bytes.append(layer.device_bytes())
+        alloc.append(torch.cuda.memory_allocated(dev))
+    assert layer.status() == 0
+    # steady state: the chunks whose INCOMING cache is full (the step's shape no longer changes)
+    full = [i for i in range(chunks) if lens_in[i] == cfg.H * cfg.M]
+    first = full[0] if full else chunks
+    steady = ms[first:] if full else ms
+    med = statistics.median(steady)
+    dense_kv = 2 * dense.n * cfg.H * cfg.d * (2 if cfg.dtype == "bf16" else 4)
+    out = {"chunks": chunks, "frames": chunks * cfg.F, "first_full_chunk": first,
+           "ms_median_full": round(med, 4), "ms_max_dev_frac_full": round(max(abs(x - med) / med for x in steady), 4),
+           "ms_per_chunk": [round(x, 4) for x in ms],
+           "cache_entries_per_chunk": lens, "evicted_per_chunk": evicted, "fifo_dropped_per_chunk": dropped,
+           "device_bytes": sorted(set(dev_bytes)), "memory_allocated": [min(alloc), max(alloc)],
+           "dense_ms_per_chunk": [round(x, 3) for x in dense_ms], "dense_keys_last": int(dense.n),
+           "dense_kv_bytes_last": dense_kv,
+           "note": "per-chunk graph replay (after the chunk's upload and a synchronize) with the L2 flushed "
+                   "before each; flat = max deviation from the median over the chunks that start from a full "
+                   "cache"}
+    del layer, dense, graphs
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):

@@ -85,12 +85,14 @@ extern "C" {
 #define FASTAR_OP_SPARSE_ATTN 3
 #define FASTAR_OP_ANNCA 4
 #define FASTAR_OP_MATCH_ANN 5
+#define FASTAR_OP_CROSS_ATTN 6
 
 /* Bytes of workspace `op` needs for the given sizes (0 if it needs none).
  * MATCH: n = Nq, M = cache capacity.  SORT: n = elements per head before the
  * r fan-out.  SPARSE_ATTN: n = Nq, M = cache capacity (the bf16 path keeps a
  * bucket-ordered copy of the cache K/V in it).  ANNCA: F frames, P prompt tokens.
- * MATCH_ANN: n = Nq, M, d, B, r.
+ * MATCH_ANN: n = Nq, M, d, B, r.  CROSS_ATTN: d, P, F (the bf16 path's gathered copy of
+ * the kept prompt rows).
  * Unused arguments are ignored.  Returns 0 for an unknown op. */
 size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r,
                               int64_t P, int F);
@@ -319,13 +321,18 @@ int fastar_annca_select_noalloc(const void* q, int dtype, int H, int F, int64_t 
  * frame-relevant prompt subset").  For query i of frame f:
  *   O[h,i] = sum_{t < kcnt[h,f]} softmax_t(q_i . kp_{kidx[h,f,t]} * scale) vp_{kidx[h,f,t]}
  * kp, vp [H,P,d] contiguous; kidx/kcnt from fastar_annca_select.  kcnt = 0 gives
- * O = 0, lse = -inf.  lse float [H, F*tpf] optional. */
+ * O = 0, lse = -inf.  lse float [H, F*tpf] optional.
+ * workspace (optional, bf16 only): fastar_workspace_bytes(FASTAR_OP_CROSS_ATTN, H, 0, 0,
+ * d, 0, 0, P, F) bytes; with it the kept rows are first gathered into contiguous
+ * per-frame planes and read as tensor-engine tiles (faster); NULL reads them in place.
+ * Same results either way.  A non-NULL workspace that is too small: FASTAR_EWORKSPACE. */
 int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                              int64_t q_head_stride, int64_t q_token_stride,
                              const void* kp, const void* vp, int64_t P,
                              const int32_t* kidx, const int32_t* kcnt, float scale,
                              void* out, int64_t o_head_stride, int64_t o_token_stride,
-                             float* lse, cudaStream_t stream);
+                             float* lse, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
 
 /* ---- 8. dense attention (the baseline) ------------------------------------------
  * The dense softmax attention FAST-AR is compared against (technical summary,

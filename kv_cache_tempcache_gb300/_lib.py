@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libfastar.so")
 F32, BF16 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECAPACITY, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
 DEV_BAD_LEN, DEV_BAD_BUCKET, DEV_BAD_INDEX = 1, 2, 4
-OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA, OP_MATCH_ANN = 1, 2, 3, 4, 5
+OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA, OP_MATCH_ANN, OP_CROSS_ATTN = 1, 2, 3, 4, 5, 6
 MAX_B, MAX_R, MAX_P = 256, 8, 1024
 
 _P = ctypes.c_void_p
@@ -51,7 +51,8 @@ _SIGS = {
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
                             _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
-    "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P],
+    "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P, _S,
+                                 _P],
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _P, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
@@ -260,12 +261,13 @@ def fastar_annca_select_noalloc(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx
           stream_handle(stream))
 
 
-def fastar_cross_attn_subset(q, F, kp, vp, kidx, kcnt, scale, out, lse=None, stream=None):
+def fastar_cross_attn_subset(q, F, kp, vp, kidx, kcnt, scale, out, lse=None, stream=None, workspace=None):
     H, nq, d = q.shape
     qh, qt = tok_strides(q)
     oh, ot = tok_strides(out)
     _call("fastar_cross_attn_subset", ptr(q), dtype_code(q.dtype), H, F, nq // F, d, qh, qt, ptr(kp), ptr(vp),
-          kp.shape[1], ptr(kidx), ptr(kcnt), float(scale), ptr(out), oh, ot, ptr(lse), stream_handle(stream))
+          kp.shape[1], ptr(kidx), ptr(kcnt), float(scale), ptr(out), oh, ot, ptr(lse), ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
 def fastar_dense_attn(q, k, v, nk, scale, out, lse=None, stream=None):

@@ -76,6 +76,9 @@ size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B,
     case FASTAR_OP_MATCH_ANN:
       if ((d != 64 && d != 128) || B < 1 || r < 1 || M < 1) return 0;
       return fastar::match_ann_workspace(H, n, d, r, B, M);
+    case FASTAR_OP_CROSS_ATTN:
+      if ((d != 64 && d != 128) || P < 1 || F < 1) return 0;
+      return 2 * sizeof(uint16_t) * (size_t)H * F * P * d + 1024;
     default: return 0;
   }
 }
@@ -335,7 +338,8 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
 int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
                              int64_t q_token_stride, const void* kp, const void* vp, int64_t P,
                              const int32_t* kidx, const int32_t* kcnt, float scale, void* out,
-                             int64_t o_head_stride, int64_t o_token_stride, float* lse, cudaStream_t stream) {
+                             int64_t o_head_stride, int64_t o_token_stride, float* lse, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || F < 0 || tpf < 0 || P < 0) return FASTAR_EINVAL;
@@ -362,6 +366,13 @@ int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf
   a.o_hs = o_head_stride;
   a.o_ts = o_token_stride;
   a.lse = lse;
+  if (workspace && dtype == FASTAR_BF16 && P > 0) {
+    const size_t plane = sizeof(uint16_t) * (size_t)H * F * P * d;
+    if (workspace_bytes < 2 * plane + 1024) return FASTAR_EWORKSPACE;
+    const uintptr_t at = (reinterpret_cast<uintptr_t>(workspace) + 1023) & ~static_cast<uintptr_t>(1023);
+    a.ksorted = reinterpret_cast<void*>(at);
+    a.vsorted = reinterpret_cast<uint8_t*>(at) + plane;
+  }
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
 }
 

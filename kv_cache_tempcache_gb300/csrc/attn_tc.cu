@@ -359,6 +359,12 @@ __device__ __forceinline__ float key_bias(const AttnArgs& a, const ItemInfo& it,
   return group_log2(a.gcount[(int64_t)it.h * a.gc_hs + u], a.status);
 }
 
+// The third tensor-map coordinate of the item's K/V tiles: the head, or for AnnCA the
+// (head, frame) plane of the gathered kept-prompt rows.
+__device__ __forceinline__ int kv_plane(const AttnArgs& a, const ItemInfo& it) {
+  return a.mode == kCross ? it.h * a.F + it.f : it.h;
+}
+
 // Query row `pos` of item `it` (valid below q1): its source offset and output row
 // (sparse: the (query, slot) pair index; otherwise the token row), or -1 for none.
 __device__ __forceinline__ void query_row(const AttnArgs& a, const ItemInfo& it, int64_t pos, int64_t q1,
@@ -574,8 +580,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             const int y = (int)(it.kbase + (int64_t)j * kKT);
             tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
             for (int kh = 0; kh < D / 64; ++kh) {
-              tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
-              tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+              tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, kv_plane(a, it),
+                              &sm.kv_full[st]);
+              tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, kv_plane(a, it),
+                              &sm.kv_full[st]);
             }
           }
         }
@@ -658,9 +666,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                   const int y = (int)(it.kbase + (int64_t)j * kKT);
                   tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
                   for (int kh = 0; kh < D / 64; ++kh) {
-                    tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h,
+                    tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, kv_plane(a, it),
                                     &sm.kv_full[st]);
-                    tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h,
+                    tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, kv_plane(a, it),
                                     &sm.kv_full[st]);
                   }
                 }
@@ -683,8 +691,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
               } else {
                 tc::mbar_arrive_tx(&sm.kv_full[st], (uint32_t)(2 * Lay::kstage));
                 for (int kh = 0; kh < D / 64; ++kh) {
-                  tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, it.h, &sm.kv_full[st]);
-                  tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, it.h, &sm.kv_full[st]);
+                  tc::tma_load_3d(sk + (size_t)st * Lay::kstage + kh * kBlkK, &tm_k, kh * 64, y, kv_plane(a, it),
+                                  &sm.kv_full[st]);
+                  tc::tma_load_3d(sv + (size_t)st * Lay::kstage + kh * kBlkK, &tm_v, kh * 64, y, kv_plane(a, it),
+                                  &sm.kv_full[st]);
                 }
               }
             }
@@ -1118,6 +1128,43 @@ __global__ void __launch_bounds__(256) sparse_sort_rows_kernel(const AttnArgs a)
   }
 }
 
+// AnnCA's kept prompt rows gathered into contiguous (head, frame) planes [H*F, P, d]
+// (kept order), so that the attention reads them as tiled TMA boxes; the rows from the
+// kept count up to the next 64-row tile are zeroed (they are masked, and P = 0 times a
+// finite value stays 0 in the P.V product).
+template <int D>
+__global__ void __launch_bounds__(256) cross_gather_rows_kernel(const AttnArgs a) {
+  constexpr int CPR = D / 8;
+  const int64_t total = (int64_t)a.H * a.F * a.P * CPR;
+  const uint4* K = static_cast<const uint4*>(a.k);
+  const uint4* V = static_cast<const uint4*>(a.v);
+  uint4* KS = static_cast<uint4*>(a.ksorted);
+  uint4* VS = static_cast<uint4*>(a.vsorted);
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < total; g += (int64_t)gridDim.x * 256) {
+    const int64_t row = g / CPR;
+    const int c = (int)(g % CPR);
+    const int64_t hf = row / a.P, t = row % a.P;
+    int64_t n = a.kcnt[hf];
+    n = n < 0 ? 0 : (n > a.P ? a.P : n);
+    int64_t lim = (n + kKT - 1) / kKT * kKT;
+    lim = lim < a.P ? lim : a.P;
+    if (t >= lim) continue;
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+    if (t < n) {
+      const int p = a.kidx[hf * a.P + t];
+      if (p >= 0 && p < a.P) {
+        const int64_t src = ((hf / a.F) * a.P + p) * CPR + c;
+        kv = K[src];
+        vv = V[src];
+      } else if (c == 0) {
+        flag_status(a.status, FASTAR_DEV_BAD_INDEX);
+      }
+    }
+    KS[g] = kv;
+    VS[g] = vv;
+  }
+}
+
 // Merges the r slot partials of every AnnSA query by the exact log-sum-exp rule:
 // o = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s), and
 // lse = max + log(sum_s w_s).  One warp per (head, query); lane l owns columns
@@ -1201,6 +1248,33 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
         sparse_sort_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a);
         count_launches(1);
         b.kv_tma = 1;
+      }
+    }
+  } else if (a.mode == kCross) {
+    // with a workspace: the kept rows gathered into contiguous planes, read (like the
+    // queries of each frame, which are contiguous rows) by tiled TMA
+    if (a.ksorted && a.vsorted && a.P <= INT_MAX &&
+        make_tmap_bf16_3d(&tk, a.ksorted, D, (uint64_t)a.P, (uint64_t)a.H * a.F, (uint64_t)D * 2,
+                          (uint64_t)a.P * D * 2, 64, kKT) &&
+        make_tmap_bf16_3d(&tv, a.vsorted, D, (uint64_t)a.P, (uint64_t)a.H * a.F, (uint64_t)D * 2,
+                          (uint64_t)a.P * D * 2, 64, kKT)) {
+      const int64_t chunks = (int64_t)a.H * a.F * a.P * (D / 8);
+      const int64_t blocks = (chunks + 255) / 256;
+      if (blocks > 0 && blocks <= INT_MAX) {
+        cross_gather_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a);
+        count_launches(1);
+        b.kv_tma = 1;
+        const int64_t nrow = (int64_t)a.F * a.tpf;
+        const bool tmaj = a.H > 1 && a.q.hs < a.q.ts;
+        const bool qok = nrow <= INT_MAX &&
+                         (tmaj ? make_tmap_bf16_3d(&tq, a.q.p, D, (uint64_t)a.H, (uint64_t)nrow, (uint64_t)a.q.hs * 2,
+                                                   (uint64_t)a.q.ts * 2, 64, 1, kAT)
+                               : make_tmap_bf16_3d(&tq, a.q.p, D, (uint64_t)nrow, (uint64_t)a.H, (uint64_t)a.q.ts * 2,
+                                                   (uint64_t)a.q.hs * 2, 64, kAT));
+        if (qok) {
+          b.q_tma = 1;
+          b.q_token_major = tmaj ? 1 : 0;
+        }
       }
     }
   } else if (a.mode == kDense && a.kv_ts == D && a.nk <= INT_MAX &&

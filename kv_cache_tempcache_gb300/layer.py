@@ -115,6 +115,7 @@ class FastARLayer:
 
         self.ws_match = ws(L.OP_MATCH, n=Nq, M=M, d=d)
         self.ws_attn = ws(L.OP_SPARSE_ATTN, n=Nq, M=M, d=d, B=B, r=r)
+        self.ws_cross = ws(L.OP_CROSS_ATTN, n=0, d=d, P=P, F=F) if P > 0 else None
         self.side = torch.cuda.Stream(device=dev)
         self.mside = torch.cuda.Stream(device=dev)
         self.match_first = True
@@ -225,7 +226,7 @@ class FastARLayer:
             t("annca_select", side, "end")
             t("cross_attn_subset", side, "begin")
             L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale,
-                                       self.o_cross, self.lse_cross)
+                                       self.o_cross, self.lse_cross, workspace=self.ws_cross)
             t("cross_attn_subset", side, "end")
         # TempCache + AnnSA on the main stream
         if early:

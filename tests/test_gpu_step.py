@@ -183,3 +183,32 @@ def test_rollout_matches_oracle_chunk_by_chunk():
             np.testing.assert_array_equal(GH.np_(c.v[h, :L]), nv)
             ck[h], cv[h] = nk, nv
         assert torch.cuda.memory_allocated() == bytes0, "the step must not allocate"
+
+
+@pytest.mark.parametrize("P,d", [(100, 128), (8, 64), (512, 128)])
+def test_cross_attention_paths_agree_bit_for_bit(P, d):
+    """The kept prompt rows read in place (no workspace) or gathered into contiguous
+    planes and read by the tensor engine (workspace): same rows, same order, so the
+    same bits; both against the oracle."""
+    from kv_cache_tempcache_gb300 import _lib as L
+    cfg = GH.small_bf16().replace(P=P, d=d, topk=min(16, P))
+    inputs = synth.layer_step_inputs(cfg, seed=6)
+    ck, cv = GH.raw_window(inputs, cfg)
+    g, layer = GH.gpu_step(cfg, inputs, ck, cv)
+    q = GH.to_dev(inputs["q"], cfg)
+    outs = []
+    for ws in (None, layer.ws_cross):
+        o = torch.zeros_like(q)
+        lse = torch.zeros(q.shape[:2], dtype=torch.float32, device="cuda")
+        L.fastar_cross_attn_subset(q, cfg.F, layer.kp, layer.vp, layer.kidx, layer.kcnt, cfg.scale, o, lse,
+                                   workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((GH.np_(o), GH.np_(lse)))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    assert np.array_equal(outs[1][0], g["o_cross"])
+    tol = parity.TOL[cfg.dtype]
+    for h in range(cfg.H):
+        kept = [np.flatnonzero(g["keep"][h][f]) for f in range(cfg.F)]
+        oc, _ = O.cross_attention_subset(inputs["q"][h], inputs["kp"][h], inputs["vp"][h], kept, cfg.F, cfg.Tf,
+                                         cfg.scale)
+        parity.close(outs[1][0][h], oc, *tol, f"o_cross head {h}")
