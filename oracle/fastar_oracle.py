@@ -18,6 +18,9 @@ pages about it:
   * AnnSA (technical summary §2.C; blog §3): reuse the same buckets; each query
     attends only to keys in its own bucket(s).
   * Problem statement: the cache grows with the rollout and is to be bounded.
+  * The quantization variant of the match (technical summary §2.A: the ANN is LSH or
+    quantization): product quantization of the cached keys, the top-1 searched among
+    the decoded keys.
   * The merge variant (technical summary §2.A, "Theoretical Basis", Lemma 5.1):
     identical keys merge with no error when their values are averaged and their
     logit is shifted by the size of the group.
@@ -160,6 +163,49 @@ def tempcache_match_ann(Q, R, K_cache, kb_cache):
     best = np.argmax(S, axis=1).astype(np.int64)                # first maximum = lowest j
     top1[has] = best[has]
     s1[has] = S[np.arange(nq), best][has]
+    return top1, s1
+
+
+# ----------------------------------------------------------------------------------
+# product quantization (technical summary §2.A / §2.B: "LSH or Quantization")
+# ----------------------------------------------------------------------------------
+# A key of dimension d is split into m consecutive sub-vectors of d/m dimensions; each
+# sub-vector is replaced by the nearest (Euclidean) of the Kc codewords of its sub-space.
+# Readings: codebooks are per head and given (an input, like the centroids); the
+# nearest codeword is the one with the smallest squared distance, lowest index on ties;
+# the quantised match ranks the cached keys by cos(q, decode(code(k))) and its eviction
+# test uses the true key, as the exact match's does.
+
+def pq_encode(X, codebooks) -> np.ndarray:
+    """codes[t, s] = argmin_c |x_t[s-th sub-vector] - codebooks[s, c]|^2 (lowest c on
+    ties).  X [n, d]; codebooks [m, Kc, d/m].  int64 [n, m]."""
+    X = _f64(X)
+    Cb = _f64(codebooks)
+    m, Kc, ds = Cb.shape
+    n = X.shape[0]
+    codes = np.zeros((n, m), np.int64)
+    for s in range(m):
+        sub = X[:, s * ds:(s + 1) * ds]
+        dist = ((sub[:, None, :] - Cb[s][None, :, :]) ** 2).sum(axis=2)     # [n, Kc]
+        codes[:, s] = np.argmin(dist, axis=1) if n else np.zeros(0, np.int64)
+    return codes
+
+
+def pq_decode(codes, codebooks) -> np.ndarray:
+    """The reconstruction: the chosen codewords concatenated.  [n, d]."""
+    Cb = _f64(codebooks)
+    codes = np.asarray(codes, np.int64)
+    m = Cb.shape[0]
+    if codes.shape[0] == 0:
+        return np.zeros((0, m * Cb.shape[2]))
+    return np.concatenate([Cb[s][codes[:, s]] for s in range(m)], axis=1)
+
+
+def tempcache_match_pq(Q, codes_cache, codebooks):
+    """The quantised TempCache match: top1[i] = argmax_j cos(q_i, k^_j) over the decoded
+    cached keys k^_j (lowest j on ties; -1 if the cache is empty); s1 = that cosine."""
+    K_hat = pq_decode(codes_cache, codebooks)
+    top1, s1, _ = tempcache_match(Q, K_hat)
     return top1, s1
 
 

@@ -169,3 +169,33 @@ def grouped_attention(qi, entries, scale):
     z = sum(w)
     dv = len(entries[0][1])
     return [sum(w[s] * float(entries[s][1][c]) for s in range(len(entries))) / z for c in range(dv)]
+
+
+def pq_encode(X, codebooks):
+    """Nearest codeword per sub-space by enumerating every codeword's squared distance."""
+    m, Kc, ds = len(codebooks), len(codebooks[0]), len(codebooks[0][0])
+    out = []
+    for x in X:
+        row = []
+        for s in range(m):
+            best, arg = None, -1
+            for c in range(Kc):
+                dist = 0.0
+                for t in range(ds):
+                    diff = float(x[s * ds + t]) - float(codebooks[s][c][t])
+                    dist += diff * diff
+                if best is None or dist < best:
+                    best, arg = dist, c
+            row.append(arg)
+        out.append(row)
+    return out
+
+
+def pq_match(q, codes, codebooks):
+    """Top-1 over the decoded cached keys by enumeration (first maximum of the cosine)."""
+    ds = len(codebooks[0][0])
+    dec = [[float(codebooks[s][cd][t]) for s, cd in enumerate(row) for t in range(ds)] for row in codes]
+    top1 = []
+    for qi in q:
+        top1.append(argmax_first([cos(qi, k) for k in dec]) if dec else -1)
+    return top1
