@@ -417,6 +417,9 @@ def run_fastar(args, rank, world, local):
     # the merge variant (Lemma 5.1): its own layer warmed through the same chunks, its
     # step timed as a graph beside the replace step above
     out["merge"] = time_merge_variant(cfg, args.seed + rank, up, flush, args.steps, ms, torch, dev)
+    # the quantised match (product quantization of the cached keys), beside the exact match
+    if hist_k and cfg.dtype == "bf16":
+        out["pq_match"] = time_pq_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib, hist_k[0], args.seed)
     # dense baseline from the same build: append-only cache, full attention
     if not args.no_dense:
         hk = np.concatenate(hist_k, axis=1)
@@ -602,6 +605,61 @@ def measure_rollout(cfg, seed, flush, torch, dev):
     del layer, dense, graphs
     torch.cuda.empty_cache()
     return out
+
+
+def time_pq_match(layer, cfg, q_d, k_d, flush, steps, torch, L, first_chunk_keys, seed, m=32, Kc=16):
+    from kv_cache_tempcache_gb300 import synth
+    dev = q_d.device
+    tdt = q_d.dtype
+    cin = layer.caches[layer.cur]
+    H, M, nq = cfg.H, cfg.M, cfg.Nq
+    cb = torch.from_numpy(synth.pq_codebooks(first_chunk_keys[:, :cfg.Tf], m, Kc, seed=seed)).to(dev).to(tdt)
+    codes = torch.zeros((H, M, m), dtype=torch.uint8, device=dev)
+    codes_cur = torch.zeros((H, nq, m), dtype=torch.uint8, device=dev)
+    L.fastar_pq_encode(cin.k, cb, codes)                    # the incoming (full) cache, once
+    ws = torch.zeros(L.workspace_bytes(L.OP_MATCH_PQ, H, nq, M, cfg.d), dtype=torch.uint8, device=dev)
+    i32 = lambda *s_: torch.zeros(s_, dtype=torch.int32, device=dev)
+    status = i32(1)
+    t_pq, s_pq = i32(H, nq), torch.zeros((H, nq), dtype=torch.float32, device=dev)
+    e_pq = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+    t_ex, s_ex = i32(H, nq), torch.zeros((H, nq), dtype=torch.float32, device=dev)
+    e_ex = torch.zeros((H, M), dtype=torch.uint8, device=dev)
+
+    def pq():
+        L.fastar_tempcache_match_pq(q_d, k_d, cin.k, cin.knorm, codes, cin.len, cb, cfg.tau, t_pq, s_pq, e_pq, status,
+                                    ws)
+
+    def encode():
+        L.fastar_pq_encode(k_d, cb, codes_cur)
+
+    def exact():
+        L.fastar_tempcache_match(q_d, k_d, cin.k, cin.knorm, cin.len, cfg.tau, t_ex, s_ex, None, e_ex, status,
+                                 layer.ws_match)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        res = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            res.append(a.elapsed_time(b))
+        return sum(res) / len(res)
+
+    pq_ms, enc_ms, ex_ms = timed(pq), timed(encode), timed(exact)
+    torch.cuda.synchronize()
+    agree = float((t_pq == t_ex).float().mean().item())
+    return {"ms": round(pq_ms, 4), "encode_chunk_ms": round(enc_ms, 4), "exact_ms": round(ex_ms, 4),
+            "m": m, "Kc": Kc, "code_bytes_per_key": m, "top1_agree_with_exact": round(agree, 4),
+            "evicted": {"pq": int(e_pq.sum().item()), "exact": int(e_ex.sum().item())},
+            "status": int(status.item()),
+            "note": "cached keys product-quantized (m sub-spaces of d/m dims, Kc codewords drawn from the first "
+                    "frame's keys); the match ranks the decoded keys on the tensor cores (decode + match + "
+                    "finaliser, eviction on the true keys); encode = the chunk's current keys"}
 
 
 def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):

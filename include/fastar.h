@@ -78,6 +78,7 @@ extern "C" {
 #define FASTAR_MAX_B 256          /* buckets per head                              */
 #define FASTAR_MAX_R 8            /* buckets per query                             */
 #define FASTAR_MAX_P 1024         /* prompt tokens per head                        */
+#define FASTAR_MAX_PQ_KC 256      /* codewords per product-quantization sub-space  */
 
 /* ---- workspace queries --------------------------------------------------------- */
 #define FASTAR_OP_MATCH 1
@@ -86,13 +87,14 @@ extern "C" {
 #define FASTAR_OP_ANNCA 4
 #define FASTAR_OP_MATCH_ANN 5
 #define FASTAR_OP_CROSS_ATTN 6
+#define FASTAR_OP_MATCH_PQ 7
 
 /* Bytes of workspace `op` needs for the given sizes (0 if it needs none).
  * MATCH: n = Nq, M = cache capacity.  SORT: n = elements per head before the
  * r fan-out.  SPARSE_ATTN: n = Nq, M = cache capacity (the bf16 path keeps a
  * bucket-ordered copy of the cache K/V in it).  ANNCA: F frames, P prompt tokens.
  * MATCH_ANN: n = Nq, M, d, B, r.  CROSS_ATTN: d, P, F (the bf16 path's gathered copy of
- * the kept prompt rows).
+ * the kept prompt rows).  MATCH_PQ: n = Nq, M, d (the decoded cached keys).
  * Unused arguments are ignored.  Returns 0 for an unknown op. */
 size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B, int r,
                               int64_t P, int F);
@@ -177,6 +179,41 @@ int fastar_tempcache_match_ann(const void* q, const void* k_cur, int dtype, int 
                                const int32_t* kperm, const int32_t* koff, float tau, int32_t* top1,
                                float* s1, uint8_t* evict, int32_t* owner, int32_t* dev_status,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---- 2c. quantised TempCache match (a variant of 2) -----------------------------------
+ * FAST-AR technical summary §2.A: the top-1 nearest key is searched with a lightweight
+ * ANN, "LSH or Quantization"; this is the quantization family (product quantization).
+ * A key of dimension d is m consecutive sub-vectors of d/m elements (d/m = 4 or 8, so m
+ * is a multiple of 4); each is coded by the nearest (smallest squared distance, lowest
+ * index on ties) of the Kc <= FASTAR_MAX_PQ_KC codewords of its sub-space.  Codebooks
+ * are per head, [H, m, Kc, d/m], same dtype, contiguous, 16-byte aligned.
+ *
+ * fastar_pq_encode: codes [H, n, m] uint8 (4-byte aligned) of the rows of x.
+ * fastar_tempcache_match_pq: as 2 with every cached key k_j replaced by its
+ *   reconstruction k^_j (its codewords concatenated; cache_codes [H, M, m] from
+ *   fastar_pq_encode, moved through compactions by fastar_pq_gather_codes):
+ *     top1[h,i] = argmax_{j < n} cos(q_i, k^_j) (lowest j on ties; -1 when n == 0),
+ *     s1 = that cosine; evict / owner as in 2, tested on the TRUE keys:
+ *     cos(kcur_i, k_top1) >= tau, with cache_knorm = |k_j|.  bf16 only.
+ *   Workspace: fastar_workspace_bytes(FASTAR_OP_MATCH_PQ, H, nq, M, d, ...).
+ * fastar_pq_gather_codes: the codes of a compacted cache: codes_out[h, s] =
+ *   codes_in[h, j] for index_map[h, s] = j < len_in[h], codes_cur[h, i] for
+ *   index_map[h, s] = len_in[h] + i, for s < len_out[h] (index_map / len_out from
+ *   fastar_cache_compact).  codes_in and codes_out must differ. */
+int fastar_pq_encode(const void* x, int dtype, int H, int64_t n, int d, int64_t head_stride,
+                     int64_t token_stride, const void* codebooks, int m, int Kc, uint8_t* codes,
+                     cudaStream_t stream);
+int fastar_tempcache_match_pq(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                              int64_t head_stride, int64_t token_stride, const void* cache_k,
+                              const float* cache_knorm, const uint8_t* cache_codes,
+                              const int32_t* cache_len, int64_t M, const void* codebooks, int m, int Kc,
+                              float tau, int32_t* top1, float* s1, uint8_t* evict, int32_t* owner,
+                              int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+int fastar_pq_gather_codes(int H, int64_t nq, int64_t M, int m, const uint8_t* codes_in,
+                           const int32_t* len_in, const uint8_t* codes_cur, const int32_t* index_map,
+                           const int32_t* len_out, uint8_t* codes_out, int32_t* dev_status,
+                           cudaStream_t stream);
 
 /* ---- 3. cache compaction -------------------------------------------------------
  * FAST-AR technical summary §2.A ("merging ... bounds the growth of the KV

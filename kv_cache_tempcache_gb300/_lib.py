@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libfastar.so")
 F32, BF16 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECAPACITY, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
 DEV_BAD_LEN, DEV_BAD_BUCKET, DEV_BAD_INDEX = 1, 2, 4
-OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA, OP_MATCH_ANN, OP_CROSS_ATTN = 1, 2, 3, 4, 5, 6
+OP_MATCH, OP_SORT, OP_SPARSE_ATTN, OP_ANNCA, OP_MATCH_ANN, OP_CROSS_ATTN, OP_MATCH_PQ = 1, 2, 3, 4, 5, 6, 7
 MAX_B, MAX_R, MAX_P = 256, 8, 1024
 
 _P = ctypes.c_void_p
@@ -44,6 +44,10 @@ _SIGS = {
     "fastar_cache_compact_merge": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
+    "fastar_pq_encode": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P],
+    "fastar_tempcache_match_pq": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _P, _L, _P, _I, _I, _F, _P, _P, _P,
+                                  _P, _P, _P, _S, _P],
+    "fastar_pq_gather_codes": [_I, _L, _L, _I, _P, _P, _P, _P, _P, _P, _P, _P],
     "fastar_sparse_attn": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P,
                            _P, _S, _P],
     "fastar_sparse_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _F, _P, _L,
@@ -208,6 +212,34 @@ def fastar_cache_compact_merge(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in,
           hs, ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(g_in),
           ptr(len_in), ptr(evict), ptr(top1), ptr(owner), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out),
           ptr(g_out), ptr(len_out), ptr(index_map), ptr(dev_status), stream_handle(stream))
+
+
+def fastar_pq_encode(x, codebooks, codes, stream=None):
+    """codebooks [H, m, Kc, d/m]; codes [H, n, m] uint8."""
+    H, n, d = x.shape
+    hs, ts = tok_strides(x)
+    _call("fastar_pq_encode", ptr(x), dtype_code(x.dtype), H, n, d, hs, ts, ptr(codebooks), codebooks.shape[1],
+          codebooks.shape[2], ptr(codes), stream_handle(stream))
+
+
+def fastar_tempcache_match_pq(q, k_cur, cache_k, cache_knorm, cache_codes, cache_len, codebooks, tau, top1, s1,
+                              evict, dev_status, workspace, stream=None, owner=None):
+    H, nq, d = q.shape
+    hs, ts = tok_strides(q)
+    if tok_strides(k_cur) != (hs, ts):
+        raise ValueError("q and k_cur must share strides")
+    _call("fastar_tempcache_match_pq", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, nq, d, hs, ts, ptr(cache_k),
+          ptr(cache_knorm), ptr(cache_codes), ptr(cache_len), cache_k.shape[1], ptr(codebooks), codebooks.shape[1],
+          codebooks.shape[2], float(tau), ptr(top1), ptr(s1), ptr(evict), ptr(owner), ptr(dev_status),
+          ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+          stream_handle(stream))
+
+
+def fastar_pq_gather_codes(codes_in, len_in, codes_cur, index_map, len_out, codes_out, dev_status=None,
+                           stream=None):
+    H, M, m = codes_in.shape
+    _call("fastar_pq_gather_codes", H, codes_cur.shape[1], M, m, ptr(codes_in), ptr(len_in), ptr(codes_cur),
+          ptr(index_map), ptr(len_out), ptr(codes_out), ptr(dev_status), stream_handle(stream))
 
 
 def fastar_bucket_sort(ids, B, perm, offsets, n_valid=None, dev_status=None, stream=None):

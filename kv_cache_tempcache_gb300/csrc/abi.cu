@@ -76,6 +76,9 @@ size_t fastar_workspace_bytes(int op, int H, int64_t n, int64_t M, int d, int B,
     case FASTAR_OP_MATCH_ANN:
       if ((d != 64 && d != 128) || B < 1 || r < 1 || M < 1) return 0;
       return fastar::match_ann_workspace(H, n, d, r, B, M);
+    case FASTAR_OP_MATCH_PQ:
+      if ((d != 64 && d != 128) || M < 1) return 0;
+      return fastar::match_pq_workspace(H, n, M, d);
     case FASTAR_OP_CROSS_ATTN:
       if ((d != 64 && d != 128) || P < 1 || F < 1) return 0;
       return 2 * sizeof(uint16_t) * (size_t)H * F * P * d + 1024;
@@ -207,6 +210,64 @@ int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M, c
       dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
       kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
       len_out, index_map, dev_status, top1, owner, g_in, g_out, stream));
+}
+
+int fastar_pq_encode(const void* x, int dtype, int H, int64_t n, int d, int64_t head_stride, int64_t token_stride,
+                     const void* codebooks, int m, int Kc, uint8_t* codes, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || n < 0 || m < 1 || Kc < 1) return FASTAR_EINVAL;
+  if (d % m || (d / m != 4 && d / m != 8) || Kc > FASTAR_MAX_PQ_KC) return FASTAR_EUNSUPPORTED;
+  if (H == 0 || n == 0) return FASTAR_OK;
+  if ((rc = check_tok(x, dtype, d, head_stride, token_stride, n, H))) return rc;
+  if (!codebooks || !aligned16(codebooks) || !codes || (reinterpret_cast<uintptr_t>(codes) & 3)) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_pq_encode(dtype, d, TokView{x, head_stride, token_stride}, H, n, m, Kc, codebooks,
+                                          codes, stream));
+}
+
+int fastar_tempcache_match_pq(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
+                              int64_t head_stride, int64_t token_stride, const void* cache_k,
+                              const float* cache_knorm, const uint8_t* cache_codes, const int32_t* cache_len,
+                              int64_t M, const void* codebooks, int m, int Kc, float tau, int32_t* top1, float* s1,
+                              uint8_t* evict, int32_t* owner, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (dtype != FASTAR_BF16) return FASTAR_EUNSUPPORTED;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || nq > INT32_MAX || m < 1 || Kc < 1) return FASTAR_EINVAL;
+  if (d % m || (d / m != 4 && d / m != 8) || Kc > FASTAR_MAX_PQ_KC) return FASTAR_EUNSUPPORTED;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (!cache_k || !aligned16(cache_k) || !cache_knorm || !cache_codes || !cache_len || !evict || !codebooks ||
+      !aligned16(codebooks))
+    return FASTAR_EINVAL;
+  if (nq > 0 && (!top1 || !s1)) return FASTAR_EINVAL;
+  const size_t need = fastar::match_pq_workspace(H, nq, M, d);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
+  if (nq == 0) {
+    cudaError_t e = cudaMemsetAsync(evict, 0, (size_t)H * M, stream);
+    if (e == cudaSuccess && owner) e = cudaMemsetAsync(owner, 0xff, sizeof(int32_t) * (size_t)H * M, stream);
+    return cuda_rc(e);
+  }
+  return cuda_rc(fastar::launch_tempcache_match_pq(
+      d, TokView{q, head_stride, token_stride}, TokView{k_cur, head_stride, token_stride}, H, nq, cache_k,
+      cache_knorm, cache_codes, cache_len, M, codebooks, m, Kc, tau, top1, s1, evict, owner, dev_status, workspace,
+      stream));
+}
+
+int fastar_pq_gather_codes(int H, int64_t nq, int64_t M, int m, const uint8_t* codes_in, const int32_t* len_in,
+                           const uint8_t* codes_cur, const int32_t* index_map, const int32_t* len_out,
+                           uint8_t* codes_out, int32_t* dev_status, cudaStream_t stream) {
+  if (H < 0 || nq < 0 || M < 1 || m < 4 || (m & 3) || M > INT32_MAX) return FASTAR_EINVAL;
+  if (H == 0) return FASTAR_OK;
+  const void* ptrs[] = {codes_in, codes_out};
+  for (const void* p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 3)) return FASTAR_EINVAL;
+  if (nq > 0 && (!codes_cur || (reinterpret_cast<uintptr_t>(codes_cur) & 3))) return FASTAR_EINVAL;
+  if (!len_in || !index_map || !len_out || codes_in == codes_out) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_pq_gather_codes(H, nq, M, m, codes_in, len_in, codes_cur, index_map, len_out,
+                                                codes_out, dev_status, stream));
 }
 
 int fastar_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B, const int32_t* n_valid,

@@ -43,6 +43,19 @@ cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kcur, in
                                    const int32_t* cache_len, int64_t M, float tau, int32_t* top1,
                                    float* s1, float* s2, uint8_t* evict, int32_t* owner,
                                    int32_t* status, void* ws, cudaStream_t s);
+// ---- product quantization (the quantised match) ---------------------------------------
+cudaError_t launch_pq_encode(int dtype, int d, TokView x, int H, int64_t n, int m, int Kc, const void* cb,
+                             uint8_t* codes, cudaStream_t s);
+cudaError_t launch_pq_decode(int d, int H, int64_t M, int m, int Kc, const uint8_t* codes, const int32_t* clen,
+                             const void* cb, void* khat, float* khat_norm, int32_t* status, cudaStream_t s);
+cudaError_t launch_pq_gather_codes(int H, int64_t nq, int64_t M, int m, const uint8_t* codes_in,
+                                   const int32_t* len_in, const uint8_t* codes_cur, const int32_t* imap,
+                                   const int32_t* len_out, uint8_t* codes_out, int32_t* status, cudaStream_t s);
+size_t match_pq_workspace(int H, int64_t nq, int64_t M, int d);
+cudaError_t launch_tempcache_match_pq(int d, TokView q, TokView kc, int H, int64_t nq, const void* ck,
+                                      const float* cknorm, const uint8_t* codes, const int32_t* clen, int64_t M,
+                                      const void* cb, int m, int Kc, float tau, int32_t* top1, float* s1,
+                                      uint8_t* evict, int32_t* owner, int32_t* status, void* ws, cudaStream_t s);
 cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M, TokView kcur,
                                  TokView vcur, const float* kcur_norm, const int32_t* kcur_bucket,
                                  const void* k_in, const void* v_in, const float* knorm_in,

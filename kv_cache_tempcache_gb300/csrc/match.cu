@@ -274,7 +274,14 @@ template <typename T, int D>
 static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const void* ck,
                               const float* cknorm, const int32_t* clen, int64_t M, float tau,
                               int32_t* top1, float* s1, float* s2, uint8_t* evict, int32_t* owner,
-                              int32_t* status, void* ws, cudaStream_t s) {
+                              int32_t* status, void* ws, cudaStream_t s, const void* ck_ev = nullptr,
+                              const float* kn_ev = nullptr) {
+  // the keys ranked (ck, cknorm) and the keys the eviction test uses (ck_ev, kn_ev) are
+  // the same except in the quantised match, which ranks decoded keys
+  if (!ck_ev) {
+    ck_ev = ck;
+    kn_ev = cknorm;
+  }
   float4* part = static_cast<float4*>(ws);
   if (sizeof(T) == 2 && nq > 0) {
     // bf16: the tensor-core kernel (the SIMT kernel below only if its set-up is refused)
@@ -286,7 +293,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
       const int64_t warps = (int64_t)H * nq;
       match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
           static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-          static_cast<const T*>(ck), cknorm, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner);
+          static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner);
       count_launches(1);
       return cudaGetLastError();
     }
@@ -319,7 +326,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   const int64_t warps = (int64_t)H * nq;
   match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-      static_cast<const T*>(ck), cknorm, clen, M, tau, splits, part, top1, s1, s2, evict, owner);
+      static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, splits, part, top1, s1, s2, evict, owner);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -338,6 +345,30 @@ cudaError_t launch_tempcache_match(int dtype, int d, TokView q, TokView kc, int 
   if (d == 128)
     return match_impl<float, 128>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner, status, ws, s);
   return match_impl<float, 64>(q, kc, H, nq, ck, cknorm, clen, M, tau, top1, s1, s2, evict, owner, status, ws, s);
+}
+
+// The quantised match: the cached keys' codes decoded into the workspace (bf16 rows and
+// their norms), ranked by the tensor-core match, the eviction tested on the true keys.
+size_t match_pq_workspace(int H, int64_t nq, int64_t M, int d) {
+  const size_t part = (match_workspace(H, nq, M) + 1023) & ~(size_t)1023;
+  return part + sizeof(uint16_t) * (size_t)H * M * d + sizeof(float) * (size_t)H * M + 1024;
+}
+
+cudaError_t launch_tempcache_match_pq(int d, TokView q, TokView kc, int H, int64_t nq, const void* ck,
+                                      const float* cknorm, const uint8_t* codes, const int32_t* clen, int64_t M,
+                                      const void* cb, int m, int Kc, float tau, int32_t* top1, float* s1,
+                                      uint8_t* evict, int32_t* owner, int32_t* status, void* ws, cudaStream_t s) {
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(ws) + 1023) & ~static_cast<uintptr_t>(1023);
+  uint8_t* khat = reinterpret_cast<uint8_t*>(base) + ((match_workspace(H, nq, M) + 1023) & ~(size_t)1023);
+  float* khat_norm = reinterpret_cast<float*>(khat + sizeof(uint16_t) * (size_t)H * M * d);
+  cudaError_t e = launch_pq_decode(d, H, M, m, Kc, codes, clen, cb, khat, khat_norm, status, s);
+  if (e != cudaSuccess) return e;
+  void* part = reinterpret_cast<void*>(base);
+  if (d == 128)
+    return match_impl<__nv_bfloat16, 128>(q, kc, H, nq, khat, khat_norm, clen, M, tau, top1, s1, nullptr, evict,
+                                          owner, status, part, s, ck, cknorm);
+  return match_impl<__nv_bfloat16, 64>(q, kc, H, nq, khat, khat_norm, clen, M, tau, top1, s1, nullptr, evict, owner,
+                                       status, part, s, ck, cknorm);
 }
 
 }  // namespace fastar

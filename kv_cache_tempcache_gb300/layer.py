@@ -19,6 +19,10 @@ merge=True runs the merge variant (technical summary §2.A, Theoretical Basis: L
 5.1): every cache entry carries a group count g; an evicted entry is folded into the
 current entry that owns it (count-weighted mean value, summed count) instead of being
 dropped, and AnnSA shifts every key's logit by ln g.
+
+pq=(m, Kc) runs the quantization variant of the match (technical summary §2.A, "LSH or
+Quantization"): every cache entry also carries its product-quantization code, the
+current keys are encoded each step, and the match ranks the decoded cached keys.
 """
 from __future__ import annotations
 
@@ -42,16 +46,17 @@ class CacheState:
     """One half of the double-buffered TempCache: rows, norms, buckets, lengths (and,
     for the merge variant, group counts)."""
 
-    def __init__(self, H, M, d, dtype, dev, grouped=False):
+    def __init__(self, H, M, d, dtype, dev, grouped=False, pq_m=0):
         self.k = torch.zeros((H, M, d), dtype=dtype, device=dev)
         self.v = torch.zeros((H, M, d), dtype=dtype, device=dev)
         self.knorm = _f32(H, M, dev=dev)
         self.kb = _i32(H, M, 1, dev=dev)
         self.len = _i32(H, dev=dev)
         self.g = _i32(H, M, dev=dev) if grouped else None
+        self.codes = torch.zeros((H, M, pq_m), dtype=torch.uint8, device=dev) if pq_m else None
 
     def nbytes(self) -> int:
-        ts = [self.k, self.v, self.knorm, self.kb, self.len] + ([self.g] if self.g is not None else [])
+        ts = [self.k, self.v, self.knorm, self.kb, self.len] + [t for t in (self.g, self.codes) if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
 
 
@@ -61,10 +66,11 @@ class FastARLayer:
     def __init__(self, H: int, d: int, Tf: int, F: int, M: int, B: int, r: int, P: int, tau: float,
                  tau_ca: float, topk: int = 16, dtype: torch.dtype = torch.bfloat16, gate: bool = True,
                  device: str | torch.device = "cuda", scale: Optional[float] = None,
-                 diagnostics: bool = False, merge: bool = False):
+                 diagnostics: bool = False, merge: bool = False, pq: Optional[tuple] = None):
         """diagnostics=True also produces the second-best match cosine s2 (a slower
         match epilogue); the step's results are the same either way.  merge=True: the
-        Lemma 5.1 merge variant (group counts, folded values, ln g logit shift)."""
+        Lemma 5.1 merge variant (group counts, folded values, ln g logit shift).  pq=(m, Kc):
+        the quantised match (set the codebooks with set_codebooks before loading a cache)."""
         L.load()
         if M < F * Tf:
             raise ValueError(f"cache cap M={M} must hold one chunk of {F * Tf} tokens")
@@ -73,12 +79,14 @@ class FastARLayer:
         self.tau, self.tau_ca, self.topk, self.gate = float(tau), float(tau_ca), int(topk), bool(gate)
         self.diagnostics = bool(diagnostics)
         self.merge = bool(merge)
+        self.pq = tuple(pq) if pq else None
+        pq_m = self.pq[0] if self.pq else 0
         self.dtype = dtype
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
         dev = torch.device(device)
         self.dev = dev
         Nq = self.Nq
-        self.caches = [CacheState(H, M, d, dtype, dev, self.merge), CacheState(H, M, d, dtype, dev, self.merge)]
+        self.caches = [CacheState(H, M, d, dtype, dev, self.merge, pq_m), CacheState(H, M, d, dtype, dev, self.merge, pq_m)]
         self.cur = 0
         # prompt
         self.kp = torch.zeros((H, P, d), dtype=dtype, device=dev)
@@ -93,7 +101,7 @@ class FastARLayer:
         self.s1 = _f32(H, Nq, dev=dev)
         self.s2 = _f32(H, Nq, dev=dev)
         self.evict = torch.zeros((H, M), dtype=torch.uint8, device=dev)
-        self.owner = _i32(H, M, dev=dev) if self.merge else None
+        self.owner = _i32(H, M, dev=dev) if (self.merge or pq) else None
         self.index_map = _i32(H, M, dev=dev)
         self.kperm = _i32(H, M, dev=dev)
         self.koff = _i32(H, B + 1, dev=dev)
@@ -116,6 +124,11 @@ class FastARLayer:
         self.ws_match = ws(L.OP_MATCH, n=Nq, M=M, d=d)
         self.ws_attn = ws(L.OP_SPARSE_ATTN, n=Nq, M=M, d=d, B=B, r=r)
         self.ws_cross = ws(L.OP_CROSS_ATTN, n=0, d=d, P=P, F=F) if P > 0 else None
+        if self.pq:
+            m, Kc = self.pq
+            self.codebooks = torch.zeros((H, m, Kc, d // m), dtype=dtype, device=dev)
+            self.codes_cur = torch.zeros((H, Nq, m), dtype=torch.uint8, device=dev)
+            self.ws_match_pq = ws(L.OP_MATCH_PQ, n=Nq, M=M, d=d)
         self.side = torch.cuda.Stream(device=dev)
         self.mside = torch.cuda.Stream(device=dev)
         self.match_first = True
@@ -137,6 +150,10 @@ class FastARLayer:
 
     def set_centroids(self, C: torch.Tensor):
         self.centroids.copy_(C)
+
+    def set_codebooks(self, cb: torch.Tensor):
+        """Product-quantization codebooks [H, m, Kc, d/m] (quantised-match mode)."""
+        self.codebooks.copy_(cb)
 
     def set_prompt(self, kp: torch.Tensor, vp: torch.Tensor):
         """Installs the prompt and assigns its key buckets (once per rollout)."""
@@ -161,6 +178,10 @@ class FastARLayer:
             L.fastar_bucket_assign(c.k[:, :n], self.centroids, 1, kb, None, kn)
             c.kb[:, :n].copy_(kb)
             c.knorm[:, :n].copy_(kn)
+        if c.codes is not None and n:
+            codes = torch.zeros((self.H, n, self.pq[0]), dtype=torch.uint8, device=self.dev)
+            L.fastar_pq_encode(c.k[:, :n], self.codebooks, codes)   # [H, n, m], contiguous
+            c.codes[:, :n].copy_(codes)
         if c.g is not None:
             if g is None:
                 c.g[:, :n].fill_(1)
@@ -189,9 +210,14 @@ class FastARLayer:
 
         def match(stream):
             t("tempcache_match", stream, "begin")
-            L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
-                                     self.s2 if self.diagnostics else None,
-                                     self.evict, self.dev_status, self.ws_match, owner=self.owner)
+            if self.pq:
+                L.fastar_tempcache_match_pq(q, k_cur, cin.k, cin.knorm, cin.codes, cin.len, self.codebooks,
+                                            self.tau, self.top1, self.s1, self.evict, self.dev_status,
+                                            self.ws_match_pq, owner=self.owner)
+            else:
+                L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1,
+                                         self.s2 if self.diagnostics else None,
+                                         self.evict, self.dev_status, self.ws_match, owner=self.owner)
             t("tempcache_match", stream, "end")
 
         # the match needs only the step's inputs and the incoming cache: it starts at once
@@ -209,6 +235,10 @@ class FastARLayer:
         L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
         L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
         t("bucket_assign", main, "end")
+        if self.pq:
+            t("pq_encode", main, "begin")
+            L.fastar_pq_encode(k_cur, self.codebooks, self.codes_cur)
+            t("pq_encode", main, "end")
         # the (query, slot) pairs by bucket serve both AnnSA and AnnCA
         t("bucket_sort_q", main, "begin")
         L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
@@ -242,6 +272,9 @@ class FastARLayer:
             L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                    cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
                                    self.index_map, self.dev_status)
+        if self.pq:
+            L.fastar_pq_gather_codes(cin.codes, cin.len, self.codes_cur, self.index_map, cout.len, cout.codes,
+                                     self.dev_status)
         t("cache_compact", main, "end")
         t("bucket_sort", main, "begin")
         L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)

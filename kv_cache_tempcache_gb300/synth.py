@@ -211,6 +211,21 @@ class DriftingMixture:
         return (np.concatenate(ks, axis=1), np.concatenate(vs, axis=1), np.concatenate(qs, axis=1))
 
 
+def pq_codebooks(keys: np.ndarray, m: int, Kc: int, seed: int = 0, dtype: str = "bf16") -> np.ndarray:
+    """Product-quantization codebooks [H, m, Kc, d/m] drawn from data: per head and
+    sub-space, the sub-vectors of Kc distinct rows of `keys` [H, n, d] picked at random
+    (a common codebook initialisation; no training)."""
+    H, n, d = keys.shape
+    ds = d // m
+    rng = np.random.default_rng(seed)
+    cb = np.empty((H, m, Kc, ds), np.float32)
+    for h in range(H):
+        for s in range(m):
+            rows = rng.choice(n, size=Kc, replace=False)
+            cb[h, s] = keys[h, rows, s * ds:(s + 1) * ds]
+    return bf16_round(cb) if dtype == "bf16" else cb
+
+
 def layer_step_inputs(cfg: LayerConfig, seed: int = 0, prior_frames: Optional[int] = None) -> dict:
     """Inputs of one layer step after `prior_frames` frames of history.
 

@@ -176,19 +176,26 @@ def tempcache_match_ann(Q, R, K_cache, kb_cache):
 # the quantised match ranks the cached keys by cos(q, decode(code(k))) and its eviction
 # test uses the true key, as the exact match's does.
 
-def pq_encode(X, codebooks) -> np.ndarray:
-    """codes[t, s] = argmin_c |x_t[s-th sub-vector] - codebooks[s, c]|^2 (lowest c on
-    ties).  X [n, d]; codebooks [m, Kc, d/m].  int64 [n, m]."""
+def pq_distances(X, codebooks) -> np.ndarray:
+    """dist[t, s, c] = |x_t[s-th sub-vector] - codebooks[s, c]|^2.  X [n, d];
+    codebooks [m, Kc, d/m].  [n, m, Kc]."""
     X = _f64(X)
     Cb = _f64(codebooks)
     m, Kc, ds = Cb.shape
-    n = X.shape[0]
-    codes = np.zeros((n, m), np.int64)
+    dist = np.zeros((X.shape[0], m, Kc))
     for s in range(m):
         sub = X[:, s * ds:(s + 1) * ds]
-        dist = ((sub[:, None, :] - Cb[s][None, :, :]) ** 2).sum(axis=2)     # [n, Kc]
-        codes[:, s] = np.argmin(dist, axis=1) if n else np.zeros(0, np.int64)
-    return codes
+        dist[:, s, :] = ((sub[:, None, :] - Cb[s][None, :, :]) ** 2).sum(axis=2)
+    return dist
+
+
+def pq_encode(X, codebooks) -> np.ndarray:
+    """codes[t, s] = argmin_c |x_t[s-th sub-vector] - codebooks[s, c]|^2 (lowest c on
+    ties).  int64 [n, m]."""
+    dist = pq_distances(X, codebooks)
+    if dist.shape[0] == 0:
+        return np.zeros((0, dist.shape[1]), np.int64)
+    return np.argmin(dist, axis=2).astype(np.int64)
 
 
 def pq_decode(codes, codebooks) -> np.ndarray:
