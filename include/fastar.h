@@ -395,6 +395,28 @@ int fastar_dense_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d
                               void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
                               cudaStream_t stream);
 
+/* ---- 9. the transformer around the attention step (a Wan-1.3B-shaped DiT) ---------
+ * Not on the pages: the dense operations of the diffusion transformer the attention
+ * layer sits in (projections, FFN, embeddings, norms, rotary positions), so that a
+ * whole chunk denoise runs on the library.  bf16 tensors, fp32 arithmetic. */
+
+#define FASTAR_ACT_NONE 0
+#define FASTAR_ACT_GELU_TANH 1    /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+#define FASTAR_ACT_SILU 2         /* v / (1 + exp(-v))                              */
+
+/* C[m, n] = R[m, n] + gate[n] * act(sum_k A[m, k] W[n, k] + bias[n])  on the tensor cores.
+ * A [M, K], W [N, K] (a torch Linear weight), C [M, N], R [M, N]: row-major bf16 with
+ * leading dimensions lda, ldw, ldc, ldr in elements (multiples of 8; 16-byte aligned
+ * bases).  bias [N] fp32 (NULL: 0).  R NULL: no residual term (C = act(...)).  With R,
+ * gate[n] = gate_a[n] + gate_b[n] (fp32; gate_b may be NULL; gate_a NULL: gate 1).
+ * c_dtype: FASTAR_BF16 or FASTAR_F32 for C (R is always bf16).
+ * M >= 1, N a multiple of 256, K a multiple of 64 (FASTAR_EUNSUPPORTED otherwise).
+ * C must not overlap A or W; it may be R (in-place residual update). */
+int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,
+                const void* R, int64_t ldr, const float* gate_a, const float* gate_b, void* C,
+                int64_t ldc, int c_dtype, int64_t M, int64_t N, int64_t K, int act, int32_t* dev_status,
+                cudaStream_t stream);
+
 /* Appends nq rows of k_cur/v_cur to an append-only dense cache [H, cap, d] at row
  * `at` (the dense baseline's growing cache).  Requires at + nq <= cap. */
 int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,

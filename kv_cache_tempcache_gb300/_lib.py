@@ -60,6 +60,7 @@ _SIGS = {
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _P, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
+    "fastar_gemm": [_P, _L, _P, _L, _P, _P, _L, _P, _P, _P, _L, _I, _L, _L, _L, _I, _P, _P],
 }
 _RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
              "fastar_kernel_launches": ctypes.c_longlong, "fastar_last_cuda_error": ctypes.c_char_p}
@@ -320,6 +321,21 @@ def fastar_dense_attn_grouped(q, k, v, nk, group_count, scale, out, lse=None, st
     _call("fastar_dense_attn_grouped", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, ptr(k), ptr(v), int(nk), kh,
           kt, ptr(group_count), group_count.shape[1], float(scale), ptr(out), oh, ot, ptr(lse),
           stream_handle(stream))
+
+
+ACT_NONE, ACT_GELU_TANH, ACT_SILU = 0, 1, 2
+
+
+def fastar_gemm(A, W, C, bias=None, R=None, gate_a=None, gate_b=None, act=ACT_NONE, dev_status=None, stream=None):
+    """C = R + gate * act(A @ W^T + bias); A [M, K], W [N, K], C/R [M, N] (2-D row views)."""
+    M, K = A.shape
+    N = W.shape[0]
+    for t in (A, W, C) + ((R,) if R is not None else ()):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("GEMM operands must be 2-D row-major views")
+    _call("fastar_gemm", A.data_ptr(), A.stride(0), W.data_ptr(), W.stride(0), ptr(bias),
+          None if R is None else R.data_ptr(), 0 if R is None else R.stride(0), ptr(gate_a), ptr(gate_b),
+          C.data_ptr(), C.stride(0), dtype_code(C.dtype), M, N, K, int(act), ptr(dev_status), stream_handle(stream))
 
 
 def fastar_dense_append(k_cur, v_cur, k_cache, v_cache, at, stream=None):

@@ -497,6 +497,22 @@ int dense_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t 
 
 extern "C" {
 
+int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias, const void* R,
+                int64_t ldr, const float* gate_a, const float* gate_b, void* C, int64_t ldc, int c_dtype, int64_t M,
+                int64_t N, int64_t K, int act, int32_t* dev_status, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || act < FASTAR_ACT_NONE || act > FASTAR_ACT_SILU) return FASTAR_EINVAL;
+  if (c_dtype != FASTAR_BF16 && c_dtype != FASTAR_F32) return FASTAR_EUNSUPPORTED;
+  if (M == 0 || N == 0) return FASTAR_OK;
+  if (K == 0 || N % 256 || K % 64) return FASTAR_EUNSUPPORTED;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FASTAR_ECAPACITY;
+  if (!A || !W || !C || !aligned16(A) || !aligned16(W) || !aligned16(C)) return FASTAR_EINVAL;
+  if (lda < K || ldw < K || ldc < N || (lda & 7) || (ldw & 7) || (ldc & 7)) return FASTAR_EINVAL;
+  if (R && (!aligned16(R) || ldr < N || (ldr & 7))) return FASTAR_EINVAL;
+  if (C == A || C == W) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_gemm_tc(A, lda, W, ldw, bias, R, ldr, gate_a, gate_b, C, ldc,
+                                        c_dtype == FASTAR_F32 ? 1 : 0, M, N, K, act, dev_status, stream));
+}
+
 int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,
                         int64_t head_stride, int64_t token_stride, void* k_cache, void* v_cache, int64_t cap,
                         int64_t at, cudaStream_t stream) {

@@ -147,6 +147,11 @@ cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64
                                 int32_t* kidx, int32_t* kcnt, float* score, void* ws,
                                 cudaStream_t s);
 
+// ---- the transformer around the attention step ----------------------------------------
+cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,
+                           const void* res, int64_t ldr, const float* gate_a, const float* gate_b, void* C, int64_t ldc,
+                           int c_f32, int64_t M, int64_t N, int64_t K, int act, int32_t* status, cudaStream_t s);
+
 // ---- dense cache append --------------------------------------------------------------
 cudaError_t launch_dense_append(int dtype, int d, int H, int64_t nq, TokView kcur, TokView vcur,
                                 void* k_cache, void* v_cache, int64_t cap, int64_t at,
