@@ -417,6 +417,32 @@ int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const fl
                 int64_t ldc, int c_dtype, int64_t M, int64_t N, int64_t K, int act, int32_t* dev_status,
                 cudaStream_t stream);
 
+/* Layer norm of the n rows of x [n, C] (row stride ldx; bf16, C a multiple of 8, <= 4096)
+ * with adaptive modulation, into out (row stride ldo; may be x):
+ *   y = (x - mean) / sqrt(var + eps)  [* weight[c] + bias[c]]  (weight NULL: no affine)
+ *   out = y * (1 + scale[c]) + shift[c],  scale = scale_a + scale_b, shift = shift_a + shift_b
+ * (fp32 vectors [C]; any of the four may be NULL, counting 0).  var is the biased
+ * variance.  eps > 0. */
+int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps, const float* weight,
+                         const float* bias, const float* shift_a, const float* shift_b,
+                         const float* scale_a, const float* scale_b, void* out, int64_t ldo,
+                         cudaStream_t stream);
+
+/* In place on the n rows of x [n, C] (bf16, row stride ldx), C = H * d:
+ *   weight non-NULL: RMS norm over the row, x / sqrt(mean(x^2) + eps) * weight[c];
+ *   rope != 0: rotary positions per head of d channels, split into frame / row / column
+ *   parts of dt = d - 4 floor(d / 6), dh = dw = 2 floor(d / 6) channels; in a part of da
+ *   channels the pair (2j, 2j + 1) turns by the angle pos * theta^(-2j / da), where token i
+ *   sits at frame t0 + i / (grid_h grid_w), row (i / grid_w) % grid_h, column i % grid_w.
+ * d even and >= 12, C a multiple of d and of 8, C <= 4096. */
+int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* weight,
+                        int rope, int t0, int grid_h, int grid_w, float theta, cudaStream_t stream);
+
+/* The sinusoidal timestep embedding of the nb timesteps t (device fp32): out[b, i] =
+ * cos(t_b f_i), out[b, dim/2 + i] = sin(t_b f_i), f_i = 10000^(-i / (dim/2)); bf16 rows of
+ * stride ldo. */
+int fastar_sinusoidal_embedding(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t stream);
+
 /* Appends nq rows of k_cur/v_cur to an append-only dense cache [H, cap, d] at row
  * `at` (the dense baseline's growing cache).  Requires at + nq <= cap. */
 int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,

@@ -61,6 +61,9 @@ _SIGS = {
     "fastar_dense_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _P, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
     "fastar_gemm": [_P, _L, _P, _L, _P, _P, _L, _P, _P, _P, _L, _I, _L, _L, _L, _I, _P, _P],
+    "fastar_layernorm_mod": [_P, _L, _L, _I, _F, _P, _P, _P, _P, _P, _P, _P, _L, _P],
+    "fastar_rmsnorm_rope": [_P, _L, _L, _I, _I, _F, _P, _I, _I, _I, _I, _F, _P],
+    "fastar_sinusoidal_embedding": [_P, _I, _I, _P, _L, _P],
 }
 _RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
              "fastar_kernel_launches": ctypes.c_longlong, "fastar_last_cuda_error": ctypes.c_char_p}
@@ -336,6 +339,26 @@ def fastar_gemm(A, W, C, bias=None, R=None, gate_a=None, gate_b=None, act=ACT_NO
     _call("fastar_gemm", A.data_ptr(), A.stride(0), W.data_ptr(), W.stride(0), ptr(bias),
           None if R is None else R.data_ptr(), 0 if R is None else R.stride(0), ptr(gate_a), ptr(gate_b),
           C.data_ptr(), C.stride(0), dtype_code(C.dtype), M, N, K, int(act), ptr(dev_status), stream_handle(stream))
+
+
+def fastar_layernorm_mod(x, out, eps=1e-6, weight=None, bias=None, shift_a=None, shift_b=None, scale_a=None,
+                         scale_b=None, stream=None):
+    """out = LN(x) [* weight + bias] * (1 + scale) + shift over the rows of x [n, C]."""
+    n, C = x.shape
+    _call("fastar_layernorm_mod", x.data_ptr(), x.stride(0), n, C, float(eps), ptr(weight), ptr(bias), ptr(shift_a),
+          ptr(shift_b), ptr(scale_a), ptr(scale_b), out.data_ptr(), out.stride(0), stream_handle(stream))
+
+
+def fastar_rmsnorm_rope(x, d, weight=None, rope=False, t0=0, grid=(1, 1), eps=1e-6, theta=10000.0, stream=None):
+    """In place on x [n, C]: RMS norm (weight given) then rotary positions (rope)."""
+    n, C = x.shape
+    _call("fastar_rmsnorm_rope", x.data_ptr(), x.stride(0), n, C, int(d), float(eps), ptr(weight), int(bool(rope)),
+          int(t0), int(grid[0]), int(grid[1]), float(theta), stream_handle(stream))
+
+
+def fastar_sinusoidal_embedding(t, out, stream=None):
+    nb, dim = out.shape
+    _call("fastar_sinusoidal_embedding", ptr(t), nb, dim, out.data_ptr(), out.stride(0), stream_handle(stream))
 
 
 def fastar_dense_append(k_cur, v_cur, k_cache, v_cache, at, stream=None):

@@ -513,6 +513,34 @@ int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const fl
                                         c_dtype == FASTAR_F32 ? 1 : 0, M, N, K, act, dev_status, stream));
 }
 
+int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps, const float* weight,
+                         const float* bias, const float* shift_a, const float* shift_b, const float* scale_a,
+                         const float* scale_b, void* out, int64_t ldo, cudaStream_t stream) {
+  if (n < 0 || C < 8 || C % 8 || C > 4096 || !(eps > 0.f)) return FASTAR_EINVAL;
+  if (n == 0) return FASTAR_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out) || ldx < C || ldo < C || (ldx & 7) || (ldo & 7))
+    return FASTAR_EINVAL;
+  if (bias && !weight) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_layernorm_mod(x, ldx, n, C, eps, weight, bias, shift_a, shift_b, scale_a, scale_b,
+                                              out, ldo, stream));
+}
+
+int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* weight, int rope,
+                        int t0, int grid_h, int grid_w, float theta, cudaStream_t stream) {
+  if (n < 0 || C < 8 || C % 8 || C > 4096 || d < 12 || d % 2 || C % d || !(eps > 0.f)) return FASTAR_EINVAL;
+  if (rope && (grid_h < 1 || grid_w < 1 || !(theta > 1.f) || t0 < 0)) return FASTAR_EINVAL;
+  if (n == 0) return FASTAR_OK;
+  if (!x || !aligned16(x) || ldx < C || (ldx & 7)) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_rmsnorm_rope(x, ldx, n, C, d, eps, weight, rope, t0, grid_h, grid_w, theta, stream));
+}
+
+int fastar_sinusoidal_embedding(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t stream) {
+  if (nb < 0 || dim < 2 || dim % 2 || ldo < dim) return FASTAR_EINVAL;
+  if (nb == 0) return FASTAR_OK;
+  if (!t || !out) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_sinusoidal(t, nb, dim, out, ldo, stream));
+}
+
 int fastar_dense_append(int dtype, int H, int64_t nq, int d, const void* k_cur, const void* v_cur,
                         int64_t head_stride, int64_t token_stride, void* k_cache, void* v_cache, int64_t cap,
                         int64_t at, cudaStream_t stream) {

@@ -152,6 +152,13 @@ cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ld
                            const void* res, int64_t ldr, const float* gate_a, const float* gate_b, void* C, int64_t ldc,
                            int c_f32, int64_t M, int64_t N, int64_t K, int act, int32_t* status, cudaStream_t s);
 
+cudaError_t launch_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps, const float* w,
+                                 const float* b, const float* sha, const float* shb, const float* sca,
+                                 const float* scb, void* out, int64_t ldo, cudaStream_t s);
+cudaError_t launch_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* w, int rope,
+                                int t0, int gh, int gw, float theta, cudaStream_t s);
+cudaError_t launch_sinusoidal(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t s);
+
 // ---- dense cache append --------------------------------------------------------------
 cudaError_t launch_dense_append(int dtype, int d, int H, int64_t nq, TokView kcur, TokView vcur,
                                 void* k_cache, void* v_cache, int64_t cap, int64_t at,

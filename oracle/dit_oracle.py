@@ -54,3 +54,69 @@ def gemm(A, W, bias=None, act: int = 0, R=None, gate=None) -> np.ndarray:
         g = np.ones(Y.shape[1]) if gate is None else _f64(gate)
         Y = _f64(R) + g[None, :] * Y
     return Y
+
+
+# ----------------------------------------------------------------------------------
+# norms, rotary positions, timestep embedding
+# ----------------------------------------------------------------------------------
+
+def layer_norm(x, eps: float, weight=None, bias=None) -> np.ndarray:
+    """(x - mean) / sqrt(var + eps) over the last axis (biased variance) [* weight + bias]."""
+    x = _f64(x)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    y = (x - mu) / np.sqrt(var + eps)
+    if weight is not None:
+        y = y * _f64(weight) + (0.0 if bias is None else _f64(bias))
+    return y
+
+
+def modulate(y, shift, scale) -> np.ndarray:
+    """adaLN: y * (1 + scale) + shift (per channel)."""
+    return _f64(y) * (1.0 + _f64(scale)) + _f64(shift)
+
+
+def rms_norm(x, weight, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * weight over the last axis."""
+    x = _f64(x)
+    return x / np.sqrt((x ** 2).mean(axis=-1, keepdims=True) + eps) * _f64(weight)
+
+
+def rope_split(d: int):
+    """Channels of a head given to the frame, row and column positions."""
+    part = 2 * (d // 6)
+    return d - 2 * part, part, part
+
+
+def token_positions(n: int, t0: int, gh: int, gw: int) -> np.ndarray:
+    """(frame, row, column) of the n tokens of a chunk, frame-major: [n, 3]."""
+    i = np.arange(n)
+    return np.stack([t0 + i // (gh * gw), (i // gw) % gh, i % gw], axis=1)
+
+
+def rope(x, d: int, pos, theta: float = 10000.0) -> np.ndarray:
+    """Rotary positions on x [n, H*d] (token-major): in each head, the channels split
+    into frame / row / column parts (rope_split); in a part of width da the pair
+    (2j, 2j + 1) is turned by pos_axis * theta^(-2j / da)."""
+    x = _f64(x).copy()
+    n, C = x.shape
+    pos = np.asarray(pos, np.float64)
+    widths = rope_split(d)
+    for h in range(C // d):
+        base = h * d
+        for axis, da in enumerate(widths):
+            for j in range(da // 2):
+                c = base + sum(widths[:axis]) + 2 * j
+                ang = pos[:, axis] * theta ** (-2.0 * j / da)
+                a0, a1 = x[:, c].copy(), x[:, c + 1].copy()
+                x[:, c] = a0 * np.cos(ang) - a1 * np.sin(ang)
+                x[:, c + 1] = a0 * np.sin(ang) + a1 * np.cos(ang)
+    return x
+
+
+def sinusoidal(t, dim: int) -> np.ndarray:
+    """[cos(t f_i), sin(t f_i)], f_i = 10000^(-i / (dim/2)), for each t: [len(t), dim]."""
+    t = _f64(np.atleast_1d(t))
+    half = dim // 2
+    ang = t[:, None] * 10000.0 ** (-np.arange(half) / half)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)

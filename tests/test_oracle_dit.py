@@ -59,3 +59,57 @@ def test_activations():
     assert D.gelu_tanh(0.0) == 0.0
     np.testing.assert_allclose(D.silu(x), x * (1 / (1 + np.exp(-x))), atol=1e-15)
     assert abs(D.silu(1.0) - 0.7310585786300049) < 1e-15           # 1 / (1 + e^-1)
+
+
+def test_layer_norm_and_modulation():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((20, 48)) * 3 + 5
+    y = D.layer_norm(x, 1e-12)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-12)
+    np.testing.assert_allclose(y.std(axis=1), 1, atol=1e-9)
+    w, b = rng.standard_normal(48), rng.standard_normal(48)
+    np.testing.assert_allclose(D.layer_norm(x, 1e-12, w, b), y * w + b, atol=1e-12)
+    # zero modulation is the identity; scale -1 leaves the shift alone
+    np.testing.assert_array_equal(D.modulate(y, np.zeros(48), np.zeros(48)), y)
+    np.testing.assert_allclose(D.modulate(y, b, -np.ones(48)), np.broadcast_to(b, y.shape), atol=0)
+
+
+def test_rms_norm():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((10, 64)) * 7
+    y = D.rms_norm(x, np.ones(64), 1e-12)
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(axis=1)), 1, atol=1e-9)
+    np.testing.assert_allclose(D.rms_norm(2 * x, np.ones(64), 1e-12), y, atol=1e-12)   # scale invariant
+
+
+def test_rope_properties():
+    rng = np.random.default_rng(6)
+    d, H, n = 36, 2, 40
+    q, k = rng.standard_normal((n, H * d)), rng.standard_normal((n, H * d))
+    pos = D.token_positions(n, 3, 4, 5)
+    assert D.rope_split(128) == (44, 42, 42)
+    # position 0 is the identity; every pair keeps its length
+    np.testing.assert_array_equal(D.rope(q, d, np.zeros((n, 3))), q)
+    r = D.rope(q, d, pos)
+    np.testing.assert_allclose((r.reshape(n, -1, 2) ** 2).sum(-1), (q.reshape(n, -1, 2) ** 2).sum(-1), atol=1e-12)
+    # the score of a rotated pair depends only on the difference of positions
+    shift = np.array([2, 1, 3])
+    qa, ka = D.rope(q, d, pos), D.rope(k, d, pos)
+    qb, kb = D.rope(q, d, pos + shift), D.rope(k, d, pos + shift)
+    for h in range(H):
+        s = slice(h * d, (h + 1) * d)
+        np.testing.assert_allclose(qa[:, s] @ ka[:, s].T, qb[:, s] @ kb[:, s].T, atol=1e-9)
+    # one pair by hand: frame axis, pair 0 turns by the frame index (theta^0 = 1)
+    x = np.zeros((1, d))
+    x[0, 0] = 1.0
+    got = D.rope(x, d, np.array([[0.7, 0, 0]]))
+    np.testing.assert_allclose(got[0, :2], [np.cos(0.7), np.sin(0.7)], atol=1e-15)
+    np.testing.assert_array_equal(D.token_positions(7, 2, 2, 3)[5], [2, 1, 2])
+    np.testing.assert_array_equal(D.token_positions(7, 2, 2, 3)[6], [3, 0, 0])
+
+
+def test_sinusoidal():
+    e = D.sinusoidal([0.0, 1.0], 8)
+    np.testing.assert_array_equal(e[0], [1, 1, 1, 1, 0, 0, 0, 0])
+    np.testing.assert_allclose(e[1, 0], np.cos(1.0), atol=1e-15)
+    np.testing.assert_allclose(e[1, 4 + 2], np.sin(1.0 * 10000.0 ** (-2 / 4)), atol=1e-15)
