@@ -433,10 +433,13 @@ int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps
  *   rope != 0: rotary positions per head of d channels, split into frame / row / column
  *   parts of dt = d - 4 floor(d / 6), dh = dw = 2 floor(d / 6) channels; in a part of da
  *   channels the pair (2j, 2j + 1) turns by the angle pos * theta^(-2j / da), where token i
- *   sits at frame t0 + i / (grid_h grid_w), row (i / grid_w) % grid_h, column i % grid_w.
+ *   sits at frame f0 + i / (grid_h grid_w), row (i / grid_w) % grid_h, column i % grid_w,
+ *   f0 = t0 + *t0_dev (t0_dev optional, device int32: lets a captured graph follow the
+ *   rollout).
  * d even and >= 12, C a multiple of d and of 8, C <= 4096. */
 int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* weight,
-                        int rope, int t0, int grid_h, int grid_w, float theta, cudaStream_t stream);
+                        int rope, int t0, const int32_t* t0_dev, int grid_h, int grid_w, float theta,
+                        cudaStream_t stream);
 
 /* The sinusoidal timestep embedding of the nb timesteps t (device fp32): out[b, i] =
  * cos(t_b f_i), out[b, dim/2 + i] = sin(t_b f_i), f_i = 10000^(-i / (dim/2)); bf16 rows of

@@ -62,7 +62,7 @@ _SIGS = {
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
     "fastar_gemm": [_P, _L, _P, _L, _P, _P, _L, _P, _P, _P, _L, _I, _L, _L, _L, _I, _P, _P],
     "fastar_layernorm_mod": [_P, _L, _L, _I, _F, _P, _P, _P, _P, _P, _P, _P, _L, _P],
-    "fastar_rmsnorm_rope": [_P, _L, _L, _I, _I, _F, _P, _I, _I, _I, _I, _F, _P],
+    "fastar_rmsnorm_rope": [_P, _L, _L, _I, _I, _F, _P, _I, _I, _P, _I, _I, _F, _P],
     "fastar_sinusoidal_embedding": [_P, _I, _I, _P, _L, _P],
 }
 _RESTYPES = {"fastar_status_string": ctypes.c_char_p, "fastar_workspace_bytes": ctypes.c_size_t,
@@ -349,11 +349,13 @@ def fastar_layernorm_mod(x, out, eps=1e-6, weight=None, bias=None, shift_a=None,
           ptr(shift_b), ptr(scale_a), ptr(scale_b), out.data_ptr(), out.stride(0), stream_handle(stream))
 
 
-def fastar_rmsnorm_rope(x, d, weight=None, rope=False, t0=0, grid=(1, 1), eps=1e-6, theta=10000.0, stream=None):
-    """In place on x [n, C]: RMS norm (weight given) then rotary positions (rope)."""
+def fastar_rmsnorm_rope(x, d, weight=None, rope=False, t0=0, grid=(1, 1), eps=1e-6, theta=10000.0, stream=None,
+                        t0_dev=None):
+    """In place on x [n, C]: RMS norm (weight given) then rotary positions (rope); the
+    chunk's first frame is t0 + t0_dev[0] (t0_dev: optional device int32)."""
     n, C = x.shape
     _call("fastar_rmsnorm_rope", x.data_ptr(), x.stride(0), n, C, int(d), float(eps), ptr(weight), int(bool(rope)),
-          int(t0), int(grid[0]), int(grid[1]), float(theta), stream_handle(stream))
+          int(t0), ptr(t0_dev), int(grid[0]), int(grid[1]), float(theta), stream_handle(stream))
 
 
 def fastar_sinusoidal_embedding(t, out, stream=None):

@@ -526,12 +526,13 @@ int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps
 }
 
 int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* weight, int rope,
-                        int t0, int grid_h, int grid_w, float theta, cudaStream_t stream) {
+                        int t0, const int32_t* t0_dev, int grid_h, int grid_w, float theta, cudaStream_t stream) {
   if (n < 0 || C < 8 || C % 8 || C > 4096 || d < 12 || d % 2 || C % d || !(eps > 0.f)) return FASTAR_EINVAL;
   if (rope && (grid_h < 1 || grid_w < 1 || !(theta > 1.f) || t0 < 0)) return FASTAR_EINVAL;
   if (n == 0) return FASTAR_OK;
   if (!x || !aligned16(x) || ldx < C || (ldx & 7)) return FASTAR_EINVAL;
-  return cuda_rc(fastar::launch_rmsnorm_rope(x, ldx, n, C, d, eps, weight, rope, t0, grid_h, grid_w, theta, stream));
+  return cuda_rc(
+      fastar::launch_rmsnorm_rope(x, ldx, n, C, d, eps, weight, rope, t0, t0_dev, grid_h, grid_w, theta, stream));
 }
 
 int fastar_sinusoidal_embedding(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t stream) {

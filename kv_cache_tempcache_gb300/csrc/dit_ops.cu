@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(256)
 template <int NV>
 __global__ void __launch_bounds__(256)
     rmsnorm_rope_kernel(__nv_bfloat16* __restrict__ x, int64_t ldx, int64_t n, int C, int d, float eps,
-                        const float* __restrict__ w, int rope, int t0, int gh, int gw, float theta) {
+                        const float* __restrict__ w, int rope, int t0, const int32_t* t0_dev, int gh, int gw,
+                        float theta) {
   const int64_t row = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= n) return;
@@ -114,7 +115,8 @@ __global__ void __launch_bounds__(256)
     }
   }
   const float r = w ? rsqrtf(warp_sum(q) / (float)C + eps) : 1.f;
-  const int pos[3] = {t0 + (int)(row / ((int64_t)gh * gw)), (int)((row / gw) % gh), (int)(row % gw)};
+  const int f0 = t0 + (t0_dev ? t0_dev[0] : 0);   // a device offset keeps replayed graphs current
+  const int pos[3] = {f0 + (int)(row / ((int64_t)gh * gw)), (int)((row / gw) % gh), (int)(row % gw)};
   const int part = 2 * (d / 6);
   const int dt = d - 2 * part;
 #pragma unroll
@@ -176,10 +178,10 @@ cudaError_t ln_impl(const void* x, int64_t ldx, int64_t n, int C, float eps, con
 
 template <int NV>
 cudaError_t rope_impl(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* w, int rope, int t0,
-                      int gh, int gw, float theta, cudaStream_t s) {
+                      const int32_t* t0_dev, int gh, int gw, float theta, cudaStream_t s) {
   const int64_t blocks = (n * 32 + 255) / 256;
   rmsnorm_rope_kernel<NV><<<(unsigned)blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(x), ldx, n, C, d, eps, w,
-                                                           rope, t0, gh, gw, theta);
+                                                           rope, t0, t0_dev, gh, gw, theta);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -196,11 +198,11 @@ cudaError_t launch_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, f
 }
 
 cudaError_t launch_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* w, int rope,
-                                int t0, int gh, int gw, float theta, cudaStream_t s) {
+                                int t0, const int32_t* t0_dev, int gh, int gw, float theta, cudaStream_t s) {
   const int nv = (C / 8 + 31) / 32;
-  if (nv <= 2) return rope_impl<2>(x, ldx, n, C, d, eps, w, rope, t0, gh, gw, theta, s);
-  if (nv <= 6) return rope_impl<6>(x, ldx, n, C, d, eps, w, rope, t0, gh, gw, theta, s);
-  return rope_impl<kMaxV>(x, ldx, n, C, d, eps, w, rope, t0, gh, gw, theta, s);
+  if (nv <= 2) return rope_impl<2>(x, ldx, n, C, d, eps, w, rope, t0, t0_dev, gh, gw, theta, s);
+  if (nv <= 6) return rope_impl<6>(x, ldx, n, C, d, eps, w, rope, t0, t0_dev, gh, gw, theta, s);
+  return rope_impl<kMaxV>(x, ldx, n, C, d, eps, w, rope, t0, t0_dev, gh, gw, theta, s);
 }
 
 cudaError_t launch_sinusoidal(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t s) {

@@ -156,7 +156,7 @@ cudaError_t launch_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, f
                                  const float* b, const float* sha, const float* shb, const float* sca,
                                  const float* scb, void* out, int64_t ldo, cudaStream_t s);
 cudaError_t launch_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* w, int rope,
-                                int t0, int gh, int gw, float theta, cudaStream_t s);
+                                int t0, const int32_t* t0_dev, int gh, int gw, float theta, cudaStream_t s);
 cudaError_t launch_sinusoidal(const float* t, int nb, int dim, void* out, int64_t ldo, cudaStream_t s);
 
 // ---- dense cache append --------------------------------------------------------------

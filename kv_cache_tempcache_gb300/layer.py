@@ -293,6 +293,41 @@ class FastARLayer:
             ev2.record(side)
             main.wait_event(ev2)
 
+    # ---- the two halves of the step, for a transformer block that projects its own
+    # cross-attention queries (the self step commits the cache only with advance=True) ----
+    def step_self(self, q, k_cur, v_cur, out=None, advance: bool = True):
+        """TempCache + AnnSA on the current stream: bucket assignment of q and k_cur, the
+        match against the current cache, compaction into the other half, the bucket sorts
+        and the bucket-restricted attention -> out ([H, Nq, d] view; default o_self)."""
+        cin, cout = self.caches[self.cur], self.caches[1 - self.cur]
+        o = self.o_self if out is None else out
+        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
+        L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
+        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, None,
+                                 self.evict, self.dev_status, self.ws_match)
+        L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb, cin.len,
+                               self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len, self.index_map,
+                               self.dev_status)
+        L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
+        L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
+                             self.scale, o, self.lse_self, self.dev_status, self.ws_attn)
+        if advance:
+            self.cur = 1 - self.cur
+        return o
+
+    def step_cross(self, q, out=None):
+        """AnnCA on the current stream for its own queries q: their buckets, the
+        frame-relevant prompt tokens, cross-attention over them -> out (default o_cross)."""
+        o = self.o_cross if out is None else out
+        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
+        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate, self.keep,
+                              self.kidx, self.kcnt, self.score, B=self.B, qperm=self.qperm, qoff=self.qoff)
+        L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale, o,
+                                   self.lse_cross, workspace=self.ws_cross)
+        return o
+
     def step(self, q, k_cur, v_cur, advance: bool = True, timer=None, serial: bool = False):
         """Runs one chunk step (asynchronously, on the current stream).  With
         advance=False the cache state is not swapped, so the same step can be repeated;
@@ -354,6 +389,22 @@ class DenseLayer:
     def set_prompt(self, kp, vp):
         self.kp.copy_(kp)
         self.vp.copy_(vp)
+
+    def step_self(self, q, k_cur, v_cur, out=None, advance: bool = True):
+        """Appends the chunk (at the current length; committed with advance=True) and
+        attends over every key so far -> out ([H, Nq, d] view; default o_self)."""
+        o = self.o_self if out is None else out
+        nq = q.shape[1]
+        L.fastar_dense_append(k_cur, v_cur, self.k, self.v, self.n)
+        L.fastar_dense_attn(q, self.k, self.v, self.n + nq, self.scale, o, self.lse_self)
+        if advance:
+            self.n += nq
+        return o
+
+    def step_cross(self, q, out=None):
+        o = self.o_cross if out is None else out
+        L.fastar_dense_attn(q, self.kp, self.vp, self.P, self.scale, o, self.lse_cross)
+        return o
 
     def step(self, q, k_cur, v_cur, advance: bool = True, timer=None):
         nq = q.shape[1]

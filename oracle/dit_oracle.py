@@ -120,3 +120,70 @@ def sinusoidal(t, dim: int) -> np.ndarray:
     half = dim // 2
     ang = t[:, None] * 10000.0 ** (-np.arange(half) / half)[None, :]
     return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+# ----------------------------------------------------------------------------------
+# the denoising step of the transformer (dense attention; the history is the oracle's)
+# ----------------------------------------------------------------------------------
+
+def softmax_attention(Q, K, V, scale: float) -> np.ndarray:
+    """Row softmax(Q K^T * scale) V, max-subtracted.  Q [n, d], K, V [m, d]."""
+    S = _f64(Q) @ _f64(K).T * scale
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    return (P / P.sum(axis=1, keepdims=True)) @ _f64(V)
+
+
+def heads_attention(Q, K, V, H: int) -> np.ndarray:
+    """Multi-head attention on token-major [n, H*d] tensors, scale 1/sqrt(d)."""
+    d = Q.shape[1] // H
+    out = np.zeros((Q.shape[0], H * d))
+    for h in range(H):
+        s = slice(h * d, (h + 1) * d)
+        out[:, s] = softmax_attention(Q[:, s], K[:, s], V[:, s], 1.0 / np.sqrt(d))
+    return out
+
+
+def text_context(p, text) -> np.ndarray:
+    """The text encoder output projected to the model width: GELU MLP."""
+    return gemm(gemm(text, p["text_w1"], p["text_b1"], act=1), p["text_w2"], p["text_b2"])
+
+
+def block_text_kv(b, ctx, d: int, eps: float):
+    """A block's cross-attention keys (RMS-normed) and values over the text."""
+    return rms_norm(gemm(ctx, b["ck_w"], b["ck_b"]), b["norm_ck"], eps), gemm(ctx, b["cv_w"], b["cv_b"])
+
+
+def dit_step(p, cfg, lat, t: float, t_next: float, frame0: int, history, text_kv, rope_on: bool = True):
+    """One denoising step of the chunk.  p: parameters (float arrays; blocks a list of
+    dicts); lat [tokens, patch_ch] the latent; history[i] = (K, V) of block i's earlier
+    chunks (token-major, keys already rotated); text_kv[i] = (K, V) over the text.
+    Returns (the updated latent, [(k, v) of the chunk for every block])."""
+    D, H, d, eps = cfg.dim, cfg.heads, cfg.dim // cfg.heads, cfg.eps
+    emb = sinusoidal([t * 1000.0], cfg.freq_dim)
+    e1 = gemm(emb, p["time_w1"], p["time_b1"], act=2)
+    e = gemm(e1, p["time_w2"], p["time_b2"])[0]
+    e0 = gemm(silu(e)[None, :], p["proj_w"], p["proj_b"])[0].reshape(6, D)
+    x = gemm(lat, p["patch_w"], p["patch_b"])
+    pos = token_positions(x.shape[0], frame0, cfg.grid_h, cfg.grid_w)
+    kv_out = []
+    for b, (hk, hv), (tk, tv) in zip(p["blocks"], history, text_kv):
+        m = b["mod"] + e0
+        h = modulate(layer_norm(x, eps), m[0], m[1])
+        qkv = gemm(h, b["qkv_w"], b["qkv_b"])
+        q = rms_norm(qkv[:, :D], b["norm_q"], eps)
+        k = rms_norm(qkv[:, D:2 * D], b["norm_k"], eps)
+        v = qkv[:, 2 * D:]
+        if rope_on:
+            q, k = rope(q, d, pos, cfg.theta), rope(k, d, pos, cfg.theta)
+        kv_out.append((k, v))
+        o = heads_attention(q, np.concatenate([hk, k]), np.concatenate([hv, v]), H)
+        x = gemm(o, b["o_w"], b["o_b"], R=x, gate=m[2])
+        qc = rms_norm(gemm(layer_norm(x, eps, b["norm3_w"], b["norm3_b"]), b["cq_w"], b["cq_b"]), b["norm_cq"], eps)
+        x = gemm(heads_attention(qc, tk, tv, H), b["co_w"], b["co_b"], R=x)
+        h = modulate(layer_norm(x, eps), m[3], m[4])
+        x = gemm(gemm(h, b["f1_w"], b["f1_b"], act=1), b["f2_w"], b["f2_b"], R=x, gate=m[5])
+    hm = p["head_mod"] + e
+    h = modulate(layer_norm(x, eps), hm[0], hm[1])
+    vel = gemm(h, p["head_w"], p["head_b"])
+    return _f64(lat) + (t_next - t) * vel, kv_out

@@ -113,3 +113,50 @@ def test_sinusoidal():
     np.testing.assert_array_equal(e[0], [1, 1, 1, 1, 0, 0, 0, 0])
     np.testing.assert_allclose(e[1, 0], np.cos(1.0), atol=1e-15)
     np.testing.assert_allclose(e[1, 4 + 2], np.sin(1.0 * 10000.0 ** (-2 / 4)), atol=1e-15)
+
+
+def test_heads_attention_matches_the_step_oracle():
+    from oracle import fastar_oracle as O
+    rng = np.random.default_rng(12)
+    H, d = 3, 16
+    Q, K, V = rng.standard_normal((9, H * d)), rng.standard_normal((14, H * d)), rng.standard_normal((14, H * d))
+    got = D.heads_attention(Q, K, V, H)
+    for h in range(H):
+        s = slice(h * d, (h + 1) * d)
+        want, _ = O.dense_attention(Q[:, s], K[:, s], V[:, s], 1 / np.sqrt(d))
+        np.testing.assert_allclose(got[:, s], want, atol=1e-12)
+
+
+class _Cfg:
+    dim, heads, eps, freq_dim, grid_h, grid_w, theta = 16, 2, 1e-6, 8, 2, 3, 10000.0
+
+
+def _params(rng, zero_blocks):
+    Dm, f = 16, 32
+    z = (lambda *s: np.zeros(s)) if zero_blocks else (lambda *s: rng.standard_normal(s) * 0.3)
+    blocks = [dict(mod=z(6, Dm), qkv_w=z(3 * Dm, Dm), qkv_b=z(3 * Dm), norm_q=np.ones(Dm), norm_k=np.ones(Dm),
+                   o_w=z(Dm, Dm), o_b=z(Dm), norm3_w=np.ones(Dm), norm3_b=z(Dm), cq_w=z(Dm, Dm), cq_b=z(Dm),
+                   norm_cq=np.ones(Dm), co_w=z(Dm, Dm), co_b=z(Dm), f1_w=z(f, Dm), f1_b=z(f), f2_w=z(Dm, f),
+                   f2_b=z(Dm)) for _ in range(2)]
+    r = lambda *s: rng.standard_normal(s) * 0.3
+    return dict(time_w1=r(Dm, 8), time_b1=r(Dm), time_w2=r(Dm, Dm), time_b2=r(Dm), proj_w=r(6 * Dm, Dm),
+                proj_b=r(6 * Dm), patch_w=r(Dm, 4), patch_b=r(Dm), head_mod=r(2, Dm), head_w=r(4, Dm),
+                head_b=r(4), blocks=blocks)
+
+
+def test_dit_step_with_silent_blocks_is_the_head_alone():
+    rng = np.random.default_rng(13)
+    p = _params(rng, zero_blocks=True)
+    lat = rng.standard_normal((6, 4))
+    hist = [(np.zeros((0, 16)), np.zeros((0, 16)))] * 2
+    tkv = [(rng.standard_normal((5, 16)), rng.standard_normal((5, 16)))] * 2
+    got, _ = D.dit_step(p, _Cfg, lat, 0.75, 0.5, 0, hist, tkv)
+    # by hand: the embedding MLP, the patch map, then LN + modulation + the head map
+    emb = np.concatenate([np.cos(750.0 * 10000.0 ** (-np.arange(4) / 4)), np.sin(750.0 * 10000.0 ** (-np.arange(4) / 4))])
+    s1 = emb @ p["time_w1"].T + p["time_b1"]
+    e = (s1 / (1 + np.exp(-s1))) @ p["time_w2"].T + p["time_b2"]
+    x = lat @ p["patch_w"].T + p["patch_b"]
+    xn = (x - x.mean(1, keepdims=True)) / np.sqrt(x.var(1, keepdims=True) + 1e-6)
+    h = xn * (1 + p["head_mod"][1] + e) + p["head_mod"][0] + e
+    want = lat - 0.25 * (h @ p["head_w"].T + p["head_b"])
+    np.testing.assert_allclose(got, want, atol=1e-12)
