@@ -42,6 +42,8 @@ def parse_args():
     p.add_argument("--no-dense", action="store_true", help="skip the dense-baseline timing")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-rollout", action="store_true", help="skip the long-rollout stability run")
+    p.add_argument("--no-dit", action="store_true", help="skip the whole-transformer (DiT) chunk denoise run")
+    p.add_argument("--dit-chunks", type=int, default=20, help="chunks of the DiT rollout (3 latent frames each)")
     return p.parse_args()
 
 
@@ -444,6 +446,13 @@ def run_fastar(args, rank, world, local):
         del dense
     if not args.no_rollout and cfg.name == "wan13b_layer":
         out["rollout"] = measure_rollout(cfg, args.seed + rank, flush, torch, dev)
+    if not args.no_dit and cfg.name == "wan13b_layer":
+        del layer, graph
+        torch.cuda.empty_cache()
+        try:
+            out["dit"] = measure_dit(args.dit_chunks, args.seed + rank, torch, dev)
+        except Exception as exc:   # the layer's line must survive a failure of the wider run
+            out["dit"] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=15.0)
     return out
@@ -660,6 +669,68 @@ def time_pq_match(layer, cfg, q_d, k_d, flush, steps, torch, L, first_chunk_keys
             "note": "cached keys product-quantized (m sub-spaces of d/m dims, Kc codewords drawn from the first "
                     "frame's keys); the match ranks the decoded keys on the tensor cores (decode + match + "
                     "finaliser, eviction on the true keys); encode = the chunk's current keys"}
+
+
+def measure_dit(chunks, seed, torch, dev):
+    """The Wan-1.3B-shaped DiT (random weights) denoising a rollout of `chunks` chunks of 3
+    latent frames (4 Euler steps each, every block's attention FAST-AR or dense), timed
+    per chunk over the replayed step graphs; plus the tensor-core GEMM alone at the
+    feed-forward shape."""
+    from kv_cache_tempcache_gb300 import _lib as L
+    from kv_cache_tempcache_gb300.dit import WAN13B_DIT, DiT
+    cfg = WAN13B_DIT
+    N = cfg.tokens
+    g = torch.Generator(device=dev).manual_seed(seed)
+    text = torch.randn(cfg.text_len, cfg.text_dim, generator=g, device=dev).to(torch.bfloat16)
+    noises = [torch.randn(N, cfg.patch_ch, generator=g, device=dev).to(torch.bfloat16) for _ in range(chunks)]
+    res = {"config": f"{cfg.name}: {cfg.layers} blocks, dim {cfg.dim}, {cfg.heads} heads, FFN {cfg.ffn}, "
+                     f"chunk {cfg.frames}x{cfg.grid_h}x{cfg.grid_w} = {N} tokens, {cfg.steps} steps, text "
+                     f"{cfg.text_len}x{cfg.text_dim}, random weights",
+           "chunks": chunks, "frames": chunks * cfg.frames}
+    # the GEMM alone: the feed-forward up-projection, L2 flushed before each
+    A = torch.randn(N, cfg.dim, generator=g, device=dev).to(torch.bfloat16)
+    W = (torch.randn(cfg.ffn, cfg.dim, generator=g, device=dev) / cfg.dim ** 0.5).to(torch.bfloat16)
+    C = torch.empty(N, cfg.ffn, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        L.fastar_gemm(A, W, C, act=L.ACT_GELU_TANH)
+    ms = []
+    for _ in range(10):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        L.fastar_gemm(A, W, C, act=L.ACT_GELU_TANH)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    gms = statistics.median(ms)
+    peaks = load_peaks()
+    tf = 2.0 * N * cfg.ffn * cfg.dim / (gms * 1e-3) / 1e12
+    res["gemm_ffn_up"] = {"shape": [N, cfg.ffn, cfg.dim], "ms": round(gms, 4), "tflops": round(tf, 1),
+                          "frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 3) if peaks.get("bf16_tflops") else None}
+    del A, W, C
+    for attention in ("fastar", "dense"):
+        model = DiT(cfg, attention, seed=seed, device=dev, dense_capacity=chunks * N)
+        model.set_text(text)
+        per_chunk = []
+        for c in range(chunks):
+            ev = []
+            model.denoise_chunk(noises[c], use_graph=True,
+                                timer=lambda ph: ev.append(torch.cuda.Event(enable_timing=True)) or ev[-1].record())
+            torch.cuda.synchronize(dev)
+            per_chunk.append(sum(ev[i].elapsed_time(ev[i + 1]) for i in range(0, len(ev), 2)))
+        assert model.status_word() == 0
+        total = sum(per_chunk)
+        res[attention] = {"ms_per_chunk": [round(x, 2) for x in per_chunk], "total_ms": round(total, 1),
+                          "latent_frames_per_s": round(chunks * cfg.frames / (total * 1e-3), 2),
+                          "peak_bytes": int(torch.cuda.max_memory_allocated(dev))}
+        del model
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+    res["speedup_fastar_vs_dense"] = round(res["dense"]["total_ms"] / res["fastar"]["total_ms"], 3)
+    res["note"] = ("per chunk: the 4 replayed denoising-step graphs (graph capture excluded); FAST-AR caches "
+                   "capped at M per block, the dense caches append every chunk")
+    return res
 
 
 def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):
