@@ -409,7 +409,8 @@ int fastar_dense_attn_grouped(const void* q, int dtype, int H, int64_t nq, int d
  * leading dimensions lda, ldw, ldc, ldr in elements (multiples of 8; 16-byte aligned
  * bases).  bias [N] fp32 (NULL: 0).  R NULL: no residual term (C = act(...)).  With R,
  * gate[n] = gate_a[n] + gate_b[n] (fp32; gate_b may be NULL; gate_a NULL: gate 1).
- * c_dtype: FASTAR_BF16 or FASTAR_F32 for C (R is always bf16).
+ * c_dtype: FASTAR_BF16 or FASTAR_F32 for C (R is always bf16).  bias and the gates must be
+ * 16-byte aligned.
  * M >= 1, N a multiple of 256, K a multiple of 64 (FASTAR_EUNSUPPORTED otherwise).
  * C must not overlap A or W; it may be R (in-place residual update). */
 int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,

@@ -509,6 +509,8 @@ int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const fl
   if (lda < K || ldw < K || ldc < N || (lda & 7) || (ldw & 7) || (ldc & 7)) return FASTAR_EINVAL;
   if (R && (!aligned16(R) || ldr < N || (ldr & 7))) return FASTAR_EINVAL;
   if (C == A || C == W) return FASTAR_EINVAL;
+  if ((bias && !aligned16(bias)) || (gate_a && !aligned16(gate_a)) || (gate_b && !aligned16(gate_b)))
+    return FASTAR_EINVAL;
   return cuda_rc(fastar::launch_gemm_tc(A, lda, W, ldw, bias, R, ldr, gate_a, gate_b, C, ldc,
                                         c_dtype == FASTAR_F32 ? 1 : 0, M, N, K, act, dev_status, stream));
 }

@@ -7,12 +7,13 @@
 //             with a residual: v = R[m, n] + (gate_a[n] + gate_b[n]) * v  (gates optional,
 //             a missing gate counts as 1 / 0 as documented in the header).
 //
-// One persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer: 128 x 64 tiles of A and 256 x 64 tiles of W through a
-//               4-stage shared-memory ring (128-byte swizzle);
-//   warp 1      owns TMEM (2 accumulator stages x 256 fp32 columns) and issues
-//               tcgen05.mma (M = 128, N = 256, K = 16) from one thread;
-//   warps 2..9  epilogue: each reads 32 rows x 128 columns of the accumulator (its TMEM
+// One persistent CTA per SM, warp-specialised, output tiles of 128 x BN (BN = 256, or 128
+// when 256-column tiles would leave the last wave of CTAs mostly idle):
+//   warp 0      TMA producer: 128 x 64 tiles of A and BN x 64 tiles of W through a
+//               shared-memory ring of 4 (BN 256) or 6 (BN 128) stages (128-byte swizzle);
+//   warp 1      owns TMEM (2 accumulator stages x BN fp32 columns) and issues
+//               tcgen05.mma (M = 128, N = BN, K = 16) from one thread;
+//   warps 2..9  epilogue: each reads 32 rows x BN/2 columns of the accumulator (its TMEM
 //               lane quadrant, its column half), hands the stage back, applies the
 //               epilogue in fp32 and stores bf16 rows with 16-byte writes.
 // Output tiles are taken round-robin (M fastest, so CTAs in flight share W tiles in L2).
@@ -28,16 +29,23 @@ namespace fastar {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kGS = 4;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kEpiW = 8;
 constexpr int kThreadsG = (2 + kEpiW) * 32;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 
+// Output tiles of 128 x BN; the ring holds as many 64-column stages as fit 192 KB.
+template <int BN>
+struct GemmShape {
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStages = (192 * 1024) / (kABytes + kBBytes);   // 4 (BN 256) or 6 (BN 128)
+};
+
+template <int BN>
 struct alignas(1024) GemmSmem {
-  uint8_t a[kGS][kABytes];
-  uint8_t b[kGS][kBBytes];
-  uint64_t full[kGS], empty[kGS];
+  uint8_t a[GemmShape<BN>::kStages][kABytes];
+  uint8_t b[GemmShape<BN>::kStages][GemmShape<BN>::kBBytes];
+  uint64_t full[GemmShape<BN>::kStages], empty[GemmShape<BN>::kStages];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
@@ -57,21 +65,33 @@ struct GemmArgs {
   int32_t* status;
 };
 
+// Hyperbolic tangent from the SFU (PTX tanh.approx.f32; its error, about 2^-11, is below
+// the bf16 rounding of the output).
+__device__ __forceinline__ float tanh_sfu(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float act_fn(float v, int act) {
   if (act == FASTAR_ACT_GELU_TANH) {
     // 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
     const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
-    return 0.5f * v * (1.0f + tanhf(u));
+    return 0.5f * v * (1.0f + tanh_sfu(u));
   }
   if (act == FASTAR_ACT_SILU) return v / (1.0f + __expf(-v));
   return v;
 }
 
+template <int kBN>
 __global__ void __launch_bounds__(kThreadsG, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                    const GemmArgs g) {
+  constexpr int kGS = GemmShape<kBN>::kStages;
+  constexpr int kBBytes = GemmShape<kBN>::kBBytes;
   extern __shared__ uint8_t smem_raw[];
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  GemmSmem<kBN>& sm =
+      *reinterpret_cast<GemmSmem<kBN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = (int)((g.M + kBM - 1) / kBM), NT = (int)(g.N / kBN), KT = (int)(g.K / kBK);
   const int tiles = MT * NT;
@@ -90,7 +110,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     tc::mbar_fence_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&sm.tmem_base, 512);
+    tc::tmem_alloc(&sm.tmem_base, 2 * kBN);
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -167,7 +187,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   } else {
     // ---------------- epilogue ----------------
     const int quad = warp & 3;              // the TMEM lane quadrant this warp may read
-    const int half = (warp - 2) >> 2;       // which 128 columns of the 256-column tile
+    const int half = (warp - 2) >> 2;       // which half of the tile's columns
     const int row = quad * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
@@ -176,12 +196,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       if (!tc::mbar_wait(&sm.acc_full[acc], aph, abort)) break;
       tc::tc_fence_after();
       const int64_t m = (int64_t)tm * kBM + row;
-      const int64_t n0 = (int64_t)tn * kBN + half * 128;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + half * 128);
-      // two passes of 64 columns (64 registers of scores at a time); the accumulator
-      // stage is handed back once the second pass's scores are in registers
+      const int64_t n0 = (int64_t)tn * kBN + half * (kBN / 2);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + half * (kBN / 2));
+      // passes of 64 columns (64 registers of scores at a time); the accumulator stage is
+      // handed back once the last pass's scores are in registers
+      constexpr int kPasses = kBN / 128;
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
+      for (int pass = 0; pass < kPasses; ++pass) {
         float v[2][32];
         __syncwarp();   // the TMEM loads are warp-collective: every lane, converged
         tc::tmem_ld32(taddr + (uint32_t)(pass * 64), v[0]);
@@ -189,7 +210,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         tc::tmem_wait_ld();
         tc::tmem_pin32(v[0]);
         tc::tmem_pin32(v[1]);
-        if (pass == 1) {
+        if (pass == kPasses - 1) {
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sm.acc_empty[acc]);
@@ -212,30 +233,35 @@ __global__ void __launch_bounds__(kThreadsG, 1)
               }
             }
           }
+          // four columns at a time: their bias and gate values as 16-byte loads (the
+          // same for every lane)
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0 = v[c][i], x1 = v[c][i + 1];
-            if (g.bias) {
-              x0 += g.bias[nc + i];
-              x1 += g.bias[nc + i + 1];
-            }
-            x0 = act_fn(x0, g.act);
-            x1 = act_fn(x1, g.act);
-            if (g.res) {
-              float g0 = 1.f, g1 = 1.f;
-              if (g.gate_a) {
-                g0 = g.gate_a[nc + i] + (g.gate_b ? g.gate_b[nc + i] : 0.f);
-                g1 = g.gate_a[nc + i + 1] + (g.gate_b ? g.gate_b[nc + i + 1] : 0.f);
+          for (int q = 0; q < 8; ++q) {
+            const float4 b4 = g.bias ? reinterpret_cast<const float4*>(g.bias + nc)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (g.res && g.gate_a) {
+              g4 = reinterpret_cast<const float4*>(g.gate_a + nc)[q];
+              if (g.gate_b) {
+                const float4 h4 = reinterpret_cast<const float4*>(g.gate_b + nc)[q];
+                g4.x += h4.x, g4.y += h4.y, g4.z += h4.z, g4.w += h4.w;
               }
-              x0 = fmaf(g0, x0, r[i]);
-              x1 = fmaf(g1, x1, r[i + 1]);
             }
-            if (g.c_f32) {
-              *reinterpret_cast<float2*>(static_cast<float*>(g.C) + m * g.ldc + nc + i) = make_float2(x0, x1);
-            } else {
-              __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-              pk[i >> 1] = *reinterpret_cast<uint32_t*>(&h);
+            const float bq[4] = {b4.x, b4.y, b4.z, b4.w}, gq[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const int i = 4 * q + u;
+              float x0 = act_fn(v[c][i] + bq[u], g.act), x1 = act_fn(v[c][i + 1] + bq[u + 1], g.act);
+              if (g.res) {
+                x0 = fmaf(gq[u], x0, r[i]);
+                x1 = fmaf(gq[u + 1], x1, r[i + 1]);
+              }
+              if (g.c_f32) {
+                *reinterpret_cast<float2*>(static_cast<float*>(g.C) + m * g.ldc + nc + i) = make_float2(x0, x1);
+              } else {
+                __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                pk[i >> 1] = *reinterpret_cast<uint32_t*>(&h);
+              }
             }
           }
           if (!g.c_f32) {
@@ -255,24 +281,34 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_dealloc(tmem, 2 * kBN);
   }
   if (threadIdx.x == 0 && sm.abort) flag_status(g.status, FASTAR_DEV_TIMEOUT);
 }
 
 }  // namespace
 
+template <int kBN>
+static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_t ldw, const GemmArgs& g,
+                               cudaStream_t s) {
+  constexpr size_t smem = sizeof(GemmSmem<kBN>) + 1024;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(gemm_tc_kernel<kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return attr;
+  CUtensorMap ta, tw;
+  if (!make_tmap_bf16_3d(&ta, A, (uint64_t)g.K, (uint64_t)g.M, 1, (uint64_t)lda * 2, 0, kBK, kBM) ||
+      !make_tmap_bf16_3d(&tw, W, (uint64_t)g.K, (uint64_t)g.N, 1, (uint64_t)ldw * 2, 0, kBK, kBN))
+    return cudaErrorInvalidValue;
+  const int64_t tiles = ((g.M + kBM - 1) / kBM) * (g.N / kBN);
+  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  gemm_tc_kernel<kBN><<<grid, kThreadsG, smem, s>>>(ta, tw, g);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,
                            const void* res, int64_t ldr, const float* gate_a, const float* gate_b, void* C, int64_t ldc,
                            int c_f32, int64_t M, int64_t N, int64_t K, int act, int32_t* status, cudaStream_t s) {
-  constexpr size_t smem = sizeof(GemmSmem) + 1024;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (attr != cudaSuccess) return attr;
-  CUtensorMap ta, tw;
-  if (!make_tmap_bf16_3d(&ta, A, (uint64_t)K, (uint64_t)M, 1, (uint64_t)lda * 2, 0, kBK, kBM) ||
-      !make_tmap_bf16_3d(&tw, W, (uint64_t)K, (uint64_t)N, 1, (uint64_t)ldw * 2, 0, kBK, kBN))
-    return cudaErrorInvalidValue;
   GemmArgs g;
   g.M = M;
   g.N = N;
@@ -287,11 +323,15 @@ cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ld
   g.c_f32 = c_f32;
   g.act = act;
   g.status = status;
-  const int64_t tiles = ((M + kBM - 1) / kBM) * (N / kBN);
-  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  gemm_tc_kernel<<<grid, kThreadsG, smem, s>>>(ta, tw, g);
-  count_launches(1);
-  return cudaGetLastError();
+  // 128 x 256 tiles, unless 128 x 128 tiles fill the machine enough better: waves of the
+  // narrow tiles are half as long but cost about 0.6 of a wide one when K is short (the
+  // epilogue and the pipeline fill dominate a tile); with a long K the narrow tiles' main
+  // loop is markedly slower (measured), so they are kept to K <= 2048
+  const int64_t sms = sm_count();
+  const int64_t t256 = ((M + kBM - 1) / kBM) * (N / 256);
+  const int64_t w256 = (t256 + sms - 1) / sms, w128 = (2 * t256 + sms - 1) / sms;
+  if (K <= 2048 && 3 * w128 < 5 * w256) return gemm_launch<128>(A, lda, W, ldw, g, s);
+  return gemm_launch<256>(A, lda, W, ldw, g, s);
 }
 
 }  // namespace fastar
