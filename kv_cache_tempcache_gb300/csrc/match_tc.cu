@@ -12,17 +12,19 @@
 //               columns) and issues tcgen05.mma (one thread, operand descriptors
 //               as precomputed offsets), committing to the ring's "empty" barriers
 //               and the accumulator's "full" barrier;
-//   warps 2..17 epilogue, four warps per TMEM lane quadrant (2 M-tiles x 2 halves
-//               of the tile's columns): each thread reads its row's 64 fp32 scores
-//               in 32-column chunks, scales them by 1/|k_j| (norms prefetched a tile
+//   warps 2..17 epilogue, four warps per TMEM lane quadrant (4 column parts of 32
+//               keys): each thread owns the same row of both M-tiles, reads its two
+//               32-score chunks, scales them by 1/|k_j| (norms prefetched a tile
 //               ahead, packed f32x2 multiplies) and keeps the running top-1 (and
-//               top-2 when asked) with three-input max trees.  The reduction is
-//               latency-bound, so the 16 warps are there to keep enough of it in
-//               flight per SM (8 warps measured about 20% slower).
+//               top-2 when asked) of both rows with three-input max trees.  The
+//               1/|k_j| values reach the lanes as shared-memory broadcasts, which
+//               share the data pipe with the tensor core's operand reads: one
+//               broadcast serving both M-tiles halves that traffic.  16 warps keep
+//               enough of the latency-bound reduction in flight per SM.
 // The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
 // 256-query block, key segment); segments split the cache so the unit count
 // fills the machine, and a small finaliser merges the partial top-2s of the
-// segments and column halves.
+// segments and column parts.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
@@ -39,8 +41,8 @@ constexpr int kQ = 256;         // queries per unit
 constexpr int kN = 128;         // keys per tile
 constexpr int kStages = 4;      // B ring depth
 constexpr int kTS = 2;          // TMEM accumulator stages (kTS x 2 M-tiles x kN = 512 columns)
-constexpr int kEpW = 16;        // epilogue warps: 4 lane quadrants x 2 M-tiles x kParts column parts
-constexpr int kParts = kEpW / 8;
+constexpr int kEpW = 16;        // epilogue warps: 4 lane quadrants x kParts column parts
+constexpr int kParts = kEpW / 4;
 constexpr int kCW = kN / kParts;   // key columns per epilogue thread and tile
 constexpr int kCPL = kCW / 32;     // key columns per epilogue lane for the norm loads
 constexpr int kThreads = (2 + kEpW) * 32;
@@ -148,6 +150,37 @@ __device__ __forceinline__ void fold32(Best& b, const float* w, int j0) {
     int idx = 31;
 #pragma unroll
     for (int i = 31; i >= 0; --i)
+      if (w[i] == gm) idx = i;
+    b.m1 = gm;
+    b.i1 = j0 + idx;
+  }
+}
+
+template <bool kTop2>
+__device__ __forceinline__ void fold16(Best& b, const float* w, int j0) {
+  float a0 = max3f(w[0], w[1], w[2]), a1 = max3f(w[3], w[4], w[5]);
+  float a2 = max3f(w[6], w[7], w[8]), a3 = max3f(w[9], w[10], w[11]);
+  a0 = max3f(a0, w[12], w[13]);
+  a1 = max3f(a1, w[14], w[15]);
+  const float gm = max3f(a0, a1, fmaxf(a2, a3));
+  if (kTop2) {
+    if (gm > b.m2) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float v = w[i];
+        if (v > b.m1) {
+          b.m2 = b.m1;
+          b.m1 = v;
+          b.i1 = j0 + i;
+        } else if (v > b.m2) {
+          b.m2 = v;
+        }
+      }
+    }
+  } else if (gm > b.m1) {
+    int idx = 15;
+#pragma unroll
+    for (int i = 15; i >= 0; --i)
       if (w[i] == gm) idx = i;
     b.m1 = gm;
     b.i1 = j0 + idx;
@@ -281,78 +314,80 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ---------------- epilogue ----------------
-    // kEpW warps: (lane quadrant, M-tile, column part).  Each thread owns one query row
-    // and kCW of the tile's key columns: it loads them from TMEM, hands the stage back
-    // to the MMA, then scales by 1/|k_j| and folds them into its running best.
+    // kEpW warps: (lane quadrant, column part).  Each thread owns one query row in each
+    // M-tile and kCW of the tile's key columns: it loads both rows' scores from TMEM,
+    // hands the stage back to the MMA, then scales by 1/|k_j| and folds them into the
+    // two running bests.
+    static_assert(kCW == 32 && kCPL == 1, "one 32-column chunk per M-tile and tile");
     const int ew = warp - 2;          // 0..kEpW-1
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int m = (ew >> 2) & 1;      // which M-tile (accumulator) this warp reads
-    const int part = ew >> 3;         // which kCW-column part of the tile
+    const int part = ew >> 2;         // which kCW-column part of the tile
     float* inv = sm.invk[ew];
     int acc = 0;
     uint32_t tph = 0;
     for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
       const Unit w = decode(g, u, clen);
-      const int rloc = m * 128 + quad * 32 + lane;
-      const int64_t i = (int64_t)w.qb * kQ + rloc;
-      Best b{neg_inf(), INT_MAX, neg_inf()};
+      const bool two = w.nm > 1;      // warp-uniform: the second M-tile holds queries
+      Best b0{neg_inf(), INT_MAX, neg_inf()}, b1{neg_inf(), INT_MAX, neg_inf()};
       const float* kn = cknorm + (int64_t)w.h * g.M;
-      // |k_j| of this lane's columns of the first tile (prefetched one tile ahead)
-      float kx[kCPL] = {};
+      // |k_j| of this lane's column of the first tile (prefetched one tile ahead)
+      float kx = 0.f;
       if (w.t_beg < w.t_end) {
-        const int64_t j = (int64_t)w.t_beg * kN + part * kCW + lane * kCPL;
-#pragma unroll
-        for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
+        const int64_t j = (int64_t)w.t_beg * kN + part * kCW + lane;
+        kx = j < w.n ? kn[j] : 0.f;
       }
       for (int t = w.t_beg; t < w.t_end; ++t) {
         const int64_t j0 = (int64_t)t * kN + part * kCW;
         if (!tc::mbar_wait(&sm.t_full[acc], tph, abort)) break;
         tc::tc_fence_after();
-        const bool active = m < w.nm;
         const uint32_t taddr =
-            tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * kN + m * kN + part * kCW);
-        float vc[32];
-        if (active) tc::tmem_ld32(taddr, vc);
-        // 1/|k_j| of this tile into the warp's buffer while the TMEM load is in flight
-#pragma unroll
-        for (int c = 0; c < kCPL; ++c) inv[lane * kCPL + c] = kx[c] > 0.f ? __frcp_rn(kx[c]) : 0.f;
+            tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * kN + part * kCW);
+        // 1/|k_j| of this tile into the warp's buffer while the first TMEM loads are in flight
+        float v0[16], v1[16];
+        tc::tmem_ld16(taddr, v0);
+        if (two) tc::tmem_ld16(taddr + (uint32_t)kN, v1);
+        inv[lane] = kx > 0.f ? __frcp_rn(kx) : 0.f;
         // prefetch the next tile's norms
         if (t + 1 < w.t_end) {
-          const int64_t j = j0 + kN + lane * kCPL;
-#pragma unroll
-          for (int c = 0; c < kCPL; ++c) kx[c] = j + c < w.n ? kn[j + c] : 0.f;
+          const int64_t j = j0 + kN + lane;
+          kx = j < w.n ? kn[j] : 0.f;
         }
         __syncwarp();
-        if (active) {
+        // two 16-column halves; each broadcast of four scales serves both M-tiles
 #pragma unroll
-          for (int c = 0; c < kCW / 32; ++c) {
-            if (c > 0) tc::tmem_ld32(taddr + (uint32_t)(c * 32), vc);
-            tc::tmem_wait_ld();
-            if (c == kCW / 32 - 1) {
-              // the last scores are in registers: hand the stage back to the MMA now
-              tc::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
-            }
-            // scale by 1/|k_j| two lanes at a time (packed f32x2 multiply, round to nearest)
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 s = *reinterpret_cast<const float4*>(inv + c * 32 + q4 * 4);
-              mul2(vc[q4 * 4 + 0], vc[q4 * 4 + 1], s.x, s.y);
-              mul2(vc[q4 * 4 + 2], vc[q4 * 4 + 3], s.z, s.w);
-            }
-            const int64_t jc = j0 + c * 32;
-            if (jc + 32 > w.n) {
-#pragma unroll
-              for (int x = 0; x < 32; ++x)
-                if (jc + x >= w.n) vc[x] = neg_inf();
-            }
-            fold32<kTop2>(b, vc, (int)jc);
+        for (int c = 0; c < 2; ++c) {
+          if (c > 0) {
+            tc::tmem_ld16(taddr + 16u, v0);
+            if (two) tc::tmem_ld16(taddr + (uint32_t)kN + 16u, v1);
           }
-        } else {
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+          tc::tmem_wait_ld();
+          tc::tmem_pin16(v0);
+          if (two) tc::tmem_pin16(v1);
+          if (c == 1) {
+            // both rows' scores are in registers: hand the stage back to the MMA now
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
+          }
+          // scale by 1/|k_j| two lanes at a time (packed f32x2 multiply, round to nearest)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 s = *reinterpret_cast<const float4*>(inv + c * 16 + q4 * 4);
+            mul2(v0[q4 * 4 + 0], v0[q4 * 4 + 1], s.x, s.y);
+            mul2(v0[q4 * 4 + 2], v0[q4 * 4 + 3], s.z, s.w);
+            if (two) {
+              mul2(v1[q4 * 4 + 0], v1[q4 * 4 + 1], s.x, s.y);
+              mul2(v1[q4 * 4 + 2], v1[q4 * 4 + 3], s.z, s.w);
+            }
+          }
+          const int64_t jc = j0 + c * 16;
+          if (jc + 16 > w.n) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              if (jc + x >= w.n) v0[x] = v1[x] = neg_inf();
+          }
+          fold16<kTop2>(b0, v0, (int)jc);
+          if (two) fold16<kTop2>(b1, v1, (int)jc);
         }
         if (++acc == kTS) {
           acc = 0;
@@ -360,9 +395,13 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncwarp();   // every lane is done with inv before the next tile rewrites it
       }
-      if (m * 128 < w.rows && rloc < w.rows && !*abort)
-        part_out[(((int64_t)w.seg * kParts + part) * g.H + w.h) * g.nq + i] =
-            make_float4(b.m1, __int_as_float(b.i1), b.m2, 0.f);
+      if (!*abort) {
+        const int64_t base = (((int64_t)w.seg * kParts + part) * g.H + w.h) * g.nq + (int64_t)w.qb * kQ;
+        const int r0 = quad * 32 + lane;
+        if (r0 < w.rows) part_out[base + r0] = make_float4(b0.m1, __int_as_float(b0.i1), b0.m2, 0.f);
+        if (r0 + 128 < w.rows)
+          part_out[base + r0 + 128] = make_float4(b1.m1, __int_as_float(b1.i1), b1.m2, 0.f);
+      }
     }
   }
   tc::tc_fence_before();
