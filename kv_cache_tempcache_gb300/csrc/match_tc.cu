@@ -23,8 +23,8 @@
 //               enough of the latency-bound reduction in flight per SM.
 // The MMA of tile t+1 overlaps the epilogue of tile t.  A work unit is (head,
 // 256-query block, key segment); segments split the cache so the unit count
-// fills the machine, and a small finaliser merges the partial top-2s of the
-// segments and column parts.
+// fills the machine; the column parts of a row are merged in shared memory at the
+// end of each unit, and a small finaliser merges the segments' partial top-2s.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 
@@ -53,6 +53,7 @@ struct alignas(1024) MatchSmem {
   uint8_t a[2][D / 64][kTile];
   uint8_t b[kStages][D / 64][kN * 128];
   float invk[kEpW][kCW];
+  float4 best[kParts][kQ];   // per-unit (m1, i1, m2) of every column part, merged in place
   uint64_t a_full, a_empty;
   uint64_t b_full[kStages], b_empty[kStages];
   uint64_t t_full[kTS], t_empty[kTS];
@@ -325,7 +326,9 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* inv = sm.invk[ew];
     int acc = 0;
     uint32_t tph = 0;
-    for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+    // Every epilogue warp walks every unit (no early exit on abort: after one, each
+    // wait returns at once), so the two named barriers per unit always fill.
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode(g, u, clen);
       const bool two = w.nm > 1;      // warp-uniform: the second M-tile holds queries
       Best b0{neg_inf(), INT_MAX, neg_inf()}, b1{neg_inf(), INT_MAX, neg_inf()};
@@ -395,13 +398,33 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncwarp();   // every lane is done with inv before the next tile rewrites it
       }
-      if (!*abort) {
-        const int64_t base = (((int64_t)w.seg * kParts + part) * g.H + w.h) * g.nq + (int64_t)w.qb * kQ;
-        const int r0 = quad * 32 + lane;
-        if (r0 < w.rows) part_out[base + r0] = make_float4(b0.m1, __int_as_float(b0.i1), b0.m2, 0.f);
-        if (r0 + 128 < w.rows)
-          part_out[base + r0 + 128] = make_float4(b1.m1, __int_as_float(b1.i1), b1.m2, 0.f);
+      // the four column parts of each row meet in shared memory; the part-0 warps merge
+      // them (ties to the lower key index) and write one partial top-2 per segment
+      const int r0 = quad * 32 + lane;
+      sm.best[part][r0] = make_float4(b0.m1, __int_as_float(b0.i1), b0.m2, 0.f);
+      sm.best[part][r0 + 128] = make_float4(b1.m1, __int_as_float(b1.i1), b1.m2, 0.f);
+      tc::named_bar(1, kEpW * 32);
+      if (part == 0) {
+        const int64_t base = ((int64_t)w.seg * g.H + w.h) * g.nq + (int64_t)w.qb * kQ;
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+          const int r = r0 + mm * 128;
+          float4 a = sm.best[0][r];
+#pragma unroll
+          for (int p2 = 1; p2 < kParts; ++p2) {
+            const float4 c = sm.best[p2][r];
+            if (beats(c.x, __float_as_int(c.y), a.x, __float_as_int(a.y))) {
+              a.z = fmaxf(a.x, c.z);
+              a.x = c.x;
+              a.y = c.y;
+            } else {
+              a.z = fmaxf(a.z, c.x);
+            }
+          }
+          if (r < w.rows && !*abort) part_out[base + r] = a;
+        }
       }
+      tc::named_bar(1, kEpW * 32);   // the merge has read sm.best before the next unit refills it
     }
   }
   tc::tc_fence_before();
@@ -439,7 +462,7 @@ int match_tc_splits(int H, int64_t nq, int64_t M) {
 }
 
 size_t match_tc_workspace(int H, int64_t nq, int64_t M) {
-  return sizeof(float4) * (size_t)8 * kParts * H * (size_t)nq;   // up to 8 segments x kParts column parts
+  return sizeof(float4) * (size_t)8 * H * (size_t)nq;   // up to 8 segments
 }
 
 // Launches the tensor-core match (writes `part` as [S, H, nq] and clears evict).
@@ -483,7 +506,7 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
     match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, owner, status);
   }
   count_launches(1);
-  return g.S * kParts;   // partial top-2s per (segment, column part)
+  return g.S;   // partial top-2s, one per segment
 }
 
 int launch_match_tc(int d, TokView q, int H, int64_t nq, const void* ck, const float* cknorm, const int32_t* clen,
