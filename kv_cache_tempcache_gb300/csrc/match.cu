@@ -202,19 +202,9 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   const int64_t i = w - (int64_t)h * nq;
   int64_t n = clen[h];
   n = n < 0 ? 0 : (n > M ? M : n);
-  Top2 t{neg_inf(), INT_MAX, neg_inf()};
-  for (int s = sub; s < splits; s += 8) {
-    const float4 p = part[((int64_t)s * H + h) * nq + i];
-    t = top2_merge(t, Top2{p.x, __float_as_int(p.y), p.z});
-  }
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) {
-    Top2 u;
-    u.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
-    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
-    u.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
-    t = top2_merge(t, u);
-  }
+  // this lane's first partial and the two rows are loaded before any of them is used
+  float4 p0 = make_float4(neg_inf(), __int_as_float(INT_MAX), neg_inf(), 0.f);
+  if (sub < splits) p0 = part[((int64_t)sub * H + h) * nq + i];
   // |q_i| and |kcur_i|
   constexpr int E = D / 8;
   const T* qr = q + h * hs + i * ts + sub * E;
@@ -236,6 +226,19 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   for (int o = 4; o > 0; o >>= 1) {
     qq += __shfl_xor_sync(0xffffffffu, qq, o);
     kk += __shfl_xor_sync(0xffffffffu, kk, o);
+  }
+  Top2 t{p0.x, __float_as_int(p0.y), p0.z};
+  for (int s = sub + 8; s < splits; s += 8) {
+    const float4 p = part[((int64_t)s * H + h) * nq + i];
+    t = top2_merge(t, Top2{p.x, __float_as_int(p.y), p.z});
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    Top2 u;
+    u.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
+    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    u.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
+    t = top2_merge(t, u);
   }
   qq = sqrtf(qq);
   kk = sqrtf(kk);

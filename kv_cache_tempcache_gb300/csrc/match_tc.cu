@@ -118,53 +118,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 template <bool kTop2>
-__device__ __forceinline__ void fold32(Best& b, const float* w, int j0) {
-  // maximum of the 32 values: four independent three-input chains, then merge
-  float a0 = max3f(w[0], w[1], w[2]), a1 = max3f(w[3], w[4], w[5]);
-  float a2 = max3f(w[6], w[7], w[8]), a3 = max3f(w[9], w[10], w[11]);
-  a0 = max3f(a0, w[12], w[13]);
-  a1 = max3f(a1, w[14], w[15]);
-  a2 = max3f(a2, w[16], w[17]);
-  a3 = max3f(a3, w[18], w[19]);
-  a0 = max3f(a0, w[20], w[21]);
-  a1 = max3f(a1, w[22], w[23]);
-  a2 = max3f(a2, w[24], w[25]);
-  a3 = max3f(a3, w[26], w[27]);
-  a0 = max3f(a0, w[28], w[29]);
-  a1 = max3f(a1, w[30], w[31]);
-  const float gm = max3f(a0, a1, fmaxf(a2, a3));
-  if (kTop2) {
-    if (gm > b.m2) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float v = w[i];
-        if (v > b.m1) {
-          b.m2 = b.m1;
-          b.m1 = v;
-          b.i1 = j0 + i;
-        } else if (v > b.m2) {
-          b.m2 = v;
-        }
-      }
-    }
-  } else if (gm > b.m1) {
-    int idx = 31;
-#pragma unroll
-    for (int i = 31; i >= 0; --i)
-      if (w[i] == gm) idx = i;
-    b.m1 = gm;
-    b.i1 = j0 + idx;
-  }
-}
-
-template <bool kTop2>
 __device__ __forceinline__ void fold16(Best& b, const float* w, int j0) {
-  float a0 = max3f(w[0], w[1], w[2]), a1 = max3f(w[3], w[4], w[5]);
-  float a2 = max3f(w[6], w[7], w[8]), a3 = max3f(w[9], w[10], w[11]);
-  a0 = max3f(a0, w[12], w[13]);
-  a1 = max3f(a1, w[14], w[15]);
-  const float gm = max3f(a0, a1, fmaxf(a2, a3));
   if (kTop2) {
+    float a0 = max3f(w[0], w[1], w[2]), a1 = max3f(w[3], w[4], w[5]);
+    float a2 = max3f(w[6], w[7], w[8]), a3 = max3f(w[9], w[10], w[11]);
+    a0 = max3f(a0, w[12], w[13]);
+    a1 = max3f(a1, w[14], w[15]);
+    const float gm = max3f(a0, a1, fmaxf(a2, a3));
     if (gm > b.m2) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -178,13 +138,24 @@ __device__ __forceinline__ void fold16(Best& b, const float* w, int j0) {
         }
       }
     }
-  } else if (gm > b.m1) {
-    int idx = 15;
-#pragma unroll
-    for (int i = 15; i >= 0; --i)
-      if (w[i] == gm) idx = i;
-    b.m1 = gm;
-    b.i1 = j0 + idx;
+  } else {
+    // maxima of four groups of consecutive columns, so that a new best is located by
+    // its group first (the lowest group holding it, then the lowest column in it)
+    const float g0 = fmaxf(max3f(w[0], w[1], w[2]), w[3]);
+    const float g1 = fmaxf(max3f(w[4], w[5], w[6]), w[7]);
+    const float g2 = fmaxf(max3f(w[8], w[9], w[10]), w[11]);
+    const float g3 = fmaxf(max3f(w[12], w[13], w[14]), w[15]);
+    const float gm = max3f(g0, g1, fmaxf(g2, g3));
+    if (gm > b.m1) {
+      const bool in0 = g0 == gm, in1 = g1 == gm, in2 = g2 == gm;
+      const int base = in0 ? 0 : in1 ? 4 : in2 ? 8 : 12;
+      const float x0 = in0 ? w[0] : in1 ? w[4] : in2 ? w[8] : w[12];
+      const float x1 = in0 ? w[1] : in1 ? w[5] : in2 ? w[9] : w[13];
+      const float x2 = in0 ? w[2] : in1 ? w[6] : in2 ? w[10] : w[14];
+      const int k = x0 == gm ? 0 : x1 == gm ? 1 : x2 == gm ? 2 : 3;
+      b.m1 = gm;
+      b.i1 = j0 + base + k;
+    }
   }
 }
 
