@@ -423,7 +423,8 @@ int fastar_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, const fl
  *   y = (x - mean) / sqrt(var + eps)  [* weight[c] + bias[c]]  (weight NULL: no affine)
  *   out = y * (1 + scale[c]) + shift[c],  scale = scale_a + scale_b, shift = shift_a + shift_b
  * (fp32 vectors [C]; any of the four may be NULL, counting 0).  var is the biased
- * variance.  eps > 0. */
+ * variance.  eps > 0.  x, out and every non-NULL vector 16-byte aligned (the vectors
+ * are read 16 bytes at a time); FASTAR_EINVAL otherwise. */
 int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps, const float* weight,
                          const float* bias, const float* shift_a, const float* shift_b,
                          const float* scale_a, const float* scale_b, void* out, int64_t ldo,
@@ -437,7 +438,8 @@ int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps
  *   sits at frame f0 + i / (grid_h grid_w), row (i / grid_w) % grid_h, column i % grid_w,
  *   f0 = t0 + *t0_dev (t0_dev optional, device int32: lets a captured graph follow the
  *   rollout).
- * d even and >= 12, C a multiple of d and of 8, C <= 4096. */
+ * d even and >= 12, C a multiple of d and of 8, C <= 4096; x and weight (fp32 [C], read
+ * 16 bytes at a time) 16-byte aligned, else FASTAR_EINVAL. */
 int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps, const float* weight,
                         int rope, int t0, const int32_t* t0_dev, int grid_h, int grid_w, float theta,
                         cudaStream_t stream);

@@ -523,6 +523,8 @@ int fastar_layernorm_mod(const void* x, int64_t ldx, int64_t n, int C, float eps
   if (!x || !out || !aligned16(x) || !aligned16(out) || ldx < C || ldo < C || (ldx & 7) || (ldo & 7))
     return FASTAR_EINVAL;
   if (bias && !weight) return FASTAR_EINVAL;
+  for (const float* v : {weight, bias, shift_a, shift_b, scale_a, scale_b})
+    if (v && !aligned16(v)) return FASTAR_EINVAL;   // read as 16-byte vectors
   return cuda_rc(fastar::launch_layernorm_mod(x, ldx, n, C, eps, weight, bias, shift_a, shift_b, scale_a, scale_b,
                                               out, ldo, stream));
 }
@@ -533,6 +535,7 @@ int fastar_rmsnorm_rope(void* x, int64_t ldx, int64_t n, int C, int d, float eps
   if (rope && (grid_h < 1 || grid_w < 1 || !(theta > 1.f) || t0 < 0)) return FASTAR_EINVAL;
   if (n == 0) return FASTAR_OK;
   if (!x || !aligned16(x) || ldx < C || (ldx & 7)) return FASTAR_EINVAL;
+  if (weight && !aligned16(weight)) return FASTAR_EINVAL;   // read as 16-byte vectors
   return cuda_rc(
       fastar::launch_rmsnorm_rope(x, ldx, n, C, d, eps, weight, rope, t0, t0_dev, grid_h, grid_w, theta, stream));
 }

@@ -34,12 +34,20 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return u;
 }
 
-__device__ __forceinline__ float vsum(const float* a, const float* b, int i) {
-  return (a ? a[i] : 0.f) + (b ? b[i] : 0.f);
+// The 8 fp32 values of a vector starting at channel c (16-byte aligned), or zeros.
+__device__ __forceinline__ void load8f(const float* p, int c, float* f) {
+  if (!p) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    return;
+  }
+  const float4 x = reinterpret_cast<const float4*>(p + c)[0], y = reinterpret_cast<const float4*>(p + c)[1];
+  f[0] = x.x, f[1] = x.y, f[2] = x.z, f[3] = x.w, f[4] = y.x, f[5] = y.y, f[6] = y.z, f[7] = y.w;
 }
 
 // y = LN(x) [* w + b] then y * (1 + scale) + shift, scale = scale_a + scale_b, shift =
-// shift_a + shift_b (any may be null).  Lane l owns vectors l, l + 32, ... (8 channels).
+// shift_a + shift_b (any may be null).  Lane l owns vectors l, l + 32, ... (8 channels);
+// the per-channel vectors are read 16 bytes at a time (they are 16-byte aligned).
 template <int NV>
 __global__ void __launch_bounds__(256)
     layernorm_mod_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int64_t n, int C, float eps,
@@ -76,24 +84,52 @@ __global__ void __launch_bounds__(256)
   for (int k = 0; k < NV; ++k) {
     const int c8 = lane + 32 * k;
     if (c8 >= nv) continue;
-    float y[8];
+    float y[8], p0[8], p1[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = c8 * 8 + e;
-      float t = (v[k][e] - mean) * rstd;
-      if (w) t = fmaf(t, w[c], b ? b[c] : 0.f);
-      const float sc = vsum(scale_a, scale_b, c), sh = vsum(shift_a, shift_b, c);
-      y[e] = fmaf(t, 1.0f + sc, sh);
+    for (int e = 0; e < 8; ++e) y[e] = (v[k][e] - mean) * rstd;
+    if (w) {
+      load8f(w, c8 * 8, p0);
+      load8f(b, c8 * 8, p1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = fmaf(y[e], p0[e], p1[e]);
+    }
+    if (scale_a || scale_b || shift_a || shift_b) {
+      float q0[8], q1[8];
+      load8f(scale_a, c8 * 8, p0);
+      load8f(scale_b, c8 * 8, p1);
+      load8f(shift_a, c8 * 8, q0);
+      load8f(shift_b, c8 * 8, q1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = fmaf(y[e], 1.0f + (p0[e] + p1[e]), q0[e] + q1[e]);
     }
     reinterpret_cast<uint4*>(out + row * ldo)[c8] = pack8(y);
   }
 }
 
+// The rotation of the channel pair (cin, cin + 1) inside a head of width d: the head
+// splits into frame / row / column parts of dt = d - 4 (d / 6), dh = dw = 2 (d / 6) channels;
+// within a part of width da, the pair (2j, 2j + 1) turns by pos * theta^(-2j/da).
+__device__ __forceinline__ void rope_angle(int cin, int d, int pf, int ph, int pw, float theta, float& sn,
+                                           float& cs) {
+  const int part = 2 * (d / 6);
+  const int dt = d - 2 * part;
+  int p, j, da;
+  if (cin < dt) {
+    p = pf, j = cin / 2, da = dt;
+  } else if (cin < dt + part) {
+    p = ph, j = (cin - dt) / 2, da = part;
+  } else {
+    p = pw, j = (cin - dt - part) / 2, da = part;
+  }
+  const float ang = (float)p * powf(theta, -2.0f * (float)j / (float)da);
+  sincosf(ang, &sn, &cs);
+}
+
 // In place on a token-major row of C = H * d channels: optional RMS norm over the whole
-// row (x / sqrt(mean x^2 + eps) * w), then optional rotary positions per head: the head
-// dimension splits into frame / row / column parts of dt = d - 4 (d / 6), dh = dw = 2 (d / 6)
-// channels; within a part of width da, the pair (2j, 2j + 1) turns by pos * theta^(-2j/da).
+// row (x / sqrt(mean x^2 + eps) * w), then optional rotary positions per head (rope_angle).
 // Token i of the chunk sits at frame t0 + i / (gh gw), row (i / gw) % gh, column i % gw.
+// Lane l owns vectors l + 32 k; when d divides 256 their channels sit at the same offsets
+// inside their heads for every k, so the lane's four rotations are computed once per row.
 template <int NV>
 __global__ void __launch_bounds__(256)
     rmsnorm_rope_kernel(__nv_bfloat16* __restrict__ x, int64_t ldx, int64_t n, int C, int d, float eps,
@@ -116,34 +152,34 @@ __global__ void __launch_bounds__(256)
   }
   const float r = w ? rsqrtf(warp_sum(q) / (float)C + eps) : 1.f;
   const int f0 = t0 + (t0_dev ? t0_dev[0] : 0);   // a device offset keeps replayed graphs current
-  const int pos[3] = {f0 + (int)(row / ((int64_t)gh * gw)), (int)((row / gw) % gh), (int)(row % gw)};
-  const int part = 2 * (d / 6);
-  const int dt = d - 2 * part;
+  const int pf = f0 + (int)(row / ((int64_t)gh * gw)), ph = (int)((row / gw) % gh), pw = (int)(row % gw);
+  const bool shared_rot = (256 % d) == 0;
+  float sn[4], cs[4];
+  if (rope && shared_rot) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rope_angle((8 * lane) % d + 2 * e, d, pf, ph, pw, theta, sn[e], cs[e]);
+  }
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int c8 = lane + 32 * k;
     if (c8 >= nv) continue;
     float y[8];
+    if (w) {
+      float wv[8];
+      load8f(w, c8 * 8, wv);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = w ? v[k][e] * r * w[c8 * 8 + e] : v[k][e];
+      for (int e = 0; e < 8; ++e) y[e] = v[k][e] * r * wv[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = v[k][e];
+    }
     if (rope) {
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const int cin = (c8 * 8 + e) % d;   // even channel of the pair inside its head
-        int axis, j, da;
-        if (cin < dt) {
-          axis = 0, j = cin / 2, da = dt;
-        } else if (cin < dt + part) {
-          axis = 1, j = (cin - dt) / 2, da = part;
-        } else {
-          axis = 2, j = (cin - dt - part) / 2, da = part;
-        }
-        const float ang = (float)pos[axis] * powf(theta, -2.0f * (float)j / (float)da);
-        float sn, cs;
-        sincosf(ang, &sn, &cs);
-        const float a0 = y[e], a1 = y[e + 1];
-        y[e] = a0 * cs - a1 * sn;
-        y[e + 1] = a0 * sn + a1 * cs;
+      for (int e = 0; e < 4; ++e) {
+        if (!shared_rot) rope_angle((c8 * 8 + 2 * e) % d, d, pf, ph, pw, theta, sn[e], cs[e]);
+        const float a0 = y[2 * e], a1 = y[2 * e + 1];
+        y[2 * e] = a0 * cs[e] - a1 * sn[e];
+        y[2 * e + 1] = a0 * sn[e] + a1 * cs[e];
       }
     }
     reinterpret_cast<uint4*>(x + row * ldx)[c8] = pack8(y);

@@ -3,7 +3,8 @@
 //
 //   C[m, n] = epilogue( sum_k A[m, k] W[n, k] ),  A [M, K], W [N, K] row-major bf16, C [M, N]
 //   row-major bf16 (or fp32)
-//   epilogue: v = acc + bias[n];  v = act(v)  (none, GELU with the tanh form, SiLU);
+//   epilogue: v = acc + bias[n];  v = act(v)  (none, GELU with the tanh form, SiLU; one
+//             kernel instance per activation);
 //             with a residual: v = R[m, n] + (gate_a[n] + gate_b[n]) * v  (gates optional,
 //             a missing gate counts as 1 / 0 as documented in the header).
 //
@@ -61,7 +62,6 @@ struct GemmArgs {
   void* C;
   int64_t ldc;
   int c_f32;   // C is fp32 instead of bf16
-  int act;
   int32_t* status;
 };
 
@@ -73,17 +73,19 @@ __device__ __forceinline__ float tanh_sfu(float x) {
   return y;
 }
 
-__device__ __forceinline__ float act_fn(float v, int act) {
-  if (act == FASTAR_ACT_GELU_TANH) {
+template <int kAct>
+__device__ __forceinline__ float act_fn(float v) {
+  if (kAct == FASTAR_ACT_GELU_TANH) {
     // 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
     const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
     return 0.5f * v * (1.0f + tanh_sfu(u));
   }
-  if (act == FASTAR_ACT_SILU) return v / (1.0f + __expf(-v));
+  if (kAct == FASTAR_ACT_SILU) return v / (1.0f + __expf(-v));
   return v;
 }
 
-template <int kBN>
+// kAct: the activation, fixed per instance so that the epilogue carries one body.
+template <int kBN, int kAct>
 __global__ void __launch_bounds__(kThreadsG, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                    const GemmArgs g) {
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 #pragma unroll
             for (int u = 0; u < 4; u += 2) {
               const int i = 4 * q + u;
-              float x0 = act_fn(v[c][i] + bq[u], g.act), x1 = act_fn(v[c][i + 1] + bq[u + 1], g.act);
+              float x0 = act_fn<kAct>(v[c][i] + bq[u]), x1 = act_fn<kAct>(v[c][i + 1] + bq[u + 1]);
               if (g.res) {
                 x0 = fmaf(gq[u], x0, r[i]);
                 x1 = fmaf(gq[u + 1], x1, r[i + 1]);
@@ -288,12 +290,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
 }  // namespace
 
-template <int kBN>
+template <int kBN, int kAct>
 static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_t ldw, const GemmArgs& g,
                                cudaStream_t s) {
   constexpr size_t smem = sizeof(GemmSmem<kBN>) + 1024;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(gemm_tc_kernel<kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(gemm_tc_kernel<kBN, kAct>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return attr;
   CUtensorMap ta, tw;
   if (!make_tmap_bf16_3d(&ta, A, (uint64_t)g.K, (uint64_t)g.M, 1, (uint64_t)lda * 2, 0, kBK, kBM) ||
@@ -301,7 +303,7 @@ static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_
     return cudaErrorInvalidValue;
   const int64_t tiles = ((g.M + kBM - 1) / kBM) * (g.N / kBN);
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  gemm_tc_kernel<kBN><<<grid, kThreadsG, smem, s>>>(ta, tw, g);
+  gemm_tc_kernel<kBN, kAct><<<grid, kThreadsG, smem, s>>>(ta, tw, g);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -321,7 +323,6 @@ cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ld
   g.C = C;
   g.ldc = ldc;
   g.c_f32 = c_f32;
-  g.act = act;
   g.status = status;
   // 128 x 256 tiles, unless 128 x 128 tiles fill the machine enough better: waves of the
   // narrow tiles are half as long but cost about 0.6 of a wide one when K is short (the
@@ -330,8 +331,18 @@ cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ld
   const int64_t sms = sm_count();
   const int64_t t256 = ((M + kBM - 1) / kBM) * (N / 256);
   const int64_t w256 = (t256 + sms - 1) / sms, w128 = (2 * t256 + sms - 1) / sms;
-  if (K <= 2048 && 3 * w128 < 5 * w256) return gemm_launch<128>(A, lda, W, ldw, g, s);
-  return gemm_launch<256>(A, lda, W, ldw, g, s);
+  const bool narrow = K <= 2048 && 3 * w128 < 5 * w256;
+  switch (act) {
+    case FASTAR_ACT_GELU_TANH:
+      return narrow ? gemm_launch<128, FASTAR_ACT_GELU_TANH>(A, lda, W, ldw, g, s)
+                    : gemm_launch<256, FASTAR_ACT_GELU_TANH>(A, lda, W, ldw, g, s);
+    case FASTAR_ACT_SILU:
+      return narrow ? gemm_launch<128, FASTAR_ACT_SILU>(A, lda, W, ldw, g, s)
+                    : gemm_launch<256, FASTAR_ACT_SILU>(A, lda, W, ldw, g, s);
+    default:
+      return narrow ? gemm_launch<128, FASTAR_ACT_NONE>(A, lda, W, ldw, g, s)
+                    : gemm_launch<256, FASTAR_ACT_NONE>(A, lda, W, ldw, g, s);
+  }
 }
 
 }  // namespace fastar

@@ -103,6 +103,13 @@ def test_argument_validation_rejects_before_launch(lib):
                                           s) == L.EINVAL
     assert lib.fastar_dense_attn_grouped(FAKE, L.BF16, 2, 64, 128, 8192, 128, FAKE, FAKE, 100, 12800, 128, FAKE, 50,
                                          0.1, FAKE, 8192, 128, None, s) == L.EINVAL
+    # the row kernels read their per-channel vectors 16 bytes at a time: misaligned ones are refused
+    assert lib.fastar_layernorm_mod(FAKE, 1536, 10, 1536, 1e-6, None, None, FAKE + 4, None, None, None, FAKE,
+                                    1536, s) == L.EINVAL
+    assert lib.fastar_layernorm_mod(FAKE, 1536, 10, 1536, 1e-6, FAKE + 8, FAKE, None, None, None, None, FAKE,
+                                    1536, s) == L.EINVAL
+    assert lib.fastar_rmsnorm_rope(FAKE, 1536, 10, 1536, 128, 1e-6, FAKE + 4, 0, 0, None, 1, 1, 10000.0,
+                                   s) == L.EINVAL
     # dense append past capacity
     assert lib.fastar_dense_append(L.BF16, 1, 64, 128, FAKE, FAKE, 8192, 128, FAKE, FAKE, 100, 50, s) == L.ECAPACITY
     # empty work is a successful no-op that touches nothing
