@@ -84,8 +84,9 @@ __device__ __forceinline__ float act_fn(float v) {
   return v;
 }
 
-// kAct: the activation, fixed per instance so that the epilogue carries one body.
-template <int kBN, int kAct>
+// kAct (the activation) and kRes (a residual is added) are fixed per instance, so that
+// the epilogue carries one body without per-element branches.
+template <int kBN, int kAct, bool kRes>
 __global__ void __launch_bounds__(kThreadsG, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                    const GemmArgs g) {
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         for (int c = 0; c < 2 && m < g.M; ++c) {   // rows past M: nothing to store
           const int64_t nc = n0 + pass * 64 + c * 32;
           float r[32];
-          if (g.res) {
+          if (kRes) {
             const uint4* rp = reinterpret_cast<const uint4*>(g.res + m * g.ldr + nc);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           for (int q = 0; q < 8; ++q) {
             const float4 b4 = g.bias ? reinterpret_cast<const float4*>(g.bias + nc)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
             float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (g.res && g.gate_a) {
+            if (kRes && g.gate_a) {
               g4 = reinterpret_cast<const float4*>(g.gate_a + nc)[q];
               if (g.gate_b) {
                 const float4 h4 = reinterpret_cast<const float4*>(g.gate_b + nc)[q];
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             for (int u = 0; u < 4; u += 2) {
               const int i = 4 * q + u;
               float x0 = act_fn<kAct>(v[c][i] + bq[u]), x1 = act_fn<kAct>(v[c][i + 1] + bq[u + 1]);
-              if (g.res) {
+              if (kRes) {
                 x0 = fmaf(gq[u], x0, r[i]);
                 x1 = fmaf(gq[u + 1], x1, r[i + 1]);
               }
@@ -290,12 +291,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
 }  // namespace
 
-template <int kBN, int kAct>
+template <int kBN, int kAct, bool kRes>
 static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_t ldw, const GemmArgs& g,
                                cudaStream_t s) {
   constexpr size_t smem = sizeof(GemmSmem<kBN>) + 1024;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(gemm_tc_kernel<kBN, kAct>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(gemm_tc_kernel<kBN, kAct, kRes>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return attr;
   CUtensorMap ta, tw;
   if (!make_tmap_bf16_3d(&ta, A, (uint64_t)g.K, (uint64_t)g.M, 1, (uint64_t)lda * 2, 0, kBK, kBM) ||
@@ -303,9 +304,19 @@ static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_
     return cudaErrorInvalidValue;
   const int64_t tiles = ((g.M + kBM - 1) / kBM) * (g.N / kBN);
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  gemm_tc_kernel<kBN, kAct><<<grid, kThreadsG, smem, s>>>(ta, tw, g);
+  gemm_tc_kernel<kBN, kAct, kRes><<<grid, kThreadsG, smem, s>>>(ta, tw, g);
   count_launches(1);
   return cudaGetLastError();
+}
+
+template <int kAct>
+static cudaError_t gemm_pick(bool res, bool narrow, const void* A, int64_t lda, const void* W, int64_t ldw,
+                             const GemmArgs& g, cudaStream_t s) {
+  if (res)
+    return narrow ? gemm_launch<128, kAct, true>(A, lda, W, ldw, g, s)
+                  : gemm_launch<256, kAct, true>(A, lda, W, ldw, g, s);
+  return narrow ? gemm_launch<128, kAct, false>(A, lda, W, ldw, g, s)
+                : gemm_launch<256, kAct, false>(A, lda, W, ldw, g, s);
 }
 
 cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,
@@ -334,14 +345,11 @@ cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ld
   const bool narrow = K <= 2048 && 3 * w128 < 5 * w256;
   switch (act) {
     case FASTAR_ACT_GELU_TANH:
-      return narrow ? gemm_launch<128, FASTAR_ACT_GELU_TANH>(A, lda, W, ldw, g, s)
-                    : gemm_launch<256, FASTAR_ACT_GELU_TANH>(A, lda, W, ldw, g, s);
+      return gemm_pick<FASTAR_ACT_GELU_TANH>(res != nullptr, narrow, A, lda, W, ldw, g, s);
     case FASTAR_ACT_SILU:
-      return narrow ? gemm_launch<128, FASTAR_ACT_SILU>(A, lda, W, ldw, g, s)
-                    : gemm_launch<256, FASTAR_ACT_SILU>(A, lda, W, ldw, g, s);
+      return gemm_pick<FASTAR_ACT_SILU>(res != nullptr, narrow, A, lda, W, ldw, g, s);
     default:
-      return narrow ? gemm_launch<128, FASTAR_ACT_NONE>(A, lda, W, ldw, g, s)
-                    : gemm_launch<256, FASTAR_ACT_NONE>(A, lda, W, ldw, g, s);
+      return gemm_pick<FASTAR_ACT_NONE>(res != nullptr, narrow, A, lda, W, ldw, g, s);
   }
 }
 
