@@ -429,10 +429,15 @@ struct Pending {
   }
 };
 
-template <int D, bool kGrouped>
+// kMode is the AttnMode of the launch, fixed per instance: every mode test below folds at
+// compile time, so an instance carries only its own mode's code (one instance serving all
+// modes spent a large share of its cycles waiting on instruction fetches).
+template <int D, bool kGrouped, int kMode>
 __global__ void __launch_bounds__(kThreadsA, 1)
-    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_q) {
+    attn_tc_kernel(const AttnArgs args, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
+  AttnArgs a = args;
+  a.mode = kMode;
   using Lay = AttnLayout<D>;
   constexpr int CPR = D / 8;   // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
@@ -1217,14 +1222,22 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   if (lane == 0 && a.lse) a.lse[(int64_t)h * a.nq + qi] = W > 0.f ? mx + __logf(W) : neg_inf();
 }
 
+// Launches the instance of one (group counts, mode) pair, setting its shared-memory size
+// once; false if the attribute is refused.
+template <int D, bool kGrouped, int kMode>
+bool attn_launch(int grid, cudaStream_t s, const AttnArgs& b, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& tq) {
+  constexpr size_t smem = AttnLayout<D>::bytes;
+  static const cudaError_t attr = cudaFuncSetAttribute(attn_tc_kernel<D, kGrouped, kMode>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return false;
+  attn_tc_kernel<D, kGrouped, kMode><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
+  count_launches(1);
+  return true;
+}
+
 template <int D>
 bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
-  constexpr size_t smem = AttnLayout<D>::bytes;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  static const cudaError_t attr_g =
-      cudaFuncSetAttribute(attn_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (attr != cudaSuccess || attr_g != cudaSuccess) return false;
   int64_t upper;
   AttnArgs b = a;
   CUtensorMap tk, tv, tq;
@@ -1313,12 +1326,17 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (upper <= 0) return true;
   const int sms = sm_count();
   const int grid = (int)(upper < sms ? upper : sms);
-  // group counts (the merge variant) select the instance that stages the logit shifts
-  if (a.gcount)
-    attn_tc_kernel<D, true><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
+  // group counts (the merge variant) select the instances that stage the logit shifts
+  bool ok;
+  if (a.mode == kSparse)
+    ok = a.gcount ? attn_launch<D, true, kSparse>(grid, s, b, tk, tv, tq)
+                  : attn_launch<D, false, kSparse>(grid, s, b, tk, tv, tq);
+  else if (a.mode == kCross)
+    ok = !a.gcount && attn_launch<D, false, kCross>(grid, s, b, tk, tv, tq);
   else
-    attn_tc_kernel<D, false><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
-  count_launches(1);
+    ok = a.gcount ? attn_launch<D, true, kDense>(grid, s, b, tk, tv, tq)
+                  : attn_launch<D, false, kDense>(grid, s, b, tk, tv, tq);
+  if (!ok) return false;
   if (a.mode == kSparse) {
     const int64_t threads = (int64_t)a.H * a.nq * 32;
     sparse_merge_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
@@ -1503,14 +1521,9 @@ cudaError_t launch_match_ann_impl(TokView q, TokView kcur, int H, int64_t nq, in
     sparse_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
     count_launches(1);
   }
-  constexpr size_t smem = AttnLayout<D>::bytes;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (attr != cudaSuccess) return attr;
   const int64_t upper = (int64_t)H * ((np + kAT - 1) / kAT + B);
   const int grid = (int)(upper < sm_count() ? upper : sm_count());
-  attn_tc_kernel<D, false><<<grid, kThreadsA, smem, s>>>(b, tk, tz, tz);
-  count_launches(1);
+  if (!attn_launch<D, false, kMatchAnn>(grid, s, b, tk, tz, tz)) return cudaErrorInvalidValue;
   const int64_t threads = (int64_t)H * nq * 32;
   ann_match_finalize_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, kcur, cache_knorm, tau, top1,
                                                                                    s1, evict, owner);
