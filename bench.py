@@ -210,6 +210,13 @@ def stage_units(cfg, layer, n_in):
     return u
 
 
+def hold_gpu(torch, cycles=6_000_000):
+    """Keeps the GPU busy (a spin of about 3 ms) while the host enqueues an eager step, so
+    that per-stage events bracket GPU work only, not the host's launch time between calls."""
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(cycles)
+
+
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_wan13b_layer.json")
 
 
@@ -345,6 +352,7 @@ def run_fastar(args, rank, world, local):
         stage_ev.setdefault(name, []).append(e)
 
     for _ in range(args.steps):
+        hold_gpu(torch)
         flush.zero_()
         layer.step(q_d, k_d, v_d, advance=False, timer=timer, serial=True)
     torch.cuda.synchronize(dev)
@@ -399,7 +407,8 @@ def run_fastar(args, rank, world, local):
                             f"{int(n_in.sum())} entries in, {int(layer.caches[1 - layer.cur].len.sum())} out",
                    "l2": "flushed between timed steps (256 MiB memset outside the events)",
                    "warmup_extra": f"{soak} untimed replays while the clock sampler started",
-                   "stages": "per-stage times from an eager pass with all kernels on one stream",
+                   "stages": "per-stage times from an eager pass with all kernels on one stream, enqueued behind a "
+                             "GPU spin so that host launch time between calls is not counted",
                    "parallelism": f"replicas x{world} (independent head groups, no exchange)"},
         "latent_frames_per_s": round(value / cfg.Tf, 2),
         "roofline": roof,
@@ -433,6 +442,7 @@ def run_fastar(args, rank, world, local):
             dense.step(q_d, k_d, v_d, advance=False)
         dts = []
         for _ in range(max(3, args.steps // 4)):
+            hold_gpu(torch)
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -519,6 +529,7 @@ def time_ann_match(layer, cfg, q_d, k_d, flush, steps, torch, L):
             fn()
         ms = []
         for _ in range(steps):
+            hold_gpu(torch)
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
@@ -659,6 +670,7 @@ def time_pq_match(layer, cfg, q_d, k_d, flush, steps, torch, L, first_chunk_keys
             fn()
         res = []
         for _ in range(steps):
+            hold_gpu(torch)
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
@@ -705,6 +717,7 @@ def measure_dit(chunks, seed, torch, dev):
         L.fastar_gemm(A, W, C, act=L.ACT_GELU_TANH)
     ms = []
     for _ in range(10):
+        hold_gpu(torch)
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
@@ -779,6 +792,7 @@ def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):
         stage_ev.setdefault(name, []).append(e)
 
     for _ in range(steps):
+        hold_gpu(torch)
         flush.zero_()
         layer.step(q_d, k_d, v_d, advance=False, timer=timer, serial=True)
     torch.cuda.synchronize(dev)

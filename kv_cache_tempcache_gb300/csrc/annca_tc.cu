@@ -14,7 +14,8 @@
 //   warps 2-9  epilogue, two warps per TMEM lane quadrant (each folds half of the
 //              tile's columns).  Per query tile they first derive the column facts —
 //              1/|q_j| (fp32 sum of squares of the shared-memory Q tile) and q_j's
-//              bucket ids packed as bytes (loaded a tile ahead) — then fold each
+//              bucket ids packed as bytes (loaded a tile ahead), one 8-byte entry per
+//              column (a NaN scale marks an unusable column) — then fold each
 //              prompt row: candidate = s_pj / |q_j| where pb[p] is one of q_j's
 //              buckets, running maximum per row; at the end score = max / |kp_p|.
 // Up to four buckets per query (r <= 4) on this path.
@@ -40,7 +41,7 @@ template <int D>
 struct alignas(1024) CaSmem {
   uint8_t a[D / 64][kCaTile];               // prompt tile
   uint8_t b[kCaStages][D / 64][kCaTile];    // query tiles
-  uint4 col[kCaTS][128];                    // per query column j: {1/|q_j|, bucket-id bytes, ok, -}
+  float2 col[kCaTS][128];                   // per query column j: {1/|q_j| (NaN: unusable), bucket-id bytes}
   float bx[128];                            // second column half's row maxima
   uint64_t a_full, a_empty;
   uint64_t b_full[kCaStages], b_empty[kCaStages];
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         }
       }
       uint32_t nw = 0, nok = 0;
-      if (!norm_role) load_ids(h, f, 0, nw, nok);
+      if (norm_role) load_ids(h, f, 0, nw, nok);
       // 1/|kp_p| from the prompt tile, then hand the tile's shared memory back
       bool got = ca_wait_all(&sm.a_full, aph, abort);
       aph ^= 1;
@@ -253,15 +254,14 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         got = ca_wait_all(&sm.b_full[stage], ph, abort);
         if (got) {
           if (norm_role) {
+            // one 8-byte entry per column, so that the fold's broadcast loads are 8 bytes:
+            // a column without usable bucket ids gets a NaN scale, which fmaxf ignores
             float qi = 0.f;
             if ((int64_t)c * 128 + fcol < g.tpf) {
               const float ss = row_sumsq<D>(&sm.b[stage][0][0], fcol);
               qi = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
             }
-            sm.col[acc][fcol].x = __float_as_uint(qi);
-          } else {
-            sm.col[acc][fcol].y = nw;
-            sm.col[acc][fcol].z = nok;
+            sm.col[acc][fcol] = make_float2(nok ? qi : __uint_as_float(0x7fc00000u), __uint_as_float(nw));
             load_ids(h, f, c + 1, nw, nok);   // next tile's ids, consumed one fold later
           }
           __syncwarp();
@@ -289,10 +289,10 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         if (mypb >= 0) {
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
-            const uint4 cf = sm.col[acc][half * 64 + j];
-            const uint32_t x = cf.y ^ pb4;   // a zero byte where q_j's bucket equals pb[p]
-            const bool hit = ((x - 0x01010101u) & ~x & 0x80808080u) != 0u && cf.z != 0u;
-            best = hit ? fmaxf(best, v[j] * __uint_as_float(cf.x)) : best;
+            const float2 cf = sm.col[acc][half * 64 + j];
+            const uint32_t x = __float_as_uint(cf.y) ^ pb4;   // a zero byte where q_j's bucket is pb[p]
+            const bool hit = ((x - 0x01010101u) & ~x & 0x80808080u) != 0u;
+            best = hit ? fmaxf(best, v[j] * cf.x) : best;   // a NaN scale leaves best unchanged
           }
         }
         if (++acc == kCaTS) {

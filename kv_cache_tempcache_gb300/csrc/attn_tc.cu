@@ -1184,6 +1184,18 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   const int64_t qi = wq % a.nq;
   const int64_t np = a.nq * a.r;
   const int64_t pb = (int64_t)h * np + qi * a.r;   // the query's r slots are adjacent rows
+  // the first two slot rows are loaded together with the lse values, before the weights
+  // are known (every pair has a row in the partial buffer; a row is used only when its
+  // weight is nonzero)
+  float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+  auto load_row = [&](int sl) -> float4 {
+    const float* src = a.part_o + (pb + sl) * D + lane * E;
+    if (E == 4) return __ldcs(reinterpret_cast<const float4*>(src));
+    const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+    return make_float4(v.x, v.y, 0.f, 0.f);
+  };
+  p0 = load_row(0);
+  if (a.r > 1) p1 = load_row(1);
   const float ls = lane < a.r ? a.part_lse[pb + lane] : neg_inf();
   float mx = ls;
 #pragma unroll
@@ -1192,24 +1204,19 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   float W = w;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int sl = 0; sl < a.r; ++sl) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  auto add_row = [&](float ws, const float4& v) {
+    acc[0] = fmaf(ws, v.x, acc[0]);
+    acc[1] = fmaf(ws, v.y, acc[1]);
+    acc[2] = fmaf(ws, v.z, acc[2]);
+    acc[3] = fmaf(ws, v.w, acc[3]);
+  };
+  const float w0 = __shfl_sync(0xffffffffu, w, 0), w1 = __shfl_sync(0xffffffffu, w, 1);
+  if (w0 != 0.f) add_row(w0, p0);
+  if (a.r > 1 && w1 != 0.f) add_row(w1, p1);
+  for (int sl = 2; sl < a.r; ++sl) {
     const float ws = __shfl_sync(0xffffffffu, w, sl);
-    if (ws == 0.f) continue;
-    const float* src = a.part_o + (pb + sl) * D + lane * E;
-    if (E == 4) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
-      acc[0] = fmaf(ws, v.x, acc[0]);
-      acc[1] = fmaf(ws, v.y, acc[1]);
-      acc[2] = fmaf(ws, v.z, acc[2]);
-      acc[3] = fmaf(ws, v.w, acc[3]);
-    } else {
-      const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
-      acc[0] = fmaf(ws, v.x, acc[0]);
-      acc[1] = fmaf(ws, v.y, acc[1]);
-    }
+    if (ws != 0.f) add_row(ws, load_row(sl));
   }
   const float invW = W > 0.f ? 1.0f / W : 0.f;
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + h * a.o_hs + qi * a.o_ts + lane * E;

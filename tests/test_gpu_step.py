@@ -36,6 +36,13 @@ def test_small_bf16_step(seed):
     assert (g["len_out"] == cfg.M).all()
 
 
+@pytest.mark.parametrize("r", [3, 4])
+def test_more_buckets_per_query(r):
+    # r > 2: AnnSA merges more than two slot partials per query, AnnCA gates on more ids
+    _, g, _ = _run(GH.small_bf16().replace(r=r, name=f"bf16_r{r}"))
+    assert g["evict"].sum() > 0
+
+
 def test_bf16_d64_and_f32_d128():
     _run(GH.small_bf16().replace(d=64, name="bf16_d64"))
     _run(GH.small_bf16().replace(dtype="f32", name="f32_d128", H=1, Tf=130, prior_frames=4, M=600))
