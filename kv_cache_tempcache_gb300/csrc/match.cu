@@ -185,6 +185,8 @@ match_simt_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int64_t nq,
 // cosines, and test the matched entry for eviction: cos(kcur_i, k_top1) >= tau.  The
 // owner of an evicted entry is the lowest evicting query (an atomic minimum over the
 // unsigned view, where the cleared value -1 is the largest).
+constexpr int kFinLanes = 4;   // finaliser lanes per query
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t hs, int64_t ts,
@@ -193,9 +195,10 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
                       const float4* __restrict__ part, int32_t* __restrict__ top1,
                       float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict,
                       int32_t* __restrict__ owner) {
-  // eight lanes per query: each lane owns D/8 consecutive elements (vector loads)
-  const int sub = threadIdx.x & 7;
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+  // kFinLanes lanes per query: each lane owns D / kFinLanes consecutive elements (vector
+  // loads); four lanes keep every warp of the layer resident at once
+  const int sub = threadIdx.x & (kFinLanes - 1);
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kFinLanes;
   const bool in = wid < (int64_t)H * nq;
   const int64_t w = in ? wid : 0;
   const int h = (int)(w / nq);
@@ -206,7 +209,7 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   float4 p0 = make_float4(neg_inf(), __int_as_float(INT_MAX), neg_inf(), 0.f);
   if (sub < splits) p0 = part[((int64_t)sub * H + h) * nq + i];
   // |q_i| and |kcur_i|
-  constexpr int E = D / 8;
+  constexpr int E = D / kFinLanes;
   const T* qr = q + h * hs + i * ts + sub * E;
   const T* kr = kc + h * hs + i * ts + sub * E;
   float kv[E];
@@ -223,17 +226,17 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
     }
   }
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) {
+  for (int o = kFinLanes / 2; o > 0; o >>= 1) {
     qq += __shfl_xor_sync(0xffffffffu, qq, o);
     kk += __shfl_xor_sync(0xffffffffu, kk, o);
   }
   Top2 t{p0.x, __float_as_int(p0.y), p0.z};
-  for (int s = sub + 8; s < splits; s += 8) {
+  for (int s = sub + kFinLanes; s < splits; s += kFinLanes) {
     const float4 p = part[((int64_t)s * H + h) * nq + i];
     t = top2_merge(t, Top2{p.x, __float_as_int(p.y), p.z});
   }
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) {
+  for (int o = kFinLanes / 2; o > 0; o >>= 1) {
     Top2 u;
     u.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
     u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
@@ -256,7 +259,7 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
     }
   }
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  for (int o = kFinLanes / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
   if (in && sub == 0) {
     top1[(int64_t)h * nq + i] = j;
     const float inv_q = qq > 0.f ? 1.0f / qq : 0.f;
@@ -294,7 +297,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       const int64_t warps = (int64_t)H * nq;
-      match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
+      match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
           static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
           static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner);
       count_launches(1);
@@ -327,7 +330,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = (int64_t)H * nq;
-  match_finalize_kernel<T, D><<<(unsigned)((warps * 8 + 255) / 256), 256, 0, s>>>(
+  match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
       static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, splits, part, top1, s1, s2, evict, owner);
   count_launches(1);

@@ -105,6 +105,26 @@ def query_buckets(Q, C, r: int) -> np.ndarray:
     return order_desc(S)[:, :r].astype(np.int64)
 
 
+def bucket_order(ids, B: int, n_valid=None):
+    """Tokens grouped by bucket (technical summary §2.C: each query attends to the keys of
+    its own buckets; the spec fixes the grouping as a stable counting sort).  ids [H, n, r]
+    bucket ids of the (token, slot) elements, element e = token * r + slot; only the first
+    n_valid[h] tokens of head h take part.  Returns perm [H, n*r]: the head's elements in
+    bucket order, ascending element id inside a bucket (entries past the head's count are
+    -1), and offsets [H, B+1]: where each bucket starts, offsets[h, B] = the count."""
+    ids = np.asarray(ids)
+    H, n, r = ids.shape
+    perm = np.full((H, n * r), -1, dtype=np.int64)
+    offsets = np.zeros((H, B + 1), dtype=np.int64)
+    for h in range(H):
+        nv = n if n_valid is None else int(n_valid[h])
+        flat = ids[h, :nv].reshape(-1)
+        order = np.argsort(flat, kind="stable")
+        perm[h, :order.size] = order
+        offsets[h, 1:] = np.cumsum(np.bincount(flat, minlength=B)[:B])
+    return perm, offsets
+
+
 # ----------------------------------------------------------------------------------
 # TempCache (technical summary §2.A)
 # ----------------------------------------------------------------------------------

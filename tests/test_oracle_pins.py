@@ -364,3 +364,27 @@ def _strict_evict(top1, ce, n, tau):
         if j >= 0 and ce[i] > tau:
             e[j] = True
     return e
+
+
+def test_bucket_order_against_a_bucket_by_bucket_scan():
+    # the grouping written out as loops: bucket 0's elements in ascending element id,
+    # then bucket 1's, ...; offsets are where each bucket's run starts
+    rng = np.random.default_rng(5)
+    H, n, r, B = 3, 37, 2, 6
+    ids = rng.integers(0, B, size=(H, n, r))
+    n_valid = np.array([37, 20, 0])
+    perm, off = O.bucket_order(ids, B, n_valid)
+    for h in range(H):
+        flat = [int(ids[h, i, s]) for i in range(int(n_valid[h])) for s in range(r)]
+        want, starts = [], []
+        for b in range(B):
+            starts.append(len(want))
+            want += [e for e, bb in enumerate(flat) if bb == b]
+        assert perm[h, :len(want)].tolist() == want
+        assert (perm[h, len(want):] == -1).all()
+        assert off[h].tolist() == starts + [len(want)]
+    # a plausible mistake, descending element ids inside each bucket, differs from it
+    flat0 = ids[0].reshape(-1)
+    bad = (flat0.size - 1) - np.argsort(flat0[::-1], kind="stable")
+    assert np.array_equal(np.sort(bad), np.arange(flat0.size))
+    assert bad.tolist() != perm[0, :flat0.size].tolist()
