@@ -16,6 +16,9 @@
  * identical keys is exact when their values are averaged and their logit is shifted
  * by the group size) replaces step 3 with fastar_cache_compact_merge and step 5 with
  * fastar_sparse_attn_grouped, using the owner output of step 2.
+ * Steps 3-5 can also run as fastar_cache_compact_sorted (the compaction, the key sort of
+ * step 4 and a bucket-ordered copy of the new K/V rows, written as the rows move) followed
+ * by fastar_sparse_attn_presorted, which reads that copy instead of making its own.
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers unless stated otherwise.  The caller allocates
@@ -260,6 +263,27 @@ int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M,
                                int32_t* g_out, int32_t* len_out, int32_t* index_map,
                                int32_t* dev_status, cudaStream_t stream);
 
+/* ---- 3+4. compaction that also leaves AnnSA's input ready ---------------------------
+ * Exactly fastar_cache_compact (same outputs, same slot order), then the stable counting
+ * sort of the new cache's bucket ids kb_out over its first len_out[h] slots (fastar_
+ * bucket_sort with r = 1, n_valid = len_out: kperm int32 [H, M], koff int32 [H, B+1]),
+ * and a copy of the new K/V rows in that bucket order: k_sorted[h, p] = k_out[h,
+ * kperm[h, p]] for p < len_out[h] (same for V; [H, M, d], dtype; rows past len_out
+ * untouched).  kpos int32 [H, M] receives each slot's position in the bucket order (the
+ * inverse of kperm; caller-owned scratch).  The sorted copy is written as the rows move,
+ * instead of being re-read from the new cache by fastar_sparse_attn.  1 <= B <=
+ * FASTAR_MAX_B; k_sorted / v_sorted 16-byte aligned and distinct from the in and out
+ * caches; a bucket id outside [0, B) flags FASTAR_DEV_BAD_BUCKET. */
+int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M,
+                                const void* k_cur, const void* v_cur, int64_t head_stride,
+                                int64_t token_stride, const float* kcur_norm, const int32_t* kcur_bucket,
+                                const void* k_in, const void* v_in, const float* knorm_in,
+                                const int32_t* kb_in, const int32_t* len_in, const uint8_t* evict,
+                                void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
+                                int32_t* len_out, int32_t* index_map, int B, int32_t* kperm,
+                                int32_t* koff, int32_t* kpos, void* k_sorted, void* v_sorted,
+                                int32_t* dev_status, cudaStream_t stream);
+
 /* ---- 4. counting sort by bucket --------------------------------------------------
  * Groups tokens by ANN bucket so that bucket-restricted attention runs on dense
  * blocks (FAST-AR technical summary §2.C: "block-sparse operation"; the
@@ -307,6 +331,21 @@ int fastar_sparse_attn_grouped(const void* q, int dtype, int H, int64_t nq, int 
                                float scale, void* out, int64_t o_head_stride, int64_t o_token_stride,
                                float* lse, int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+
+/* ---- 5c. bucket-restricted self-attention reading a caller-made bucket-ordered copy ---
+ * As 5, with k_sorted / v_sorted ([H, M, d], dtype, 16-byte aligned) the rows of k / v in
+ * kperm order, as fastar_cache_compact_sorted writes them: the tensor-core path reads
+ * them directly instead of copying the rows itself; k, v and kperm are still required
+ * (any other path gathers through them).  Same outputs, workspace and errors as 5. */
+int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, int d,
+                                 int64_t q_head_stride, int64_t q_token_stride, int r, int B,
+                                 const int32_t* qperm, const int32_t* qoff,
+                                 const void* k, const void* v, int64_t M,
+                                 const int32_t* kperm, const int32_t* koff,
+                                 const void* k_sorted, const void* v_sorted, float scale,
+                                 void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                                 int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
 
 /* ---- 6. AnnCA prompt selection ---------------------------------------------------
  * FAST-AR technical summary §2.B and blog §2: keep the prompt tokens that share

@@ -43,6 +43,8 @@ _SIGS = {
                              _P, _P, _P, _P],
     "fastar_cache_compact_merge": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "fastar_cache_compact_sorted": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P],
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
     "fastar_pq_encode": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P],
     "fastar_tempcache_match_pq": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _P, _L, _P, _I, _I, _F, _P, _P, _P,
@@ -52,6 +54,8 @@ _SIGS = {
                            _P, _S, _P],
     "fastar_sparse_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _F, _P, _L,
                                    _L, _P, _P, _P, _S, _P],
+    "fastar_sparse_attn_presorted": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _P, _F,
+                                     _P, _L, _L, _P, _P, _P, _S, _P],
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
                             _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
@@ -205,6 +209,19 @@ def fastar_cache_compact(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm
           ptr(dev_status), stream_handle(stream))
 
 
+def fastar_cache_compact_sorted(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict,
+                                k_out, v_out, knorm_out, kb_out, len_out, index_map, B, kperm, koff, kpos, k_sorted,
+                                v_sorted, dev_status, stream=None):
+    H, nq, d = k_cur.shape
+    hs, ts = tok_strides(k_cur)
+    if tok_strides(v_cur) != (hs, ts):
+        raise ValueError("k_cur and v_cur must share strides")
+    _call("fastar_cache_compact_sorted", dtype_code(k_cur.dtype), H, nq, d, k_in.shape[1], ptr(k_cur), ptr(v_cur),
+          hs, ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(len_in),
+          ptr(evict), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out), ptr(len_out), ptr(index_map), int(B),
+          ptr(kperm), ptr(koff), ptr(kpos), ptr(k_sorted), ptr(v_sorted), ptr(dev_status), stream_handle(stream))
+
+
 def fastar_cache_compact_merge(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, g_in, len_in,
                                evict, top1, owner, k_out, v_out, knorm_out, kb_out, g_out, len_out, index_map,
                                dev_status, stream=None):
@@ -261,6 +278,17 @@ def fastar_sparse_attn(q, r, B, qperm, qoff, k, v, kperm, koff, scale, out, lse,
           ptr(v), k.shape[1], ptr(kperm), ptr(koff), float(scale), ptr(out), oh, ot, ptr(lse), ptr(dev_status),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))
+
+
+def fastar_sparse_attn_presorted(q, r, B, qperm, qoff, k, v, kperm, koff, k_sorted, v_sorted, scale, out, lse,
+                                 dev_status, workspace, stream=None):
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    oh, ot = tok_strides(out)
+    _call("fastar_sparse_attn_presorted", ptr(q), dtype_code(q.dtype), H, nq, d, qh, qt, r, B, ptr(qperm),
+          ptr(qoff), ptr(k), ptr(v), k.shape[1], ptr(kperm), ptr(koff), ptr(k_sorted), ptr(v_sorted), float(scale),
+          ptr(out), oh, ot, ptr(lse), ptr(dev_status), ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
 
 
 def fastar_sparse_attn_grouped(q, r, B, qperm, qoff, k, v, kperm, koff, group_count, scale, out, lse, dev_status,

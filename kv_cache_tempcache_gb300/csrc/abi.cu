@@ -182,6 +182,37 @@ int fastar_cache_compact(int dtype, int H, int64_t nq, int d, int64_t M, const v
       len_out, index_map, dev_status, nullptr, nullptr, nullptr, nullptr, stream));
 }
 
+int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
+                                const void* v_cur, int64_t head_stride, int64_t token_stride,
+                                const float* kcur_norm, const int32_t* kcur_bucket, const void* k_in,
+                                const void* v_in, const float* knorm_in, const int32_t* kb_in,
+                                const int32_t* len_in, const uint8_t* evict, void* k_out, void* v_out,
+                                float* knorm_out, int32_t* kb_out, int32_t* len_out, int32_t* index_map, int B,
+                                int32_t* kperm, int32_t* koff, int32_t* kpos, void* k_sorted, void* v_sorted,
+                                int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || B < 1) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B) return FASTAR_ECAPACITY;
+  if (M < nq) return FASTAR_ECAPACITY;
+  if (H == 0) return FASTAR_OK;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if ((rc = check_tok(v_cur, dtype, d, head_stride, token_stride, nq, H))) return rc;
+  if (nq > 0 && (!kcur_norm || !kcur_bucket)) return FASTAR_EINVAL;
+  const void* ptrs[] = {k_in, v_in, k_out, v_out, k_sorted, v_sorted};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return FASTAR_EINVAL;
+  if (!knorm_in || !kb_in || !len_in || !evict || !knorm_out || !kb_out || !len_out || !index_map || !kperm ||
+      !koff || !kpos)
+    return FASTAR_EINVAL;
+  if (k_in == k_out || v_in == v_out || knorm_in == knorm_out || kb_in == kb_out) return FASTAR_EINVAL;
+  if (k_sorted == k_in || k_sorted == k_out || v_sorted == v_in || v_sorted == v_out) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_cache_compact_sorted(
+      dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
+      kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
+      len_out, index_map, B, kperm, koff, kpos, k_sorted, v_sorted, dev_status, stream));
+}
+
 int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
                                const void* v_cur, int64_t head_stride, int64_t token_stride,
                                const float* kcur_norm, const int32_t* kcur_bucket, const void* k_in,
@@ -288,7 +319,8 @@ int sparse_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t
                      const void* k, const void* v, int64_t M, const int32_t* kperm, const int32_t* koff,
                      const int32_t* group_count, float scale, void* out, int64_t o_head_stride,
                      int64_t o_token_stride, float* lse, int32_t* dev_status, void* workspace,
-                     size_t workspace_bytes, cudaStream_t stream) {
+                     size_t workspace_bytes, cudaStream_t stream, const void* k_sorted = nullptr,
+                     const void* v_sorted = nullptr) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || nq < 0 || M < 1 || r < 1 || B < 1 || M > INT32_MAX) return FASTAR_EINVAL;
@@ -332,6 +364,11 @@ int sparse_attn_impl(const void* q, int dtype, int H, int64_t nq, int d, int64_t
     a.vsorted = ks + sizeof(uint16_t) * (size_t)H * M * d;
     a.lg_sorted = reinterpret_cast<float*>(ks + 2 * sizeof(uint16_t) * (size_t)H * M * d);
   }
+  if (k_sorted) {   // the caller's bucket-ordered copy replaces the workspace one
+    a.ksorted = const_cast<void*>(k_sorted);
+    a.vsorted = const_cast<void*>(v_sorted);
+    a.presorted = 1;
+  }
   a.gcount = group_count;
   a.gc_hs = M;
   a.status = dev_status;
@@ -367,6 +404,18 @@ int fastar_sparse_attn_grouped(const void* q, int dtype, int H, int64_t nq, int 
   return sparse_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, r, B, qperm, qoff, k, v, M, kperm, koff,
                           group_count, scale, out, o_head_stride, o_token_stride, lse, dev_status, workspace,
                           workspace_bytes, stream);
+}
+
+int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, int d, int64_t q_head_stride,
+                                 int64_t q_token_stride, int r, int B, const int32_t* qperm, const int32_t* qoff,
+                                 const void* k, const void* v, int64_t M, const int32_t* kperm,
+                                 const int32_t* koff, const void* k_sorted, const void* v_sorted, float scale,
+                                 void* out, int64_t o_head_stride, int64_t o_token_stride, float* lse,
+                                 int32_t* dev_status, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_sorted || !v_sorted || !aligned16(k_sorted) || !aligned16(v_sorted)) return FASTAR_EINVAL;
+  return sparse_attn_impl(q, dtype, H, nq, d, q_head_stride, q_token_stride, r, B, qperm, qoff, k, v, M, kperm, koff,
+                          nullptr, scale, out, o_head_stride, o_token_stride, lse, dev_status, workspace,
+                          workspace_bytes, stream, k_sorted, v_sorted);
 }
 
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,

@@ -1254,7 +1254,14 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   b.kv_tma = 0;
   b.q_tma = 0;
   b.q_token_major = 0;
-  if (a.mode == kSparse) {
+  if (a.mode == kSparse && a.presorted) {
+    // the caller's bucket-ordered copies (written by the compaction as it moved the rows)
+    if (make_tmap_bf16_3d(&tk, a.ksorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2, (uint64_t)a.M * D * 2,
+                          64, kKT) &&
+        make_tmap_bf16_3d(&tv, a.vsorted, D, (uint64_t)a.M, (uint64_t)a.H, (uint64_t)D * 2, (uint64_t)a.M * D * 2,
+                          64, kKT))
+      b.kv_tma = 1;
+  } else if (a.mode == kSparse) {
     // bucket-ordered copies of the cache rows, read as contiguous tiles
     // (the queries stay gathered: copying the pairs' rows costs more than it saves)
     if (a.ksorted && a.vsorted &&

@@ -137,7 +137,8 @@ constexpr int kSortStage = 8192;   // ids of a chunk staged in shared memory whe
 
 __global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortWarpsC * 32)
 bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, const int32_t* __restrict__ n_valid,
-                   int32_t* __restrict__ perm, int32_t* __restrict__ offsets, int32_t* status) {
+                   int32_t* __restrict__ perm, int32_t* __restrict__ offsets, int32_t* __restrict__ inv,
+                   int32_t* status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ int cnt[kSortWarpsC][FASTAR_MAX_B];
@@ -162,6 +163,7 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, con
   const int64_t ce = cb + per < E ? cb + per : E;
   const int32_t* id = ids + (int64_t)h * n * r;
   int32_t* out = perm + (int64_t)h * n * r;
+  int32_t* where = inv ? inv + (int64_t)h * n * r : nullptr;   // element -> its sorted position
   for (int i = t; i < kSortWarpsC * FASTAR_MAX_B; i += blockDim.x) (&cnt[0][0])[i] = 0;
   const bool staged = ce - cb <= kSortStage;
   if (staged)
@@ -236,7 +238,9 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, con
     if (b >= 0) start = cnt[warp][b];
     __syncwarp();
     if (b >= 0) {
-      out[start + __popc(peers & ((1u << lane) - 1u))] = (int32_t)e;
+      const int dst = start + __popc(peers & ((1u << lane) - 1u));
+      out[dst] = (int32_t)e;
+      if (where) where[e] = dst;
       if (lane == __ffs(peers) - 1) cnt[warp][b] = start + __popc(peers);
     }
     __syncwarp();
@@ -245,8 +249,8 @@ bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, con
 
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
-                               int32_t* status, cudaStream_t s) {
-  bucket_sort_kernel<<<H * kSortCtas, kSortWarpsC * 32, 0, s>>>(ids, n, r, B, n_valid, perm, offsets, status);
+                               int32_t* status, cudaStream_t s, int32_t* inv) {
+  bucket_sort_kernel<<<H * kSortCtas, kSortWarpsC * 32, 0, s>>>(ids, n, r, B, n_valid, perm, offsets, inv, status);
   count_launches(1);
   return cudaGetLastError();
 }

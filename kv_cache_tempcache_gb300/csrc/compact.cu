@@ -92,6 +92,37 @@ struct MergeIO {
   int32_t* g_out;         // [H, M] outgoing group counts
 };
 
+// The bucket-ordered copy written beside the cache (all null otherwise): slot s of head h
+// also goes to row kpos[h, s] of ksorted / vsorted.
+struct SortedIO {
+  const int32_t* kpos;
+  void* ksorted;
+  void* vsorted;
+};
+
+// Bucket id of every slot of the new cache (before the rows move, so that the sort can
+// run first): the source entry's, through the index map.
+__global__ void __launch_bounds__(256)
+compact_bucket_kernel(int H, int64_t nq, int64_t M, const int32_t* __restrict__ kcb, const int32_t* __restrict__ kbin,
+                      const int32_t* __restrict__ len_in, const int32_t* __restrict__ len_out,
+                      const int32_t* __restrict__ index_map, int32_t* __restrict__ kbout, int32_t* status) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= (int64_t)H * M) return;
+  const int h = (int)(row / M);
+  if (row - (int64_t)h * M >= len_out[h]) return;
+  int64_t n = len_in[h];
+  n = n < 0 ? 0 : (n > M ? M : n);
+  const int64_t src = index_map[row];
+  if (src >= 0 && src < n) {
+    kbout[row] = kbin[(int64_t)h * M + src];
+  } else if (src >= n && src < n + nq) {
+    kbout[row] = kcb[(int64_t)h * nq + (src - n)];
+  } else {
+    flag_status(status, FASTAR_DEV_BAD_INDEX);
+    kbout[row] = -1;
+  }
+}
+
 // wa * a + wb * b element-wise over one 16-byte chunk (fp32 arithmetic, rounded once).
 template <typename T>
 __device__ __forceinline__ uint4 blend16(uint4 a, uint4 b, float wa, float wb) {
@@ -114,7 +145,7 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
                     const int32_t* __restrict__ kbin, const int32_t* __restrict__ len_in,
                     const int32_t* __restrict__ len_out, const int32_t* __restrict__ index_map,
                     T* __restrict__ kout, T* __restrict__ vout, float* __restrict__ knout,
-                    int32_t* __restrict__ kbout, int32_t* status, const MergeIO mg) {
+                    int32_t* __restrict__ kbout, int32_t* status, const MergeIO mg, const SortedIO so) {
   constexpr int VPR = D * (int)sizeof(T) / 16;
   const int64_t total = (int64_t)H * M * VPR;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -153,7 +184,21 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
       if (c == 0) flag_status(status, FASTAR_DEV_BAD_INDEX);
       continue;
     }
-    reinterpret_cast<uint4*>(kout + row * D)[c] = __ldg(ks);
+    // the bucket-ordered row this slot also goes to (null: none)
+    uint4* ksd = nullptr;
+    uint4* vsd = nullptr;
+    if (so.kpos) {
+      const int32_t p = so.kpos[row];
+      if (p >= 0 && p < M) {
+        ksd = reinterpret_cast<uint4*>(static_cast<T*>(so.ksorted) + ((int64_t)h * M + p) * D) + c;
+        vsd = reinterpret_cast<uint4*>(static_cast<T*>(so.vsorted) + ((int64_t)h * M + p) * D) + c;
+      } else if (c == 0) {
+        flag_status(status, FASTAR_DEV_BAD_INDEX);
+      }
+    }
+    const uint4 kr = __ldg(ks);
+    reinterpret_cast<uint4*>(kout + row * D)[c] = kr;
+    if (ksd) *ksd = kr;
     if (kMerge && absorb >= 0) {
       int32_t gj = mg.g_in[(int64_t)h * M + absorb];
       if (gj < 0) {
@@ -162,10 +207,14 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
       }
       const float inv = 1.0f / (1.0f + (float)gj);
       const uint4 vj = __ldg(reinterpret_cast<const uint4*>(vin + ((int64_t)h * M + absorb) * D) + c);
-      reinterpret_cast<uint4*>(vout + row * D)[c] = blend16<T>(__ldg(vs), vj, inv, (float)gj * inv);
+      const uint4 vr = blend16<T>(__ldg(vs), vj, inv, (float)gj * inv);
+      reinterpret_cast<uint4*>(vout + row * D)[c] = vr;
+      if (vsd) *vsd = vr;
       gc = 1 + gj;
     } else {
-      reinterpret_cast<uint4*>(vout + row * D)[c] = __ldg(vs);
+      const uint4 vr = __ldg(vs);
+      reinterpret_cast<uint4*>(vout + row * D)[c] = vr;
+      if (vsd) *vsd = vr;
     }
     if (c == 0) {
       knout[row] = kn;
@@ -180,7 +229,7 @@ static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView v
                              const int32_t* kcb, const void* kin, const void* vin, const float* knin,
                              const int32_t* kbin, const int32_t* len_in, const int32_t* len_out,
                              const int32_t* imap, void* kout, void* vout, float* knout, int32_t* kbout,
-                             int32_t* status, const MergeIO& mg, cudaStream_t s) {
+                             int32_t* status, const MergeIO& mg, cudaStream_t s, const SortedIO& so = SortedIO{}) {
   constexpr int VPR = D * (int)sizeof(T) / 16;
   const int64_t total = (int64_t)H * M * VPR;
   int64_t blocks = (total + 255) / 256;
@@ -190,7 +239,7 @@ static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView v
   kern<<<(unsigned)blocks, 256, 0, s>>>(
       H, nq, M, static_cast<const T*>(kc.p), static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb,
       static_cast<const T*>(kin), static_cast<const T*>(vin), knin, kbin, len_in, len_out, imap,
-      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg);
+      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg, so);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -219,6 +268,39 @@ cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M,
                                  vout, knout, kbout, status, mg, s);
   return copy_impl<float, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout,
                               knout, kbout, status, mg, s);
+}
+
+cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int64_t M, TokView kc, TokView vc,
+                                        const float* kcn, const int32_t* kcb, const void* kin, const void* vin,
+                                        const float* knin, const int32_t* kbin, const int32_t* len_in,
+                                        const uint8_t* evict, void* kout, void* vout, float* knout,
+                                        int32_t* kbout, int32_t* len_out, int32_t* imap, int B, int32_t* kperm,
+                                        int32_t* koff, int32_t* kpos, void* ksorted, void* vsorted,
+                                        int32_t* status, cudaStream_t s) {
+  compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status);
+  count_launches(1);
+  const int64_t rows = (int64_t)H * M;
+  compact_bucket_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(H, nq, M, kcb, kbin, len_in, len_out, imap,
+                                                                        kbout, status);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_bucket_sort(kbout, H, M, 1, B, len_out, kperm, koff, status, s, kpos);
+  if (e != cudaSuccess) return e;
+  const MergeIO mg{nullptr, nullptr, nullptr, nullptr};
+  const SortedIO so{kpos, ksorted, vsorted};
+  if (dtype == FASTAR_BF16) {
+    if (d == 128)
+      return copy_impl<__nv_bfloat16, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap,
+                                           kout, vout, knout, kbout, status, mg, s, so);
+    return copy_impl<__nv_bfloat16, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap,
+                                        kout, vout, knout, kbout, status, mg, s, so);
+  }
+  if (d == 128)
+    return copy_impl<float, 128>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout,
+                                 vout, knout, kbout, status, mg, s, so);
+  return copy_impl<float, 64>(H, nq, M, kc, vc, kcn, kcb, kin, vin, knin, kbin, len_in, len_out, imap, kout, vout,
+                              knout, kbout, status, mg, s, so);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -24,9 +24,10 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 // Tensor-core bucket assignment (bf16); false if it could not be set up.
 bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int B, int r, int32_t* ids,
                       float* scores, float* norms, cudaStream_t s);
+// inv (optional, [H, n*r]): each element's position in its head's sorted order.
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
-                               int32_t* status, cudaStream_t s);
+                               int32_t* status, cudaStream_t s, int32_t* inv = nullptr);
 
 // ---- TempCache ----------------------------------------------------------------------
 int match_splits(int H, int64_t nq, int64_t M);
@@ -65,6 +66,17 @@ cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M,
                                  const int32_t* top1, const int32_t* owner, const int32_t* g_in,
                                  int32_t* g_out, cudaStream_t s);
 
+// The compaction that also leaves AnnSA's input ready: the new cache's bucket ids, their
+// stable counting sort (kperm, koff, and kpos = each slot's position in bucket order) and
+// a bucket-ordered copy of the new K/V rows (ksorted, vsorted), written as the rows move.
+cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int64_t M, TokView kc, TokView vc,
+                                        const float* kcn, const int32_t* kcb, const void* kin, const void* vin,
+                                        const float* knin, const int32_t* kbin, const int32_t* len_in,
+                                        const uint8_t* evict, void* kout, void* vout, float* knout,
+                                        int32_t* kbout, int32_t* len_out, int32_t* imap, int B, int32_t* kperm,
+                                        int32_t* koff, int32_t* kpos, void* ksorted, void* vsorted,
+                                        int32_t* status, cudaStream_t s);
+
 // ---- attention ------------------------------------------------------------------------
 enum AttnMode { kDense = 0, kCross = 1, kSparse = 2, kMatchAnn = 3 };
 
@@ -100,6 +112,7 @@ struct AttnArgs {
   void* items;      // sparse: work list written by the planning kernel (tensor-core path)
   void* ksorted;    // sparse: the cache K/V rows in bucket order [H, M, d] (tensor-core path)
   void* vsorted;
+  int presorted;    // sparse: ksorted / vsorted already hold that copy (the caller's buffers)
   int kv_tma;       // keys/values arrive as contiguous TMA tiles (set by the launcher)
   int q_tma;        // so do the query tiles: one thread drives every copy (set by the launcher)
   int q_token_major;  // the query tensor map is (d, H, tokens) rather than (d, tokens, H)

@@ -105,6 +105,13 @@ class FastARLayer:
         self.index_map = _i32(H, M, dev=dev)
         self.kperm = _i32(H, M, dev=dev)
         self.koff = _i32(H, B + 1, dev=dev)
+        # the replace variant in bf16: the compaction also sorts the new cache's keys and
+        # writes AnnSA's bucket-ordered copy of K/V as it moves the rows
+        self.presort = dtype == torch.bfloat16 and not self.merge
+        if self.presort:
+            self.kpos = _i32(H, M, dev=dev)
+            self.k_sorted = torch.zeros((H, M, d), dtype=dtype, device=dev)
+            self.v_sorted = torch.zeros((H, M, d), dtype=dtype, device=dev)
         self.qperm = _i32(H, Nq * r, dev=dev)
         self.qoff = _i32(H, B + 1, dev=dev)
         self.o_self = torch.zeros((H, Nq, d), dtype=dtype, device=dev)
@@ -268,6 +275,11 @@ class FastARLayer:
             L.fastar_cache_compact_merge(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                          cin.g, cin.len, self.evict, self.top1, self.owner, cout.k, cout.v,
                                          cout.knorm, cout.kb, cout.g, cout.len, self.index_map, self.dev_status)
+        elif self.presort:
+            L.fastar_cache_compact_sorted(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                                          cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
+                                          self.index_map, self.B, self.kperm, self.koff, self.kpos, self.k_sorted,
+                                          self.v_sorted, self.dev_status)
         else:
             L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                    cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
@@ -276,14 +288,19 @@ class FastARLayer:
             L.fastar_pq_gather_codes(cin.codes, cin.len, self.codes_cur, self.index_map, cout.len, cout.codes,
                                      self.dev_status)
         t("cache_compact", main, "end")
-        t("bucket_sort", main, "begin")
-        L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
-        t("bucket_sort", main, "end")
+        if not self.presort:   # (the sorted compaction has grouped the keys already)
+            t("bucket_sort", main, "begin")
+            L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
+            t("bucket_sort", main, "end")
         t("sparse_attn", main, "begin")
         if self.merge:
             L.fastar_sparse_attn_grouped(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm,
                                          self.koff, cout.g, self.scale, self.o_self, self.lse_self, self.dev_status,
                                          self.ws_attn)
+        elif self.presort:
+            L.fastar_sparse_attn_presorted(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm,
+                                           self.koff, self.k_sorted, self.v_sorted, self.scale, self.o_self,
+                                           self.lse_self, self.dev_status, self.ws_attn)
         else:
             L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
                                  self.scale, self.o_self, self.lse_self, self.dev_status, self.ws_attn)
@@ -306,12 +323,21 @@ class FastARLayer:
         L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
         L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, None,
                                  self.evict, self.dev_status, self.ws_match)
-        L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb, cin.len,
-                               self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len, self.index_map,
-                               self.dev_status)
-        L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
-        L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
-                             self.scale, o, self.lse_self, self.dev_status, self.ws_attn)
+        if self.presort:
+            L.fastar_cache_compact_sorted(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                                          cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
+                                          self.index_map, self.B, self.kperm, self.koff, self.kpos, self.k_sorted,
+                                          self.v_sorted, self.dev_status)
+            L.fastar_sparse_attn_presorted(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm,
+                                           self.koff, self.k_sorted, self.v_sorted, self.scale, o, self.lse_self,
+                                           self.dev_status, self.ws_attn)
+        else:
+            L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
+                                   cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
+                                   self.index_map, self.dev_status)
+            L.fastar_bucket_sort(cout.kb, self.B, self.kperm, self.koff, cout.len, self.dev_status)
+            L.fastar_sparse_attn(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm, self.koff,
+                                 self.scale, o, self.lse_self, self.dev_status, self.ws_attn)
         if advance:
             self.cur = 1 - self.cur
         return o

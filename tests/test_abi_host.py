@@ -103,6 +103,24 @@ def test_argument_validation_rejects_before_launch(lib):
                                           s) == L.EINVAL
     assert lib.fastar_dense_attn_grouped(FAKE, L.BF16, 2, 64, 128, 8192, 128, FAKE, FAKE, 100, 12800, 128, FAKE, 50,
                                          0.1, FAKE, 8192, 128, None, s) == L.EINVAL
+    # the sorted compaction needs its sorted copies, distinct from the caches, and a bucket count
+    base = [L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+            FAKE + 1024, FAKE + 2048, FAKE + 16, FAKE + 32, FAKE + 48, FAKE + 64]
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, None, FAKE + 4096, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 8, FAKE + 4096, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 1024, FAKE + 4096, None,
+                                           s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 0, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, None,
+                                           s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 300, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, None,
+                                           s) == L.ECAPACITY
+    # the presorted attention needs both sorted copies, 16-byte aligned
+    assert lib.fastar_sparse_attn_presorted(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE,
+                                            128, FAKE, FAKE, None, FAKE, 0.1, FAKE, 8192, 128, None, None, FAKE,
+                                            1 << 30, s) == L.EINVAL
+    assert lib.fastar_sparse_attn_presorted(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE,
+                                            128, FAKE, FAKE, FAKE + 2, FAKE, 0.1, FAKE, 8192, 128, None, None,
+                                            FAKE, 1 << 30, s) == L.EINVAL
     # the row kernels read their per-channel vectors 16 bytes at a time: misaligned ones are refused
     assert lib.fastar_layernorm_mod(FAKE, 1536, 10, 1536, 1e-6, None, None, FAKE + 4, None, None, None, FAKE,
                                     1536, s) == L.EINVAL
