@@ -128,7 +128,8 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 // the total (the bucket offsets) and the count in the chunks before its own.  Pass 2
 // replays the chunk and scatters each element to bucket offset + earlier chunks +
 // earlier warps + its rank among same-bucket lanes of the batch, so the order inside
-// a bucket is ascending element id.  The CTAs of a cluster are co-scheduled by the
+// a bucket is ascending element id.  Optionally each element's sorted position is written
+// too (the inverse permutation).  The CTAs of a cluster are co-scheduled by the
 // hardware and every thread executes both cluster barriers unconditionally.
 // ---------------------------------------------------------------------------------------
 constexpr int kSortCtas = 8;

@@ -6,7 +6,10 @@
 // the method spec's.
 //
 // Two kernels: a one-CTA-per-head scan that writes the slot -> source map and the
-// new length, then a bandwidth kernel that moves rows with 16-byte accesses.
+// new length, then a bandwidth kernel that moves rows with 16-byte accesses.  The sorted
+// form puts the new cache's bucket ids and their stable counting sort between the two,
+// so that the copy can also write each row to its place in a bucket-ordered copy (the
+// layout the bucket-restricted attention reads as contiguous tiles).
 //
 // The merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1 — identical
 // keys merge exactly when their values are averaged and the logit is shifted by the
