@@ -14,10 +14,6 @@ from oracle import fastar_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-def _bf(a):
-    return torch.from_numpy(np.ascontiguousarray(synth.bf16_round(a.astype(np.float32)))).cuda().to(torch.bfloat16)
-
-
 def _i32(a):
     return torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()
 
@@ -26,13 +22,19 @@ def _np(t):
     return t.detach().float().cpu().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
 
 
-@pytest.mark.parametrize("H,M,nq,B,lens", [
-    (3, 1000, 600, 16, [1000, 700, 0]),       # full, partial and empty incoming caches
-    (2, 9360, 4680, 64, [9360, 9000]),        # the Wan-1.3B layer's cap and chunk
+@pytest.mark.parametrize("H,M,nq,B,lens,d,dtype", [
+    (3, 1000, 600, 16, [1000, 700, 0], 128, "bf16"),     # full, partial and empty incoming caches
+    (2, 9360, 4680, 64, [9360, 9000], 128, "bf16"),      # the Wan-1.3B layer's cap and chunk
+    (2, 700, 300, 8, [650, 700], 64, "f32"),             # fp32 rows, d = 64 (the SIMT attention path)
 ])
-def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
+def test_sorted_compaction_matches_oracle(H, M, nq, B, lens, d, dtype):
     rng = np.random.default_rng(M + B)
-    d = 128
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    rnd = synth.bf16_round if dtype == "bf16" else (lambda a: a.astype(np.float32))
+
+    def _rows(a):
+        return torch.from_numpy(np.ascontiguousarray(rnd(a.astype(np.float32)))).cuda().to(tdt)
+
     k_in, v_in = rng.standard_normal((2, H, M, d)).astype(np.float32)
     k_cur, v_cur = rng.standard_normal((2, H, nq, d)).astype(np.float32)
     kb_in = rng.integers(0, B, size=(H, M))
@@ -42,12 +44,12 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
     evict = (rng.random((H, M)) < 0.2).astype(np.uint8)
     len_in = np.array(lens)
     dev = dict(
-        k_cur=_bf(k_cur), v_cur=_bf(v_cur), kcur_norm=torch.from_numpy(knorm_cur).cuda(),
-        kcur_bucket=_i32(kb_cur[..., None]), k_in=_bf(k_in), v_in=_bf(v_in),
+        k_cur=_rows(k_cur), v_cur=_rows(v_cur), kcur_norm=torch.from_numpy(knorm_cur).cuda(),
+        kcur_bucket=_i32(kb_cur[..., None]), k_in=_rows(k_in), v_in=_rows(v_in),
         knorm_in=torch.from_numpy(knorm_in).cuda(), kb_in=_i32(kb_in[..., None]), len_in=_i32(len_in),
         evict=torch.from_numpy(evict).cuda())
-    out = dict(k_out=torch.zeros((H, M, d), dtype=torch.bfloat16, device="cuda"),
-               v_out=torch.zeros((H, M, d), dtype=torch.bfloat16, device="cuda"),
+    out = dict(k_out=torch.zeros((H, M, d), dtype=tdt, device="cuda"),
+               v_out=torch.zeros((H, M, d), dtype=tdt, device="cuda"),
                knorm_out=torch.zeros((H, M), dtype=torch.float32, device="cuda"),
                kb_out=torch.zeros((H, M, 1), dtype=torch.int32, device="cuda"),
                len_out=torch.zeros(H, dtype=torch.int32, device="cuda"),
@@ -55,8 +57,8 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
     kperm = torch.zeros((H, M), dtype=torch.int32, device="cuda")
     koff = torch.zeros((H, B + 1), dtype=torch.int32, device="cuda")
     kpos = torch.zeros((H, M), dtype=torch.int32, device="cuda")
-    k_sorted = torch.zeros((H, M, d), dtype=torch.bfloat16, device="cuda")
-    v_sorted = torch.zeros((H, M, d), dtype=torch.bfloat16, device="cuda")
+    k_sorted = torch.zeros((H, M, d), dtype=tdt, device="cuda")
+    v_sorted = torch.zeros((H, M, d), dtype=tdt, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     L.fastar_cache_compact_sorted(dev["k_cur"], dev["v_cur"], dev["kcur_norm"], dev["kcur_bucket"], dev["k_in"],
                                   dev["v_in"], dev["knorm_in"], dev["kb_in"], dev["len_in"], dev["evict"],
@@ -66,8 +68,8 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
     assert int(status.item()) == 0
     g = {k: _np(v) for k, v in out.items()}
     kperm_g, koff_g, ks_g, vs_g = _np(kperm), _np(koff), _np(k_sorted), _np(v_sorted)
-    kin_b, vin_b = synth.bf16_round(k_in), synth.bf16_round(v_in)
-    kcur_b, vcur_b = synth.bf16_round(k_cur), synth.bf16_round(v_cur)
+    kin_b, vin_b = rnd(k_in), rnd(v_in)
+    kcur_b, vcur_b = rnd(k_cur), rnd(v_cur)
     kb_new = []
     for h in range(H):
         n = int(len_in[h])
@@ -92,7 +94,7 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
 
     # the attention that reads this copy equals the one that makes its own, bit for bit
     r = 2
-    q = _bf(rng.standard_normal((H, nq, d)).astype(np.float32))
+    q = _rows(rng.standard_normal((H, nq, d)).astype(np.float32))
     qb = _i32(rng.integers(0, B, size=(H, nq, r)))
     qperm = torch.zeros((H, nq * r), dtype=torch.int32, device="cuda")
     qoff = torch.zeros((H, B + 1), dtype=torch.int32, device="cuda")
@@ -101,7 +103,7 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens):
                      device="cuda")
     res = []
     for presorted in (False, True):
-        o = torch.zeros((H, nq, d), dtype=torch.bfloat16, device="cuda")
+        o = torch.zeros((H, nq, d), dtype=tdt, device="cuda")
         lse = torch.zeros((H, nq), dtype=torch.float32, device="cuda")
         if presorted:
             L.fastar_sparse_attn_presorted(q, r, B, qperm, qoff, out["k_out"], out["v_out"], kperm, koff, k_sorted,
