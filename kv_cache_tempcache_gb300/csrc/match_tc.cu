@@ -13,10 +13,11 @@
 //               as precomputed offsets), committing to the ring's "empty" barriers
 //               and the accumulator's "full" barrier;
 //   warps 2..17 epilogue, four warps per TMEM lane quadrant (4 column parts of 32
-//               keys): each thread owns the same row of both M-tiles, reads its two
-//               32-score chunks, scales them by 1/|k_j| (norms prefetched a tile
-//               ahead, packed f32x2 multiplies) and keeps the running top-1 (and
-//               top-2 when asked) of both rows with three-input max trees.  The
+//               keys): each thread owns the same row of both M-tiles, reads the 32
+//               scores of each in two 16-column halves, scales them by 1/|k_j| (norms
+//               prefetched a tile ahead, packed f32x2 multiplies) and keeps the
+//               running top-1 (and top-2 when asked) of both rows with three-input
+//               max trees over groups of four columns.  The
 //               1/|k_j| values reach the lanes as shared-memory broadcasts, which
 //               share the data pipe with the tensor core's operand reads: one
 //               broadcast serving both M-tiles halves that traffic.  16 warps keep
