@@ -158,3 +158,30 @@ def test_product_path_has_no_cpu_fallback():
 def test_last_cuda_error_starts_clean(lib):
     # nothing has failed in this process: the CUDA-error diagnostic reports no error
     assert lib.fastar_last_cuda_error().decode() == "no error"
+
+
+def _header_params():
+    """name -> the C parameter types of every fastar_* declaration in the header."""
+    out = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", f)).read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(fastar_\w+)\s*\(([^)]*)\)\s*;", text):
+            params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+            out[m.group(1)] = [re.sub(r"\s+\w+$", "", p) if "*" not in p else p for p in params]
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    # every declared parameter has a ctypes type of the same kind, in the same order
+    from kv_cache_tempcache_gb300 import _lib
+    kind = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "float": ctypes.c_float, "size_t": ctypes.c_size_t,
+            "cudaStream_t": ctypes.c_void_p}
+    decls = _header_params()
+    assert len(decls) >= 12
+    for name, params in decls.items():
+        got = _lib._SIGS[name]
+        want = [ctypes.c_void_p if "*" in p else kind[p.replace("const ", "").strip()] for p in params]
+        assert got == want, f"{name}: binding {[t.__name__ for t in got]} vs header {params}"
