@@ -388,3 +388,30 @@ def test_bucket_order_against_a_bucket_by_bucket_scan():
     bad = (flat0.size - 1) - np.argsort(flat0[::-1], kind="stable")
     assert np.array_equal(np.sort(bad), np.arange(flat0.size))
     assert bad.tolist() != perm[0, :flat0.size].tolist()
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_dense_baseline_step_matches_library_attention(seed):
+    # the dense baseline is plain softmax attention over every past key plus the chunk,
+    # and over the whole prompt: the library routine (float64) gives the same numbers
+    rng = np.random.default_rng(seed)
+    n_hist, nq, P, d = 57, 19, 13, 16
+    q, k_cur, v_cur = rng.standard_normal((3, nq, d))
+    hk, hv = rng.standard_normal((2, n_hist, d))
+    kp, vp = rng.standard_normal((2, P, d))
+    scale = 0.7 / math.sqrt(d)
+    out = O.head_dense_step(q, hk, hv, k_cur, v_cur, kp, vp, scale)
+    t = lambda x: torch.tensor(np.asarray(x), dtype=torch.float64)
+    K, V = t(np.concatenate([hk, k_cur])), t(np.concatenate([hv, v_cur]))
+    sdpa = torch.nn.functional.scaled_dot_product_attention
+    np.testing.assert_allclose(out["o_self"], sdpa(t(q)[None], K[None], V[None], scale=scale)[0].numpy(),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["o_cross"], sdpa(t(q)[None], t(kp)[None], t(vp)[None], scale=scale)[0].numpy(),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["lse_self"], torch.logsumexp(t(q) @ K.T * scale, dim=1).numpy(), rtol=0,
+                               atol=1e-12)
+    np.testing.assert_allclose(out["lse_cross"], torch.logsumexp(t(q) @ t(kp).T * scale, dim=1).numpy(), rtol=0,
+                               atol=1e-12)
+    # a plausible mistake, the current chunk left out of the self-attention keys, differs
+    miss, _ = O.dense_attention(q, hk, hv, scale)
+    assert np.abs(miss - out["o_self"]).max() > 1e-3
