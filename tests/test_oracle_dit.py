@@ -160,3 +160,25 @@ def test_dit_step_with_silent_blocks_is_the_head_alone():
     h = xn * (1 + p["head_mod"][1] + e) + p["head_mod"][0] + e
     want = lat - 0.25 * (h @ p["head_w"].T + p["head_b"])
     np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+def test_text_context_and_cross_kv_reduce_with_identity_weights():
+    # identity projections without bias: the text context is the tanh-form GELU of the
+    # text itself (known values at 0 and for large |x|), and a block's cross keys are the
+    # RMS-normed context rows (unit mean square), its values the context itself
+    rng = np.random.default_rng(4)
+    n, c = 9, 12
+    text = rng.standard_normal((n, c)) * 3
+    eye, zero = np.eye(c), np.zeros(c)
+    p = dict(text_w1=eye, text_b1=zero, text_w2=eye, text_b2=zero)
+    ctx = D.text_context(p, text)
+    x = text
+    np.testing.assert_allclose(ctx, 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3))),
+                               rtol=0, atol=1e-12)
+    edge = D.text_context(p, np.array([[0.0] * (c - 2) + [40.0, -40.0]]))
+    np.testing.assert_allclose(edge[0, -2:], [40.0, 0.0], atol=1e-12)
+    b = dict(ck_w=eye, ck_b=zero, cv_w=eye, cv_b=zero, norm_ck=np.ones(c))
+    k, v = D.block_text_kv(b, ctx, 4, 0.0)
+    np.testing.assert_allclose((k ** 2).mean(axis=1), 1.0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(k * np.sqrt((ctx ** 2).mean(axis=1, keepdims=True)), ctx, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(v, ctx, rtol=0, atol=1e-12)
