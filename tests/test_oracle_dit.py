@@ -182,3 +182,160 @@ def test_text_context_and_cross_kv_reduce_with_identity_weights():
     np.testing.assert_allclose((k ** 2).mean(axis=1), 1.0, rtol=0, atol=1e-12)
     np.testing.assert_allclose(k * np.sqrt((ctx ** 2).mean(axis=1, keepdims=True)), ctx, rtol=0, atol=1e-12)
     np.testing.assert_allclose(v, ctx, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------------
+# the block body, worked by hand (tests/golden/dit_block_2d.json)
+# ----------------------------------------------------------------------------------
+
+def _golden_block():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "dit_block_2d.json")))
+    c = g["config"]
+
+    class Cfg:
+        pass
+
+    for k, v in c.items():
+        setattr(Cfg, k, v)
+    p = {k: np.asarray(v, np.float64) for k, v in g["params"].items() if k != "block"}
+    p["blocks"] = [{k: np.asarray(v, np.float64) for k, v in g["params"]["block"].items()}]
+    tk = np.array([[float(x) if x != "ln3" else math.log(3.0) for x in row] for row in g["text_k"]])
+    tv = np.asarray(g["text_v"], np.float64)
+    return g, Cfg, p, tk, tv
+
+
+def _run_golden(p, Cfg, g, tk, tv):
+    hist = [(np.zeros((0, 2)), np.zeros((0, 2)))]
+    return D.dit_step(p, Cfg, np.asarray(g["lat"], np.float64), g["t"], g["t_next"], g["frame0"], hist, [(tk, tv)])
+
+
+def _block_only(p, Cfg, g, tk, tv, m):
+    """dit_block on the golden's single token with the given modulation rows."""
+    x = np.asarray(g["lat"], np.float64)            # identity patch map, zero patch bias
+    pos = D.token_positions(1, g["frame0"], 1, 1)
+    sa = lambda q, k, v: D.heads_attention(q, k, v, 1)
+    ca = lambda qc: D.heads_attention(qc, tk, tv, 1)
+    return D.dit_block(p["blocks"][0], Cfg, x, np.asarray(m, np.float64), pos, sa, ca)
+
+
+def test_dit_block_hand_worked():
+    g, Cfg, p, tk, tv = _golden_block()
+    x3, (k, v) = _block_only(p, Cfg, g, tk, tv, g["modulation"])
+    np.testing.assert_allclose(x3, g["expected"]["x_after_block"], rtol=0, atol=1e-9)
+    np.testing.assert_allclose(v, g["expected"]["v"], rtol=0, atol=1e-9)
+    kd = np.asarray(g["expected"]["k_direction"], np.float64)
+    np.testing.assert_allclose(k, kd / np.sqrt((kd ** 2).mean()), rtol=0, atol=1e-9)   # RMS-normed, frame 0
+    # the cross-attention and feed-forward branches off: what the self-attention branch leaves
+    zero_ca = lambda qc: np.zeros_like(qc)
+    m = np.asarray(g["modulation"], np.float64).copy()
+    m[5] = 0.0
+    x1, _ = D.dit_block(p["blocks"][0], Cfg, np.asarray(g["lat"], np.float64), m, D.token_positions(1, 0, 1, 1),
+                        lambda q, k_, v_: D.heads_attention(q, k_, v_, 1), zero_ca)
+    np.testing.assert_allclose(x1, g["expected"]["x_after_self_attention"], rtol=0, atol=1e-9)
+
+
+def test_dit_step_hand_worked():
+    # the whole step: timestep projection added to the block table, the block, the head
+    g, Cfg, p, tk, tv = _golden_block()
+    lat, kv = _run_golden(p, Cfg, g, tk, tv)
+    np.testing.assert_allclose(lat, g["expected"]["lat_next"], rtol=0, atol=1e-9)
+    np.testing.assert_allclose(kv[0][1], g["expected"]["v"], rtol=0, atol=1e-9)
+
+
+@pytest.mark.parametrize("swap", [(0, 1), (3, 4), (2, 5), (0, 3), (1, 4)])
+def test_dit_block_golden_tells_modulation_rows_apart(swap):
+    # each plausible misreading of the six modulation rows (shift <-> scale, the gates of
+    # the two branches, the two branches' shifts or scales) moves the hand-worked result
+    g, Cfg, p, tk, tv = _golden_block()
+    m = np.asarray(g["modulation"], np.float64).copy()
+    a, b = swap
+    m[[a, b]] = m[[b, a]]
+    x3, _ = _block_only(p, Cfg, g, tk, tv, m)
+    assert np.abs(x3 - np.asarray(g["expected"]["x_after_block"])).max() > 0.1
+
+
+def test_dit_block_golden_catches_planted_mistakes(monkeypatch):
+    g, Cfg, p, tk, tv = _golden_block()
+    want = np.asarray(g["expected"]["x_after_block"])
+    run = lambda: _block_only(p, Cfg, g, tk, tv, g["modulation"])[0]
+    ln = D.layer_norm
+    # (1) the cross-attention's layer norm without its affine map
+    monkeypatch.setattr(D, "layer_norm", lambda x, eps, weight=None, bias=None: ln(x, eps))
+    assert np.abs(run() - want).max() > 0.5
+    monkeypatch.setattr(D, "layer_norm", ln)
+    # (2) adaLN with shift and scale exchanged inside the modulation
+    mod = D.modulate
+    monkeypatch.setattr(D, "modulate", lambda y, shift, scale: mod(y, scale, shift))
+    assert np.abs(run() - want).max() > 0.5
+    monkeypatch.setattr(D, "modulate", mod)
+    # (3) the feed-forward's activation left out
+    gelu = D.ACTS[1]
+    monkeypatch.setitem(D.ACTS, 1, lambda v: v)
+    assert np.abs(run() - want).max() > 0.5
+    monkeypatch.setitem(D.ACTS, 1, gelu)
+    # (4) a gate on the cross-attention branch (the self-attention's)
+    gemm = D.gemm
+    co_w = p["blocks"][0]["co_w"]
+
+    def gated_cross(A, W, bias=None, act=0, R=None, gate=None):
+        if W is co_w:      # the cross-attention's output map, given the self-attention's gate
+            gate = np.asarray(g["modulation"][2], np.float64)
+        return gemm(A, W, bias, act, R, gate)
+
+    monkeypatch.setattr(D, "gemm", gated_cross)
+    assert np.abs(run() - want).max() > 0.5
+    monkeypatch.setattr(D, "gemm", gemm)
+    np.testing.assert_allclose(run(), want, rtol=0, atol=1e-9)
+
+
+# ----------------------------------------------------------------------------------
+# FAST-AR attention inside the DiT oracle
+# ----------------------------------------------------------------------------------
+
+def test_dit_fastar_textbook_reduction_equals_dense():
+    # one bucket, r = 1, tau > 1 (nothing evicted), tau_ca = -1 (every text token kept),
+    # M large enough for every chunk: each block's FAST-AR attention is dense attention
+    # over its whole history, so the step equals the dense step chunk after chunk
+    rng = np.random.default_rng(31)
+    p = _params(rng, zero_blocks=False)
+    for b in p["blocks"]:
+        b["mod"][2] += 1.0
+    H, d, frames = 2, 8, 2
+    cent = [np.ones((H, 1, d)) / np.sqrt(d) for _ in p["blocks"]]
+    fa = D.FastARAttention(cent, F=frames, Tf=3, M=64, r=1, tau=2.0, tau_ca=-1.0, topk=16)
+    tkv = [(rng.standard_normal((5, 16)), rng.standard_normal((5, 16))) for _ in p["blocks"]]
+    hist = [(np.zeros((0, 16)), np.zeros((0, 16))) for _ in p["blocks"]]
+    for chunk in range(3):
+        lat = rng.standard_normal((6, 4))
+        want, kv = D.dit_step(p, _Cfg, lat, 0.5, 0.25, chunk * frames, hist, tkv)
+        got, caches = D.dit_step(p, _Cfg, lat, 0.5, 0.25, chunk * frames, None, tkv, fastar=fa)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+        fa.caches = caches
+        hist = [(np.concatenate([hk, k]), np.concatenate([hv, v])) for (hk, hv), (k, v) in zip(hist, kv)]
+        for i, (k, v) in enumerate(hist):
+            for h in range(H):
+                np.testing.assert_allclose(caches[i][h][0], k[:, h * d:(h + 1) * d], atol=1e-15)
+
+
+def test_dit_fastar_restricts_and_bounds():
+    # with real buckets and a cap the FAST-AR step differs from the dense one, keeps at
+    # most M entries per head, and a replayed decision set reproduces its own result
+    rng = np.random.default_rng(32)
+    p = _params(rng, zero_blocks=False)
+    H, d, B = 2, 8, 4
+    cent = []
+    for _ in p["blocks"]:
+        c = rng.standard_normal((H, B, d))
+        cent.append(c / np.linalg.norm(c, axis=2, keepdims=True))
+    tkv = [(rng.standard_normal((20, 16)), rng.standard_normal((20, 16))) for _ in p["blocks"]]
+    fa = D.FastARAttention(cent, F=2, Tf=3, M=8, r=2, tau=0.3, tau_ca=0.5, topk=2)
+    lat = rng.standard_normal((6, 4))
+    for chunk in range(3):
+        out, caches = D.dit_step(p, _Cfg, lat, 0.5, 0.25, chunk * 2, None, tkv, fastar=fa)
+        fa.caches = caches
+        assert all(c[0].shape[0] <= 8 for blk in caches for c in blk)
+    dense, _ = D.dit_step(p, _Cfg, lat, 0.5, 0.25, 6, [(np.zeros((0, 16)), np.zeros((0, 16)))] * 2, tkv)
+    fast, _ = D.dit_step(p, _Cfg, lat, 0.5, 0.25, 6, None, tkv, fastar=fa)
+    assert np.abs(fast - dense).max() > 1e-3
