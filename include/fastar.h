@@ -44,6 +44,10 @@
  *     offending element is skipped.  No kernel traps or asserts, and none
  *     waits on a block outside its own thread-block cluster (whose blocks the
  *     hardware schedules together).
+ *   - Devices: a call works on the device current on the calling thread.  Per-device
+ *     set-up (kernel shared-memory opt-ins, the no-allocation entry's scratch address)
+ *     is done on the first call on each device and kept for the life of the process;
+ *     do not call the library on a device after cudaDeviceReset.
  *   - Ties of every arg-max / top-k decision go to the lowest index.
  *   - The softmax scale of every attention call must be positive and finite
  *     (FASTAR_EINVAL otherwise).
@@ -363,6 +367,11 @@ int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, in
  * (query, slot) pairs of qb grouped by bucket, as fastar_bucket_sort writes them;
  * with them the gated scoring reads each bucket's queries directly instead of
  * scanning qb (same results either way).
+ * Failure: a (head, frame) whose scores could not all be formed (a bounded wait of the
+ * tensor-core scorer timed out, which a working device never does) or hold a NaN (NaN
+ * inputs) is not ranked: kcnt = -1, keep 0 and kidx -1 throughout, score NaN.
+ * fastar_cross_attn_subset reports such a kcnt as FASTAR_DEV_BAD_INDEX in its status
+ * word and attends to no prompt token for that frame.
  * Workspace: fastar_workspace_bytes(FASTAR_OP_ANNCA, H, ..., P, F).  P <= FASTAR_MAX_P. */
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                         int64_t q_head_stride, int64_t q_token_stride,
@@ -382,9 +391,13 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
  * library's device image (FASTAR_NOALLOC_MAX_SCORES floats, 1 MiB, held on every
  * GPU that loads the library until the process exits).  H * F * P above that
  * limit returns FASTAR_ECAPACITY.  The first call on a device (with that device
- * current) looks up the array's address; make it before any stream capture.
+ * current) looks up the array's address; make it before any stream capture.  The
+ * address, like every other per-device set-up of the library, lasts for the process:
+ * after a cudaDeviceReset the library is not to be called on that device again.
  * All calls share the array: calls that may overlap on the GPU race and must be
- * ordered by the caller.  Calls no allocation routine of any kind. */
+ * ordered by the caller.  A call never reads scores that it did not write itself,
+ * so a smaller call after a larger one needs no clearing.  The failure rule of 6
+ * applies (kcnt = -1).  Calls no allocation routine of any kind. */
 #define FASTAR_NOALLOC_MAX_SCORES 262144
 int fastar_annca_select_noalloc(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                                 int64_t q_head_stride, int64_t q_token_stride,

@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -133,6 +134,7 @@ annca_score_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int64
 
 // One CTA per (head, frame): rank = #{p' : (s', p') precedes (s, p)} in the order
 // (score desc, index asc), -inf last; keep = s >= tau_ca or rank < min(topk, P).
+// A (head, frame) holding a NaN score is not ranked: kcnt = -1, no token kept.
 __global__ void __launch_bounds__(1024)
 annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restrict__ score,
                   uint8_t* __restrict__ keep, int32_t* __restrict__ kidx, int32_t* __restrict__ kcnt) {
@@ -141,8 +143,23 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
   const int hf = blockIdx.x;
   const int p = threadIdx.x;
   const float* sc = score + (int64_t)hf * P;
-  if (p < P) s[p] = sc[p];
+  __shared__ int bad;
+  if (p == 0) bad = 0;
   __syncthreads();
+  if (p < P) {
+    s[p] = sc[p];
+    if (s[p] != s[p]) bad = 1;   // a NaN score: the scorer timed out, or an input held a NaN
+  }
+  __syncthreads();
+  if (bad) {
+    // the (head, frame) cannot be ranked: no kept token, kcnt = -1 marks it
+    if (p < P) {
+      keep[(int64_t)hf * P + p] = 0;
+      kidx[(int64_t)hf * P + p] = -1;
+    }
+    if (p == 0) kcnt[hf] = -1;
+    return;
+  }
   int k = 0;
   if (p < P) {
     const float mine = s[p];
@@ -366,8 +383,8 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
     // prompt tokens whose bucket no CTA visits would keep stale scores: the bucket
     // kernel covers every p (each has exactly one bucket, and every bucket has a CTA)
     const size_t bsmem = annca_bucket_smem<D>((int64_t)F * tpf);
-    static const cudaError_t battr = cudaFuncSetAttribute(
-        annca_bucket_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)annca_bucket_smem<D>(kBMaxQ));
+    const cudaError_t battr =
+        opt_in_smem((const void*)annca_bucket_kernel<T, D>, (int)annca_bucket_smem<D>(kBMaxQ));
     if (battr != cudaSuccess) return battr;
     const unsigned nb = bo.B > 0 ? (unsigned)bo.B : (unsigned)FASTAR_MAX_B;
     annca_bucket_kernel<T, D><<<dim3(nb, H), 256, bsmem, s>>>(
@@ -378,7 +395,7 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
   const size_t smem = sizeof(float) * ((size_t)D * kCQ + (size_t)D * kCP + kCQ + kCP + 16 * kCP) +
                       sizeof(int) * ((size_t)kCQ * FASTAR_MAX_R + kCP);
   auto kern = annca_score_kernel<T, D>;
-  static const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t attr = opt_in_smem((const void*)kern, (int)smem);
   if (attr != cudaSuccess) return attr;
   kern<<<dim3((unsigned)((P + kCP - 1) / kCP), H, F), 256, smem, s>>>(
       static_cast<const T*>(q.p), q.hs, q.ts, F, tpf, qb, r, static_cast<const T*>(kp), pb, P, gate, score);

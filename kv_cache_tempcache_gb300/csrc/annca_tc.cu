@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         w |= ((uint32_t)b & 0xffu) << (8 * sl);
       }
     };
+    int u_fail = units;   // the first unit left unscored after a timed-out wait
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int pt = u % g.PT, f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
       const int64_t p = (int64_t)pt * 128 + row;
@@ -246,7 +247,10 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.a_empty);
       }
-      if (!tc::named_bar_and(1, kCaEpW * 32, got)) break;
+      if (!tc::named_bar_and(1, kCaEpW * 32, got)) {
+        u_fail = u;
+        break;
+      }
       const uint32_t pb4 = mypb >= 0 ? (uint32_t)mypb * 0x01010101u : 0u;
       float best = neg_inf();
       bool ok = true;
@@ -300,7 +304,10 @@ __global__ void __launch_bounds__(kCaThreads, 1)
           tph ^= 1;
         }
       }
-      if (!ok) break;
+      if (!ok) {
+        u_fail = u;
+        break;
+      }
       // combine the two column halves of each row
       if (half == 1) sm.bx[row] = best;
       tc::named_bar(1, kCaEpW * 32);
@@ -310,6 +317,14 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       }
       tc::named_bar(1, kCaEpW * 32);
     }
+    // After a timed-out wait every score row this CTA still owed is written as NaN, so
+    // that the ranking sees the failure instead of an earlier call's values.
+    if (half == 0)
+      for (int u = u_fail; u < units; u += gridDim.x) {
+        const int pt = u % g.PT, f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
+        const int64_t p = (int64_t)pt * 128 + row;
+        if (p < g.P) score[((int64_t)h * g.F + f) * g.P + p] = __uint_as_float(0x7fc00000u);
+      }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -350,8 +365,7 @@ bool launch_annca_tc_impl(TokView q, int H, int F, int64_t tpf, const int32_t* q
   const int units = H * F * g.PT;
   const int grid = units < sm_count() ? units : sm_count();
   constexpr size_t smem = sizeof(CaSmem<D>) + 1024;
-  static const cudaError_t a =
-      cudaFuncSetAttribute(annca_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t a = opt_in_smem((const void*)annca_tc_kernel<D>, (int)smem);
   if (a != cudaSuccess) return false;
   annca_tc_kernel<D><<<grid, kCaThreads, smem, s>>>(tq, tp, qb, pb, g, score, status);
   count_launches(1);

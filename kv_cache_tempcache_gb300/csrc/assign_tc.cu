@@ -197,9 +197,9 @@ bool assign_tc_impl(TokView x, int H, int64_t n, const void* cent, int B, int r,
   while ((int)tcols < NP) tcols <<= 1;
   const size_t smem = assign_tc_smem<D>(NP);
   const int smax = (int)assign_tc_smem<D>(256);
-  static const cudaError_t a1 = cudaFuncSetAttribute(assign_tc_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-  static const cudaError_t a2 = cudaFuncSetAttribute(assign_tc_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-  static const cudaError_t a0 = cudaFuncSetAttribute(assign_tc_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+  const cudaError_t a1 = opt_in_smem((const void*)assign_tc_kernel<D, 1>, smax);
+  const cudaError_t a2 = opt_in_smem((const void*)assign_tc_kernel<D, 2>, smax);
+  const cudaError_t a0 = opt_in_smem((const void*)assign_tc_kernel<D, 0>, smax);
   if (a1 != cudaSuccess || a2 != cudaSuccess || a0 != cudaSuccess) return false;
   const dim3 grid((unsigned)((n + kRows - 1) / kRows), H);
   const int tm = token_major ? 1 : 0;

@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -321,7 +322,7 @@ template <typename T, int D>
 static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
   constexpr size_t smem = attn_simt_smem<D>();
   auto kern = attn_simt_kernel<T, D>;
-  static const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t attr = opt_in_smem((const void*)kern, (int)smem);
   if (attr != cudaSuccess) return attr;
   cudaError_t e;
   dim3 grid;

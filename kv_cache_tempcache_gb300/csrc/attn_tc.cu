@@ -1235,8 +1235,7 @@ template <int D, bool kGrouped, int kMode>
 bool attn_launch(int grid, cudaStream_t s, const AttnArgs& b, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& tq) {
   constexpr size_t smem = AttnLayout<D>::bytes;
-  static const cudaError_t attr = cudaFuncSetAttribute(attn_tc_kernel<D, kGrouped, kMode>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t attr = opt_in_smem((const void*)attn_tc_kernel<D, kGrouped, kMode>, (int)smem);
   if (attr != cudaSuccess) return false;
   attn_tc_kernel<D, kGrouped, kMode><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
   count_launches(1);

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -89,10 +90,9 @@ static cudaError_t assign_impl(TokView x, int H, int64_t n, const void* cent, in
   const int Bp = (B + 31) & ~31;
   const size_t smem = sizeof(float) * ((size_t)D * Bp + (size_t)kAssignWarps * D);
   auto kern = bucket_assign_kernel<T, D>;
-  // opt in once to the largest footprint (B = FASTAR_MAX_B); no per-launch attribute calls
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)(sizeof(float) * ((size_t)D * FASTAR_MAX_B + (size_t)kAssignWarps * D)));
+  // opt in to the largest footprint (B = FASTAR_MAX_B), once per device
+  const cudaError_t attr = opt_in_smem(
+      (const void*)kern, (int)(sizeof(float) * ((size_t)D * FASTAR_MAX_B + (size_t)kAssignWarps * D)));
   if (attr != cudaSuccess) return attr;
   int64_t gx = (n + kAssignWarps - 1) / kAssignWarps;
   const int64_t cap = (4 * 152 + H - 1) / H;

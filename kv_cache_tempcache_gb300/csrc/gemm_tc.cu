@@ -295,8 +295,7 @@ template <int kBN, int kAct, bool kRes>
 static cudaError_t gemm_launch(const void* A, int64_t lda, const void* W, int64_t ldw, const GemmArgs& g,
                                cudaStream_t s) {
   constexpr size_t smem = sizeof(GemmSmem<kBN>) + 1024;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(gemm_tc_kernel<kBN, kAct, kRes>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t attr = opt_in_smem((const void*)gemm_tc_kernel<kBN, kAct, kRes>, (int)smem);
   if (attr != cudaSuccess) return attr;
   CUtensorMap ta, tw;
   if (!make_tmap_bf16_3d(&ta, A, (uint64_t)g.K, (uint64_t)g.M, 1, (uint64_t)lda * 2, 0, kBK, kBM) ||

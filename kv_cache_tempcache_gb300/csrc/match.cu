@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -309,7 +310,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   chunk = (chunk + kNT - 1) / kNT * kNT;
   const size_t smem = sizeof(float) * ((size_t)D * kMT + (size_t)D * kNT + kNT);
   auto k1 = match_simt_kernel<T, D>;
-  static const cudaError_t attr = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t attr = opt_in_smem((const void*)k1, (int)smem);
   if (attr != cudaSuccess) return attr;
   cudaError_t e;
   const unsigned gx = (unsigned)((nq + kMT - 1) / kMT);

@@ -467,13 +467,11 @@ static int launch_match_tc_impl(TokView q, int H, int64_t nq, const void* ck, co
   const int grid = units < sm_count() ? units : sm_count();
   constexpr size_t smem = match_tc_smem<D>();
   if (top2) {
-    static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, true>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t a = opt_in_smem((const void*)match_tc_kernel<D, true>, (int)smem);
     if (a != cudaSuccess) return -1;
     match_tc_kernel<D, true><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, owner, status);
   } else {
-    static const cudaError_t a = cudaFuncSetAttribute(match_tc_kernel<D, false>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t a = opt_in_smem((const void*)match_tc_kernel<D, false>, (int)smem);
     if (a != cudaSuccess) return -1;
     match_tc_kernel<D, false><<<grid, kThreads, smem, s>>>(tq, tk, cknorm, clen, g, part, evict, owner, status);
   }

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -208,7 +209,7 @@ cudaError_t encode_impl(TokView x, int H, int64_t n, int m, int Kc, const void* 
       sizeof(float) * ((size_t)m * Kc * DS + (size_t)kEncKeys * (m * DS + 4)) + (size_t)kEncKeys * m;
   auto kern = pq_encode_kernel<T, DS>;
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = opt_in_smem((const void*)kern, (int)smem);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)((n + kEncKeys - 1) / kEncKeys), (unsigned)H);
@@ -243,14 +244,12 @@ cudaError_t launch_pq_decode(int d, int H, int64_t M, int m, int Kc, const uint8
   cudaError_t e;
   if (d / m == 4) {
     if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(pq_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
+        (e = opt_in_smem((const void*)pq_decode_kernel<4>, (int)smem)) != cudaSuccess)
       return e;
     pq_decode_kernel<4><<<blocks, 256, smem, s>>>(H, M, m, Kc, codes, clen, c, k, khat_norm, status);
   } else {
     if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(pq_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
+        (e = opt_in_smem((const void*)pq_decode_kernel<8>, (int)smem)) != cudaSuccess)
       return e;
     pq_decode_kernel<8><<<blocks, 256, smem, s>>>(H, M, m, Kc, codes, clen, c, k, khat_norm, status);
   }

@@ -3,6 +3,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "tmap.h"
 
 namespace fastar {
@@ -39,14 +42,40 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kMaxOptIns = 512;
+std::mutex g_dev_mutex;
+std::atomic<int> g_sms[kMaxDevices];
+struct OptIn {
+  const void* func;
+  int dev, bytes;
+};
+OptIn g_opt_in[kMaxOptIns];   // a fixed table: set-up allocates nothing, not even on the host
+int g_n_opt_in = 0;
+}  // namespace
+
 int sm_count() {
-  static int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 148;
-    return v;
-  }();
-  return n;
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  const int cached = g_sms[dev].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 148;
+  g_sms[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+cudaError_t opt_in_smem(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  for (int i = 0; i < g_n_opt_in; ++i)
+    if (g_opt_in[i].func == func && g_opt_in[i].dev == dev && g_opt_in[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (g_n_opt_in < kMaxOptIns) g_opt_in[g_n_opt_in++] = OptIn{func, dev, bytes};   // else: set again next time
+  return cudaSuccess;
 }
 
 }  // namespace fastar

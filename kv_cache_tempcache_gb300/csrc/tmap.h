@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace fastar {
@@ -13,7 +14,12 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                        uint32_t box2 = 1);
 
-// Streaming multiprocessors of the current device (cached).
+// Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+
+// Opts kernel `func` into `bytes` of dynamic shared memory on the current device.  The
+// attribute belongs to the device's context, so it is set once per (kernel, device)
+// and remembered; returns the CUDA error of the first failed attempt.
+cudaError_t opt_in_smem(const void* func, int bytes);
 
 }  // namespace fastar

@@ -191,9 +191,12 @@ class DiT:
             a.set_prompt(self._heads(k).contiguous(), self._heads(v).contiguous())
 
     # ---- the denoising step ------------------------------------------------------------------
-    def _enqueue_step(self, advance: bool):
+    def _enqueue_step(self, advance: bool, probe=None):
         """One denoising step of the current chunk (reads self.t_dev, self.dt_vec and the
-        latent; updates the latent in place)."""
+        latent; updates the latent in place).  probe (eager steps only): called as
+        probe("self", i, layer, q, k, v, out) after block i's self-attention and
+        probe("cross", i, layer, qc, out) after its cross-attention, with [H, N, d] views
+        of the block's attention inputs and output, for inspection between kernels."""
         cfg, D, N = self.cfg, self.cfg.dim, self.cfg.tokens
         st = self.status
         # timestep embedding -> e (head) and the blocks' modulation e0
@@ -207,7 +210,7 @@ class DiT:
         L.fastar_gemm(self.lat, self.patch_w, self.x, bias=self.patch_b, dev_status=st)
         q, k, v = (self._heads(self.qkv[:, i * D:(i + 1) * D]) for i in range(3))
         o = self._heads(self.o)
-        for b, a in zip(self.blocks, self.attn):
+        for i, (b, a) in enumerate(zip(self.blocks, self.attn)):
             L.fastar_layernorm_mod(self.x, self.h, eps=cfg.eps, shift_a=b.mod[0], shift_b=e0[0], scale_a=b.mod[1],
                                    scale_b=e0[1])
             L.fastar_gemm(self.h, b.qkv_w, self.qkv, bias=b.qkv_b, dev_status=st)
@@ -216,11 +219,15 @@ class DiT:
             L.fastar_rmsnorm_rope(self.qkv[:, D:2 * D], cfg.d, weight=b.norm_k, rope=True, t0_dev=self.frame_dev,
                                   grid=(cfg.grid_h, cfg.grid_w), eps=cfg.eps, theta=cfg.theta)
             a.step_self(q, k, v, out=o, advance=advance)
+            if probe is not None:
+                probe("self", i, a, q, k, v, o)
             L.fastar_gemm(self.o, b.o_w, self.x, bias=b.o_b, R=self.x, gate_a=b.mod[2], gate_b=e0[2], dev_status=st)
             L.fastar_layernorm_mod(self.x, self.h, eps=cfg.eps, weight=b.norm3_w, bias=b.norm3_b)
             L.fastar_gemm(self.h, b.cq_w, self.qc, bias=b.cq_b, dev_status=st)
             L.fastar_rmsnorm_rope(self.qc, cfg.d, weight=b.norm_cq, eps=cfg.eps)
             a.step_cross(self._heads(self.qc), out=o)
+            if probe is not None:
+                probe("cross", i, a, self._heads(self.qc), o)
             L.fastar_gemm(self.o, b.co_w, self.x, bias=b.co_b, R=self.x, dev_status=st)
             L.fastar_layernorm_mod(self.x, self.h, eps=cfg.eps, shift_a=b.mod[3], shift_b=e0[3], scale_a=b.mod[4],
                                    scale_b=e0[4])
@@ -282,10 +289,13 @@ class DiT:
         self._graphs[key] = gr
         return gr
 
-    def denoise_chunk(self, noise: torch.Tensor, use_graph: bool = True, timer=None):
+    def denoise_chunk(self, noise: torch.Tensor, use_graph: bool = True, timer=None, probe=None):
         """Denoises one chunk from noise (patch-token layout [tokens, 64]) in cfg.steps
-        Euler steps, commits its keys and values to the caches, and returns the latent."""
+        Euler steps, commits its keys and values to the caches, and returns the latent.
+        probe: see _enqueue_step (eager steps only)."""
         cfg = self.cfg
+        if probe is not None and use_graph:
+            raise ValueError("a probe needs eager steps (use_graph=False)")
         self.lat.zero_()
         self.lat[:, :cfg.patch_ch].copy_(noise)
         ts = timesteps(cfg.steps)
@@ -297,7 +307,7 @@ class DiT:
             if gr is not None:
                 gr.replay()
             else:
-                self._enqueue_step(advance=False)
+                self._enqueue_step(advance=False, probe=probe)
             if timer:
                 timer("end")
         self._commit()

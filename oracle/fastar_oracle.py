@@ -4,8 +4,10 @@ Only the tests, the package's smoke check and the benchmark's CPU-baseline arm m
 import or run this module.  It shares no code with the CUDA path and imports nothing
 from it; the product path never calls it.
 
-Everything is computed in float64 NumPy, one head at a time, straight from the
-definitions.  Source: "Fast Autoregressive Video Diffusion and World Models with
+Everything is computed in float64 NumPy (FLOAT), one head at a time, straight from
+the definitions.  The benchmark's CPU-baseline leg may set FLOAT to float32, the
+precision the method spec names for a CPU baseline, to time the same code in fp32;
+the parity tests always run it in float64.  Source: "Fast Autoregressive Video Diffusion and World Models with
 Temporal Cache Compression and Sparse Attention" (FAST-AR), as described on the
 pages about it:
   * TempCache (technical summary §2.A; blog §1): for each current-frame query, the
@@ -42,8 +44,12 @@ class CapacityError(ValueError):
     """The cache cap M cannot hold one chunk (M < Nq)."""
 
 
+# The floating-point type every array of the oracle is computed in (see the header).
+FLOAT = np.float64
+
+
 def _f64(x) -> np.ndarray:
-    return np.asarray(x, dtype=np.float64)
+    return np.asarray(x, dtype=FLOAT)
 
 
 # ----------------------------------------------------------------------------------
@@ -142,7 +148,7 @@ def tempcache_match(Q, K_cache):
     K = _f64(K_cache)
     nq, n = Q.shape[0], K.shape[0]
     if n == 0:
-        return (np.full(nq, -1, np.int64), np.full(nq, NEG_INF), np.full(nq, NEG_INF))
+        return (np.full(nq, -1, np.int64), np.full(nq, NEG_INF, FLOAT), np.full(nq, NEG_INF, FLOAT))
     S = cosine_matrix(Q, K)
     top1 = np.argmax(S, axis=1).astype(np.int64)       # first maximum = lowest j
     rows = np.arange(nq)
@@ -151,7 +157,7 @@ def tempcache_match(Q, K_cache):
         S[rows, top1] = NEG_INF
         s2 = S.max(axis=1)
     else:
-        s2 = np.full(nq, NEG_INF)
+        s2 = np.full(nq, NEG_INF, FLOAT)
     return top1, s1, s2
 
 
@@ -173,7 +179,7 @@ def tempcache_match_ann(Q, R, K_cache, kb_cache):
     kb = np.asarray(kb_cache, np.int64)
     nq, n = Q.shape[0], K.shape[0]
     top1 = np.full(nq, -1, np.int64)
-    s1 = np.full(nq, NEG_INF)
+    s1 = np.full(nq, NEG_INF, FLOAT)
     if n == 0:
         return top1, s1
     S = cosine_matrix(Q, K)
@@ -202,7 +208,7 @@ def pq_distances(X, codebooks) -> np.ndarray:
     X = _f64(X)
     Cb = _f64(codebooks)
     m, Kc, ds = Cb.shape
-    dist = np.zeros((X.shape[0], m, Kc))
+    dist = np.zeros((X.shape[0], m, Kc), FLOAT)
     for s in range(m):
         sub = X[:, s * ds:(s + 1) * ds]
         dist[:, s, :] = ((sub[:, None, :] - Cb[s][None, :, :]) ** 2).sum(axis=2)
@@ -224,7 +230,7 @@ def pq_decode(codes, codebooks) -> np.ndarray:
     codes = np.asarray(codes, np.int64)
     m = Cb.shape[0]
     if codes.shape[0] == 0:
-        return np.zeros((0, m * Cb.shape[2]))
+        return np.zeros((0, m * Cb.shape[2]), FLOAT)
     return np.concatenate([Cb[s][codes[:, s]] for s in range(m)], axis=1)
 
 
@@ -246,7 +252,7 @@ def evict_flags(top1, K_cur, K_cache, tau: float):
     top1 = np.asarray(top1, np.int64)
     n = np.asarray(K_cache).shape[0]
     e = np.zeros(n, bool)
-    ce = np.full(top1.shape[0], NEG_INF)
+    ce = np.full(top1.shape[0], NEG_INF, FLOAT)
     ok = top1 >= 0
     if ok.any():
         ce[ok] = cosine_rows(np.asarray(K_cur)[ok], np.asarray(K_cache)[top1[ok]])
@@ -361,8 +367,8 @@ def masked_softmax_attention(Q, K, V, allowed, scale: float, log_g=None):
     K = _f64(K)
     V = _f64(V)
     nq, nk = Q.shape[0], K.shape[0]
-    O = np.zeros((nq, V.shape[1]))
-    lse = np.full(nq, NEG_INF)
+    O = np.zeros((nq, V.shape[1]), FLOAT)
+    lse = np.full(nq, NEG_INF, FLOAT)
     if nk == 0 or nq == 0:
         return O, lse
     step = max(1, (1 << 24) // max(nk, 1))           # row blocks bound the memory
@@ -387,7 +393,7 @@ def masked_softmax_attention(Q, K, V, allowed, scale: float, log_g=None):
 def group_log(g) -> np.ndarray:
     """ln g per entry of the merge variant (-inf for g = 0: an empty group)."""
     g = _f64(g)
-    out = np.full(g.shape, NEG_INF)
+    out = np.full(g.shape, NEG_INF, FLOAT)
     np.log(g, out=out, where=g > 0)
     return out
 
@@ -425,7 +431,7 @@ def annca_select(Q, R, Kp, pb, F: int, Tf: int, tau_ca: float, topk: int, gate: 
     P = Kp.shape[0]
     R = np.asarray(R, np.int64)
     pb = np.asarray(pb, np.int64)
-    score = np.full((F, P), NEG_INF)
+    score = np.full((F, P), NEG_INF, FLOAT)
     keep = np.zeros((F, P), bool)
     kidx, kcnt = [], np.zeros(F, np.int64)
     for f in range(F):
@@ -449,8 +455,8 @@ def annca_select(Q, R, Kp, pb, F: int, Tf: int, tau_ca: float, topk: int, gate: 
 def cross_attention_subset(Q, Kp, Vp, kidx, F: int, Tf: int, scale: float):
     """Cross-attention of each frame's queries over its kept prompt tokens only."""
     Q = _f64(Q)
-    O = np.zeros((Q.shape[0], np.asarray(Vp).shape[1]))
-    lse = np.full(Q.shape[0], NEG_INF)
+    O = np.zeros((Q.shape[0], np.asarray(Vp).shape[1]), FLOAT)
+    lse = np.full(Q.shape[0], NEG_INF, FLOAT)
     for f in range(F):
         idx = np.asarray(kidx[f], np.int64)
         o, l = masked_softmax_attention(Q[f * Tf:(f + 1) * Tf], _f64(Kp)[idx], _f64(Vp)[idx], None, scale)

@@ -13,6 +13,18 @@ import numpy as np
 
 MARGIN = 1e-4
 
+# Near-tie and ambiguous-decision counts reported by the parity tests: each entry is
+# (what was checked, {kind: count}).  conftest.py prints them at the end of the run.
+REPORTS = []
+
+
+def report(what: str, counts) -> None:
+    """Records the number of decisions that differed from the oracle's own choice but were
+    accepted as correct (near-ties under the margin), and any other counts of interest."""
+    if hasattr(counts, "__dataclass_fields__"):
+        counts = {k: getattr(counts, k) for k in counts.__dataclass_fields__}
+    REPORTS.append((what, dict(counts)))
+
 
 def _tol(x):
     return MARGIN * np.maximum(np.abs(x), 0.0)

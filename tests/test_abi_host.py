@@ -185,3 +185,21 @@ def test_binding_signatures_match_the_header():
         got = _lib._SIGS[name]
         want = [ctypes.c_void_p if "*" in p else kind[p.replace("const ", "").strip()] for p in params]
         assert got == want, f"{name}: binding {[t.__name__ for t in got]} vs header {params}"
+
+
+def test_library_sources_call_no_allocator():
+    # the library never allocates or frees device (or pinned host) memory: the caller owns
+    # every buffer, and the allocation-free entry point relies on that for its whole path
+    import os
+    import re
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "kv_cache_tempcache_gb300", "csrc")
+    pat = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cudaHostAlloc|cudaMallocHost|cuMemAlloc\w*|cuMemCreate|"
+                     r"cudaMemPoolCreate|malloc|calloc|realloc|new\s+\w)")
+    hits = []
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            for n, line in enumerate(open(os.path.join(csrc, f)), 1):
+                code = line.split("//")[0]
+                if pat.search(code):
+                    hits.append(f"{f}:{n}: {line.strip()}")
+    assert not hits, "allocation calls in the library:\n" + "\n".join(hits)

@@ -26,6 +26,7 @@ def _run(cfg, seed=0, gate=True, q_layout="HND", cache=None):
 def test_tiny_fp32_step(seed):
     _, g, counts = _run(synth.TINY_FP32, seed)
     assert g["evict"].sum() > 0, "the tiny workload should evict"
+    parity.report(f"tiny_fp32 layer step, seed {seed}", counts)
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -34,6 +35,7 @@ def test_small_bf16_step(seed):
     _, g, counts = _run(cfg, seed)
     assert g["evict"].sum() > 0
     assert (g["len_out"] == cfg.M).all()
+    parity.report(f"small_bf16 layer step, seed {seed}", counts)
 
 
 @pytest.mark.parametrize("r", [3, 4])
