@@ -44,6 +44,9 @@ def parse_args():
     p.add_argument("--no-rollout", action="store_true", help="skip the long-rollout stability run")
     p.add_argument("--no-dit", action="store_true", help="skip the whole-transformer (DiT) chunk denoise run")
     p.add_argument("--dit-chunks", type=int, default=20, help="chunks of the DiT rollout (3 latent frames each)")
+    p.add_argument("--no-configs", action="store_true", help="skip the other layer shapes (HunyuanVideo 720p, tiny)")
+    p.add_argument("--cpu-sample", nargs=4, metavar=("CONFIG", "FLOAT", "HEADS", "SEED"), default=None,
+                   help=argparse.SUPPRESS)   # internal: one timed oracle sample (run in a child process)
     return p.parse_args()
 
 
@@ -182,12 +185,13 @@ def load_peaks():
 def stage_units(cfg, layer, n_in):
     """Algorithmic bytes and flops of each stage for the measured step (bf16 = 2 B).
 
-    n_in: per-head cache length entering the step.  Counts follow the definitions:
-    every operand read once, every result written once, flops of the contractions
-    the method defines (2 per multiply-add); the sparse attention counts
-    4*d*sum_b |Q_b||K_b| from the step's own bucket histograms."""
+    n_in: per-head cache length entering the step.  Bytes are the method minimum: each
+    operand a stage needs is read once and each result written once; implementation
+    overheads (moving surviving cache rows, the slots' partial results) are not counted.
+    Flops are the contractions the method defines (2 per multiply-add); the sparse
+    attention counts 4*d*sum_b |Q_b||K_b| from the step's own bucket histograms."""
     import numpy as np
-    H, d, Nq, B, r, P, F, Tf = cfg.H, cfg.d, cfg.Nq, cfg.B, cfg.r, cfg.P, cfg.F, cfg.Tf
+    H, d, Nq, B, r, P, F, Tf, M = cfg.H, cfg.d, cfg.Nq, cfg.B, cfg.r, cfg.P, cfg.F, cfg.Tf, cfg.M
     e = 2 if cfg.dtype == "bf16" else 4
     row = d * e
     qoff = layer.qoff.cpu().numpy().astype(np.int64)
@@ -200,7 +204,8 @@ def stage_units(cfg, layer, n_in):
     u = {}
     u["bucket_assign"] = dict(bytes=2 * H * Nq * row + 2 * H * B * row, flops=2.0 * 2 * H * Nq * B * d)
     u["tempcache_match"] = dict(bytes=H * Nq * row * 2 + n_tot * (row + 4), flops=2.0 * Nq * d * n_tot)
-    u["cache_compact"] = dict(bytes=2 * 2 * float(L_out.sum()) * row, flops=0.0)
+    # the chunk's K/V read and appended to the cache, the index map written
+    u["cache_compact"] = dict(bytes=4.0 * H * Nq * row + 4.0 * H * M, flops=0.0)
     u["bucket_sort"] = dict(bytes=4.0 * float(L_out.sum()) * 2, flops=0.0)
     u["bucket_sort_q"] = dict(bytes=4.0 * H * Nq * r * 2, flops=0.0)
     u["sparse_attn"] = dict(bytes=H * Nq * row * 2 + 2 * float(L_out.sum()) * row, flops=4.0 * d * pairs)
@@ -240,9 +245,13 @@ def recorded_traffic(stage, workload):
     return int(e["bytes_per_launch"])
 
 
-def roofline_of(name, avg_ms, units, peaks, sustained=True):
+PEAK_NOTE = ("measured burst bf16 peak: each stage is timed alone in an eager pass well under a "
+             "millisecond, not inside a seconds-long loop")
+
+
+def roofline_of(name, avg_ms, units, peaks):
     b, f = units["bytes"], units["flops"]
-    tpk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    tpk = peaks["bf16_tflops"]
     t_mem = b / (peaks["hbm_gbs"] * 1e9)
     t_tc = f / (tpk * 1e12)
     s = avg_ms * 1e-3
@@ -250,36 +259,68 @@ def roofline_of(name, avg_ms, units, peaks, sustained=True):
         ach = f / s / 1e12
         return {"kernel": name, "bound": "tensor", "achieved": round(ach, 3), "peak": tpk, "unit": "TFLOP/s",
                 "frac": round(ach / tpk, 5), "traffic": None, "algorithmic_flops": f, "avg_ms": round(avg_ms, 4),
-                "peak_source": peaks["source"] + (" sustained" if sustained else " burst")}
+                "peak_source": peaks["source"] + " burst (" + PEAK_NOTE + ")"}
     ach = b / s / 1e9
     return {"kernel": name, "bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm_gbs"], 5), "traffic": None, "algorithmic_bytes": b,
             "avg_ms": round(avg_ms, 4), "peak_source": peaks["source"]}
 
 
+def step_roofline(units, peaks, ms):
+    """Sum over the stages of max(method-minimum bytes / HBM, flops / bf16 burst), against
+    the measured step."""
+    t = sum(max(u["bytes"] / (peaks["hbm_gbs"] * 1e9), u["flops"] / (peaks["bf16_tflops"] * 1e12))
+            for u in units.values())
+    return {"time_us": round(t * 1e6, 2), "frac": round(t * 1e3 / ms, 5),
+            "note": "sum over the stages of max(method-minimum bytes / measured HBM, algorithmic flops / measured "
+                    "bf16 burst), divided by the measured step (graph replay)"}
+
+
+def config_of(cfg, world):
+    """The workload description both arms print (identical strings)."""
+    return {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} chunk={cfg.F}x{cfg.Tf} (Nq={cfg.Nq}) "
+                        f"M={cfg.M} B={cfg.B} r={cfg.r} P={cfg.P} tau={cfg.tau} tau_ca={cfg.tau_ca}",
+            "l2": "GPU arm: flushed between timed steps (256 MiB memset outside the events); CPU oracle arm: n/a",
+            "parallelism": f"replicas x{world} (independent head groups, no exchange)"}
+
+
 # ---------------------------------------------------------------------------------------
 # the CUDA arm
 # ---------------------------------------------------------------------------------------
 
-def run_fastar(args, rank, world, local):
+def make_layer(cfg, tdt, dev, **kw):
+    from kv_cache_tempcache_gb300.layer import FastARLayer
+    args = dict(H=cfg.H, d=cfg.d, Tf=cfg.Tf, F=cfg.F, M=cfg.M, B=cfg.B, r=cfg.r, P=cfg.P, tau=cfg.tau,
+                tau_ca=cfg.tau_ca, topk=cfg.topk, dtype=tdt, device=dev)
+    args.update(kw)
+    return FastARLayer(**args)
+
+
+def timed_graph(graph, flush, steps, torch):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def measure_layer(cfg, args, world, dev, flush, clocks=None, main=True):
+    """One layer shape: the step as a replayed CUDA graph (L2 flushed before each), its
+    stages one by one, the roofline, the end-to-end pipeline through the public API with
+    host buffers, the dense baseline; main=True adds the variants and ablations."""
     import numpy as np
     import torch
     from kv_cache_tempcache_gb300 import synth, _lib
-    from kv_cache_tempcache_gb300.build_lib import build
-    from kv_cache_tempcache_gb300.layer import FastARLayer, DenseLayer
+    from kv_cache_tempcache_gb300.layer import DenseLayer
 
-    if rank == 0 or not os.path.exists(os.path.join(ROOT, "kv_cache_tempcache_gb300", "libfastar.so")):
-        build()
-    barrier(world)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    cfg = synth.CONFIGS[args.config]
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(tdt)
-
+    rank = int(os.environ.get("RANK", "0"))
     gen = synth.DriftingMixture(cfg, seed=args.seed + rank)
-    layer = FastARLayer(H=cfg.H, d=cfg.d, Tf=cfg.Tf, F=cfg.F, M=cfg.M, B=cfg.B, r=cfg.r, P=cfg.P, tau=cfg.tau,
-                        tau_ca=cfg.tau_ca, topk=cfg.topk, dtype=tdt, device=dev)
+    layer = make_layer(cfg, tdt, dev)
     layer.set_centroids(up(gen.centroids))
     kp, vp = gen.prompt
     layer.set_prompt(up(kp), up(vp))
@@ -301,36 +342,27 @@ def run_fastar(args, rank, world, local):
     assert layer.status() == 0, f"device status {layer.status()}"
     graph = layer.capture(q_d, k_d, v_d)
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    clocks = ClockSampler(local)
-    clocks.start()
-    # keep the GPU under load while the clock sampler comes up (at most 5 s), so that
-    # its samples see the clocks of a busy GPU; then the counted warm-up steps
-    t_soak = time.time()
     soak = 0
-    while not clocks.ready(2) and time.time() - t_soak < 5.0:
-        for _ in range(20):
-            flush.zero_()
-            graph.replay()
-        soak += 20
-        torch.cuda.synchronize(dev)
+    if clocks is not None:
+        # keep the GPU under load while the clock sampler comes up (at most 5 s), so that
+        # its samples see the clocks of a busy GPU; then the counted warm-up steps
+        t_soak = time.time()
+        while not clocks.ready(2) and time.time() - t_soak < 5.0:
+            for _ in range(20):
+                flush.zero_()
+                graph.replay()
+            soak += 20
+            torch.cuda.synchronize(dev)
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         graph.replay()
     torch.cuda.synchronize(dev)
     barrier(world)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     barrier(world)
-    for e0, e1 in ev:
-        flush.zero_()
-        e0.record()
-        graph.replay()
-        e1.record()
-    torch.cuda.synchronize(dev)
+    step_ms = timed_graph(graph, flush, args.steps, torch)
     barrier(world)
-    clk = clocks.stop()
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    clk = clocks.stop() if clocks is not None else None
     ms = sum(step_ms) / len(step_ms)
     # the same replays without the flush (inputs and cache may stay in L2): context only
     ev_w = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -362,13 +394,10 @@ def run_fastar(args, rank, world, local):
         stages[name] = sum(d) / len(d)
     peaks = load_peaks()
     units = stage_units(cfg, layer, n_in)
-    dom = max((s for s in stages if s in units), key=lambda s: stages[s])
-    roof_all = {s: roofline_of(s, stages[s], units[s], peaks) for s in stages if s in units}
+    dom = max((s_ for s_ in stages if s_ in units), key=lambda s_: stages[s_])
+    roof_all = {s_: roofline_of(s_, stages[s_], units[s_], peaks) for s_ in stages if s_ in units}
     for s_, r_ in roof_all.items():
         r_["traffic"] = recorded_traffic(s_, cfg.name)
-    roof = roof_all[dom]
-    roof_time = sum(max(units[s]["bytes"] / (peaks["hbm_gbs"] * 1e9),
-                        units[s]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) for s in units)
 
     # end to end through the public API, as a streaming pipeline: every step copies its
     # inputs in from pinned host memory and its outputs back out, and step i+1's inputs
@@ -383,17 +412,17 @@ def run_fastar(args, rank, world, local):
     outs_h = [(torch.empty_like(layer.o_self, device="cpu").pin_memory(),
                torch.empty_like(layer.o_cross, device="cpu").pin_memory()) for _ in range(2)]
     os_h, oc_h = outs_h[0]
-    main = torch.cuda.current_stream(dev)
+    mainst = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()
     in_ready, in_free, out_ready, out_free = [ev() for _ in range(2)], [ev() for _ in range(2)], \
         [ev() for _ in range(2)], [ev() for _ in range(2)]
     for b in range(2):
-        in_free[b].record(main)
-        out_free[b].record(main)
+        in_free[b].record(mainst)
+        out_free[b].record(mainst)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(main)
+    e0.record(mainst)
     s_in.wait_event(e0)
 
     def copy_in(i):
@@ -409,24 +438,25 @@ def run_fastar(args, rank, world, local):
         b = i % 2
         if i + 1 < args.steps:
             copy_in(i + 1)
-        main.wait_event(in_ready[b])
+        mainst.wait_event(in_ready[b])
         flush.zero_()
         graphs2[b].replay()
-        in_free[b].record(main)
-        main.wait_event(out_free[b])
+        in_free[b].record(mainst)
+        mainst.wait_event(out_free[b])
         stage[b][0].copy_(layer.o_self)
         stage[b][1].copy_(layer.o_cross)
-        out_ready[b].record(main)
+        out_ready[b].record(mainst)
         s_out.wait_event(out_ready[b])
         with torch.cuda.stream(s_out):
             outs_h[b][0].copy_(stage[b][0], non_blocking=True)
             outs_h[b][1].copy_(stage[b][1], non_blocking=True)
         out_free[b].record(s_out)
-    main.wait_stream(s_out)
-    e1.record(main)
+    mainst.wait_stream(s_out)
+    e1.record(mainst)
     torch.cuda.synchronize(dev)
     e2e_val, _ = aggregate(cfg.Nq * args.steps, e0.elapsed_time(e1) * 1e-3, world)
     nb = lambda t: t.numel() * t.element_size()
+    del graphs2
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -436,40 +466,42 @@ def run_fastar(args, rank, world, local):
                     "note": "same graph replayed back to back without the L2 flush"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded drifting Gaussian-mixture keys; no dataset, no weights)",
-        "config": {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} chunk={cfg.F}x{cfg.Tf} (Nq={cfg.Nq}) "
-                               f"M={cfg.M} B={cfg.B} r={cfg.r} P={cfg.P} tau={cfg.tau} tau_ca={cfg.tau_ca}",
-                   "cache": f"warmed by {n_prior_chunks} earlier chunks ({cfg.prior_frames} frames); "
-                            f"{int(n_in.sum())} entries in, {int(layer.caches[1 - layer.cur].len.sum())} out",
-                   "l2": "flushed between timed steps (256 MiB memset outside the events)",
-                   "warmup_extra": f"{soak} untimed replays while the clock sampler started",
-                   "stages": "per-stage times from an eager pass with all kernels on one stream, enqueued behind a "
-                             "GPU spin so that host launch time between calls is not counted",
-                   "parallelism": f"replicas x{world} (independent head groups, no exchange)"},
+        "config": config_of(cfg, world),
+        "notes": {"cache": f"warmed by {n_prior_chunks} earlier chunks ({cfg.prior_frames} frames); "
+                           f"{int(n_in.sum())} entries in, {int(layer.caches[1 - layer.cur].len.sum())} out",
+                  "warmup_extra": f"{soak} untimed replays while the clock sampler started",
+                  "stages": "per-stage times from an eager pass with all kernels on one stream, enqueued behind a "
+                            "GPU spin so that host launch time between calls is not counted"},
         "latent_frames_per_s": round(value / cfg.Tf, 2),
-        "roofline": roof,
-        "step_roofline": {"time_us": round(roof_time * 1e6, 2), "frac": round(roof_time * 1e3 / ms, 5),
-                          "note": "sum over stages of max(bytes/HBM, flops/bf16 sustained) / measured step"},
-        "stages_ms": {s: round(v, 4) for s, v in stages.items()},
-        "stages_roofline_frac": {s: r["frac"] for s, r in roof_all.items()},
+        "roofline": roof_all[dom],
+        "step_roofline": step_roofline(units, peaks, ms),
+        "stages_ms": {s_: round(v_, 4) for s_, v_ in stages.items()},
+        "stages_roofline_frac": {s_: r_["frac"] for s_, r_ in roof_all.items()},
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": nb(q_h) + nb(k_h) + nb(v_h),
                 "d2h_bytes_per_step": nb(os_h) + nb(oc_h),
                 "note": "one timed region over all steps: copy-in of step i+1 and copy-out of step i overlap "
                         "step i+1's compute (two input sets, outputs staged on the device); L2 flushed before "
                         "every step inside the region"},
         "gpu_launches": int(launches_per_step * args.steps),
-        "clocks": clk,
         "device_bytes": layer.device_bytes(),
     }
-    # the ANN-restricted match (a variant of the TempCache match): timed beside the exact
-    # match on the measured chunk's incoming cache, with the agreement of their choices
-    out["ann_match"] = time_ann_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib)
-    # the merge variant (Lemma 5.1): its own layer warmed through the same chunks, its
-    # step timed as a graph beside the replace step above
-    out["merge"] = time_merge_variant(cfg, args.seed + rank, up, flush, args.steps, ms, torch, dev)
-    # the quantised match (product quantization of the cached keys), beside the exact match
-    if hist_k and cfg.dtype == "bf16":
-        out["pq_match"] = time_pq_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib, hist_k[0], args.seed)
+    if clk is not None:
+        out["clocks"] = clk
+    if main:
+        # the ANN-restricted match (a variant of the TempCache match): timed beside the exact
+        # match on the measured chunk's incoming cache, with the agreement of their choices
+        out["ann_match"] = time_ann_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib)
+        # the merge variant (Lemma 5.1): its own layer warmed through the same chunks, its
+        # step timed as a graph beside the replace step above
+        out["merge"] = time_merge_variant(cfg, args.seed + rank, up, flush, args.steps, ms, torch, dev)
+        # the quantised match (product quantization of the cached keys), beside the exact match
+        if hist_k and cfg.dtype == "bf16":
+            out["pq_match"] = time_pq_match(layer, cfg, q_d, k_d, flush, args.steps, torch, _lib, hist_k[0],
+                                            args.seed)
+    del graph
+    layer._graph = None
     # dense baseline from the same build: append-only cache, full attention
+    dms = None
     if not args.no_dense:
         hk = np.concatenate(hist_k, axis=1)
         hv = np.concatenate(hist_v, axis=1)
@@ -482,27 +514,130 @@ def run_fastar(args, rank, world, local):
         for _ in range(max(3, args.steps // 4)):
             hold_gpu(torch)
             flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
             dense.step(q_d, k_d, v_d, advance=False)
-            e1.record()
-            dts.append((e0, e1))
+            b_.record()
+            dts.append((a_, b_))
         torch.cuda.synchronize(dev)
-        dms = sum(a.elapsed_time(b) for a, b in dts) / len(dts)
+        dms = sum(a_.elapsed_time(b_) for a_, b_ in dts) / len(dts)
         out["dense"] = {"ms_per_step": round(dms, 4), "keys": int(hk.shape[1] + cfg.Nq),
                         "speedup_fastar_vs_dense": round(dms / ms, 3)}
         del dense
+    if main:
+        out["tempcache_only"] = time_tempcache_only(cfg, args, dev, flush, dms)
+    del layer
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_tempcache_only(cfg, args, dev, flush, dense_ms):
+    """The TempCache ablation (technical summary, Key Results: TempCache alone): the exact
+    match, eviction and compaction bound the cache as in the full step, but attention is
+    dense over the bounded cache (one bucket per head, r = 1) and cross-attention is over
+    every prompt token (tau_ca = -1 keeps all); timed as a graph like the full step."""
+    import numpy as np
+    import torch
+    from kv_cache_tempcache_gb300 import synth
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(tdt)
+    rank = int(os.environ.get("RANK", "0"))
+    gen = synth.DriftingMixture(cfg, seed=args.seed + rank)
+    layer = make_layer(cfg, tdt, dev, B=1, r=1, tau_ca=-1.0, topk=cfg.P)
+    one = np.zeros((cfg.H, 1, cfg.d), np.float32)
+    one[:, 0, 0] = 1.0                           # every key and query in the one bucket
+    layer.set_centroids(up(one))
+    kp, vp = gen.prompt
+    layer.set_prompt(up(kp), up(vp))
+    for _ in range(cfg.prior_frames // cfg.F):
+        k, v, q = gen.next_chunk()
+        layer.step(up(q), up(k), up(v))
+    k, v, q = gen.next_chunk()
+    q_d, k_d, v_d = up(q), up(k), up(v)
+    graph = layer.capture(q_d, k_d, v_d)
+    for _ in range(3):
+        flush.zero_()
+        graph.replay()
+    ms = statistics.mean(timed_graph(graph, flush, args.steps, torch))
+    assert layer.status() == 0
+    res = {"ms_per_step": round(ms, 4), "keys_attended": int(layer.caches[1 - layer.cur].len.sum()) // cfg.H,
+           "note": "exact match + eviction + compaction (cache capped at M), dense attention over the bounded "
+                   "cache, cross-attention over the whole prompt; graph replay, L2 flushed before each"}
+    if dense_ms:
+        res["speedup_vs_dense"] = round(dense_ms / ms, 3)
+    del graph, layer
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_tiny(args, dev, flush):
+    """Latency of the tiny fp32 layer step (1 head, 256 queries, a 768-entry cache) as a
+    replayed graph: the launch-bound case, reported as time per step."""
+    import numpy as np
+    import torch
+    from kv_cache_tempcache_gb300 import synth
+    cfg = synth.TINY_FP32
+    inp = synth.layer_step_inputs(cfg, seed=args.seed)
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+    layer = make_layer(cfg, torch.float32, dev)
+    layer.set_centroids(up(inp["centroids"]))
+    layer.set_prompt(up(inp["kp"]), up(inp["vp"]))
+    n = min(cfg.M, inp["history_k"].shape[1])
+    layer.load_cache(up(inp["history_k"][:, -n:]), up(inp["history_v"][:, -n:]))
+    q_d, k_d, v_d = up(inp["q"]), up(inp["k_cur"]), up(inp["v_cur"])
+    graph = layer.capture(q_d, k_d, v_d)
+    for _ in range(10):
+        graph.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for e0, e1 in ev:
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize(dev)
+    warm = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    cold = statistics.median(timed_graph(graph, flush, 20, torch))
+    assert layer.status() == 0
+    res = {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} Nq={cfg.Nq} n={n} M={cfg.M} B={cfg.B} r={cfg.r} "
+                       f"P={cfg.P} fp32", "latency_us_median": round(warm * 1e3, 2),
+           "latency_us_median_l2_flushed": round(cold * 1e3, 2),
+           "note": "the whole step as one replayed graph; launch-bound at this size"}
+    del graph, layer
+    return res
+
+
+def run_fastar(args, rank, world, local):
+    import torch
+    from kv_cache_tempcache_gb300 import synth
+    from kv_cache_tempcache_gb300.build_lib import build
+
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "kv_cache_tempcache_gb300", "libfastar.so")):
+        build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS[args.config]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    out = measure_layer(cfg, args, world, dev, flush, clocks=clocks, main=True)
     if not args.no_rollout and cfg.name == "wan13b_layer":
         out["rollout"] = measure_rollout(cfg, args.seed + rank, flush, torch, dev)
+    if not args.no_configs and cfg.name == "wan13b_layer":
+        # the other layer shapes: the HunyuanVideo-shaped 720p layer, measured the same way,
+        # and the latency of the tiny fp32 step
+        other = synth.HUNYUAN720P_LAYER
+        line = measure_layer(other, args, world, dev, flush, clocks=None, main=False)
+        if rank == 0 and world == 1 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline(other, args.seed, budget_s=5.0, variants=False)
+        out["configs"] = {other.name: line, "tiny_fp32": measure_tiny(args, dev, flush)}
     if not args.no_dit and cfg.name == "wan13b_layer":
-        del layer, graph
         torch.cuda.empty_cache()
         try:
             out["dit"] = measure_dit(args.dit_chunks, args.seed + rank, torch, dev)
         except Exception as exc:   # the layer's line must survive a failure of the wider run
             out["dit"] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu:
-        out["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=15.0)
+        out["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=12.0)
     return out
 
 
@@ -524,21 +659,108 @@ def _oracle_head(cfg, inp, ck, cv, h):
                        tau_ca=cfg.tau_ca, topk=cfg.topk, scale=cfg.scale)
 
 
-def cpu_baseline(cfg, seed, budget_s=15.0):
-    """The oracle as it stands, on whole heads of the same step until the budget is
-    spent; scaled to query tokens per second of the whole layer."""
+MARGIN = 1e-4   # the method spec's near-tie margin (relative; absolute for the thresholds)
+
+
+def near_ties(cfg, inp, h, res):
+    """Decisions of one head whose oracle scores leave them within the near-tie margin,
+    where either choice is a correct answer: query top-r and key arg-max buckets, top-1
+    matches, eviction and prompt-keep thresholds, the top-k edge of the kept sets."""
+    import numpy as np
+    from oracle import fastar_oracle as O
+    C = inp["centroids"][h]
+
+    def gap(S, k):   # rows whose k-th and (k+1)-th largest scores are within the margin
+        if S.shape[1] <= k:
+            return 0
+        part = -np.sort(-S, axis=1)[:, :k + 1]
+        return int((part[:, k - 1] - part[:, k] < MARGIN * np.abs(part[:, k - 1])).sum())
+
+    c = {"query_buckets": gap(O.centroid_scores(inp["q"][h], C), cfg.r),
+         "key_buckets": gap(O.centroid_scores(inp["k_cur"][h], C), 1)}
+    s1, s2 = res["s1"], res["s2"]
+    fin = np.isfinite(s2)
+    c["top1"] = int((s1[fin] - s2[fin] < MARGIN * np.abs(s1[fin])).sum())
+    ce = res["cos_evict"]
+    c["evict_threshold"] = int((np.abs(ce[np.isfinite(ce)] - cfg.tau) < MARGIN).sum())
+    sc = res["score"]
+    keep_amb = int((np.abs(sc[np.isfinite(sc)] - cfg.tau_ca) < MARGIN).sum())
+    k = min(cfg.topk, cfg.P)
+    for f in range(sc.shape[0]):
+        o = -np.sort(-sc[f])
+        if 0 < k < cfg.P and np.isfinite(o[k - 1]):
+            keep_amb += int((np.abs(sc[f] - o[k - 1]) <= MARGIN * abs(o[k - 1])).sum()) - 1
+    c["keep"] = keep_amb
+    return c
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
+
+
+def oracle_sample(cfg, seed, float_name, heads, budget_s):
+    """Times the oracle (as it stands, in the given float type) on up to `heads` whole heads
+    of one step, at least one, stopping once the budget is spent.  Returns (heads done,
+    seconds, near-tie counts summed over those heads)."""
+    import numpy as np
+    from oracle import fastar_oracle as O
     inp, ck, cv = _oracle_case(cfg, seed)
+    O.FLOAT = np.float32 if float_name == "float32" else np.float64
     t0 = time.perf_counter()
-    heads = 0
-    while heads < cfg.H and (heads == 0 or time.perf_counter() - t0 < budget_s):
-        _oracle_head(cfg, inp, ck, cv, heads)
-        heads += 1
+    done, ties = 0, {}
+    while done < min(heads, cfg.H) and (done == 0 or time.perf_counter() - t0 < budget_s):
+        res = _oracle_head(cfg, inp, ck, cv, done)
+        if O.FLOAT == np.float64:
+            for k_, v_ in near_ties(cfg, inp, done, res).items():
+                ties[k_] = ties.get(k_, 0) + v_
+        done += 1
     dt = time.perf_counter() - t0
+    O.FLOAT = np.float64
+    return done, dt, ties
+
+
+def cpu_baseline(cfg, seed, budget_s=12.0, variants=True):
+    """The oracle as it stands (float64 NumPy, every core's BLAS threads) on whole heads of
+    the same step until the budget is spent, scaled to query tokens per second of the whole
+    layer; beside it the same code in float32 (the precision the method spec names for a CPU
+    baseline) and both with one thread (child processes with the BLAS thread pools set to
+    one).  Also the number of near-tie decisions in the sampled heads."""
+    heads, dt, ties = oracle_sample(cfg, seed, "float64", cfg.H, budget_s)
     per_step = dt / heads * cfg.H
-    return {"value": round(cfg.Nq / per_step, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{heads} of {cfg.H} heads of one {cfg.name} step (float64 NumPy, cache of the "
-                      f"{ck.shape[1]} most recent history entries), scaled by {cfg.H}/{heads}",
-            "seconds": round(dt, 2)}
+    out = {"value": round(cfg.Nq / per_step, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "cpu_model": cpu_model(),
+           "sample": f"{heads} of {cfg.H} heads of one {cfg.name} step (float64 NumPy, all cores, cache of the "
+                     f"{min(cfg.M, cfg.prior_frames * cfg.Tf)} most recent history entries), scaled by "
+                     f"{cfg.H}/{heads}",
+           "seconds": round(dt, 2),
+           "near_ties": dict(ties, note=f"oracle decisions within the {MARGIN:g} margin in the sampled heads, where "
+                                        "either choice is accepted")}
+    if not variants:
+        return out
+    var = {"float64_all_cores": {"value": out["value"], "heads": heads, "seconds": round(dt, 2)}}
+    h32, dt32, _ = oracle_sample(cfg, seed, "float32", cfg.H, budget_s * 0.6)
+    var["float32_all_cores"] = {"value": round(cfg.Nq / (dt32 / h32 * cfg.H), 2), "heads": h32,
+                                "seconds": round(dt32, 2)}
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    for fl in ("float64", "float32"):
+        try:
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", cfg.name, fl, "1",
+                                str(seed)], capture_output=True, text=True, env=env, timeout=300)
+            h1, dt1 = json.loads(r.stdout.strip().splitlines()[-1])
+            var[f"{fl}_one_thread"] = {"value": round(cfg.Nq / (dt1 / h1 * cfg.H), 2), "heads": h1,
+                                       "seconds": round(dt1, 2)}
+        except (OSError, subprocess.SubprocessError, ValueError, IndexError) as exc:
+            var[f"{fl}_one_thread"] = {"error": f"{type(exc).__name__}"}
+    out["variants"] = var
+    return out
 
 
 def time_ann_match(layer, cfg, q_d, k_d, flush, steps, torch, L):
@@ -852,14 +1074,16 @@ def time_merge_variant(cfg, seed, up, flush, steps, replace_ms, torch, dev):
 
 
 def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is one head of the layer step (a
+    bounded sample); value counts the layer's query tokens that step covers (Nq / H)
+    over its measured time, and ms_per_step is that measured time."""
     if rank != 0:
         return None
     from kv_cache_tempcache_gb300 import synth
     cfg = synth.CONFIGS[args.config]
     inp, ck, cv = _oracle_case(cfg, args.seed)
     W = max(args.warmup, 3)
-    # one step = one head of the layer step (a bounded sample); warm-up steps are
-    # capped at one so the run stays within minutes
+    # warm-up steps are capped at one so that the run stays within minutes
     for i in range(min(W, 1)):
         _oracle_head(cfg, inp, ck, cv, 0)
     times = []
@@ -867,21 +1091,27 @@ def run_reference(args, rank, world):
         t0 = time.perf_counter()
         _oracle_head(cfg, inp, ck, cv, i % cfg.H)
         times.append(time.perf_counter() - t0)
-    per_step = sum(times) / len(times) * cfg.H
-    value = cfg.Nq / per_step
-    sample = f"each step: 1 of {cfg.H} heads of one {cfg.name} step, scaled by {cfg.H}"
+    per_step = sum(times) / len(times)
+    value = (cfg.Nq / cfg.H) / per_step
+    sample = (f"each step: one of the {cfg.H} heads of one {cfg.name} step (Nq/H = {cfg.Nq / cfg.H:g} layer query "
+              f"tokens), float64 NumPy, all cores")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": W, "ms_per_step": round(per_step * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: H={cfg.H} d={cfg.d} Nq={cfg.Nq} M={cfg.M} B={cfg.B} r={cfg.r} "
-                                   f"P={cfg.P}", "l2": "n/a (CPU)"},
+            "config": config_of(cfg, world),
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
     args = parse_args()
+    if args.cpu_sample:
+        from kv_cache_tempcache_gb300 import synth
+        name, fl, heads, seed = args.cpu_sample
+        h, dt, _ = oracle_sample(synth.CONFIGS[name], int(seed), fl, int(heads), 0.0)
+        print(json.dumps([h, dt]))
+        return
     rank, world, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
