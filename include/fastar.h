@@ -137,6 +137,16 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d,
                          const void* centroids, int B, int r,
                          int32_t* ids, float* scores, float* norms, cudaStream_t stream);
 
+/* ---- 1b. both assignments of a step in one call ---------------------------------------
+ * The two uses of 1 in a layer step, one launch: q_ids [H, n, r] = the queries' top-r
+ * sets, k_ids [H, n] = the current keys' arg-max buckets, k_norms [H, n] (optional) =
+ * |k_cur|.  Identical results to fastar_bucket_assign(q, ..., r, q_ids, NULL, NULL) and
+ * fastar_bucket_assign(k_cur, ..., 1, k_ids, NULL, k_norms).  q and k_cur share
+ * (head_stride, token_stride).  Limits and errors as 1. */
+int fastar_bucket_assign_qk(const void* q, const void* k_cur, int dtype, int H, int64_t n, int d,
+                            int64_t head_stride, int64_t token_stride, const void* centroids, int B, int r,
+                            int32_t* q_ids, int32_t* k_ids, float* k_norms, cudaStream_t stream);
+
 /* ---- 2. TempCache match + eviction flags ------------------------------------------
  * FAST-AR technical summary §2.A and blog §1: for each current-frame query, the
  * top-1 nearest key among the cached (previous-frame) keys; a cached entry whose

@@ -35,6 +35,7 @@ _SIGS = {
     "fastar_status_string": [_I],
     "fastar_workspace_bytes": [_I, _I, _L, _L, _I, _I, _I, _L, _I],
     "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
+    "fastar_bucket_assign_qk": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
     "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _P,
                                _S, _P],
     "fastar_tempcache_match_ann": [_P, _P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _F, _P,
@@ -171,6 +172,15 @@ def fastar_bucket_assign(x, centroids, r, ids, scores=None, norms=None, stream=N
     hs, ts = tok_strides(x)
     _call("fastar_bucket_assign", ptr(x), dtype_code(x.dtype), H, n, d, hs, ts, ptr(centroids),
           centroids.shape[1], r, ptr(ids), ptr(scores), ptr(norms), stream_handle(stream))
+
+
+def fastar_bucket_assign_qk(q, k_cur, centroids, r, q_ids, k_ids, k_norms=None, stream=None):
+    H, n, d = q.shape
+    hs, ts = tok_strides(q)
+    if tok_strides(k_cur) != (hs, ts):
+        raise ValueError("q and k_cur must share strides")
+    _call("fastar_bucket_assign_qk", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, n, d, hs, ts, ptr(centroids),
+          centroids.shape[1], r, ptr(q_ids), ptr(k_ids), ptr(k_norms), stream_handle(stream))
 
 
 def fastar_tempcache_match(q, k_cur, cache_k, cache_knorm, cache_len, tau, top1, s1, s2, evict, dev_status,

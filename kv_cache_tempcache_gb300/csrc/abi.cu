@@ -100,6 +100,22 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d, int6
                                               centroids, B, r, ids, scores, norms, stream));
 }
 
+int fastar_bucket_assign_qk(const void* q, const void* k_cur, int dtype, int H, int64_t n, int d,
+                            int64_t head_stride, int64_t token_stride, const void* centroids, int B, int r,
+                            int32_t* q_ids, int32_t* k_ids, float* k_norms, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (H < 0 || n < 0 || B < 1 || r < 1) return FASTAR_EINVAL;
+  if (B > FASTAR_MAX_B || r > FASTAR_MAX_R || r > B) return FASTAR_ECAPACITY;
+  if (H == 0 || n == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, head_stride, token_stride, n, H))) return rc;
+  if ((rc = check_tok(k_cur, dtype, d, head_stride, token_stride, n, H))) return rc;
+  if (!centroids || !aligned16(centroids) || !q_ids || !k_ids) return FASTAR_EINVAL;
+  return cuda_rc(fastar::launch_bucket_assign_qk(dtype, d, TokView{q, head_stride, token_stride},
+                                                 TokView{k_cur, head_stride, token_stride}, H, n, centroids, B, r,
+                                                 q_ids, k_ids, k_norms, stream));
+}
+
 int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
                            int64_t head_stride, int64_t token_stride, const void* cache_k,
                            const float* cache_knorm, const int32_t* cache_len, int64_t M, float tau,

@@ -5,7 +5,8 @@
 // FAST-AR technical summary §2.C / §2.B: tokens go to ANN buckets; the key bucket is
 // the arg-max centroid, a query's set the r best (ties to the lower index).
 //
-// One CTA per (head, 128-token tile), 4 warps.  Thread 0 loads the token tile and the
+// One CTA per (head, 128-token tile), 4 warps (a step's query and key assignments can
+// also run as one launch, one grid plane each).  Thread 0 loads the token tile and the
 // head's centroids with TMA and issues the MMA; every thread then owns one token row:
 // it reads its scores from TMEM in 32-column chunks, keeps a sorted top-r, and
 // computes |x| from the token tile still in shared memory.  Several CTAs share an SM
@@ -32,11 +33,12 @@ struct AssignCtl {
   int abort;
 };
 
+// The assignment of one (head h, 128-token tile) (every thread of the CTA calls it).
 template <int D, int RT>
-__global__ void __launch_bounds__(128)
-assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c, int H,
-                 int64_t n, int token_major, int B, int NP, int r, uint32_t tcols, int32_t* __restrict__ ids,
-                 float* __restrict__ scores, float* __restrict__ norms, int32_t* status) {
+__device__ __forceinline__ void assign_tile(const CUtensorMap* tm_x, const CUtensorMap* tm_c, int h, int64_t t0,
+                                            int64_t n, int token_major, int B, int NP, int r, uint32_t tcols,
+                                            int32_t* __restrict__ ids, float* __restrict__ scores,
+                                            float* __restrict__ norms, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -45,8 +47,6 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   uint8_t* sb = base + KH * kBlk;                      // [KH][NP * 128]
   AssignCtl& sm = *reinterpret_cast<AssignCtl*>(sb + KH * NP * 128);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int64_t t0 = (int64_t)blockIdx.x * kRows;
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.tma_bar, 1);
     tc::mbar_init(&sm.mma_bar, 1);
@@ -66,10 +66,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     tc::mbar_arrive_tx(&sm.tma_bar, (uint32_t)(KH * kBlk + KH * NP * 128));
     for (int kh = 0; kh < KH; ++kh) {
       if (token_major)
-        tc::tma_load_3d(sa + kh * kBlk, &tm_x, kh * 64, h, (int)t0, &sm.tma_bar);
+        tc::tma_load_3d(sa + kh * kBlk, tm_x, kh * 64, h, (int)t0, &sm.tma_bar);
       else
-        tc::tma_load_3d(sa + kh * kBlk, &tm_x, kh * 64, (int)t0, h, &sm.tma_bar);
-      tc::tma_load_3d(sb + kh * NP * 128, &tm_c, kh * 64, 0, h, &sm.tma_bar);
+        tc::tma_load_3d(sa + kh * kBlk, tm_x, kh * 64, (int)t0, h, &sm.tma_bar);
+      tc::tma_load_3d(sb + kh * NP * 128, tm_c, kh * 64, 0, h, &sm.tma_bar);
     }
     if (tc::mbar_wait(&sm.tma_bar, 0, abort)) {
       tc::tc_fence_after();
@@ -171,6 +171,30 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   if (threadIdx.x == 0 && sm.abort) flag_status(status, FASTAR_DEV_TIMEOUT);
 }
 
+template <int D, int RT>
+__global__ void __launch_bounds__(128)
+assign_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c, int H,
+                 int64_t n, int token_major, int B, int NP, int r, uint32_t tcols, int32_t* __restrict__ ids,
+                 float* __restrict__ scores, float* __restrict__ norms, int32_t* status) {
+  assign_tile<D, RT>(&tm_x, &tm_c, blockIdx.y, (int64_t)blockIdx.x * kRows, n, token_major, B, NP, r, tcols, ids,
+                     scores, norms, status);
+}
+
+// Both assignments of a step in one launch: blockIdx.z = 0 takes a query tile (top-r
+// sets), blockIdx.z = 1 a current-key tile (arg-max bucket and |k|).
+template <int D, int RTQ>
+__global__ void __launch_bounds__(128)
+assign_qk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_c, int64_t n, int token_major, int B, int NP, int r,
+                    uint32_t tcols, int32_t* __restrict__ qb, int32_t* __restrict__ kb, float* __restrict__ knorm) {
+  if (blockIdx.z == 0)
+    assign_tile<D, RTQ>(&tm_q, &tm_c, blockIdx.y, (int64_t)blockIdx.x * kRows, n, token_major, B, NP, r, tcols, qb,
+                        nullptr, nullptr, nullptr);
+  else
+    assign_tile<D, 1>(&tm_k, &tm_c, blockIdx.y, (int64_t)blockIdx.x * kRows, n, token_major, B, NP, 1, tcols, kb,
+                      nullptr, knorm, nullptr);
+}
+
 template <int D>
 size_t assign_tc_smem(int NP) {
   return (size_t)(D / 64) * (kBlk + (size_t)NP * 128) + sizeof(AssignCtl) + 1024;
@@ -213,12 +237,57 @@ bool assign_tc_impl(TokView x, int H, int64_t n, const void* cent, int B, int r,
   return true;
 }
 
+template <int D>
+bool assign_qk_tc_impl(TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r, int32_t* qb,
+                       int32_t* kb, float* knorm, cudaStream_t s) {
+  const int NP = (B + 31) / 32 * 32;
+  if (NP > 256 || n > INT32_MAX) return false;
+  CUtensorMap tq, tk, tcen;
+  const bool token_major = H > 1 && q.hs < q.ts;
+  for (int i = 0; i < 2; ++i) {
+    const TokView& x = i == 0 ? q : k;
+    CUtensorMap* m = i == 0 ? &tq : &tk;
+    if (token_major) {
+      if (!make_tmap_bf16_3d(m, x.p, D, (uint64_t)H, (uint64_t)n, (uint64_t)x.hs * 2, (uint64_t)x.ts * 2, 64, 1,
+                             128))
+        return false;
+    } else if (!make_tmap_bf16_3d(m, x.p, D, (uint64_t)n, (uint64_t)H, (uint64_t)x.ts * 2, (uint64_t)x.hs * 2, 64,
+                                  128)) {
+      return false;
+    }
+  }
+  if (!make_tmap_bf16_3d(&tcen, cent, D, (uint64_t)B, (uint64_t)H, (uint64_t)D * 2, (uint64_t)B * D * 2, 64,
+                         (uint32_t)NP))
+    return false;
+  uint32_t tcols = 32;
+  while ((int)tcols < NP) tcols <<= 1;
+  const size_t smem = assign_tc_smem<D>(NP);
+  const int smax = (int)assign_tc_smem<D>(256);
+  const cudaError_t a2 = opt_in_smem((const void*)assign_qk_tc_kernel<D, 2>, smax);
+  const cudaError_t a0 = opt_in_smem((const void*)assign_qk_tc_kernel<D, 0>, smax);
+  if (a2 != cudaSuccess || a0 != cudaSuccess) return false;
+  const dim3 grid((unsigned)((n + kRows - 1) / kRows), H, 2);
+  const int tm = token_major ? 1 : 0;
+  if (r == 2)
+    assign_qk_tc_kernel<D, 2><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm);
+  else
+    assign_qk_tc_kernel<D, 0><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm);
+  count_launches(1);
+  return true;
+}
+
 }  // namespace
 
 bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int B, int r, int32_t* ids,
                       float* scores, float* norms, cudaStream_t s) {
   return d == 128 ? assign_tc_impl<128>(x, H, n, cent, B, r, ids, scores, norms, s)
                   : assign_tc_impl<64>(x, H, n, cent, B, r, ids, scores, norms, s);
+}
+
+bool launch_assign_qk_tc(int d, TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r,
+                         int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s) {
+  return d == 128 ? assign_qk_tc_impl<128>(q, k, H, n, cent, B, r, qb, kb, knorm, s)
+                  : assign_qk_tc_impl<64>(q, k, H, n, cent, B, r, qb, kb, knorm, s);
 }
 
 }  // namespace fastar

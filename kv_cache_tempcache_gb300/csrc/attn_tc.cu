@@ -27,9 +27,9 @@
 // AnnSA's items (head, bucket, 128-pair tile) are planned by every CTA in its prologue
 // (an exclusive prefix of the tile counts in shared memory, searched per item) when
 // H·B < 2048, else listed by a one-CTA planning kernel;
-// each item writes its slot partials (o, lse) at the (query, slot) pair rows — staged
-// through shared memory so every store is a 128-byte row segment — and a merge kernel
-// combines the r adjacent slot rows of every query afterwards.
+// each item writes its slot partials (o in bf16, lse in fp32) at the (query, slot) pair
+// rows — staged through shared memory so every store is a full row segment — and a merge
+// kernel combines the r adjacent slot rows of every query afterwards.
 // Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.
 #include <climits>
 #include <cstring>
@@ -974,9 +974,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       const float inv = live ? 1.0f / l : 0.f;
       const float lse = live ? (m_used + __log2f(l)) * 0.6931471805599453f : neg_inf();
       if (a.mode == kSparse) {
-        // slot partials at their (query, slot) pair rows: each 32-column slice goes through
-        // the transpose buffer and leaves as 128-byte row segments (edst: the row of each)
+        // slot partials (bf16) at their (query, slot) pair rows: each 32-column slice goes
+        // through the transpose buffer and leaves as 64-byte row segments (edst: the row of
+        // each)
         const int64_t prow0 = (int64_t)h * np;
+        __nv_bfloat16* part16 = reinterpret_cast<__nv_bfloat16*>(a.part_o);
         sm.edst[row] = dst;
         const int ew = warp - kEpiWarp0;
 #pragma unroll 1
@@ -1002,7 +1004,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             const int er = sm.edst[rr];
             if (rr < nrows && er >= 0) {
               const float4 v4 = *reinterpret_cast<const float4*>(so + rr * 32 + ((ch ^ (rr & 7)) << 2));
-              *reinterpret_cast<float4*>(a.part_o + (prow0 + er) * D + c * 32 + ch * 4) = v4;
+              *reinterpret_cast<uint2*>(part16 + (prow0 + er) * D + c * 32 + ch * 4) =
+                  make_uint2(pack_bf16(v4.x, v4.y), pack_bf16(v4.z, v4.w));
             }
           }
           tc::named_bar(2, 128);
@@ -1173,7 +1176,8 @@ __global__ void __launch_bounds__(256) cross_gather_rows_kernel(const AttnArgs a
 // Merges the r slot partials of every AnnSA query by the exact log-sum-exp rule:
 // o = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s), and
 // lse = max + log(sum_s w_s).  One warp per (head, query); lane l owns columns
-// [l*D/32, (l+1)*D/32), so every slot row is read as one coalesced 4*D-byte line.
+// [l*D/32, (l+1)*D/32), so every slot row (bf16, as the attention stored it) is read as
+// one coalesced 2*D-byte line.
 template <int D>
 __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   constexpr int E = D / 32;
@@ -1188,11 +1192,18 @@ __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   // are known (every pair has a row in the partial buffer; a row is used only when its
   // weight is nonzero)
   float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+  const __nv_bfloat16* part16 = reinterpret_cast<const __nv_bfloat16*>(a.part_o);
   auto load_row = [&](int sl) -> float4 {
-    const float* src = a.part_o + (pb + sl) * D + lane * E;
-    if (E == 4) return __ldcs(reinterpret_cast<const float4*>(src));
-    const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
-    return make_float4(v.x, v.y, 0.f, 0.f);
+    const __nv_bfloat16* src = part16 + (pb + sl) * D + lane * E;
+    if (E == 4) {
+      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(src));
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      return make_float4(x.x, x.y, y.x, y.y);
+    }
+    const unsigned u = __ldcs(reinterpret_cast<const unsigned*>(src));
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+    return make_float4(x.x, x.y, 0.f, 0.f);
   };
   p0 = load_row(0);
   if (a.r > 1) p1 = load_row(1);

@@ -118,6 +118,17 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
   return assign_impl<float, 64>(x, H, n, cent, B, r, ids, scores, norms, s);
 }
 
+cudaError_t launch_bucket_assign_qk(int dtype, int d, TokView q, TokView k, int H, int64_t n, const void* cent,
+                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if (dtype == FASTAR_BF16 && launch_assign_qk_tc(d, q, k, H, n, cent, B, r, qb, kb, knorm, s))
+    return cudaGetLastError();
+  // otherwise the two assignments one after the other
+  cudaError_t e = launch_bucket_assign(dtype, d, q, H, n, cent, B, r, qb, nullptr, nullptr, s);
+  if (e != cudaSuccess) return e;
+  return launch_bucket_assign(dtype, d, k, H, n, cent, B, 1, kb, nullptr, knorm, s);
+}
+
 // ---------------------------------------------------------------------------------------
 // Stable counting sort: one thread-block cluster of kSortCtas CTAs per head.
 // CTA c of the cluster owns the c-th contiguous chunk of the head's element range and,

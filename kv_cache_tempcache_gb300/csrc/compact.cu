@@ -6,10 +6,11 @@
 // the method spec's.
 //
 // Two kernels: a one-CTA-per-head scan that writes the slot -> source map and the
-// new length, then a bandwidth kernel that moves rows with 16-byte accesses.  The sorted
-// form puts the new cache's bucket ids and their stable counting sort between the two,
-// so that the copy can also write each row to its place in a bucket-ordered copy (the
-// layout the bucket-restricted attention reads as contiguous tiles).
+// new length, then a bandwidth kernel that moves rows with 16-byte accesses.  In the
+// sorted form the scan also writes the new cache's bucket ids and their stable counting
+// sort runs between the two, so that the copy can also write each row to its place in a
+// bucket-ordered copy (the layout the bucket-restricted attention reads as contiguous
+// tiles).
 //
 // The merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1 — identical
 // keys merge exactly when their values are averaged and the logit is shifted by the
@@ -25,11 +26,14 @@ namespace fastar {
 constexpr int kScanThreads = 1024;
 
 // Slot s of the new cache takes: survivor number (s + drop) if s + drop < S, else
-// current token (s + drop - S); drop = max(0, S + nq - M).
+// current token (s + drop - S); drop = max(0, S + nq - M).  With kbout the slot's bucket
+// id is written too (the source entry's), so that the key sort can run before the rows
+// move.
 __global__ void __launch_bounds__(kScanThreads)
 compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
                     const uint8_t* __restrict__ evict, int32_t* __restrict__ len_out,
-                    int32_t* __restrict__ index_map, int32_t* status) {
+                    int32_t* __restrict__ index_map, int32_t* status, const int32_t* __restrict__ kcb = nullptr,
+                    const int32_t* __restrict__ kbin = nullptr, int32_t* __restrict__ kbout = nullptr) {
   __shared__ int warp_tot[kScanThreads / 32];
   __shared__ int s_total;
   const int h = blockIdx.x;
@@ -72,16 +76,24 @@ compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
   const int64_t drop = total > M ? total - M : 0;
   const int64_t L = total - drop;
   int64_t rank = warp_tot[warp] + incl - local;
+  const int32_t* kbi = kbin ? kbin + (int64_t)h * M : nullptr;
+  int32_t* kbo = kbout ? kbout + (int64_t)h * M : nullptr;
   for (int64_t j = beg; j < end; ++j) {
     if (!e[j]) {
       const int64_t slot = rank - drop;
-      if (slot >= 0) imap[slot] = (int32_t)j;
+      if (slot >= 0) {
+        imap[slot] = (int32_t)j;
+        if (kbo) kbo[slot] = kbi[j];
+      }
       ++rank;
     }
   }
   for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
     const int64_t slot = S + i - drop;
-    if (slot >= 0) imap[slot] = (int32_t)(n + i);
+    if (slot >= 0) {
+      imap[slot] = (int32_t)(n + i);
+      if (kbo) kbo[slot] = kcb[(int64_t)h * nq + i];
+    }
   }
   for (int64_t s = L + threadIdx.x; s < M; s += blockDim.x) imap[s] = -1;
   if (threadIdx.x == 0) len_out[h] = (int32_t)L;
@@ -102,29 +114,6 @@ struct SortedIO {
   void* ksorted;
   void* vsorted;
 };
-
-// Bucket id of every slot of the new cache (before the rows move, so that the sort can
-// run first): the source entry's, through the index map.
-__global__ void __launch_bounds__(256)
-compact_bucket_kernel(int H, int64_t nq, int64_t M, const int32_t* __restrict__ kcb, const int32_t* __restrict__ kbin,
-                      const int32_t* __restrict__ len_in, const int32_t* __restrict__ len_out,
-                      const int32_t* __restrict__ index_map, int32_t* __restrict__ kbout, int32_t* status) {
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= (int64_t)H * M) return;
-  const int h = (int)(row / M);
-  if (row - (int64_t)h * M >= len_out[h]) return;
-  int64_t n = len_in[h];
-  n = n < 0 ? 0 : (n > M ? M : n);
-  const int64_t src = index_map[row];
-  if (src >= 0 && src < n) {
-    kbout[row] = kbin[(int64_t)h * M + src];
-  } else if (src >= n && src < n + nq) {
-    kbout[row] = kcb[(int64_t)h * nq + (src - n)];
-  } else {
-    flag_status(status, FASTAR_DEV_BAD_INDEX);
-    kbout[row] = -1;
-  }
-}
 
 // wa * a + wb * b element-wise over one 16-byte chunk (fp32 arithmetic, rounded once).
 template <typename T>
@@ -280,11 +269,8 @@ cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int
                                         int32_t* kbout, int32_t* len_out, int32_t* imap, int B, int32_t* kperm,
                                         int32_t* koff, int32_t* kpos, void* ksorted, void* vsorted,
                                         int32_t* status, cudaStream_t s) {
-  compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status);
-  count_launches(1);
-  const int64_t rows = (int64_t)H * M;
-  compact_bucket_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(H, nq, M, kcb, kbin, len_in, len_out, imap,
-                                                                        kbout, status);
+  // the scan also writes the new slots' bucket ids (the key sort's input)
+  compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status, kcb, kbin, kbout);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

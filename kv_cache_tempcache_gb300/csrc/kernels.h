@@ -24,6 +24,12 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 // Tensor-core bucket assignment (bf16); false if it could not be set up.
 bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int B, int r, int32_t* ids,
                       float* scores, float* norms, cudaStream_t s);
+// Both assignments of a step in one launch (bf16): queries' top-r sets into qb
+// [H, n, r], current keys' buckets into kb [H, n] and their norms into knorm [H, n].
+bool launch_assign_qk_tc(int d, TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r,
+                         int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s);
+cudaError_t launch_bucket_assign_qk(int dtype, int d, TokView q, TokView k, int H, int64_t n, const void* cent,
+                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s);
 // inv (optional, [H, n*r]): each element's position in its head's sorted order.
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
@@ -107,7 +113,7 @@ struct AttnArgs {
   void* out;
   int64_t o_hs, o_ts;
   float* lse;
-  float* part_o;    // sparse partials [H, nq*r, d], row = (query, slot) pair
+  float* part_o;    // sparse partials [H, nq*r, d], row = (query, slot) pair (bf16 on the tensor-core path)
   float* part_lse;  // [H, nq*r]
   void* items;      // sparse: work list written by the planning kernel (tensor-core path)
   void* ksorted;    // sparse: the cache K/V rows in bucket order [H, M, d] (tensor-core path)

@@ -239,8 +239,7 @@ class FastARLayer:
             evm = torch.cuda.Event()
             evm.record(self.mside)
         t("bucket_assign", main, "begin")
-        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
-        L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
+        L.fastar_bucket_assign_qk(q, k_cur, self.centroids, self.r, self.qb, self.kb_cur, self.kcur_norm)
         t("bucket_assign", main, "end")
         if self.pq:
             t("pq_encode", main, "begin")
@@ -318,8 +317,7 @@ class FastARLayer:
         and the bucket-restricted attention -> out ([H, Nq, d] view; default o_self)."""
         cin, cout = self.caches[self.cur], self.caches[1 - self.cur]
         o = self.o_self if out is None else out
-        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
-        L.fastar_bucket_assign(k_cur, self.centroids, 1, self.kb_cur, None, self.kcur_norm)
+        L.fastar_bucket_assign_qk(q, k_cur, self.centroids, self.r, self.qb, self.kb_cur, self.kcur_norm)
         L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
         L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, None,
                                  self.evict, self.dev_status, self.ws_match)

@@ -221,3 +221,29 @@ def test_cross_attention_paths_agree_bit_for_bit(P, d):
         oc, _ = O.cross_attention_subset(inputs["q"][h], inputs["kp"][h], inputs["vp"][h], kept, cfg.F, cfg.Tf,
                                          cfg.scale)
         parity.close(outs[1][0][h], oc, *tol, f"o_cross head {h}")
+
+
+@pytest.mark.parametrize("r,layout", [(2, "HND"), (3, "HND"), (2, "NHD")])
+def test_fused_assignment_equals_two_calls(r, layout):
+    # fastar_bucket_assign_qk: the queries' top-r sets and the current keys' buckets and
+    # norms in one launch, bit for bit the two separate calls
+    from kv_cache_tempcache_gb300 import _lib as L
+    cfg = GH.small_bf16()
+    inp = synth.layer_step_inputs(cfg, seed=3)
+    if layout == "NHD":
+        q = GH.to_dev(inp["q"].transpose(1, 0, 2), cfg).transpose(0, 1)
+        k = GH.to_dev(inp["k_cur"].transpose(1, 0, 2), cfg).transpose(0, 1)
+    else:
+        q, k = GH.to_dev(inp["q"], cfg), GH.to_dev(inp["k_cur"], cfg)
+    C = GH.to_dev(inp["centroids"], cfg)
+    H, n = cfg.H, cfg.Nq
+    i32 = lambda *s: torch.full(s, -5, dtype=torch.int32, device="cuda")
+    qb1, kb1, qb2, kb2 = i32(H, n, r), i32(H, n, 1), i32(H, n, r), i32(H, n, 1)
+    kn1 = torch.zeros((H, n), dtype=torch.float32, device="cuda")
+    kn2 = torch.zeros_like(kn1)
+    L.fastar_bucket_assign(q, C, r, qb1)
+    L.fastar_bucket_assign(k, C, 1, kb1, None, kn1)
+    L.fastar_bucket_assign_qk(q, k, C, r, qb2, kb2, kn2)
+    torch.cuda.synchronize()
+    assert torch.equal(qb1, qb2) and torch.equal(kb1, kb2) and torch.equal(kn1, kn2)
+    parity.check_topr(O.centroid_scores(inp["q"][0], inp["centroids"][0]), GH.np_(qb2)[0], "fused query buckets")
