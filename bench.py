@@ -208,6 +208,10 @@ def stage_units(cfg, layer, n_in):
     u["cache_compact"] = dict(bytes=4.0 * H * Nq * row + 4.0 * H * M, flops=0.0)
     u["bucket_sort"] = dict(bytes=4.0 * float(L_out.sum()) * 2, flops=0.0)
     u["bucket_sort_q"] = dict(bytes=4.0 * H * Nq * r * 2, flops=0.0)
+    if getattr(layer, "presort", False):
+        # the sorted compaction's planning launch also sorts the new keys and the step's
+        # (query, slot) pairs by bucket: those bytes belong to its stage
+        u["cache_compact"]["bytes"] += u["bucket_sort"]["bytes"] + u["bucket_sort_q"]["bytes"]
     u["sparse_attn"] = dict(bytes=H * Nq * row * 2 + 2 * float(L_out.sum()) * row, flops=4.0 * d * pairs)
     u["annca_select"] = dict(bytes=H * Nq * row + H * P * row, flops=2.0 * H * Nq * P * d)
     u["cross_attn_subset"] = dict(bytes=H * Nq * row * 2 + 2 * float(kcnt.sum()) * row,

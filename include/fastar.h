@@ -16,7 +16,7 @@
  * identical keys is exact when their values are averaged and their logit is shifted
  * by the group size) replaces step 3 with fastar_cache_compact_merge and step 5 with
  * fastar_sparse_attn_grouped, using the owner output of step 2.
- * Steps 3-5 can also run as fastar_cache_compact_sorted (the compaction, the key sort of
+ * Steps 3-5 can also run as fastar_cache_compact_sorted (the compaction, both sorts of
  * step 4 and a bucket-ordered copy of the new K/V rows, written as the rows move) followed
  * by fastar_sparse_attn_presorted, which reads that copy instead of making its own.
  *
@@ -287,7 +287,14 @@ int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M,
  * inverse of kperm; caller-owned scratch).  The sorted copy is written as the rows move,
  * instead of being re-read from the new cache by fastar_sparse_attn.  1 <= B <=
  * FASTAR_MAX_B; k_sorted / v_sorted 16-byte aligned and distinct from the in and out
- * caches; a bucket id outside [0, B) flags FASTAR_DEV_BAD_BUCKET. */
+ * caches; a bucket id outside [0, B) flags FASTAR_DEV_BAD_BUCKET.
+ * qb int32 [H, nq, r] (may be NULL): the step's query buckets.  When given, the same
+ * launch also writes AnnSA's query-side order, exactly fastar_bucket_sort(qb, H, nq, r, B,
+ * NULL, qperm, qoff): qperm int32 [H, nq*r], qoff int32 [H, B+1] (both required then;
+ * 1 <= r <= FASTAR_MAX_R, else FASTAR_EINVAL / FASTAR_ECAPACITY before any work), so
+ * that the step needs no separate sort launch.  Without qb, r, qperm and qoff are
+ * ignored.  Two kernel launches either way: one thread-block cluster per head plans
+ * (the pairs' sort, the survivor scan, the key sort), then the rows move. */
 int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M,
                                 const void* k_cur, const void* v_cur, int64_t head_stride,
                                 int64_t token_stride, const float* kcur_norm, const int32_t* kcur_bucket,
@@ -296,6 +303,7 @@ int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M,
                                 void* k_out, void* v_out, float* knorm_out, int32_t* kb_out,
                                 int32_t* len_out, int32_t* index_map, int B, int32_t* kperm,
                                 int32_t* koff, int32_t* kpos, void* k_sorted, void* v_sorted,
+                                const int32_t* qb, int r, int32_t* qperm, int32_t* qoff,
                                 int32_t* dev_status, cudaStream_t stream);
 
 /* ---- 4. counting sort by bucket --------------------------------------------------
@@ -382,6 +390,13 @@ int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, in
  * inputs) is not ranked: kcnt = -1, keep 0 and kidx -1 throughout, score NaN.
  * fastar_cross_attn_subset reports such a kcnt as FASTAR_DEV_BAD_INDEX in its status
  * word and attends to no prompt token for that frame.
+ * kp_kept, vp_kept (optional, together; bf16 only, else FASTAR_EUNSUPPORTED): [H,F,P,d]
+ * planes that the ranking launch fills with the kept rows: kp_kept[h,f,t] =
+ * kp[h, kidx[h,f,t]] for t < kcnt[h,f] (vp_kept from vp, [H,P,d] contiguous, required
+ * then), zero rows from kcnt up to the next multiple of 64 (at most P), other rows
+ * untouched; after a failure (kcnt = -1) nothing is written.  16-byte aligned and distinct
+ * from kp and vp.  They are fastar_cross_attn_kept's input, so that the cross-attention
+ * needs no gather launch of its own.
  * Workspace: fastar_workspace_bytes(FASTAR_OP_ANNCA, H, ..., P, F).  P <= FASTAR_MAX_P. */
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                         int64_t q_head_stride, int64_t q_token_stride,
@@ -389,6 +404,7 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
                         float tau_ca, int topk, int gate, int B,
                         const int32_t* qperm, const int32_t* qoff,
                         uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
+                        const void* vp, void* kp_kept, void* vp_kept,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---- 6b. AnnCA prompt selection without any caller allocation ------------------------
@@ -432,6 +448,20 @@ int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf
                              void* out, int64_t o_head_stride, int64_t o_token_stride,
                              float* lse, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
+
+/* ---- 7b. cross-attention over kept-row planes ------------------------------------------
+ * 7 with the kept rows already gathered by fastar_annca_select into kp_kept / vp_kept
+ * [H,F,P,d] (rows 0..kcnt[h,f) of plane (h,f) are the kept prompt tokens in kidx order):
+ *   O[h,i] = sum_{t < kcnt[h,f]} softmax_t(q_i . kp_kept[h,f,t] * scale) vp_kept[h,f,t]
+ * for query i of frame f.  The same results as fastar_cross_attn_subset with a workspace
+ * on the same selection, in one kernel launch (the tensor-core engine reads the planes as
+ * tiles).  bf16 only (FASTAR_EUNSUPPORTED otherwise); planes 16-byte aligned; kcnt < 0 is
+ * reported as FASTAR_DEV_BAD_INDEX and attends to nothing (O = 0, lse = -inf), as in 7. */
+int fastar_cross_attn_kept(const void* q, int dtype, int H, int F, int64_t tpf, int d,
+                           int64_t q_head_stride, int64_t q_token_stride,
+                           const void* kp_kept, const void* vp_kept, int64_t P, const int32_t* kcnt,
+                           float scale, void* out, int64_t o_head_stride, int64_t o_token_stride,
+                           float* lse, cudaStream_t stream);
 
 /* ---- 8. dense attention (the baseline) ------------------------------------------
  * The dense softmax attention FAST-AR is compared against (technical summary,

@@ -45,7 +45,7 @@ _SIGS = {
     "fastar_cache_compact_merge": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "fastar_cache_compact_sorted": [_I, _I, _L, _I, _L, _P, _P, _L, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                    _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P],
+                                    _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P],
     "fastar_bucket_sort": [_P, _I, _L, _I, _I, _P, _P, _P, _P, _P],
     "fastar_pq_encode": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P],
     "fastar_tempcache_match_pq": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _P, _L, _P, _I, _I, _F, _P, _P, _P,
@@ -58,10 +58,11 @@ _SIGS = {
     "fastar_sparse_attn_presorted": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _P, _F,
                                      _P, _L, _L, _P, _P, _P, _S, _P],
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
-                            _P, _P, _S, _P],
+                            _P, _P, _P, _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
     "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P, _S,
                                  _P],
+    "fastar_cross_attn_kept": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_attn_grouped": [_P, _I, _I, _L, _I, _L, _L, _P, _P, _L, _L, _L, _P, _L, _F, _P, _L, _L, _P, _P],
     "fastar_dense_append": [_I, _I, _L, _I, _P, _P, _L, _L, _P, _P, _L, _L, _P],
@@ -221,7 +222,9 @@ def fastar_cache_compact(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm
 
 def fastar_cache_compact_sorted(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict,
                                 k_out, v_out, knorm_out, kb_out, len_out, index_map, B, kperm, koff, kpos, k_sorted,
-                                v_sorted, dev_status, stream=None):
+                                v_sorted, dev_status, stream=None, qb=None, qperm=None, qoff=None):
+    """qb [H, nq, r] int32 (optional): also sort the step's (query, slot) pairs by bucket
+    into qperm [H, nq*r] and qoff [H, B+1] in the same launch as the key sort."""
     H, nq, d = k_cur.shape
     hs, ts = tok_strides(k_cur)
     if tok_strides(v_cur) != (hs, ts):
@@ -229,7 +232,8 @@ def fastar_cache_compact_sorted(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in
     _call("fastar_cache_compact_sorted", dtype_code(k_cur.dtype), H, nq, d, k_in.shape[1], ptr(k_cur), ptr(v_cur),
           hs, ts, ptr(kcur_norm), ptr(kcur_bucket), ptr(k_in), ptr(v_in), ptr(knorm_in), ptr(kb_in), ptr(len_in),
           ptr(evict), ptr(k_out), ptr(v_out), ptr(knorm_out), ptr(kb_out), ptr(len_out), ptr(index_map), int(B),
-          ptr(kperm), ptr(koff), ptr(kpos), ptr(k_sorted), ptr(v_sorted), ptr(dev_status), stream_handle(stream))
+          ptr(kperm), ptr(koff), ptr(kpos), ptr(k_sorted), ptr(v_sorted), ptr(qb),
+          int(qb.shape[2]) if qb is not None else 0, ptr(qperm), ptr(qoff), ptr(dev_status), stream_handle(stream))
 
 
 def fastar_cache_compact_merge(k_cur, v_cur, kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, g_in, len_in,
@@ -313,13 +317,15 @@ def fastar_sparse_attn_grouped(q, r, B, qperm, qoff, k, v, kperm, koff, group_co
 
 
 def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, score=None, workspace=None,
-                        stream=None, B=0, qperm=None, qoff=None):
+                        stream=None, B=0, qperm=None, qoff=None, vp=None, kp_kept=None, vp_kept=None):
+    """kp_kept / vp_kept [H, F, P, d] (optional, with vp): the kept rows copied by the
+    ranking launch, fastar_cross_attn_kept's input."""
     H, nq, d = q.shape
     qh, qt = tok_strides(q)
     tpf = nq // F
     _call("fastar_annca_select", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2], ptr(kp),
           ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), int(B), ptr(qperm), ptr(qoff), ptr(keep),
-          ptr(kidx), ptr(kcnt), ptr(score),
+          ptr(kidx), ptr(kcnt), ptr(score), ptr(vp), ptr(kp_kept), ptr(vp_kept),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))
 
@@ -342,6 +348,15 @@ def fastar_cross_attn_subset(q, F, kp, vp, kidx, kcnt, scale, out, lse=None, str
     _call("fastar_cross_attn_subset", ptr(q), dtype_code(q.dtype), H, F, nq // F, d, qh, qt, ptr(kp), ptr(vp),
           kp.shape[1], ptr(kidx), ptr(kcnt), float(scale), ptr(out), oh, ot, ptr(lse), ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), stream_handle(stream))
+
+
+def fastar_cross_attn_kept(q, F, kp_kept, vp_kept, kcnt, scale, out, lse=None, stream=None):
+    """Cross-attention over the kept-row planes [H, F, P, d] fastar_annca_select wrote."""
+    H, nq, d = q.shape
+    qh, qt = tok_strides(q)
+    oh, ot = tok_strides(out)
+    _call("fastar_cross_attn_kept", ptr(q), dtype_code(q.dtype), H, F, nq // F, d, qh, qt, ptr(kp_kept),
+          ptr(vp_kept), kp_kept.shape[2], ptr(kcnt), float(scale), ptr(out), oh, ot, ptr(lse), stream_handle(stream))
 
 
 def fastar_dense_attn(q, k, v, nk, scale, out, lse=None, stream=None):

@@ -205,7 +205,8 @@ int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M, 
                                 const int32_t* len_in, const uint8_t* evict, void* k_out, void* v_out,
                                 float* knorm_out, int32_t* kb_out, int32_t* len_out, int32_t* index_map, int B,
                                 int32_t* kperm, int32_t* koff, int32_t* kpos, void* k_sorted, void* v_sorted,
-                                int32_t* dev_status, cudaStream_t stream) {
+                                const int32_t* qb, int r, int32_t* qperm, int32_t* qoff, int32_t* dev_status,
+                                cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || nq < 0 || M < 1 || M > INT32_MAX || B < 1) return FASTAR_EINVAL;
@@ -223,10 +224,16 @@ int fastar_cache_compact_sorted(int dtype, int H, int64_t nq, int d, int64_t M, 
     return FASTAR_EINVAL;
   if (k_in == k_out || v_in == v_out || knorm_in == knorm_out || kb_in == kb_out) return FASTAR_EINVAL;
   if (k_sorted == k_in || k_sorted == k_out || v_sorted == v_in || v_sorted == v_out) return FASTAR_EINVAL;
+  if (qb) {
+    if (r < 1) return FASTAR_EINVAL;
+    if (r > FASTAR_MAX_R || nq * r > INT32_MAX) return FASTAR_ECAPACITY;
+    if (!qperm || !qoff) return FASTAR_EINVAL;
+  }
   return cuda_rc(fastar::launch_cache_compact_sorted(
       dtype, d, H, nq, M, TokView{k_cur, head_stride, token_stride}, TokView{v_cur, head_stride, token_stride},
       kcur_norm, kcur_bucket, k_in, v_in, knorm_in, kb_in, len_in, evict, k_out, v_out, knorm_out, kb_out,
-      len_out, index_map, B, kperm, koff, kpos, k_sorted, v_sorted, dev_status, stream));
+      len_out, index_map, B, kperm, koff, kpos, k_sorted, v_sorted, qb, qb ? r : 0, qb ? qperm : nullptr,
+      qb ? qoff : nullptr, dev_status, stream));
 }
 
 int fastar_cache_compact_merge(int dtype, int H, int64_t nq, int d, int64_t M, const void* k_cur,
@@ -438,7 +445,8 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
                         int64_t q_token_stride, const int32_t* qb, int r, const void* kp, const int32_t* pb,
                         int64_t P, float tau_ca, int topk, int gate, int B, const int32_t* qperm,
                         const int32_t* qoff, uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                        const void* vp, void* kp_kept, void* vp_kept, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (B < 0 || B > FASTAR_MAX_B) return FASTAR_EINVAL;
@@ -451,6 +459,13 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
     if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, (int64_t)F * tpf, H))) return rc;
     if (tpf > 0 && !qb) return FASTAR_EINVAL;
     if (!kp || !aligned16(kp) || !pb || !keep || !kidx) return FASTAR_EINVAL;
+    if ((kp_kept != nullptr) != (vp_kept != nullptr)) return FASTAR_EINVAL;
+    if (kp_kept) {
+      if (dtype != FASTAR_BF16) return FASTAR_EUNSUPPORTED;
+      if (!vp || !aligned16(vp) || !aligned16(kp_kept) || !aligned16(vp_kept)) return FASTAR_EINVAL;
+      if (kp_kept == vp_kept || kp_kept == kp || kp_kept == vp || vp_kept == kp || vp_kept == vp)
+        return FASTAR_EINVAL;
+    }
     if (!score) {
       const size_t need = fastar::annca_workspace(H, F, P);
       if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FASTAR_EWORKSPACE;
@@ -458,7 +473,8 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
   }
   return cuda_rc(fastar::launch_annca_select(dtype, d, TokView{q, q_head_stride, q_token_stride}, H, F, tpf,
                                              qb, r, kp, pb, P, tau_ca, topk, gate, B, qperm, qoff, keep, kidx,
-                                             kcnt, score, workspace, stream));
+                                             kcnt, score, P > 0 ? vp : nullptr, P > 0 ? kp_kept : nullptr,
+                                             P > 0 ? vp_kept : nullptr, workspace, stream));
 }
 
 int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
@@ -499,6 +515,41 @@ int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf
     a.ksorted = reinterpret_cast<void*>(at);
     a.vsorted = reinterpret_cast<uint8_t*>(at) + plane;
   }
+  return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
+}
+
+int fastar_cross_attn_kept(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
+                           int64_t q_token_stride, const void* kp_kept, const void* vp_kept, int64_t P,
+                           const int32_t* kcnt, float scale, void* out, int64_t o_head_stride,
+                           int64_t o_token_stride, float* lse, cudaStream_t stream) {
+  int rc = check_dtype_d(dtype, d);
+  if (rc) return rc;
+  if (dtype != FASTAR_BF16) return FASTAR_EUNSUPPORTED;
+  if (H < 0 || F < 0 || tpf < 0 || P < 0) return FASTAR_EINVAL;
+  if (P > FASTAR_MAX_P) return FASTAR_ECAPACITY;
+  if (H == 0 || F == 0 || tpf == 0) return FASTAR_OK;
+  if ((rc = check_tok(q, dtype, d, q_head_stride, q_token_stride, (int64_t)F * tpf, H))) return rc;
+  if ((rc = check_tok(out, dtype, d, o_head_stride, o_token_stride, (int64_t)F * tpf, H))) return rc;
+  if (!kcnt) return FASTAR_EINVAL;
+  if (P > 0 && (!kp_kept || !vp_kept || !aligned16(kp_kept) || !aligned16(vp_kept))) return FASTAR_EINVAL;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return FASTAR_EINVAL;
+  fastar::AttnArgs a{};
+  a.mode = fastar::kCross;
+  a.H = H;
+  a.q = TokView{q, q_head_stride, q_token_stride};
+  a.nq = (int64_t)F * tpf;
+  a.F = F;
+  a.tpf = tpf;
+  a.kcnt = kcnt;
+  a.P = P;
+  a.scale = scale;
+  a.out = out;
+  a.o_hs = o_head_stride;
+  a.o_ts = o_token_stride;
+  a.lse = lse;
+  a.ksorted = const_cast<void*>(kp_kept);
+  a.vsorted = const_cast<void*>(vp_kept);
+  a.presorted = 1;
   return cuda_rc(fastar::launch_attention(dtype, d, a, stream));
 }
 

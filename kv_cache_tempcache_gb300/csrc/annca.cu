@@ -132,15 +132,32 @@ annca_score_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int64
   }
 }
 
-// One CTA per (head, frame): rank = #{p' : (s', p') precedes (s, p)} in the order
+// The kept rows' copy written beside the selection (all null otherwise): kp_kept /
+// vp_kept [H, F, P, d] receive, for each (head, frame), kp / vp rows kidx[0..kcnt) in
+// order, then zero rows up to the next multiple of 64 (at most P); cpr 16-byte chunks
+// per row.
+struct KeptPlanes {
+  const uint4* kp;
+  const uint4* vp;
+  uint4* kk;
+  uint4* vk;
+  int cpr;
+};
+
+// gridDim.y CTAs per (head, frame): rank = #{p' : (s', p') precedes (s, p)} in the order
 // (score desc, index asc), -inf last; keep = s >= tau_ca or rank < min(topk, P).
-// A (head, frame) holding a NaN score is not ranked: kcnt = -1, no token kept.
+// A (head, frame) holding a NaN score is not ranked: kcnt = -1, no token kept.  Every CTA
+// of a (head, frame) ranks (P scores: cheap); the first writes keep / kidx / kcnt and all
+// share the copy of the kept rows when planes are asked for.
 __global__ void __launch_bounds__(1024)
 annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restrict__ score,
-                  uint8_t* __restrict__ keep, int32_t* __restrict__ kidx, int32_t* __restrict__ kcnt) {
+                  uint8_t* __restrict__ keep, int32_t* __restrict__ kidx, int32_t* __restrict__ kcnt,
+                  const KeptPlanes kpl) {
   __shared__ float s[FASTAR_MAX_P];
+  __shared__ int kl[FASTAR_MAX_P];   // the kept list, ascending
   __shared__ int wsum[32];
   const int hf = blockIdx.x;
+  const bool lead = blockIdx.y == 0;
   const int p = threadIdx.x;
   const float* sc = score + (int64_t)hf * P;
   __shared__ int bad;
@@ -153,11 +170,11 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
   __syncthreads();
   if (bad) {
     // the (head, frame) cannot be ranked: no kept token, kcnt = -1 marks it
-    if (p < P) {
+    if (lead && p < P) {
       keep[(int64_t)hf * P + p] = 0;
       kidx[(int64_t)hf * P + p] = -1;
     }
-    if (p == 0) kcnt[hf] = -1;
+    if (lead && p == 0) kcnt[hf] = -1;
     return;
   }
   int k = 0;
@@ -175,7 +192,7 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
       }
       k = rank < lim ? 1 : 0;
     }
-    keep[(int64_t)hf * P + p] = (uint8_t)k;
+    if (lead) keep[(int64_t)hf * P + p] = (uint8_t)k;
   }
   // exclusive scan of the keep flags in index order
   const int lane = p & 31, warp = p >> 5;
@@ -202,12 +219,51 @@ annca_rank_kernel(int F, int64_t P, float tau_ca, int topk, const float* __restr
   __shared__ int total;
   if (p == blockDim.x - 1) total = pos + k;
   __syncthreads();
-  if (p < P) {
-    int32_t* out = kidx + (int64_t)hf * P;
-    if (k) out[pos] = p;
-    if (p >= total) out[p] = -1;
+  if (p < P && k) kl[pos] = p;
+  if (lead) {
+    if (p < P) {
+      int32_t* out = kidx + (int64_t)hf * P;
+      if (k) out[pos] = p;
+      if (p >= total) out[p] = -1;
+    }
+    if (p == 0) kcnt[hf] = total;
   }
-  if (p == 0) kcnt[hf] = total;
+  if (!kpl.kk) return;
+  __syncthreads();
+  // the kept rows of this (head, frame), then zero rows to the next 64-row boundary; the
+  // gridDim.y CTAs take interleaved 16-byte chunks, four in flight per thread
+  const int64_t lim = (int64_t)(total + 63) / 64 * 64 < P ? (int64_t)(total + 63) / 64 * 64 : P;
+  const int64_t chunks = lim * kpl.cpr;
+  const int64_t h = hf / F;
+  const uint4* ksrc = kpl.kp + h * P * kpl.cpr;
+  const uint4* vsrc = kpl.vp + h * P * kpl.cpr;
+  uint4* kdst = kpl.kk + (int64_t)hf * P * kpl.cpr;
+  uint4* vdst = kpl.vk + (int64_t)hf * P * kpl.cpr;
+  const int64_t step = (int64_t)gridDim.y * blockDim.x;
+  for (int64_t g0 = (int64_t)blockIdx.y * blockDim.x + p; g0 < chunks; g0 += 4 * step) {
+    uint4 kv[4], vv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t g = g0 + u * step;
+      kv[u] = vv[u] = make_uint4(0, 0, 0, 0);
+      if (g < chunks) {
+        const int64_t row = g / kpl.cpr;
+        if (row < total) {
+          const int64_t src = (int64_t)kl[row] * kpl.cpr + (g - row * kpl.cpr);
+          kv[u] = __ldg(ksrc + src);
+          vv[u] = __ldg(vsrc + src);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t g = g0 + u * step;
+      if (g < chunks) {
+        kdst[g] = kv[u];
+        vdst[g] = vv[u];
+      }
+    }
+  }
 }
 
 size_t annca_workspace(int H, int F, int64_t P) { return sizeof(float) * (size_t)H * F * P + 256; }
@@ -406,7 +462,8 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb,
                                 int r, const void* kp, const int32_t* pb, int64_t P, float tau_ca, int topk,
                                 int gate, int B, const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
-                                int32_t* kidx, int32_t* kcnt, float* score, void* ws, cudaStream_t s) {
+                                int32_t* kidx, int32_t* kcnt, float* score, const void* vp, void* kp_kept,
+                                void* vp_kept, void* ws, cudaStream_t s) {
   if (H == 0 || F == 0) return cudaSuccess;
   float* sc = score ? score : static_cast<float*>(ws);
   cudaError_t e = cudaSuccess;
@@ -423,7 +480,16 @@ cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64
   }
   int threads = (int)((P + 31) / 32 * 32);
   if (threads < 32) threads = 32;
-  annca_rank_kernel<<<H * F, threads, 0, s>>>(F, P, tau_ca, topk, sc, keep, kidx, kcnt);
+  KeptPlanes kpl{nullptr, nullptr, nullptr, nullptr, 0};
+  unsigned copiers = 1;
+  if (kp_kept && P > 0) {
+    const int esize = dtype == FASTAR_BF16 ? 2 : 4;
+    kpl = KeptPlanes{static_cast<const uint4*>(kp), static_cast<const uint4*>(vp), static_cast<uint4*>(kp_kept),
+                     static_cast<uint4*>(vp_kept), d * esize / 16};
+    copiers = 4;   // CTAs per (head, frame) sharing the copy of its kept rows
+  }
+  annca_rank_kernel<<<dim3((unsigned)(H * F), copiers), threads, 0, s>>>(F, P, tau_ca, topk, sc, keep, kidx, kcnt,
+                                                                         kpl);
   count_launches(1);
   return cudaGetLastError();
 }

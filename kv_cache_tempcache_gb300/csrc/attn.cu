@@ -341,6 +341,8 @@ static cudaError_t attn_impl(const AttnArgs& a, cudaStream_t s) {
     // bf16: the tensor-core kernels (for AnnSA: planning, attention, slot merge)
     if (launch_attn_tc(D, a, s)) return cudaGetLastError();
   }
+  // cross-attention over the caller's kept-row planes has no index list for this path
+  if (a.mode == kCross && a.presorted) return cudaErrorNotSupported;
   {
     AttnArgs b = a;
     kern<<<grid, 256, smem, s>>>(b);

@@ -1298,8 +1298,10 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
       const int64_t chunks = (int64_t)a.H * a.F * a.P * (D / 8);
       const int64_t blocks = (chunks + 255) / 256;
       if (blocks > 0 && blocks <= INT_MAX) {
-        cross_gather_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a);
-        count_launches(1);
+        if (!a.presorted) {   // (the caller's planes hold the kept rows already)
+          cross_gather_rows_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(a);
+          count_launches(1);
+        }
         b.kv_tma = 1;
         const int64_t nrow = (int64_t)a.F * a.tpf;
         const bool tmaj = a.H > 1 && a.q.hs < a.q.ts;
@@ -1333,6 +1335,8 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   }
   // group counts need the tensor-engine K/V path (the shifts are staged with its tiles)
   if (a.gcount && !b.kv_tma) return false;
+  // so do the caller's kept-row planes (there is no index list to gather by)
+  if (a.mode == kCross && a.presorted && !b.kv_tma) return false;
   if (a.mode == kSparse) {
     if (!a.items || !a.n_items) return false;
     if ((int64_t)a.H * a.B + 1 <= kPrefixMax) {

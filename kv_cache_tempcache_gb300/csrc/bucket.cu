@@ -6,8 +6,7 @@
 // buckets).  The centroid-argmax ANN is the method spec's fixed choice.
 #include <climits>
 
-#include <cooperative_groups.h>
-
+#include "cluster_sort.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -130,133 +129,25 @@ cudaError_t launch_bucket_assign_qk(int dtype, int d, TokView q, TokView k, int 
 }
 
 // ---------------------------------------------------------------------------------------
-// Stable counting sort: one thread-block cluster of kSortCtas CTAs per head.
-// CTA c of the cluster owns the c-th contiguous chunk of the head's element range and,
-// inside it, each warp a contiguous segment.  Pass 1 builds per-warp histograms (a
-// warp-level match gives each bucket one leader per batch of 32 elements).  The CTA's
-// histogram sits in its shared memory; after a cluster barrier every CTA reads all of
-// the cluster's histograms through distributed shared memory, which gives per bucket
-// the total (the bucket offsets) and the count in the chunks before its own.  Pass 2
-// replays the chunk and scatters each element to bucket offset + earlier chunks +
-// earlier warps + its rank among same-bucket lanes of the batch, so the order inside
-// a bucket is ascending element id.  Optionally each element's sorted position is written
-// too (the inverse permutation).  The CTAs of a cluster are co-scheduled by the
-// hardware and every thread executes both cluster barriers unconditionally.
+// Stable counting sort: one thread-block cluster of kSortCtas CTAs per head (the body is
+// cluster_counting_sort in cluster_sort.cuh, shared with the compaction's plan kernel).
 // ---------------------------------------------------------------------------------------
-constexpr int kSortCtas = 8;
-constexpr int kSortWarpsC = 8;
-constexpr int kSortStage = 8192;   // ids of a chunk staged in shared memory when they fit
-
 __global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortWarpsC * 32)
 bucket_sort_kernel(const int32_t* __restrict__ ids, int64_t n, int r, int B, const int32_t* __restrict__ n_valid,
                    int32_t* __restrict__ perm, int32_t* __restrict__ offsets, int32_t* __restrict__ inv,
                    int32_t* status) {
-  namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
-  __shared__ int cnt[kSortWarpsC][FASTAR_MAX_B];
-  __shared__ int hist[FASTAR_MAX_B];
-  __shared__ int base[FASTAR_MAX_B];
-  __shared__ int wsum[kSortWarpsC];
-  __shared__ int ids_s[kSortStage];
-  const int c = (int)cluster.block_rank();
+  __shared__ SortSmem sm;
   const int h = blockIdx.x / kSortCtas;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   int64_t nv = n;
   if (n_valid) {
     nv = n_valid[h];
     if (nv < 0 || nv > n) {
-      if (t == 0 && c == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
+      if (threadIdx.x == 0 && blockIdx.x % kSortCtas == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
       nv = nv < 0 ? 0 : n;
     }
   }
-  const int64_t E = nv * r;
-  const int64_t per = (E + kSortCtas - 1) / kSortCtas;
-  const int64_t cb = (int64_t)c * per < E ? (int64_t)c * per : E;
-  const int64_t ce = cb + per < E ? cb + per : E;
-  const int32_t* id = ids + (int64_t)h * n * r;
-  int32_t* out = perm + (int64_t)h * n * r;
-  int32_t* where = inv ? inv + (int64_t)h * n * r : nullptr;   // element -> its sorted position
-  for (int i = t; i < kSortWarpsC * FASTAR_MAX_B; i += blockDim.x) (&cnt[0][0])[i] = 0;
-  const bool staged = ce - cb <= kSortStage;
-  if (staged)
-    for (int64_t e = cb + t; e < ce; e += blockDim.x) ids_s[e - cb] = id[e];
-  __syncthreads();
-  auto bucket_of = [&](int64_t e) -> int { return staged ? ids_s[e - cb] : id[e]; };
-  const int64_t wseg = (ce - cb + kSortWarpsC - 1) / kSortWarpsC;
-  const int64_t wb = cb + warp * wseg < ce ? cb + warp * wseg : ce;
-  const int64_t we = wb + wseg < ce ? wb + wseg : ce;
-  for (int64_t bse = wb; bse < we; bse += 32) {
-    const int64_t e = bse + lane;
-    int b = e < we ? bucket_of(e) : -1;
-    if (e < we && (b < 0 || b >= B)) {
-      flag_status(status, FASTAR_DEV_BAD_BUCKET);
-      b = -1;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    if (b >= 0 && lane == __ffs(peers) - 1) cnt[warp][b] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  if (t < B) {
-    int sum = 0;
-#pragma unroll
-    for (int w = 0; w < kSortWarpsC; ++w) sum += cnt[w][t];
-    hist[t] = sum;
-  }
-  cluster.sync();   // every CTA's histogram is complete
-  int total = 0, before = 0;
-  if (t < B) {
-    for (int k = 0; k < kSortCtas; ++k) {
-      const int v = cluster.map_shared_rank(hist, k)[t];
-      total += v;
-      if (k < c) before += v;
-    }
-  }
-  cluster.sync();   // no CTA leaves (its histogram) while another may still read it
-  // exclusive scan of the bucket totals (B <= blockDim.x)
-  int incl = total;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int wpre = 0;
-  for (int w = 0; w < warp; ++w) wpre += wsum[w];
-  const int off = wpre + incl - total;
-  if (t < B) {
-    base[t] = off + before;
-    if (c == 0) offsets[(int64_t)h * (B + 1) + t] = off;
-  }
-  if (c == 0 && t == B - 1) offsets[(int64_t)h * (B + 1) + B] = off + total;
-  __syncthreads();
-  if (t < B) {
-    int acc = base[t];
-#pragma unroll
-    for (int w = 0; w < kSortWarpsC; ++w) {
-      const int x = cnt[w][t];
-      cnt[w][t] = acc;
-      acc += x;
-    }
-  }
-  __syncthreads();
-  for (int64_t bse = wb; bse < we; bse += 32) {
-    const int64_t e = bse + lane;
-    int b = e < we ? bucket_of(e) : -1;
-    if (b >= B || b < -1) b = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    int start = 0;
-    if (b >= 0) start = cnt[warp][b];
-    __syncwarp();
-    if (b >= 0) {
-      const int dst = start + __popc(peers & ((1u << lane) - 1u));
-      out[dst] = (int32_t)e;
-      if (where) where[e] = dst;
-      if (lane == __ffs(peers) - 1) cnt[warp][b] = start + __popc(peers);
-    }
-    __syncwarp();
-  }
+  cluster_counting_sort(sm, ids + (int64_t)h * n * r, nv * r, B, perm + (int64_t)h * n * r,
+                        offsets + (int64_t)h * (B + 1), inv ? inv + (int64_t)h * n * r : nullptr, status);
 }
 
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,

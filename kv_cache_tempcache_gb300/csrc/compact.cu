@@ -6,11 +6,13 @@
 // the method spec's.
 //
 // Two kernels: a one-CTA-per-head scan that writes the slot -> source map and the
-// new length, then a bandwidth kernel that moves rows with 16-byte accesses.  In the
-// sorted form the scan also writes the new cache's bucket ids and their stable counting
-// sort runs between the two, so that the copy can also write each row to its place in a
-// bucket-ordered copy (the layout the bucket-restricted attention reads as contiguous
-// tiles).
+// new length, then a bandwidth kernel that moves rows with 16-byte accesses.  The sorted
+// form plans with one thread-block cluster per head instead: the survivor scan across
+// the cluster's CTAs (chunk totals exchanged through distributed shared memory), the new
+// slots' bucket ids, their stable counting sort, and optionally the step's (query, slot)
+// pairs' counting sort as well, so that the copy can also write each row to its place in
+// a bucket-ordered copy (the layout the bucket-restricted attention reads as contiguous
+// tiles) and the step needs no separate sort launch.
 //
 // The merge variant (technical summary §2.A, Theoretical Basis: Lemma 5.1 — identical
 // keys merge exactly when their values are averaged and the logit is shifted by the
@@ -18,6 +20,7 @@
 // owner, the lowest current entry i that evicted it, whose value becomes
 // (v_i + g_j v_j) / (1 + g_j) and whose count becomes 1 + g_j; i's key stays.  The slot
 // order is the replace variant's.
+#include "cluster_sort.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,14 +29,11 @@ namespace fastar {
 constexpr int kScanThreads = 1024;
 
 // Slot s of the new cache takes: survivor number (s + drop) if s + drop < S, else
-// current token (s + drop - S); drop = max(0, S + nq - M).  With kbout the slot's bucket
-// id is written too (the source entry's), so that the key sort can run before the rows
-// move.
+// current token (s + drop - S); drop = max(0, S + nq - M).
 __global__ void __launch_bounds__(kScanThreads)
 compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
                     const uint8_t* __restrict__ evict, int32_t* __restrict__ len_out,
-                    int32_t* __restrict__ index_map, int32_t* status, const int32_t* __restrict__ kcb = nullptr,
-                    const int32_t* __restrict__ kbin = nullptr, int32_t* __restrict__ kbout = nullptr) {
+                    int32_t* __restrict__ index_map, int32_t* status) {
   __shared__ int warp_tot[kScanThreads / 32];
   __shared__ int s_total;
   const int h = blockIdx.x;
@@ -76,27 +76,110 @@ compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
   const int64_t drop = total > M ? total - M : 0;
   const int64_t L = total - drop;
   int64_t rank = warp_tot[warp] + incl - local;
-  const int32_t* kbi = kbin ? kbin + (int64_t)h * M : nullptr;
-  int32_t* kbo = kbout ? kbout + (int64_t)h * M : nullptr;
   for (int64_t j = beg; j < end; ++j) {
     if (!e[j]) {
       const int64_t slot = rank - drop;
-      if (slot >= 0) {
-        imap[slot] = (int32_t)j;
-        if (kbo) kbo[slot] = kbi[j];
-      }
+      if (slot >= 0) imap[slot] = (int32_t)j;
       ++rank;
     }
   }
   for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
     const int64_t slot = S + i - drop;
-    if (slot >= 0) {
-      imap[slot] = (int32_t)(n + i);
-      if (kbo) kbo[slot] = kcb[(int64_t)h * nq + i];
-    }
+    if (slot >= 0) imap[slot] = (int32_t)(n + i);
   }
   for (int64_t s = L + threadIdx.x; s < M; s += blockDim.x) imap[s] = -1;
   if (threadIdx.x == 0) len_out[h] = (int32_t)L;
+}
+
+// The sorted compaction's plan, one cluster of kSortCtas CTAs per head (every thread of
+// every CTA runs every phase, so the cluster barriers always fill):
+//   (optional) the stable counting sort of the (query, slot) pairs' buckets qb -> qperm, qoff;
+//   the survivor scan: slot s takes survivor number (s + drop) if s + drop < S, else current
+//   token (s + drop - S), drop = max(0, S + nq - M); writes index_map, len_out and the new
+//   slots' bucket ids kbout (the source entry's);
+//   the stable counting sort of kbout over the len_out slots -> kperm, koff, kpos.
+__global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortWarpsC * 32)
+compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, const uint8_t* __restrict__ evict,
+                    int32_t* __restrict__ len_out, int32_t* __restrict__ index_map, const int32_t* __restrict__ kcb,
+                    const int32_t* __restrict__ kbin, int32_t* __restrict__ kbout, int B, int32_t* __restrict__ kperm,
+                    int32_t* __restrict__ koff, int32_t* __restrict__ kpos, const int32_t* __restrict__ qb, int r,
+                    int32_t* __restrict__ qperm, int32_t* __restrict__ qoff, int32_t* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ SortSmem sm;
+  __shared__ int warp_tot[kSortWarpsC];
+  __shared__ int cta_tot;
+  const int c = (int)cluster.block_rank();
+  const int h = blockIdx.x / kSortCtas;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  constexpr int kT = kSortWarpsC * 32;
+  if (qb)
+    cluster_counting_sort(sm, qb + (int64_t)h * nq * r, nq * r, B, qperm + (int64_t)h * nq * r,
+                          qoff + (int64_t)h * (B + 1), nullptr, status);
+  // ---- survivor scan: CTA c owns a contiguous chunk, each thread a contiguous piece ----
+  int64_t n = len_in[h];
+  if (n < 0 || n > M) {
+    if (t == 0 && c == 0) flag_status(status, FASTAR_DEV_BAD_LEN);
+    n = n < 0 ? 0 : M;
+  }
+  const uint8_t* e = evict + (int64_t)h * M;
+  const int64_t cper = (n + kSortCtas - 1) / kSortCtas;
+  const int64_t cb = (int64_t)c * cper < n ? (int64_t)c * cper : n;
+  const int64_t ce = cb + cper < n ? cb + cper : n;
+  const int64_t tper = (ce - cb + kT - 1) / kT;
+  const int64_t beg = cb + t * tper < ce ? cb + t * tper : ce;
+  const int64_t end = beg + tper < ce ? beg + tper : ce;
+  int local = 0;
+  for (int64_t j = beg; j < end; ++j) local += e[j] ? 0 : 1;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int wpre = 0;
+  for (int w = 0; w < warp; ++w) wpre += warp_tot[w];
+  if (t == kT - 1) cta_tot = wpre + incl;
+  cluster.sync();   // every CTA's survivor count is published
+  int64_t S = 0, before = 0;
+  for (int k = 0; k < kSortCtas; ++k) {
+    const int v = *cluster.map_shared_rank(&cta_tot, k);
+    S += v;
+    if (k < c) before += v;
+  }
+  const int64_t total = S + nq;
+  const int64_t drop = total > M ? total - M : 0;
+  const int64_t L = total - drop;
+  int32_t* imap = index_map + (int64_t)h * M;
+  const int32_t* kbi = kbin + (int64_t)h * M;
+  int32_t* kbo = kbout + (int64_t)h * M;
+  int64_t rank = before + wpre + incl - local;
+  for (int64_t j = beg; j < end; ++j) {
+    if (!e[j]) {
+      const int64_t slot = rank - drop;
+      if (slot >= 0) {
+        imap[slot] = (int32_t)j;
+        kbo[slot] = kbi[j];
+      }
+      ++rank;
+    }
+  }
+  for (int64_t i = (int64_t)c * kT + t; i < nq; i += (int64_t)kSortCtas * kT) {
+    const int64_t slot = S + i - drop;
+    if (slot >= 0) {
+      imap[slot] = (int32_t)(n + i);
+      kbo[slot] = kcb[(int64_t)h * nq + i];
+    }
+  }
+  for (int64_t s2 = L + (int64_t)c * kT + t; s2 < M; s2 += (int64_t)kSortCtas * kT) imap[s2] = -1;
+  if (t == 0 && c == 0) len_out[h] = (int32_t)L;
+  // the slots' bucket ids are written (global memory, ordered by the barrier's release and
+  // acquire) and no CTA reads cta_tot any more
+  cluster.sync();
+  cluster_counting_sort(sm, kbo, L, B, kperm + (int64_t)h * M, koff + (int64_t)h * (B + 1), kpos + (int64_t)h * M,
+                        status);
 }
 
 // The group-merge inputs and outputs of the merge variant (all null otherwise).
@@ -268,13 +351,15 @@ cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int
                                         const uint8_t* evict, void* kout, void* vout, float* knout,
                                         int32_t* kbout, int32_t* len_out, int32_t* imap, int B, int32_t* kperm,
                                         int32_t* koff, int32_t* kpos, void* ksorted, void* vsorted,
-                                        int32_t* status, cudaStream_t s) {
-  // the scan also writes the new slots' bucket ids (the key sort's input)
-  compact_scan_kernel<<<H, kScanThreads, 0, s>>>(nq, M, len_in, evict, len_out, imap, status, kcb, kbin, kbout);
+                                        const int32_t* qb, int r, int32_t* qperm, int32_t* qoff, int32_t* status,
+                                        cudaStream_t s) {
+  // one cluster per head plans the step: the query pairs' sort, the survivor scan with
+  // the new slots' bucket ids, and the key sort
+  compact_plan_kernel<<<H * kSortCtas, kSortWarpsC * 32, 0, s>>>(nq, M, len_in, evict, len_out, imap, kcb, kbin,
+                                                                 kbout, B, kperm, koff, kpos, qb, r, qperm, qoff,
+                                                                 status);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = launch_bucket_sort(kbout, H, M, 1, B, len_out, kperm, koff, status, s, kpos);
   if (e != cudaSuccess) return e;
   const MergeIO mg{nullptr, nullptr, nullptr, nullptr};
   const SortedIO so{kpos, ksorted, vsorted};

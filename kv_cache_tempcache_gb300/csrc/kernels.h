@@ -73,15 +73,17 @@ cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M,
                                  int32_t* g_out, cudaStream_t s);
 
 // The compaction that also leaves AnnSA's input ready: the new cache's bucket ids, their
-// stable counting sort (kperm, koff, and kpos = each slot's position in bucket order) and
-// a bucket-ordered copy of the new K/V rows (ksorted, vsorted), written as the rows move.
+// stable counting sort (kperm, koff, and kpos = each slot's position in bucket order), a
+// bucket-ordered copy of the new K/V rows (ksorted, vsorted), written as the rows move,
+// and (qb non-null) the (query, slot) pairs' counting sort (qperm, qoff): two launches.
 cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int64_t M, TokView kc, TokView vc,
                                         const float* kcn, const int32_t* kcb, const void* kin, const void* vin,
                                         const float* knin, const int32_t* kbin, const int32_t* len_in,
                                         const uint8_t* evict, void* kout, void* vout, float* knout,
                                         int32_t* kbout, int32_t* len_out, int32_t* imap, int B, int32_t* kperm,
                                         int32_t* koff, int32_t* kpos, void* ksorted, void* vsorted,
-                                        int32_t* status, cudaStream_t s);
+                                        const int32_t* qb, int r, int32_t* qperm, int32_t* qoff, int32_t* status,
+                                        cudaStream_t s);
 
 // ---- attention ------------------------------------------------------------------------
 enum AttnMode { kDense = 0, kCross = 1, kSparse = 2, kMatchAnn = 3 };
@@ -119,6 +121,7 @@ struct AttnArgs {
   void* ksorted;    // sparse: the cache K/V rows in bucket order [H, M, d] (tensor-core path)
   void* vsorted;
   int presorted;    // sparse: ksorted / vsorted already hold that copy (the caller's buffers)
+                    // cross: ksorted / vsorted are the caller's kept-row planes [H, F, P, d]
   int kv_tma;       // keys/values arrive as contiguous TMA tiles (set by the launcher)
   int q_tma;        // so do the query tiles: one thread drives every copy (set by the launcher)
   int q_token_major;  // the query tensor map is (d, H, tokens) rather than (d, tokens, H)
@@ -163,8 +166,8 @@ cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64
                                 const int32_t* qb, int r, const void* kp, const int32_t* pb,
                                 int64_t P, float tau_ca, int topk, int gate, int B,
                                 const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
-                                int32_t* kidx, int32_t* kcnt, float* score, void* ws,
-                                cudaStream_t s);
+                                int32_t* kidx, int32_t* kcnt, float* score, const void* vp,
+                                void* kp_kept, void* vp_kept, void* ws, cudaStream_t s);
 
 // ---- the transformer around the attention step ----------------------------------------
 cudaError_t launch_gemm_tc(const void* A, int64_t lda, const void* W, int64_t ldw, const float* bias,

@@ -130,7 +130,13 @@ class FastARLayer:
 
         self.ws_match = ws(L.OP_MATCH, n=Nq, M=M, d=d)
         self.ws_attn = ws(L.OP_SPARSE_ATTN, n=Nq, M=M, d=d, B=B, r=r)
-        self.ws_cross = ws(L.OP_CROSS_ATTN, n=0, d=d, P=P, F=F) if P > 0 else None
+        # bf16: the selection's ranking launch copies the kept prompt rows into per-frame
+        # planes, which the cross-attention reads as tiles (no gather launch of its own)
+        self.kept = dtype == torch.bfloat16 and P > 0
+        self.ws_cross = ws(L.OP_CROSS_ATTN, n=0, d=d, P=P, F=F) if P > 0 and not self.kept else None
+        if self.kept:
+            self.kp_kept = torch.zeros((H, F, P, d), dtype=dtype, device=dev)
+            self.vp_kept = torch.zeros((H, F, P, d), dtype=dtype, device=dev)
         if self.pq:
             m, Kc = self.pq
             self.codebooks = torch.zeros((H, m, Kc, d // m), dtype=dtype, device=dev)
@@ -245,10 +251,13 @@ class FastARLayer:
             t("pq_encode", main, "begin")
             L.fastar_pq_encode(k_cur, self.codebooks, self.codes_cur)
             t("pq_encode", main, "end")
-        # the (query, slot) pairs by bucket serve both AnnSA and AnnCA
-        t("bucket_sort_q", main, "begin")
-        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
-        t("bucket_sort_q", main, "end")
+        # the (query, slot) pairs by bucket: AnnSA's query-side order (the sorted compaction
+        # writes it in its own planning launch; the other paths sort here, where AnnCA's
+        # SIMT scorer can use it too)
+        if not self.presort:
+            t("bucket_sort_q", main, "begin")
+            L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+            t("bucket_sort_q", main, "end")
         # AnnCA branch on the side stream
         if not serial:
             ev = torch.cuda.Event()
@@ -256,13 +265,10 @@ class FastARLayer:
             side.wait_event(ev)
         with torch.cuda.stream(side):
             t("annca_select", side, "begin")
-            L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate,
-                                  self.keep, self.kidx, self.kcnt, self.score, B=self.B, qperm=self.qperm,
-                                  qoff=self.qoff)
+            self._annca(q, self.qperm if not self.presort else None, self.qoff if not self.presort else None)
             t("annca_select", side, "end")
             t("cross_attn_subset", side, "begin")
-            L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale,
-                                       self.o_cross, self.lse_cross, workspace=self.ws_cross)
+            self._cross(q, self.o_cross)
             t("cross_attn_subset", side, "end")
         # TempCache + AnnSA on the main stream
         if early:
@@ -278,7 +284,8 @@ class FastARLayer:
             L.fastar_cache_compact_sorted(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                           cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
                                           self.index_map, self.B, self.kperm, self.koff, self.kpos, self.k_sorted,
-                                          self.v_sorted, self.dev_status)
+                                          self.v_sorted, self.dev_status, qb=self.qb, qperm=self.qperm,
+                                          qoff=self.qoff)
         else:
             L.fastar_cache_compact(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                    cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
@@ -318,14 +325,16 @@ class FastARLayer:
         cin, cout = self.caches[self.cur], self.caches[1 - self.cur]
         o = self.o_self if out is None else out
         L.fastar_bucket_assign_qk(q, k_cur, self.centroids, self.r, self.qb, self.kb_cur, self.kcur_norm)
-        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        if not self.presort:
+            L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
         L.fastar_tempcache_match(q, k_cur, cin.k, cin.knorm, cin.len, self.tau, self.top1, self.s1, None,
                                  self.evict, self.dev_status, self.ws_match)
         if self.presort:
             L.fastar_cache_compact_sorted(k_cur, v_cur, self.kcur_norm, self.kb_cur, cin.k, cin.v, cin.knorm, cin.kb,
                                           cin.len, self.evict, cout.k, cout.v, cout.knorm, cout.kb, cout.len,
                                           self.index_map, self.B, self.kperm, self.koff, self.kpos, self.k_sorted,
-                                          self.v_sorted, self.dev_status)
+                                          self.v_sorted, self.dev_status, qb=self.qb, qperm=self.qperm,
+                                          qoff=self.qoff)
             L.fastar_sparse_attn_presorted(q, self.r, self.B, self.qperm, self.qoff, cout.k, cout.v, self.kperm,
                                            self.koff, self.k_sorted, self.v_sorted, self.scale, o, self.lse_self,
                                            self.dev_status, self.ws_attn)
@@ -345,12 +354,27 @@ class FastARLayer:
         frame-relevant prompt tokens, cross-attention over them -> out (default o_cross)."""
         o = self.o_cross if out is None else out
         L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
-        L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
-        L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate, self.keep,
-                              self.kidx, self.kcnt, self.score, B=self.B, qperm=self.qperm, qoff=self.qoff)
-        L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale, o,
-                                   self.lse_cross, workspace=self.ws_cross)
+        # the bf16 scorer masks dense tiles with qb itself; the bucket order helps the SIMT one
+        order = q.dtype != torch.bfloat16
+        if order:
+            L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
+        self._annca(q, self.qperm if order else None, self.qoff if order else None)
+        self._cross(q, o)
         return o
+
+    def _annca(self, q, qperm, qoff):
+        """The prompt selection for queries q (and, in bf16, the kept rows' planes)."""
+        kw = dict(vp=self.vp, kp_kept=self.kp_kept, vp_kept=self.vp_kept) if self.kept else {}
+        L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate, self.keep,
+                              self.kidx, self.kcnt, self.score, B=self.B, qperm=qperm, qoff=qoff, **kw)
+
+    def _cross(self, q, o):
+        """Cross-attention of q over the kept prompt tokens -> o."""
+        if self.kept:
+            L.fastar_cross_attn_kept(q, self.F, self.kp_kept, self.vp_kept, self.kcnt, self.scale, o, self.lse_cross)
+        else:
+            L.fastar_cross_attn_subset(q, self.F, self.kp, self.vp, self.kidx, self.kcnt, self.scale, o,
+                                       self.lse_cross, workspace=self.ws_cross)
 
     def step(self, q, k_cur, v_cur, advance: bool = True, timer=None, serial: bool = False):
         """Runs one chunk step (asynchronously, on the current stream).  With

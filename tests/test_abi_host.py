@@ -82,12 +82,29 @@ def test_argument_validation_rejects_before_launch(lib):
                                   0.1, FAKE, 8192, 128, None, None, FAKE, 16, s) == L.EWORKSPACE
     # prompt beyond the limit
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 2000, 0.2, 16, 1,
-                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.ECAPACITY
+                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.ECAPACITY
     # a bucket order needs the bucket count, and both of its arrays
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
+                                   0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   8, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, 0, s) == L.EINVAL
+                                   8, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
+    # kept-row planes: both or neither, with the values, bf16 only
+    assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
+                                   0, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4096, None, None, 0,
+                                   s) == L.EINVAL
+    assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
+                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, FAKE + 8192, None, 0,
+                                   s) == L.EINVAL
+    assert lib.fastar_annca_select(FAKE, L.F32, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
+                                   0, None, None, FAKE, FAKE, FAKE, FAKE, FAKE + 2048, FAKE + 4096, FAKE + 8192, None,
+                                   0, s) == L.EUNSUPPORTED
+    # the cross-attention over planes: bf16 planes, present and aligned
+    assert lib.fastar_cross_attn_kept(FAKE, L.F32, 1, 1, 64, 128, 8192, 128, FAKE, FAKE, 100, FAKE, 0.1, FAKE, 8192,
+                                      128, None, s) == L.EUNSUPPORTED
+    assert lib.fastar_cross_attn_kept(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, None, FAKE, 100, FAKE, 0.1, FAKE, 8192,
+                                      128, None, s) == L.EINVAL
+    assert lib.fastar_cross_attn_kept(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, FAKE + 8, 100, FAKE, 0.1, FAKE,
+                                      8192, 128, None, s) == L.EINVAL
     # merge variant: the group counts are required, and compaction stays out-of-place for them too
     assert lib.fastar_cache_compact_merge(L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE,
                                           FAKE + 16, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE + 32, FAKE + 48,
@@ -106,14 +123,22 @@ def test_argument_validation_rejects_before_launch(lib):
     # the sorted compaction needs its sorted copies, distinct from the caches, and a bucket count
     base = [L.BF16, 1, 10, 128, 50, FAKE, FAKE, 1280, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
             FAKE + 1024, FAKE + 2048, FAKE + 16, FAKE + 32, FAKE + 48, FAKE + 64]
-    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, None, FAKE + 4096, None, s) == L.EINVAL
-    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 8, FAKE + 4096, None, s) == L.EINVAL
-    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 1024, FAKE + 4096, None,
+    noq = [None, 0, None, None]   # no (query, slot) pair sort
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, None, FAKE + 4096, *noq, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 8, FAKE + 4096, *noq, None,
                                            s) == L.EINVAL
-    assert lib.fastar_cache_compact_sorted(*base, 0, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, None,
+    assert lib.fastar_cache_compact_sorted(*base, 8, FAKE, FAKE, FAKE, FAKE + 1024, FAKE + 4096, *noq, None,
                                            s) == L.EINVAL
-    assert lib.fastar_cache_compact_sorted(*base, 300, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, None,
+    assert lib.fastar_cache_compact_sorted(*base, 0, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, *noq, None,
+                                           s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, 300, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096, *noq, None,
                                            s) == L.ECAPACITY
+    # with the pair sort: r in [1, FASTAR_MAX_R] and both outputs
+    ok = [8, FAKE, FAKE, FAKE, FAKE + 3072, FAKE + 4096]
+    assert lib.fastar_cache_compact_sorted(*base, *ok, FAKE, 0, FAKE, FAKE, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, *ok, FAKE, 2, None, FAKE, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, *ok, FAKE, 2, FAKE, None, None, s) == L.EINVAL
+    assert lib.fastar_cache_compact_sorted(*base, *ok, FAKE, 99, FAKE, FAKE, None, s) == L.ECAPACITY
     # the presorted attention needs both sorted copies, 16-byte aligned
     assert lib.fastar_sparse_attn_presorted(FAKE, L.BF16, 1, 64, 128, 8192, 128, 2, 8, FAKE, FAKE, FAKE, FAKE,
                                             128, FAKE, FAKE, None, FAKE, 0.1, FAKE, 8192, 128, None, None, FAKE,

@@ -2,8 +2,10 @@
 keys grouped by bucket, and a bucket-ordered copy of its K/V rows), through the C ABI,
 against the oracle bit for bit: the cache order from compact_plan / gather_rows, the
 bucket order from bucket_order, and every sorted row equal to the new cache's row at
-its kperm entry.  The attention that reads the caller's sorted copy must give exactly
-what the entry that makes its own copy gives."""
+its kperm entry.  The step's (query, slot) pairs, sorted in the same planning launch,
+must be bucket_order's too, and equal to the stand-alone sort's.  The attention that
+reads the caller's sorted copy must give exactly what the entry that makes its own copy
+gives."""
 import numpy as np
 import pytest
 import torch
@@ -60,12 +62,21 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens, d, dtype):
     k_sorted = torch.zeros((H, M, d), dtype=tdt, device="cuda")
     v_sorted = torch.zeros((H, M, d), dtype=tdt, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = 2
+    qb_h = rng.integers(0, B, size=(H, nq, r))
+    qb = _i32(qb_h)
+    qperm_c = torch.full((H, nq * r), -5, dtype=torch.int32, device="cuda")
+    qoff_c = torch.full((H, B + 1), -5, dtype=torch.int32, device="cuda")
     L.fastar_cache_compact_sorted(dev["k_cur"], dev["v_cur"], dev["kcur_norm"], dev["kcur_bucket"], dev["k_in"],
                                   dev["v_in"], dev["knorm_in"], dev["kb_in"], dev["len_in"], dev["evict"],
                                   out["k_out"], out["v_out"], out["knorm_out"], out["kb_out"], out["len_out"],
-                                  out["index_map"], B, kperm, koff, kpos, k_sorted, v_sorted, status)
+                                  out["index_map"], B, kperm, koff, kpos, k_sorted, v_sorted, status, qb=qb,
+                                  qperm=qperm_c, qoff=qoff_c)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    want_qperm, want_qoff = O.bucket_order(qb_h, B)
+    np.testing.assert_array_equal(_np(qperm_c), want_qperm)
+    np.testing.assert_array_equal(_np(qoff_c), want_qoff)
     g = {k: _np(v) for k, v in out.items()}
     kperm_g, koff_g, ks_g, vs_g = _np(kperm), _np(koff), _np(k_sorted), _np(v_sorted)
     kin_b, vin_b = rnd(k_in), rnd(v_in)
@@ -93,12 +104,12 @@ def test_sorted_compaction_matches_oracle(H, M, nq, B, lens, d, dtype):
         np.testing.assert_array_equal(vs_g[h, :length], g["v_out"][h, want_perm[h, :length]])
 
     # the attention that reads this copy equals the one that makes its own, bit for bit
-    r = 2
     q = _rows(rng.standard_normal((H, nq, d)).astype(np.float32))
-    qb = _i32(rng.integers(0, B, size=(H, nq, r)))
     qperm = torch.zeros((H, nq * r), dtype=torch.int32, device="cuda")
     qoff = torch.zeros((H, B + 1), dtype=torch.int32, device="cuda")
     L.fastar_bucket_sort(qb, B, qperm, qoff, None, status)
+    torch.cuda.synchronize()
+    assert torch.equal(qperm, qperm_c) and torch.equal(qoff, qoff_c)
     ws = torch.zeros(L.workspace_bytes(L.OP_SPARSE_ATTN, H, n=nq, M=M, d=d, B=B, r=r), dtype=torch.uint8,
                      device="cuda")
     res = []

@@ -196,9 +196,11 @@ def test_rollout_matches_oracle_chunk_by_chunk():
 
 @pytest.mark.parametrize("P,d", [(100, 128), (8, 64), (512, 128)])
 def test_cross_attention_paths_agree_bit_for_bit(P, d):
-    """The kept prompt rows read in place (no workspace) or gathered into contiguous
-    planes and read by the tensor engine (workspace): same rows, same order, so the
-    same bits; both against the oracle."""
+    """The kept prompt rows read in place (no workspace), gathered into contiguous planes
+    and read by the tensor engine (workspace), or read from the planes the selection's
+    ranking launch wrote (fastar_cross_attn_kept, the layer's path): same rows, same order,
+    so the same bits; against the oracle.  The planes hold exactly the kept rows, then
+    zero rows to the next 64-row boundary."""
     from kv_cache_tempcache_gb300 import _lib as L
     cfg = GH.small_bf16().replace(P=P, d=d, topk=min(16, P))
     inputs = synth.layer_step_inputs(cfg, seed=6)
@@ -206,15 +208,29 @@ def test_cross_attention_paths_agree_bit_for_bit(P, d):
     g, layer = GH.gpu_step(cfg, inputs, ck, cv)
     q = GH.to_dev(inputs["q"], cfg)
     outs = []
-    for ws in (None, layer.ws_cross):
+    ws = torch.zeros(L.workspace_bytes(L.OP_CROSS_ATTN, cfg.H, n=0, d=d, P=P, F=cfg.F), dtype=torch.uint8,
+                     device="cuda")
+    for path in ("in_place", "workspace", "planes"):
         o = torch.zeros_like(q)
         lse = torch.zeros(q.shape[:2], dtype=torch.float32, device="cuda")
-        L.fastar_cross_attn_subset(q, cfg.F, layer.kp, layer.vp, layer.kidx, layer.kcnt, cfg.scale, o, lse,
-                                   workspace=ws)
+        if path == "planes":
+            L.fastar_cross_attn_kept(q, cfg.F, layer.kp_kept, layer.vp_kept, layer.kcnt, cfg.scale, o, lse)
+        else:
+            L.fastar_cross_attn_subset(q, cfg.F, layer.kp, layer.vp, layer.kidx, layer.kcnt, cfg.scale, o, lse,
+                                       workspace=ws if path == "workspace" else None)
         torch.cuda.synchronize()
         outs.append((GH.np_(o), GH.np_(lse)))
-    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
-    assert np.array_equal(outs[1][0], g["o_cross"])
+    for i in (1, 2):
+        assert np.array_equal(outs[0][0], outs[i][0]) and np.array_equal(outs[0][1], outs[i][1])
+    assert np.array_equal(outs[2][0], g["o_cross"])
+    kp, vp = GH.np_(layer.kp), GH.np_(layer.vp)
+    kpk, vpk = GH.np_(layer.kp_kept), GH.np_(layer.vp_kept)
+    for h in range(cfg.H):
+        for f in range(cfg.F):
+            idx = np.flatnonzero(g["keep"][h][f])
+            n, lim = len(idx), min(P, -(-len(idx) // 64) * 64)
+            assert np.array_equal(kpk[h, f, :n], kp[h, idx]) and np.array_equal(vpk[h, f, :n], vp[h, idx])
+            assert not kpk[h, f, n:lim].any() and not vpk[h, f, n:lim].any()
     tol = parity.TOL[cfg.dtype]
     for h in range(cfg.H):
         kept = [np.flatnonzero(g["keep"][h][f]) for f in range(cfg.F)]
