@@ -9,18 +9,21 @@
 //
 // One persistent CTA per SM; a work unit is (head, frame, 128-prompt tile):
 //   warp 0     TMA: the unit's prompt tile (M = 128 rows) once, then the frame's query
-//              tiles (N = 128 rows each) through a 3-deep shared-memory ring;
+//              tiles (N = 128 rows each) through a 4-deep shared-memory ring;
 //   warp 1     owns TMEM (2 accumulator stages of 128 columns) and issues tcgen05.mma;
-//   warps 2-9  epilogue, two warps per TMEM lane quadrant (each folds half of the
-//              tile's columns).  Per query tile they first derive the column facts —
-//              1/|q_j| (fp32 sum of squares of the shared-memory Q tile) and q_j's
-//              bucket ids packed as bytes (loaded a tile ahead), one 8-byte entry per
-//              column (a NaN scale marks an unusable column) — then fold each
-//              prompt row: candidate = s_pj / |q_j| where pb[p] is one of q_j's
-//              buckets, running maximum per row; at the end score = max / |kp_p|.
-// Up to four buckets per query (r <= 4) on this path.
-// Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT and unwinds.  The four
-// epilogue warps share named barriers and leave their loop together.
+//   warps 2-5  column facts, one query column per thread, a tile ahead of the fold:
+//              1/|q_j| (fp32 sum of squares of the shared-memory Q row) and, per bucket b,
+//              the 128-bit mask of the tile's columns whose bucket set holds b (built with
+//              shared-memory atomics from qb; a column with an id outside [0, B) gets no
+//              bit); two buffers;
+//   warps 6-13 fold, two warps per TMEM lane quadrant (each takes half of the tile's
+//              columns): prompt row p reads the two mask words of its own bucket pb[p] and
+//              keeps the running maximum of s_pj / |q_j| over the columns whose bit is
+//              set; at the end score = max / |kp_p|.
+// Every wait is bounded; a timeout sets FASTAR_DEV_TIMEOUT, every role still walks every
+// unit (a wait after the timeout returns at once), so the named barriers of the facts and
+// fold groups always fill, and the rows of every unit that was not scored completely are
+// written as NaN.
 #include <climits>
 
 #include "common.cuh"
@@ -31,21 +34,26 @@
 namespace fastar {
 namespace {
 
-constexpr int kCaStages = 3;          // Q ring depth
-constexpr int kCaTS = 2;              // TMEM accumulator stages
-constexpr int kCaEpW = 8;             // epilogue warps: 4 lane quadrants x 2 column halves
-constexpr int kCaThreads = (2 + kCaEpW) * 32;
+constexpr int kCaStages = 4;          // Q ring depth
+constexpr int kCaTS = 2;              // TMEM accumulator stages (and column-fact buffers)
+constexpr int kCaFactW = 4;           // column-fact warps (one query column per thread)
+constexpr int kCaFoldW = 8;           // fold warps: 4 lane quadrants x 2 column halves
+constexpr int kCaFact0 = 2;           // first column-fact warp
+constexpr int kCaFold0 = kCaFact0 + kCaFactW;
+constexpr int kCaThreads = (kCaFold0 + kCaFoldW) * 32;
 constexpr int kCaTile = 128 * 128;    // one 128-row x 64-element bf16 block (128-B swizzle)
 
 template <int D>
 struct alignas(1024) CaSmem {
   uint8_t a[D / 64][kCaTile];               // prompt tile
   uint8_t b[kCaStages][D / 64][kCaTile];    // query tiles
-  float2 col[kCaTS][128];                   // per query column j: {1/|q_j| (NaN: unusable), bucket-id bytes}
+  float inv[kCaTS][128];                    // 1/|q_j| per query column
+  uint32_t mask[kCaTS][FASTAR_MAX_B][4];    // per bucket: the columns whose bucket set holds it
   float bx[128];                            // second column half's row maxima
   uint64_t a_full, a_empty;
   uint64_t b_full[kCaStages], b_empty[kCaStages];
   uint64_t t_full[kCaTS], t_empty[kCaTS];
+  uint64_t f_full[kCaTS], f_empty[kCaTS];
   uint32_t tmem_base;
   int abort;
 };
@@ -97,14 +105,16 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int nch = (int)((g.tpf + 127) / 128);   // query tiles per frame
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.a_full, 1);
-    tc::mbar_init(&sm.a_empty, 1 + kCaEpW);
+    tc::mbar_init(&sm.a_empty, 1 + kCaFoldW / 2);   // the MMA's commit + the half-0 fold warps
     for (int s = 0; s < kCaStages; ++s) {
       tc::mbar_init(&sm.b_full[s], 1);
-      tc::mbar_init(&sm.b_empty[s], 1 + kCaEpW);
+      tc::mbar_init(&sm.b_empty[s], 1 + kCaFactW);  // the MMA's commit + the column-fact warps
     }
     for (int s = 0; s < kCaTS; ++s) {
       tc::mbar_init(&sm.t_full[s], 1);
-      tc::mbar_init(&sm.t_empty[s], kCaEpW);
+      tc::mbar_init(&sm.t_empty[s], kCaFoldW);
+      tc::mbar_init(&sm.f_full[s], kCaFactW);
+      tc::mbar_init(&sm.f_empty[s], kCaFoldW);
     }
     sm.abort = 0;
     tc::mbar_fence_init();
@@ -191,37 +201,77 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         tc::mma_commit(&sm.a_empty);
       }
     }
-  } else {
-    // ---------------- epilogue: 8 warps, two per TMEM lane quadrant ----------------
-    // Fold: warp (quad, half) takes prompt rows quad*32.. and the tile's columns
-    // half*64 .. half*64+63.  Column facts: thread et < 128 computes 1/|q_j| of column
-    // j = et from the Q tile; thread et >= 128 packs the bucket ids of column et-128,
-    // loaded one query tile ahead into registers so their latency hides behind a fold.
-    const int ew = warp - 2;
-    const int quad = warp & 3, half = ew >> 2;
-    const int row = quad * 32 + lane;
-    const int et = ew * 32 + lane, fcol = et & 127;
-    const bool norm_role = et < 128;
-    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    int stage = 0, acc = 0;
-    uint32_t ph = 0, aph = 0, tph = 0;
-    // bucket ids of column fcol of query tile c of (h, f) as bytes, and whether they are usable
-    auto load_ids = [&](int h, int f, int c, uint32_t& w, uint32_t& okc) {
-      w = 0;
-      okc = 0;
-      const int64_t tl = (int64_t)c * 128 + fcol;
-      if (c >= nch || tl >= g.tpf) return;
-      const int32_t* ids = qb + ((int64_t)h * g.F * g.tpf + (int64_t)f * g.tpf + tl) * g.r;
-      const int b0 = ids[0];
-      okc = 1;
+  } else if (warp < kCaFold0) {
+    // ---------------- column facts: thread ft owns query column ft of every tile ----------------
+    const int ft = (warp - kCaFact0) * 32 + lane;
+    const int nmask = g.B * 4;
+    int stage = 0, fb = 0;
+    uint32_t ph = 0, fph = 0;
+    // the column's bucket ids of tile c of (h, f), loaded a tile ahead of their use
+    auto load_ids = [&](int h, int f, int c, int (&ids)[FASTAR_MAX_R]) -> bool {
+      const int64_t tl = (int64_t)c * 128 + ft;
+      if (c >= nch || tl >= g.tpf) return false;
+      const int32_t* src = qb + ((int64_t)h * g.F * g.tpf + (int64_t)f * g.tpf + tl) * g.r;
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        const int b = sl < g.r ? ids[sl] : b0;
-        if (b < 0 || b >= g.B) okc = 0;
-        w |= ((uint32_t)b & 0xffu) << (8 * sl);
-      }
+      for (int sl = 0; sl < FASTAR_MAX_R; ++sl) ids[sl] = sl < g.r ? src[sl] : 0;
+      return true;
     };
-    int u_fail = units;   // the first unit left unscored after a timed-out wait
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
+      int nids[FASTAR_MAX_R];
+      bool nok = load_ids(h, f, 0, nids);
+      for (int c = 0; c < nch; ++c) {
+        int ids[FASTAR_MAX_R];
+#pragma unroll
+        for (int sl = 0; sl < FASTAR_MAX_R; ++sl) ids[sl] = nids[sl];
+        bool okc = nok;
+        nok = load_ids(h, f, c + 1, nids);   // in flight during this tile's waits and math
+        bool live = ca_wait_all(&sm.f_empty[fb], fph ^ 1, abort);
+        if (live)
+          for (int i = ft; i < nmask; i += kCaFactW * 32) (&sm.mask[fb][0][0])[i] = 0u;
+        live = tc::named_bar_and(2, kCaFactW * 32, live);   // cleared before any bit is set
+        live = live && ca_wait_all(&sm.b_full[stage], ph, abort);
+        if (live) {
+          float qi = 0.f;
+          if (okc) {
+            const float ss = row_sumsq<D>(&sm.b[stage][0][0], ft);
+            qi = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+#pragma unroll
+            for (int sl = 0; sl < FASTAR_MAX_R; ++sl)
+              if (sl < g.r && (ids[sl] < 0 || ids[sl] >= g.B)) okc = false;
+          }
+          sm.inv[fb][ft] = qi;
+          if (okc) {
+#pragma unroll
+            for (int sl = 0; sl < FASTAR_MAX_R; ++sl)
+              if (sl < g.r) atomicOr(&sm.mask[fb][ids[sl]][ft >> 5], 1u << (ft & 31));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&sm.b_empty[stage]);
+          tc::mbar_arrive(&sm.f_full[fb]);
+        }
+        if (++stage == kCaStages) {
+          stage = 0;
+          ph ^= 1;
+        }
+        if (++fb == kCaTS) {
+          fb = 0;
+          fph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- fold: warp (quad, half) takes prompt rows quad*32.. and the tile's
+    // columns half*64 .. half*64+63 ----------------
+    const int fw = warp - kCaFold0;
+    const int quad = warp & 3, half = fw >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    int acc = 0;
+    uint32_t aph = 0, tph = 0;
+    bool alive = true;   // false from the first timed-out wait on
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int pt = u % g.PT, f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
       const int64_t p = (int64_t)pt * 128 + row;
@@ -233,98 +283,69 @@ __global__ void __launch_bounds__(kCaThreads, 1)
           mypb = -1;
         }
       }
-      uint32_t nw = 0, nok = 0;
-      if (norm_role) load_ids(h, f, 0, nw, nok);
       // 1/|kp_p| from the prompt tile, then hand the tile's shared memory back
       bool got = ca_wait_all(&sm.a_full, aph, abort);
       aph ^= 1;
+      alive = alive && got;
       float pinv = 0.f;
-      if (got) {
-        if (half == 0) {
+      if (half == 0) {
+        if (got) {
           const float ss = row_sumsq<D>(&sm.a[0][0], row);
           pinv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.a_empty);
       }
-      if (!tc::named_bar_and(1, kCaEpW * 32, got)) {
-        u_fail = u;
-        break;
-      }
-      const uint32_t pb4 = mypb >= 0 ? (uint32_t)mypb * 0x01010101u : 0u;
       float best = neg_inf();
-      bool ok = true;
       for (int c = 0; c < nch; ++c) {
-        got = ca_wait_all(&sm.b_full[stage], ph, abort);
-        if (got) {
-          if (norm_role) {
-            // one 8-byte entry per column, so that the fold's broadcast loads are 8 bytes:
-            // a column without usable bucket ids gets a NaN scale, which fmaxf ignores
-            float qi = 0.f;
-            if ((int64_t)c * 128 + fcol < g.tpf) {
-              const float ss = row_sumsq<D>(&sm.b[stage][0][0], fcol);
-              qi = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
-            }
-            sm.col[acc][fcol] = make_float2(nok ? qi : __uint_as_float(0x7fc00000u), __uint_as_float(nw));
-            load_ids(h, f, c + 1, nw, nok);   // next tile's ids, consumed one fold later
-          }
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sm.b_empty[stage]);
-        }
-        if (++stage == kCaStages) {
-          stage = 0;
-          ph ^= 1;
-        }
-        got = got && ca_wait_all(&sm.t_full[acc], tph, abort);
-        if (!tc::named_bar_and(1, kCaEpW * 32, got)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
+        got = ca_wait_all(&sm.t_full[acc], tph, abort);
         float v[64];
-        tc::tmem_ld32(tmem + lane_addr + (uint32_t)(acc * 128 + half * 64), v);
-        tc::tmem_ld32(tmem + lane_addr + (uint32_t)(acc * 128 + half * 64 + 32), v + 32);
-        tc::tmem_wait_ld();
-        tc::tmem_pin32(v);
-        tc::tmem_pin32(v + 32);
-        tc::tc_fence_before();
+        if (got) {
+          tc::tc_fence_after();
+          tc::tmem_ld32(tmem + lane_addr + (uint32_t)(acc * 128 + half * 64), v);
+          tc::tmem_ld32(tmem + lane_addr + (uint32_t)(acc * 128 + half * 64 + 32), v + 32);
+          tc::tmem_wait_ld();
+          tc::tmem_pin32(v);
+          tc::tmem_pin32(v + 32);
+          tc::tc_fence_before();
+        }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.t_empty[acc]);
-        if (mypb >= 0) {
+        got = got && ca_wait_all(&sm.f_full[acc], tph, abort);
+        alive = alive && got;
+        if (got && mypb >= 0) {
+          const uint32_t m0 = sm.mask[acc][mypb][half * 2], m1 = sm.mask[acc][mypb][half * 2 + 1];
+          const float* iv = sm.inv[acc] + half * 64;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float2 cf = sm.col[acc][half * 64 + j];
-            const uint32_t x = __float_as_uint(cf.y) ^ pb4;   // a zero byte where q_j's bucket is pb[p]
-            const bool hit = ((x - 0x01010101u) & ~x & 0x80808080u) != 0u;
-            best = hit ? fmaxf(best, v[j] * cf.x) : best;   // a NaN scale leaves best unchanged
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 s4 = *reinterpret_cast<const float4*>(iv + j4 * 4);
+            const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = j4 * 4 + e;
+              const uint32_t m = j < 32 ? m0 : m1;
+              if ((m >> (j & 31)) & 1u) best = fmaxf(best, v[j] * sc[e]);
+            }
           }
         }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.f_empty[acc]);
         if (++acc == kCaTS) {
           acc = 0;
           tph ^= 1;
         }
       }
-      if (!ok) {
-        u_fail = u;
-        break;
-      }
-      // combine the two column halves of each row
+      // combine the two column halves of each row; a unit not scored completely (a wait
+      // timed out) writes NaN, so that the ranking sees the failure
       if (half == 1) sm.bx[row] = best;
-      tc::named_bar(1, kCaEpW * 32);
+      const bool unit_ok = tc::named_bar_and(1, kCaFoldW * 32, alive);
       if (half == 0 && p < g.P) {
         best = fmaxf(best, sm.bx[row]);
-        score[((int64_t)h * g.F + f) * g.P + p] = best == neg_inf() ? neg_inf() : best * pinv;
+        const float sc = best == neg_inf() ? neg_inf() : best * pinv;
+        score[((int64_t)h * g.F + f) * g.P + p] = unit_ok ? sc : __uint_as_float(0x7fc00000u);
       }
-      tc::named_bar(1, kCaEpW * 32);
+      tc::named_bar(1, kCaFoldW * 32);
     }
-    // After a timed-out wait every score row this CTA still owed is written as NaN, so
-    // that the ranking sees the failure instead of an earlier call's values.
-    if (half == 0)
-      for (int u = u_fail; u < units; u += gridDim.x) {
-        const int pt = u % g.PT, f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
-        const int64_t p = (int64_t)pt * 128 + row;
-        if (p < g.P) score[((int64_t)h * g.F + f) * g.P + p] = __uint_as_float(0x7fc00000u);
-      }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -376,7 +397,7 @@ bool launch_annca_tc_impl(TokView q, int H, int F, int64_t tpf, const int32_t* q
 
 bool launch_annca_tc(int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r, const void* kp,
                      const int32_t* pb, int64_t P, int B, float* score, int32_t* status, cudaStream_t s) {
-  if (B < 1 || B > FASTAR_MAX_B || r < 1 || r > 4) return false;
+  if (B < 1 || B > FASTAR_MAX_B || r < 1 || r > FASTAR_MAX_R) return false;
   if (d == 128) return launch_annca_tc_impl<128>(q, H, F, tpf, qb, r, kp, pb, P, B, score, status, s);
   return launch_annca_tc_impl<64>(q, H, F, tpf, qb, r, kp, pb, P, B, score, status, s);
 }
