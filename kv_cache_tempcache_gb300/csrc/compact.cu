@@ -91,13 +91,15 @@ compact_scan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in,
   if (threadIdx.x == 0) len_out[h] = (int32_t)L;
 }
 
-// The sorted compaction's plan, one cluster of kSortCtas CTAs per head (every thread of
-// every CTA runs every phase, so the cluster barriers always fill):
-//   (optional) the stable counting sort of the (query, slot) pairs' buckets qb -> qperm, qoff;
+// The sorted compaction's plan, clusters of kSortCtas CTAs (every thread of a cluster's
+// CTAs runs every phase of its role, so the cluster barriers always fill).  Per head, one
+// cluster runs
 //   the survivor scan: slot s takes survivor number (s + drop) if s + drop < S, else current
 //   token (s + drop - S), drop = max(0, S + nq - M); writes index_map, len_out and the new
 //   slots' bucket ids kbout (the source entry's);
-//   the stable counting sort of kbout over the len_out slots -> kperm, koff, kpos.
+//   then the stable counting sort of kbout over the len_out slots -> kperm, koff, kpos;
+// and, when qb is given, a second cluster the stable counting sort of the (query, slot)
+// pairs' buckets qb -> qperm, qoff at the same time (clusters 2h and 2h + 1).
 __global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortWarpsC * 32)
 compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, const uint8_t* __restrict__ evict,
                     int32_t* __restrict__ len_out, int32_t* __restrict__ index_map, const int32_t* __restrict__ kcb,
@@ -110,12 +112,15 @@ compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, c
   __shared__ int warp_tot[kSortWarpsC];
   __shared__ int cta_tot;
   const int c = (int)cluster.block_rank();
-  const int h = blockIdx.x / kSortCtas;
+  const int cid = blockIdx.x / kSortCtas;
+  const int h = qb ? cid >> 1 : cid;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   constexpr int kT = kSortWarpsC * 32;
-  if (qb)
+  if (qb && (cid & 1)) {   // the pairs' sort, beside the other cluster's scan and key sort
     cluster_counting_sort(sm, qb + (int64_t)h * nq * r, nq * r, B, qperm + (int64_t)h * nq * r,
                           qoff + (int64_t)h * (B + 1), nullptr, status);
+    return;
+  }
   // ---- survivor scan: CTA c owns a contiguous chunk, each thread a contiguous piece ----
   int64_t n = len_in[h];
   if (n < 0 || n > M) {
@@ -355,9 +360,8 @@ cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int
                                         cudaStream_t s) {
   // one cluster per head plans the step: the query pairs' sort, the survivor scan with
   // the new slots' bucket ids, and the key sort
-  compact_plan_kernel<<<H * kSortCtas, kSortWarpsC * 32, 0, s>>>(nq, M, len_in, evict, len_out, imap, kcb, kbin,
-                                                                 kbout, B, kperm, koff, kpos, qb, r, qperm, qoff,
-                                                                 status);
+  compact_plan_kernel<<<H * kSortCtas * (qb ? 2 : 1), kSortWarpsC * 32, 0, s>>>(
+      nq, M, len_in, evict, len_out, imap, kcb, kbin, kbout, B, kperm, koff, kpos, qb, r, qperm, qoff, status);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
