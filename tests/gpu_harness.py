@@ -161,6 +161,68 @@ def check_head(cfg, inputs, cache_k, cache_v, g, h, gate=True, counts=None, chec
     return c
 
 
+def check_head_sampled(cfg, inputs, cache_k, cache_v, g, h, rows, counts=None):
+    """check_head for a head whose per-query outputs are checked on the query rows `rows`
+    only (top-1 and its score, AnnSA and cross-attention outputs); everything whose oracle
+    is cheap at any size stays complete: every bucket id, the eviction flags from the GPU's
+    top-1, the compaction, both sorts and the AnnCA selection."""
+    c = counts or Counts()
+    tol = parity.TOL[cfg.dtype]
+    rows = np.asarray(rows)
+    C = inputs["centroids"][h]
+    q, kc, vc = inputs["q"][h], inputs["k_cur"][h], inputs["v_cur"][h]
+    ck, cv = cache_k[h], cache_v[h]
+    kp, vp = inputs["kp"][h], inputs["vp"][h]
+    n, Nq, M, B = ck.shape[0], q.shape[0], cfg.M, cfg.B
+    c.topr_ties += parity.check_topr(O.centroid_scores(q, C), g["qb"][h], "query buckets")
+    c.key_ties += parity.check_argmax(O.centroid_scores(kc, C), g["kb_cur"][h], "current key buckets")
+    c.key_ties += parity.check_argmax(O.centroid_scores(ck, C), g["kb_in"][h][:n], "cache key buckets")
+    c.key_ties += parity.check_argmax(O.centroid_scores(kp, C), g["pb"][h], "prompt buckets")
+    # the match on the sampled queries, each against the whole incoming cache
+    top1 = g["top1"][h].astype(np.int64)
+    c.top1_ties += parity.check_argmax(O.cosine_matrix(q[rows], ck), top1[rows], "tempcache top-1 (sampled)")
+    _, o_s1, _ = O.tempcache_match(q[rows], ck)
+    np.testing.assert_allclose(g["s1"][h][rows], o_s1, rtol=0, atol=2e-5)
+    assert ((top1 >= 0) & (top1 < n)).all()
+    # eviction from the GPU's top-1 of every query, then the compaction and the sorts exactly
+    c.evict_amb += parity.check_evict(O.cosine_rows(kc, ck[top1]), top1, g["evict"][h], n, cfg.tau)
+    e_gpu = g["evict"][h][:n].astype(bool)
+    imap, L = O.compact_plan(e_gpu, n, Nq, M)
+    assert int(g["len_out"][h]) == L
+    assert np.array_equal(g["index_map"][h].astype(np.int64), imap), "index map"
+    np.testing.assert_array_equal(g["k_out"][h][:L], O.gather_rows(imap, L, ck, kc))
+    np.testing.assert_array_equal(g["v_out"][h][:L], O.gather_rows(imap, L, cv, vc))
+    kb_new = O.gather_rows(imap, L, g["kb_in"][h][:n], g["kb_cur"][h])
+    np.testing.assert_array_equal(g["kb_out"][h][:L], kb_new)
+    koff = np.concatenate([[0], np.cumsum(np.bincount(kb_new, minlength=B))])
+    assert np.array_equal(g["koff"][h], koff)
+    assert np.array_equal(g["kperm"][h][:L], np.argsort(kb_new, kind="stable"))
+    qflat = g["qb"][h].reshape(-1)
+    assert np.array_equal(g["qoff"][h], np.concatenate([[0], np.cumsum(np.bincount(qflat, minlength=B))]))
+    assert np.array_equal(g["qperm"][h], np.argsort(qflat, kind="stable"))
+    # AnnSA on the sampled queries (each over its own buckets' keys of the new cache)
+    new_k, new_v = O.gather_rows(imap, L, ck, kc), O.gather_rows(imap, L, cv, vc)
+    o, lse, n_empty = O.annsa_attention(q[rows], g["qb"][h][rows], new_k, new_v, kb_new, cfg.scale)
+    c.empty_queries += n_empty
+    parity.close(g["o_self"][h][rows], o, *tol, f"o_self head {h} (sampled)")
+    # the AnnCA selection on every prompt token and frame
+    keep_o, _, _, score_o = O.annca_select(q, g["qb"][h], kp, g["pb"][h], cfg.F, cfg.Tf, cfg.tau_ca, cfg.topk, True)
+    fin = np.isfinite(score_o)
+    assert np.array_equal(np.isfinite(g["score"][h]), fin), "AnnCA gating"
+    np.testing.assert_allclose(g["score"][h][fin], score_o[fin], rtol=0, atol=2e-5)
+    for f in range(cfg.F):
+        c.keep_amb += parity.check_keep(score_o[f], g["keep"][h][f], cfg.tau_ca, cfg.topk, f"keep head {h} frame {f}")
+        idx = np.flatnonzero(g["keep"][h][f])
+        assert int(g["kcnt"][h][f]) == len(idx)
+        assert np.array_equal(g["kidx"][h][f][:len(idx)], idx)
+        # cross-attention of the frame's sampled queries over the GPU's kept set
+        rf = rows[rows // cfg.Tf == f]
+        if len(rf):
+            oc, _ = O.cross_attention_subset(q[rf], kp, vp, [idx], 1, len(rf), cfg.scale)
+            parity.close(g["o_cross"][h][rf], oc, *tol, f"o_cross head {h} frame {f} (sampled)")
+    return c
+
+
 def check_step(cfg, inputs, cache_k, cache_v, g, heads=None, gate=True):
     assert g["status"] == 0, f"device status {g['status']}"
     counts = Counts()

@@ -1,8 +1,9 @@
 """Parity at the benchmark's full sizes, in the launch configuration the benchmark uses
 (the layer step as one replayed CUDA graph).  The Wan-1.3B-shaped layer is checked on
-every head; the HunyuanVideo-shaped 720p layer (24 heads, 28 800-entry cache) on six
-heads spread over the layer, every output of those heads, plus size-independent
-properties on all.  The near-tie counts of both are reported."""
+every head; the HunyuanVideo-shaped 720p layer (24 heads, 28 800-entry cache) on every
+output of six heads spread over the layer, and on the other 18 heads completely where the
+oracle is cheap (bucket ids, eviction flags from the GPU's top-1, compaction, both sorts,
+AnnCA selection) and on sampled queries for the rest (top-1, AnnSA, cross-attention).  The near-tie counts of both are reported."""
 import numpy as np
 import pytest
 import torch
@@ -62,8 +63,15 @@ def test_hunyuan720p_layer_full_size_sampled_heads():
     counts = GH.Counts()
     for h in HUNYUAN_HEADS:
         GH.check_head(cfg, inputs, ck, cv, g, h, counts=counts)
+    # every other head: complete where the oracle is cheap, sampled queries elsewhere
+    rng = np.random.default_rng(7)
+    for h in range(cfg.H):
+        if h not in HUNYUAN_HEADS:
+            rows = np.unique(np.concatenate([[0, cfg.Nq - 1], rng.choice(cfg.Nq, 160, replace=False)]))
+            GH.check_head_sampled(cfg, inputs, ck, cv, g, h, rows, counts=counts)
     # properties that hold on every head at any size
     assert (g["len_out"] <= cfg.M).all()
     assert np.isfinite(g["o_self"]).all() and np.isfinite(g["o_cross"]).all()
     assert (g["kcnt"] >= cfg.topk).all()
-    parity.report(f"{cfg.name} layer step, heads {HUNYUAN_HEADS}", counts)
+    parity.report(f"{cfg.name} layer step, heads {HUNYUAN_HEADS} in full, the other {cfg.H - len(HUNYUAN_HEADS)} "
+                  "on 162 sampled queries each", counts)
