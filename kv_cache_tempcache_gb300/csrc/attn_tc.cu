@@ -477,6 +477,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     sm.abort = 0;
     tc::mbar_fence_init();
   }
+  // the slot merge after it (AnnSA) may start launching: its CTAs are small and wait for
+  // this grid to finish
+  pdl_trigger();
   int* pre = reinterpret_cast<int*>(base + Lay::prefix);
   if (pair_items(a) && !a.items) {
     // plan the AnnSA items here: exclusive prefix over the (head, bucket) entries of
@@ -1180,6 +1183,7 @@ __global__ void __launch_bounds__(256) cross_gather_rows_kernel(const AttnArgs a
 // one coalesced 2*D-byte line.
 template <int D>
 __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
+  pdl_wait();   // the slot partials of the attention before it in the stream
   constexpr int E = D / 32;
   const int64_t wq = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -1367,7 +1371,9 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
   if (!ok) return false;
   if (a.mode == kSparse) {
     const int64_t threads = (int64_t)a.H * a.nq * 32;
-    sparse_merge_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
+    if (launch_dependent(sparse_merge_kernel<D>, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, a) !=
+        cudaSuccess)
+      return false;
     count_launches(1);
   }
   return true;

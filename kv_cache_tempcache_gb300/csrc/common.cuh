@@ -72,4 +72,30 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
   if (status) atomicOr(reinterpret_cast<int*>(status), bits);
 }
 
+// Programmatic dependent launch between consecutive kernels of one stream: a kernel
+// launched with launch_dependent() may start (its CTAs placed on SMs the previous kernel
+// has freed, its set-up done) before the previous kernel has finished; pdl_wait() then
+// blocks until that kernel has completed and its memory writes are visible, so every read
+// of its results must come after it.  pdl_trigger() lets the next kernel start launching
+// (only once every CTA of this grid has executed it or exited).  Both are no-ops when no
+// such dependency exists.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace fastar
