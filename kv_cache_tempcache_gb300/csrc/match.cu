@@ -195,7 +195,7 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
                       const int32_t* __restrict__ clen, int64_t M, float tau, int splits,
                       const float4* __restrict__ part, int32_t* __restrict__ top1,
                       float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict,
-                      int32_t* __restrict__ owner) {
+                      int32_t* __restrict__ owner, int qn_part) {
   // kFinLanes lanes per query: each lane owns D / kFinLanes consecutive elements (vector
   // loads); four lanes keep every warp of the layer resident at once
   const int sub = threadIdx.x & (kFinLanes - 1);
@@ -209,7 +209,7 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   // this lane's first partial and the two rows are loaded before any of them is used
   float4 p0 = make_float4(neg_inf(), __int_as_float(INT_MAX), neg_inf(), 0.f);
   if (sub < splits) p0 = part[((int64_t)sub * H + h) * nq + i];
-  // |q_i| and |kcur_i|
+  // |q_i| (from the partials when the match kernel summed it: qn_part) and |kcur_i|
   constexpr int E = D / kFinLanes;
   const T* qr = q + h * hs + i * ts + sub * E;
   const T* kr = kc + h * hs + i * ts + sub * E;
@@ -217,15 +217,17 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   float qq = 0.f, kk = 0.f;
 #pragma unroll
   for (int c = 0; c < E; c += 8) {
-    float a[8];
-    load8(qr + c, a);
     load8(kr + c, kv + c);
+    if (!qn_part) {
+      float a[8];
+      load8(qr + c, a);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      qq = fmaf(a[u], a[u], qq);
-      kk = fmaf(kv[c + u], kv[c + u], kk);
+      for (int u = 0; u < 8; ++u) qq = fmaf(a[u], a[u], qq);
     }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) kk = fmaf(kv[c + u], kv[c + u], kk);
   }
+  if (qn_part) qq = sub == 0 ? p0.w : 0.f;   // segment 0's |q|^2, summed below like the shares
 #pragma unroll
   for (int o = kFinLanes / 2; o > 0; o >>= 1) {
     qq += __shfl_xor_sync(0xffffffffu, qq, o);
@@ -300,7 +302,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
       const int64_t warps = (int64_t)H * nq;
       match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
           static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-          static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner);
+          static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner, 1);
       count_launches(1);
       return cudaGetLastError();
     }
@@ -333,7 +335,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   const int64_t warps = (int64_t)H * nq;
   match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-      static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, splits, part, top1, s1, s2, evict, owner);
+      static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, splits, part, top1, s1, s2, evict, owner, 0);
   count_launches(1);
   return cudaGetLastError();
 }

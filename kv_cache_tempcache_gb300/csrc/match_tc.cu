@@ -54,7 +54,8 @@ struct alignas(1024) MatchSmem {
   uint8_t a[2][D / 64][kTile];
   uint8_t b[kStages][D / 64][kN * 128];
   float invk[kEpW][kCW];
-  float4 best[kParts][kQ];   // per-unit (m1, i1, m2) of every column part, merged in place
+  float4 best[kParts][kQ];
+  float qsq[kParts][kQ];     // per-unit shares of |q|^2 of every row, one per column part   // per-unit (m1, i1, m2) of every column part, merged in place
   uint64_t a_full, a_empty;
   uint64_t b_full[kStages], b_empty[kStages];
   uint64_t t_full[kTS], t_empty[kTS];
@@ -183,7 +184,7 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm.a_full, 1);
-    tc::mbar_init(&sm.a_empty, 1);
+    tc::mbar_init(&sm.a_empty, 1 + kEpW);   // the MMA's commit + the epilogue warps (|q|^2 read)
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&sm.b_full[s], 1);
       tc::mbar_init(&sm.b_empty[s], 1);
@@ -300,10 +301,42 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t tph = 0;
     // Every epilogue warp walks every unit (no early exit on abort: after one, each
     // wait returns at once), so the two named barriers per unit always fill.
+    uint32_t aph = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode(g, u, clen);
       const bool two = w.nm > 1;      // warp-uniform: the second M-tile holds queries
       Best b0{neg_inf(), INT_MAX, neg_inf()}, b1{neg_inf(), INT_MAX, neg_inf()};
+      // this part's share of |q|^2 of both rows, from the unit's query tile (for the
+      // finaliser's cosine; the parts' shares are summed in the merge below)
+      // (a unit without key tiles loads no query tile and reports no match: nothing to read)
+      if (w.t_end > w.t_beg) {
+        float qs0 = 0.f, qs1 = 0.f;
+        const int r0 = quad * 32 + lane;
+        if (tc::mbar_wait(&sm.a_full, aph, abort)) {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            const int gc = part * (D / 32) + i;   // 16-byte chunk of the row
+#pragma unroll
+            for (int mm = 0; mm < 2; ++mm) {
+              const uint4 v = *reinterpret_cast<const uint4*>(&sm.a[mm][gc >> 3][0] + tc::sw128_off(r0, gc & 7));
+              const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+              float acc = 0.f;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(x[e] << 16), hi = __uint_as_float(x[e] & 0xffff0000u);
+                acc = fmaf(lo, lo, acc);
+                acc = fmaf(hi, hi, acc);
+              }
+              if (mm == 0) qs0 += acc; else qs1 += acc;
+            }
+          }
+        }
+        aph ^= 1;
+        sm.qsq[part][r0] = qs0;
+        sm.qsq[part][r0 + 128] = qs1;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.a_empty);
+      }
       const float* kn = cknorm + (int64_t)w.h * g.M;
       // |k_j| of this lane's column of the first tile (prefetched one tile ahead)
       float kx = 0.f;
@@ -382,9 +415,11 @@ match_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int mm = 0; mm < 2; ++mm) {
           const int r = r0 + mm * 128;
           float4 a = sm.best[0][r];
+          a.w = sm.qsq[0][r];
 #pragma unroll
           for (int p2 = 1; p2 < kParts; ++p2) {
             const float4 c = sm.best[p2][r];
+            a.w += sm.qsq[p2][r];   // |q|^2, summed over the parts in order
             if (beats(c.x, __float_as_int(c.y), a.x, __float_as_int(a.y))) {
               a.z = fmaxf(a.x, c.z);
               a.x = c.x;
