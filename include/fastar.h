@@ -388,8 +388,8 @@ int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, in
  * Failure: a (head, frame) whose scores could not all be formed (a bounded wait of the
  * tensor-core scorer timed out, which a working device never does) or hold a NaN (NaN
  * inputs) is not ranked: kcnt = -1, keep 0 and kidx -1 throughout, score NaN.
- * fastar_cross_attn_subset reports such a kcnt as FASTAR_DEV_BAD_INDEX in its status
- * word and attends to no prompt token for that frame.
+ * fastar_cross_attn_subset and fastar_cross_attn_kept (no status word) attend to no
+ * prompt token for such a frame, exactly as for kcnt = 0: the count is the signal.
  * kp_kept, vp_kept (optional, together; bf16 only, else FASTAR_EUNSUPPORTED): [H,F,P,d]
  * planes that the ranking launch fills with the kept rows: kp_kept[h,f,t] =
  * kp[h, kidx[h,f,t]] for t < kcnt[h,f] (vp_kept from vp, [H,P,d] contiguous, required
@@ -455,8 +455,8 @@ int fastar_cross_attn_subset(const void* q, int dtype, int H, int F, int64_t tpf
  *   O[h,i] = sum_{t < kcnt[h,f]} softmax_t(q_i . kp_kept[h,f,t] * scale) vp_kept[h,f,t]
  * for query i of frame f.  The same results as fastar_cross_attn_subset with a workspace
  * on the same selection, in one kernel launch (the tensor-core engine reads the planes as
- * tiles).  bf16 only (FASTAR_EUNSUPPORTED otherwise); planes 16-byte aligned; kcnt < 0 is
- * reported as FASTAR_DEV_BAD_INDEX and attends to nothing (O = 0, lse = -inf), as in 7. */
+ * tiles).  bf16 only (FASTAR_EUNSUPPORTED otherwise); planes 16-byte aligned; a frame with
+ * kcnt <= 0 (kcnt = -1: a failed selection) attends to nothing (O = 0, lse = -inf), as in 7. */
 int fastar_cross_attn_kept(const void* q, int dtype, int H, int F, int64_t tpf, int d,
                            int64_t q_head_stride, int64_t q_token_stride,
                            const void* kp_kept, const void* vp_kept, int64_t P, const int32_t* kcnt,
