@@ -134,6 +134,24 @@ __device__ __forceinline__ float group_log2(int32_t g, int32_t* status) {
   return g > 0 ? log2f((float)g) : neg_inf();
 }
 
+// 16 consecutive 32-bit TMEM columns of this thread's lane (P as packed bf16 pairs).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+
+// D[tmem] (+)= A B^T with A read from TMEM (M = 128 rows on the lanes, each 32-bit column a
+// bf16 pair of consecutive K elements: a K = 16 step reads 8 columns) and B from shared
+// memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Three-input maximum (PTX max.f32 with three sources).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float y;
@@ -185,11 +203,12 @@ __device__ __forceinline__ float row_max(uint32_t s_addr, int vcols, float sl2 =
   return m;
 }
 
-// Softmax pass 2: P = 2^(s * sl2 + bias - m) as bf16 into this thread's row of the P
-// tile (128-byte swizzled, one block per 64 columns); returns the row sum of P.
+// Softmax pass 2: P = 2^(s * sl2 + bias - m) as bf16 pairs into this thread's TMEM lane,
+// over the S columns already read (P's kKT / 2 columns start at s_addr: chunk c of 32
+// scores becomes columns 16c .. 16c + 15, after S columns 0 .. 32c + 31 have been loaded);
+// returns the row sum of P.  The P.V product then reads P from TMEM as its A operand.
 template <bool kFull, bool kBias = false>
-__device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, uint8_t* pst, int row,
-                                         const float* bias = nullptr) {
+__device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, float m, const float* bias = nullptr) {
   const float nm = m == neg_inf() ? 0.f : -m;
   float xa[32], xb[32];
   float s0 = 0.f, s1 = 0.f;
@@ -220,14 +239,7 @@ __device__ __forceinline__ float row_exp(uint32_t s_addr, int vcols, float sl2, 
       s1 += p1;
       pk[i >> 1] = pack_bf16(p0, p1);
     }
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const int c16 = c * 4 + q4;   // 16-byte chunk of the P row
-      const uint32_t addr = tc::smem_u32(pst + (c16 >> 3) * kBlkA) + tc::sw128_off(row, c16 & 7);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]),
-                   "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
-                   : "memory");
-    }
+    tmem_st16u(s_addr + (uint32_t)(c * 16), pk);
     if (c + 1 < kKT / 32) {
       tc::tmem_wait_ld();
       tc::tmem_pin32(nxt);
@@ -754,12 +766,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const int st = gt % kKS;
         if (!tc::mbar_wait(&sm.p_full[st], (gt / kKS) & 1, abort)) return false;
         tc::tc_fence_after();
+        // A = P from TMEM (the stage's S columns, 8 per 16 keys), B = V from shared memory
 #pragma unroll
         for (int ks = 0; ks < kKT / 16; ++ks) {
-          const uint32_t aoff = (uint32_t)(st * Lay::pstride + (ks >> 2) * kBlkA + (ks & 3) * 32);
           const uint32_t boff = (uint32_t)(st * Lay::kstage + ks * 2048);
-          tc::mma_bf16(tmem + Lay::o_col + (uint32_t)(qs * 128), p_desc + (aoff >> 4), v_desc + (boff >> 4),
-                       idesc_pv, (!first || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + Lay::o_col + (uint32_t)(qs * 128), tmem + Lay::s_col + (uint32_t)(st * kKT + ks * 8),
+                      v_desc + (boff >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&sm.kv_empty[st]);
         tc::mma_commit(&sm.pv_done);
@@ -914,17 +926,15 @@ __global__ void __launch_bounds__(kThreadsA, 1)
           }
           tc::tmem_wait_st();
         }
-        // pass 2: P = 2^(s - m) as bf16 into the P tile, and its row sum
-        uint8_t* pst = sp + (size_t)st * Lay::pstride;
+        // pass 2: P = 2^(s - m) as bf16 into TMEM over the consumed S columns, and its row sum
         float sum;
         if (grouped)
-          sum = full ? row_exp<true, true>(s_addr, vcols, sl2, m_used, pst, row, bias)
-                     : row_exp<false, true>(s_addr, vcols, sl2, m_used, pst, row, bias);
+          sum = full ? row_exp<true, true>(s_addr, vcols, sl2, m_used, bias)
+                     : row_exp<false, true>(s_addr, vcols, sl2, m_used, bias);
         else
-          sum = full ? row_exp<true>(s_addr, vcols, sl2, m_used, pst, row)
-                     : row_exp<false>(s_addr, vcols, sl2, m_used, pst, row);
+          sum = full ? row_exp<true>(s_addr, vcols, sl2, m_used) : row_exp<false>(s_addr, vcols, sl2, m_used);
         l = l * alpha + sum;
-        tc::fence_proxy_async();
+        tc::tmem_wait_st();   // P has landed in TMEM before the P.V product may read it
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
