@@ -492,6 +492,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   // the slot merge after it (AnnSA) may start launching: its CTAs are small and wait for
   // this grid to finish
   pdl_trigger();
+  // the inputs written by the kernel before it in the stream (the sorted compaction's
+  // bucket-ordered rows and offsets, the AnnCA selection's kept rows): everything above
+  // touched shared memory only
+  pdl_wait();
   int* pre = reinterpret_cast<int*>(base + Lay::prefix);
   if (pair_items(a) && !a.items) {
     // plan the AnnSA items here: exclusive prefix over the (head, bucket) entries of
@@ -1262,9 +1266,10 @@ bool attn_launch(int grid, cudaStream_t s, const AttnArgs& b, const CUtensorMap&
   constexpr size_t smem = AttnLayout<D>::bytes;
   const cudaError_t attr = opt_in_smem((const void*)attn_tc_kernel<D, kGrouped, kMode>, (int)smem);
   if (attr != cudaSuccess) return false;
-  attn_tc_kernel<D, kGrouped, kMode><<<grid, kThreadsA, smem, s>>>(b, tk, tv, tq);
+  const cudaError_t e =
+      launch_dependent(attn_tc_kernel<D, kGrouped, kMode>, dim3(grid), dim3(kThreadsA), smem, s, b, tk, tv, tq);
   count_launches(1);
-  return true;
+  return e == cudaSuccess;
 }
 
 template <int D>

@@ -106,6 +106,7 @@ compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, c
                     const int32_t* __restrict__ kbin, int32_t* __restrict__ kbout, int B, int32_t* __restrict__ kperm,
                     int32_t* __restrict__ koff, int32_t* __restrict__ kpos, const int32_t* __restrict__ qb, int r,
                     int32_t* __restrict__ qperm, int32_t* __restrict__ qoff, int32_t* status) {
+  pdl_wait();   // the eviction flags of the match before it in the stream
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ SortSmem sm;
@@ -226,6 +227,7 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
                     const int32_t* __restrict__ len_out, const int32_t* __restrict__ index_map,
                     T* __restrict__ kout, T* __restrict__ vout, float* __restrict__ knout,
                     int32_t* __restrict__ kbout, int32_t* status, const MergeIO mg, const SortedIO so) {
+  pdl_wait();   // the index map of the planning kernel before it in the stream
   constexpr int VPR = D * (int)sizeof(T) / 16;
   const int64_t total = (int64_t)H * M * VPR;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -316,12 +318,13 @@ static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView v
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   auto kern = mg.g_out ? compact_copy_kernel<T, D, true> : compact_copy_kernel<T, D, false>;
-  kern<<<(unsigned)blocks, 256, 0, s>>>(
-      H, nq, M, static_cast<const T*>(kc.p), static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb,
-      static_cast<const T*>(kin), static_cast<const T*>(vin), knin, kbin, len_in, len_out, imap,
-      static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg, so);
+  const cudaError_t e = launch_dependent(
+      kern, dim3((unsigned)blocks), dim3(256), 0, s, H, nq, M, static_cast<const T*>(kc.p),
+      static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb, static_cast<const T*>(kin), static_cast<const T*>(vin),
+      knin, kbin, len_in, len_out, imap, static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg,
+      so);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_cache_compact(int dtype, int d, int H, int64_t nq, int64_t M, TokView kc,
@@ -360,10 +363,10 @@ cudaError_t launch_cache_compact_sorted(int dtype, int d, int H, int64_t nq, int
                                         cudaStream_t s) {
   // one cluster per head plans the step: the query pairs' sort, the survivor scan with
   // the new slots' bucket ids, and the key sort
-  compact_plan_kernel<<<H * kSortCtas * (qb ? 2 : 1), kSortWarpsC * 32, 0, s>>>(
-      nq, M, len_in, evict, len_out, imap, kcb, kbin, kbout, B, kperm, koff, kpos, qb, r, qperm, qoff, status);
+  cudaError_t e = launch_dependent(compact_plan_kernel, dim3(H * kSortCtas * (qb ? 2 : 1)), dim3(kSortWarpsC * 32),
+                                   0, s, nq, M, len_in, evict, len_out, imap, kcb, kbin, kbout, B, kperm, koff,
+                                   kpos, qb, r, qperm, qoff, status);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const MergeIO mg{nullptr, nullptr, nullptr, nullptr};
   const SortedIO so{kpos, ksorted, vsorted};

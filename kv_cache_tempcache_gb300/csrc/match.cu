@@ -196,6 +196,7 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
                       const float4* __restrict__ part, int32_t* __restrict__ top1,
                       float* __restrict__ s1, float* __restrict__ s2, uint8_t* __restrict__ evict,
                       int32_t* __restrict__ owner, int qn_part) {
+  pdl_wait();   // the partials (and cleared flags) of the match kernel before it in the stream
   // kFinLanes lanes per query: each lane owns D / kFinLanes consecutive elements (vector
   // loads); four lanes keep every warp of the layer resident at once
   const int sub = threadIdx.x & (kFinLanes - 1);
@@ -300,11 +301,12 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       const int64_t warps = (int64_t)H * nq;
-      match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
-          static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
-          static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits, part, top1, s1, s2, evict, owner, 1);
+      e = launch_dependent(match_finalize_kernel<T, D>, dim3((unsigned)((warps * kFinLanes + 255) / 256)),
+                           dim3(256), 0, s, static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs,
+                           q.ts, nq, H, static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits,
+                           (const float4*)part, top1, s1, s2, evict, owner, 1);
       count_launches(1);
-      return cudaGetLastError();
+      return e;
     }
   }
   const int splits = match_splits(H, nq, M);
