@@ -71,6 +71,29 @@ def test_partial_cache_no_fifo_drop():
     assert (g["len_out"] < cfg.M).all()
 
 
+def test_threshold_extremes():
+    # tau = -1: a cosine is never below -1, so every cache entry that is some current key's
+    # top-1 match is evicted; tau_ca above 1: no score reaches it, so each frame keeps
+    # exactly its top-k floor
+    cfg = GH.small_bf16().replace(tau=-1.0, tau_ca=1.5, name="bf16_extremes")
+    _, g, _ = _run(cfg)
+    n = min(cfg.M, cfg.prior_frames * cfg.Tf)
+    for h in range(cfg.H):
+        t1 = g["top1"][h]
+        matched = np.unique(t1[t1 >= 0])
+        assert len(matched) > 0
+        assert g["evict"][h, :n].sum() == len(matched) and g["evict"][h, matched].all()
+    assert (g["kcnt"] == cfg.topk).all()
+
+
+def test_largest_bucket_and_prompt_counts():
+    # the largest sizes the interface accepts for the ANN parts: B = 256 buckets, r = 8
+    # buckets per query, P = 1024 prompt tokens
+    cfg = GH.small_bf16().replace(B=256, r=8, P=1024, name="bf16_max_sizes")
+    _, g, _ = _run(cfg)
+    assert g["qb"].max() < 256 and (g["kcnt"] >= cfg.topk).all()
+
+
 def test_prompt_smaller_than_topk_and_ungated():
     cfg = GH.small_bf16().replace(P=8, topk=16)
     _, g, _ = _run(cfg)
