@@ -1194,16 +1194,15 @@ __global__ void __launch_bounds__(256) cross_gather_rows_kernel(const AttnArgs a
 // o = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s), and
 // lse = max + log(sum_s w_s).  One warp per (head, query); lane l owns columns
 // [l*D/32, (l+1)*D/32), so every slot row (bf16, as the attention stored it) is read as
-// one coalesced 2*D-byte line.
+// one coalesced 2*D-byte line.  Grid: (queries / 8, heads), eight warps per CTA.
 template <int D>
 __global__ void __launch_bounds__(256) sparse_merge_kernel(const AttnArgs a) {
   pdl_wait();   // the slot partials of the attention before it in the stream
   constexpr int E = D / 32;
-  const int64_t wq = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+  const int h = (int)blockIdx.y;
+  const int64_t qi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (wq >= (int64_t)a.H * a.nq) return;
-  const int h = (int)(wq / a.nq);
-  const int64_t qi = wq % a.nq;
+  if (qi >= a.nq) return;
   const int64_t np = a.nq * a.r;
   const int64_t pb = (int64_t)h * np + qi * a.r;   // the query's r slots are adjacent rows
   // the first two slot rows are loaded together with the lse values, before the weights
@@ -1385,9 +1384,8 @@ bool attn_tc_impl(const AttnArgs& a, cudaStream_t s) {
                   : attn_launch<D, false, kDense>(grid, s, b, tk, tv, tq);
   if (!ok) return false;
   if (a.mode == kSparse) {
-    const int64_t threads = (int64_t)a.H * a.nq * 32;
-    if (launch_dependent(sparse_merge_kernel<D>, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, a) !=
-        cudaSuccess)
+    if (launch_dependent(sparse_merge_kernel<D>, dim3((unsigned)((a.nq + 7) / 8), (unsigned)a.H), dim3(256), 0, s,
+                         a) != cudaSuccess)
       return false;
     count_launches(1);
   }

@@ -23,6 +23,7 @@
 #include "cluster_sort.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fastar {
 
@@ -228,17 +229,19 @@ compact_copy_kernel(int H, int64_t nq, int64_t M, const T* __restrict__ kc, cons
                     T* __restrict__ kout, T* __restrict__ vout, float* __restrict__ knout,
                     int32_t* __restrict__ kbout, int32_t* status, const MergeIO mg, const SortedIO so) {
   pdl_wait();   // the index map of the planning kernel before it in the stream
+  // grid: (CTAs per head, heads); a head's occupied slots [0, len_out) in 16-byte chunks
   constexpr int VPR = D * (int)sizeof(T) / 16;
-  const int64_t total = (int64_t)H * M * VPR;
+  const int h = (int)blockIdx.y;
+  int64_t n = len_in[h];
+  n = n < 0 ? 0 : (n > M ? M : n);
+  int64_t lo = len_out[h];
+  lo = lo < 0 ? 0 : (lo > M ? M : lo);
+  const int64_t total = lo * VPR;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
        g += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = g / VPR;
-    const int c = (int)(g - row * VPR);
-    const int h = (int)(row / M);
-    const int64_t slot = row - (int64_t)h * M;
-    if (slot >= len_out[h]) continue;
-    int64_t n = len_in[h];
-    n = n < 0 ? 0 : (n > M ? M : n);
+    const int64_t slot = g / VPR;
+    const int c = (int)(g - slot * VPR);
+    const int64_t row = (int64_t)h * M + slot;
     const int64_t src = index_map[row];
     const uint4* ks;
     const uint4* vs;
@@ -313,13 +316,14 @@ static cudaError_t copy_impl(int H, int64_t nq, int64_t M, TokView kc, TokView v
                              const int32_t* imap, void* kout, void* vout, float* knout, int32_t* kbout,
                              int32_t* status, const MergeIO& mg, cudaStream_t s, const SortedIO& so = SortedIO{}) {
   constexpr int VPR = D * (int)sizeof(T) / 16;
-  const int64_t total = (int64_t)H * M * VPR;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  // about 16 CTAs of 256 threads per SM over all heads, each head's CTAs striding its slots
+  int64_t blocks = ((int64_t)M * VPR + 255) / 256;
+  const int64_t cap = ((int64_t)sm_count() * 16 + H - 1) / H;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   auto kern = mg.g_out ? compact_copy_kernel<T, D, true> : compact_copy_kernel<T, D, false>;
   const cudaError_t e = launch_dependent(
-      kern, dim3((unsigned)blocks), dim3(256), 0, s, H, nq, M, static_cast<const T*>(kc.p),
+      kern, dim3((unsigned)blocks, (unsigned)H), dim3(256), 0, s, H, nq, M, static_cast<const T*>(kc.p),
       static_cast<const T*>(vc.p), kc.hs, kc.ts, kcn, kcb, static_cast<const T*>(kin), static_cast<const T*>(vin),
       knin, kbin, len_in, len_out, imap, static_cast<T*>(kout), static_cast<T*>(vout), knout, kbout, status, mg,
       so);

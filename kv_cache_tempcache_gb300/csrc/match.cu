@@ -199,12 +199,12 @@ match_finalize_kernel(const T* __restrict__ q, const T* __restrict__ kc, int64_t
   pdl_wait();   // the partials (and cleared flags) of the match kernel before it in the stream
   // kFinLanes lanes per query: each lane owns D / kFinLanes consecutive elements (vector
   // loads); four lanes keep every warp of the layer resident at once
+  // grid: (queries / (256 / kFinLanes), heads)
   const int sub = threadIdx.x & (kFinLanes - 1);
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kFinLanes;
-  const bool in = wid < (int64_t)H * nq;
-  const int64_t w = in ? wid : 0;
-  const int h = (int)(w / nq);
-  const int64_t i = w - (int64_t)h * nq;
+  const int h = (int)blockIdx.y;
+  const int64_t iq = (int64_t)blockIdx.x * (256 / kFinLanes) + threadIdx.x / kFinLanes;
+  const bool in = iq < nq;
+  const int64_t i = in ? iq : 0;   // (out-of-range lanes still take part in the shuffles)
   int64_t n = clen[h];
   n = n < 0 ? 0 : (n > M ? M : n);
   // this lane's first partial and the two rows are loaded before any of them is used
@@ -300,9 +300,8 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
     if (tsplits > 0) {
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
-      const int64_t warps = (int64_t)H * nq;
-      e = launch_dependent(match_finalize_kernel<T, D>, dim3((unsigned)((warps * kFinLanes + 255) / 256)),
-                           dim3(256), 0, s, static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs,
+      e = launch_dependent(match_finalize_kernel<T, D>,
+                           dim3((unsigned)((nq * kFinLanes + 255) / 256), (unsigned)H), dim3(256), 0, s, static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs,
                            q.ts, nq, H, static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, tsplits,
                            (const float4*)part, top1, s1, s2, evict, owner, 1);
       count_launches(1);
@@ -334,8 +333,7 @@ static cudaError_t match_impl(TokView q, TokView kc, int H, int64_t nq, const vo
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t warps = (int64_t)H * nq;
-  match_finalize_kernel<T, D><<<(unsigned)((warps * kFinLanes + 255) / 256), 256, 0, s>>>(
+  match_finalize_kernel<T, D><<<dim3((unsigned)((nq * kFinLanes + 255) / 256), (unsigned)H), 256, 0, s>>>(
       static_cast<const T*>(q.p), static_cast<const T*>(kc.p), q.hs, q.ts, nq, H,
       static_cast<const T*>(ck_ev), kn_ev, clen, M, tau, splits, part, top1, s1, s2, evict, owner, 0);
   count_launches(1);
