@@ -136,8 +136,29 @@ compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, c
   const int64_t tper = (ce - cb + kT - 1) / kT;
   const int64_t beg = cb + t * tper < ce ? cb + t * tper : ce;
   const int64_t end = beg + tper < ce ? beg + tper : ce;
+  const int32_t* kbi = kbin + (int64_t)h * M;
+  // a piece of up to kPre entries has its flags and bucket ids loaded here, all at once,
+  // for both passes (longer pieces read them entry by entry)
+  constexpr int kPre = 16;
+  const bool pre = end - beg <= kPre;
+  uint8_t ev[kPre];
+  int32_t kbv[kPre];
   int local = 0;
-  for (int64_t j = beg; j < end; ++j) local += e[j] ? 0 : 1;
+  if (pre) {
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+      ev[k] = 1;
+      kbv[k] = 0;
+      if (beg + k < end) {
+        ev[k] = e[beg + k];
+        kbv[k] = kbi[beg + k];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) local += ev[k] ? 0 : 1;
+  } else {
+    for (int64_t j = beg; j < end; ++j) local += e[j] ? 0 : 1;
+  }
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -160,24 +181,48 @@ compact_plan_kernel(int64_t nq, int64_t M, const int32_t* __restrict__ len_in, c
   const int64_t drop = total > M ? total - M : 0;
   const int64_t L = total - drop;
   int32_t* imap = index_map + (int64_t)h * M;
-  const int32_t* kbi = kbin + (int64_t)h * M;
   int32_t* kbo = kbout + (int64_t)h * M;
   int64_t rank = before + wpre + incl - local;
-  for (int64_t j = beg; j < end; ++j) {
-    if (!e[j]) {
-      const int64_t slot = rank - drop;
-      if (slot >= 0) {
-        imap[slot] = (int32_t)j;
-        kbo[slot] = kbi[j];
+  if (pre) {
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+      if (!ev[k]) {
+        const int64_t slot = rank - drop;
+        if (slot >= 0) {
+          imap[slot] = (int32_t)(beg + k);
+          kbo[slot] = kbv[k];
+        }
+        ++rank;
       }
-      ++rank;
+    }
+  } else {
+    for (int64_t j = beg; j < end; ++j) {
+      if (!e[j]) {
+        const int64_t slot = rank - drop;
+        if (slot >= 0) {
+          imap[slot] = (int32_t)j;
+          kbo[slot] = kbi[j];
+        }
+        ++rank;
+      }
     }
   }
-  for (int64_t i = (int64_t)c * kT + t; i < nq; i += (int64_t)kSortCtas * kT) {
-    const int64_t slot = S + i - drop;
-    if (slot >= 0) {
-      imap[slot] = (int32_t)(n + i);
-      kbo[slot] = kcb[(int64_t)h * nq + i];
+  // the new entries, four per thread and round: their bucket ids loaded before any store
+  for (int64_t i0 = (int64_t)c * kT + t; i0 < nq; i0 += 4 * (int64_t)kSortCtas * kT) {
+    int32_t b4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + (int64_t)k * kSortCtas * kT;
+      b4[k] = i < nq ? kcb[(int64_t)h * nq + i] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + (int64_t)k * kSortCtas * kT;
+      const int64_t slot = S + i - drop;
+      if (i < nq && slot >= 0) {
+        imap[slot] = (int32_t)(n + i);
+        kbo[slot] = b4[k];
+      }
     }
   }
   for (int64_t s2 = L + (int64_t)c * kT + t; s2 < M; s2 += (int64_t)kSortCtas * kT) imap[s2] = -1;
