@@ -140,12 +140,13 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d,
 /* ---- 1b. both assignments of a step in one call ---------------------------------------
  * The two uses of 1 in a layer step, one launch: q_ids [H, n, r] = the queries' top-r
  * sets, k_ids [H, n] = the current keys' arg-max buckets, k_norms [H, n] (optional) =
- * |k_cur|.  Identical results to fastar_bucket_assign(q, ..., r, q_ids, NULL, NULL) and
+ * |k_cur|, q_norms [H, n] (optional) = |q| (for fastar_annca_select's q_norms).
+ * Identical results to fastar_bucket_assign(q, ..., r, q_ids, NULL, q_norms) and
  * fastar_bucket_assign(k_cur, ..., 1, k_ids, NULL, k_norms).  q and k_cur share
  * (head_stride, token_stride).  Limits and errors as 1. */
 int fastar_bucket_assign_qk(const void* q, const void* k_cur, int dtype, int H, int64_t n, int d,
                             int64_t head_stride, int64_t token_stride, const void* centroids, int B, int r,
-                            int32_t* q_ids, int32_t* k_ids, float* k_norms, cudaStream_t stream);
+                            int32_t* q_ids, int32_t* k_ids, float* k_norms, float* q_norms, cudaStream_t stream);
 
 /* ---- 2. TempCache match + eviction flags ------------------------------------------
  * FAST-AR technical summary §2.A and blog §1: for each current-frame query, the
@@ -384,7 +385,10 @@ int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, in
  * B: the bucket count (0 if unknown).  qperm/qoff (optional, need B > 0): the
  * (query, slot) pairs of qb grouped by bucket, as fastar_bucket_sort writes them;
  * with them the gated scoring reads each bucket's queries directly instead of
- * scanning qb (same results either way).
+ * scanning qb (same results either way).  q_norms (optional, float [H, F*tpf]): |q_i|
+ * as fastar_bucket_assign / _qk write it (fp32 sum of squares); the bf16 tensor-core
+ * scorer then divides by these instead of forming |q_i| itself (the cosines agree to
+ * fp32 rounding); the other scorers ignore it.  NULL: the call forms the norms.
  * Failure: a (head, frame) whose scores could not all be formed (a bounded wait of the
  * tensor-core scorer timed out, which a working device never does) or hold a NaN (NaN
  * inputs) is not ranked: kcnt = -1, keep 0 and kidx -1 throughout, score NaN.
@@ -402,7 +406,7 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
                         int64_t q_head_stride, int64_t q_token_stride,
                         const int32_t* qb, int r, const void* kp, const int32_t* pb, int64_t P,
                         float tau_ca, int topk, int gate, int B,
-                        const int32_t* qperm, const int32_t* qoff,
+                        const int32_t* qperm, const int32_t* qoff, const float* q_norms,
                         uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
                         const void* vp, void* kp_kept, void* vp_kept,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -412,8 +416,8 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
  * allocate device memory when they run the step (a server that reserves all
  * device memory at start-up, a process under a fixed shared memory budget, a
  * latency-critical host thread where cudaMalloc may block or synchronise).
- * Same arguments and results as fastar_annca_select without the score output and
- * the workspace: the per-token scores go to a fixed scratch array inside the
+ * Same arguments and results as fastar_annca_select without the query norms, the
+ * score output and the workspace: the per-token scores go to a fixed scratch array inside the
  * library's device image (FASTAR_NOALLOC_MAX_SCORES floats, 1 MiB, held on every
  * GPU that loads the library until the process exits).  H * F * P above that
  * limit returns FASTAR_ECAPACITY.  The first call on a device (with that device

@@ -35,7 +35,7 @@ _SIGS = {
     "fastar_status_string": [_I],
     "fastar_workspace_bytes": [_I, _I, _L, _L, _I, _I, _I, _L, _I],
     "fastar_bucket_assign": [_P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
-    "fastar_bucket_assign_qk": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P],
+    "fastar_bucket_assign_qk": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _I, _I, _P, _P, _P, _P, _P],
     "fastar_tempcache_match": [_P, _P, _I, _I, _L, _I, _L, _L, _P, _P, _P, _L, _F, _P, _P, _P, _P, _P, _P, _P,
                                _S, _P],
     "fastar_tempcache_match_ann": [_P, _P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _F, _P,
@@ -58,7 +58,7 @@ _SIGS = {
     "fastar_sparse_attn_presorted": [_P, _I, _I, _L, _I, _L, _L, _I, _I, _P, _P, _P, _P, _L, _P, _P, _P, _P, _F,
                                      _P, _L, _L, _P, _P, _P, _S, _P],
     "fastar_annca_select": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _I, _P, _P, _P, _P, _P,
-                            _P, _P, _P, _P, _P, _S, _P],
+                            _P, _P, _P, _P, _P, _P, _S, _P],
     "fastar_annca_select_noalloc": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _I, _P, _P, _L, _F, _I, _I, _P, _P, _P, _P],
     "fastar_cross_attn_subset": [_P, _I, _I, _I, _L, _I, _L, _L, _P, _P, _L, _P, _P, _F, _P, _L, _L, _P, _P, _S,
                                  _P],
@@ -175,13 +175,13 @@ def fastar_bucket_assign(x, centroids, r, ids, scores=None, norms=None, stream=N
           centroids.shape[1], r, ptr(ids), ptr(scores), ptr(norms), stream_handle(stream))
 
 
-def fastar_bucket_assign_qk(q, k_cur, centroids, r, q_ids, k_ids, k_norms=None, stream=None):
+def fastar_bucket_assign_qk(q, k_cur, centroids, r, q_ids, k_ids, k_norms=None, stream=None, q_norms=None):
     H, n, d = q.shape
     hs, ts = tok_strides(q)
     if tok_strides(k_cur) != (hs, ts):
         raise ValueError("q and k_cur must share strides")
     _call("fastar_bucket_assign_qk", ptr(q), ptr(k_cur), dtype_code(q.dtype), H, n, d, hs, ts, ptr(centroids),
-          centroids.shape[1], r, ptr(q_ids), ptr(k_ids), ptr(k_norms), stream_handle(stream))
+          centroids.shape[1], r, ptr(q_ids), ptr(k_ids), ptr(k_norms), ptr(q_norms), stream_handle(stream))
 
 
 def fastar_tempcache_match(q, k_cur, cache_k, cache_knorm, cache_len, tau, top1, s1, s2, evict, dev_status,
@@ -317,14 +317,16 @@ def fastar_sparse_attn_grouped(q, r, B, qperm, qoff, k, v, kperm, koff, group_co
 
 
 def fastar_annca_select(q, F, qb, kp, pb, tau_ca, topk, gate, keep, kidx, kcnt, score=None, workspace=None,
-                        stream=None, B=0, qperm=None, qoff=None, vp=None, kp_kept=None, vp_kept=None):
+                        stream=None, B=0, qperm=None, qoff=None, vp=None, kp_kept=None, vp_kept=None, q_norms=None):
     """kp_kept / vp_kept [H, F, P, d] (optional, with vp): the kept rows copied by the
-    ranking launch, fastar_cross_attn_kept's input."""
+    ranking launch, fastar_cross_attn_kept's input.  q_norms [H, F * tpf] (optional): the
+    queries' norms as fastar_bucket_assign_qk writes them."""
     H, nq, d = q.shape
     qh, qt = tok_strides(q)
     tpf = nq // F
     _call("fastar_annca_select", ptr(q), dtype_code(q.dtype), H, F, tpf, d, qh, qt, ptr(qb), qb.shape[2], ptr(kp),
-          ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), int(B), ptr(qperm), ptr(qoff), ptr(keep),
+          ptr(pb), kp.shape[1], float(tau_ca), int(topk), int(gate), int(B), ptr(qperm), ptr(qoff), ptr(q_norms),
+          ptr(keep),
           ptr(kidx), ptr(kcnt), ptr(score), ptr(vp), ptr(kp_kept), ptr(vp_kept),
           ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
           stream_handle(stream))

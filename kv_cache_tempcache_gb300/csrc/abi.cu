@@ -102,7 +102,7 @@ int fastar_bucket_assign(const void* x, int dtype, int H, int64_t n, int d, int6
 
 int fastar_bucket_assign_qk(const void* q, const void* k_cur, int dtype, int H, int64_t n, int d,
                             int64_t head_stride, int64_t token_stride, const void* centroids, int B, int r,
-                            int32_t* q_ids, int32_t* k_ids, float* k_norms, cudaStream_t stream) {
+                            int32_t* q_ids, int32_t* k_ids, float* k_norms, float* q_norms, cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
   if (rc) return rc;
   if (H < 0 || n < 0 || B < 1 || r < 1) return FASTAR_EINVAL;
@@ -113,7 +113,7 @@ int fastar_bucket_assign_qk(const void* q, const void* k_cur, int dtype, int H, 
   if (!centroids || !aligned16(centroids) || !q_ids || !k_ids) return FASTAR_EINVAL;
   return cuda_rc(fastar::launch_bucket_assign_qk(dtype, d, TokView{q, head_stride, token_stride},
                                                  TokView{k_cur, head_stride, token_stride}, H, n, centroids, B, r,
-                                                 q_ids, k_ids, k_norms, stream));
+                                                 q_ids, k_ids, k_norms, q_norms, stream));
 }
 
 int fastar_tempcache_match(const void* q, const void* k_cur, int dtype, int H, int64_t nq, int d,
@@ -444,7 +444,8 @@ int fastar_sparse_attn_presorted(const void* q, int dtype, int H, int64_t nq, in
 int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int d, int64_t q_head_stride,
                         int64_t q_token_stride, const int32_t* qb, int r, const void* kp, const int32_t* pb,
                         int64_t P, float tau_ca, int topk, int gate, int B, const int32_t* qperm,
-                        const int32_t* qoff, uint8_t* keep, int32_t* kidx, int32_t* kcnt, float* score,
+                        const int32_t* qoff, const float* q_norms, uint8_t* keep, int32_t* kidx, int32_t* kcnt,
+                        float* score,
                         const void* vp, void* kp_kept, void* vp_kept, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream) {
   int rc = check_dtype_d(dtype, d);
@@ -472,7 +473,7 @@ int fastar_annca_select(const void* q, int dtype, int H, int F, int64_t tpf, int
     }
   }
   return cuda_rc(fastar::launch_annca_select(dtype, d, TokView{q, q_head_stride, q_token_stride}, H, F, tpf,
-                                             qb, r, kp, pb, P, tau_ca, topk, gate, B, qperm, qoff, keep, kidx,
+                                             qb, r, kp, pb, P, tau_ca, topk, gate, B, qperm, qoff, q_norms, keep, kidx,
                                              kcnt, score, P > 0 ? vp : nullptr, P > 0 ? kp_kept : nullptr,
                                              P > 0 ? vp_kept : nullptr, workspace, stream));
 }

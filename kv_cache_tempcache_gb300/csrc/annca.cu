@@ -430,10 +430,10 @@ annca_bucket_kernel(const T* __restrict__ q, int64_t hs, int64_t ts, int F, int6
 template <typename T, int D>
 static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r,
                               const void* kp, const int32_t* pb, int64_t P, int gate, const BucketOrder bo,
-                              float* score, cudaStream_t s) {
+                              const float* qnorm, float* score, cudaStream_t s) {
   // bf16: the tensor-core scorer (dense Kp.Q^T with the bucket condition as a mask)
   if (sizeof(T) == 2 && gate &&
-      launch_annca_tc(D, q, H, F, tpf, qb, r, kp, pb, P, bo.B > 0 ? bo.B : FASTAR_MAX_B, score, nullptr, s))
+      launch_annca_tc(D, q, H, F, tpf, qb, r, kp, pb, P, bo.B > 0 ? bo.B : FASTAR_MAX_B, qnorm, score, nullptr, s))
     return cudaGetLastError();
   if (gate && F <= kBMaxF && (int64_t)F * tpf <= kBMaxQ && P <= FASTAR_MAX_P) {
     // prompt tokens whose bucket no CTA visits would keep stale scores: the bucket
@@ -461,7 +461,8 @@ static cudaError_t annca_impl(TokView q, int H, int F, int64_t tpf, const int32_
 
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb,
                                 int r, const void* kp, const int32_t* pb, int64_t P, float tau_ca, int topk,
-                                int gate, int B, const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
+                                int gate, int B, const int32_t* qperm, const int32_t* qoff, const float* qnorm,
+                                uint8_t* keep,
                                 int32_t* kidx, int32_t* kcnt, float* score, const void* vp, void* kp_kept,
                                 void* vp_kept, void* ws, cudaStream_t s) {
   if (H == 0 || F == 0) return cudaSuccess;
@@ -470,11 +471,11 @@ cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64
   const BucketOrder bo{B, qperm, qoff};
   if (P > 0) {
     if (dtype == FASTAR_BF16) {
-      e = d == 128 ? annca_impl<__nv_bfloat16, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s)
-                   : annca_impl<__nv_bfloat16, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s);
+      e = d == 128 ? annca_impl<__nv_bfloat16, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, qnorm, sc, s)
+                   : annca_impl<__nv_bfloat16, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, qnorm, sc, s);
     } else {
-      e = d == 128 ? annca_impl<float, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s)
-                   : annca_impl<float, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, sc, s);
+      e = d == 128 ? annca_impl<float, 128>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, qnorm, sc, s)
+                   : annca_impl<float, 64>(q, H, F, tpf, qb, r, kp, pb, P, gate, bo, qnorm, sc, s);
     }
     if (e != cudaSuccess) return e;
   }

@@ -66,6 +66,6 @@ extern "C" int fastar_annca_select_noalloc(const void* q, int dtype, int H, int 
   // the scores land in the fixed scratch array, which is passed as the (otherwise
   // caller-owned) score output of the regular entry point
   return fastar_annca_select(q, dtype, H, F, tpf, d, q_head_stride, q_token_stride, qb, r, kp, pb, P, tau_ca,
-                             topk, gate, 0, nullptr, nullptr, keep, kidx, kcnt, scratch, nullptr, nullptr, nullptr,
+                             topk, gate, 0, nullptr, nullptr, nullptr, keep, kidx, kcnt, scratch, nullptr, nullptr, nullptr,
                              nullptr, 0, stream);
 }

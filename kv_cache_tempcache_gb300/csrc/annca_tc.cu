@@ -12,7 +12,9 @@
 //              tiles (N = 128 rows each) through a 4-deep shared-memory ring;
 //   warp 1     owns TMEM (2 accumulator stages of 128 columns) and issues tcgen05.mma;
 //   warps 2-5  column facts, one query column per thread, a tile ahead of the fold:
-//              1/|q_j| (fp32 sum of squares of the shared-memory Q row) and, per bucket b,
+//              1/|q_j| (from the caller's query norms when given, loaded a tile ahead with
+//              the bucket ids; else the fp32 sum of squares of the shared-memory Q row, and
+//              only then do these warps wait for the Q tile) and, per bucket b,
 //              the 128-bit mask of the tile's columns whose bucket set holds b (built with
 //              shared-memory atomics from qb; a column with an id outside [0, B) gets no
 //              bit); two buffers;
@@ -93,8 +95,8 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* tile, int row) {
 template <int D>
 __global__ void __launch_bounds__(kCaThreads, 1)
     annca_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_p,
-                    const int32_t* __restrict__ qb, const int32_t* __restrict__ pb, CaGeom g,
-                    float* __restrict__ score, int32_t* status) {
+                    const int32_t* __restrict__ qb, const int32_t* __restrict__ pb,
+                    const float* __restrict__ qn, CaGeom g, float* __restrict__ score, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   CaSmem<D>& sm = *reinterpret_cast<CaSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -108,7 +110,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     tc::mbar_init(&sm.a_empty, 1 + kCaFoldW / 2);   // the MMA's commit + the half-0 fold warps
     for (int s = 0; s < kCaStages; ++s) {
       tc::mbar_init(&sm.b_full[s], 1);
-      tc::mbar_init(&sm.b_empty[s], 1 + kCaFactW);  // the MMA's commit + the column-fact warps
+      // the MMA's commit + the column-fact warps when they read the Q tile themselves
+      tc::mbar_init(&sm.b_empty[s], qn ? 1 : 1 + kCaFactW);
     }
     for (int s = 0; s < kCaTS; ++s) {
       tc::mbar_init(&sm.t_full[s], 1);
@@ -207,35 +210,44 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     const int nmask = g.B * 4;
     int stage = 0, fb = 0;
     uint32_t ph = 0, fph = 0;
-    // the column's bucket ids of tile c of (h, f), loaded a tile ahead of their use
-    auto load_ids = [&](int h, int f, int c, int (&ids)[FASTAR_MAX_R]) -> bool {
+    // the column's bucket ids (and norm, when given) of tile c of (h, f), loaded a tile
+    // ahead of their use
+    auto load_ids = [&](int h, int f, int c, int (&ids)[FASTAR_MAX_R], float& nrm) -> bool {
       const int64_t tl = (int64_t)c * 128 + ft;
       if (c >= nch || tl >= g.tpf) return false;
-      const int32_t* src = qb + ((int64_t)h * g.F * g.tpf + (int64_t)f * g.tpf + tl) * g.r;
+      const int64_t qi = (int64_t)h * g.F * g.tpf + (int64_t)f * g.tpf + tl;
+      const int32_t* src = qb + qi * g.r;
 #pragma unroll
       for (int sl = 0; sl < FASTAR_MAX_R; ++sl) ids[sl] = sl < g.r ? src[sl] : 0;
+      if (qn) nrm = qn[qi];
       return true;
     };
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int f = (u / g.PT) % g.F, h = u / (g.PT * g.F);
       int nids[FASTAR_MAX_R];
-      bool nok = load_ids(h, f, 0, nids);
+      float nnrm = 0.f;
+      bool nok = load_ids(h, f, 0, nids, nnrm);
       for (int c = 0; c < nch; ++c) {
         int ids[FASTAR_MAX_R];
 #pragma unroll
         for (int sl = 0; sl < FASTAR_MAX_R; ++sl) ids[sl] = nids[sl];
+        const float nrm = nnrm;
         bool okc = nok;
-        nok = load_ids(h, f, c + 1, nids);   // in flight during this tile's waits and math
+        nok = load_ids(h, f, c + 1, nids, nnrm);   // in flight during this tile's waits and math
         bool live = ca_wait_all(&sm.f_empty[fb], fph ^ 1, abort);
         if (live)
           for (int i = ft; i < nmask; i += kCaFactW * 32) (&sm.mask[fb][0][0])[i] = 0u;
         live = tc::named_bar_and(2, kCaFactW * 32, live);   // cleared before any bit is set
-        live = live && ca_wait_all(&sm.b_full[stage], ph, abort);
+        if (!qn) live = live && ca_wait_all(&sm.b_full[stage], ph, abort);
         if (live) {
           float qi = 0.f;
           if (okc) {
-            const float ss = row_sumsq<D>(&sm.b[stage][0][0], ft);
-            qi = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+            if (qn) {
+              qi = nrm > 0.f ? 1.0f / nrm : 0.f;
+            } else {
+              const float ss = row_sumsq<D>(&sm.b[stage][0][0], ft);
+              qi = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+            }
 #pragma unroll
             for (int sl = 0; sl < FASTAR_MAX_R; ++sl)
               if (sl < g.r && (ids[sl] < 0 || ids[sl] >= g.B)) okc = false;
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          tc::mbar_arrive(&sm.b_empty[stage]);
+          if (!qn) tc::mbar_arrive(&sm.b_empty[stage]);
           tc::mbar_arrive(&sm.f_full[fb]);
         }
         if (++stage == kCaStages) {
@@ -359,7 +371,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
 
 template <int D>
 bool launch_annca_tc_impl(TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r, const void* kp,
-                          const int32_t* pb, int64_t P, int B, float* score, int32_t* status, cudaStream_t s) {
+                          const int32_t* pb, int64_t P, int B, const float* qnorm, float* score, int32_t* status,
+                          cudaStream_t s) {
   const int64_t nq = (int64_t)F * tpf;
   if (P <= 0 || tpf <= 0 || nq > INT_MAX || P > INT_MAX) return false;
   CUtensorMap tq, tp;
@@ -388,7 +401,7 @@ bool launch_annca_tc_impl(TokView q, int H, int F, int64_t tpf, const int32_t* q
   constexpr size_t smem = sizeof(CaSmem<D>) + 1024;
   const cudaError_t a = opt_in_smem((const void*)annca_tc_kernel<D>, (int)smem);
   if (a != cudaSuccess) return false;
-  annca_tc_kernel<D><<<grid, kCaThreads, smem, s>>>(tq, tp, qb, pb, g, score, status);
+  annca_tc_kernel<D><<<grid, kCaThreads, smem, s>>>(tq, tp, qb, pb, qnorm, g, score, status);
   count_launches(1);
   return true;
 }
@@ -396,10 +409,11 @@ bool launch_annca_tc_impl(TokView q, int H, int F, int64_t tpf, const int32_t* q
 }  // namespace
 
 bool launch_annca_tc(int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r, const void* kp,
-                     const int32_t* pb, int64_t P, int B, float* score, int32_t* status, cudaStream_t s) {
+                     const int32_t* pb, int64_t P, int B, const float* qnorm, float* score, int32_t* status,
+                     cudaStream_t s) {
   if (B < 1 || B > FASTAR_MAX_B || r < 1 || r > FASTAR_MAX_R) return false;
-  if (d == 128) return launch_annca_tc_impl<128>(q, H, F, tpf, qb, r, kp, pb, P, B, score, status, s);
-  return launch_annca_tc_impl<64>(q, H, F, tpf, qb, r, kp, pb, P, B, score, status, s);
+  if (d == 128) return launch_annca_tc_impl<128>(q, H, F, tpf, qb, r, kp, pb, P, B, qnorm, score, status, s);
+  return launch_annca_tc_impl<64>(q, H, F, tpf, qb, r, kp, pb, P, B, qnorm, score, status, s);
 }
 
 }  // namespace fastar

@@ -186,10 +186,11 @@ template <int D, int RTQ>
 __global__ void __launch_bounds__(128)
 assign_qk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_c, int64_t n, int token_major, int B, int NP, int r,
-                    uint32_t tcols, int32_t* __restrict__ qb, int32_t* __restrict__ kb, float* __restrict__ knorm) {
+                    uint32_t tcols, int32_t* __restrict__ qb, int32_t* __restrict__ kb, float* __restrict__ knorm,
+                    float* __restrict__ qnorm) {
   if (blockIdx.z == 0)
     assign_tile<D, RTQ>(&tm_q, &tm_c, blockIdx.y, (int64_t)blockIdx.x * kRows, n, token_major, B, NP, r, tcols, qb,
-                        nullptr, nullptr, nullptr);
+                        nullptr, qnorm, nullptr);
   else
     assign_tile<D, 1>(&tm_k, &tm_c, blockIdx.y, (int64_t)blockIdx.x * kRows, n, token_major, B, NP, 1, tcols, kb,
                       nullptr, knorm, nullptr);
@@ -239,7 +240,7 @@ bool assign_tc_impl(TokView x, int H, int64_t n, const void* cent, int B, int r,
 
 template <int D>
 bool assign_qk_tc_impl(TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r, int32_t* qb,
-                       int32_t* kb, float* knorm, cudaStream_t s) {
+                       int32_t* kb, float* knorm, float* qnorm, cudaStream_t s) {
   const int NP = (B + 31) / 32 * 32;
   if (NP > 256 || n > INT32_MAX) return false;
   CUtensorMap tq, tk, tcen;
@@ -269,9 +270,9 @@ bool assign_qk_tc_impl(TokView q, TokView k, int H, int64_t n, const void* cent,
   const dim3 grid((unsigned)((n + kRows - 1) / kRows), H, 2);
   const int tm = token_major ? 1 : 0;
   if (r == 2)
-    assign_qk_tc_kernel<D, 2><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm);
+    assign_qk_tc_kernel<D, 2><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm, qnorm);
   else
-    assign_qk_tc_kernel<D, 0><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm);
+    assign_qk_tc_kernel<D, 0><<<grid, 128, smem, s>>>(tq, tk, tcen, n, tm, B, NP, r, tcols, qb, kb, knorm, qnorm);
   count_launches(1);
   return true;
 }
@@ -285,9 +286,9 @@ bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int 
 }
 
 bool launch_assign_qk_tc(int d, TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r,
-                         int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s) {
-  return d == 128 ? assign_qk_tc_impl<128>(q, k, H, n, cent, B, r, qb, kb, knorm, s)
-                  : assign_qk_tc_impl<64>(q, k, H, n, cent, B, r, qb, kb, knorm, s);
+                         int32_t* qb, int32_t* kb, float* knorm, float* qnorm, cudaStream_t s) {
+  return d == 128 ? assign_qk_tc_impl<128>(q, k, H, n, cent, B, r, qb, kb, knorm, qnorm, s)
+                  : assign_qk_tc_impl<64>(q, k, H, n, cent, B, r, qb, kb, knorm, qnorm, s);
 }
 
 }  // namespace fastar

@@ -118,12 +118,13 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 }
 
 cudaError_t launch_bucket_assign_qk(int dtype, int d, TokView q, TokView k, int H, int64_t n, const void* cent,
-                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s) {
+                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, float* qnorm,
+                                    cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  if (dtype == FASTAR_BF16 && launch_assign_qk_tc(d, q, k, H, n, cent, B, r, qb, kb, knorm, s))
+  if (dtype == FASTAR_BF16 && launch_assign_qk_tc(d, q, k, H, n, cent, B, r, qb, kb, knorm, qnorm, s))
     return cudaGetLastError();
   // otherwise the two assignments one after the other
-  cudaError_t e = launch_bucket_assign(dtype, d, q, H, n, cent, B, r, qb, nullptr, nullptr, s);
+  cudaError_t e = launch_bucket_assign(dtype, d, q, H, n, cent, B, r, qb, nullptr, qnorm, s);
   if (e != cudaSuccess) return e;
   return launch_bucket_assign(dtype, d, k, H, n, cent, B, 1, kb, nullptr, knorm, s);
 }

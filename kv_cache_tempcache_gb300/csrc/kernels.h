@@ -25,11 +25,13 @@ cudaError_t launch_bucket_assign(int dtype, int d, TokView x, int H, int64_t n, 
 bool launch_assign_tc(int d, TokView x, int H, int64_t n, const void* cent, int B, int r, int32_t* ids,
                       float* scores, float* norms, cudaStream_t s);
 // Both assignments of a step in one launch (bf16): queries' top-r sets into qb
-// [H, n, r], current keys' buckets into kb [H, n] and their norms into knorm [H, n].
+// [H, n, r], current keys' buckets into kb [H, n] and their norms into knorm [H, n];
+// the queries' norms into qnorm [H, n] when it is not null.
 bool launch_assign_qk_tc(int d, TokView q, TokView k, int H, int64_t n, const void* cent, int B, int r,
-                         int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s);
+                         int32_t* qb, int32_t* kb, float* knorm, float* qnorm, cudaStream_t s);
 cudaError_t launch_bucket_assign_qk(int dtype, int d, TokView q, TokView k, int H, int64_t n, const void* cent,
-                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, cudaStream_t s);
+                                    int B, int r, int32_t* qb, int32_t* kb, float* knorm, float* qnorm,
+                                    cudaStream_t s);
 // inv (optional, [H, n*r]): each element's position in its head's sorted order.
 cudaError_t launch_bucket_sort(const int32_t* ids, int H, int64_t n, int r, int B,
                                const int32_t* n_valid, int32_t* perm, int32_t* offsets,
@@ -160,12 +162,14 @@ cudaError_t launch_attention(int dtype, int d, const AttnArgs& a, cudaStream_t s
 // ---- AnnCA --------------------------------------------------------------------------
 size_t annca_workspace(int H, int F, int64_t P);
 // Tensor-core AnnCA scores (bf16, bucket-gated); false if it could not be set up.
+// qnorm (optional, [H, F * tpf]): the queries' norms, used instead of forming them.
 bool launch_annca_tc(int d, TokView q, int H, int F, int64_t tpf, const int32_t* qb, int r, const void* kp,
-                     const int32_t* pb, int64_t P, int B, float* score, int32_t* status, cudaStream_t s);
+                     const int32_t* pb, int64_t P, int B, const float* qnorm, float* score, int32_t* status,
+                     cudaStream_t s);
 cudaError_t launch_annca_select(int dtype, int d, TokView q, int H, int F, int64_t tpf,
                                 const int32_t* qb, int r, const void* kp, const int32_t* pb,
                                 int64_t P, float tau_ca, int topk, int gate, int B,
-                                const int32_t* qperm, const int32_t* qoff, uint8_t* keep,
+                                const int32_t* qperm, const int32_t* qoff, const float* qnorm, uint8_t* keep,
                                 int32_t* kidx, int32_t* kcnt, float* score, const void* vp,
                                 void* kp_kept, void* vp_kept, void* ws, cudaStream_t s);
 

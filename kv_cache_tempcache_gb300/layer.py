@@ -97,6 +97,7 @@ class FastARLayer:
         self.qb = _i32(H, Nq, r, dev=dev)
         self.kb_cur = _i32(H, Nq, 1, dev=dev)
         self.kcur_norm = _f32(H, Nq, dev=dev)
+        self.qnorm = _f32(H, Nq, dev=dev)   # the queries' norms, written by the assignment for AnnCA
         self.top1 = _i32(H, Nq, dev=dev)
         self.s1 = _f32(H, Nq, dev=dev)
         self.s2 = _f32(H, Nq, dev=dev)
@@ -245,7 +246,8 @@ class FastARLayer:
             evm = torch.cuda.Event()
             evm.record(self.mside)
         t("bucket_assign", main, "begin")
-        L.fastar_bucket_assign_qk(q, k_cur, self.centroids, self.r, self.qb, self.kb_cur, self.kcur_norm)
+        L.fastar_bucket_assign_qk(q, k_cur, self.centroids, self.r, self.qb, self.kb_cur, self.kcur_norm,
+                                  q_norms=self.qnorm)
         t("bucket_assign", main, "end")
         if self.pq:
             t("pq_encode", main, "begin")
@@ -265,7 +267,8 @@ class FastARLayer:
             side.wait_event(ev)
         with torch.cuda.stream(side):
             t("annca_select", side, "begin")
-            self._annca(q, self.qperm if not self.presort else None, self.qoff if not self.presort else None)
+            self._annca(q, self.qperm if not self.presort else None, self.qoff if not self.presort else None,
+                        self.qnorm)
             t("annca_select", side, "end")
             t("cross_attn_subset", side, "begin")
             self._cross(q, self.o_cross)
@@ -353,20 +356,22 @@ class FastARLayer:
         """AnnCA on the current stream for its own queries q: their buckets, the
         frame-relevant prompt tokens, cross-attention over them -> out (default o_cross)."""
         o = self.o_cross if out is None else out
-        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb)
+        L.fastar_bucket_assign(q, self.centroids, self.r, self.qb, None, self.qnorm)
         # the bf16 scorer masks dense tiles with qb itself; the bucket order helps the SIMT one
         order = q.dtype != torch.bfloat16
         if order:
             L.fastar_bucket_sort(self.qb, self.B, self.qperm, self.qoff, None, self.dev_status)
-        self._annca(q, self.qperm if order else None, self.qoff if order else None)
+        self._annca(q, self.qperm if order else None, self.qoff if order else None, self.qnorm)
         self._cross(q, o)
         return o
 
-    def _annca(self, q, qperm, qoff):
-        """The prompt selection for queries q (and, in bf16, the kept rows' planes)."""
+    def _annca(self, q, qperm, qoff, qnorm=None):
+        """The prompt selection for queries q (and, in bf16, the kept rows' planes); qnorm:
+        q's norms as the bucket assignment wrote them."""
         kw = dict(vp=self.vp, kp_kept=self.kp_kept, vp_kept=self.vp_kept) if self.kept else {}
         L.fastar_annca_select(q, self.F, self.qb, self.kp, self.pb, self.tau_ca, self.topk, self.gate, self.keep,
-                              self.kidx, self.kcnt, self.score, B=self.B, qperm=qperm, qoff=qoff, **kw)
+                              self.kidx, self.kcnt, self.score, B=self.B, qperm=qperm, qoff=qoff, q_norms=qnorm,
+                              **kw)
 
     def _cross(self, q, o):
         """Cross-attention of q over the kept prompt tokens -> o."""

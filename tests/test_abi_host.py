@@ -82,21 +82,21 @@ def test_argument_validation_rejects_before_launch(lib):
                                   0.1, FAKE, 8192, 128, None, None, FAKE, 16, s) == L.EWORKSPACE
     # prompt beyond the limit
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 2000, 0.2, 16, 1,
-                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.ECAPACITY
+                                   0, None, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.ECAPACITY
     # a bucket order needs the bucket count, and both of its arrays
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
+                                   0, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   8, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
+                                   8, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, s) == L.EINVAL
     # kept-row planes: both or neither, with the values, bf16 only
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   0, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4096, None, None, 0,
+                                   0, None, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4096, None, None, 0,
                                    s) == L.EINVAL
     assert lib.fastar_annca_select(FAKE, L.BF16, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   0, None, None, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, FAKE + 8192, None, 0,
+                                   0, None, None, None, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, FAKE + 8192, None, 0,
                                    s) == L.EINVAL
     assert lib.fastar_annca_select(FAKE, L.F32, 1, 1, 64, 128, 8192, 128, FAKE, 2, FAKE, FAKE, 100, 0.2, 16, 1,
-                                   0, None, None, FAKE, FAKE, FAKE, FAKE, FAKE + 2048, FAKE + 4096, FAKE + 8192, None,
+                                   0, None, None, None, FAKE, FAKE, FAKE, FAKE, FAKE + 2048, FAKE + 4096, FAKE + 8192, None,
                                    0, s) == L.EUNSUPPORTED
     # the cross-attention over planes: bf16 planes, present and aligned
     assert lib.fastar_cross_attn_kept(FAKE, L.F32, 1, 1, 64, 128, 8192, 128, FAKE, FAKE, 100, FAKE, 0.1, FAKE, 8192,

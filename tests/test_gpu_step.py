@@ -264,8 +264,8 @@ def test_cross_attention_paths_agree_bit_for_bit(P, d):
 
 @pytest.mark.parametrize("r,layout", [(2, "HND"), (3, "HND"), (2, "NHD")])
 def test_fused_assignment_equals_two_calls(r, layout):
-    # fastar_bucket_assign_qk: the queries' top-r sets and the current keys' buckets and
-    # norms in one launch, bit for bit the two separate calls
+    # fastar_bucket_assign_qk: the queries' top-r sets and norms and the current keys'
+    # buckets and norms in one launch, bit for bit the two separate calls
     from kv_cache_tempcache_gb300 import _lib as L
     cfg = GH.small_bf16()
     inp = synth.layer_step_inputs(cfg, seed=3)
@@ -279,10 +279,53 @@ def test_fused_assignment_equals_two_calls(r, layout):
     i32 = lambda *s: torch.full(s, -5, dtype=torch.int32, device="cuda")
     qb1, kb1, qb2, kb2 = i32(H, n, r), i32(H, n, 1), i32(H, n, r), i32(H, n, 1)
     kn1 = torch.zeros((H, n), dtype=torch.float32, device="cuda")
-    kn2 = torch.zeros_like(kn1)
-    L.fastar_bucket_assign(q, C, r, qb1)
+    kn2, qn1, qn2 = torch.zeros_like(kn1), torch.zeros_like(kn1), torch.zeros_like(kn1)
+    L.fastar_bucket_assign(q, C, r, qb1, None, qn1)
     L.fastar_bucket_assign(k, C, 1, kb1, None, kn1)
-    L.fastar_bucket_assign_qk(q, k, C, r, qb2, kb2, kn2)
+    L.fastar_bucket_assign_qk(q, k, C, r, qb2, kb2, kn2, q_norms=qn2)
     torch.cuda.synchronize()
-    assert torch.equal(qb1, qb2) and torch.equal(kb1, kb2) and torch.equal(kn1, kn2)
+    assert torch.equal(qb1, qb2) and torch.equal(kb1, kb2) and torch.equal(kn1, kn2) and torch.equal(qn1, qn2)
+    # the norms of the bf16 rows, against float64
+    qf = GH.to_dev(inp["q"], cfg).float().cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(GH.np_(qn2), np.linalg.norm(qf, axis=-1), rtol=1e-5)
     parity.check_topr(O.centroid_scores(inp["q"][0], inp["centroids"][0]), GH.np_(qb2)[0], "fused query buckets")
+
+
+def test_annca_with_the_assignment_norms():
+    # fastar_annca_select given the queries' norms from the assignment: the cosines agree with
+    # the call that forms the norms itself to fp32 rounding, and both selections are correct
+    # answers for the oracle's
+    from kv_cache_tempcache_gb300 import _lib as L
+    cfg = GH.small_bf16()
+    inp = synth.layer_step_inputs(cfg, seed=6)
+    q, k, kp = GH.to_dev(inp["q"], cfg), GH.to_dev(inp["k_cur"], cfg), GH.to_dev(inp["kp"], cfg)
+    C = GH.to_dev(inp["centroids"], cfg)
+    H, n, P, F = cfg.H, cfg.Nq, cfg.P, cfg.F
+    dev = torch.device("cuda")
+    qb = torch.zeros((H, n, cfg.r), dtype=torch.int32, device=dev)
+    kb = torch.zeros((H, n, 1), dtype=torch.int32, device=dev)
+    pb = torch.zeros((H, P, 1), dtype=torch.int32, device=dev)
+    kn, qn = (torch.zeros((H, n), dtype=torch.float32, device=dev) for _ in range(2))
+    L.fastar_bucket_assign_qk(q, k, C, cfg.r, qb, kb, kn, q_norms=qn)
+    L.fastar_bucket_assign(kp, C, 1, pb)
+    res = []
+    for norms in (None, qn):
+        keep = torch.zeros((H, F, P), dtype=torch.uint8, device=dev)
+        kidx = torch.zeros((H, F, P), dtype=torch.int32, device=dev)
+        kcnt = torch.zeros((H, F), dtype=torch.int32, device=dev)
+        score = torch.zeros((H, F, P), dtype=torch.float32, device=dev)
+        L.fastar_annca_select(q, F, qb, kp, pb, cfg.tau_ca, cfg.topk, 1, keep, kidx, kcnt, score, B=cfg.B,
+                              q_norms=norms)
+        torch.cuda.synchronize()
+        res.append((GH.np_(keep), GH.np_(kcnt), GH.np_(score)))
+    s0, s1 = res[0][2], res[1][2]
+    fin = np.isfinite(s0)
+    assert np.array_equal(fin, np.isfinite(s1))
+    np.testing.assert_allclose(s1[fin], s0[fin], rtol=2e-6, atol=1e-7)
+    qbn, pbn = GH.np_(qb), GH.np_(pb)[..., 0]
+    for keep, kcnt, _ in res:
+        for h in range(H):
+            _, _, _, ref = O.annca_select(inp["q"][h], qbn[h], inp["kp"][h], pbn[h], F, cfg.Tf, cfg.tau_ca, cfg.topk)
+            for f in range(F):
+                parity.check_keep(ref[f], keep[h, f], cfg.tau_ca, cfg.topk, f"keep head {h} frame {f}")
+                assert int(kcnt[h, f]) == int(keep[h, f].sum())
