@@ -3,8 +3,8 @@
 // layout of the restricted attention).
 //
 // CTA c of the cluster owns the c-th contiguous chunk of the element range and, inside
-// it, each warp a contiguous segment.  Pass 1 builds per-warp histograms (a warp-level
-// match gives each bucket one leader per batch of 32 elements).  The CTA's histogram
+// it, each warp a contiguous segment.  Pass 1 builds per-warp histograms (shared-memory
+// atomic adds).  The CTA's histogram
 // sits in its shared memory; after a cluster barrier every CTA reads all of the
 // cluster's histograms through distributed shared memory, which gives per bucket the
 // total (the bucket offsets) and the count in the chunks before its own.  Pass 2 replays
@@ -63,9 +63,7 @@ __device__ __forceinline__ void cluster_counting_sort(SortSmem& sm, const int32_
       flag_status(status, FASTAR_DEV_BAD_BUCKET);
       b = -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    if (b >= 0 && lane == __ffs(peers) - 1) sm.cnt[warp][b] += __popc(peers);
-    __syncwarp();
+    if (b >= 0) atomicAdd(&sm.cnt[warp][b], 1);   // counts only: the order of the adds is immaterial
   }
   __syncthreads();
   if (t < B) {
